@@ -1,17 +1,17 @@
 """GB300-native convolution backward-data (dgrad) as an implicit GEMM.
 
 The compute lives in ``libdgrad_gb300.so`` (CUDA kernels for sm_103a behind a
-C ABI declared in ``include/dgrad.h``); ``dgrad`` is a thin ctypes binding over
-it.  Importing this package does not load the library: the first call that
-needs it does, and raises if it is missing (there is no CPU fallback).
+C ABI declared in ``include/dgrad.h``); ``binding`` is a thin ctypes layer
+over it.  Importing this package does not load the library: the first call
+that needs it does, and raises if it is missing (there is no CPU fallback).
 """
 from __future__ import annotations
 
-__all__ = ["Plan", "DgradError", "dgrad", "describe", "load_library", "workloads"]
+__all__ = ["Plan", "DgradError", "dgrad", "describe", "describe_taps", "load_library", "workloads"]
 
 
 def __getattr__(name):
-    if name in ("Plan", "DgradError", "dgrad", "describe", "load_library"):
+    if name in ("Plan", "DgradError", "dgrad", "describe", "describe_taps", "load_library"):
         from . import binding
         return getattr(binding, name)
     if name == "workloads":

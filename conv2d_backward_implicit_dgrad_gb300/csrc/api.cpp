@@ -1,0 +1,346 @@
+// C ABI of libdgrad_gb300 (declared in include/dgrad.h): plan creation,
+// validation, launches and error reporting.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstdlib>
+#include <cstring>
+#include <new>
+
+#include "dgrad.h"
+#include "dgrad_internal.h"
+
+struct dgrad_plan_s {
+    int device;
+    int precision;
+    dgrad::Geometry g;
+    dgrad::Tiling t;
+    dgrad::MainParams mp;
+    dgrad::PrepackParams pp;
+    float *wp;             // packed weights (device)
+    uint32_t *err;         // device error word
+    float *stage_go;       // dgrad_run_host staging (device), allocated on first use
+    float *stage_w;
+    float *stage_gi;
+    size_t workspace_bytes;
+    int packed;            // dgrad_prepack (or dgrad_run) has run at least once
+};
+
+namespace {
+
+using dgrad::Geometry;
+using dgrad::Tiling;
+
+constexpr long long kTimeoutNs = 1000000000LL;   // bounded in-kernel waits: 1 s
+
+size_t go_elems(const Geometry &g) { return (size_t)g.N * g.Co * g.oH * g.oW; }
+size_t w_elems(const Geometry &g) { return (size_t)g.Co * g.Ci * g.kH * g.kW; }
+size_t gi_elems(const Geometry &g) { return (size_t)g.N * g.Ci * g.H * g.W; }
+
+void fill_info(const Geometry &g, const Tiling &t, int precision, size_t ws, dgrad_plan_info_t *info) {
+    std::memset(info, 0, sizeof(*info));
+    info->N = g.N; info->Ci = g.Ci; info->H = g.H; info->W = g.W; info->Co = g.Co;
+    info->kH = g.kH; info->kW = g.kW; info->stride = g.s; info->pad_h = g.ph; info->pad_w = g.pw;
+    info->oH = g.oH; info->oW = g.oW;
+    info->precision = precision;
+    info->path = t.path;
+    info->n_phases = g.n_phases;
+    info->n_taps = g.n_taps;
+    info->Ph = g.Ph; info->Pw = g.Pw; info->Hv = g.Hv; info->Wp = g.Wp;
+    info->positions = g.positions;
+    info->max_shift = g.max_shift;
+    info->tile_blocks = t.tm; info->slice_n = t.bn; info->n_slices = t.n_slices;
+    info->chunk_k = t.kc; info->n_chunks = t.n_chunks;
+    info->n_work = t.n_work;
+    info->grid = t.path == DGRAD_PATH_SIMT ? (int)t.n_work : t.grid;
+    info->b_resident = t.b_resident;
+    info->smem_bytes = t.smem_bytes;
+    info->tmem_cols = t.tmem_cols;
+    info->workspace_bytes = ws;
+    info->packed_weight_bytes = t.packed_bytes;
+    info->useful_flops = 2.0 * g.N * g.Co * g.oH * g.oW * (double)g.Ci * g.kH * g.kW;
+    info->algorithmic_bytes = 4.0 * ((double)go_elems(g) + (double)w_elems(g) + (double)gi_elems(g));
+}
+
+dgrad_status_t plan_host(int N, int Ci, int H, int W, int Co, int kH, int kW, int stride, int pad_h,
+                         int pad_w, dgrad_precision_t precision, const dgrad_options_t *opts, int sm_count,
+                         Geometry *g, Tiling *t) {
+    if (precision != DGRAD_PREC_FP32 && precision != DGRAD_PREC_TF32) return DGRAD_ERR_INVALID_ARG;
+    dgrad_status_t st = dgrad::make_geometry(N, Ci, H, W, Co, kH, kW, stride, pad_h, pad_w, g);
+    if (st != DGRAD_OK) return st;
+    return dgrad::choose_tiling(*g, precision, opts, sm_count, t);
+}
+
+void fill_params(dgrad_plan_s *pl) {
+    const Geometry &g = pl->g;
+    const Tiling &t = pl->t;
+    dgrad::MainParams &m = pl->mp;
+    std::memset(&m, 0, sizeof(m));
+    m.wp = pl->wp;
+    m.err = pl->err;
+    m.N = g.N; m.Ci = g.Ci; m.Co = g.Co; m.H = g.H; m.W = g.W; m.oH = g.oH; m.oW = g.oW; m.s = g.s;
+    m.Ph = g.Ph; m.Pw = g.Pw; m.Hv = g.Hv; m.Wp = g.Wp; m.HvWp = g.Hv * g.Wp;
+    m.positions = (int)g.positions;
+    m.tm = t.tm; m.bn = t.bn; m.n_slices = t.n_slices; m.kc = t.kc; m.n_chunks = t.n_chunks;
+    m.n_tiles = t.n_tiles; m.n_work = (int)t.n_work;
+    m.a_rows = t.a_rows; m.a_stages = t.a_stages; m.b_stages = t.b_stages; m.b_resident = t.b_resident;
+    m.chunk_bytes = t.chunk_bytes;
+    m.acc_bufs = t.acc_bufs; m.acc_cols = t.acc_cols; m.tmem_cols = t.tmem_cols;
+    m.round_tf32 = pl->precision == DGRAD_PREC_TF32 ? 1 : 0;
+    m.n_phases = g.n_phases;
+    m.n_taps = g.n_taps;
+    m.idesc = dgrad::tf32_idesc(dgrad::kBlockM, t.bn);
+    m.timeout_ns = kTimeoutNs;
+    for (int i = 0; i < g.n_phases; ++i) m.phase[i] = g.phase[i];
+    for (int i = 0; i < g.n_taps; ++i) m.tap[i] = g.tap[i];
+
+    dgrad::PrepackParams &q = pl->pp;
+    std::memset(&q, 0, sizeof(q));
+    q.wp = pl->wp;
+    q.Co = g.Co; q.Ci = g.Ci; q.kH = g.kH; q.kW = g.kW;
+    q.n_taps = g.n_taps; q.bn = t.bn; q.n_slices = t.n_slices; q.kc = t.kc; q.n_chunks = t.n_chunks;
+    q.round_tf32 = m.round_tf32;
+    q.total = (long long)(t.packed_bytes / 4);
+    for (int i = 0; i < g.n_taps; ++i) {
+        q.tap_kh[i] = g.tap[i].kh;
+        q.tap_kw[i] = g.tap[i].kw;
+    }
+}
+
+bool overlaps(const void *a, size_t abytes, const void *b, size_t bbytes) {
+    uintptr_t a0 = (uintptr_t)a, a1 = a0 + abytes, b0 = (uintptr_t)b, b1 = b0 + bbytes;
+    return a0 < b1 && b0 < a1;
+}
+
+bool aligned16(const void *p) { return p != nullptr && ((uintptr_t)p & 15u) == 0; }
+
+dgrad_status_t check_device(const dgrad_plan_s *plan) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return DGRAD_ERR_CUDA;
+    return dev == plan->device ? DGRAD_OK : DGRAD_ERR_WRONG_DEVICE;
+}
+
+dgrad_status_t launch_prepack_on(dgrad_plan_s *plan, const float *weight, cudaStream_t s) {
+    dgrad::PrepackParams pp = plan->pp;
+    pp.w = weight;
+    if (dgrad::launch_prepack(pp, s) != cudaSuccess) return DGRAD_ERR_CUDA;
+    plan->packed = 1;
+    return DGRAD_OK;
+}
+
+dgrad_status_t launch_main_on(dgrad_plan_s *plan, const float *grad_out, float *grad_input, cudaStream_t s) {
+    dgrad::MainParams mp = plan->mp;
+    mp.go = grad_out;
+    mp.gi = grad_input;
+    cudaError_t e = plan->t.path == DGRAD_PATH_TCGEN05 ? dgrad::launch_tc(mp, plan->t, s, true)
+                                                       : dgrad::launch_simt(mp, plan->t, s);
+    return e == cudaSuccess ? DGRAD_OK : DGRAD_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *dgrad_status_string(dgrad_status_t s) {
+    switch (s) {
+        case DGRAD_OK: return "ok";
+        case DGRAD_ERR_INVALID_ARG: return "invalid argument (shape, stride, padding or plan)";
+        case DGRAD_ERR_UNSUPPORTED: return "shape outside the supported limits";
+        case DGRAD_ERR_MISALIGNED: return "tensor pointer is NULL or not 16-byte aligned";
+        case DGRAD_ERR_ALIAS: return "grad_input overlaps grad_out or weight";
+        case DGRAD_ERR_OOM: return "device workspace allocation failed";
+        case DGRAD_ERR_CUDA: return "CUDA runtime error or kernel launch failure";
+        case DGRAD_ERR_DEVICE_TIMEOUT: return "a bounded in-kernel wait ran out";
+        case DGRAD_ERR_NO_DEVICE: return "no CUDA device of compute capability 10.3";
+        case DGRAD_ERR_WRONG_DEVICE: return "current CUDA device is not the plan's device";
+    }
+    return "unknown status";
+}
+
+dgrad_status_t dgrad_describe(int N, int Ci, int H, int W, int Co, int kH, int kW, int stride, int pad_h,
+                              int pad_w, dgrad_precision_t precision, const dgrad_options_t *opts,
+                              dgrad_plan_info_t *info) {
+    if (!info) return DGRAD_ERR_INVALID_ARG;
+    Geometry g;
+    Tiling t;
+    int sms = (opts && opts->sm_count > 0) ? opts->sm_count : 148;
+    dgrad_status_t st = plan_host(N, Ci, H, W, Co, kH, kW, stride, pad_h, pad_w, precision, opts, sms, &g, &t);
+    if (st != DGRAD_OK) return st;
+    fill_info(g, t, precision, t.packed_bytes + 256, info);
+    return DGRAD_OK;
+}
+
+dgrad_status_t dgrad_describe_taps(int N, int Ci, int H, int W, int Co, int kH, int kW, int stride, int pad_h,
+                                   int pad_w, int cap, int *phases, int *n_phases, int *taps, int *n_taps) {
+    if (!phases || !n_phases || !taps || !n_taps || cap < 0) return DGRAD_ERR_INVALID_ARG;
+    Geometry g;
+    dgrad_status_t st = dgrad::make_geometry(N, Ci, H, W, Co, kH, kW, stride, pad_h, pad_w, &g);
+    if (st != DGRAD_OK) return st;
+    *n_phases = g.n_phases;
+    *n_taps = g.n_taps;
+    for (int i = 0; i < g.n_phases && i < cap; ++i) {
+        const dgrad::PhaseDesc &p = g.phase[i];
+        int *o = phases + 6 * i;
+        o[0] = p.a; o[1] = p.b; o[2] = p.Hq; o[3] = p.Wq; o[4] = p.tap_begin; o[5] = p.tap_count;
+    }
+    for (int i = 0; i < g.n_taps && i < cap; ++i) {
+        taps[3 * i] = g.tap[i].kh;
+        taps[3 * i + 1] = g.tap[i].kw;
+        taps[3 * i + 2] = g.tap[i].shift;
+    }
+    return DGRAD_OK;
+}
+
+dgrad_status_t dgrad_plan_ex(int N, int Ci, int H, int W, int Co, int kH, int kW, int stride, int pad_h,
+                             int pad_w, dgrad_precision_t precision, const dgrad_options_t *opts,
+                             dgrad_plan_t *plan_out) {
+    if (!plan_out) return DGRAD_ERR_INVALID_ARG;
+    *plan_out = nullptr;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return DGRAD_ERR_NO_DEVICE;
+    cudaDeviceProp prop;
+    if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) return DGRAD_ERR_NO_DEVICE;
+    if (prop.major != 10 || prop.minor != 3) return DGRAD_ERR_NO_DEVICE;
+
+    dgrad_plan_s *pl = new (std::nothrow) dgrad_plan_s;
+    if (!pl) return DGRAD_ERR_OOM;
+    std::memset(pl, 0, sizeof(*pl));
+    pl->device = dev;
+    pl->precision = precision;
+    dgrad_status_t st = plan_host(N, Ci, H, W, Co, kH, kW, stride, pad_h, pad_w, precision, opts,
+                                  prop.multiProcessorCount, &pl->g, &pl->t);
+    if (st != DGRAD_OK) {
+        delete pl;
+        return st;
+    }
+    // Workspace: the error word (256 B) then the packed weights.
+    size_t ws = 256 + pl->t.packed_bytes;
+    void *mem = nullptr;
+    if (cudaMalloc(&mem, ws) != cudaSuccess) {
+        cudaGetLastError();
+        delete pl;
+        return DGRAD_ERR_OOM;
+    }
+    if (cudaMemset(mem, 0, 256) != cudaSuccess) {
+        cudaFree(mem);
+        delete pl;
+        return DGRAD_ERR_CUDA;
+    }
+    pl->err = static_cast<uint32_t *>(mem);
+    pl->wp = reinterpret_cast<float *>(static_cast<uint8_t *>(mem) + 256);
+    pl->workspace_bytes = ws;
+    fill_params(pl);
+    *plan_out = pl;
+    return DGRAD_OK;
+}
+
+dgrad_status_t dgrad_plan(int N, int Ci, int H, int W, int Co, int kH, int kW, int stride, int pad_h, int pad_w,
+                          dgrad_precision_t precision, dgrad_plan_t *plan_out) {
+    return dgrad_plan_ex(N, Ci, H, W, Co, kH, kW, stride, pad_h, pad_w, precision, nullptr, plan_out);
+}
+
+dgrad_status_t dgrad_plan_info(dgrad_plan_t plan, dgrad_plan_info_t *info) {
+    if (!plan || !info) return DGRAD_ERR_INVALID_ARG;
+    fill_info(plan->g, plan->t, plan->precision, plan->workspace_bytes, info);
+    return DGRAD_OK;
+}
+
+dgrad_status_t dgrad_run(dgrad_plan_t plan, const float *grad_out, const float *weight, float *grad_input,
+                         void *stream) {
+    if (!plan) return DGRAD_ERR_INVALID_ARG;
+    if (!aligned16(grad_out) || !aligned16(weight) || !aligned16(grad_input)) return DGRAD_ERR_MISALIGNED;
+    const Geometry &g = plan->g;
+    const size_t gi_bytes = gi_elems(g) * 4;
+    if (overlaps(grad_input, gi_bytes, grad_out, go_elems(g) * 4) ||
+        overlaps(grad_input, gi_bytes, weight, w_elems(g) * 4))
+        return DGRAD_ERR_ALIAS;
+    dgrad_status_t st = check_device(plan);
+    if (st != DGRAD_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (g.n_taps == 0) {   // no term reaches any input element
+        plan->packed = 1;
+        return cudaMemsetAsync(grad_input, 0, gi_bytes, s) == cudaSuccess ? DGRAD_OK : DGRAD_ERR_CUDA;
+    }
+    st = launch_prepack_on(plan, weight, s);
+    if (st != DGRAD_OK) return st;
+    return launch_main_on(plan, grad_out, grad_input, s);
+}
+
+dgrad_status_t dgrad_prepack(dgrad_plan_t plan, const float *weight, void *stream) {
+    if (!plan) return DGRAD_ERR_INVALID_ARG;
+    if (!aligned16(weight)) return DGRAD_ERR_MISALIGNED;
+    dgrad_status_t st = check_device(plan);
+    if (st != DGRAD_OK) return st;
+    if (plan->g.n_taps == 0) {
+        plan->packed = 1;
+        return DGRAD_OK;
+    }
+    return launch_prepack_on(plan, weight, static_cast<cudaStream_t>(stream));
+}
+
+dgrad_status_t dgrad_run_packed(dgrad_plan_t plan, const float *grad_out, float *grad_input, void *stream) {
+    if (!plan || !plan->packed) return DGRAD_ERR_INVALID_ARG;
+    if (!aligned16(grad_out) || !aligned16(grad_input)) return DGRAD_ERR_MISALIGNED;
+    const Geometry &g = plan->g;
+    const size_t gi_bytes = gi_elems(g) * 4;
+    if (overlaps(grad_input, gi_bytes, grad_out, go_elems(g) * 4)) return DGRAD_ERR_ALIAS;
+    dgrad_status_t st = check_device(plan);
+    if (st != DGRAD_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (g.n_taps == 0)
+        return cudaMemsetAsync(grad_input, 0, gi_bytes, s) == cudaSuccess ? DGRAD_OK : DGRAD_ERR_CUDA;
+    return launch_main_on(plan, grad_out, grad_input, s);
+}
+
+dgrad_status_t dgrad_run_host(dgrad_plan_t plan, const float *grad_out_host, const float *weight_host,
+                              float *grad_input_host, void *stream) {
+    if (!plan) return DGRAD_ERR_INVALID_ARG;
+    if (!grad_out_host || !weight_host || !grad_input_host) return DGRAD_ERR_MISALIGNED;
+    dgrad_status_t st = check_device(plan);
+    if (st != DGRAD_OK) return st;
+    const Geometry &g = plan->g;
+    const size_t go_b = go_elems(g) * 4, w_b = w_elems(g) * 4, gi_b = gi_elems(g) * 4;
+    if (!plan->stage_go) {
+        void *m = nullptr;
+        auto up = [](size_t b) { return (b + 255) & ~size_t(255); };
+        if (cudaMalloc(&m, up(go_b) + up(w_b) + up(gi_b)) != cudaSuccess) {
+            cudaGetLastError();
+            return DGRAD_ERR_OOM;
+        }
+        plan->stage_go = static_cast<float *>(m);
+        plan->stage_w = reinterpret_cast<float *>(static_cast<uint8_t *>(m) + up(go_b));
+        plan->stage_gi = reinterpret_cast<float *>(static_cast<uint8_t *>(m) + up(go_b) + up(w_b));
+    }
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaMemcpyAsync(plan->stage_go, grad_out_host, go_b, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+        cudaMemcpyAsync(plan->stage_w, weight_host, w_b, cudaMemcpyHostToDevice, s) != cudaSuccess)
+        return DGRAD_ERR_CUDA;
+    st = dgrad_run(plan, plan->stage_go, plan->stage_w, plan->stage_gi, stream);
+    if (st != DGRAD_OK) return st;
+    if (cudaMemcpyAsync(grad_input_host, plan->stage_gi, gi_b, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return DGRAD_ERR_CUDA;
+    return cudaStreamSynchronize(s) == cudaSuccess ? DGRAD_OK : DGRAD_ERR_CUDA;
+}
+
+dgrad_status_t dgrad_plan_check(dgrad_plan_t plan) {
+    if (!plan) return DGRAD_ERR_INVALID_ARG;
+    uint32_t word = 0;
+    if (cudaMemcpy(&word, plan->err, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess) return DGRAD_ERR_CUDA;
+    if (word == 0) return DGRAD_OK;
+    if (cudaMemset(plan->err, 0, sizeof(word)) != cudaSuccess) return DGRAD_ERR_CUDA;
+    return DGRAD_ERR_DEVICE_TIMEOUT;
+}
+
+void dgrad_plan_destroy(dgrad_plan_t plan) {
+    if (!plan) return;
+    int cur = -1;
+    cudaGetDevice(&cur);
+    if (cur != plan->device) cudaSetDevice(plan->device);
+    cudaDeviceSynchronize();
+    cudaFree(plan->err);
+    if (plan->stage_go) cudaFree(plan->stage_go);
+    if (cur >= 0 && cur != plan->device) cudaSetDevice(cur);
+    delete plan;
+}
+
+}  // extern "C"

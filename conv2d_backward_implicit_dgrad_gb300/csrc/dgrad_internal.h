@@ -1,0 +1,137 @@
+// Internal declarations of libdgrad_gb300: geometry of the phase-split
+// implicit GEMM, kernel parameter blocks and launchers.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+#include "dgrad.h"
+
+namespace dgrad {
+
+constexpr int kMaxTaps = 128;
+constexpr int kMaxPhases = 16;
+constexpr int kMaxStride = 4;
+constexpr int kBlockM = 128;          // GEMM rows (output positions) per MMA block
+constexpr int kMaxSmem = 232448;      // opt-in dynamic shared memory per CTA on sm_103
+constexpr int kTmemCols = 512;        // tensor-memory columns per SM
+
+// Instruction descriptor of tcgen05.mma .kind::tf32 (PTX ISA, "instruction
+// descriptor" table for .kind::f16 / .kind::tf32): fp32 accumulator, TF32 A
+// and B, both K-major, no negation, dense.
+constexpr uint32_t tf32_idesc(int M, int N) {
+    return (1u << 4)                                  // D format: F32
+           | (2u << 7)                                // A format: TF32
+           | (2u << 10)                               // B format: TF32
+           | (static_cast<uint32_t>(N >> 3) << 17)    // N / 8
+           | (static_cast<uint32_t>(M >> 4) << 24);   // M / 16
+}
+
+// Device error word values (a bit set; the host maps it to dgrad_status_t).
+constexpr uint32_t kErrTimeout = 1u;
+
+// One kernel tap that feeds a phase.  In the zero-padded grad_out frame V
+// (see Geometry) the tap reads V at (output position + shift).
+struct TapDesc {
+    int kh, kw;   // position inside the kernel
+    int shift;    // dr * Wp + dc, >= 0
+};
+
+// One sub-pixel phase (a, b): input rows ih = s*q + a, columns iw = s*u + b.
+struct PhaseDesc {
+    int a, b;
+    int Hq, Wq;             // output rows/cols of the phase: ceil((H-a)/s), ceil((W-b)/s)
+    int tap_begin, tap_count;
+};
+
+// Phase split of the strided dgrad plus the flattened, zero-padded grad_out
+// frame V that turns every phase into shifted copies of one matrix:
+//   V[n][y][x] = grad_out[n][.][y - Ph][x - Pw]  (0 outside), y < Hv, x < Wp,
+//   flattened position  P = (n*Hv + y)*Wp + x.
+// Output (n, q, u) of any phase sits at P = (n*Hv + q)*Wp + u and its tap t
+// reads V at P + shift[t].  Hv and Wp are large enough that every read made
+// for a valid output either lands on the intended element or on a zero.
+struct Geometry {
+    int N, Ci, H, W, Co, kH, kW, s, ph, pw, oH, oW;
+    int n_phases;
+    PhaseDesc phase[kMaxPhases];
+    int n_taps;
+    TapDesc tap[kMaxTaps];
+    int Ph, Pw, Hv, Wp;
+    long long positions;   // N * Hv * Wp
+    int max_shift;
+};
+
+dgrad_status_t make_geometry(int N, int Ci, int H, int W, int Co, int kH, int kW,
+                             int stride, int pad_h, int pad_w, Geometry *g);
+
+// Tiling of the main kernel.
+struct Tiling {
+    int path;          // dgrad_path_t (SIMT or TCGEN05)
+    int tm;            // M blocks (kBlockM positions) per work unit
+    int bn;            // input channels per slice
+    int n_slices;
+    int kc;            // output channels per chunk (multiple of 8)
+    int n_chunks;
+    int n_tiles;
+    long long n_work;
+    int grid;
+    int a_rows;        // rows of one A stage
+    int a_stages, b_stages;
+    int b_resident;
+    int chunk_bytes;   // packed weight bytes of one (slice, chunk)
+    int acc_bufs;      // tensor-memory accumulator sets
+    int acc_cols;      // columns of one set
+    int tmem_cols;
+    int smem_bytes;
+    size_t packed_bytes;
+};
+
+dgrad_status_t choose_tiling(const Geometry &g, int precision, const dgrad_options_t *opts,
+                             int sm_count, Tiling *t);
+
+// ---------------------------------------------------------------- kernels
+// Packed weights: for slice sl, chunk c, tap t, channel group gq (4 output
+// channels), input channel j of the slice and e in [0,4):
+//   wp[((((sl*n_chunks + c)*n_taps + t)*(kc/4) + gq)*bn + j)*4 + e]
+//     = weight[co = c*kc + 4*gq + e][ci = sl*bn + j][kh_t][kw_t]   (0 if out of range)
+// so one (slice, chunk) is one contiguous block of chunk_bytes, and inside it
+// the 16-byte groups are the K-major "core matrix" rows of the GEMM's B.
+struct PrepackParams {
+    const float *w;
+    float *wp;
+    int Co, Ci, kH, kW;
+    int n_taps, bn, n_slices, kc, n_chunks;
+    int round_tf32;
+    long long total;   // floats written
+    int tap_kh[kMaxTaps];
+    int tap_kw[kMaxTaps];
+};
+
+struct MainParams {
+    const float *go;
+    const float *wp;
+    float *gi;
+    uint32_t *err;
+    int N, Ci, Co, H, W, oH, oW, s;
+    int Ph, Pw, Hv, Wp, HvWp;
+    int positions;
+    int tm, bn, n_slices, kc, n_chunks, n_tiles;
+    int n_work;
+    int a_rows, a_stages, b_stages, b_resident, chunk_bytes;
+    int acc_bufs, acc_cols, tmem_cols;
+    int round_tf32;
+    int n_phases, n_taps;
+    uint32_t idesc;
+    long long timeout_ns;
+    PhaseDesc phase[kMaxPhases];
+    TapDesc tap[kMaxTaps];
+};
+
+cudaError_t launch_prepack(const PrepackParams &p, cudaStream_t stream);
+cudaError_t launch_simt(const MainParams &p, const Tiling &t, cudaStream_t stream);
+cudaError_t launch_tc(const MainParams &p, const Tiling &t, cudaStream_t stream, bool pdl);
+
+}  // namespace dgrad

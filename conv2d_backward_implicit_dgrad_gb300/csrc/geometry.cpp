@@ -1,0 +1,279 @@
+// Host-side planning: the sub-pixel phase split, the zero-padded grad_out
+// frame, and the tiling of the main kernels.  No CUDA calls here, so
+// dgrad_describe() works without a device.
+#include <algorithm>
+#include <climits>
+#include <cstring>
+
+#include "dgrad_internal.h"
+
+namespace dgrad {
+
+namespace {
+
+int out_extent(int in, int k, int s, int p) {
+    long long num = (long long)in + 2LL * p - k;
+    if (num < 0) return 0;
+    return (int)(num / s + 1);
+}
+
+int ceil_div(int a, int b) { return (a + b - 1) / b; }
+int round_up(int a, int b) { return ceil_div(a, b) * b; }
+
+// Row (or column) taps of phase a along one axis.
+//
+// Input row ih = s*q + a receives kernel row kh exactly when
+// (a + pad - kh) is a multiple of s (meganeura's divisibility test, general-
+// stride branch of its B-tile load; doppler's "(py - ky) % stride" skip).
+// Those rows are kh = r + s*j with r = (a + pad) mod s, and they read
+// grad_out row oh = q + c - j with c = floor((a + pad)/s).  A tap whose
+// grad_out rows lie outside [0, o) for every output row q < nq only ever
+// meets padding; it contributes nothing and is dropped.
+struct AxisTaps {
+    int r, c, nq;
+    int count;
+    int j[64];
+};
+
+AxisTaps axis_taps(int a, int pad, int s, int k, int in, int o) {
+    AxisTaps t{};
+    t.r = (a + pad) % s;
+    t.c = (a + pad) / s;
+    t.nq = a < in ? ceil_div(in - a, s) : 0;
+    t.count = 0;
+    for (int j = 0; t.r + s * j < k; ++j) {
+        int lo = t.c - j, hi = t.c - j + t.nq - 1;   // grad_out rows read by q = 0 .. nq-1
+        if (t.nq > 0 && hi >= 0 && lo <= o - 1) t.j[t.count++] = j;
+    }
+    return t;
+}
+
+}  // namespace
+
+dgrad_status_t make_geometry(int N, int Ci, int H, int W, int Co, int kH, int kW,
+                             int stride, int pad_h, int pad_w, Geometry *g) {
+    if (N < 1 || Ci < 1 || H < 1 || W < 1 || Co < 1 || kH < 1 || kW < 1 || stride < 1 ||
+        pad_h < 0 || pad_w < 0)
+        return DGRAD_ERR_INVALID_ARG;
+    int oH = out_extent(H, kH, stride, pad_h), oW = out_extent(W, kW, stride, pad_w);
+    if (oH < 1 || oW < 1) return DGRAD_ERR_INVALID_ARG;
+    if (stride > kMaxStride || kH > 64 || kW > 64 || kH * kW > kMaxTaps) return DGRAD_ERR_UNSUPPORTED;
+    const long long lim = INT_MAX;
+    if ((long long)N * Co * oH * oW > lim || (long long)N * Ci * H * W > lim ||
+        (long long)Co * Ci * kH * kW > lim)
+        return DGRAD_ERR_UNSUPPORTED;
+
+    std::memset(g, 0, sizeof(*g));
+    g->N = N; g->Ci = Ci; g->H = H; g->W = W; g->Co = Co; g->kH = kH; g->kW = kW;
+    g->s = stride; g->ph = pad_h; g->pw = pad_w; g->oH = oH; g->oW = oW;
+
+    AxisTaps rows[kMaxStride], cols[kMaxStride];
+    for (int a = 0; a < stride; ++a) rows[a] = axis_taps(a, pad_h, stride, kH, H, oH);
+    for (int b = 0; b < stride; ++b) cols[b] = axis_taps(b, pad_w, stride, kW, W, oW);
+
+    // Leading zero rows/cols so that every kept tap has a non-negative offset.
+    int Ph = 0, Pw = 0;
+    for (int a = 0; a < stride; ++a)
+        for (int i = 0; i < rows[a].count; ++i) Ph = std::max(Ph, rows[a].j[i] - rows[a].c);
+    for (int b = 0; b < stride; ++b)
+        for (int i = 0; i < cols[b].count; ++i) Pw = std::max(Pw, cols[b].j[i] - cols[b].c);
+
+    int max_dr = 0, max_dc = 0, nq_max = 0, nu_max = 0;
+    int tap_dr[kMaxTaps], tap_dc[kMaxTaps];
+    g->n_phases = 0;
+    g->n_taps = 0;
+    for (int a = 0; a < stride; ++a) {
+        for (int b = 0; b < stride; ++b) {
+            const AxisTaps &R = rows[a], &C = cols[b];
+            if (R.nq == 0 || C.nq == 0) continue;   // no input element in this phase
+            PhaseDesc &p = g->phase[g->n_phases++];
+            p.a = a; p.b = b; p.Hq = R.nq; p.Wq = C.nq;
+            p.tap_begin = g->n_taps;
+            p.tap_count = R.count * C.count;
+            nq_max = std::max(nq_max, R.nq);
+            nu_max = std::max(nu_max, C.nq);
+            for (int x = 0; x < R.count; ++x)
+                for (int y = 0; y < C.count; ++y) {
+                    int j = R.j[x], i = C.j[y];
+                    TapDesc &t = g->tap[g->n_taps++];
+                    t.kh = R.r + stride * j;
+                    t.kw = C.r + stride * i;
+                    int dr = R.c - j + Ph, dc = C.c - i + Pw;
+                    max_dr = std::max(max_dr, dr);
+                    max_dc = std::max(max_dc, dc);
+                    tap_dr[g->n_taps - 1] = dr;
+                    tap_dc[g->n_taps - 1] = dc;
+                    t.shift = 0;   // set below once Wp is known
+                }
+        }
+    }
+    // Frame size: hold every grad_out row (oH + Ph) and every output row
+    // (nq_max), and let the deepest read of the last valid output row wrap
+    // only into the next image's leading zero rows (nq_max + max_dr - Ph).
+    // Same for columns, where a wrap lands in the next row's leading zeros.
+    int Hv = std::max(nq_max, std::max(oH + Ph, nq_max + max_dr - Ph));
+    int Wp = std::max(nu_max, std::max(oW + Pw, nu_max + max_dc - Pw));
+    g->Ph = Ph; g->Pw = Pw; g->Hv = Hv; g->Wp = Wp;
+    g->max_shift = 0;
+    for (int t = 0; t < g->n_taps; ++t) {
+        g->tap[t].shift = tap_dr[t] * Wp + tap_dc[t];
+        g->max_shift = std::max(g->max_shift, g->tap[t].shift);
+    }
+    g->positions = (long long)N * Hv * Wp;
+    if (g->positions + g->max_shift + 4LL * kBlockM > lim) return DGRAD_ERR_UNSUPPORTED;
+    return DGRAD_OK;
+}
+
+namespace {
+
+int pow2_at_least(int x) {
+    int p = 32;
+    while (p < x) p *= 2;
+    return p;
+}
+
+constexpr int kBarrierBytes = 1024;   // mbarriers and the TMEM address slot
+constexpr int kMaxResidentChunks = 32;
+
+// Fill the sizes that follow from (tm, bn, kc) for the tcgen05 path; returns
+// false when no pipeline depth fits in shared memory.
+bool size_tc(const Geometry &g, Tiling &t, int want_resident) {
+    t.n_slices = ceil_div(g.Ci, t.bn);
+    t.n_chunks = ceil_div(g.Co, t.kc);
+    t.a_rows = round_up(t.tm * kBlockM + g.max_shift, 8);
+    int a_bytes = t.a_rows * t.kc * 4;
+    t.chunk_bytes = g.n_taps * t.kc * t.bn * 4;
+    if (g.n_taps == 0) t.chunk_bytes = 0;
+    int budget = kMaxSmem - kBarrierBytes;
+    t.b_resident = 0;
+    if (want_resident && t.n_slices == 1 && t.n_chunks <= kMaxResidentChunks) {
+        long long b_all = (long long)t.n_chunks * t.chunk_bytes;
+        if (b_all + 2LL * a_bytes <= budget) {
+            t.b_resident = 1;
+            t.b_stages = t.n_chunks;
+            t.a_stages = (int)std::min<long long>(4, (budget - b_all) / a_bytes);
+        }
+    }
+    if (!t.b_resident) {
+        int bs = t.chunk_bytes > 0 ? 2 : 1;
+        if ((long long)bs * t.chunk_bytes + 2LL * a_bytes > budget) return false;
+        t.b_stages = bs;
+        t.a_stages = (int)std::min<long long>(4, (budget - (long long)bs * t.chunk_bytes) / a_bytes);
+        if (t.a_stages >= 4 && t.chunk_bytes > 0 &&
+            3LL * t.chunk_bytes + 3LL * a_bytes <= budget) {
+            t.b_stages = 3;
+            t.a_stages = 3;
+        }
+    }
+    if (t.a_stages < 2) return false;
+    t.smem_bytes = kBarrierBytes + t.a_stages * a_bytes + t.b_stages * t.chunk_bytes;
+    t.acc_cols = t.tm * g.n_phases * t.bn;
+    if (t.acc_cols > kTmemCols) return false;
+    t.acc_bufs = (2 * t.acc_cols <= kTmemCols) ? 2 : 1;
+    t.tmem_cols = pow2_at_least(t.acc_bufs * t.acc_cols);
+    t.n_tiles = (int)((g.positions + (long long)t.tm * kBlockM - 1) / ((long long)t.tm * kBlockM));
+    t.n_work = (long long)t.n_tiles * t.n_slices;
+    t.packed_bytes = (size_t)t.n_slices * t.n_chunks * (size_t)t.chunk_bytes;
+    return true;
+}
+
+bool size_simt(const Geometry &g, Tiling &t) {
+    t.tm = 1;
+    t.n_slices = ceil_div(g.Ci, t.bn);
+    t.n_chunks = ceil_div(g.Co, t.kc);
+    t.a_rows = round_up(kBlockM + g.max_shift, 8);
+    t.chunk_bytes = g.n_taps * t.kc * t.bn * 4;
+    int max_phase_taps = 0;
+    for (int p = 0; p < g.n_phases; ++p) max_phase_taps = std::max(max_phase_taps, g.phase[p].tap_count);
+    int a_bytes = t.a_rows * t.kc * 4;
+    int b_bytes = max_phase_taps * t.kc * t.bn * 4;
+    t.a_stages = 1;
+    t.b_stages = 1;
+    t.b_resident = 0;
+    t.smem_bytes = a_bytes + b_bytes;
+    if (t.smem_bytes > kMaxSmem) return false;
+    t.acc_bufs = t.acc_cols = t.tmem_cols = 0;
+    t.n_tiles = (int)((g.positions + kBlockM - 1) / kBlockM);
+    t.n_work = (long long)t.n_tiles * t.n_slices * g.n_phases;
+    t.grid = 0;
+    t.packed_bytes = (size_t)t.n_slices * t.n_chunks * (size_t)t.chunk_bytes;
+    return true;
+}
+
+}  // namespace
+
+dgrad_status_t choose_tiling(const Geometry &g, int precision, const dgrad_options_t *opts,
+                             int sm_count, Tiling *out) {
+    dgrad_options_t o{};
+    if (opts) o = *opts;
+    if (sm_count < 1) sm_count = 148;
+    int path = o.path;
+    if (path == DGRAD_PATH_AUTO) path = (precision == DGRAD_PREC_TF32) ? DGRAD_PATH_TCGEN05 : DGRAD_PATH_SIMT;
+    if (path != DGRAD_PATH_SIMT && path != DGRAD_PATH_TCGEN05) return DGRAD_ERR_INVALID_ARG;
+    if (path == DGRAD_PATH_TCGEN05 && precision != DGRAD_PREC_TF32) return DGRAD_ERR_UNSUPPORTED;
+    if (o.slice_n && (o.slice_n % 16 || o.slice_n > 256)) return DGRAD_ERR_INVALID_ARG;
+    if (o.chunk_k && (o.chunk_k % 8 || o.chunk_k > 64)) return DGRAD_ERR_INVALID_ARG;
+    if (o.tile_blocks < 0 || o.tile_blocks > 4 || o.grid < 0) return DGRAD_ERR_INVALID_ARG;
+
+    Tiling t{};
+    t.path = path;
+    if (path == DGRAD_PATH_SIMT) {
+        int ci16 = round_up(g.Ci, 16);
+        t.bn = o.slice_n ? o.slice_n : (ci16 <= 16 ? 16 : ci16 <= 32 ? 32 : 64);
+        if (t.bn != 16 && t.bn != 32 && t.bn != 64) return DGRAD_ERR_INVALID_ARG;
+        t.kc = o.chunk_k ? o.chunk_k : 16;
+        if (t.kc != 8 && t.kc != 16 && t.kc != 32) return DGRAD_ERR_INVALID_ARG;
+        if (!size_simt(g, t)) return DGRAD_ERR_UNSUPPORTED;
+        *out = t;
+        return DGRAD_OK;
+    }
+
+    // tcgen05: one MMA block is 128 positions x bn input channels; every
+    // active phase has its own fp32 accumulator in tensor memory.
+    int ci16 = round_up(g.Ci, 16);
+    int bn_cap = std::min(256, (kTmemCols / g.n_phases) / 16 * 16);
+    int bn = std::min(ci16, bn_cap);
+    int tiles1 = (int)((g.positions + kBlockM - 1) / kBlockM);
+    // Split the channels when the position tiles alone cannot fill the GPU.
+    while (!o.slice_n && bn > 64 && (long long)tiles1 * ceil_div(g.Ci, bn) < sm_count &&
+           (bn / 2) % 16 == 0)
+        bn /= 2;
+    if (o.slice_n) bn = o.slice_n;
+    if (g.n_phases * bn > kTmemCols) return DGRAD_ERR_UNSUPPORTED;
+
+    int tm_pref[4] = {0, 0, 0, 0};
+    int n_tm = 0;
+    if (o.tile_blocks) {
+        tm_pref[n_tm++] = o.tile_blocks;
+    } else {
+        long long units2 = (long long)ceil_div(tiles1, 2) * ceil_div(g.Ci, bn);
+        if (units2 >= 2LL * sm_count) tm_pref[n_tm++] = 2;
+        tm_pref[n_tm++] = 1;
+    }
+    if (o.chunk_k && o.chunk_k != 8 && o.chunk_k != 16 && o.chunk_k != 32) return DGRAD_ERR_INVALID_ARG;
+    int kc_pref[3] = {32, 16, 8};
+    bool ok = false;
+    for (int i = 0; i < n_tm && !ok; ++i) {
+        for (int want_res = 1; want_res >= 0 && !ok; --want_res) {
+            for (int k = 0; k < 3 && !ok; ++k) {
+                int kc = o.chunk_k ? o.chunk_k : kc_pref[k];
+                Tiling c = t;
+                c.tm = tm_pref[i];
+                c.bn = bn;
+                c.kc = kc;
+                if (size_tc(g, c, want_res) && (c.a_stages >= 3 || c.b_resident || kc == 8 || o.chunk_k)) {
+                    t = c;
+                    ok = true;
+                }
+                if (o.chunk_k) break;
+            }
+        }
+    }
+    if (!ok) return DGRAD_ERR_UNSUPPORTED;
+    long long grid = o.grid ? o.grid : std::min<long long>(t.n_work, sm_count);
+    t.grid = (int)std::max<long long>(1, std::min<long long>(grid, t.n_work));
+    *out = t;
+    return DGRAD_OK;
+}
+
+}  // namespace dgrad

@@ -1,0 +1,192 @@
+/*
+ * dgrad.h -- C ABI of libdgrad_gb300.so: convolution backward-data (dgrad) on
+ * one NVIDIA GB300 (sm_103a).
+ *
+ * Operation (meganeura, src/shaders/conv2d_grad_input_gemm.wgsl, header
+ * comment and Params struct; @simulatte/doppler 0.1.0,
+ * conv2d_backward_input.wgsl, header comment and "forward mapping" comment):
+ *
+ *   grad_input[n,ci,ih,iw] = sum over (co,kh,kw) of
+ *                            grad_out[n,co,oh,ow] * weight[co,ci,kh,kw]
+ *   where ih = oh*stride - pad_h + kh and iw = ow*stride - pad_w + kw,
+ *
+ * i.e. the input-adjoint of a 2-D convolution with one stride, symmetric
+ * padding pad_h (rows) and pad_w (columns), dilation 1 and one group.  Per
+ * batch item it is the implicit GEMM C[Ci, H*W] = W^T[Ci, Co*kH*kW] x
+ * im2col(grad_out)[Co*kH*kW, H*W] (meganeura's header comment).
+ *
+ * Tensors (all fp32, contiguous, row-major; layouts from meganeura's storage
+ * declarations):
+ *   grad_out   [N, Co, oH, oW]   NCHW
+ *   weight     [Co, Ci, kH, kW]  OIHW
+ *   grad_input [N, Ci, H, W]     NCHW
+ * with oH = floor((H + 2*pad_h - kH)/stride) + 1 and likewise oW.  H and W are
+ * the authoritative input size; input rows or columns that no term reaches are
+ * written as 0.
+ *
+ * Semantics shared by every entry point:
+ *  - grad_input is fully OVERWRITTEN (both pages store the sum, never add to
+ *    the destination).  grad_out and weight are never written.
+ *  - Ownership: the caller owns the three tensors.  A plan owns its device
+ *    workspace (the packed weights, a device error word) and is bound to the
+ *    CUDA device that was current when it was created.
+ *  - Errors are returned as dgrad_status_t; nothing aborts the process and no
+ *    kernel traps.  Kernel waits are bounded: a wait that runs out records
+ *    DGRAD_ERR_DEVICE_TIMEOUT in the plan's device error word, which
+ *    dgrad_plan_check() reports once the stream has been synchronised.
+ *  - Not supported (neither page has them): dilation, groups, different row
+ *    and column strides, asymmetric per-side padding, output padding.
+ *  - Limits: kH*kW <= 128 kernel taps, stride <= 4, all extents and element
+ *    counts below 2^31.  Larger shapes return DGRAD_ERR_UNSUPPORTED.
+ *  - Streams are passed as `void *` holding a cudaStream_t (NULL = the legacy
+ *    default stream) so this header needs no CUDA include.
+ */
+#ifndef DGRAD_GB300_H
+#define DGRAD_GB300_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct dgrad_plan_s *dgrad_plan_t;
+
+typedef enum {
+    DGRAD_OK = 0,
+    DGRAD_ERR_INVALID_ARG = 1,    /* a dimension <= 0, stride < 1, pad < 0, oH or oW < 1, NULL plan */
+    DGRAD_ERR_UNSUPPORTED = 2,    /* outside the limits above */
+    DGRAD_ERR_MISALIGNED = 3,     /* a tensor pointer is NULL or not 16-byte aligned */
+    DGRAD_ERR_ALIAS = 4,          /* grad_input overlaps grad_out or weight */
+    DGRAD_ERR_OOM = 5,            /* workspace allocation failed */
+    DGRAD_ERR_CUDA = 6,           /* a CUDA runtime call or kernel launch failed */
+    DGRAD_ERR_DEVICE_TIMEOUT = 7, /* a bounded in-kernel wait ran out (reported by dgrad_plan_check) */
+    DGRAD_ERR_NO_DEVICE = 8,      /* no CUDA device, or the device is not sm_103 */
+    DGRAD_ERR_WRONG_DEVICE = 9    /* the current device is not the plan's device */
+} dgrad_status_t;
+
+/* Arithmetic of the contraction.
+ *  FP32: exact fp32 products, fp32 accumulation (FFMA on the CUDA cores).
+ *  TF32: both operands rounded to TF32 (round to nearest, ties away from zero),
+ *        products accumulated in fp32 on the tcgen05 tensor cores. */
+typedef enum { DGRAD_PREC_FP32 = 0, DGRAD_PREC_TF32 = 1 } dgrad_precision_t;
+
+/* Kernel family.  AUTO picks TCGEN05 for TF32 and SIMT for FP32. */
+typedef enum {
+    DGRAD_PATH_AUTO = 0,
+    DGRAD_PATH_SIMT = 1,     /* FFMA implicit GEMM (exact fp32; also accepts TF32-rounded operands) */
+    DGRAD_PATH_TCGEN05 = 2   /* warp-specialised tcgen05/TMEM implicit GEMM (TF32 only) */
+} dgrad_path_t;
+
+/* Optional tuning overrides for dgrad_plan_ex / dgrad_describe; 0 = automatic. */
+typedef struct {
+    int path;          /* dgrad_path_t */
+    int tile_blocks;   /* 128-position M blocks per work unit (tcgen05 path) */
+    int slice_n;       /* input channels per work unit (GEMM N), multiple of 16 */
+    int chunk_k;       /* output channels per pipeline stage, multiple of 8 */
+    int grid;          /* CTAs launched (persistent kernels) */
+    int sm_count;      /* dgrad_describe only: SM count to plan for */
+} dgrad_options_t;
+
+/* Everything a plan decided, for tests, benchmarks and logs. */
+typedef struct {
+    int N, Ci, H, W, Co, kH, kW, stride, pad_h, pad_w;
+    int oH, oW;
+    int precision;         /* dgrad_precision_t */
+    int path;              /* dgrad_path_t actually used */
+    int n_phases;          /* sub-pixel phases with at least one output (<= stride^2) */
+    int n_taps;            /* kernel taps kept over all phases (taps that only ever meet padding are dropped) */
+    int Ph, Pw, Hv, Wp;    /* zero-padded grad_out frame: Ph/Pw leading zero rows/cols, Hv x Wp per image */
+    long long positions;   /* N*Hv*Wp flattened output positions (GEMM M before tiling) */
+    int max_shift;         /* largest tap offset in flattened positions */
+    int tile_blocks, slice_n, n_slices, chunk_k, n_chunks;
+    long long n_work;      /* work units of the main kernel */
+    int grid;              /* CTAs of the main kernel */
+    int b_resident;        /* 1: packed weights stay in shared memory for the whole launch */
+    int smem_bytes;        /* dynamic shared memory of the main kernel */
+    int tmem_cols;         /* tensor-memory columns allocated per CTA (tcgen05 path) */
+    size_t workspace_bytes;/* device workspace owned by the plan */
+    size_t packed_weight_bytes;
+    double useful_flops;   /* 2*N*Co*oH*oW*Ci*kH*kW */
+    double algorithmic_bytes; /* 4*(|grad_out| + |weight| + |grad_input|) */
+} dgrad_plan_info_t;
+
+/* Create a plan on the current CUDA device: validates the shape, derives the
+ * sub-pixel phase and tap tables, picks tiles and allocates the device
+ * workspace (cudaMalloc).  On success *plan_out owns that memory until
+ * dgrad_plan_destroy.  On failure *plan_out is set to NULL. */
+dgrad_status_t dgrad_plan(int N, int Ci, int H, int W, int Co, int kH, int kW,
+                          int stride, int pad_h, int pad_w,
+                          dgrad_precision_t precision, dgrad_plan_t *plan_out);
+
+/* Same as dgrad_plan with tuning overrides (opts may be NULL). */
+dgrad_status_t dgrad_plan_ex(int N, int Ci, int H, int W, int Co, int kH, int kW,
+                             int stride, int pad_h, int pad_w,
+                             dgrad_precision_t precision, const dgrad_options_t *opts,
+                             dgrad_plan_t *plan_out);
+
+/* Host-only: the decisions dgrad_plan_ex would take for opts->sm_count SMs
+ * (148 if 0), without touching any device.  Fills *info. */
+dgrad_status_t dgrad_describe(int N, int Ci, int H, int W, int Co, int kH, int kW,
+                              int stride, int pad_h, int pad_w,
+                              dgrad_precision_t precision, const dgrad_options_t *opts,
+                              dgrad_plan_info_t *info);
+
+/* Host-only: the sub-pixel phase and tap tables behind dgrad_describe, for
+ * checking the decomposition without a device.  Writes up to `cap` phases
+ * (a, b, Hq, Wq, tap_begin, tap_count: 6 ints each, into `phases`) and up to
+ * `cap` taps (kh, kw, shift: 3 ints each, into `taps`); *n_phases and *n_taps
+ * receive the full counts.  Phase (a, b) holds input rows ih = stride*q + a
+ * and columns iw = stride*u + b, q < Hq, u < Wq; its output (n, q, u) is the
+ * flattened frame position (n*Hv + q)*Wp + u, and tap t of the phase reads
+ * the zero-padded grad_out frame at that position plus shift (see
+ * dgrad_plan_info_t for Ph, Pw, Hv, Wp). */
+dgrad_status_t dgrad_describe_taps(int N, int Ci, int H, int W, int Co, int kH, int kW,
+                                   int stride, int pad_h, int pad_w, int cap,
+                                   int *phases, int *n_phases, int *taps, int *n_taps);
+
+/* Copy the plan's decisions into *info. */
+dgrad_status_t dgrad_plan_info(dgrad_plan_t plan, dgrad_plan_info_t *info);
+
+/* Compute grad_input from grad_out and weight, asynchronously on `stream`.
+ * All three are DEVICE pointers on the plan's device, 16-byte aligned, shaped
+ * as above.  Launches the weight pre-pack kernel and then the main kernel,
+ * both on `stream`.  One plan must not run on two streams at once (they would
+ * share the packed-weight workspace).  Returns after the launches; errors
+ * detected inside the kernels surface through dgrad_plan_check. */
+dgrad_status_t dgrad_run(dgrad_plan_t plan, const float *grad_out, const float *weight,
+                         float *grad_input, void *stream);
+
+/* The two halves of dgrad_run, for callers whose weights stay fixed over
+ * several calls: dgrad_prepack packs `weight` into the plan's workspace (the
+ * weight pre-pack kernel), dgrad_run_packed runs the main kernel on the
+ * weights packed last.  Same pointer rules, stream order and errors as
+ * dgrad_run; dgrad_run_packed before any dgrad_prepack on the plan returns
+ * DGRAD_ERR_INVALID_ARG. */
+dgrad_status_t dgrad_prepack(dgrad_plan_t plan, const float *weight, void *stream);
+dgrad_status_t dgrad_run_packed(dgrad_plan_t plan, const float *grad_out, float *grad_input,
+                                void *stream);
+
+/* The same computation from HOST buffers: copies grad_out and weight to
+ * device staging buffers owned by the plan (allocated on the first call),
+ * runs dgrad_run, copies grad_input back and synchronises `stream`.  Page-
+ * locked host buffers give the fastest copies; pageable ones also work. */
+dgrad_status_t dgrad_run_host(dgrad_plan_t plan, const float *grad_out_host,
+                              const float *weight_host, float *grad_input_host,
+                              void *stream);
+
+/* Read and clear the plan's device error word.  Call after synchronising the
+ * stream of the last dgrad_run.  Returns DGRAD_OK or the recorded error. */
+dgrad_status_t dgrad_plan_check(dgrad_plan_t plan);
+
+/* Free the plan's workspace (synchronises the plan's device first). NULL is a no-op. */
+void dgrad_plan_destroy(dgrad_plan_t plan);
+
+/* Static English description of a status code. */
+const char *dgrad_status_string(dgrad_status_t status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DGRAD_GB300_H */

@@ -1,0 +1,174 @@
+"""Host-side checks of the C ABI (no GPU): the library loads, exports every
+function include/dgrad.h declares, validates shapes, and its phase / tap /
+frame tables reproduce the oracle when the main kernels' arithmetic is
+emulated with numpy on the CPU."""
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle
+import conv2d_backward_implicit_dgrad_gb300 as dg
+from conv2d_backward_implicit_dgrad_gb300 import binding
+from conv2d_backward_implicit_dgrad_gb300.workloads import ORDER, WORKLOADS, make_tensors
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def header_functions():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if not fn.endswith(".h"):
+            continue
+        src = open(os.path.join(ROOT, "include", fn)).read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        for m in re.finditer(r"^[A-Za-z_][\w\s\*]*?\b(dgrad_\w+)\s*\(", src, flags=re.M):
+            names.add(m.group(1))
+    return names
+
+
+def test_library_exports_every_declared_function():
+    lib = dg.load_library()
+    declared = header_functions()
+    assert declared, "no declarations found"
+    assert declared == set(binding.EXPORTS)
+    for name in declared:
+        assert hasattr(lib, name), name
+
+
+def test_status_strings():
+    lib = dg.load_library()
+    for code in range(10):
+        assert lib.dgrad_status_string(code)
+    assert lib.dgrad_status_string(99) == b"unknown status"
+
+
+@pytest.mark.parametrize("bad", [
+    (0, 1, 4, 4, 1, 3, 3, 1, 1, 1), (1, 0, 4, 4, 1, 3, 3, 1, 1, 1), (1, 1, 4, 4, 1, 3, 3, 0, 1, 1),
+    (1, 1, 4, 4, 1, 3, 3, 1, -1, 1), (1, 1, 2, 2, 1, 5, 5, 1, 0, 0), (1, 1, 4, 4, 0, 3, 3, 1, 1, 1)])
+def test_describe_rejects_invalid(bad):
+    with pytest.raises(dg.DgradError) as e:
+        dg.describe(*bad)
+    assert e.value.status == 1
+
+
+@pytest.mark.parametrize("bad", [(1, 1, 32, 32, 1, 3, 3, 5, 1, 1), (1, 1, 40, 40, 1, 12, 12, 1, 0, 0)])
+def test_describe_rejects_unsupported(bad):
+    with pytest.raises(dg.DgradError) as e:
+        dg.describe(*bad)
+    assert e.value.status == 2
+
+
+def test_describe_rejects_bad_options():
+    with pytest.raises(dg.DgradError) as e:
+        dg.describe(2, 8, 8, 8, 8, 3, 3, 1, 1, 1, "fp32", path="tcgen05")
+    assert e.value.status == 2
+    for bad in (dict(slice_n=24), dict(chunk_k=12), dict(tile_blocks=5)):
+        with pytest.raises(dg.DgradError) as e:
+            dg.describe(2, 8, 8, 8, 8, 3, 3, 1, 1, 1, "tf32", **bad)
+        assert e.value.status == 1
+
+
+def test_plan_without_device_fails_cleanly():
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    with pytest.raises(dg.DgradError) as e:
+        dg.Plan(1, 1, 4, 4, 1, 3, 3, 1, 1, 1)
+    assert e.value.status in (8, 6)
+
+
+@pytest.mark.parametrize("name", ORDER)
+def test_describe_workloads(name):
+    wl = WORKLOADS[name]
+    for prec in ("tf32", "fp32"):
+        d = dg.describe(*wl.plan_args(), precision=prec)
+        assert (d["oH"], d["oW"]) == (wl.oH, wl.oW)
+        assert d["useful_flops"] == 2 * wl.N * wl.Co * wl.oH * wl.oW * wl.Ci * wl.kH * wl.kW
+        assert d["path"] == ("tcgen05" if prec == "tf32" else "simt")
+        assert d["n_phases"] == min(wl.stride, wl.H) * min(wl.stride, wl.W)
+        assert d["smem_bytes"] <= 232448
+        if prec == "tf32":
+            assert 32 <= d["tmem_cols"] <= 512
+            assert d["slice_n"] % 16 == 0 and 16 <= d["slice_n"] <= 256
+            assert d["grid"] <= 148
+
+
+def test_phase_taps_partition_the_kernel():
+    # Every kernel tap belongs to exactly one phase when none is pruned.
+    phases, taps = dg.describe_taps(2, 3, 28, 28, 4, 3, 3, 2, 1, 1)
+    assert sorted((t["kh"], t["kw"]) for t in taps) == [(kh, kw) for kh in range(3) for kw in range(3)]
+    assert sum(p["tap_count"] for p in phases) == 9
+    phases, taps = dg.describe_taps(2, 3, 224, 224, 4, 7, 7, 2, 3, 3)
+    assert sorted(p["tap_count"] for p in phases) == [9, 12, 12, 16]
+    phases, taps = dg.describe_taps(2, 3, 8, 8, 4, 1, 1, 2, 0, 0)   # 1x1 stride 2: three phases have no taps
+    assert sorted(p["tap_count"] for p in phases) == [0, 0, 0, 1]
+
+
+def test_padding_only_taps_are_pruned():
+    # H = 2, k = 3, pad 1, stride 2: kernel row 0 only ever meets padding.
+    phases, taps = dg.describe_taps(1, 1, 2, 2, 1, 3, 3, 2, 1, 1)
+    assert all(t["kh"] != 0 and t["kw"] != 0 for t in taps)
+
+
+def emulate(go, w, H, W, s, ph, pw):
+    """The main kernels' arithmetic in numpy, driven only by the library's tables:
+    shifted windows of the zero-padded flattened frame, one GEMM per tap and phase."""
+    N, Co, oH, oW = go.shape
+    _, Ci, kH, kW = w.shape
+    info = dg.describe(N, Ci, H, W, Co, kH, kW, s, ph, pw)
+    phases, taps = dg.describe_taps(N, Ci, H, W, Co, kH, kW, s, ph, pw)
+    Ph, Pw, Hv, Wp = info["Ph"], info["Pw"], info["Hv"], info["Wp"]
+    assert Hv >= oH + Ph and Wp >= oW + Pw
+    P = N * Hv * Wp
+    V = np.zeros((P + info["max_shift"] + 8, Co))
+    frame = np.zeros((N, Hv, Wp, Co))
+    frame[:, Ph:Ph + oH, Pw:Pw + oW, :] = go.transpose(0, 2, 3, 1)
+    V[:P] = frame.reshape(P, Co)
+    gi = np.full((N, Ci, H, W), np.nan)
+    pos = np.arange(P)
+    n_idx, rem = pos // (Hv * Wp), pos % (Hv * Wp)
+    q_idx, u_idx = rem // Wp, rem % Wp
+    for p in phases:
+        D = np.zeros((P, Ci))
+        for t in taps[p["tap_begin"]:p["tap_begin"] + p["tap_count"]]:
+            D += V[t["shift"]:t["shift"] + P] @ w[:, :, t["kh"], t["kw"]].astype(np.float64)
+        ok = (q_idx < p["Hq"]) & (u_idx < p["Wq"])
+        ih, iw = s * q_idx[ok] + p["a"], s * u_idx[ok] + p["b"]
+        for ci in range(Ci):
+            gi[n_idx[ok], ci, ih, iw] = D[ok, ci]
+    return gi
+
+
+EMU_SHAPES = [
+    (2, 3, 4, 8, 8, 3, 3, 1, 1, 1), (1, 2, 3, 7, 5, 3, 3, 1, 0, 0), (2, 2, 3, 6, 7, 5, 3, 1, 2, 1),
+    (1, 2, 3, 9, 9, 3, 3, 2, 1, 1), (2, 3, 2, 8, 7, 3, 3, 2, 0, 0), (1, 2, 2, 9, 10, 7, 7, 2, 3, 3),
+    (1, 2, 3, 10, 9, 3, 3, 3, 1, 1), (2, 3, 2, 6, 6, 1, 1, 2, 0, 0), (1, 2, 2, 8, 8, 2, 2, 2, 0, 0),
+    (1, 2, 2, 9, 8, 4, 3, 2, 1, 2), (1, 1, 2, 2, 2, 3, 3, 2, 1, 1), (2, 2, 2, 5, 6, 3, 5, 1, 2, 2),
+    (1, 2, 2, 11, 12, 5, 5, 3, 2, 2), (1, 1, 1, 1, 1, 1, 1, 1, 0, 0), (1, 2, 3, 3, 3, 3, 3, 1, 2, 2),
+    (3, 2, 3, 4, 13, 1, 3, 1, 0, 1), (1, 2, 2, 13, 13, 3, 3, 4, 1, 1), (1, 1, 2, 1, 9, 1, 3, 2, 0, 1),
+]
+
+
+@pytest.mark.parametrize("shape", EMU_SHAPES)
+def test_emulated_decomposition_matches_oracle(shape):
+    N, Ci, Co, H, W, kH, kW, s, ph, pw = shape
+    oH, oW = (H + 2 * ph - kH) // s + 1, (W + 2 * pw - kW) // s + 1
+    go, w = make_tensors((N, Co, oH, oW), (Co, Ci, kH, kW), 61, "uniform")
+    go, w = go.numpy(), w.numpy()
+    ref, _ = oracle.dgrad(go, w, H, W, s, ph, pw)
+    emu = emulate(go, w, H, W, s, ph, pw)
+    assert not np.isnan(emu).any(), "an input element was never written"
+    np.testing.assert_allclose(emu, ref, rtol=1e-12, atol=1e-12)
+
+
+@pytest.mark.parametrize("name", ["tiny", "strided_downsample"])
+def test_emulated_decomposition_workload_shapes(name):
+    wl = WORKLOADS[name]
+    N = min(wl.N, 1)
+    go, w = make_tensors((N, wl.Co, wl.oH, wl.oW), wl.w_shape, 62, wl.dist)
+    go, w = go.numpy(), w.numpy()
+    ref, _ = oracle.dgrad(go, w, wl.H, wl.W, wl.stride, wl.pad_h, wl.pad_w)
+    emu = emulate(go, w, wl.H, wl.W, wl.stride, wl.pad_h, wl.pad_w)
+    np.testing.assert_allclose(emu, ref, rtol=1e-10, atol=1e-10)
