@@ -1,0 +1,390 @@
+#!/usr/bin/env python
+"""Benchmark: dgrad useful TFLOP/s, % of the GB300 TF32 roofline, us per call.
+
+One step = one pass of the whole hot path on one batch: the weight pre-pack
+kernel plus the main implicit-GEMM kernel, through the C ABI
+(dgrad_prepack + dgrad_run_packed), inputs resident in HBM.  L2 is flushed
+(256 MiB write) before every timed step, outside the timed events.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--precision tf32|fp32]
+  python bench.py --impl reference ...   # the CPU oracle on the host cores
+
+With N > 1 (torchrun, one rank per GPU) every rank runs an independent
+replica of the workload (the batch shards with no collective on the data
+path); ``value`` is the total useful FLOPs of all ranks / the slowest rank's
+time.  Prints one JSON line on rank 0.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "dgrad useful TFLOP/s and % of GB300 TF32 roofline at 1 GPU; µs per call"
+TF32_OVER_BF16 = 1.1 / 2.25          # nominal dense TF32 / BF16 ratio
+FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "sm_max_mhz": 2070.0}
+FLUSH_BYTES = 256 << 20
+MAIN_KERNEL_SOURCES = ["tc_kernel.cu", "simt_kernel.cu", "gather.cuh", "ptx.cuh", "dgrad_internal.h"]
+WORKLOAD_ORDER = ("tiny", "resnet_stage", "strided_downsample", "pointwise", "stem")
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return json.load(f), "measured"
+    return dict(FALLBACK), "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for name in MAIN_KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "conv2d_backward_implicit_dgrad_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload, precision):
+    """DRAM bytes per launch of the main kernel from the committed ncu summary,
+    only while the kernel sources are unchanged since the capture."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        rec = json.load(f)
+    e = rec.get(f"{workload}/{precision}")
+    if not e or e.get("source_hash") != kernel_source_hash():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons while the GPU works."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=5)
+        sms, maxs, power, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sms.append(float(parts[1]))
+                maxs.append(float(parts[2]))
+                power.append(float(parts[3]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sms) if sms else None, "sm_max_mhz": max(maxs) if maxs else None,
+                "power_w_max": max(power) if power else None, "reasons": sorted(reasons), "samples": len(sms)}
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def cpu_oracle_run(wl, images, seed=0, reps=1):
+    """Time the oracle (as it stands) on the first `images` images of the workload."""
+    import oracle
+    from conv2d_backward_implicit_dgrad_gb300.workloads import make_tensors
+    go, w = make_tensors((images, wl.Co, wl.oH, wl.oW), wl.w_shape, seed, wl.dist)
+    go, w = go.numpy(), w.numpy()
+    cores = cpu_cores()
+    oracle.build()
+    times = []
+    for _ in range(reps):
+        t0 = time.perf_counter()
+        oracle.dgrad(go, w, wl.H, wl.W, wl.stride, wl.pad_h, wl.pad_w, nthreads=cores)
+        times.append(time.perf_counter() - t0)
+    flops = 2.0 * images * wl.Co * wl.oH * wl.oW * wl.Ci * wl.kH * wl.kW
+    return flops, times, min(cores, images)
+
+
+def wl_config(wl):
+    return {"workload": wl.name, **{k: getattr(wl, k) for k in ("N", "Ci", "Co", "H", "W", "kH", "kW", "stride",
+                                                                "pad_h", "pad_w")}}
+
+
+def reference_arm(args, wl):
+    if int(os.environ.get("RANK", "0")) != 0:
+        return 0
+    images = min(wl.N, 8)
+    for _ in range(args.warmup):
+        cpu_oracle_run(wl, images)
+    step_times = []
+    flops, cores = 0.0, 1
+    for _ in range(args.steps):
+        flops, times, cores = cpu_oracle_run(wl, images)
+        step_times.append(times[0])
+    t = statistics.mean(step_times)
+    value = flops / t / 1e12
+    sample = f"{images} of {wl.N} images of {wl.name} per step (fp64 scatter oracle, {cores} threads)"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": t * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": wl_config(wl),
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def time_workload(dg, torch, wl, precision, steps, warmup, rank, barrier, device_index, clocks, e2e):
+    from conv2d_backward_implicit_dgrad_gb300.workloads import make_inputs
+    go_h, w_h = make_inputs(wl, seed=rank)
+    go, w = go_h.cuda(), w_h.cuda()
+    gi = torch.empty(wl.gi_shape, device="cuda")
+    flush = torch.empty(FLUSH_BYTES // 4, device="cuda")
+    plan = dg.Plan(*wl.plan_args(), precision=precision)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        plan.prepack(w, stream)
+        plan.run_packed(go, gi, stream)
+
+    for _ in range(max(3, warmup)):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    plan.check()
+
+    sampler = ClockSampler(device_index) if clocks else None
+    if sampler:
+        sampler.start()
+        # keep the GPU under this load long enough for the sampler to see it
+        t_end = time.perf_counter() + 1.0
+        while time.perf_counter() < t_end:
+            flush.zero_()
+            step()
+        torch.cuda.synchronize()
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+    torch.cuda.synchronize()
+    barrier()
+    for i in range(steps):
+        flush.zero_()
+        ev[i][0].record(stream)
+        plan.prepack(w, stream)
+        ev[i][1].record(stream)
+        plan.run_packed(go, gi, stream)
+        ev[i][2].record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    clock_info = sampler.stop() if sampler else None
+    plan.check()
+    step_ms = statistics.mean(e[0].elapsed_time(e[2]) for e in ev)
+    main_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
+    prepack_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
+
+    # The fused public call (pre-pack and main kernel chained with
+    # programmatic dependent launch), same flushing, for comparison.
+    fe = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(steps)]
+    for i in range(steps):
+        flush.zero_()
+        fe[i][0].record(stream)
+        plan.run(go, w, gi, stream)
+        fe[i][1].record(stream)
+    torch.cuda.synchronize()
+    fused_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in fe)
+
+    e2e_s = None
+    if e2e:
+        go_p, w_p = go_h.pin_memory(), w_h.pin_memory()
+        gi_p = torch.empty(wl.gi_shape, pin_memory=True)
+        for _ in range(3):
+            plan.run_host(go_p, w_p, gi_p, stream)
+        ts = []
+        for _ in range(max(5, min(steps, 50))):
+            flush.zero_()
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            plan.run_host(go_p, w_p, gi_p, stream)   # H2D copies, both kernels, D2H copy, stream sync
+            ts.append(time.perf_counter() - t0)
+        e2e_s = statistics.mean(ts)
+        plan.check()
+    info = plan.info
+    plan.close()
+    return {"ms_per_step": step_ms, "main_ms": main_ms, "prepack_ms": prepack_ms, "fused_ms": fused_ms,
+            "e2e_s": e2e_s, "clocks": clock_info, "plan": info, "flops": info["useful_flops"],
+            "bytes": info["algorithmic_bytes"], "steps": steps}
+
+
+def roofline(wl, precision, flops, nbytes, main_s, step_s):
+    peaks, src = load_peaks()
+    hbm = peaks["hbm_gbs"]
+    if precision == "tf32":
+        peak_tf = peaks["bf16_tflops"] * TF32_OVER_BF16
+        note = f"TF32 = {src} bf16 burst {peaks['bf16_tflops']} TFLOP/s x nominal 1.1/2.25"
+    else:
+        # FP32 FFMA: 148 SMs x 128 FMA/clk x 2 FLOP at the maximum SM clock.
+        peak_tf = 148 * 128 * 2 * peaks.get("sm_max_mhz", 2070.0) * 1e6 / 1e12
+        note = "FP32 FFMA = 148 SMs x 256 FLOP/clk x max SM clock"
+    t_flop = flops / (peak_tf * 1e12)
+    t_hbm = nbytes / (hbm * 1e9)
+    if t_flop >= t_hbm:
+        bound = "tensor" if precision == "tf32" else "alu"
+    else:
+        bound = "hbm"
+    achieved = flops / main_s / 1e12
+    return {
+        "bound": bound, "achieved": achieved, "peak": peak_tf, "unit": "TFLOP/s", "frac": achieved / peak_tf,
+        "traffic": recorded_traffic(wl.name, precision),
+        "kernel": "tc_dgrad_kernel" if precision == "tf32" else "simt_dgrad_kernel",
+        "peak_source": f"{note} ({src}); HBM {hbm} GB/s ({src})",
+        "roofline_us": max(t_flop, t_hbm) * 1e6,
+        "frac_of_roofline_step": max(t_flop, t_hbm) / step_s,
+        "frac_of_roofline_kernel": max(t_flop, t_hbm) / main_s,
+        "hbm_gbs_achieved_kernel": nbytes / main_s / 1e9,
+    }
+
+
+def build_line(args, wl, r, world):
+    flops, nbytes = r["flops"], r["bytes"]
+    step_s, main_s = r["ms_per_step"] * 1e-3, r["main_ms"] * 1e-3
+    value = world * flops / step_s / 1e12
+    go_b = 4 * wl.N * wl.Co * wl.oH * wl.oW
+    w_b = 4 * wl.Co * wl.Ci * wl.kH * wl.kW
+    gi_b = 4 * wl.N * wl.Ci * wl.H * wl.W
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": r["steps"],
+        "warmup": args.warmup, "ms_per_step": r["ms_per_step"], "us_per_call": r["ms_per_step"] * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": args.precision, "data": "synthetic",
+        "config": {**wl_config(wl), "precision": args.precision, "parallelism": f"replicas x{world}",
+                   "l2": "flushed (256 MiB write) before every timed step",
+                   "step": "weight pre-pack kernel + main kernel (C ABI dgrad_prepack + dgrad_run_packed)"},
+        "roofline": roofline(wl, args.precision, flops, nbytes, main_s, step_s),
+        "main_kernel_us": r["main_ms"] * 1e3, "prepack_us": r["prepack_ms"] * 1e3,
+        "fused_run_us": r["fused_ms"] * 1e3,
+        "gpu_launches": 2 * r["steps"],
+        "plan": {k: r["plan"][k] for k in ("path", "tile_blocks", "slice_n", "chunk_k", "n_chunks", "grid",
+                                           "n_work", "b_resident", "smem_bytes", "tmem_cols")},
+        "clocks": r["clocks"],
+    }
+    if r["e2e_s"]:
+        line["e2e"] = {"value": world * flops / r["e2e_s"] / 1e12, "unit": "TFLOP/s",
+                       "h2d_bytes_per_step": go_b + w_b, "d2h_bytes_per_step": gi_b,
+                       "us_per_call": r["e2e_s"] * 1e6, "api": "dgrad_run_host (pinned host buffers)"}
+    return line
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="resnet_stage")
+    ap.add_argument("--precision", default="tf32", choices=["tf32", "fp32"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--all", action="store_true", help="also print one info line per workload and precision")
+    args = ap.parse_args()
+
+    from conv2d_backward_implicit_dgrad_gb300.workloads import WORKLOADS
+    wl = WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return reference_arm(args, wl)
+
+    import torch
+    import torch.distributed as dist
+    import conv2d_backward_implicit_dgrad_gb300 as dg
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    r = time_workload(dg, torch, wl, args.precision, args.steps, args.warmup, rank, barrier, local,
+                      clocks=True, e2e=True)
+    if world > 1:
+        t = torch.tensor([r["ms_per_step"], r["main_ms"], r["e2e_s"] or 0.0], device="cuda", dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        r["ms_per_step"], r["main_ms"], r["e2e_s"] = t.tolist()
+
+    if rank == 0:
+        line = build_line(args, wl, r, world)
+        if world == 1 and not args.no_cpu_baseline:
+            flops, times, cores = cpu_oracle_run(wl, wl.N, reps=2)
+            line["cpu_baseline"] = {
+                "value": flops / min(times) / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                "sample": f"the whole batch ({wl.N} images) of {wl.name}, fp64 scatter oracle, "
+                          f"best of {len(times)}"}
+        print(json.dumps(line), flush=True)
+        if args.all:
+            for name in WORKLOAD_ORDER:
+                for prec in ("tf32", "fp32"):
+                    x = time_workload(dg, torch, WORKLOADS[name], prec, 50 if prec == "tf32" else 10, 5, rank,
+                                      lambda: None, local, clocks=False, e2e=False)
+                    rf = roofline(WORKLOADS[name], prec, x["flops"], x["bytes"], x["main_ms"] * 1e-3,
+                                  x["ms_per_step"] * 1e-3)
+                    print(json.dumps({"info": "workload", "workload": name, "precision": prec,
+                                      **{k: x[k] for k in ("ms_per_step", "main_ms", "prepack_ms", "fused_ms")},
+                                      "tflops": x["flops"] / (x["ms_per_step"] * 1e-3) / 1e12,
+                                      "main_tflops": rf["achieved"], "frac_peak": rf["frac"],
+                                      "frac_of_roofline_kernel": rf["frac_of_roofline_kernel"],
+                                      "plan": {k: x["plan"][k] for k in ("path", "tile_blocks", "slice_n",
+                                                                         "chunk_k", "grid", "n_work",
+                                                                         "b_resident", "smem_bytes")}}),
+                          flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,269 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle on the
+same seeded inputs.
+
+Bars (fixed by the tolerance the method is held to):
+  * FP32 path: relative L2 error ||gpu - ref||_2 / ||ref||_2 <= 1e-5 (fp64).
+  * TF32 path: per element |gpu - ref| <= 2e-3 * sum|terms|, and exactly 0
+    wherever no term reaches the element (sum|terms| = 0).
+grad_input is poisoned with NaN before every run, so an element the kernels
+fail to write fails both bars.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import conv2d_backward_implicit_dgrad_gb300 as dg
+from conv2d_backward_implicit_dgrad_gb300.workloads import ORDER, WORKLOADS, make_inputs, make_tensors
+
+pytestmark = pytest.mark.gpu
+
+FP32_REL_L2 = 1e-5
+TF32_REL_TERMS = 2e-3
+
+
+def out_ext(n, k, s, p):
+    return (n + 2 * p - k) // s + 1
+
+
+def run_gpu(args, go, w, precision, **opts):
+    N, Ci, H, W, Co, kH, kW, s, ph, pw = args
+    with dg.Plan(*args, precision=precision, **opts) as plan:
+        gi = torch.full((N, Ci, H, W), float("nan"), device="cuda")
+        plan.run(go.cuda(), w.cuda(), gi)
+        torch.cuda.synchronize()
+        plan.check()
+        info = plan.info
+    return gi.cpu().double().numpy(), info
+
+
+def assert_fp32(gpu, ref):
+    assert np.isfinite(gpu).all(), "non-finite output (unwritten element?)"
+    num = np.linalg.norm((gpu - ref).ravel())
+    den = np.linalg.norm(ref.ravel())
+    rel = num / den if den > 0 else num
+    assert rel <= FP32_REL_L2, f"relative L2 error {rel:.3e} > {FP32_REL_L2}"
+
+
+def assert_tf32(gpu, ref, mag):
+    assert np.isfinite(gpu).all(), "non-finite output (unwritten element?)"
+    err = np.abs(gpu - ref)
+    bad = err > TF32_REL_TERMS * mag
+    pos = mag > 0
+    worst = np.max(err[pos] / mag[pos]) if pos.any() else 0.0
+    assert not bad.any(), f"{bad.sum()} elements over the bound; worst err/sum|terms| = {worst:.3e}"
+    assert np.all(gpu[~pos] == 0)
+
+
+def check(args, go, w, precision, **opts):
+    N, Ci, H, W, Co, kH, kW, s, ph, pw = args
+    ref, mag = oracle.dgrad(go, w, H, W, s, ph, pw)
+    gpu, info = run_gpu(args, go, w, precision, **opts)
+    if precision == "fp32":
+        assert_fp32(gpu, ref)
+    else:
+        assert_tf32(gpu, ref, mag)
+    return info
+
+
+# ----------------------------------------------------------------- workloads
+@pytest.mark.parametrize("precision", ["tf32", "fp32"])
+@pytest.mark.parametrize("seed", [0, 1, 2])
+@pytest.mark.parametrize("name", ORDER)
+def test_workload_parity(name, seed, precision):
+    wl = WORKLOADS[name]
+    go, w = make_inputs(wl, seed)
+    info = check(wl.plan_args(), go, w, precision)
+    assert info["path"] == ("tcgen05" if precision == "tf32" else "simt")
+
+
+# ----------------------------------------------------------------- edge sweep
+EDGE = [
+    # N, Ci, Co, H, W, kH, kW, s, ph, pw
+    (1, 1, 1, 5, 7, 3, 3, 1, 0, 0),
+    (3, 3, 4, 9, 11, 5, 5, 1, 1, 1),
+    (1, 5, 33, 10, 9, 3, 3, 2, 0, 0),
+    (3, 65, 4, 7, 13, 3, 3, 3, 1, 1),
+    (1, 129, 33, 6, 10, 1, 1, 2, 0, 0),
+    (1, 3, 4, 23, 21, 7, 7, 2, 3, 3),
+    (3, 5, 33, 12, 14, 2, 2, 2, 0, 0),
+    (1, 3, 1, 11, 17, 3, 5, 1, 2, 1),
+    (3, 1, 4, 15, 8, 5, 3, 1, 1, 2),
+    (1, 65, 33, 17, 19, 4, 3, 2, 1, 2),
+    (1, 3, 4, 2, 2, 3, 3, 2, 1, 1),        # a kernel row that only meets padding
+    (1, 4, 3, 1, 1, 1, 1, 2, 1, 1),        # no term reaches any input element
+    (3, 16, 20, 31, 29, 3, 3, 1, 1, 1),    # ragged tiles, several tiles per image
+    (1, 20, 40, 40, 40, 3, 3, 4, 1, 1),    # stride 4: 16 phases
+]
+
+
+@pytest.mark.parametrize("precision", ["tf32", "fp32"])
+@pytest.mark.parametrize("shape", EDGE)
+def test_edge_shapes(shape, precision):
+    N, Ci, Co, H, W, kH, kW, s, ph, pw = shape
+    go, w = make_tensors((N, Co, out_ext(H, kH, s, ph), out_ext(W, kW, s, pw)), (Co, Ci, kH, kW), 71, "uniform")
+    check((N, Ci, H, W, Co, kH, kW, s, ph, pw), go, w, precision)
+
+
+# Tilings of the tcgen05 kernel: pipeline depth, chunk size, slices, persistent
+# CTAs that walk several work units (grid smaller than the unit count).
+TILINGS = [
+    dict(tile_blocks=1, chunk_k=8), dict(tile_blocks=1, chunk_k=16), dict(tile_blocks=1, chunk_k=32),
+    dict(tile_blocks=2, chunk_k=16), dict(tile_blocks=2, chunk_k=8, grid=3), dict(tile_blocks=1, slice_n=16, grid=5),
+    dict(tile_blocks=1, slice_n=32, chunk_k=32, grid=7), dict(tile_blocks=3, chunk_k=8, grid=2),
+    dict(tile_blocks=4, chunk_k=8, grid=1), dict(tile_blocks=4, slice_n=16, chunk_k=16, grid=2),
+]
+
+
+@pytest.mark.parametrize("opts", TILINGS)
+@pytest.mark.parametrize("shape", [(2, 40, 36, 19, 23, 3, 3, 1, 1, 1), (2, 48, 20, 17, 18, 3, 3, 2, 1, 1),
+                                   (3, 33, 70, 9, 14, 1, 1, 1, 0, 0)])
+def test_tc_tilings(shape, opts):
+    N, Ci, Co, H, W, kH, kW, s, ph, pw = shape
+    try:
+        dg.describe(N, Ci, H, W, Co, kH, kW, s, ph, pw, "tf32", path="tcgen05", **opts)
+    except dg.DgradError as e:
+        if e.status == 2:
+            pytest.skip("accumulators of this tiling exceed tensor memory")
+        raise
+    go, w = make_tensors((N, Co, out_ext(H, kH, s, ph), out_ext(W, kW, s, pw)), (Co, Ci, kH, kW), 73, "kaiming")
+    info = check((N, Ci, H, W, Co, kH, kW, s, ph, pw), go, w, "tf32", path="tcgen05", **opts)
+    for k in ("tile_blocks", "slice_n", "chunk_k"):
+        if k in opts:
+            assert info[k] == opts[k]
+
+
+@pytest.mark.parametrize("opts", [dict(slice_n=16), dict(slice_n=32, chunk_k=8), dict(chunk_k=32)])
+def test_simt_tilings(opts):
+    shape = (2, 40, 36, 19, 23, 3, 3, 2, 1, 1)
+    N, Ci, Co, H, W, kH, kW, s, ph, pw = shape
+    go, w = make_tensors((N, Co, out_ext(H, kH, s, ph), out_ext(W, kW, s, pw)), (Co, Ci, kH, kW), 79, "kaiming")
+    check((N, Ci, H, W, Co, kH, kW, s, ph, pw), go, w, "fp32", path="simt", **opts)
+
+
+def test_simt_with_tf32_operands():
+    # The FFMA path on TF32-rounded operands satisfies the TF32 bar too.
+    shape = (2, 24, 40, 13, 15, 3, 3, 1, 1, 1)
+    N, Ci, Co, H, W, kH, kW, s, ph, pw = shape
+    go, w = make_tensors((N, Co, H, W), (Co, Ci, kH, kW), 83, "kaiming")
+    check((N, Ci, H, W, Co, kH, kW, s, ph, pw), go, w, "tf32", path="simt")
+
+
+# ----------------------------------------------------------------- semantics
+def test_infinite_weight_on_padding_only_tap_stays_finite():
+    # H = W = 2, 3x3, pad 1, stride 2: kernel row 0 and column 0 only ever meet
+    # padding, so the definition never multiplies them; the result is finite.
+    N, Ci, Co, H, W = 1, 3, 4, 2, 2
+    go, w = make_tensors((N, Co, 1, 1), (Co, Ci, 3, 3), 89, "uniform")
+    w[:, :, 0, :] = float("inf")
+    w[:, :, :, 0] = float("-inf")
+    ref, mag = oracle.dgrad(go, w, H, W, 2, 1, 1)
+    assert np.isfinite(ref).all()
+    for prec in ("tf32", "fp32"):
+        gpu, _ = run_gpu((N, Ci, H, W, Co, 3, 3, 2, 1, 1), go, w, prec)
+        assert np.isfinite(gpu).all()
+        if prec == "fp32":
+            assert_fp32(gpu, ref)
+        else:
+            assert_tf32(gpu, ref, mag)
+
+
+def test_overwrites_and_leaves_inputs_alone():
+    wl = WORKLOADS["tiny"]
+    go, w = make_inputs(wl, 5)
+    with dg.Plan(*wl.plan_args(), precision="tf32") as plan:
+        gd, wd = go.cuda(), w.cuda()
+        gi = torch.full(wl.gi_shape, 123.0, device="cuda")
+        plan.run(gd, wd, gi)
+        first = gi.clone()
+        plan.run(gd, wd, gi)
+        torch.cuda.synchronize()
+        plan.check()
+        assert torch.equal(first, gi), "second run differs: not an overwrite, or not deterministic"
+        assert torch.equal(gd.cpu(), go) and torch.equal(wd.cpu(), w)
+
+
+def test_prepack_then_run_packed_matches_run():
+    wl = WORKLOADS["strided_downsample"]
+    go, w = make_tensors((2, wl.Co, wl.oH, wl.oW), wl.w_shape, 97, wl.dist)
+    args = (2,) + wl.plan_args()[1:]
+    with dg.Plan(*args, precision="tf32") as plan:
+        gd, wd = go.cuda(), w.cuda()
+        a = plan.run(gd, wd)
+        plan.prepack(wd)
+        b = plan.run_packed(gd)
+        c = plan.run_packed(gd)
+        torch.cuda.synchronize()
+        assert torch.equal(a, b) and torch.equal(b, c)
+
+
+def test_run_host_matches_device():
+    wl = WORKLOADS["tiny"]
+    go, w = make_inputs(wl, 7)
+    with dg.Plan(*wl.plan_args(), precision="tf32") as plan:
+        dev = plan.run(go.cuda(), w.cuda())
+        host = plan.run_host(go.pin_memory(), w.pin_memory())
+        torch.cuda.synchronize()
+        assert torch.equal(dev.cpu(), host)
+        plan.check()
+
+
+def test_side_stream():
+    wl = WORKLOADS["tiny"]
+    go, w = make_inputs(wl, 8)
+    ref, mag = oracle.dgrad(go, w, wl.H, wl.W, 1, 1, 1)
+    s = torch.cuda.Stream()
+    with dg.Plan(*wl.plan_args(), precision="tf32") as plan:
+        with torch.cuda.stream(s):
+            gd, wd = go.cuda(), w.cuda()
+            gi = plan.run(gd, wd, stream=s)
+        s.synchronize()
+        assert_tf32(gi.cpu().double().numpy(), ref, mag)
+
+
+def test_rejects_bad_pointers():
+    wl = WORKLOADS["tiny"]
+    with dg.Plan(*wl.plan_args(), precision="tf32") as plan:
+        lib = dg.load_library()
+        go = torch.zeros(wl.go_shape, device="cuda")
+        w = torch.zeros(wl.w_shape, device="cuda")
+        gi = torch.zeros(wl.gi_shape, device="cuda")
+        stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+        buf = torch.zeros(go.numel() + 16, device="cuda")
+        misaligned = ctypes.c_void_p(buf.data_ptr() + 4)
+        assert lib.dgrad_run(plan._h, misaligned, ctypes.c_void_p(w.data_ptr()),
+                             ctypes.c_void_p(gi.data_ptr()), stream) == 3
+        assert lib.dgrad_run(plan._h, ctypes.c_void_p(go.data_ptr()), ctypes.c_void_p(w.data_ptr()),
+                             ctypes.c_void_p(go.data_ptr()), stream) == 4
+        assert lib.dgrad_run(plan._h, None, ctypes.c_void_p(w.data_ptr()),
+                             ctypes.c_void_p(gi.data_ptr()), stream) == 3
+        assert lib.dgrad_run(None, ctypes.c_void_p(go.data_ptr()), ctypes.c_void_p(w.data_ptr()),
+                             ctypes.c_void_p(gi.data_ptr()), stream) == 1
+        torch.cuda.synchronize()
+        plan.check()
+
+
+def test_run_packed_before_prepack_is_rejected():
+    wl = WORKLOADS["tiny"]
+    with dg.Plan(*wl.plan_args(), precision="tf32") as plan:
+        with pytest.raises(dg.DgradError) as e:
+            plan.run_packed(torch.zeros(wl.go_shape, device="cuda"))
+        assert e.value.status == 1
+
+
+# ----------------------------------------------------------------- full size, sampled
+@pytest.mark.parametrize("name", ["resnet_stage", "strided_downsample", "pointwise", "stem"])
+def test_full_size_sampled_definition(name):
+    """At full size in the benchmark's launch configuration: 4096 sampled
+    elements against the definition computed one by one."""
+    wl = WORKLOADS[name]
+    go, w = make_inputs(wl, 0)
+    gpu, _ = run_gpu(wl.plan_args(), go, w, "tf32")
+    rng = np.random.default_rng(101)
+    idx = np.stack([rng.integers(0, wl.N, 4096), rng.integers(0, wl.Ci, 4096),
+                    rng.integers(0, wl.H, 4096), rng.integers(0, wl.W, 4096)], 1)
+    acc, mag = oracle.dgrad_at(go, w, wl.H, wl.W, wl.stride, wl.pad_h, wl.pad_w, idx)
+    g = gpu[idx[:, 0], idx[:, 1], idx[:, 2], idx[:, 3]]
+    assert np.all(np.abs(g - acc) <= TF32_REL_TERMS * mag)
