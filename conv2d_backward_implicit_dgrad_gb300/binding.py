@@ -28,8 +28,8 @@ PATH_NAME = {v: k for k, v in PATH.items()}
 
 # Every function declared in include/dgrad.h (checked by the CPU tests).
 EXPORTS = ("dgrad_plan", "dgrad_plan_ex", "dgrad_describe", "dgrad_describe_taps", "dgrad_plan_info", "dgrad_run",
-           "dgrad_prepack", "dgrad_run_packed", "dgrad_run_host", "dgrad_plan_check", "dgrad_plan_destroy",
-           "dgrad_status_string")
+           "dgrad_prepack", "dgrad_run_packed", "dgrad_run_host", "dgrad_run_noalloc", "dgrad_plan_check",
+           "dgrad_plan_destroy", "dgrad_status_string")
 
 
 class Options(ctypes.Structure):

@@ -175,6 +175,33 @@ dgrad_status_t dgrad_run_host(dgrad_plan_t plan, const float *grad_out_host,
                               const float *weight_host, float *grad_input_host,
                               void *stream);
 
+/* Allocation-free dgrad: the same result as dgrad_run, from DEVICE pointers,
+ * without creating a plan and without allocating any device memory.  The
+ * pages have no counterpart; it exists for callers that may not allocate,
+ * for example code running inside a framework whose own allocator owns the
+ * whole device memory budget (a second allocator would overrun or fragment
+ * it), or latency-critical code that cannot accept the device-wide
+ * synchronisation a cudaMalloc/cudaFree pair can cause mid-step.
+ *
+ * Scratch: the packed weights and the error word go into one fixed 4 MiB
+ * array that the library reserves statically on every device that loads it,
+ * for the life of the process.  Shapes whose packed weights need more
+ * (dgrad_describe's packed_weight_bytes > 4 MiB - 256 B) are refused with
+ * DGRAD_ERR_UNSUPPORTED before anything is launched.  The first call on a
+ * device looks up that array's device address (cudaGetSymbolAddress, with the
+ * device current) and caches it; make that first call before any stream
+ * capture.  Every call on a device shares the one array and it keeps the last
+ * call's contents (each call clears the error word and rewrites the packed
+ * weights), so calls whose kernels can overlap on the GPU (different streams
+ * or threads) race and give wrong results: serialise them.  In-kernel wait
+ * timeouts are not reported here (use a plan and dgrad_plan_check for that).
+ * Pointer rules, layouts, stream semantics and the other errors are those of
+ * dgrad_run; tiles are chosen as dgrad_plan would choose them. */
+dgrad_status_t dgrad_run_noalloc(int N, int Ci, int H, int W, int Co, int kH, int kW,
+                                 int stride, int pad_h, int pad_w, dgrad_precision_t precision,
+                                 const float *grad_out, const float *weight, float *grad_input,
+                                 void *stream);
+
 /* Read and clear the plan's device error word.  Call after synchronising the
  * stream of the last dgrad_run.  Returns DGRAD_OK or the recorded error. */
 dgrad_status_t dgrad_plan_check(dgrad_plan_t plan);

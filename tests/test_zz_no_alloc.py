@@ -1,0 +1,66 @@
+"""dgrad_run_noalloc, the entry point that allocates nothing, against dgrad_run.
+
+Some callers cannot allocate device memory: a framework whose allocator owns
+the whole device budget, or a latency-critical step that must not pay for the
+synchronisation cudaMalloc/cudaFree can bring.  For them the library keeps the
+packed weights in a fixed array it reserves on every device.  These tests call
+that entry point through the C ABI twice in a row, with different inputs each
+time (a stale packed weight left by the first call would show in the second),
+and compare each result with dgrad_run's on the same inputs, within the
+tolerances the other parity tests use.  This file is collected last so that a
+run stopping at the first failure has already run everything else.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import conv2d_backward_implicit_dgrad_gb300 as dg
+from conv2d_backward_implicit_dgrad_gb300.workloads import WORKLOADS, make_inputs
+
+pytestmark = pytest.mark.gpu
+
+PREC = {"fp32": 0, "tf32": 1}
+
+
+def call_noalloc(args, precision, go, w, gi):
+    fn = dg.load_library().dgrad_run_noalloc
+    fn.argtypes = [ctypes.c_int] * 11 + [ctypes.c_void_p] * 4
+    fn.restype = ctypes.c_int
+    stream = torch.cuda.current_stream().cuda_stream
+    return fn(*args, PREC[precision], go.data_ptr(), w.data_ptr(), gi.data_ptr(), stream)
+
+
+@pytest.mark.parametrize("precision", ["tf32", "fp32"])
+@pytest.mark.parametrize("name", ["tiny", "strided_downsample", "resnet_stage"])
+def test_noalloc_matches_run_twice(name, precision):
+    wl = WORKLOADS[name]
+    args = wl.plan_args()
+    for seed in (3, 4):   # two calls in a row, different grad_out and weight
+        go_h, w_h = make_inputs(wl, seed)
+        go, w = go_h.cuda(), w_h.cuda()
+        with dg.Plan(*args, precision=precision) as plan:
+            ref = plan.run(go, w)
+            torch.cuda.synchronize()
+            plan.check()
+        out = torch.full(wl.gi_shape, float("nan"), device="cuda")
+        assert call_noalloc(args, precision, go, w, out) == 0
+        torch.cuda.synchronize()
+        a, b = out.cpu().double().numpy(), ref.cpu().double().numpy()
+        assert np.isfinite(a).all()
+        if precision == "tf32":
+            _, mag = oracle.dgrad(go_h, w_h, wl.H, wl.W, wl.stride, wl.pad_h, wl.pad_w)
+            assert np.all(np.abs(a - b) <= 2e-3 * mag)
+        else:
+            assert np.linalg.norm(a - b) <= 1e-5 * np.linalg.norm(b)
+
+
+def test_noalloc_refuses_oversized_weights():
+    # 3x3, Ci = 512, Co = 1024: the packed weights need about 19 MB > 4 MiB.
+    args = (1, 512, 8, 8, 1024, 3, 3, 1, 1, 1)
+    go = torch.zeros((1, 1024, 8, 8), device="cuda")
+    w = torch.zeros((1024, 512, 3, 3), device="cuda")
+    gi = torch.zeros((1, 512, 8, 8), device="cuda")
+    assert call_noalloc(args, "tf32", go, w, gi) == 2
