@@ -317,6 +317,25 @@ def build_line(args, wl, r, world):
     return line
 
 
+def profile_steps(dg, torch, wl, args):
+    """W warm-up steps then K steps, each after an L2 flush; nothing else."""
+    from conv2d_backward_implicit_dgrad_gb300.workloads import make_inputs
+    go_h, w_h = make_inputs(wl, 0)
+    go, w = go_h.cuda(), w_h.cuda()
+    gi = torch.empty(wl.gi_shape, device="cuda")
+    flush = torch.empty(FLUSH_BYTES // 4, device="cuda")
+    with dg.Plan(*wl.plan_args(), precision=args.precision) as plan:
+        for _ in range(args.warmup + args.steps):
+            flush.zero_()
+            plan.prepack(w)
+            plan.run_packed(go, gi)
+        torch.cuda.synchronize()
+        plan.check()
+        print(json.dumps({"profile": wl.name, "precision": args.precision, "steps": args.steps,
+                          "warmup": args.warmup, "plan": plan.info}), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -327,6 +346,8 @@ def main():
     ap.add_argument("--precision", default="tf32", choices=["tf32", "fp32"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--all", action="store_true", help="also print one info line per workload and precision")
+    ap.add_argument("--profile", action="store_true",
+                    help="only run W + K steps (for ncu captures: few launches, no extra timing loops)")
     args = ap.parse_args()
 
     from conv2d_backward_implicit_dgrad_gb300.workloads import WORKLOADS
@@ -337,6 +358,9 @@ def main():
     import torch
     import torch.distributed as dist
     import conv2d_backward_implicit_dgrad_gb300 as dg
+
+    if args.profile:
+        return profile_steps(dg, torch, wl, args)
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
