@@ -49,14 +49,17 @@ def up_to_date() -> bool:
     return all(os.path.getmtime(d) <= t for d in _deps())
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
-    if not force and not extra_flags and up_to_date():
+def build(force: bool = False, verbose: bool = False, extra_flags=(), out: str | None = None) -> str:
+    """Compile and link; `extra_flags` (e.g. -DDGRAD_TRACE) builds a variant into `out`."""
+    if out is None and not force and not extra_flags and up_to_date():
         return LIB
-    os.makedirs(os.path.join(BUILD, "obj"), exist_ok=True)
+    lib = out or LIB
+    objdir = os.path.join(BUILD, "obj" if out is None else "obj_" + os.path.basename(out).replace(".", "_"))
+    os.makedirs(objdir, exist_ok=True)
     exe = nvcc()
 
     def compile_one(src):
-        obj = os.path.join(BUILD, "obj", os.path.basename(src) + ".o")
+        obj = os.path.join(objdir, os.path.basename(src) + ".o")
         cmd = [exe, *ARCH, *CFLAGS, *extra_flags, "-c", src, "-o", obj]
         if verbose:
             print(" ".join(cmd), flush=True)
@@ -69,13 +72,13 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
 
     with cf.ThreadPoolExecutor(max_workers=min(8, os.cpu_count() or 1)) as ex:
         objs = list(ex.map(compile_one, sources()))
-    tmp = LIB + f".{os.getpid()}.tmp"
+    tmp = lib + f".{os.getpid()}.tmp"
     cmd = [exe, *ARCH, "-shared", "-cudart", "static", "-o", tmp, *objs]
     res = subprocess.run(cmd, capture_output=True, text=True)
     if res.returncode != 0:
         raise RuntimeError(f"link failed:\n{res.stdout}\n{res.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":

@@ -85,6 +85,8 @@ void fill_params(dgrad_plan_s *pl) {
     m.n_tiles = t.n_tiles; m.n_work = (int)t.n_work;
     m.a_rows = t.a_rows; m.a_stages = t.a_stages; m.b_stages = t.b_stages; m.b_resident = t.b_resident;
     m.chunk_bytes = t.chunk_bytes;
+    m.tap_group = t.tap_group; m.n_tgroups = t.n_tgroups;
+    m.vec_producer = dgrad::use_vec_producer(g, t) ? 1 : 0;
     m.acc_bufs = t.acc_bufs; m.acc_cols = t.acc_cols; m.tmem_cols = t.tmem_cols;
     m.round_tf32 = pl->precision == DGRAD_PREC_TF32 ? 1 : 0;
     m.n_phases = g.n_phases;
@@ -100,6 +102,7 @@ void fill_params(dgrad_plan_s *pl) {
     q.Co = g.Co; q.Ci = g.Ci; q.kH = g.kH; q.kW = g.kW;
     q.n_taps = g.n_taps; q.bn = t.bn; q.n_slices = t.n_slices; q.kc = t.kc; q.n_chunks = t.n_chunks;
     q.round_tf32 = m.round_tf32;
+    q.layout = t.path == DGRAD_PATH_TCGEN05 ? 1 : 0;
     q.total = (long long)(t.packed_bytes / 4);
     for (int i = 0; i < g.n_taps; ++i) {
         q.tap_kh[i] = g.tap[i].kh;

@@ -37,6 +37,7 @@ constexpr uint32_t kErrTimeout = 1u;
 struct TapDesc {
     int kh, kw;   // position inside the kernel
     int shift;    // dr * Wp + dc, >= 0
+    int phase;    // index of the phase the tap feeds
 };
 
 // One sub-pixel phase (a, b): input rows ih = s*q + a, columns iw = s*u + b.
@@ -81,7 +82,9 @@ struct Tiling {
     int a_rows;        // rows of one A stage
     int a_stages, b_stages;
     int b_resident;
-    int chunk_bytes;   // packed weight bytes of one (slice, chunk)
+    int tap_group;     // taps per B stage (tcgen05 path)
+    int n_tgroups;     // B stages per channel chunk
+    int chunk_bytes;   // bytes of one B stage (tap_group taps)
     int acc_bufs;      // tensor-memory accumulator sets
     int acc_cols;      // columns of one set
     int tmem_cols;
@@ -92,18 +95,33 @@ struct Tiling {
 dgrad_status_t choose_tiling(const Geometry &g, int precision, const dgrad_options_t *opts,
                              int sm_count, Tiling *t);
 
+// The tcgen05 producers can copy grad_out in aligned 4-element quads of a
+// channel plane when every plane starts 16-byte aligned (oH*oW % 4 == 0) and
+// one A band spans only a few images (each image is one contiguous quad
+// range of the band).
+constexpr int kMaxBandImages = 4;
+inline bool use_vec_producer(const Geometry &g, const Tiling &t) {
+    const long long img = (long long)g.Hv * g.Wp;
+    return t.path == DGRAD_PATH_TCGEN05 && (g.oH * g.oW) % 4 == 0 && (t.a_rows + img - 1) / img + 1 <= kMaxBandImages;
+}
+
 // ---------------------------------------------------------------- kernels
-// Packed weights: for slice sl, chunk c, tap t, channel group gq (4 output
-// channels), input channel j of the slice and e in [0,4):
-//   wp[((((sl*n_chunks + c)*n_taps + t)*(kc/4) + gq)*bn + j)*4 + e]
-//     = weight[co = c*kc + 4*gq + e][ci = sl*bn + j][kh_t][kw_t]   (0 if out of range)
-// so one (slice, chunk) is one contiguous block of chunk_bytes, and inside it
-// the 16-byte groups are the K-major "core matrix" rows of the GEMM's B.
+// Packed weights.  One (slice sl, chunk c) is one contiguous block of
+// chunk_bytes holding, for every tap t, input channel j of the slice and
+// output channel co = c*kc + k of the chunk, weight[co][sl*bn + j][kh_t][kw_t]
+// (0 outside the tensor), in one of two layouts:
+//  layout 0 (FFMA kernel), 16-byte groups of 4 output channels:
+//    wp[((((sl*n_chunks + c)*n_taps + t)*(kc/4) + k/4)*bn + j)*4 + k%4]
+//  layout 1 (tcgen05 kernel, kc = 32), one 128-byte row per input channel,
+//  its 16-byte chunks permuted by the 128-byte swizzle of the tensor core's
+//  K-major operand layout (chunk k/4 stored at position (k/4) ^ (j % 8)):
+//    wp[(((sl*n_chunks + c)*n_taps + t)*bn + j)*32 + (((k/4) ^ (j%8))*4) + k%4]
 struct PrepackParams {
     const float *w;
     float *wp;
     int Co, Ci, kH, kW;
     int n_taps, bn, n_slices, kc, n_chunks;
+    int layout;
     int round_tf32;
     long long total;   // floats written
     int tap_kh[kMaxTaps];
@@ -121,6 +139,8 @@ struct MainParams {
     int tm, bn, n_slices, kc, n_chunks, n_tiles;
     int n_work;
     int a_rows, a_stages, b_stages, b_resident, chunk_bytes;
+    int tap_group, n_tgroups;
+    int vec_producer;   // 1: 16-byte quad loads + register transpose; 0: 4-byte asynchronous copies
     int acc_bufs, acc_cols, tmem_cols;
     int round_tf32;
     int n_phases, n_taps;

@@ -78,6 +78,21 @@ __device__ __forceinline__ void fill_a_stage(float *As, const MainParams &p, int
     }
 }
 
+// Element offset of V[v][channel 0] in grad_out (add co * oH * oW for
+// channel co), or -1 where the frame is zero.
+__device__ __forceinline__ int frame_row_offset(const MainParams &p, int v) {
+    if (v >= p.positions) return -1;
+    const int n = v / p.HvWp;
+    const int rem = v - n * p.HvWp;
+    const int y = rem / p.Wp;
+    const int x = rem - y * p.Wp;
+    const int oh = y - p.Ph, ow = x - p.Pw;
+    if (static_cast<unsigned>(oh) >= static_cast<unsigned>(p.oH) ||
+        static_cast<unsigned>(ow) >= static_cast<unsigned>(p.oW))
+        return -1;
+    return (n * p.Co * p.oH + oh) * p.oW + ow;
+}
+
 // Decode a flattened output position into (n, q, u).
 __device__ __forceinline__ void decode_position(const MainParams &p, int P, int &n, int &q, int &u) {
     n = P / p.HvWp;

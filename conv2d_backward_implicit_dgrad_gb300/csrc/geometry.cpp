@@ -98,6 +98,7 @@ dgrad_status_t make_geometry(int N, int Ci, int H, int W, int Co, int kH, int kW
                     TapDesc &t = g->tap[g->n_taps++];
                     t.kh = R.r + stride * j;
                     t.kw = C.r + stride * i;
+                    t.phase = g->n_phases - 1;
                     int dr = R.c - j + Ph, dc = C.c - i + Pw;
                     max_dr = std::max(max_dr, dr);
                     max_dc = std::max(max_dc, dc);
@@ -132,48 +133,65 @@ int pow2_at_least(int x) {
     return p;
 }
 
-constexpr int kBarrierBytes = 1024;   // mbarriers and the TMEM address slot
+constexpr int kBarrierBytes = 4096;   // mbarriers + TMEM slot (1 KB), tap table (2 KB), 1024-byte alignment slack
 constexpr int kMaxResidentChunks = 32;
+constexpr int kMaxTcRows = 1024;   // frame rows one tcgen05 A stage may hold (16 per producer thread)
 
-// Fill the sizes that follow from (tm, bn, kc) for the tcgen05 path; returns
-// false when no pipeline depth fits in shared memory.
+// Fill the sizes that follow from (tm, bn) for the tcgen05 path (kc = 32);
+// returns false when no pipeline depth fits in shared memory.  The packed
+// weights of one channel chunk are streamed in groups of tap_group taps;
+// when all of them fit next to two A stages they stay resident instead.
 bool size_tc(const Geometry &g, Tiling &t, int want_resident) {
     t.n_slices = ceil_div(g.Ci, t.bn);
     t.n_chunks = ceil_div(g.Co, t.kc);
     t.a_rows = round_up(t.tm * kBlockM + g.max_shift, 8);
-    int a_bytes = t.a_rows * t.kc * 4;
-    t.chunk_bytes = g.n_taps * t.kc * t.bn * 4;
-    if (g.n_taps == 0) t.chunk_bytes = 0;
-    int budget = kMaxSmem - kBarrierBytes;
+    if (t.a_rows > kMaxTcRows) return false;
+    const long long a_bytes = (long long)t.a_rows * t.kc * 4;
+    const long long tap_bytes = (long long)t.bn * t.kc * 4;
+    const long long budget = kMaxSmem - kBarrierBytes;
+    const int taps = std::max(1, g.n_taps);
     t.b_resident = 0;
     if (want_resident && t.n_slices == 1 && t.n_chunks <= kMaxResidentChunks) {
-        long long b_all = (long long)t.n_chunks * t.chunk_bytes;
-        if (b_all + 2LL * a_bytes <= budget) {
+        long long b_all = (long long)t.n_chunks * taps * tap_bytes;
+        if (b_all + 2 * a_bytes <= budget) {
             t.b_resident = 1;
+            t.tap_group = taps;
+            t.n_tgroups = 1;
             t.b_stages = t.n_chunks;
+            t.chunk_bytes = (int)(taps * tap_bytes);
             t.a_stages = (int)std::min<long long>(4, (budget - b_all) / a_bytes);
         }
     }
+    if (want_resident && !t.b_resident) return false;
     if (!t.b_resident) {
-        int bs = t.chunk_bytes > 0 ? 2 : 1;
-        if ((long long)bs * t.chunk_bytes + 2LL * a_bytes > budget) return false;
-        t.b_stages = bs;
-        t.a_stages = (int)std::min<long long>(4, (budget - (long long)bs * t.chunk_bytes) / a_bytes);
-        if (t.a_stages >= 4 && t.chunk_bytes > 0 &&
-            3LL * t.chunk_bytes + 3LL * a_bytes <= budget) {
-            t.b_stages = 3;
+        // Largest tap group with two B stages and at least two A stages
+        // (three when they fit without shrinking the group below half).
+        long long tg = (budget - 2 * a_bytes) / (2 * tap_bytes);
+        if (tg < 1) return false;
+        tg = std::min<long long>(tg, taps);
+        long long tg3 = (budget - 3 * a_bytes) / (2 * tap_bytes);
+        t.a_stages = 2;
+        if (tg3 >= std::min<long long>(taps, std::max<long long>(1, (tg + 1) / 2))) {
+            tg = std::min<long long>(tg3, taps);
             t.a_stages = 3;
         }
+        t.tap_group = (int)tg;
+        t.n_tgroups = ceil_div(taps, t.tap_group);
+        t.tap_group = ceil_div(taps, t.n_tgroups);   // balance the groups
+        t.chunk_bytes = (int)(t.tap_group * tap_bytes);
+        t.b_stages = 2;
+        long long left = budget - (long long)t.b_stages * t.chunk_bytes;
+        t.a_stages = (int)std::min<long long>(4, left / a_bytes);
     }
     if (t.a_stages < 2) return false;
-    t.smem_bytes = kBarrierBytes + t.a_stages * a_bytes + t.b_stages * t.chunk_bytes;
+    t.smem_bytes = (int)(kBarrierBytes + t.a_stages * a_bytes + (long long)t.b_stages * t.chunk_bytes);
     t.acc_cols = t.tm * g.n_phases * t.bn;
     if (t.acc_cols > kTmemCols) return false;
     t.acc_bufs = (2 * t.acc_cols <= kTmemCols) ? 2 : 1;
     t.tmem_cols = pow2_at_least(t.acc_bufs * t.acc_cols);
     t.n_tiles = (int)((g.positions + (long long)t.tm * kBlockM - 1) / ((long long)t.tm * kBlockM));
     t.n_work = (long long)t.n_tiles * t.n_slices;
-    t.packed_bytes = (size_t)t.n_slices * t.n_chunks * (size_t)t.chunk_bytes;
+    t.packed_bytes = (size_t)t.n_slices * t.n_chunks * (size_t)taps * (size_t)tap_bytes;
     return true;
 }
 
@@ -250,22 +268,18 @@ dgrad_status_t choose_tiling(const Geometry &g, int precision, const dgrad_optio
         if (units2 >= 2LL * sm_count) tm_pref[n_tm++] = 2;
         tm_pref[n_tm++] = 1;
     }
-    if (o.chunk_k && o.chunk_k != 8 && o.chunk_k != 16 && o.chunk_k != 32) return DGRAD_ERR_INVALID_ARG;
-    int kc_pref[3] = {32, 16, 8};
+    // Operand rows are one 128-byte swizzle row: 32 output channels per chunk.
+    if (o.chunk_k && o.chunk_k != 32) return DGRAD_ERR_INVALID_ARG;
     bool ok = false;
-    for (int i = 0; i < n_tm && !ok; ++i) {
-        for (int want_res = 1; want_res >= 0 && !ok; --want_res) {
-            for (int k = 0; k < 3 && !ok; ++k) {
-                int kc = o.chunk_k ? o.chunk_k : kc_pref[k];
-                Tiling c = t;
-                c.tm = tm_pref[i];
-                c.bn = bn;
-                c.kc = kc;
-                if (size_tc(g, c, want_res) && (c.a_stages >= 3 || c.b_resident || kc == 8 || o.chunk_k)) {
-                    t = c;
-                    ok = true;
-                }
-                if (o.chunk_k) break;
+    for (int want_res = 1; want_res >= 0 && !ok; --want_res) {
+        for (int i = 0; i < n_tm && !ok; ++i) {
+            Tiling c = t;
+            c.tm = tm_pref[i];
+            c.bn = bn;
+            c.kc = 32;
+            if (size_tc(g, c, want_res)) {
+                t = c;
+                ok = true;
             }
         }
     }

@@ -25,10 +25,19 @@ __global__ void __launch_bounds__(kThreads) prepack_kernel(const __grid_constant
         long long rest = i;
         const int e = static_cast<int>(rest % 4);
         rest /= 4;
-        const int j = static_cast<int>(rest % p.bn);
-        rest /= p.bn;
-        const int gq = static_cast<int>(rest % G);
-        rest /= G;
+        int j, gq;
+        if (p.layout == 1) {   // [tap][j][swizzled 16-byte chunk][4]
+            const int pos = static_cast<int>(rest % G);
+            rest /= G;
+            j = static_cast<int>(rest % p.bn);
+            rest /= p.bn;
+            gq = pos ^ (j & 7);
+        } else {               // [tap][gq][j][4]
+            j = static_cast<int>(rest % p.bn);
+            rest /= p.bn;
+            gq = static_cast<int>(rest % G);
+            rest /= G;
+        }
         const int t = static_cast<int>(rest % p.n_taps);
         rest /= p.n_taps;
         const int c = static_cast<int>(rest % p.n_chunks);

@@ -85,6 +85,28 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t
         : "memory");
 }
 
+// 4-byte asynchronous global -> shared copy; src_bytes = 0 writes a zero
+// without reading (the source address must still be a valid address).
+__device__ __forceinline__ void cp_async_4(uint32_t dst, const void *src, uint32_t src_bytes) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+
+// Arrive on `bar` (as one of its expected arrivals) once every cp.async this
+// thread issued so far has landed in shared memory.
+__device__ __forceinline__ void cp_async_arrive(uint32_t bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_wait_all() {
+    asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
+// Prefetch a contiguous global range into L2 (TMA engine; nothing is
+// written anywhere).  addr 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_prefetch_l2(const void *addr, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(addr), "r"(bytes) : "memory");
+}
+
 // ------------------------------------------------ programmatic dependent launch
 __device__ __forceinline__ void grid_dependency_wait() {
     asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -113,6 +135,25 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint3
     d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
     d |= static_cast<uint64_t>(1) << 46;   // descriptor version for tcgen05
     // base offset 0, relative leading-dimension mode, swizzle mode 0 (none)
+    return d;
+}
+
+// Shared-memory matrix descriptor, 128-byte swizzle, K-major: each operand
+// row is 128 bytes (32 TF32 values along K) whose 16-byte chunk c sits at
+// position c ^ (row % 8); 8-row groups are 1024 bytes apart (sbo).  The
+// swizzle is a function of the absolute shared address (bits 4-6 XOR bits
+// 7-9), so the start may be any 128-byte row of data written that way, and
+// may advance by 32 bytes per K step of 8; base_offset stays 0 for such
+// starts (checked on sm_103a against the CPU oracle: a non-zero row phase
+// there permutes the operand).
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr, uint32_t base_offset) {
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((addr & 0x3FFFFu) >> 4);
+    d |= static_cast<uint64_t>(1) << 16;                  // leading byte offset (unused for this layout)
+    d |= static_cast<uint64_t>(1024 >> 4) << 32;          // stride byte offset: 8 rows x 128 bytes
+    d |= static_cast<uint64_t>(1) << 46;                  // descriptor version for tcgen05
+    d |= static_cast<uint64_t>(base_offset & 7) << 49;
+    d |= static_cast<uint64_t>(2) << 61;                  // swizzle mode: 128 bytes
     return d;
 }
 
@@ -146,11 +187,42 @@ __device__ __forceinline__ void mma_tf32(uint32_t d_tmem, uint64_t adesc, uint64
         : "memory");
 }
 
+// The same MMA issued by one elected lane of a converged warp.  Running the
+// issue loop on the whole warp keeps the descriptors warp-uniform, which lets
+// them stay in uniform registers: issued from a single divergent lane the
+// same loop cost about twice the tensor core's time per MMA on sm_103a.
+__device__ __forceinline__ void mma_tf32_elect(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                               uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "elect.sync _|p, 0xffffffff;\n\t"
+        "setp.ne.b32 q, %4, 0;\n\t"
+        "@p tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, q;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// tcgen05.commit from the lane elect.sync picks (the same lane that issued
+// the MMAs in mma_tf32_elect: the lowest active lane of the full warp).
+__device__ __forceinline__ void mma_commit_elect(uint32_t bar) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "elect.sync _|p, 0xffffffff;\n\t"
+        "@p tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(bar)
+        : "memory");
+}
+
 // Arrive once on `bar` when every tcgen05 operation issued so far by this
 // thread has completed.
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
                  : "memory");
+}
+
+// Descriptor advanced by a byte offset (a multiple of 16 that keeps the
+// address inside the 256 KB shared window): only the start-address field moves.
+__device__ __forceinline__ uint64_t desc_add(uint64_t desc, uint32_t bytes) {
+    return desc + static_cast<uint64_t>(bytes >> 4);
 }
 
 // 32 lanes x 32 bits, 16 consecutive columns: thread i of the warp gets lane

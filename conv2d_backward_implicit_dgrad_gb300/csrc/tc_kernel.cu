@@ -9,9 +9,12 @@
 //
 // Roles (448 threads):
 //   warps 0-3   epilogue: tensor memory -> registers -> grad_input (NCHW)
-//   warp  4     tensor-memory allocation and the single MMA-issuing thread
+//   warp  4     tensor-memory allocation; the MMA loop (whole warp, one
+//               elected lane issues)
 //   warp  5     one thread streaming packed weights with bulk copies (TMA)
-//   warps 6-13  producers: grad_out band -> shared memory (A operand)
+//   warps 6-13  producers: a band of the frame -> shared memory (A operand),
+//               32 channels per stage, rows in the 128-byte swizzled K-major
+//               layout of the tensor core
 // Pipelines (all mbarriers, all waits bounded):
 //   A ring   a_stages  producers -> MMA        (A_full / A_empty)
 //   B ring   b_stages  weight loader -> MMA    (B_full / B_empty); when the
@@ -35,6 +38,12 @@ constexpr int kProdWarps = 8;
 constexpr int kThreads = (kProdWarp0 + kProdWarps) * 32;
 constexpr int kMaxAStages = 4;
 constexpr int kMaxBStages = 32;
+constexpr int kRowSlots = kProdWarps * 32 / 4;   // 4-byte producer: threads per channel lane
+constexpr int kMaxRowsPerThread = 16;            // a_rows <= kRowSlots * kMaxRowsPerThread
+constexpr int kGroupThreads = 128;               // quad producer: threads per producer group
+constexpr int kQuadBatch = 4;                    // quad producer: warp items with loads in flight
+constexpr int kTapTableOffset = 1024;            // bytes into shared memory
+constexpr int kStageOffset = 3072;               // operand stages start at the next 1024-byte boundary
 
 struct Barriers {
     uint64_t a_full[kMaxAStages];
@@ -47,27 +56,292 @@ struct Barriers {
     uint32_t tmem_base;
     volatile int abort_flag;
 };
-static_assert(sizeof(Barriers) <= 1024, "barrier block exceeds its reserved bytes");
+static_assert(sizeof(Barriers) <= kTapTableOffset, "barrier block exceeds its reserved bytes");
+static_assert(kTapTableOffset + kMaxTaps * 16 <= kStageOffset, "tap table exceeds its reserved bytes");
+
+// Cycle accounting per CTA, compiled in only with -DDGRAD_TRACE (a tracing
+// build used to see where a launch spends its time).  Slots: MMA waits on
+// acc_empty / A_full / B_full, MMA issue, producer waits on A_empty,
+// producer issue, epilogue waits on acc_full, epilogue work, units, chunks,
+// launch-relative cycle of the first MMA, of the MMA loop's end, of the
+// producers' end, of the epilogue's end.
+#ifdef DGRAD_TRACE
+constexpr int kTraceSlots = 16;
+constexpr int kTraceCtas = 1024;
+__device__ unsigned long long g_trace[kTraceCtas * kTraceSlots];
+#define DGRAD_TRACE_ADD(slot, v) \
+    atomicAdd(&g_trace[(blockIdx.x % kTraceCtas) * kTraceSlots + (slot)], (unsigned long long)(v))
+#define DGRAD_TRACE_CLOCK(x) const long long x = clock64()
+#else
+#define DGRAD_TRACE_ADD(slot, v) ((void)0)
+#define DGRAD_TRACE_CLOCK(x) ((void)0)
+#endif
 
 __device__ __forceinline__ void fail(Barriers *bars, const MainParams &p) {
     bars->abort_flag = 1;
     atomicOr(p.err, kErrTimeout);
 }
 
+// Ring position: stage index and the parity of its current round.
+struct Ring {
+    int stage = 0;
+    uint32_t parity = 0;
+    __device__ __forceinline__ void next(int n) {
+        if (++stage == n) {
+            stage = 0;
+            parity ^= 1;
+        }
+    }
+};
+
+// ------------------------------------------------------------------ producers
+// Number of grad_out elements of image n (plane order j = oh*oW + ow) whose
+// frame position is below P.
+__device__ __forceinline__ int plane_elems_below(const MainParams &p, int n, int P) {
+    const int rel = P - (n * p.Hv + p.Ph) * p.Wp - p.Pw;
+    if (rel <= 0) return 0;
+    const int oh = rel / p.Wp;
+    if (oh >= p.oH) return p.oH * p.oW;
+    return oh * p.oW + min(rel - oh * p.Wp, p.oW);
+}
+
+// Quad producer.  The 256 producer threads form two groups of 128 that fill
+// alternate A stages, so two stages' loads are in flight.  Inside a stage, a
+// warp item is 8 consecutive aligned quads (4 plane elements) x 16 channels:
+// lane (qsub, cg) loads channels cg*4..cg*4+3 of its quad with 16-byte loads
+// (each load instruction reads four full 128-byte lines), transposes the
+// 4x4 block in registers, rounds to TF32 and writes four 16-byte row chunks.
+// Lanes 8p..8p+7 hold quads 2p, 2p+1 x cg 0..3: their rows sit 4 apart, so
+// the swizzled chunk positions of one store phase are all distinct.  Frame
+// rows with no grad_out element are written as zeros.
+template <int KC>
+__device__ __forceinline__ void produce_quads(const MainParams &p, Barriers *bars, float *a_base, int a_stage_floats,
+                                              int tile_rows, long long tmo) {
+    const int gtid = threadIdx.x - kProdWarp0 * 32;
+    const int group = gtid / kGroupThreads;
+    const int tid = gtid % kGroupThreads;
+    const int gw = tid / 32, lane = tid % 32;
+    const int qsub = ((lane >> 3) << 1) | ((lane >> 2) & 1);
+    const int cg = lane & 3;
+    const int plane = p.oH * p.oW;
+    const int img = p.Hv * p.Wp;
+    const uint32_t a0 = dev::smem_u32(a_base);
+    constexpr int kZeroRowsPerThread = (kRowSlots * kMaxRowsPerThread + kGroupThreads - 1) / kGroupThreads;
+    Ring ring;
+    uint32_t it = 0;
+    for (int w = blockIdx.x; w < p.n_work && !bars->abort_flag; w += gridDim.x) {
+        const int P0 = (w / p.n_slices) * tile_rows;
+        const int P1 = P0 + p.a_rows;
+        // Rows of this thread that hold no grad_out element (zeros), as a mask.
+        uint32_t zero_mask = 0;
+#pragma unroll
+        for (int i = 0; i < kZeroRowsPerThread; ++i) {
+            const int r = tid + kGroupThreads * i;
+            if (r < p.a_rows && dev::frame_row_offset(p, P0 + r) < 0) zero_mask |= 1u << i;
+        }
+        // Images overlapping the band and their quad ranges.
+        const int n_lo = min(P0 / img, p.N - 1);
+        const int n_hi = min((P1 - 1) / img, p.N - 1);
+        int seg_n[kMaxBandImages], seg_jlo[kMaxBandImages], seg_jhi[kMaxBandImages], seg_q0[kMaxBandImages];
+        int seg_start[kMaxBandImages + 1];
+        int items = 0;
+#pragma unroll
+        for (int s = 0; s < kMaxBandImages; ++s) {
+            const int n = n_lo + s;
+            seg_n[s] = n;
+            seg_jlo[s] = seg_jhi[s] = seg_q0[s] = 0;
+            seg_start[s] = items;
+            if (n <= n_hi) {
+                const int jlo = plane_elems_below(p, n, P0), jhi = plane_elems_below(p, n, P1);
+                seg_jlo[s] = jlo;
+                seg_jhi[s] = jhi;
+                seg_q0[s] = jlo >> 2;
+                if (jhi > jlo) items += (((jhi + 3) >> 2) - seg_q0[s] + 7) / 8 * 2;   // octets x 2 halves
+            }
+        }
+        seg_start[kMaxBandImages] = items;
+
+        for (int c = 0; c < p.n_chunks; ++c, ++it, ring.next(p.a_stages)) {
+            if (static_cast<int>(it & 1) != group) continue;
+            DGRAD_TRACE_CLOCK(tw0);
+            if (!dev::mbar_wait(dev::smem_u32(&bars->a_empty[ring.stage]), ring.parity ^ 1, tmo)) {
+                fail(bars, p);
+                return;
+            }
+            DGRAD_TRACE_CLOCK(tw1);
+            if (gtid == 0) DGRAD_TRACE_ADD(4, tw1 - tw0);
+            const uint32_t as = a0 + static_cast<uint32_t>(ring.stage) * a_stage_floats * 4;
+            // zero rows
+#pragma unroll
+            for (int i = 0; i < kZeroRowsPerThread; ++i) {
+                if (zero_mask & (1u << i)) {
+                    const uint32_t row = as + static_cast<uint32_t>(tid + kGroupThreads * i) * 128;
+#pragma unroll
+                    for (int k = 0; k < 8; ++k)
+                        asm volatile("st.shared.v4.f32 [%0], {%1, %1, %1, %1};" ::"r"(row + 16 * k), "f"(0.f)
+                                     : "memory");
+                }
+            }
+            // data quads, kQuadBatch warp items with their loads in flight
+            for (int base = gw; base < items; base += 4 * kQuadBatch) {
+                float4 v[kQuadBatch][4];
+                int jq[kQuadBatch], nq[kQuadBatch], jloq[kQuadBatch], jhiq[kQuadBatch], hq[kQuadBatch];
+#pragma unroll
+                for (int b = 0; b < kQuadBatch; ++b) {
+                    const int item = base + 4 * b;
+                    jq[b] = -1;
+                    nq[b] = jloq[b] = jhiq[b] = hq[b] = 0;
+                    if (item < items) {
+                        // segment of the item (selects over static indices: no local memory)
+                        int sn = seg_n[0], sjlo = seg_jlo[0], sjhi = seg_jhi[0], sq0 = seg_q0[0], sst = seg_start[0];
+#pragma unroll
+                        for (int k = 1; k < kMaxBandImages; ++k) {
+                            if (item >= seg_start[k]) {
+                                sn = seg_n[k];
+                                sjlo = seg_jlo[k];
+                                sjhi = seg_jhi[k];
+                                sq0 = seg_q0[k];
+                                sst = seg_start[k];
+                            }
+                        }
+                        const int local = item - sst;
+                        const int half = local & 1;
+                        const int j = (sq0 + (local >> 1) * 8 + qsub) * 4;
+                        if (j < sjhi) {
+                            jq[b] = j;
+                            nq[b] = sn;
+                            jloq[b] = sjlo;
+                            jhiq[b] = sjhi;
+                            hq[b] = half;
+                            const int ch = c * KC + half * 16 + cg * 4;
+                            const float4 *src = reinterpret_cast<const float4 *>(
+                                p.go + (static_cast<size_t>(sn) * p.Co + ch) * plane + j);
+#pragma unroll
+                            for (int k = 0; k < 4; ++k)
+                                v[b][k] = (ch + k < p.Co) ? __ldg(src + static_cast<size_t>(k) * (plane / 4))
+                                                          : make_float4(0.f, 0.f, 0.f, 0.f);
+                        }
+                    }
+                }
+                DGRAD_TRACE_CLOCK(tq1);
+                if (gtid == 0) DGRAD_TRACE_ADD(14, tq1 - tw1);
+#pragma unroll
+                for (int b = 0; b < kQuadBatch; ++b) {
+                    if (jq[b] < 0) continue;
+                    const int j = jq[b];
+                    const int n = nq[b];
+                    int oh = j / p.oW, ow = j - oh * p.oW;
+                    const float ev[4][4] = {{v[b][0].x, v[b][1].x, v[b][2].x, v[b][3].x},
+                                            {v[b][0].y, v[b][1].y, v[b][2].y, v[b][3].y},
+                                            {v[b][0].z, v[b][1].z, v[b][2].z, v[b][3].z},
+                                            {v[b][0].w, v[b][1].w, v[b][2].w, v[b][3].w}};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int je = j + e;
+                        if (je >= jloq[b] && je < jhiq[b]) {
+                            const int r = (n * p.Hv + oh + p.Ph) * p.Wp + ow + p.Pw - P0;
+                            float x0 = ev[e][0], x1 = ev[e][1], x2 = ev[e][2], x3 = ev[e][3];
+                            if (p.round_tf32) {
+                                x0 = dev::round_tf32(x0);
+                                x1 = dev::round_tf32(x1);
+                                x2 = dev::round_tf32(x2);
+                                x3 = dev::round_tf32(x3);
+                            }
+                            const uint32_t dst = as + static_cast<uint32_t>(r) * 128 +
+                                                 (static_cast<uint32_t>((hq[b] * 4 + cg) ^ (r & 7)) << 4);
+                            asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "f"(x0), "f"(x1),
+                                         "f"(x2), "f"(x3)
+                                         : "memory");
+                        }
+                        if (++ow == p.oW) {
+                            ow = 0;
+                            ++oh;
+                        }
+                    }
+                }
+            }
+            DGRAD_TRACE_CLOCK(tw2);
+            if (gtid == 0) DGRAD_TRACE_ADD(5, tw2 - tw1);
+            if (gtid == 0) DGRAD_TRACE_ADD(15, 1);
+            // The writer makes its stores visible to the tensor core's
+            // (async-proxy) operand reads, then releases the stage.
+            dev::fence_proxy_async_smem();
+            dev::mbar_arrive(dev::smem_u32(&bars->a_full[ring.stage]));
+        }
+    }
+}
+
+// 4-byte producer (any shape).  Thread (pr, e) copies frame rows
+// r = pr + kRowSlots*i, channel e of every 4-channel group with
+// asynchronous copies (zero-fill for padding).  One warp instruction moves 8
+// consecutive rows x 4 channels into eight distinct 16-byte chunks of the
+// swizzled rows.  The tensor core reads the TF32 part of these fp32 values.
+template <int KC>
+__device__ __forceinline__ void produce_async4(const MainParams &p, Barriers *bars, float *a_base, int a_stage_floats,
+                                               int tile_rows, long long tmo) {
+    const int ptid = threadIdx.x - kProdWarp0 * 32;
+    const int e = ptid & 3, pr = ptid >> 2;
+    const int sw = pr & 7;
+    const size_t plane = static_cast<size_t>(p.oH) * p.oW;
+    const uint32_t a0 = dev::smem_u32(a_base) + e * 4;
+    Ring ring;
+    for (int w = blockIdx.x; w < p.n_work && !bars->abort_flag; w += gridDim.x) {
+        const int P0 = (w / p.n_slices) * tile_rows;
+        int off[kMaxRowsPerThread];
+#pragma unroll
+        for (int i = 0; i < kMaxRowsPerThread; ++i) {
+            const int r = pr + kRowSlots * i;
+            off[i] = r < p.a_rows ? dev::frame_row_offset(p, P0 + r) : -1;
+        }
+        for (int c = 0; c < p.n_chunks; ++c, ring.next(p.a_stages)) {
+            if (!dev::mbar_wait(dev::smem_u32(&bars->a_empty[ring.stage]), ring.parity ^ 1, tmo)) {
+                fail(bars, p);
+                dev::cp_async_wait_all();
+                return;
+            }
+            const uint32_t as = a0 + static_cast<uint32_t>(ring.stage) * a_stage_floats * 4;
+            const int co0 = c * KC + e;
+#pragma unroll
+            for (int i = 0; i < kMaxRowsPerThread; ++i) {
+                const int r = pr + kRowSlots * i;
+                if (r < p.a_rows) {
+                    const uint32_t dst = as + static_cast<uint32_t>(r) * 128;
+#pragma unroll
+                    for (int g = 0; g < KC / 4; ++g) {
+                        const int co = co0 + 4 * g;
+                        const bool v = off[i] >= 0 && co < p.Co;
+                        const float *src = v ? p.go + static_cast<size_t>(off[i]) + co * plane : p.go;
+                        dev::cp_async_4(dst + ((g ^ sw) << 4), src, v ? 4u : 0u);
+                    }
+                }
+            }
+            dev::cp_async_arrive(dev::smem_u32(&bars->a_full[ring.stage]));
+        }
+    }
+    dev::cp_async_wait_all();
+}
+
 template <int KC>
 __global__ void __launch_bounds__(kThreads, 1) tc_dgrad_kernel(const __grid_constant__ MainParams p) {
+    static_assert(KC == 32, "operand rows are one 128-byte swizzle row of 32 TF32 values");
     extern __shared__ __align__(1024) uint8_t smem[];
     Barriers *bars = reinterpret_cast<Barriers *>(smem);
-    float *a_base = reinterpret_cast<float *>(smem + 1024);
+    uint4 *tap_table = reinterpret_cast<uint4 *>(smem + kTapTableOffset);
+    // Operand stages start on a 1024-byte boundary of the shared window: the
+    // 128-byte swizzle is a function of the address bits inside that pattern.
+    const uint32_t smem0 = dev::smem_u32(smem);
+    const uint32_t stage0 = (smem0 + kStageOffset + 1023) & ~1023u;
+    float *a_base = reinterpret_cast<float *>(smem + (stage0 - smem0));
     const int a_stage_floats = p.a_rows * KC;
-    uint8_t *b_base = smem + 1024 + static_cast<size_t>(p.a_stages) * a_stage_floats * 4;
+    uint8_t *b_base = reinterpret_cast<uint8_t *>(a_base) + static_cast<size_t>(p.a_stages) * a_stage_floats * 4;
 
     const int warp = threadIdx.x / 32;
     const int lane = threadIdx.x % 32;
 
     if (threadIdx.x == 0) {
+        const uint32_t a_arrivals = p.vec_producer ? kGroupThreads : kProdWarps * 32;
         for (int i = 0; i < p.a_stages; ++i) {
-            dev::mbar_init(dev::smem_u32(&bars->a_full[i]), kProdWarps * 32);
+            dev::mbar_init(dev::smem_u32(&bars->a_full[i]), a_arrivals);
             dev::mbar_init(dev::smem_u32(&bars->a_empty[i]), 1);
         }
         for (int i = 0; i < p.b_stages; ++i) {
@@ -85,150 +359,193 @@ __global__ void __launch_bounds__(kThreads, 1) tc_dgrad_kernel(const __grid_cons
     if (warp == kMmaWarp) {
         dev::tmem_alloc(dev::smem_u32(&bars->tmem_base), p.tmem_cols);
         dev::tmem_relinquish();
+        // Per-tap MMA data: A row offset (bytes), accumulator column offset,
+        // and whether the tap is the first of its phase.
+        for (int t = lane; t < p.n_taps; t += 32) {
+            const TapDesc td = p.tap[t];
+            tap_table[t] = make_uint4(static_cast<uint32_t>(td.shift) * 128, static_cast<uint32_t>(td.phase * p.bn),
+                                      t == p.phase[td.phase].tap_begin ? 1u : 0u, 0u);
+        }
     }
     dev::tc_fence_before();
     __syncthreads();
     dev::tc_fence_after();
     const uint32_t tmem_base = bars->tmem_base;
     const long long tmo = p.timeout_ns;
+    DGRAD_TRACE_CLOCK(t_start);
     const int tile_rows = p.tm * kBlockM;
 
     if (warp >= kProdWarp0) {
         // ------------------------------------------------------ producers
-        const int ptid = threadIdx.x - kProdWarp0 * 32;
-        uint32_t it = 0;
-        for (int w = blockIdx.x; w < p.n_work && !bars->abort_flag; w += gridDim.x) {
-            const int P0 = (w / p.n_slices) * tile_rows;
-            for (int c = 0; c < p.n_chunks; ++c, ++it) {
-                const int stage = it % p.a_stages;
-                const uint32_t round = it / p.a_stages;
-                if (!dev::mbar_wait(dev::smem_u32(&bars->a_empty[stage]), (round & 1) ^ 1, tmo)) {
-                    fail(bars, p);
-                    break;
-                }
-                float *As = a_base + static_cast<size_t>(stage) * a_stage_floats;
-                dev::fill_a_stage<KC>(As, p, P0, c * KC, ptid, kProdWarps * 32);
-                dev::fence_proxy_async_smem();
-                dev::mbar_arrive(dev::smem_u32(&bars->a_full[stage]));
-            }
-        }
+        if (p.vec_producer)
+            produce_quads<KC>(p, bars, a_base, a_stage_floats, tile_rows, tmo);
+        else
+            produce_async4<KC>(p, bars, a_base, a_stage_floats, tile_rows, tmo);
+        DGRAD_TRACE_CLOCK(t_pend);
+        if (threadIdx.x == kProdWarp0 * 32) DGRAD_TRACE_ADD(12, t_pend - t_start);
     } else if (warp == kLoadWarp) {
         // ------------------------------------------------- weight loader
+        // B stage (c, tg) = taps [tg*tap_group, ...) of channel chunk c of the
+        // work unit's slice: one contiguous block of the packed weights.
         if (lane == 0) {
             dev::grid_dependency_wait();   // packed weights come from the preceding kernel
-            int last_round[kMaxBStages];
-            for (int i = 0; i < kMaxBStages; ++i) last_round[i] = -1;
-            if (p.b_resident) {
+            const size_t tap_bytes = static_cast<size_t>(p.bn) * 128;
+            int last_parity[kMaxBStages];   // parity of each stage's last fill, -1 if never filled
+            for (int i = 0; i < kMaxBStages; ++i) last_parity[i] = -1;
+            if (p.b_resident) {   // one slice, one group per chunk: load everything once
                 for (int c = 0; c < p.n_chunks; ++c) {
                     const uint32_t bar = dev::smem_u32(&bars->b_full[c]);
                     dev::mbar_arrive_expect_tx(bar, p.chunk_bytes);
                     dev::bulk_g2s(dev::smem_u32(b_base + static_cast<size_t>(c) * p.chunk_bytes),
                                   reinterpret_cast<const uint8_t *>(p.wp) + static_cast<size_t>(c) * p.chunk_bytes,
                                   p.chunk_bytes, bar);
-                    last_round[c] = 0;
+                    last_parity[c] = 0;
                 }
             } else {
-                uint32_t it = 0;
-                for (int w = blockIdx.x; w < p.n_work && !bars->abort_flag; w += gridDim.x) {
+                Ring ring;
+                bool ok = true;
+                for (int w = blockIdx.x; ok && w < p.n_work && !bars->abort_flag; w += gridDim.x) {
                     const int slice = w % p.n_slices;
-                    bool ok = true;
-                    for (int c = 0; c < p.n_chunks; ++c, ++it) {
-                        const int stage = it % p.b_stages;
-                        const uint32_t round = it / p.b_stages;
-                        if (!dev::mbar_wait(dev::smem_u32(&bars->b_empty[stage]), (round & 1) ^ 1, tmo)) {
-                            fail(bars, p);
-                            ok = false;
-                            break;
+                    for (int c = 0; ok && c < p.n_chunks; ++c) {
+                        for (int tg = 0; tg < p.n_tgroups; ++tg) {
+                            if (!dev::mbar_wait(dev::smem_u32(&bars->b_empty[ring.stage]), ring.parity ^ 1, tmo)) {
+                                fail(bars, p);
+                                ok = false;
+                                break;
+                            }
+                            const int t0 = tg * p.tap_group;
+                            const int nt = min(p.tap_group, p.n_taps - t0);
+                            const uint32_t bytes = static_cast<uint32_t>(nt * tap_bytes);
+                            const uint32_t bar = dev::smem_u32(&bars->b_full[ring.stage]);
+                            dev::mbar_arrive_expect_tx(bar, bytes);
+                            const size_t off =
+                                ((static_cast<size_t>(slice) * p.n_chunks + c) * p.n_taps + t0) * tap_bytes;
+                            dev::bulk_g2s(dev::smem_u32(b_base + static_cast<size_t>(ring.stage) * p.chunk_bytes),
+                                          reinterpret_cast<const uint8_t *>(p.wp) + off, bytes, bar);
+                            last_parity[ring.stage] = static_cast<int>(ring.parity);
+                            ring.next(p.b_stages);
                         }
-                        const uint32_t bar = dev::smem_u32(&bars->b_full[stage]);
-                        dev::mbar_arrive_expect_tx(bar, p.chunk_bytes);
-                        const size_t off = (static_cast<size_t>(slice) * p.n_chunks + c) * p.chunk_bytes;
-                        dev::bulk_g2s(dev::smem_u32(b_base + static_cast<size_t>(stage) * p.chunk_bytes),
-                                      reinterpret_cast<const uint8_t *>(p.wp) + off, p.chunk_bytes, bar);
-                        last_round[stage] = static_cast<int>(round);
                     }
-                    if (!ok) break;
                 }
             }
             // Never leave with a copy in flight into this CTA's shared memory.
             for (int i = 0; i < p.b_stages && i < kMaxBStages; ++i)
-                if (last_round[i] >= 0)
-                    dev::mbar_wait(dev::smem_u32(&bars->b_full[i]), last_round[i] & 1, tmo);
+                if (last_parity[i] >= 0) dev::mbar_wait(dev::smem_u32(&bars->b_full[i]), last_parity[i], tmo);
         }
         __syncwarp();
     } else if (warp == kMmaWarp) {
         // ---------------------------------------------------- MMA issuer
-        if (lane == 0) {
-            const uint32_t a_lbo = static_cast<uint32_t>(p.a_rows) * 16;
-            const uint32_t b_lbo = static_cast<uint32_t>(p.bn) * 16;
-            const uint32_t a0 = dev::smem_u32(a_base);
-            const uint32_t b0 = dev::smem_u32(b_base);
-            uint32_t a_it = 0, b_it = 0, local = 0;
-            bool ok = true;
-            for (int w = blockIdx.x; ok && w < p.n_work && !bars->abort_flag; w += gridDim.x, ++local) {
-                const int buf = local % p.acc_bufs;
-                const uint32_t around = local / p.acc_bufs;
-                if (!dev::mbar_wait(dev::smem_u32(&bars->acc_empty[buf]), (around & 1) ^ 1, tmo)) {
-                    fail(bars, p);
+        // The whole warp runs this loop converged; every wait is taken by all
+        // lanes and agreed with a vote, and one elected lane issues the MMAs
+        // and commits (warp-uniform descriptors stay in uniform registers).
+        const uint32_t a_addr0 = dev::smem_u32(a_base);
+        const uint32_t b_addr0 = dev::smem_u32(b_base);
+        const uint32_t tap_b_bytes = static_cast<uint32_t>(p.bn) * 128;   // one tap of one chunk of B
+        Ring ra, rb, racc;
+        bool ok = true;
+        bool first_chunk = true;
+        for (int w = blockIdx.x; ok && w < p.n_work && !bars->abort_flag; w += gridDim.x, racc.next(p.acc_bufs)) {
+            DGRAD_TRACE_CLOCK(tm0);
+            if (!__all_sync(0xffffffffu,
+                            dev::mbar_wait(dev::smem_u32(&bars->acc_empty[racc.stage]), racc.parity ^ 1, tmo))) {
+                if (lane == 0) fail(bars, p);
+                break;
+            }
+            DGRAD_TRACE_CLOCK(tm1);
+            if (lane == 0) {
+                DGRAD_TRACE_ADD(0, tm1 - tm0);
+                DGRAD_TRACE_ADD(8, 1);
+            }
+            dev::tc_fence_after();
+            const uint32_t d_base = tmem_base + racc.stage * p.acc_cols;
+            for (int c = 0; ok && c < p.n_chunks; ++c, ra.next(p.a_stages)) {
+                DGRAD_TRACE_CLOCK(tc0);
+                if (!__all_sync(0xffffffffu, dev::mbar_wait(dev::smem_u32(&bars->a_full[ra.stage]), ra.parity, tmo))) {
+                    if (lane == 0) fail(bars, p);
+                    ok = false;
                     break;
                 }
-                dev::tc_fence_after();
-                const uint32_t d_base = tmem_base + buf * p.acc_cols;
-                for (int c = 0; c < p.n_chunks; ++c, ++a_it, ++b_it) {
-                    const int sa = a_it % p.a_stages;
-                    const int sb = p.b_resident ? c : static_cast<int>(b_it % p.b_stages);
-                    const uint32_t rb = p.b_resident ? 0u : b_it / p.b_stages;
-                    if (!dev::mbar_wait(dev::smem_u32(&bars->a_full[sa]), (a_it / p.a_stages) & 1, tmo) ||
-                        !dev::mbar_wait(dev::smem_u32(&bars->b_full[sb]), rb & 1, tmo)) {
-                        fail(bars, p);
+                DGRAD_TRACE_CLOCK(tc1);
+                if (lane == 0) {
+                    DGRAD_TRACE_ADD(1, tc1 - tc0);
+                    DGRAD_TRACE_ADD(9, 1);
+                    if (first_chunk) DGRAD_TRACE_ADD(10, tc1 - t_start);
+                }
+                first_chunk = false;
+                // Stages written with cp.async (4-byte producer) reach the
+                // consumer through the barrier only; make them visible to the
+                // tensor core's operand reads here.  The quad producer fences
+                // its own stores instead, so this fence (which would also wait
+                // for this thread's MMAs in flight) is not taken on that path.
+                if (!p.vec_producer) dev::fence_proxy_async_smem();
+                const uint32_t a_stage = a_addr0 + static_cast<uint32_t>(ra.stage) * a_stage_floats * 4;
+                for (int tg = 0; tg < p.n_tgroups; ++tg) {
+                    const int sb = p.b_resident ? c : rb.stage;
+                    const uint32_t pb = p.b_resident ? 0u : rb.parity;
+                    DGRAD_TRACE_CLOCK(tb0);
+                    if (!__all_sync(0xffffffffu, dev::mbar_wait(dev::smem_u32(&bars->b_full[sb]), pb, tmo))) {
+                        if (lane == 0) fail(bars, p);
                         ok = false;
                         break;
                     }
+                    DGRAD_TRACE_CLOCK(tb1);
+                    if (lane == 0) DGRAD_TRACE_ADD(2, tb1 - tb0);
                     dev::tc_fence_after();
-                    const uint32_t a_stage = a0 + static_cast<uint32_t>(sa) * a_stage_floats * 4;
-                    const uint32_t b_stage = b0 + static_cast<uint32_t>(sb) * p.chunk_bytes;
+                    const int t0 = tg * p.tap_group, t1 = min(p.n_taps, t0 + p.tap_group);
+                    const uint64_t bd_s = dev::smem_desc_sw128(b_addr0 + static_cast<uint32_t>(sb) * p.chunk_bytes, 0);
                     for (int m = 0; m < p.tm; ++m) {
-                        for (int ph = 0; ph < p.n_phases; ++ph) {
-                            const PhaseDesc &pd = p.phase[ph];
-                            const uint32_t d = d_base + (m * p.n_phases + ph) * p.bn;
-                            for (int t = pd.tap_begin; t < pd.tap_begin + pd.tap_count; ++t) {
-                                const uint32_t a_row = static_cast<uint32_t>(m * kBlockM + p.tap[t].shift) * 16;
+                        const uint32_t a_m = a_stage + static_cast<uint32_t>(m * kBlockM) * 128;
+                        const uint32_t d_m = d_base + static_cast<uint32_t>(m * p.n_phases * p.bn);
+                        uint4 nxt = tap_table[t0];
+                        for (int t = t0; t < t1; ++t) {
+                            const uint4 cur = nxt;
+                            if (t + 1 < t1) nxt = tap_table[t + 1];   // prefetch the next tap's entry
+                            // A window of tap t: frame rows [m*128 + shift, +128) of the
+                            // stage.  The swizzle follows the absolute address bits, so the
+                            // window may start on any 128-byte row with base offset 0.
+                            const uint64_t ad_t = dev::smem_desc_sw128(a_m + cur.x, 0);
+                            const uint64_t bd_t = dev::desc_add(bd_s, static_cast<uint32_t>(t - t0) * tap_b_bytes);
+                            const uint32_t d = d_m + cur.y;
+                            const uint32_t acc0 = (c > 0 || cur.z == 0) ? 1u : 0u;
 #pragma unroll
-                                for (int k8 = 0; k8 < KC / 8; ++k8) {
-                                    const uint64_t ad = dev::smem_desc(a_stage + 2 * k8 * a_lbo + a_row, a_lbo, 128);
-                                    const uint64_t bd = dev::smem_desc(
-                                        b_stage + static_cast<uint32_t>((t * (KC / 4) + 2 * k8) * p.bn) * 16, b_lbo,
-                                        128);
-                                    const uint32_t acc = (c > 0 || t > pd.tap_begin || k8 > 0) ? 1u : 0u;
-                                    dev::mma_tf32(d, ad, bd, p.idesc, acc);
-                                }
-                            }
+                            for (int k8 = 0; k8 < KC / 8; ++k8)
+                                dev::mma_tf32_elect(d, dev::desc_add(ad_t, 32 * k8), dev::desc_add(bd_t, 32 * k8),
+                                                    p.idesc, k8 > 0 ? 1u : acc0);
                         }
                     }
-                    dev::mma_commit(dev::smem_u32(&bars->a_empty[sa]));
-                    if (!p.b_resident) dev::mma_commit(dev::smem_u32(&bars->b_empty[sb]));
+                    if (!p.b_resident) {
+                        dev::mma_commit_elect(dev::smem_u32(&bars->b_empty[sb]));
+                        rb.next(p.b_stages);
+                    }
+                    DGRAD_TRACE_CLOCK(tb2);
+                    if (lane == 0) DGRAD_TRACE_ADD(3, tb2 - tb1);
                 }
                 if (!ok) break;
-                dev::mma_commit(dev::smem_u32(&bars->acc_full[buf]));
+                dev::mma_commit_elect(dev::smem_u32(&bars->a_empty[ra.stage]));
             }
-            // Drain: every MMA issued above has finished before TMEM is freed.
-            dev::mma_commit(dev::smem_u32(&bars->drain));
-            if (!dev::mbar_wait(dev::smem_u32(&bars->drain), 0, tmo)) fail(bars, p);
+            if (!ok) break;
+            dev::mma_commit_elect(dev::smem_u32(&bars->acc_full[racc.stage]));
         }
-        __syncwarp();
+        // Drain: every MMA issued above has finished before TMEM is freed.
+        dev::mma_commit_elect(dev::smem_u32(&bars->drain));
+        if (!__all_sync(0xffffffffu, dev::mbar_wait(dev::smem_u32(&bars->drain), 0, tmo)) && lane == 0)
+            fail(bars, p);
+        DGRAD_TRACE_CLOCK(t_mend);
+        if (lane == 0) DGRAD_TRACE_ADD(11, t_mend - t_start);
     } else {
         // ------------------------------------------------------- epilogue
         const int ew = warp;   // 0..3: tensor-memory lanes 32*ew .. 32*ew+31
         const size_t plane = static_cast<size_t>(p.H) * p.W;
-        uint32_t local = 0;
-        for (int w = blockIdx.x; w < p.n_work && !bars->abort_flag; w += gridDim.x, ++local) {
+        Ring racc;
+        for (int w = blockIdx.x; w < p.n_work && !bars->abort_flag; w += gridDim.x, racc.next(p.acc_bufs)) {
             const int tile = w / p.n_slices, slice = w % p.n_slices;
-            const int buf = local % p.acc_bufs;
-            const uint32_t around = local / p.acc_bufs;
-            if (!dev::mbar_wait(dev::smem_u32(&bars->acc_full[buf]), around & 1, tmo)) {
+            DGRAD_TRACE_CLOCK(te0);
+            if (!dev::mbar_wait(dev::smem_u32(&bars->acc_full[racc.stage]), racc.parity, tmo)) {
                 fail(bars, p);
                 break;
             }
+            DGRAD_TRACE_CLOCK(te1);
+            if (threadIdx.x == 0) DGRAD_TRACE_ADD(6, te1 - te0);
             dev::tc_fence_after();
             const int ci0 = slice * p.bn;
             const int nci = min(p.bn, p.Ci - ci0);
@@ -241,30 +558,41 @@ __global__ void __launch_bounds__(kThreads, 1) tc_dgrad_kernel(const __grid_cons
                     const PhaseDesc &pd = p.phase[ph];
                     const bool valid = pos_ok && q < pd.Hq && u < pd.Wq;
                     const int ih = p.s * q + pd.a, iw = p.s * u + pd.b;
-                    float *dst = p.gi + (static_cast<size_t>(n) * p.Ci + ci0) * plane +
-                                 static_cast<size_t>(ih) * p.W + iw;
+                    float *dst =
+                        p.gi + (static_cast<size_t>(n) * p.Ci + ci0) * plane + static_cast<size_t>(ih) * p.W + iw;
                     if (pd.tap_count == 0) {
                         if (valid)
                             for (int j = 0; j < nci; ++j) dst[j * plane] = 0.f;
                         continue;
                     }
-                    const uint32_t col0 = tmem_base + (static_cast<uint32_t>(ew * 32) << 16) + buf * p.acc_cols +
-                                          (m * p.n_phases + ph) * p.bn;
-                    for (int c0 = 0; c0 < p.bn; c0 += 16) {
-                        uint32_t r[16];
-                        dev::tmem_ld16(col0 + c0, r);
+                    const uint32_t col0 = tmem_base + (static_cast<uint32_t>(ew * 32) << 16) +
+                                          racc.stage * p.acc_cols + (m * p.n_phases + ph) * p.bn;
+                    for (int c0 = 0; c0 < p.bn; c0 += 32) {
+                        uint32_t r0[16], r1[16];
+                        const bool two = c0 + 16 < p.bn;   // warp-uniform
+                        dev::tmem_ld16(col0 + c0, r0);
+                        if (two) dev::tmem_ld16(col0 + c0 + 16, r1);
                         dev::tmem_wait_ld();
                         if (valid) {
 #pragma unroll
                             for (int j = 0; j < 16; ++j)
-                                if (c0 + j < nci) dst[(c0 + j) * plane] = __uint_as_float(r[j]);
+                                if (c0 + j < nci) dst[(c0 + j) * plane] = __uint_as_float(r0[j]);
+                            if (two) {
+#pragma unroll
+                                for (int j = 0; j < 16; ++j)
+                                    if (c0 + 16 + j < nci) dst[(c0 + 16 + j) * plane] = __uint_as_float(r1[j]);
+                            }
                         }
                     }
                 }
             }
             dev::tc_fence_before();
-            dev::mbar_arrive(dev::smem_u32(&bars->acc_empty[buf]));
+            dev::mbar_arrive(dev::smem_u32(&bars->acc_empty[racc.stage]));
+            DGRAD_TRACE_CLOCK(te2);
+            if (threadIdx.x == 0) DGRAD_TRACE_ADD(7, te2 - te1);
         }
+        DGRAD_TRACE_CLOCK(t_eend);
+        if (threadIdx.x == 0) DGRAD_TRACE_ADD(13, t_eend - t_start);
     }
 
     dev::tc_fence_before();
@@ -293,13 +621,19 @@ cudaError_t launch_kc(const MainParams &p, const Tiling &t, cudaStream_t stream,
 
 }  // namespace
 
+#ifdef DGRAD_TRACE
+// Tracing builds only: copy (and clear) the per-CTA cycle counters.
+extern "C" int dgrad_trace_read(unsigned long long *host, int n) {
+    if (n > kTraceCtas * kTraceSlots) n = kTraceCtas * kTraceSlots;
+    if (cudaMemcpyFromSymbol(host, g_trace, sizeof(unsigned long long) * n) != cudaSuccess) return -1;
+    static unsigned long long zeros[kTraceCtas * kTraceSlots];
+    return cudaMemcpyToSymbol(g_trace, zeros, sizeof(zeros)) == cudaSuccess ? 0 : -1;
+}
+#endif
+
 cudaError_t launch_tc(const MainParams &p, const Tiling &t, cudaStream_t stream, bool pdl) {
-    switch (t.kc) {
-        case 8: return launch_kc<8>(p, t, stream, pdl);
-        case 16: return launch_kc<16>(p, t, stream, pdl);
-        case 32: return launch_kc<32>(p, t, stream, pdl);
-        default: return cudaErrorInvalidValue;
-    }
+    if (t.kc != 32) return cudaErrorInvalidValue;
+    return launch_kc<32>(p, t, stream, pdl);
 }
 
 }  // namespace dgrad

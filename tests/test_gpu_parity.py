@@ -110,10 +110,9 @@ def test_edge_shapes(shape, precision):
 # Tilings of the tcgen05 kernel: pipeline depth, chunk size, slices, persistent
 # CTAs that walk several work units (grid smaller than the unit count).
 TILINGS = [
-    dict(tile_blocks=1, chunk_k=8), dict(tile_blocks=1, chunk_k=16), dict(tile_blocks=1, chunk_k=32),
-    dict(tile_blocks=2, chunk_k=16), dict(tile_blocks=2, chunk_k=8, grid=3), dict(tile_blocks=1, slice_n=16, grid=5),
-    dict(tile_blocks=1, slice_n=32, chunk_k=32, grid=7), dict(tile_blocks=3, chunk_k=8, grid=2),
-    dict(tile_blocks=4, chunk_k=8, grid=1), dict(tile_blocks=4, slice_n=16, chunk_k=16, grid=2),
+    dict(tile_blocks=1), dict(tile_blocks=2), dict(tile_blocks=1, chunk_k=32, grid=3),
+    dict(tile_blocks=2, grid=3), dict(tile_blocks=1, slice_n=16, grid=5), dict(tile_blocks=1, slice_n=32, grid=7),
+    dict(tile_blocks=3, grid=2), dict(tile_blocks=4, grid=1), dict(tile_blocks=4, slice_n=16, grid=2),
 ]
 
 

@@ -64,7 +64,7 @@ def test_describe_rejects_bad_options():
     with pytest.raises(dg.DgradError) as e:
         dg.describe(2, 8, 8, 8, 8, 3, 3, 1, 1, 1, "fp32", path="tcgen05")
     assert e.value.status == 2
-    for bad in (dict(slice_n=24), dict(chunk_k=12), dict(tile_blocks=5)):
+    for bad in (dict(slice_n=24), dict(chunk_k=12), dict(chunk_k=16), dict(tile_blocks=5)):
         with pytest.raises(dg.DgradError) as e:
             dg.describe(2, 8, 8, 8, 8, 3, 3, 1, 1, 1, "tf32", **bad)
         assert e.value.status == 1
