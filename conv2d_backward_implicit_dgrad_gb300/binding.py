@@ -34,7 +34,8 @@ EXPORTS = ("dgrad_plan", "dgrad_plan_ex", "dgrad_describe", "dgrad_describe_taps
 
 class Options(ctypes.Structure):
     _fields_ = [("path", ctypes.c_int), ("tile_blocks", ctypes.c_int), ("slice_n", ctypes.c_int),
-                ("chunk_k", ctypes.c_int), ("grid", ctypes.c_int), ("sm_count", ctypes.c_int)]
+                ("chunk_k", ctypes.c_int), ("grid", ctypes.c_int), ("sm_count", ctypes.c_int),
+                ("a_source", ctypes.c_int)]
 
 
 class PlanInfo(ctypes.Structure):
@@ -44,7 +45,8 @@ class PlanInfo(ctypes.Structure):
         ("positions", ctypes.c_longlong), ("max_shift", ctypes.c_int),
         ("tile_blocks", ctypes.c_int), ("slice_n", ctypes.c_int), ("n_slices", ctypes.c_int),
         ("chunk_k", ctypes.c_int), ("n_chunks", ctypes.c_int), ("n_work", ctypes.c_longlong),
-        ("grid", ctypes.c_int), ("b_resident", ctypes.c_int), ("smem_bytes", ctypes.c_int),
+        ("grid", ctypes.c_int), ("b_resident", ctypes.c_int), ("a_source", ctypes.c_int),
+        ("smem_bytes", ctypes.c_int),
         ("tmem_cols", ctypes.c_int), ("workspace_bytes", ctypes.c_size_t),
         ("packed_weight_bytes", ctypes.c_size_t), ("useful_flops", ctypes.c_double),
         ("algorithmic_bytes", ctypes.c_double)]
@@ -52,6 +54,7 @@ class PlanInfo(ctypes.Structure):
     def as_dict(self):
         d = {name: getattr(self, name) for name, _ in self._fields_}
         d["path"] = PATH_NAME.get(d["path"], d["path"])
+        d["a_source"] = A_SOURCE_NAME.get(d["a_source"], d["a_source"])
         d["precision"] = {0: "fp32", 1: "tf32"}.get(d["precision"], d["precision"])
         return d
 
@@ -104,9 +107,13 @@ def load_library(path: str | None = None):
         return lib
 
 
-def _options(path="auto", tile_blocks=0, slice_n=0, chunk_k=0, grid=0, sm_count=0):
+A_SOURCE = {"auto": 0, "frame": 1, "producers": 2}
+A_SOURCE_NAME = {v: k for k, v in A_SOURCE.items()}
+
+
+def _options(path="auto", tile_blocks=0, slice_n=0, chunk_k=0, grid=0, sm_count=0, a_source="auto"):
     return Options(PATH[path] if isinstance(path, str) else int(path), tile_blocks, slice_n, chunk_k, grid,
-                   sm_count)
+                   sm_count, A_SOURCE[a_source] if isinstance(a_source, str) else int(a_source))
 
 
 def describe(N, Ci, H, W, Co, kH, kW, stride, pad_h, pad_w, precision="tf32", **opts) -> dict:

@@ -1,10 +1,12 @@
 // C ABI of libdgrad_gb300 (declared in include/dgrad.h): plan creation,
 // validation, launches and error reporting.
 #include <cuda_runtime.h>
+#include <cudaTypedefs.h>
 
 #include <cstdint>
 #include <cstdlib>
 #include <cstring>
+#include <mutex>
 #include <new>
 
 #include "dgrad.h"
@@ -18,6 +20,8 @@ struct dgrad_plan_s {
     dgrad::MainParams mp;
     dgrad::PrepackParams pp;
     float *wp;             // packed weights (device)
+    float *frame;          // packed grad_out frame (device), tensor-copy mode only
+    dgrad::FramePackParams fp;
     uint32_t *err;         // device error word
     float *stage_go;       // dgrad_run_host staging (device), allocated on first use
     float *stage_w;
@@ -54,6 +58,7 @@ void fill_info(const Geometry &g, const Tiling &t, int precision, size_t ws, dgr
     info->n_work = t.n_work;
     info->grid = t.path == DGRAD_PATH_SIMT ? (int)t.n_work : t.grid;
     info->b_resident = t.b_resident;
+    info->a_source = t.path == DGRAD_PATH_TCGEN05 ? (t.a_tma ? 1 : 2) : 0;
     info->smem_bytes = t.smem_bytes;
     info->tmem_cols = t.tmem_cols;
     info->workspace_bytes = ws;
@@ -87,6 +92,17 @@ void fill_params(dgrad_plan_s *pl) {
     m.chunk_bytes = t.chunk_bytes;
     m.tap_group = t.tap_group; m.n_tgroups = t.n_tgroups;
     m.vec_producer = dgrad::use_vec_producer(g, t) ? 1 : 0;
+    m.a_tma = t.a_tma; m.a_box_rows = t.a_box_rows; m.a_nbox = t.a_nbox;
+
+    dgrad::FramePackParams &f = pl->fp;
+    std::memset(&f, 0, sizeof(f));
+    f.v = pl->frame;
+    f.N = g.N; f.Co = g.Co; f.oH = g.oH; f.oW = g.oW; f.Hv = g.Hv; f.Wp = g.Wp; f.Ph = g.Ph; f.Pw = g.Pw;
+    f.co_v = t.co_v;
+    f.round_tf32 = pl->precision == DGRAD_PREC_TF32 ? 1 : 0;
+    f.positions = (int)g.positions;
+    f.pos_tiles = (int)((g.positions + dgrad::kFramePackCols - 1) / dgrad::kFramePackCols);
+    f.c_groups = (t.co_v + 31) / 32;
     m.acc_bufs = t.acc_bufs; m.acc_cols = t.acc_cols; m.tmem_cols = t.tmem_cols;
     m.round_tf32 = pl->precision == DGRAD_PREC_TF32 ? 1 : 0;
     m.n_phases = g.n_phases;
@@ -110,6 +126,39 @@ void fill_params(dgrad_plan_s *pl) {
     }
 }
 
+// cuTensorMapEncodeTiled from the driver, looked up once through the
+// runtime (no link-time dependency on the driver library).
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+        cudaGetLastError();
+    });
+    return fn;
+}
+
+// Tensor map of the packed frame [positions][co_v] (fp32): boxes of 32
+// channels (128 bytes, 128-byte swizzle: the MMA's K-major operand layout)
+// by a_box_rows positions; rows past the frame read as zeros.
+dgrad_status_t encode_frame_map(dgrad_plan_s *pl) {
+    auto fn = tensor_map_encoder();
+    if (!fn) return DGRAD_ERR_CUDA;
+    const cuuint64_t dims[2] = {(cuuint64_t)pl->t.co_v, (cuuint64_t)pl->g.positions};
+    const cuuint64_t strides[1] = {(cuuint64_t)pl->t.co_v * 4};
+    const cuuint32_t box[2] = {32u, (cuuint32_t)pl->t.a_box_rows};
+    const cuuint32_t es[2] = {1u, 1u};
+    CUresult r = fn(&pl->mp.a_map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, pl->frame, dims, strides, box, es,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? DGRAD_OK : DGRAD_ERR_CUDA;
+}
+
 bool overlaps(const void *a, size_t abytes, const void *b, size_t bbytes) {
     uintptr_t a0 = (uintptr_t)a, a1 = a0 + abytes, b0 = (uintptr_t)b, b1 = b0 + bbytes;
     return a0 < b1 && b0 < a1;
@@ -123,11 +172,16 @@ dgrad_status_t check_device(const dgrad_plan_s *plan) {
     return dev == plan->device ? DGRAD_OK : DGRAD_ERR_WRONG_DEVICE;
 }
 
-dgrad_status_t launch_prepack_on(dgrad_plan_s *plan, const float *weight, cudaStream_t s) {
+// One pack launch: the weights (when `weight` is given) and, in tensor-copy
+// mode, the grad_out frame (when `grad_out` is given).
+dgrad_status_t launch_pack_on(dgrad_plan_s *plan, const float *weight, const float *grad_out, cudaStream_t s) {
     dgrad::PrepackParams pp = plan->pp;
     pp.w = weight;
-    if (dgrad::launch_prepack(pp, s) != cudaSuccess) return DGRAD_ERR_CUDA;
-    plan->packed = 1;
+    dgrad::FramePackParams fp = plan->fp;
+    fp.go = grad_out;
+    const bool frame = plan->frame != nullptr && grad_out != nullptr;
+    if (dgrad::launch_pack(weight ? &pp : nullptr, frame ? &fp : nullptr, s) != cudaSuccess) return DGRAD_ERR_CUDA;
+    if (weight) plan->packed = 1;
     return DGRAD_OK;
 }
 
@@ -216,8 +270,10 @@ dgrad_status_t dgrad_plan_ex(int N, int Ci, int H, int W, int Co, int kH, int kW
         delete pl;
         return st;
     }
-    // Workspace: the error word (256 B) then the packed weights.
-    size_t ws = 256 + pl->t.packed_bytes;
+    // Workspace: the error word (256 B), the packed weights, then (tensor-
+    // copy mode) the packed grad_out frame, each 256-byte aligned.
+    const size_t wp_bytes = (pl->t.packed_bytes + 255) & ~size_t(255);
+    size_t ws = 256 + wp_bytes + (pl->t.path == DGRAD_PATH_TCGEN05 && pl->t.a_tma ? pl->t.frame_bytes : 0);
     void *mem = nullptr;
     if (cudaMalloc(&mem, ws) != cudaSuccess) {
         cudaGetLastError();
@@ -231,8 +287,15 @@ dgrad_status_t dgrad_plan_ex(int N, int Ci, int H, int W, int Co, int kH, int kW
     }
     pl->err = static_cast<uint32_t *>(mem);
     pl->wp = reinterpret_cast<float *>(static_cast<uint8_t *>(mem) + 256);
+    if (pl->t.path == DGRAD_PATH_TCGEN05 && pl->t.a_tma)
+        pl->frame = reinterpret_cast<float *>(static_cast<uint8_t *>(mem) + 256 + wp_bytes);
     pl->workspace_bytes = ws;
     fill_params(pl);
+    if (pl->frame && (st = encode_frame_map(pl)) != DGRAD_OK) {
+        cudaFree(mem);
+        delete pl;
+        return st;
+    }
     *plan_out = pl;
     return DGRAD_OK;
 }
@@ -264,7 +327,7 @@ dgrad_status_t dgrad_run(dgrad_plan_t plan, const float *grad_out, const float *
         plan->packed = 1;
         return cudaMemsetAsync(grad_input, 0, gi_bytes, s) == cudaSuccess ? DGRAD_OK : DGRAD_ERR_CUDA;
     }
-    st = launch_prepack_on(plan, weight, s);
+    st = launch_pack_on(plan, weight, grad_out, s);
     if (st != DGRAD_OK) return st;
     return launch_main_on(plan, grad_out, grad_input, s);
 }
@@ -278,7 +341,7 @@ dgrad_status_t dgrad_prepack(dgrad_plan_t plan, const float *weight, void *strea
         plan->packed = 1;
         return DGRAD_OK;
     }
-    return launch_prepack_on(plan, weight, static_cast<cudaStream_t>(stream));
+    return launch_pack_on(plan, weight, nullptr, static_cast<cudaStream_t>(stream));
 }
 
 dgrad_status_t dgrad_run_packed(dgrad_plan_t plan, const float *grad_out, float *grad_input, void *stream) {
@@ -292,6 +355,10 @@ dgrad_status_t dgrad_run_packed(dgrad_plan_t plan, const float *grad_out, float 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (g.n_taps == 0)
         return cudaMemsetAsync(grad_input, 0, gi_bytes, s) == cudaSuccess ? DGRAD_OK : DGRAD_ERR_CUDA;
+    if (plan->frame) {
+        st = launch_pack_on(plan, nullptr, grad_out, s);
+        if (st != DGRAD_OK) return st;
+    }
     return launch_main_on(plan, grad_out, grad_input, s);
 }
 

@@ -5,6 +5,7 @@
 #include <cstddef>
 #include <cstdint>
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "dgrad.h"
@@ -85,6 +86,11 @@ struct Tiling {
     int tap_group;     // taps per B stage (tcgen05 path)
     int n_tgroups;     // B stages per channel chunk
     int chunk_bytes;   // bytes of one B stage (tap_group taps)
+    int a_tma;         // 1: A stages are tensor copies of the packed frame; 0: producer warps gather
+    int a_box_rows;    // rows of one A tensor copy (<= 256)
+    int a_nbox;        // tensor copies per A stage
+    int co_v;          // channels per packed frame row
+    size_t frame_bytes;
     int acc_bufs;      // tensor-memory accumulator sets
     int acc_cols;      // columns of one set
     int tmem_cols;
@@ -128,7 +134,23 @@ struct PrepackParams {
     int tap_kw[kMaxTaps];
 };
 
+// Packed frame: V[P][k] = grad_out[n][k][y - Ph][x - Pw] at flattened
+// position P = (n*Hv + y)*Wp + x (0 outside grad_out and for k >= Co),
+// TF32-rounded when the plan computes in TF32; co_v channels per row.
+struct FramePackParams {
+    const float *go;
+    float *v;
+    int N, Co, oH, oW, Hv, Wp, Ph, Pw;
+    int co_v;
+    int round_tf32;
+    int positions;     // N * Hv * Wp
+    int pos_tiles;     // ceil(positions / kFramePackCols)
+    int c_groups;      // ceil(co_v / 32)
+};
+constexpr int kFramePackCols = 128;
+
 struct MainParams {
+    CUtensorMap a_map;   // packed frame [positions][co_v], box 32 x a_box_rows, 128-byte swizzle
     const float *go;
     const float *wp;
     float *gi;
@@ -141,6 +163,7 @@ struct MainParams {
     int a_rows, a_stages, b_stages, b_resident, chunk_bytes;
     int tap_group, n_tgroups;
     int vec_producer;   // 1: 16-byte quad loads + register transpose; 0: 4-byte asynchronous copies
+    int a_tma, a_box_rows, a_nbox;
     int acc_bufs, acc_cols, tmem_cols;
     int round_tf32;
     int n_phases, n_taps;
@@ -150,7 +173,10 @@ struct MainParams {
     TapDesc tap[kMaxTaps];
 };
 
-cudaError_t launch_prepack(const PrepackParams &p, cudaStream_t stream);
+// Weight pre-pack and (optional, fp may be null) frame pack in one launch;
+// either part may be skipped (pp may be null).
+cudaError_t launch_pack(const PrepackParams *pp, const FramePackParams *fp, cudaStream_t stream);
+inline cudaError_t launch_prepack(const PrepackParams &p, cudaStream_t stream) { return launch_pack(&p, nullptr, stream); }
 cudaError_t launch_simt(const MainParams &p, const Tiling &t, cudaStream_t stream);
 cudaError_t launch_tc(const MainParams &p, const Tiling &t, cudaStream_t stream, bool pdl);
 

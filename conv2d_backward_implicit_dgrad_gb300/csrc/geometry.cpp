@@ -136,6 +136,7 @@ int pow2_at_least(int x) {
 constexpr int kBarrierBytes = 4096;   // mbarriers + TMEM slot (1 KB), tap table (2 KB), 1024-byte alignment slack
 constexpr int kMaxResidentChunks = 32;
 constexpr int kMaxTcRows = 1024;   // frame rows one tcgen05 A stage may hold (16 per producer thread)
+constexpr size_t kMaxFrameBytes = size_t(64) << 20;   // packed frames up to half the L2
 
 // Fill the sizes that follow from (tm, bn) for the tcgen05 path (kc = 32);
 // returns false when no pipeline depth fits in shared memory.  The packed
@@ -144,8 +145,16 @@ constexpr int kMaxTcRows = 1024;   // frame rows one tcgen05 A stage may hold (1
 bool size_tc(const Geometry &g, Tiling &t, int want_resident) {
     t.n_slices = ceil_div(g.Ci, t.bn);
     t.n_chunks = ceil_div(g.Co, t.kc);
-    t.a_rows = round_up(t.tm * kBlockM + g.max_shift, 8);
-    if (t.a_rows > kMaxTcRows) return false;
+    const int raw_rows = t.tm * kBlockM + g.max_shift;
+    if (t.a_tma) {   // tensor copies of at most 256 rows each
+        t.a_nbox = ceil_div(raw_rows, 256);
+        t.a_box_rows = round_up(ceil_div(raw_rows, t.a_nbox), 8);
+        t.a_rows = t.a_nbox * t.a_box_rows;
+    } else {
+        t.a_nbox = t.a_box_rows = 0;
+        t.a_rows = round_up(raw_rows, 8);
+        if (t.a_rows > kMaxTcRows) return false;
+    }
     const long long a_bytes = (long long)t.a_rows * t.kc * 4;
     const long long tap_bytes = (long long)t.bn * t.kc * 4;
     const long long budget = kMaxSmem - kBarrierBytes;
@@ -270,6 +279,20 @@ dgrad_status_t choose_tiling(const Geometry &g, int precision, const dgrad_optio
     }
     // Operand rows are one 128-byte swizzle row: 32 output channels per chunk.
     if (o.chunk_k && o.chunk_k != 32) return DGRAD_ERR_INVALID_ARG;
+    if (o.a_source < 0 || o.a_source > 2) return DGRAD_ERR_INVALID_ARG;
+    // grad_out reaches the MMA either as tensor copies of a packed,
+    // channels-last frame (kept when it is small enough to stay in L2
+    // between the pack kernel and the main kernel), or through producer warps.
+    t.co_v = std::max(32, round_up(g.Co, 4));
+    t.frame_bytes = (size_t)g.positions * t.co_v * 4;
+    if (o.a_source == 1)
+        t.a_tma = 1;
+    else if (o.a_source == 2)
+        t.a_tma = 0;
+    else
+        t.a_tma = t.frame_bytes <= kMaxFrameBytes ? 1 : 0;
+    if (t.a_tma && (long long)g.positions * t.co_v > INT_MAX) return DGRAD_ERR_UNSUPPORTED;
+    if (!t.a_tma) t.frame_bytes = 0;
     bool ok = false;
     for (int want_res = 1; want_res >= 0 && !ok; --want_res) {
         for (int i = 0; i < n_tm && !ok; ++i) {

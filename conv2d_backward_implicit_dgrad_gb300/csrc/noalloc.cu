@@ -70,8 +70,11 @@ extern "C" dgrad_status_t dgrad_run_noalloc(int N, int Ci, int H, int W, int Co,
         return DGRAD_ERR_NO_DEVICE;
     if (major != 10 || minor != 3) return DGRAD_ERR_NO_DEVICE;
 
+    // No frame buffer here: producer warps carry grad_out to the MMA.
+    dgrad_options_t opts{};
+    opts.a_source = 2;
     Tiling t;
-    st = choose_tiling(g, precision, nullptr, sms, &t);
+    st = choose_tiling(g, precision, &opts, sms, &t);
     if (st != DGRAD_OK) return st;
     if (t.packed_bytes + kErrWordBytes > kNoAllocScratchBytes) return DGRAD_ERR_UNSUPPORTED;
 

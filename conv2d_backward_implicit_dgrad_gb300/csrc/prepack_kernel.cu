@@ -1,9 +1,19 @@
-// Weight pre-pack: OIHW fp32 weights -> the K-major packed layout the main
-// kernels stream (see PrepackParams).  Replaces meganeura's per-element
-// implicit W^T reads (its A-tile load decomposes k into (co, kh, kw) with
-// divisions and reads weight with a strided index) by one pass that writes
-// each (slice, chunk) block contiguously, keeps only the taps each phase
-// uses, zero-pads channels, and (TF32 precision) rounds to TF32 once.
+// Pack kernel: one launch that (a) packs the weights and (b) optionally packs
+// grad_out into the channels-last, zero-padded frame the tcgen05 kernel
+// copies with the tensor engine.
+//
+// (a) OIHW fp32 weights -> the packed layout of PrepackParams.  Replaces
+//     meganeura's per-element implicit W^T reads (its A-tile load decomposes
+//     k into (co, kh, kw) with divisions and reads weight with a strided
+//     index) by one pass that writes each (slice, chunk) block contiguously,
+//     keeps only the taps each phase uses, zero-pads channels, and (TF32
+//     precision) rounds to TF32 once.
+// (b) grad_out NCHW -> V[P][k] (FramePackParams): one block transposes
+//     kFramePackCols consecutive frame positions x 32 channels through shared
+//     memory, so both the grad_out reads (along positions) and the V writes
+//     (128-byte rows of 32 channels) are coalesced.  Frame positions
+//     outside grad_out, and channels >= Co, are written as zeros; the
+//     meganeura shader's transposed padding becomes these zero rows.
 #include <cuda_runtime.h>
 
 #include "dgrad_internal.h"
@@ -14,14 +24,19 @@ namespace dgrad {
 namespace {
 
 constexpr int kThreads = 256;
+constexpr int kMaxPrepackBlocks = 1024;
 
-__global__ void __launch_bounds__(kThreads) prepack_kernel(const __grid_constant__ PrepackParams p) {
-    // Let the main kernel start its prologue while this grid runs; it reads
-    // the packed weights only after griddepcontrol.wait.
-    dev::grid_launch_dependents();
-    const long long stride = static_cast<long long>(gridDim.x) * kThreads;
+struct PackArgs {
+    PrepackParams w;        // valid when w_blocks > 0
+    FramePackParams f;      // valid when f_blocks > 0
+    int w_blocks;
+    int f_blocks;
+};
+
+__device__ void pack_weights(const PrepackParams &p, int block, int nblocks) {
+    const long long stride = static_cast<long long>(nblocks) * kThreads;
     const int G = p.kc / 4;
-    for (long long i = static_cast<long long>(blockIdx.x) * kThreads + threadIdx.x; i < p.total; i += stride) {
+    for (long long i = static_cast<long long>(block) * kThreads + threadIdx.x; i < p.total; i += stride) {
         long long rest = i;
         const int e = static_cast<int>(rest % 4);
         rest /= 4;
@@ -52,13 +67,75 @@ __global__ void __launch_bounds__(kThreads) prepack_kernel(const __grid_constant
     }
 }
 
+__device__ void pack_frame(const FramePackParams &p, int block, float (*tile)[kFramePackCols + 1], int *off) {
+    // block -> (tile of kFramePackCols consecutive frame positions, group of
+    // 32 channels); position tiles vary fastest so neighbouring blocks read
+    // neighbouring grad_out runs.
+    const int pt = block % p.pos_tiles;
+    const int co0 = (block / p.pos_tiles) * 32;
+    const int P0 = pt * kFramePackCols;
+    const int plane = p.oH * p.oW;
+    if (threadIdx.x < kFramePackCols) {   // grad_out offset of channel 0 at each position, or -1
+        const int P = P0 + threadIdx.x;
+        int o = -1;
+        if (P < p.positions) {
+            const int img = p.Hv * p.Wp;
+            const int n = P / img, rem = P - n * img;
+            const int y = rem / p.Wp, x = rem - y * p.Wp;
+            const int oh = y - p.Ph, ow = x - p.Pw;
+            if (oh >= 0 && oh < p.oH && ow >= 0 && ow < p.oW) o = n * p.Co * plane + oh * p.oW + ow;
+        }
+        off[threadIdx.x] = o;
+    }
+    __syncthreads();
+    // read: 32 channels x kFramePackCols positions, coalesced along positions
+    for (int i = threadIdx.x; i < 32 * kFramePackCols; i += kThreads) {
+        const int c = i / kFramePackCols, xi = i % kFramePackCols;
+        const int co = co0 + c;
+        const int o = off[xi];
+        float v = 0.f;
+        if (o >= 0 && co < p.Co) v = __ldg(p.go + static_cast<size_t>(o) + static_cast<size_t>(co) * plane);
+        tile[c][xi] = p.round_tf32 ? dev::round_tf32(v) : v;
+    }
+    __syncthreads();
+    // write: rows of 32 channels (128 bytes), coalesced along channels
+    const int ncols = min(kFramePackCols, p.positions - P0);
+    const int cmax = min(32, p.co_v - co0);
+    float *dst = p.v + static_cast<size_t>(P0) * p.co_v + co0;
+    for (int i = threadIdx.x; i < 32 * ncols; i += kThreads) {
+        const int xi = i / 32, c = i % 32;
+        if (c < cmax) dst[static_cast<size_t>(xi) * p.co_v + c] = tile[c][xi];
+    }
+}
+
+__global__ void __launch_bounds__(kThreads) pack_kernel(const __grid_constant__ PackArgs a) {
+    // Let the main kernel start its prologue while this grid runs; it reads
+    // what this grid writes only after griddepcontrol.wait.
+    dev::grid_launch_dependents();
+    __shared__ float tile[32][kFramePackCols + 1];
+    __shared__ int off[kFramePackCols];
+    if (static_cast<int>(blockIdx.x) < a.w_blocks)
+        pack_weights(a.w, blockIdx.x, a.w_blocks);
+    else
+        pack_frame(a.f, blockIdx.x - a.w_blocks, tile, off);
+}
+
 }  // namespace
 
-cudaError_t launch_prepack(const PrepackParams &p, cudaStream_t stream) {
-    long long blocks = (p.total + kThreads - 1) / kThreads;
-    if (blocks > 4096) blocks = 4096;
-    if (blocks < 1) blocks = 1;
-    prepack_kernel<<<static_cast<unsigned>(blocks), kThreads, 0, stream>>>(p);
+cudaError_t launch_pack(const PrepackParams *pp, const FramePackParams *fp, cudaStream_t stream) {
+    PackArgs a{};
+    if (pp) {
+        a.w = *pp;
+        long long blocks = (pp->total + kThreads - 1) / kThreads;
+        a.w_blocks = static_cast<int>(blocks < 1 ? 1 : (blocks > kMaxPrepackBlocks ? kMaxPrepackBlocks : blocks));
+    }
+    if (fp) {
+        a.f = *fp;
+        a.f_blocks = fp->pos_tiles * fp->c_groups;
+    }
+    const int blocks = a.w_blocks + a.f_blocks;
+    if (blocks == 0) return cudaSuccess;
+    pack_kernel<<<blocks, kThreads, 0, stream>>>(a);
     return cudaGetLastError();
 }
 

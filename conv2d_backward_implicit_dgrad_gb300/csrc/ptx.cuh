@@ -101,6 +101,21 @@ __device__ __forceinline__ void cp_async_wait_all() {
     asm volatile("cp.async.wait_all;" ::: "memory");
 }
 
+// 2-D tiled tensor copy global -> shared (TMA); completion counted in bytes
+// on `bar`.  tmap: generic address of a CUtensorMap (kernel parameter);
+// c0 innermost coordinate (its byte offset must be a multiple of 16), c1 row.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *tmap, int c0, int c1, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+            dst),
+        "l"(tmap), "r"(c0), "r"(c1), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void prefetch_tensormap(const void *tmap) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
+}
+
 // Prefetch a contiguous global range into L2 (TMA engine; nothing is
 // written anywhere).  addr 16-byte aligned, bytes a multiple of 16.
 __device__ __forceinline__ void bulk_prefetch_l2(const void *addr, uint32_t bytes) {

@@ -14,7 +14,9 @@
 //   warp  5     one thread streaming packed weights with bulk copies (TMA)
 //   warps 6-13  producers: a band of the frame -> shared memory (A operand),
 //               32 channels per stage, rows in the 128-byte swizzled K-major
-//               layout of the tensor core
+//               layout of the tensor core.  In tensor-copy mode (packed
+//               channels-last frame) these warps do not exist: the warp-5
+//               thread also copies each A stage with 2-D tensor copies.
 // Pipelines (all mbarriers, all waits bounded):
 //   A ring   a_stages  producers -> MMA        (A_full / A_empty)
 //   B ring   b_stages  weight loader -> MMA    (B_full / B_empty); when the
@@ -36,6 +38,7 @@ constexpr int kLoadWarp = 5;
 constexpr int kProdWarp0 = 6;
 constexpr int kProdWarps = 8;
 constexpr int kThreads = (kProdWarp0 + kProdWarps) * 32;
+constexpr int kThreadsTmaA = kProdWarp0 * 32;
 constexpr int kMaxAStages = 4;
 constexpr int kMaxBStages = 32;
 constexpr int kRowSlots = kProdWarps * 32 / 4;   // 4-byte producer: threads per channel lane
@@ -321,8 +324,9 @@ __device__ __forceinline__ void produce_async4(const MainParams &p, Barriers *ba
     dev::cp_async_wait_all();
 }
 
-template <int KC>
-__global__ void __launch_bounds__(kThreads, 1) tc_dgrad_kernel(const __grid_constant__ MainParams p) {
+template <int KC, bool kTmaA>
+__global__ void __launch_bounds__(kTmaA ? kThreadsTmaA : kThreads, 1)
+    tc_dgrad_kernel(const __grid_constant__ MainParams p) {
     static_assert(KC == 32, "operand rows are one 128-byte swizzle row of 32 TF32 values");
     extern __shared__ __align__(1024) uint8_t smem[];
     Barriers *bars = reinterpret_cast<Barriers *>(smem);
@@ -339,7 +343,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_dgrad_kernel(const __grid_cons
     const int lane = threadIdx.x % 32;
 
     if (threadIdx.x == 0) {
-        const uint32_t a_arrivals = p.vec_producer ? kGroupThreads : kProdWarps * 32;
+        const uint32_t a_arrivals = kTmaA ? 1 : (p.vec_producer ? kGroupThreads : kProdWarps * 32);
         for (int i = 0; i < p.a_stages; ++i) {
             dev::mbar_init(dev::smem_u32(&bars->a_full[i]), a_arrivals);
             dev::mbar_init(dev::smem_u32(&bars->a_empty[i]), 1);
@@ -375,7 +379,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_dgrad_kernel(const __grid_cons
     DGRAD_TRACE_CLOCK(t_start);
     const int tile_rows = p.tm * kBlockM;
 
-    if (warp >= kProdWarp0) {
+    if (!kTmaA && warp >= kProdWarp0) {
         // ------------------------------------------------------ producers
         if (p.vec_producer)
             produce_quads<KC>(p, bars, a_base, a_stage_floats, tile_rows, tmo);
@@ -388,10 +392,13 @@ __global__ void __launch_bounds__(kThreads, 1) tc_dgrad_kernel(const __grid_cons
         // B stage (c, tg) = taps [tg*tap_group, ...) of channel chunk c of the
         // work unit's slice: one contiguous block of the packed weights.
         if (lane == 0) {
-            dev::grid_dependency_wait();   // packed weights come from the preceding kernel
+            if (kTmaA) dev::prefetch_tensormap(&p.a_map);
+            dev::grid_dependency_wait();   // packed weights (and frame) come from the preceding kernel
             const size_t tap_bytes = static_cast<size_t>(p.bn) * 128;
             int last_parity[kMaxBStages];   // parity of each stage's last fill, -1 if never filled
             for (int i = 0; i < kMaxBStages; ++i) last_parity[i] = -1;
+            int a_last_parity[kMaxAStages];
+            for (int i = 0; i < kMaxAStages; ++i) a_last_parity[i] = -1;
             if (p.b_resident) {   // one slice, one group per chunk: load everything once
                 for (int c = 0; c < p.n_chunks; ++c) {
                     const uint32_t bar = dev::smem_u32(&bars->b_full[c]);
@@ -401,13 +408,32 @@ __global__ void __launch_bounds__(kThreads, 1) tc_dgrad_kernel(const __grid_cons
                                   p.chunk_bytes, bar);
                     last_parity[c] = 0;
                 }
-            } else {
-                Ring ring;
+            }
+            if (kTmaA || !p.b_resident) {
+                Ring ring, aring;
                 bool ok = true;
+                const uint32_t a_stage_bytes = static_cast<uint32_t>(a_stage_floats) * 4;
                 for (int w = blockIdx.x; ok && w < p.n_work && !bars->abort_flag; w += gridDim.x) {
                     const int slice = w % p.n_slices;
+                    const int P0 = (w / p.n_slices) * tile_rows;
                     for (int c = 0; ok && c < p.n_chunks; ++c) {
-                        for (int tg = 0; tg < p.n_tgroups; ++tg) {
+                        if (kTmaA) {
+                            // A stage: frame rows [P0, P0 + a_rows) x channels [32c, 32c + 32)
+                            if (!dev::mbar_wait(dev::smem_u32(&bars->a_empty[aring.stage]), aring.parity ^ 1, tmo)) {
+                                fail(bars, p);
+                                ok = false;
+                                break;
+                            }
+                            const uint32_t bar = dev::smem_u32(&bars->a_full[aring.stage]);
+                            dev::mbar_arrive_expect_tx(bar, a_stage_bytes);
+                            const uint32_t dst = dev::smem_u32(a_base) + aring.stage * a_stage_bytes;
+                            for (int b = 0; b < p.a_nbox; ++b)
+                                dev::tma_load_2d(dst + static_cast<uint32_t>(b * p.a_box_rows) * 128, &p.a_map, c * KC,
+                                                 P0 + b * p.a_box_rows, bar);
+                            a_last_parity[aring.stage] = static_cast<int>(aring.parity);
+                            aring.next(p.a_stages);
+                        }
+                        for (int tg = 0; !p.b_resident && tg < p.n_tgroups; ++tg) {
                             if (!dev::mbar_wait(dev::smem_u32(&bars->b_empty[ring.stage]), ring.parity ^ 1, tmo)) {
                                 fail(bars, p);
                                 ok = false;
@@ -431,6 +457,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_dgrad_kernel(const __grid_cons
             // Never leave with a copy in flight into this CTA's shared memory.
             for (int i = 0; i < p.b_stages && i < kMaxBStages; ++i)
                 if (last_parity[i] >= 0) dev::mbar_wait(dev::smem_u32(&bars->b_full[i]), last_parity[i], tmo);
+            for (int i = 0; i < p.a_stages && i < kMaxAStages; ++i)
+                if (a_last_parity[i] >= 0) dev::mbar_wait(dev::smem_u32(&bars->a_full[i]), a_last_parity[i], tmo);
         }
         __syncwarp();
     } else if (warp == kMmaWarp) {
@@ -477,7 +505,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_dgrad_kernel(const __grid_cons
                 // tensor core's operand reads here.  The quad producer fences
                 // its own stores instead, so this fence (which would also wait
                 // for this thread's MMAs in flight) is not taken on that path.
-                if (!p.vec_producer) dev::fence_proxy_async_smem();
+                if (!kTmaA && !p.vec_producer) dev::fence_proxy_async_smem();
                 const uint32_t a_stage = a_addr0 + static_cast<uint32_t>(ra.stage) * a_stage_floats * 4;
                 for (int tg = 0; tg < p.n_tgroups; ++tg) {
                     const int sb = p.b_resident ? c : rb.stage;
@@ -601,14 +629,14 @@ __global__ void __launch_bounds__(kThreads, 1) tc_dgrad_kernel(const __grid_cons
     if (warp == kMmaWarp) dev::tmem_dealloc(tmem_base, p.tmem_cols);
 }
 
-template <int KC>
+template <int KC, bool kTmaA>
 cudaError_t launch_kc(const MainParams &p, const Tiling &t, cudaStream_t stream, bool pdl) {
-    auto kern = tc_dgrad_kernel<KC>;
+    auto kern = tc_dgrad_kernel<KC, kTmaA>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, t.smem_bytes);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(t.grid);
-    cfg.blockDim = dim3(kThreads);
+    cfg.blockDim = dim3(kTmaA ? kThreadsTmaA : kThreads);
     cfg.dynamicSmemBytes = t.smem_bytes;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
@@ -633,7 +661,7 @@ extern "C" int dgrad_trace_read(unsigned long long *host, int n) {
 
 cudaError_t launch_tc(const MainParams &p, const Tiling &t, cudaStream_t stream, bool pdl) {
     if (t.kc != 32) return cudaErrorInvalidValue;
-    return launch_kc<32>(p, t, stream, pdl);
+    return p.a_tma ? launch_kc<32, true>(p, t, stream, pdl) : launch_kc<32, false>(p, t, stream, pdl);
 }
 
 }  // namespace dgrad

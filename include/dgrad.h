@@ -86,6 +86,8 @@ typedef struct {
     int chunk_k;       /* output channels per pipeline stage, multiple of 8 */
     int grid;          /* CTAs launched (persistent kernels) */
     int sm_count;      /* dgrad_describe only: SM count to plan for */
+    int a_source;      /* tcgen05 path, how grad_out reaches the MMA: 0 automatic, 1 packed frame + tensor
+                          copies (workspace holds a channels-last copy of grad_out), 2 producer warps */
 } dgrad_options_t;
 
 /* Everything a plan decided, for tests, benchmarks and logs. */
@@ -103,6 +105,7 @@ typedef struct {
     long long n_work;      /* work units of the main kernel */
     int grid;              /* CTAs of the main kernel */
     int b_resident;        /* 1: packed weights stay in shared memory for the whole launch */
+    int a_source;          /* 1: packed frame + tensor copies, 2: producer warps (tcgen05 path) */
     int smem_bytes;        /* dynamic shared memory of the main kernel */
     int tmem_cols;         /* tensor-memory columns allocated per CTA (tcgen05 path) */
     size_t workspace_bytes;/* device workspace owned by the plan */

@@ -116,10 +116,12 @@ TILINGS = [
 ]
 
 
+@pytest.mark.parametrize("a_source", ["frame", "producers"])
 @pytest.mark.parametrize("opts", TILINGS)
 @pytest.mark.parametrize("shape", [(2, 40, 36, 19, 23, 3, 3, 1, 1, 1), (2, 48, 20, 17, 18, 3, 3, 2, 1, 1),
-                                   (3, 33, 70, 9, 14, 1, 1, 1, 0, 0)])
-def test_tc_tilings(shape, opts):
+                                   (3, 33, 70, 9, 14, 1, 1, 1, 0, 0), (2, 24, 40, 16, 16, 3, 3, 1, 1, 1)])
+def test_tc_tilings(shape, opts, a_source):
+    opts = dict(opts, a_source=a_source)
     N, Ci, Co, H, W, kH, kW, s, ph, pw = shape
     try:
         dg.describe(N, Ci, H, W, Co, kH, kW, s, ph, pw, "tf32", path="tcgen05", **opts)
@@ -129,7 +131,7 @@ def test_tc_tilings(shape, opts):
         raise
     go, w = make_tensors((N, Co, out_ext(H, kH, s, ph), out_ext(W, kW, s, pw)), (Co, Ci, kH, kW), 73, "kaiming")
     info = check((N, Ci, H, W, Co, kH, kW, s, ph, pw), go, w, "tf32", path="tcgen05", **opts)
-    for k in ("tile_blocks", "slice_n", "chunk_k"):
+    for k in ("tile_blocks", "slice_n", "chunk_k", "a_source"):
         if k in opts:
             assert info[k] == opts[k]
 
@@ -148,6 +150,15 @@ def test_simt_with_tf32_operands():
     N, Ci, Co, H, W, kH, kW, s, ph, pw = shape
     go, w = make_tensors((N, Co, H, W), (Co, Ci, kH, kW), 83, "kaiming")
     check((N, Ci, H, W, Co, kH, kW, s, ph, pw), go, w, "tf32", path="simt")
+
+
+@pytest.mark.parametrize("a_source", ["frame", "producers"])
+@pytest.mark.parametrize("shape", EDGE[:10])
+def test_edge_shapes_both_sources(shape, a_source):
+    N, Ci, Co, H, W, kH, kW, s, ph, pw = shape
+    go, w = make_tensors((N, Co, out_ext(H, kH, s, ph), out_ext(W, kW, s, pw)), (Co, Ci, kH, kW), 72, "uniform")
+    info = check((N, Ci, H, W, Co, kH, kW, s, ph, pw), go, w, "tf32", a_source=a_source)
+    assert info["a_source"] == a_source
 
 
 # ----------------------------------------------------------------- semantics
