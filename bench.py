@@ -1,10 +1,13 @@
 #!/usr/bin/env python
 """Benchmark: dgrad useful TFLOP/s, % of the GB300 TF32 roofline, us per call.
 
-One step = one pass of the whole hot path on one batch: the weight pre-pack
-kernel plus the main implicit-GEMM kernel, through the C ABI
-(dgrad_prepack + dgrad_run_packed), inputs resident in HBM.  L2 is flushed
-(256 MiB write) before every timed step, outside the timed events.
+One step = one pass of the whole hot path on one batch through the C ABI
+(dgrad_run): the pack kernel (weights and, on the frame path, grad_out into
+the channels-last frame) and the main implicit-GEMM kernel, chained with
+programmatic dependent launch, inputs resident in HBM.  L2 is flushed
+(256 MiB write) before every timed step, outside the timed events.  The main
+kernel is also timed alone (dgrad_run_main after dgrad_prepack and
+dgrad_pack_grad_out) for the roofline line.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--precision tf32|fp32]
   python bench.py --impl reference ...   # the CPU oracle on the host cores
@@ -188,8 +191,7 @@ def time_workload(dg, torch, wl, precision, steps, warmup, rank, barrier, device
     stream = torch.cuda.current_stream()
 
     def step():
-        plan.prepack(w, stream)
-        plan.run_packed(go, gi, stream)
+        plan.run(go, w, gi, stream)   # pack kernel (weights + frame) -> main kernel
 
     for _ in range(max(3, warmup)):
         flush.zero_()
@@ -207,34 +209,36 @@ def time_workload(dg, torch, wl, precision, steps, warmup, rank, barrier, device
             step()
         torch.cuda.synchronize()
 
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(steps)]
     torch.cuda.synchronize()
     barrier()
     for i in range(steps):
         flush.zero_()
         ev[i][0].record(stream)
-        plan.prepack(w, stream)
+        step()
         ev[i][1].record(stream)
-        plan.run_packed(go, gi, stream)
-        ev[i][2].record(stream)
     torch.cuda.synchronize()
     barrier()
     clock_info = sampler.stop() if sampler else None
     plan.check()
-    step_ms = statistics.mean(e[0].elapsed_time(e[2]) for e in ev)
-    main_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
-    prepack_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
+    step_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
 
-    # The fused public call (pre-pack and main kernel chained with
-    # programmatic dependent launch), same flushing, for comparison.
-    fe = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(steps)]
+    # The stages apart, same flushing: the pack kernels (weights, frame) and
+    # then the main kernel alone, each bracketed by events on this stream.
+    se = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
     for i in range(steps):
         flush.zero_()
-        fe[i][0].record(stream)
-        plan.run(go, w, gi, stream)
-        fe[i][1].record(stream)
+        se[i][0].record(stream)
+        plan.prepack(w, stream)
+        plan.pack_grad_out(go, stream)
+        se[i][1].record(stream)
+        plan.run_main(go, gi, stream)
+        se[i][2].record(stream)
     torch.cuda.synchronize()
-    fused_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in fe)
+    plan.check()
+    prepack_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in se)
+    main_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in se)
+    fused_ms = step_ms
 
     e2e_s = None
     if e2e:
@@ -301,10 +305,9 @@ def build_line(args, wl, r, world):
         "dtype": args.precision, "data": "synthetic",
         "config": {**wl_config(wl), "precision": args.precision, "parallelism": f"replicas x{world}",
                    "l2": "flushed (256 MiB write) before every timed step",
-                   "step": "weight pre-pack kernel + main kernel (C ABI dgrad_prepack + dgrad_run_packed)"},
+                   "step": "pack kernel (weights + grad_out frame) + main kernel (C ABI dgrad_run)"},
         "roofline": roofline(wl, args.precision, flops, nbytes, main_s, step_s),
-        "main_kernel_us": r["main_ms"] * 1e3, "prepack_us": r["prepack_ms"] * 1e3,
-        "fused_run_us": r["fused_ms"] * 1e3,
+        "main_kernel_us": r["main_ms"] * 1e3, "pack_stages_us": r["prepack_ms"] * 1e3,
         "gpu_launches": 2 * r["steps"],
         "plan": {k: r["plan"][k] for k in ("path", "tile_blocks", "slice_n", "chunk_k", "n_chunks", "grid",
                                            "n_work", "b_resident", "smem_bytes", "tmem_cols")},
@@ -318,7 +321,7 @@ def build_line(args, wl, r, world):
 
 
 def profile_steps(dg, torch, wl, args):
-    """W warm-up steps then K steps, each after an L2 flush; nothing else."""
+    """W warm-up steps then K steps (dgrad_run), each after an L2 flush; nothing else."""
     from conv2d_backward_implicit_dgrad_gb300.workloads import make_inputs
     go_h, w_h = make_inputs(wl, 0)
     go, w = go_h.cuda(), w_h.cuda()
@@ -327,8 +330,7 @@ def profile_steps(dg, torch, wl, args):
     with dg.Plan(*wl.plan_args(), precision=args.precision) as plan:
         for _ in range(args.warmup + args.steps):
             flush.zero_()
-            plan.prepack(w)
-            plan.run_packed(go, gi)
+            plan.run(go, w, gi)
         torch.cuda.synchronize()
         plan.check()
         print(json.dumps({"profile": wl.name, "precision": args.precision, "steps": args.steps,
@@ -397,7 +399,7 @@ def main():
                     rf = roofline(WORKLOADS[name], prec, x["flops"], x["bytes"], x["main_ms"] * 1e-3,
                                   x["ms_per_step"] * 1e-3)
                     print(json.dumps({"info": "workload", "workload": name, "precision": prec,
-                                      **{k: x[k] for k in ("ms_per_step", "main_ms", "prepack_ms", "fused_ms")},
+                                      **{k: x[k] for k in ("ms_per_step", "main_ms", "prepack_ms")},
                                       "tflops": x["flops"] / (x["ms_per_step"] * 1e-3) / 1e12,
                                       "main_tflops": rf["achieved"], "frac_peak": rf["frac"],
                                       "frac_of_roofline_kernel": rf["frac_of_roofline_kernel"],

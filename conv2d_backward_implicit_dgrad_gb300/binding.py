@@ -28,7 +28,7 @@ PATH_NAME = {v: k for k, v in PATH.items()}
 
 # Every function declared in include/dgrad.h (checked by the CPU tests).
 EXPORTS = ("dgrad_plan", "dgrad_plan_ex", "dgrad_describe", "dgrad_describe_taps", "dgrad_plan_info", "dgrad_run",
-           "dgrad_prepack", "dgrad_run_packed", "dgrad_run_host", "dgrad_run_noalloc", "dgrad_plan_check",
+           "dgrad_prepack", "dgrad_run_packed", "dgrad_pack_grad_out", "dgrad_run_main", "dgrad_run_host", "dgrad_run_noalloc", "dgrad_plan_check",
            "dgrad_plan_destroy", "dgrad_status_string")
 
 
@@ -94,6 +94,8 @@ def load_library(path: str | None = None):
         lib.dgrad_run.argtypes = [vp, p, p, p, vp]
         lib.dgrad_prepack.argtypes = [vp, p, vp]
         lib.dgrad_run_packed.argtypes = [vp, p, p, vp]
+        lib.dgrad_pack_grad_out.argtypes = [vp, p, vp]
+        lib.dgrad_run_main.argtypes = [vp, p, p, vp]
         lib.dgrad_run_host.argtypes = [vp, p, p, p, vp]
         lib.dgrad_plan_check.argtypes = [vp]
         lib.dgrad_plan_destroy.argtypes = [vp]
@@ -101,7 +103,8 @@ def load_library(path: str | None = None):
         lib.dgrad_status_string.argtypes = [i]
         lib.dgrad_status_string.restype = ctypes.c_char_p
         for f in ("dgrad_plan", "dgrad_plan_ex", "dgrad_describe", "dgrad_describe_taps", "dgrad_plan_info",
-                  "dgrad_run", "dgrad_prepack", "dgrad_run_packed", "dgrad_run_host", "dgrad_plan_check"):
+                  "dgrad_run", "dgrad_prepack", "dgrad_run_packed", "dgrad_pack_grad_out", "dgrad_run_main",
+                  "dgrad_run_host", "dgrad_plan_check"):
             getattr(lib, f).restype = i
         _LIB = lib
         return lib
@@ -236,6 +239,26 @@ class Plan:
                                         ctypes.c_void_p(grad_input.data_ptr()), _stream_handle(stream))
         if st != 0:
             raise DgradError(st, "dgrad_run_packed")
+        return grad_input
+
+    def pack_grad_out(self, grad_out, stream=None):
+        """Pack grad_out into the plan's frame (frame path; no-op otherwise)."""
+        self._check_tensor(grad_out, self.go_shape, "grad_out", "cuda")
+        st = self._lib.dgrad_pack_grad_out(self._h, ctypes.c_void_p(grad_out.data_ptr()), _stream_handle(stream))
+        if st != 0:
+            raise DgradError(st, "dgrad_pack_grad_out")
+
+    def run_main(self, grad_out, grad_input=None, stream=None):
+        """The main kernel alone, on the weights and frame packed last."""
+        import torch
+        self._check_tensor(grad_out, self.go_shape, "grad_out", "cuda")
+        if grad_input is None:
+            grad_input = torch.empty(self.gi_shape, dtype=torch.float32, device=grad_out.device)
+        self._check_tensor(grad_input, self.gi_shape, "grad_input", "cuda")
+        st = self._lib.dgrad_run_main(self._h, ctypes.c_void_p(grad_out.data_ptr()),
+                                      ctypes.c_void_p(grad_input.data_ptr()), _stream_handle(stream))
+        if st != 0:
+            raise DgradError(st, "dgrad_run_main")
         return grad_input
 
     def run_host(self, grad_out, weight, grad_input=None, stream=None):

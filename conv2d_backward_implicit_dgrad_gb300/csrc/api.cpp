@@ -28,6 +28,7 @@ struct dgrad_plan_s {
     float *stage_gi;
     size_t workspace_bytes;
     int packed;            // dgrad_prepack (or dgrad_run) has run at least once
+    int frame_packed;      // grad_out has been packed into the frame at least once
 };
 
 namespace {
@@ -182,6 +183,7 @@ dgrad_status_t launch_pack_on(dgrad_plan_s *plan, const float *weight, const flo
     const bool frame = plan->frame != nullptr && grad_out != nullptr;
     if (dgrad::launch_pack(weight ? &pp : nullptr, frame ? &fp : nullptr, s) != cudaSuccess) return DGRAD_ERR_CUDA;
     if (weight) plan->packed = 1;
+    if (frame) plan->frame_packed = 1;
     return DGRAD_OK;
 }
 
@@ -346,6 +348,24 @@ dgrad_status_t dgrad_prepack(dgrad_plan_t plan, const float *weight, void *strea
 
 dgrad_status_t dgrad_run_packed(dgrad_plan_t plan, const float *grad_out, float *grad_input, void *stream) {
     if (!plan || !plan->packed) return DGRAD_ERR_INVALID_ARG;
+    dgrad_status_t st = dgrad_pack_grad_out(plan, grad_out, stream);
+    if (st != DGRAD_OK) return st;
+    return dgrad_run_main(plan, grad_out, grad_input, stream);
+}
+
+dgrad_status_t dgrad_pack_grad_out(dgrad_plan_t plan, const float *grad_out, void *stream) {
+    if (!plan) return DGRAD_ERR_INVALID_ARG;
+    if (!aligned16(grad_out)) return DGRAD_ERR_MISALIGNED;
+    dgrad_status_t st = check_device(plan);
+    if (st != DGRAD_OK) return st;
+    if (!plan->frame || plan->g.n_taps == 0) return DGRAD_OK;
+    st = launch_pack_on(plan, nullptr, grad_out, static_cast<cudaStream_t>(stream));
+    if (st == DGRAD_OK) plan->frame_packed = 1;
+    return st;
+}
+
+dgrad_status_t dgrad_run_main(dgrad_plan_t plan, const float *grad_out, float *grad_input, void *stream) {
+    if (!plan || !plan->packed) return DGRAD_ERR_INVALID_ARG;
     if (!aligned16(grad_out) || !aligned16(grad_input)) return DGRAD_ERR_MISALIGNED;
     const Geometry &g = plan->g;
     const size_t gi_bytes = gi_elems(g) * 4;
@@ -355,10 +375,7 @@ dgrad_status_t dgrad_run_packed(dgrad_plan_t plan, const float *grad_out, float 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (g.n_taps == 0)
         return cudaMemsetAsync(grad_input, 0, gi_bytes, s) == cudaSuccess ? DGRAD_OK : DGRAD_ERR_CUDA;
-    if (plan->frame) {
-        st = launch_pack_on(plan, nullptr, grad_out, s);
-        if (st != DGRAD_OK) return st;
-    }
+    if (plan->frame && !plan->frame_packed) return DGRAD_ERR_INVALID_ARG;
     return launch_main_on(plan, grad_out, grad_input, s);
 }
 

@@ -24,6 +24,7 @@ namespace dgrad {
 namespace {
 
 constexpr int kThreads = 256;
+static_assert(kThreads % kFramePackCols == 0 && 32 % (kThreads / kFramePackCols) == 0, "frame tile split");
 constexpr int kMaxPrepackBlocks = 1024;
 
 struct PackArgs {
@@ -88,14 +89,23 @@ __device__ void pack_frame(const FramePackParams &p, int block, float (*tile)[kF
         off[threadIdx.x] = o;
     }
     __syncthreads();
-    // read: 32 channels x kFramePackCols positions, coalesced along positions
-    for (int i = threadIdx.x; i < 32 * kFramePackCols; i += kThreads) {
-        const int c = i / kFramePackCols, xi = i % kFramePackCols;
-        const int co = co0 + c;
+    // read: 32 channels x kFramePackCols positions, coalesced along positions.
+    // Each thread keeps one position and issues all of its channel loads
+    // before the first shared-memory store, so they are in flight together.
+    {
+        constexpr int kRowsPerPass = kThreads / kFramePackCols;
+        constexpr int kLoads = 32 / kRowsPerPass;
+        const int xi = threadIdx.x % kFramePackCols;
+        const int c0 = threadIdx.x / kFramePackCols;
         const int o = off[xi];
-        float v = 0.f;
-        if (o >= 0 && co < p.Co) v = __ldg(p.go + static_cast<size_t>(o) + static_cast<size_t>(co) * plane);
-        tile[c][xi] = p.round_tf32 ? dev::round_tf32(v) : v;
+        float v[kLoads];
+#pragma unroll
+        for (int k = 0; k < kLoads; ++k) {
+            const int co = co0 + c0 + kRowsPerPass * k;
+            v[k] = (o >= 0 && co < p.Co) ? __ldg(p.go + static_cast<size_t>(o) + static_cast<size_t>(co) * plane) : 0.f;
+        }
+#pragma unroll
+        for (int k = 0; k < kLoads; ++k) tile[c0 + kRowsPerPass * k][xi] = p.round_tf32 ? dev::round_tf32(v[k]) : v[k];
     }
     __syncthreads();
     // write: rows of 32 channels (128 bytes), coalesced along channels

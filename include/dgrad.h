@@ -153,22 +153,37 @@ dgrad_status_t dgrad_plan_info(dgrad_plan_t plan, dgrad_plan_info_t *info);
 
 /* Compute grad_input from grad_out and weight, asynchronously on `stream`.
  * All three are DEVICE pointers on the plan's device, 16-byte aligned, shaped
- * as above.  Launches the weight pre-pack kernel and then the main kernel,
- * both on `stream`.  One plan must not run on two streams at once (they would
- * share the packed-weight workspace).  Returns after the launches; errors
- * detected inside the kernels surface through dgrad_plan_check. */
+ * as above.  Launches two kernels on `stream`: the pack kernel (weights, and
+ * on the frame path grad_out into the plan's channels-last frame) and then
+ * the main kernel.  One plan must not run on two streams at once (they would
+ * share the workspace).  Returns after the launches; errors detected inside
+ * the kernels surface through dgrad_plan_check. */
 dgrad_status_t dgrad_run(dgrad_plan_t plan, const float *grad_out, const float *weight,
                          float *grad_input, void *stream);
 
-/* The two halves of dgrad_run, for callers whose weights stay fixed over
- * several calls: dgrad_prepack packs `weight` into the plan's workspace (the
- * weight pre-pack kernel), dgrad_run_packed runs the main kernel on the
- * weights packed last.  Same pointer rules, stream order and errors as
- * dgrad_run; dgrad_run_packed before any dgrad_prepack on the plan returns
- * DGRAD_ERR_INVALID_ARG. */
+/* The stages of dgrad_run, for callers whose weights stay fixed over
+ * several calls, or who time the stages apart:
+ *   dgrad_prepack        packs `weight` into the plan's workspace;
+ *   dgrad_run_packed     packs grad_out (frame path only) and runs the main
+ *                        kernel on the weights packed last;
+ *   dgrad_pack_grad_out  packs grad_out into the plan's frame (frame path;
+ *                        returns DGRAD_OK and launches nothing otherwise);
+ *   dgrad_run_main       the main kernel alone, on the weights packed last
+ *                        and, on the frame path, the frame packed last.
+ *                        grad_out must be the tensor whose frame was packed
+ *                        last (the other paths read it directly).
+ * dgrad_run_packed = dgrad_pack_grad_out + dgrad_run_main.  Same pointer
+ * rules, stream order and errors as dgrad_run.  dgrad_run_packed or
+ * dgrad_run_main before any dgrad_prepack/dgrad_run, or dgrad_run_main on
+ * the frame path before any grad_out was packed, returns
+ * DGRAD_ERR_INVALID_ARG.  dgrad_plan_info's a_source tells whether the plan
+ * uses a frame (1) or not. */
 dgrad_status_t dgrad_prepack(dgrad_plan_t plan, const float *weight, void *stream);
 dgrad_status_t dgrad_run_packed(dgrad_plan_t plan, const float *grad_out, float *grad_input,
                                 void *stream);
+dgrad_status_t dgrad_pack_grad_out(dgrad_plan_t plan, const float *grad_out, void *stream);
+dgrad_status_t dgrad_run_main(dgrad_plan_t plan, const float *grad_out, float *grad_input,
+                              void *stream);
 
 /* The same computation from HOST buffers: copies grad_out and weight to
  * device staging buffers owned by the plan (allocated on the first call),

@@ -209,6 +209,45 @@ def test_prepack_then_run_packed_matches_run():
         assert torch.equal(a, b) and torch.equal(b, c)
 
 
+@pytest.mark.parametrize("name", ["tiny", "strided_downsample"])
+def test_staged_calls_match_run(name):
+    """prepack + pack_grad_out + run_main, with the stages in separate calls
+    and the main kernel run twice on one packing, equals run."""
+    wl = WORKLOADS[name]
+    go, w = make_tensors((2, wl.Co, wl.oH, wl.oW), wl.w_shape, 41, wl.dist)
+    args = (2,) + wl.plan_args()[1:]
+    with dg.Plan(*args, precision="tf32") as plan:
+        gd, wd = go.cuda(), w.cuda()
+        a = plan.run(gd, wd)
+        other = torch.randn_like(gd)
+        plan.run(other, wd)                  # leaves another tensor's frame behind
+        plan.prepack(wd)
+        plan.pack_grad_out(gd)
+        b = plan.run_main(gd)
+        c = plan.run_main(gd)
+        torch.cuda.synchronize()
+        plan.check()
+        assert torch.equal(a, b) and torch.equal(b, c)
+
+
+def test_run_main_before_packing_is_rejected():
+    wl = WORKLOADS["tiny"]
+    with dg.Plan(*wl.plan_args(), precision="tf32") as plan:
+        gd = torch.zeros(wl.go_shape, device="cuda")
+        with pytest.raises(dg.DgradError) as e:
+            plan.run_main(gd)
+        assert e.value.status == 1
+        plan.prepack(torch.zeros(wl.w_shape, device="cuda"))
+        if plan.info["a_source"] == "frame":  # frame path: the frame was never packed
+            with pytest.raises(dg.DgradError) as e:
+                plan.run_main(gd)
+            assert e.value.status == 1
+        plan.pack_grad_out(gd)
+        plan.run_main(gd)
+        torch.cuda.synchronize()
+        plan.check()
+
+
 def test_run_host_matches_device():
     wl = WORKLOADS["tiny"]
     go, w = make_inputs(wl, 7)
