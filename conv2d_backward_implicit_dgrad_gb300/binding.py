@@ -29,13 +29,13 @@ PATH_NAME = {v: k for k, v in PATH.items()}
 # Every function declared in include/dgrad.h (checked by the CPU tests).
 EXPORTS = ("dgrad_plan", "dgrad_plan_ex", "dgrad_describe", "dgrad_describe_taps", "dgrad_plan_info", "dgrad_run",
            "dgrad_prepack", "dgrad_run_packed", "dgrad_pack_grad_out", "dgrad_run_main", "dgrad_run_host", "dgrad_run_noalloc", "dgrad_plan_check",
-           "dgrad_plan_destroy", "dgrad_status_string")
+           "dgrad_plan_destroy", "dgrad_status_string", "dgrad_cuda_error_string")
 
 
 class Options(ctypes.Structure):
     _fields_ = [("path", ctypes.c_int), ("tile_blocks", ctypes.c_int), ("slice_n", ctypes.c_int),
                 ("chunk_k", ctypes.c_int), ("grid", ctypes.c_int), ("sm_count", ctypes.c_int),
-                ("a_source", ctypes.c_int)]
+                ("a_source", ctypes.c_int), ("group_taps", ctypes.c_int)]
 
 
 class PlanInfo(ctypes.Structure):
@@ -47,7 +47,8 @@ class PlanInfo(ctypes.Structure):
         ("chunk_k", ctypes.c_int), ("n_chunks", ctypes.c_int), ("n_work", ctypes.c_longlong),
         ("grid", ctypes.c_int), ("b_resident", ctypes.c_int), ("a_source", ctypes.c_int),
         ("smem_bytes", ctypes.c_int),
-        ("tmem_cols", ctypes.c_int), ("workspace_bytes", ctypes.c_size_t),
+        ("tmem_cols", ctypes.c_int), ("group_taps", ctypes.c_int), ("tile_step", ctypes.c_int),
+        ("workspace_bytes", ctypes.c_size_t),
         ("packed_weight_bytes", ctypes.c_size_t), ("useful_flops", ctypes.c_double),
         ("algorithmic_bytes", ctypes.c_double)]
 
@@ -66,6 +67,8 @@ class DgradError(RuntimeError):
         msg = f"{where}: {name}" if where else name
         if _LIB is not None:
             msg += f" ({_LIB.dgrad_status_string(status).decode()})"
+            if status == 6:
+                msg += f": {_LIB.dgrad_cuda_error_string().decode()}"
         super().__init__(msg)
 
 
@@ -102,6 +105,8 @@ def load_library(path: str | None = None):
         lib.dgrad_plan_destroy.restype = None
         lib.dgrad_status_string.argtypes = [i]
         lib.dgrad_status_string.restype = ctypes.c_char_p
+        lib.dgrad_cuda_error_string.argtypes = []
+        lib.dgrad_cuda_error_string.restype = ctypes.c_char_p
         for f in ("dgrad_plan", "dgrad_plan_ex", "dgrad_describe", "dgrad_describe_taps", "dgrad_plan_info",
                   "dgrad_run", "dgrad_prepack", "dgrad_run_packed", "dgrad_pack_grad_out", "dgrad_run_main",
                   "dgrad_run_host", "dgrad_plan_check"):
@@ -114,9 +119,14 @@ A_SOURCE = {"auto": 0, "frame": 1, "producers": 2}
 A_SOURCE_NAME = {v: k for k, v in A_SOURCE.items()}
 
 
-def _options(path="auto", tile_blocks=0, slice_n=0, chunk_k=0, grid=0, sm_count=0, a_source="auto"):
+GROUP_TAPS = {"auto": 0, "on": 1, "off": 2}
+
+
+def _options(path="auto", tile_blocks=0, slice_n=0, chunk_k=0, grid=0, sm_count=0, a_source="auto",
+             group_taps="auto"):
     return Options(PATH[path] if isinstance(path, str) else int(path), tile_blocks, slice_n, chunk_k, grid,
-                   sm_count, A_SOURCE[a_source] if isinstance(a_source, str) else int(a_source))
+                   sm_count, A_SOURCE[a_source] if isinstance(a_source, str) else int(a_source),
+                   GROUP_TAPS[group_taps] if isinstance(group_taps, str) else int(group_taps))
 
 
 def describe(N, Ci, H, W, Co, kH, kW, stride, pad_h, pad_w, precision="tf32", **opts) -> dict:
@@ -135,14 +145,14 @@ def describe_taps(N, Ci, H, W, Co, kH, kW, stride, pad_h, pad_w):
     """Host-only phase and tap tables: (phases, taps) as lists of dicts."""
     lib = load_library()
     cap = 256
-    ph = (ctypes.c_int * (6 * cap))()
+    ph = (ctypes.c_int * (7 * cap))()
     tp = (ctypes.c_int * (3 * cap))()
     nph, ntp = ctypes.c_int(), ctypes.c_int()
     st = lib.dgrad_describe_taps(N, Ci, H, W, Co, kH, kW, stride, pad_h, pad_w, cap, ph, ctypes.byref(nph), tp,
                                  ctypes.byref(ntp))
     if st != 0:
         raise DgradError(st, "dgrad_describe_taps")
-    phases = [dict(zip(("a", "b", "Hq", "Wq", "tap_begin", "tap_count"), ph[6 * i:6 * i + 6]))
+    phases = [dict(zip(("a", "b", "Hq", "Wq", "tap_begin", "tap_count", "row_len"), ph[7 * i:7 * i + 7]))
               for i in range(nph.value)]
     taps = [dict(zip(("kh", "kw", "shift"), tp[3 * i:3 * i + 3])) for i in range(ntp.value)]
     return phases, taps

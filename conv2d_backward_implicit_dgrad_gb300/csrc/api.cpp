@@ -38,6 +38,16 @@ using dgrad::Tiling;
 
 constexpr long long kTimeoutNs = 1000000000LL;   // bounded in-kernel waits: 1 s
 
+// The CUDA error behind the last DGRAD_ERR_CUDA of this thread.
+thread_local cudaError_t g_last_cuda = cudaSuccess;
+
+dgrad_status_t cuda_status(cudaError_t e) {
+    if (e == cudaSuccess) return DGRAD_OK;
+    g_last_cuda = e;
+    cudaGetLastError();   // clear the (non-sticky) error
+    return DGRAD_ERR_CUDA;
+}
+
 size_t go_elems(const Geometry &g) { return (size_t)g.N * g.Co * g.oH * g.oW; }
 size_t w_elems(const Geometry &g) { return (size_t)g.Co * g.Ci * g.kH * g.kW; }
 size_t gi_elems(const Geometry &g) { return (size_t)g.N * g.Ci * g.H * g.W; }
@@ -62,6 +72,8 @@ void fill_info(const Geometry &g, const Tiling &t, int precision, size_t ws, dgr
     info->a_source = t.path == DGRAD_PATH_TCGEN05 ? (t.a_tma ? 1 : 2) : 0;
     info->smem_bytes = t.smem_bytes;
     info->tmem_cols = t.tmem_cols;
+    info->group_taps = t.grouped;
+    info->tile_step = t.tile_step;
     info->workspace_bytes = ws;
     info->packed_weight_bytes = t.packed_bytes;
     info->useful_flops = 2.0 * g.N * g.Co * g.oH * g.oW * (double)g.Ci * g.kH * g.kW;
@@ -80,51 +92,23 @@ dgrad_status_t plan_host(int N, int Ci, int H, int W, int Co, int kH, int kW, in
 void fill_params(dgrad_plan_s *pl) {
     const Geometry &g = pl->g;
     const Tiling &t = pl->t;
-    dgrad::MainParams &m = pl->mp;
-    std::memset(&m, 0, sizeof(m));
-    m.wp = pl->wp;
-    m.err = pl->err;
-    m.N = g.N; m.Ci = g.Ci; m.Co = g.Co; m.H = g.H; m.W = g.W; m.oH = g.oH; m.oW = g.oW; m.s = g.s;
-    m.Ph = g.Ph; m.Pw = g.Pw; m.Hv = g.Hv; m.Wp = g.Wp; m.HvWp = g.Hv * g.Wp;
-    m.positions = (int)g.positions;
-    m.tm = t.tm; m.bn = t.bn; m.n_slices = t.n_slices; m.kc = t.kc; m.n_chunks = t.n_chunks;
-    m.n_tiles = t.n_tiles; m.n_work = (int)t.n_work;
-    m.a_rows = t.a_rows; m.a_stages = t.a_stages; m.b_stages = t.b_stages; m.b_resident = t.b_resident;
-    m.chunk_bytes = t.chunk_bytes;
-    m.tap_group = t.tap_group; m.n_tgroups = t.n_tgroups;
-    m.vec_producer = dgrad::use_vec_producer(g, t) ? 1 : 0;
-    m.a_tma = t.a_tma; m.a_box_rows = t.a_box_rows; m.a_nbox = t.a_nbox;
+    const int round = pl->precision == DGRAD_PREC_TF32 ? 1 : 0;
+    dgrad::fill_main_params(g, t, round, &pl->mp);
+    pl->mp.wp = pl->wp;
+    pl->mp.err = pl->err;
+    pl->mp.timeout_ns = kTimeoutNs;
+    dgrad::fill_prepack_params(g, t, round, &pl->pp);
+    pl->pp.wp = pl->wp;
 
     dgrad::FramePackParams &f = pl->fp;
     std::memset(&f, 0, sizeof(f));
     f.v = pl->frame;
     f.N = g.N; f.Co = g.Co; f.oH = g.oH; f.oW = g.oW; f.Hv = g.Hv; f.Wp = g.Wp; f.Ph = g.Ph; f.Pw = g.Pw;
     f.co_v = t.co_v;
-    f.round_tf32 = pl->precision == DGRAD_PREC_TF32 ? 1 : 0;
+    f.round_tf32 = round;
     f.positions = (int)g.positions;
     f.pos_tiles = (int)((g.positions + dgrad::kFramePackCols - 1) / dgrad::kFramePackCols);
     f.c_groups = (t.co_v + 31) / 32;
-    m.acc_bufs = t.acc_bufs; m.acc_cols = t.acc_cols; m.tmem_cols = t.tmem_cols;
-    m.round_tf32 = pl->precision == DGRAD_PREC_TF32 ? 1 : 0;
-    m.n_phases = g.n_phases;
-    m.n_taps = g.n_taps;
-    m.idesc = dgrad::tf32_idesc(dgrad::kBlockM, t.bn);
-    m.timeout_ns = kTimeoutNs;
-    for (int i = 0; i < g.n_phases; ++i) m.phase[i] = g.phase[i];
-    for (int i = 0; i < g.n_taps; ++i) m.tap[i] = g.tap[i];
-
-    dgrad::PrepackParams &q = pl->pp;
-    std::memset(&q, 0, sizeof(q));
-    q.wp = pl->wp;
-    q.Co = g.Co; q.Ci = g.Ci; q.kH = g.kH; q.kW = g.kW;
-    q.n_taps = g.n_taps; q.bn = t.bn; q.n_slices = t.n_slices; q.kc = t.kc; q.n_chunks = t.n_chunks;
-    q.round_tf32 = m.round_tf32;
-    q.layout = t.path == DGRAD_PATH_TCGEN05 ? 1 : 0;
-    q.total = (long long)(t.packed_bytes / 4);
-    for (int i = 0; i < g.n_taps; ++i) {
-        q.tap_kh[i] = g.tap[i].kh;
-        q.tap_kw[i] = g.tap[i].kw;
-    }
 }
 
 // cuTensorMapEncodeTiled from the driver, looked up once through the
@@ -181,7 +165,8 @@ dgrad_status_t launch_pack_on(dgrad_plan_s *plan, const float *weight, const flo
     dgrad::FramePackParams fp = plan->fp;
     fp.go = grad_out;
     const bool frame = plan->frame != nullptr && grad_out != nullptr;
-    if (dgrad::launch_pack(weight ? &pp : nullptr, frame ? &fp : nullptr, s) != cudaSuccess) return DGRAD_ERR_CUDA;
+    dgrad_status_t st = cuda_status(dgrad::launch_pack(weight ? &pp : nullptr, frame ? &fp : nullptr, s));
+    if (st != DGRAD_OK) return st;
     if (weight) plan->packed = 1;
     if (frame) plan->frame_packed = 1;
     return DGRAD_OK;
@@ -193,12 +178,16 @@ dgrad_status_t launch_main_on(dgrad_plan_s *plan, const float *grad_out, float *
     mp.gi = grad_input;
     cudaError_t e = plan->t.path == DGRAD_PATH_TCGEN05 ? dgrad::launch_tc(mp, plan->t, s, true)
                                                        : dgrad::launch_simt(mp, plan->t, s);
-    return e == cudaSuccess ? DGRAD_OK : DGRAD_ERR_CUDA;
+    return cuda_status(e);
 }
 
 }  // namespace
 
 extern "C" {
+
+const char *dgrad_cuda_error_string(void) {
+    return g_last_cuda == cudaSuccess ? "" : cudaGetErrorString(g_last_cuda);
+}
 
 const char *dgrad_status_string(dgrad_status_t s) {
     switch (s) {
@@ -239,8 +228,9 @@ dgrad_status_t dgrad_describe_taps(int N, int Ci, int H, int W, int Co, int kH, 
     *n_taps = g.n_taps;
     for (int i = 0; i < g.n_phases && i < cap; ++i) {
         const dgrad::PhaseDesc &p = g.phase[i];
-        int *o = phases + 6 * i;
+        int *o = phases + 7 * i;
         o[0] = p.a; o[1] = p.b; o[2] = p.Hq; o[3] = p.Wq; o[4] = p.tap_begin; o[5] = p.tap_count;
+        o[6] = p.row_len;
     }
     for (int i = 0; i < g.n_taps && i < cap; ++i) {
         taps[3 * i] = g.tap[i].kh;
@@ -327,7 +317,7 @@ dgrad_status_t dgrad_run(dgrad_plan_t plan, const float *grad_out, const float *
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (g.n_taps == 0) {   // no term reaches any input element
         plan->packed = 1;
-        return cudaMemsetAsync(grad_input, 0, gi_bytes, s) == cudaSuccess ? DGRAD_OK : DGRAD_ERR_CUDA;
+        return cuda_status(cudaMemsetAsync(grad_input, 0, gi_bytes, s));
     }
     st = launch_pack_on(plan, weight, grad_out, s);
     if (st != DGRAD_OK) return st;
@@ -374,7 +364,7 @@ dgrad_status_t dgrad_run_main(dgrad_plan_t plan, const float *grad_out, float *g
     if (st != DGRAD_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (g.n_taps == 0)
-        return cudaMemsetAsync(grad_input, 0, gi_bytes, s) == cudaSuccess ? DGRAD_OK : DGRAD_ERR_CUDA;
+        return cuda_status(cudaMemsetAsync(grad_input, 0, gi_bytes, s));
     if (plan->frame && !plan->frame_packed) return DGRAD_ERR_INVALID_ARG;
     return launch_main_on(plan, grad_out, grad_input, s);
 }
@@ -406,7 +396,7 @@ dgrad_status_t dgrad_run_host(dgrad_plan_t plan, const float *grad_out_host, con
     if (st != DGRAD_OK) return st;
     if (cudaMemcpyAsync(grad_input_host, plan->stage_gi, gi_b, cudaMemcpyDeviceToHost, s) != cudaSuccess)
         return DGRAD_ERR_CUDA;
-    return cudaStreamSynchronize(s) == cudaSuccess ? DGRAD_OK : DGRAD_ERR_CUDA;
+    return cuda_status(cudaStreamSynchronize(s));
 }
 
 dgrad_status_t dgrad_plan_check(dgrad_plan_t plan) {

@@ -18,6 +18,7 @@ constexpr int kMaxStride = 4;
 constexpr int kBlockM = 128;          // GEMM rows (output positions) per MMA block
 constexpr int kMaxSmem = 232448;      // opt-in dynamic shared memory per CTA on sm_103
 constexpr int kTmemCols = 512;        // tensor-memory columns per SM
+constexpr int kMaxSub = 4;            // taps of one kernel row grouped into one MMA (sub-accumulators)
 
 // Instruction descriptor of tcgen05.mma .kind::tf32 (PTX ISA, "instruction
 // descriptor" table for .kind::f16 / .kind::tf32): fp32 accumulator, TF32 A
@@ -39,13 +40,19 @@ struct TapDesc {
     int kh, kw;   // position inside the kernel
     int shift;    // dr * Wp + dc, >= 0
     int phase;    // index of the phase the tap feeds
+    int dr, dc;   // row and column offset in the frame
 };
 
 // One sub-pixel phase (a, b): input rows ih = s*q + a, columns iw = s*u + b.
+// Its taps are listed row by row of the kernel (dr descending), row_len taps
+// per row with dc descending by one from tap to tap.
 struct PhaseDesc {
     int a, b;
     int Hq, Wq;             // output rows/cols of the phase: ceil((H-a)/s), ceil((W-b)/s)
     int tap_begin, tap_count;
+    int row_len;            // taps per kernel row of the phase
+    int sub;                // main kernel: sub-accumulators (row_len when taps are grouped, else 1)
+    int col;                // main kernel: tensor-memory column of the phase's accumulator
 };
 
 // Phase split of the strided dgrad plus the flattened, zero-padded grad_out
@@ -69,6 +76,17 @@ struct Geometry {
 dgrad_status_t make_geometry(int N, int Ci, int H, int W, int Co, int kH, int kW,
                              int stride, int pad_h, int pad_w, Geometry *g);
 
+// One tcgen05 MMA group: `ntaps` consecutive taps of one kernel row of one
+// phase, issued as one MMA of N = ntaps * bn whose A window starts at the
+// row's smallest shift.  Sub-accumulator j (columns j*bn ..) then holds the
+// tap with shift a_shift + (ntaps - 1 - j), i.e. the output position that
+// many rows further down; the epilogue shifts it back.  Ungrouped, every tap
+// is its own group.
+struct MGroup {
+    int phase, tap0, ntaps, a_shift, first;
+};
+int build_mgroups(const Geometry &g, int grouped, MGroup *out);
+
 // Tiling of the main kernel.
 struct Tiling {
     int path;          // dgrad_path_t (SIMT or TCGEN05)
@@ -83,9 +101,14 @@ struct Tiling {
     int a_rows;        // rows of one A stage
     int a_stages, b_stages;
     int b_resident;
-    int tap_group;     // taps per B stage (tcgen05 path)
+    int tap_group;     // largest number of taps in one B stage (tcgen05 path)
     int n_tgroups;     // B stages per channel chunk
     int chunk_bytes;   // bytes of one B stage (tap_group taps)
+    int grouped;       // 1: taps of a kernel row share one MMA (MGroup)
+    int tile_step;     // output positions per tile (tm*128, less the rows a grouped MMA cannot finish)
+    int n_mgroups;
+    int bg_first[kMaxTaps + 1];   // B stage i holds MMA groups [bg_first[i], bg_first[i+1])
+    int xchg_bytes;    // shared memory for the epilogue's cross-warp row exchange
     int a_tma;         // 1: A stages are tensor copies of the packed frame; 0: producer warps gather
     int a_box_rows;    // rows of one A tensor copy (<= 256)
     int a_nbox;        // tensor copies per A stage
@@ -149,6 +172,9 @@ struct FramePackParams {
 };
 constexpr int kFramePackCols = 128;
 
+// Main-kernel MMA group entry: A window offset (bytes), accumulator column
+// (bit 31: first group of its phase), B offset inside the chunk's tap block
+// (bytes), instruction descriptor (N = ntaps * bn).
 struct MainParams {
     CUtensorMap a_map;   // packed frame [positions][co_v], box 32 x a_box_rows, 128-byte swizzle
     const float *go;
@@ -169,9 +195,22 @@ struct MainParams {
     int n_phases, n_taps;
     uint32_t idesc;
     long long timeout_ns;
+    int tile_step;      // output positions per tile
+    int grouped;
+    int max_sub;        // largest sub-accumulator count of a phase
+    int vec_w;          // epilogue stores the s column phases of a row phase together (s = 2 or 4)
+    int n_mgroups;
+    int xchg_bytes;
     PhaseDesc phase[kMaxPhases];
     TapDesc tap[kMaxTaps];
+    uint4 mgroup[kMaxTaps];
+    int bg_first[kMaxTaps + 1];
+    int bg_tap0[kMaxTaps + 1];   // first tap of each B stage (and n_taps at the end)
 };
+
+// Kernel parameter blocks from a plan (host).  Pointers are left null.
+void fill_main_params(const Geometry &g, const Tiling &t, int round_tf32, MainParams *m);
+void fill_prepack_params(const Geometry &g, const Tiling &t, int round_tf32, PrepackParams *q);
 
 // Weight pre-pack and (optional, fp may be null) frame pack in one launch;
 // either part may be skipped (pp may be null).

@@ -90,6 +90,9 @@ dgrad_status_t make_geometry(int N, int Ci, int H, int W, int Co, int kH, int kW
             p.a = a; p.b = b; p.Hq = R.nq; p.Wq = C.nq;
             p.tap_begin = g->n_taps;
             p.tap_count = R.count * C.count;
+            p.row_len = C.count;
+            p.sub = 1;
+            p.col = 0;
             nq_max = std::max(nq_max, R.nq);
             nu_max = std::max(nu_max, C.nq);
             for (int x = 0; x < R.count; ++x)
@@ -104,6 +107,8 @@ dgrad_status_t make_geometry(int N, int Ci, int H, int W, int Co, int kH, int kW
                     max_dc = std::max(max_dc, dc);
                     tap_dr[g->n_taps - 1] = dr;
                     tap_dc[g->n_taps - 1] = dc;
+                    t.dr = dr;
+                    t.dc = dc;
                     t.shift = 0;   // set below once Wp is known
                 }
         }
@@ -125,6 +130,23 @@ dgrad_status_t make_geometry(int N, int Ci, int H, int W, int Co, int kH, int kW
     return DGRAD_OK;
 }
 
+int build_mgroups(const Geometry &g, int grouped, MGroup *out) {
+    int n = 0;
+    for (int ph = 0; ph < g.n_phases; ++ph) {
+        const PhaseDesc &pd = g.phase[ph];
+        const int step = grouped ? pd.row_len : 1;
+        for (int t = pd.tap_begin; t < pd.tap_begin + pd.tap_count; t += step) {
+            MGroup &m = out[n++];
+            m.phase = ph;
+            m.tap0 = t;
+            m.ntaps = step;
+            m.a_shift = g.tap[t + step - 1].shift;   // the row's last tap has the smallest column offset
+            m.first = t == pd.tap_begin ? 1 : 0;
+        }
+    }
+    return n;
+}
+
 namespace {
 
 int pow2_at_least(int x) {
@@ -133,18 +155,62 @@ int pow2_at_least(int x) {
     return p;
 }
 
-constexpr int kBarrierBytes = 4096;   // mbarriers + TMEM slot (1 KB), tap table (2 KB), 1024-byte alignment slack
+constexpr int kBarrierBytes = 4096;   // mbarriers + TMEM slot (1 KB), MMA group table (2 KB), 1024-byte alignment slack
 constexpr int kMaxResidentChunks = 32;
 constexpr int kMaxTcRows = 1024;   // frame rows one tcgen05 A stage may hold (16 per producer thread)
 constexpr size_t kMaxFrameBytes = size_t(64) << 20;   // packed frames up to half the L2
+constexpr int kEpiGroups = 2;         // epilogue warp groups (tensor-copy mode)
 
-// Fill the sizes that follow from (tm, bn) for the tcgen05 path (kc = 32);
-// returns false when no pipeline depth fits in shared memory.  The packed
-// weights of one channel chunk are streamed in groups of tap_group taps;
-// when all of them fit next to two A stages they stay resident instead.
+// Split the MMA groups of one channel chunk into B stages of at most `cap`
+// taps each, balanced; false when one MMA group alone exceeds `cap`.
+bool split_b_stages(const MGroup *mg, int n_mg, int total_taps, int cap, Tiling &t) {
+    if (cap < 1) return false;
+    for (int i = 0; i < n_mg; ++i)
+        if (mg[i].ntaps > cap) return false;
+    int stages = (total_taps + cap - 1) / cap;
+    for (;; ++stages) {
+        const int target = (total_taps + stages - 1) / stages;
+        int n = 0, taps = 0, largest = 0;
+        t.bg_first[0] = 0;
+        for (int i = 0; i < n_mg; ++i) {
+            if (taps > 0 && taps + mg[i].ntaps > target) {
+                largest = std::max(largest, taps);
+                t.bg_first[++n] = i;
+                taps = 0;
+            }
+            taps += mg[i].ntaps;
+        }
+        largest = std::max(largest, taps);
+        t.bg_first[++n] = n_mg;
+        if (largest <= cap) {
+            t.n_tgroups = n;
+            t.tap_group = largest;
+            return true;
+        }
+        if (stages > n_mg) return false;
+    }
+}
+
+// Fill the sizes that follow from (tm, bn, grouped) for the tcgen05 path
+// (kc = 32); returns false when no pipeline depth fits in shared memory or
+// the accumulators do not fit in tensor memory.  The packed weights of one
+// channel chunk are streamed in B stages of whole MMA groups; when all of
+// them fit next to two A stages they stay resident instead.
 bool size_tc(const Geometry &g, Tiling &t, int want_resident) {
     t.n_slices = ceil_div(g.Ci, t.bn);
     t.n_chunks = ceil_div(g.Co, t.kc);
+    MGroup mg[kMaxTaps];
+    t.n_mgroups = build_mgroups(g, t.grouped, mg);
+    int max_sub = 1, sub_cols = 0;
+    for (int p = 0; p < g.n_phases; ++p) {
+        const int sub = t.grouped ? g.phase[p].row_len : 1;
+        if (sub * t.bn > 256) return false;   // MMA N limit
+        max_sub = std::max(max_sub, sub);
+        sub_cols += sub * t.bn;
+    }
+    if (t.grouped && (t.tm != 1 || max_sub > kMaxSub)) return false;
+    t.tile_step = t.tm * kBlockM - (max_sub - 1);
+    t.xchg_bytes = max_sub > 1 ? kEpiGroups * 2 * 4 * (max_sub * (max_sub - 1) / 2) * 16 * 4 : 0;
     const int raw_rows = t.tm * kBlockM + g.max_shift;
     if (t.a_tma) {   // tensor copies of at most 256 rows each
         t.a_nbox = ceil_div(raw_rows, 256);
@@ -157,7 +223,7 @@ bool size_tc(const Geometry &g, Tiling &t, int want_resident) {
     }
     const long long a_bytes = (long long)t.a_rows * t.kc * 4;
     const long long tap_bytes = (long long)t.bn * t.kc * 4;
-    const long long budget = kMaxSmem - kBarrierBytes;
+    const long long budget = kMaxSmem - kBarrierBytes - t.xchg_bytes;
     const int taps = std::max(1, g.n_taps);
     t.b_resident = 0;
     if (want_resident && t.n_slices == 1 && t.n_chunks <= kMaxResidentChunks) {
@@ -166,6 +232,8 @@ bool size_tc(const Geometry &g, Tiling &t, int want_resident) {
             t.b_resident = 1;
             t.tap_group = taps;
             t.n_tgroups = 1;
+            t.bg_first[0] = 0;
+            t.bg_first[1] = t.n_mgroups;
             t.b_stages = t.n_chunks;
             t.chunk_bytes = (int)(taps * tap_bytes);
             t.a_stages = (int)std::min<long long>(4, (budget - b_all) / a_bytes);
@@ -173,32 +241,26 @@ bool size_tc(const Geometry &g, Tiling &t, int want_resident) {
     }
     if (want_resident && !t.b_resident) return false;
     if (!t.b_resident) {
-        // Largest tap group with two B stages and at least two A stages
-        // (three when they fit without shrinking the group below half).
-        long long tg = (budget - 2 * a_bytes) / (2 * tap_bytes);
-        if (tg < 1) return false;
-        tg = std::min<long long>(tg, taps);
-        long long tg3 = (budget - 3 * a_bytes) / (2 * tap_bytes);
-        t.a_stages = 2;
-        if (tg3 >= std::min<long long>(taps, std::max<long long>(1, (tg + 1) / 2))) {
-            tg = std::min<long long>(tg3, taps);
-            t.a_stages = 3;
-        }
-        t.tap_group = (int)tg;
-        t.n_tgroups = ceil_div(taps, t.tap_group);
-        t.tap_group = ceil_div(taps, t.n_tgroups);   // balance the groups
+        // Largest B stage with two B stages and at least two A stages
+        // (three when they fit without shrinking the stage below half).
+        long long cap = (budget - 2 * a_bytes) / (2 * tap_bytes);
+        if (cap < 1) return false;
+        cap = std::min<long long>(cap, taps);
+        long long cap3 = (budget - 3 * a_bytes) / (2 * tap_bytes);
+        if (cap3 >= std::min<long long>(taps, std::max<long long>(1, (cap + 1) / 2))) cap = std::min<long long>(cap3, taps);
+        if (!split_b_stages(mg, t.n_mgroups, g.n_taps, (int)cap, t)) return false;
         t.chunk_bytes = (int)(t.tap_group * tap_bytes);
         t.b_stages = 2;
         long long left = budget - (long long)t.b_stages * t.chunk_bytes;
         t.a_stages = (int)std::min<long long>(4, left / a_bytes);
     }
     if (t.a_stages < 2) return false;
-    t.smem_bytes = (int)(kBarrierBytes + t.a_stages * a_bytes + (long long)t.b_stages * t.chunk_bytes);
-    t.acc_cols = t.tm * g.n_phases * t.bn;
+    t.smem_bytes = (int)(kBarrierBytes + t.xchg_bytes + t.a_stages * a_bytes + (long long)t.b_stages * t.chunk_bytes);
+    t.acc_cols = t.tm * sub_cols;
     if (t.acc_cols > kTmemCols) return false;
     t.acc_bufs = (2 * t.acc_cols <= kTmemCols) ? 2 : 1;
     t.tmem_cols = pow2_at_least(t.acc_bufs * t.acc_cols);
-    t.n_tiles = (int)((g.positions + (long long)t.tm * kBlockM - 1) / ((long long)t.tm * kBlockM));
+    t.n_tiles = (int)((g.positions + t.tile_step - 1) / t.tile_step);
     t.n_work = (long long)t.n_tiles * t.n_slices;
     t.packed_bytes = (size_t)t.n_slices * t.n_chunks * (size_t)taps * (size_t)tap_bytes;
     return true;
@@ -220,6 +282,7 @@ bool size_simt(const Geometry &g, Tiling &t) {
     t.smem_bytes = a_bytes + b_bytes;
     if (t.smem_bytes > kMaxSmem) return false;
     t.acc_bufs = t.acc_cols = t.tmem_cols = 0;
+    t.tile_step = kBlockM;
     t.n_tiles = (int)((g.positions + kBlockM - 1) / kBlockM);
     t.n_work = (long long)t.n_tiles * t.n_slices * g.n_phases;
     t.grid = 0;
@@ -293,14 +356,37 @@ dgrad_status_t choose_tiling(const Geometry &g, int precision, const dgrad_optio
         t.a_tma = t.frame_bytes <= kMaxFrameBytes ? 1 : 0;
     if (t.a_tma && (long long)g.positions * t.co_v > INT_MAX) return DGRAD_ERR_UNSUPPORTED;
     if (!t.a_tma) t.frame_bytes = 0;
+    // Grouping the taps of a kernel row into one MMA (N = taps x bn) cuts the
+    // shared-memory reads of A per FLOP when bn alone leaves the MMA bound by
+    // its operand reads (bn < 128).  It needs the sub-accumulators to fit in
+    // tensor memory twice (double buffering) unless each CTA gets a single
+    // work unit anyway.
+    if (o.group_taps < 0 || o.group_taps > 2) return DGRAD_ERR_INVALID_ARG;
+    int max_row = 1;
+    for (int p = 0; p < g.n_phases; ++p) max_row = std::max(max_row, g.phase[p].row_len);
+    int group_pref[2] = {0, 0};
+    int n_group = 0;
+    if (o.group_taps == 1) {
+        if (o.tile_blocks > 1) return DGRAD_ERR_UNSUPPORTED;   // grouped MMAs take one 128-row block per unit
+        group_pref[n_group++] = 1;
+    } else {
+        if (o.tile_blocks > 1) max_row = 1;
+        if (o.group_taps == 0 && max_row > 1 && bn < 128) group_pref[n_group++] = 1;
+        group_pref[n_group++] = 0;
+    }
     bool ok = false;
-    for (int want_res = 1; want_res >= 0 && !ok; --want_res) {
-        for (int i = 0; i < n_tm && !ok; ++i) {
-            Tiling c = t;
-            c.tm = tm_pref[i];
-            c.bn = bn;
-            c.kc = 32;
-            if (size_tc(g, c, want_res)) {
+    for (int gi = 0; gi < n_group && !ok; ++gi) {
+        for (int want_res = 1; want_res >= 0 && !ok; --want_res) {
+            for (int i = 0; i < n_tm && !ok; ++i) {
+                Tiling c = t;
+                c.grouped = group_pref[gi];
+                c.tm = c.grouped ? 1 : tm_pref[i];
+                c.bn = bn;
+                c.kc = 32;
+                if (!size_tc(g, c, want_res)) continue;
+                if (c.grouped && o.group_taps == 0 && c.acc_bufs < 2 &&
+                    c.n_work > std::min<long long>(o.grid ? o.grid : sm_count, c.n_work))
+                    continue;   // a single accumulator set would serialise MMA and epilogue
                 t = c;
                 ok = true;
             }
@@ -311,6 +397,74 @@ dgrad_status_t choose_tiling(const Geometry &g, int precision, const dgrad_optio
     t.grid = (int)std::max<long long>(1, std::min<long long>(grid, t.n_work));
     *out = t;
     return DGRAD_OK;
+}
+
+void fill_main_params(const Geometry &g, const Tiling &t, int round_tf32, MainParams *mp) {
+    MainParams &m = *mp;
+    std::memset(&m, 0, sizeof(m));
+    m.N = g.N; m.Ci = g.Ci; m.Co = g.Co; m.H = g.H; m.W = g.W; m.oH = g.oH; m.oW = g.oW; m.s = g.s;
+    m.Ph = g.Ph; m.Pw = g.Pw; m.Hv = g.Hv; m.Wp = g.Wp; m.HvWp = g.Hv * g.Wp;
+    m.positions = (int)g.positions;
+    m.tm = t.tm; m.bn = t.bn; m.n_slices = t.n_slices; m.kc = t.kc; m.n_chunks = t.n_chunks;
+    m.n_tiles = t.n_tiles; m.n_work = (int)t.n_work;
+    m.a_rows = t.a_rows; m.a_stages = t.a_stages; m.b_stages = t.b_stages; m.b_resident = t.b_resident;
+    m.chunk_bytes = t.chunk_bytes;
+    m.tap_group = t.tap_group; m.n_tgroups = t.n_tgroups;
+    m.vec_producer = use_vec_producer(g, t) ? 1 : 0;
+    m.a_tma = t.a_tma; m.a_box_rows = t.a_box_rows; m.a_nbox = t.a_nbox;
+    m.acc_bufs = t.acc_bufs; m.acc_cols = t.acc_cols; m.tmem_cols = t.tmem_cols;
+    m.round_tf32 = round_tf32;
+    m.n_phases = g.n_phases;
+    m.n_taps = g.n_taps;
+    m.idesc = tf32_idesc(kBlockM, t.bn);
+    m.tile_step = t.tile_step;
+    m.grouped = t.grouped;
+    m.xchg_bytes = t.xchg_bytes;
+    int col = 0;
+    m.max_sub = 1;
+    for (int i = 0; i < g.n_phases; ++i) {
+        m.phase[i] = g.phase[i];
+        m.phase[i].sub = t.grouped ? g.phase[i].row_len : 1;
+        m.phase[i].col = col;
+        col += m.phase[i].sub * t.bn;
+        m.max_sub = std::max(m.max_sub, m.phase[i].sub);
+    }
+    // The epilogue stores the s column phases of a row phase together when
+    // each row is whole (W % s == 0, every phase present) and the tensor-
+    // memory loads of one batch of them fit in 64 registers.
+    m.vec_w = (t.path == DGRAD_PATH_TCGEN05 && (g.s == 2 || g.s == 4) && g.W % g.s == 0 &&
+               g.n_phases == g.s * g.s && g.s * m.max_sub <= 4) ? 1 : 0;
+    for (int i = 0; i < g.n_taps; ++i) m.tap[i] = g.tap[i];
+    if (t.path == DGRAD_PATH_TCGEN05) {
+        MGroup mg[kMaxTaps];
+        m.n_mgroups = build_mgroups(g, t.grouped, mg);
+        const uint32_t tap_b = (uint32_t)t.bn * 128u;   // bytes of one tap of one chunk of B
+        for (int i = 0; i < m.n_mgroups; ++i) {
+            const PhaseDesc &pd = m.phase[mg[i].phase];
+            m.mgroup[i].x = (uint32_t)mg[i].a_shift * 128u;
+            m.mgroup[i].y = (uint32_t)pd.col | (mg[i].first ? 0x80000000u : 0u);
+            m.mgroup[i].z = (uint32_t)mg[i].tap0 * tap_b;
+            m.mgroup[i].w = tf32_idesc(kBlockM, mg[i].ntaps * t.bn);
+        }
+        for (int i = 0; i <= t.n_tgroups; ++i) {
+            m.bg_first[i] = t.bg_first[i];
+            m.bg_tap0[i] = t.bg_first[i] < m.n_mgroups ? mg[t.bg_first[i]].tap0 : g.n_taps;
+        }
+    }
+}
+
+void fill_prepack_params(const Geometry &g, const Tiling &t, int round_tf32, PrepackParams *qp) {
+    PrepackParams &q = *qp;
+    std::memset(&q, 0, sizeof(q));
+    q.Co = g.Co; q.Ci = g.Ci; q.kH = g.kH; q.kW = g.kW;
+    q.n_taps = g.n_taps; q.bn = t.bn; q.n_slices = t.n_slices; q.kc = t.kc; q.n_chunks = t.n_chunks;
+    q.round_tf32 = round_tf32;
+    q.layout = t.path == DGRAD_PATH_TCGEN05 ? 1 : 0;
+    q.total = (long long)(t.packed_bytes / 4);
+    for (int i = 0; i < g.n_taps; ++i) {
+        q.tap_kh[i] = g.tap[i].kh;
+        q.tap_kw[i] = g.tap[i].kw;
+    }
 }
 
 }  // namespace dgrad

@@ -10,7 +10,6 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
-#include <cstring>
 #include <mutex>
 
 #include "dgrad.h"
@@ -96,39 +95,16 @@ extern "C" dgrad_status_t dgrad_run_noalloc(int N, int Ci, int H, int W, int Co,
     if (cudaMemsetAsync(err, 0, sizeof(uint32_t), s) != cudaSuccess) return DGRAD_ERR_CUDA;
     if (g.n_taps == 0) return cudaMemsetAsync(grad_input, 0, gi_b, s) == cudaSuccess ? DGRAD_OK : DGRAD_ERR_CUDA;
 
+    const int round = precision == DGRAD_PREC_TF32 ? 1 : 0;
     PrepackParams q;
-    std::memset(&q, 0, sizeof(q));
+    fill_prepack_params(g, t, round, &q);
     q.w = weight;
     q.wp = wp;
-    q.Co = Co; q.Ci = Ci; q.kH = kH; q.kW = kW;
-    q.n_taps = g.n_taps; q.bn = t.bn; q.n_slices = t.n_slices; q.kc = t.kc; q.n_chunks = t.n_chunks;
-    q.round_tf32 = precision == DGRAD_PREC_TF32 ? 1 : 0;
-    q.layout = t.path == DGRAD_PATH_TCGEN05 ? 1 : 0;
-    q.total = (long long)(t.packed_bytes / 4);
-    for (int i = 0; i < g.n_taps; ++i) {
-        q.tap_kh[i] = g.tap[i].kh;
-        q.tap_kw[i] = g.tap[i].kw;
-    }
 
     MainParams m;
-    std::memset(&m, 0, sizeof(m));
+    fill_main_params(g, t, round, &m);
     m.go = grad_out; m.wp = wp; m.gi = grad_input; m.err = err;
-    m.N = N; m.Ci = Ci; m.Co = Co; m.H = H; m.W = W; m.oH = g.oH; m.oW = g.oW; m.s = stride;
-    m.Ph = g.Ph; m.Pw = g.Pw; m.Hv = g.Hv; m.Wp = g.Wp; m.HvWp = g.Hv * g.Wp;
-    m.positions = (int)g.positions;
-    m.tm = t.tm; m.bn = t.bn; m.n_slices = t.n_slices; m.kc = t.kc; m.n_chunks = t.n_chunks;
-    m.n_tiles = t.n_tiles; m.n_work = (int)t.n_work;
-    m.a_rows = t.a_rows; m.a_stages = t.a_stages; m.b_stages = t.b_stages; m.b_resident = t.b_resident;
-    m.chunk_bytes = t.chunk_bytes;
-    m.tap_group = t.tap_group; m.n_tgroups = t.n_tgroups;
-    m.vec_producer = dgrad::use_vec_producer(g, t) ? 1 : 0;
-    m.acc_bufs = t.acc_bufs; m.acc_cols = t.acc_cols; m.tmem_cols = t.tmem_cols;
-    m.round_tf32 = q.round_tf32;
-    m.n_phases = g.n_phases; m.n_taps = g.n_taps;
-    m.idesc = tf32_idesc(kBlockM, t.bn);
     m.timeout_ns = 1000000000LL;
-    for (int i = 0; i < g.n_phases; ++i) m.phase[i] = g.phase[i];
-    for (int i = 0; i < g.n_taps; ++i) m.tap[i] = g.tap[i];
 
     if (launch_prepack(q, s) != cudaSuccess) return DGRAD_ERR_CUDA;
     cudaError_t e = t.path == DGRAD_PATH_TCGEN05 ? launch_tc(m, t, s, true) : launch_simt(m, t, s);

@@ -6,19 +6,24 @@
 //   D[P, ci] = sum over (tap t, co) of V[P + shift_t][co] * Wp[t][co][ci]
 // for every sub-pixel phase (each with its own accumulator), where V is the
 // zero-padded, flattened grad_out frame and Wp the pre-packed weights.
+// Grouped plans issue the taps of one kernel row as one MMA with N = taps x
+// slice: the A window is shared, each tap lands in its own sub-accumulator
+// one output row further down per column step, and the epilogue adds the
+// sub-accumulators back with the matching row shifts.
 //
-// Roles (448 threads):
-//   warps 0-3   epilogue: tensor memory -> registers -> grad_input (NCHW)
+// Roles (448 threads with producer warps, 320 in tensor-copy mode):
+//   warps 0-3   epilogue group 0: tensor memory -> registers -> grad_input
 //   warp  4     tensor-memory allocation; the MMA loop (whole warp, one
 //               elected lane issues)
-//   warp  5     one thread streaming packed weights with bulk copies (TMA)
-//   warps 6-13  producers: a band of the frame -> shared memory (A operand),
-//               32 channels per stage, rows in the 128-byte swizzled K-major
-//               layout of the tensor core.  In tensor-copy mode (packed
-//               channels-last frame) these warps do not exist: the warp-5
-//               thread also copies each A stage with 2-D tensor copies.
+//   warp  5     one thread streaming packed weights with bulk copies (TMA);
+//               in tensor-copy mode (packed channels-last frame) it also
+//               copies each A stage with 2-D tensor copies
+//   warps 6-9   tensor-copy mode: epilogue group 1 (takes every other unit)
+//   warps 6-13  producer mode: a band of grad_out -> shared memory (A
+//               operand), 32 channels per stage, rows in the 128-byte
+//               swizzled K-major layout of the tensor core
 // Pipelines (all mbarriers, all waits bounded):
-//   A ring   a_stages  producers -> MMA        (A_full / A_empty)
+//   A ring   a_stages  loader/producers -> MMA (A_full / A_empty)
 //   B ring   b_stages  weight loader -> MMA    (B_full / B_empty); when the
 //            whole packed weight of the launch fits, it is loaded once
 //   acc      acc_bufs  MMA -> epilogue         (acc_full / acc_empty)
@@ -38,15 +43,16 @@ constexpr int kLoadWarp = 5;
 constexpr int kProdWarp0 = 6;
 constexpr int kProdWarps = 8;
 constexpr int kThreads = (kProdWarp0 + kProdWarps) * 32;
-constexpr int kThreadsTmaA = kProdWarp0 * 32;
+constexpr int kThreadsTmaA = (kProdWarp0 + kEpiWarps) * 32;   // second epilogue group in warps 6-9
 constexpr int kMaxAStages = 4;
 constexpr int kMaxBStages = 32;
 constexpr int kRowSlots = kProdWarps * 32 / 4;   // 4-byte producer: threads per channel lane
 constexpr int kMaxRowsPerThread = 16;            // a_rows <= kRowSlots * kMaxRowsPerThread
 constexpr int kGroupThreads = 128;               // quad producer: threads per producer group
 constexpr int kQuadBatch = 4;                    // quad producer: warp items with loads in flight
-constexpr int kTapTableOffset = 1024;            // bytes into shared memory
-constexpr int kStageOffset = 3072;               // operand stages start at the next 1024-byte boundary
+constexpr int kGroupTableOffset = 1024;          // bytes into shared memory: MMA group table
+constexpr int kXchgOffset = 3072;                // epilogue row exchange; operand stages follow at the next
+                                                 // 1024-byte boundary
 
 struct Barriers {
     uint64_t a_full[kMaxAStages];
@@ -59,8 +65,8 @@ struct Barriers {
     uint32_t tmem_base;
     volatile int abort_flag;
 };
-static_assert(sizeof(Barriers) <= kTapTableOffset, "barrier block exceeds its reserved bytes");
-static_assert(kTapTableOffset + kMaxTaps * 16 <= kStageOffset, "tap table exceeds its reserved bytes");
+static_assert(sizeof(Barriers) <= kGroupTableOffset, "barrier block exceeds its reserved bytes");
+static_assert(kGroupTableOffset + kMaxTaps * 16 <= kXchgOffset, "MMA group table exceeds its reserved bytes");
 
 // Cycle accounting per CTA, compiled in only with -DDGRAD_TRACE (a tracing
 // build used to see where a launch spends its time).  Slots: MMA waits on
@@ -83,6 +89,12 @@ __device__ unsigned long long g_trace[kTraceCtas * kTraceSlots];
 __device__ __forceinline__ void fail(Barriers *bars, const MainParams &p) {
     bars->abort_flag = 1;
     atomicOr(p.err, kErrTimeout);
+}
+
+// Epilogue warp groups: two in tensor-copy mode with two accumulator sets
+// (group g takes the units of set g), else one.
+__device__ __forceinline__ int epi_groups(const MainParams &p, bool tma_mode) {
+    return (tma_mode && p.acc_bufs == 2) ? 2 : 1;
 }
 
 // Ring position: stage index and the parity of its current round.
@@ -119,7 +131,7 @@ __device__ __forceinline__ int plane_elems_below(const MainParams &p, int n, int
 // rows with no grad_out element are written as zeros.
 template <int KC>
 __device__ __forceinline__ void produce_quads(const MainParams &p, Barriers *bars, float *a_base, int a_stage_floats,
-                                              int tile_rows, long long tmo) {
+                                              int tile_step, long long tmo) {
     const int gtid = threadIdx.x - kProdWarp0 * 32;
     const int group = gtid / kGroupThreads;
     const int tid = gtid % kGroupThreads;
@@ -133,7 +145,7 @@ __device__ __forceinline__ void produce_quads(const MainParams &p, Barriers *bar
     Ring ring;
     uint32_t it = 0;
     for (int w = blockIdx.x; w < p.n_work && !bars->abort_flag; w += gridDim.x) {
-        const int P0 = (w / p.n_slices) * tile_rows;
+        const int P0 = (w / p.n_slices) * tile_step;
         const int P1 = P0 + p.a_rows;
         // Rows of this thread that hold no grad_out element (zeros), as a mask.
         uint32_t zero_mask = 0;
@@ -281,7 +293,7 @@ __device__ __forceinline__ void produce_quads(const MainParams &p, Barriers *bar
 // swizzled rows.  The tensor core reads the TF32 part of these fp32 values.
 template <int KC>
 __device__ __forceinline__ void produce_async4(const MainParams &p, Barriers *bars, float *a_base, int a_stage_floats,
-                                               int tile_rows, long long tmo) {
+                                               int tile_step, long long tmo) {
     const int ptid = threadIdx.x - kProdWarp0 * 32;
     const int e = ptid & 3, pr = ptid >> 2;
     const int sw = pr & 7;
@@ -289,7 +301,7 @@ __device__ __forceinline__ void produce_async4(const MainParams &p, Barriers *ba
     const uint32_t a0 = dev::smem_u32(a_base) + e * 4;
     Ring ring;
     for (int w = blockIdx.x; w < p.n_work && !bars->abort_flag; w += gridDim.x) {
-        const int P0 = (w / p.n_slices) * tile_rows;
+        const int P0 = (w / p.n_slices) * tile_step;
         int off[kMaxRowsPerThread];
 #pragma unroll
         for (int i = 0; i < kMaxRowsPerThread; ++i) {
@@ -324,17 +336,184 @@ __device__ __forceinline__ void produce_async4(const MainParams &p, Barriers *ba
     dev::cp_async_wait_all();
 }
 
-template <int KC, bool kTmaA>
+// ------------------------------------------------------------------ epilogue
+// Result of one 16-column batch of one phase for this warp's 32 rows (lane =
+// output position, out[j] = input channel c0 + j), from registers already
+// loaded from tensor memory: r[g] = sub-accumulator g.
+//
+// Ungrouped (S = 1) the accumulator is the result.  Grouped, sub-accumulator
+// g holds, at row o, the tap whose output is row o - (S-1-g); the result of
+// row o is the sum over g of sub-accumulator g at row o + (S-1-g).  Rows of
+// the next warp come through shared memory (each warp publishes the first
+// rows the warp above it needs); rows past the 128-row block are never
+// valid outputs (the tile step leaves them out).
+template <int S, int SMAX>
+__device__ __forceinline__ void combine(const uint32_t (&r)[SMAX][16], float (&out)[16], float *xw, const float *xn,
+                                        int lane, int bar_id) {
+    if constexpr (S == 1) {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) out[j] = __uint_as_float(r[0][j]);
+    } else {
+        int slot = 0;
+#pragma unroll
+        for (int g = 0; g < S - 1; ++g) {
+            const int sh = S - 1 - g;
+            if (lane < sh) {
+#pragma unroll
+                for (int j = 0; j < 16; ++j) xw[(slot + lane) * 16 + j] = __uint_as_float(r[g][j]);
+            }
+            slot += sh;
+        }
+        DGRAD_TRACE_CLOCK(tb0);
+        dev::named_bar(bar_id, 128);
+        DGRAD_TRACE_CLOCK(tb1);
+        if (threadIdx.x == 0) DGRAD_TRACE_ADD(5, tb1 - tb0);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) out[j] = __uint_as_float(r[S - 1][j]);
+        slot = 0;
+#pragma unroll
+        for (int g = 0; g < S - 1; ++g) {
+            const int sh = S - 1 - g;
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                float v = __shfl_down_sync(0xffffffffu, __uint_as_float(r[g][j]), sh);
+                if (lane + sh >= 32) v = xn ? xn[(slot + lane + sh - 32) * 16 + j] : 0.f;
+                out[j] += v;
+            }
+            slot += sh;
+        }
+    }
+}
+
+// Stores of one finished batch: NV = 1 writes one phase (4-byte stores, a
+// warp writes 32 consecutive positions of one channel row); NV = s (2 or 4)
+// writes the s column phases of one row phase together: positions (q, u) of
+// phases (a, 0..s-1) are the s consecutive elements s*u .. s*u+s-1 of input
+// row s*q + a, one 8- or 16-byte store.
+template <int NV>
+__device__ __forceinline__ void store_batch(float *dst, size_t plane, int ncols, const float (&res)[NV][16]) {
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+        if (j >= ncols) break;
+        float *d = dst + static_cast<size_t>(j) * plane;
+        if constexpr (NV == 1) {
+            *d = res[0][j];
+        } else if constexpr (NV == 2) {
+            *reinterpret_cast<float2 *>(d) = make_float2(res[0][j], res[1][j]);
+        } else {
+            *reinterpret_cast<float4 *>(d) = make_float4(res[0][j], res[1][j], res[2][j], res[3][j]);
+        }
+    }
+}
+
+// Epilogue state of one warp across the batches of a work unit.
+struct EpiCtx {
+    const MainParams *p;
+    uint32_t tbase;       // tensor-memory address of this warp's lanes in the unit's accumulator set
+    bool row_ok;
+    int n, q, u, ci0, nci;
+    float *xbase;         // this group's row-exchange area
+    int slots, ew, lane, bar_id;
+    uint32_t xcount;      // row exchanges done (alternates the exchange buffers)
+};
+
+// One work unit's output rows for this warp: every phase, the 16-column
+// batches c0 = c_first, c_first + c_step, ... of the slice.  Software-
+// pipelined: the tensor-memory loads of a batch are issued before the stores
+// of the previous batch, so their latency hides behind those stores.  The
+// last batch's values are returned in `pend` (stored by the caller after it
+// has released the accumulator set).
+template <int NV, int SMAX>
+__device__ __forceinline__ void epilogue_unit(EpiCtx &e, int c_first, int c_step, float (&pend)[NV][16],
+                                              float *&pend_dst, int &pend_cols) {
+    const MainParams &p = *e.p;
+    const size_t plane = static_cast<size_t>(p.H) * p.W;
+    for (int ph0 = 0; ph0 < p.n_phases; ph0 += NV) {
+        const PhaseDesc &pd0 = p.phase[ph0];
+        const bool valid = e.row_ok && e.q < pd0.Hq && e.u < pd0.Wq;
+        const int ih = p.s * e.q + pd0.a, iw = p.s * e.u + pd0.b;
+        float *dst = p.gi + (static_cast<size_t>(e.n) * p.Ci + e.ci0) * plane + static_cast<size_t>(ih) * p.W + iw;
+        for (int c0 = c_first; c0 < p.bn; c0 += c_step) {
+            uint32_t r[NV][SMAX][16];
+            DGRAD_TRACE_CLOCK(tl0);
+#pragma unroll
+            for (int v = 0; v < NV; ++v) {
+                const int sub = p.phase[ph0 + v].tap_count ? p.phase[ph0 + v].sub : 0;
+                const int col = p.phase[ph0 + v].col;
+#pragma unroll
+                for (int g = 0; g < SMAX; ++g)
+                    if (g < sub) dev::tmem_ld16(e.tbase + static_cast<uint32_t>(col + g * p.bn + c0), r[v][g]);
+            }
+            // stores of the previous batch overlap the loads above
+            if (pend_dst) store_batch<NV>(pend_dst, plane, pend_cols, pend);
+            dev::tmem_wait_ld();
+            DGRAD_TRACE_CLOCK(tl1);
+            if (threadIdx.x == 0) DGRAD_TRACE_ADD(4, tl1 - tl0);
+#pragma unroll
+            for (int v = 0; v < NV; ++v) {
+                const int sub = p.phase[ph0 + v].tap_count ? p.phase[ph0 + v].sub : 0;
+                float *xb = e.xbase + static_cast<size_t>((e.xcount & 1) * 4) * e.slots * 16;
+                float *xw = xb + e.ew * e.slots * 16;
+                const float *xn = e.ew < 3 ? xw + e.slots * 16 : nullptr;
+                if (sub == 0) {
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) pend[v][j] = 0.f;
+                } else if (sub == 1) {
+                    combine<1, SMAX>(r[v], pend[v], xw, xn, e.lane, e.bar_id);
+                } else {
+                    if constexpr (SMAX >= 2) {
+                        if (sub == 2) combine<2, SMAX>(r[v], pend[v], xw, xn, e.lane, e.bar_id);
+                    }
+                    if constexpr (SMAX >= 3) {
+                        if (sub == 3) combine<3, SMAX>(r[v], pend[v], xw, xn, e.lane, e.bar_id);
+                    }
+                    if constexpr (SMAX >= 4) {
+                        if (sub == 4) combine<4, SMAX>(r[v], pend[v], xw, xn, e.lane, e.bar_id);
+                    }
+                    ++e.xcount;
+                }
+            }
+            pend_dst = valid ? dst + static_cast<size_t>(c0) * plane : nullptr;
+            pend_cols = min(16, e.nci - c0);
+        }
+    }
+}
+
+template <int NV, int SMAX>
+__device__ __forceinline__ void epilogue_run(EpiCtx &e, int c_first, int c_step, uint64_t *acc_empty) {
+    float pend[NV][16];
+    float *pend_dst = nullptr;
+    int pend_cols = 0;
+    epilogue_unit<NV, SMAX>(e, c_first, c_step, pend, pend_dst, pend_cols);
+    // Every value of the unit is in registers: release the accumulator set
+    // to the MMA, then store the last batch.
+    dev::tc_fence_before();
+    dev::mbar_arrive(dev::smem_u32(acc_empty));
+    DGRAD_TRACE_CLOCK(ts0);
+    if (pend_dst) store_batch<NV>(pend_dst, static_cast<size_t>(e.p->H) * e.p->W, pend_cols, pend);
+    DGRAD_TRACE_CLOCK(ts1);
+    if (threadIdx.x == 0) DGRAD_TRACE_ADD(14, ts1 - ts0);
+}
+
+// kEpi selects the epilogue's store form (one instantiation each keeps the
+// register allocation of every form separate): 0 one phase at a time (up to
+// kMaxSub sub-accumulators), 1 two column phases together (stride 2, up to
+// two sub-accumulators), 2 four column phases together (stride 4).
+// Registers: each SM sub-partition holds a quarter of the register file and
+// a quarter of the block's warps (rounded up), so 10 warps leave 168 per
+// thread and 14 warps 128.
+template <int KC, bool kTmaA, int kEpi>
 __global__ void __launch_bounds__(kTmaA ? kThreadsTmaA : kThreads, 1)
     tc_dgrad_kernel(const __grid_constant__ MainParams p) {
     static_assert(KC == 32, "operand rows are one 128-byte swizzle row of 32 TF32 values");
     extern __shared__ __align__(1024) uint8_t smem[];
     Barriers *bars = reinterpret_cast<Barriers *>(smem);
-    uint4 *tap_table = reinterpret_cast<uint4 *>(smem + kTapTableOffset);
+    uint4 *group_table = reinterpret_cast<uint4 *>(smem + kGroupTableOffset);
+    float *xchg = reinterpret_cast<float *>(smem + kXchgOffset);
     // Operand stages start on a 1024-byte boundary of the shared window: the
     // 128-byte swizzle is a function of the address bits inside that pattern.
     const uint32_t smem0 = dev::smem_u32(smem);
-    const uint32_t stage0 = (smem0 + kStageOffset + 1023) & ~1023u;
+    const uint32_t stage0 = (smem0 + kXchgOffset + static_cast<uint32_t>(p.xchg_bytes) + 1023) & ~1023u;
     float *a_base = reinterpret_cast<float *>(smem + (stage0 - smem0));
     const int a_stage_floats = p.a_rows * KC;
     uint8_t *b_base = reinterpret_cast<uint8_t *>(a_base) + static_cast<size_t>(p.a_stages) * a_stage_floats * 4;
@@ -363,13 +542,7 @@ __global__ void __launch_bounds__(kTmaA ? kThreadsTmaA : kThreads, 1)
     if (warp == kMmaWarp) {
         dev::tmem_alloc(dev::smem_u32(&bars->tmem_base), p.tmem_cols);
         dev::tmem_relinquish();
-        // Per-tap MMA data: A row offset (bytes), accumulator column offset,
-        // and whether the tap is the first of its phase.
-        for (int t = lane; t < p.n_taps; t += 32) {
-            const TapDesc td = p.tap[t];
-            tap_table[t] = make_uint4(static_cast<uint32_t>(td.shift) * 128, static_cast<uint32_t>(td.phase * p.bn),
-                                      t == p.phase[td.phase].tap_begin ? 1u : 0u, 0u);
-        }
+        for (int i = lane; i < p.n_mgroups; i += 32) group_table[i] = p.mgroup[i];
     }
     dev::tc_fence_before();
     __syncthreads();
@@ -377,29 +550,31 @@ __global__ void __launch_bounds__(kTmaA ? kThreadsTmaA : kThreads, 1)
     const uint32_t tmem_base = bars->tmem_base;
     const long long tmo = p.timeout_ns;
     DGRAD_TRACE_CLOCK(t_start);
-    const int tile_rows = p.tm * kBlockM;
+    const int tile_step = p.tile_step;
+    const uint32_t tap_b_bytes = static_cast<uint32_t>(p.bn) * 128;   // one tap of one chunk of B
+    const int m_cols = p.acc_cols / p.tm;                              // accumulator columns of one M block
 
     if (!kTmaA && warp >= kProdWarp0) {
         // ------------------------------------------------------ producers
         if (p.vec_producer)
-            produce_quads<KC>(p, bars, a_base, a_stage_floats, tile_rows, tmo);
+            produce_quads<KC>(p, bars, a_base, a_stage_floats, tile_step, tmo);
         else
-            produce_async4<KC>(p, bars, a_base, a_stage_floats, tile_rows, tmo);
+            produce_async4<KC>(p, bars, a_base, a_stage_floats, tile_step, tmo);
         DGRAD_TRACE_CLOCK(t_pend);
         if (threadIdx.x == kProdWarp0 * 32) DGRAD_TRACE_ADD(12, t_pend - t_start);
     } else if (warp == kLoadWarp) {
         // ------------------------------------------------- weight loader
-        // B stage (c, tg) = taps [tg*tap_group, ...) of channel chunk c of the
-        // work unit's slice: one contiguous block of the packed weights.
+        // B stage (c, tg) = taps [bg_tap0[tg], bg_tap0[tg+1]) of channel
+        // chunk c of the work unit's slice: one contiguous block of the
+        // packed weights.
         if (lane == 0) {
             if (kTmaA) dev::prefetch_tensormap(&p.a_map);
             dev::grid_dependency_wait();   // packed weights (and frame) come from the preceding kernel
-            const size_t tap_bytes = static_cast<size_t>(p.bn) * 128;
             int last_parity[kMaxBStages];   // parity of each stage's last fill, -1 if never filled
             for (int i = 0; i < kMaxBStages; ++i) last_parity[i] = -1;
             int a_last_parity[kMaxAStages];
             for (int i = 0; i < kMaxAStages; ++i) a_last_parity[i] = -1;
-            if (p.b_resident) {   // one slice, one group per chunk: load everything once
+            if (p.b_resident) {   // one slice, one stage per chunk: load everything once
                 for (int c = 0; c < p.n_chunks; ++c) {
                     const uint32_t bar = dev::smem_u32(&bars->b_full[c]);
                     dev::mbar_arrive_expect_tx(bar, p.chunk_bytes);
@@ -415,7 +590,7 @@ __global__ void __launch_bounds__(kTmaA ? kThreadsTmaA : kThreads, 1)
                 const uint32_t a_stage_bytes = static_cast<uint32_t>(a_stage_floats) * 4;
                 for (int w = blockIdx.x; ok && w < p.n_work && !bars->abort_flag; w += gridDim.x) {
                     const int slice = w % p.n_slices;
-                    const int P0 = (w / p.n_slices) * tile_rows;
+                    const int P0 = (w / p.n_slices) * tile_step;
                     for (int c = 0; ok && c < p.n_chunks; ++c) {
                         if (kTmaA) {
                             // A stage: frame rows [P0, P0 + a_rows) x channels [32c, 32c + 32)
@@ -439,13 +614,12 @@ __global__ void __launch_bounds__(kTmaA ? kThreadsTmaA : kThreads, 1)
                                 ok = false;
                                 break;
                             }
-                            const int t0 = tg * p.tap_group;
-                            const int nt = min(p.tap_group, p.n_taps - t0);
-                            const uint32_t bytes = static_cast<uint32_t>(nt * tap_bytes);
+                            const int t0 = p.bg_tap0[tg];
+                            const uint32_t bytes = static_cast<uint32_t>(p.bg_tap0[tg + 1] - t0) * tap_b_bytes;
                             const uint32_t bar = dev::smem_u32(&bars->b_full[ring.stage]);
                             dev::mbar_arrive_expect_tx(bar, bytes);
                             const size_t off =
-                                ((static_cast<size_t>(slice) * p.n_chunks + c) * p.n_taps + t0) * tap_bytes;
+                                ((static_cast<size_t>(slice) * p.n_chunks + c) * p.n_taps + t0) * tap_b_bytes;
                             dev::bulk_g2s(dev::smem_u32(b_base + static_cast<size_t>(ring.stage) * p.chunk_bytes),
                                           reinterpret_cast<const uint8_t *>(p.wp) + off, bytes, bar);
                             last_parity[ring.stage] = static_cast<int>(ring.parity);
@@ -468,7 +642,6 @@ __global__ void __launch_bounds__(kTmaA ? kThreadsTmaA : kThreads, 1)
         // and commits (warp-uniform descriptors stay in uniform registers).
         const uint32_t a_addr0 = dev::smem_u32(a_base);
         const uint32_t b_addr0 = dev::smem_u32(b_base);
-        const uint32_t tap_b_bytes = static_cast<uint32_t>(p.bn) * 128;   // one tap of one chunk of B
         Ring ra, rb, racc;
         bool ok = true;
         bool first_chunk = true;
@@ -519,26 +692,28 @@ __global__ void __launch_bounds__(kTmaA ? kThreadsTmaA : kThreads, 1)
                     DGRAD_TRACE_CLOCK(tb1);
                     if (lane == 0) DGRAD_TRACE_ADD(2, tb1 - tb0);
                     dev::tc_fence_after();
-                    const int t0 = tg * p.tap_group, t1 = min(p.n_taps, t0 + p.tap_group);
-                    const uint64_t bd_s = dev::smem_desc_sw128(b_addr0 + static_cast<uint32_t>(sb) * p.chunk_bytes, 0);
+                    // B stage base, rebased so that a group's tap offset indexes it directly
+                    const uint32_t b_stage = b_addr0 + static_cast<uint32_t>(sb) * p.chunk_bytes -
+                                             static_cast<uint32_t>(p.bg_tap0[tg]) * tap_b_bytes;
+                    const int g0 = p.bg_first[tg], g1 = p.bg_first[tg + 1];
                     for (int m = 0; m < p.tm; ++m) {
                         const uint32_t a_m = a_stage + static_cast<uint32_t>(m * kBlockM) * 128;
-                        const uint32_t d_m = d_base + static_cast<uint32_t>(m * p.n_phases * p.bn);
-                        uint4 nxt = tap_table[t0];
-                        for (int t = t0; t < t1; ++t) {
+                        const uint32_t d_m = d_base + static_cast<uint32_t>(m * m_cols);
+                        uint4 nxt = group_table[g0];
+                        for (int gi = g0; gi < g1; ++gi) {
                             const uint4 cur = nxt;
-                            if (t + 1 < t1) nxt = tap_table[t + 1];   // prefetch the next tap's entry
-                            // A window of tap t: frame rows [m*128 + shift, +128) of the
+                            if (gi + 1 < g1) nxt = group_table[gi + 1];   // prefetch the next group's entry
+                            // A window of the group: frame rows [m*128 + shift, +128) of the
                             // stage.  The swizzle follows the absolute address bits, so the
                             // window may start on any 128-byte row with base offset 0.
-                            const uint64_t ad_t = dev::smem_desc_sw128(a_m + cur.x, 0);
-                            const uint64_t bd_t = dev::desc_add(bd_s, static_cast<uint32_t>(t - t0) * tap_b_bytes);
-                            const uint32_t d = d_m + cur.y;
-                            const uint32_t acc0 = (c > 0 || cur.z == 0) ? 1u : 0u;
+                            const uint64_t ad = dev::smem_desc_sw128(a_m + cur.x, 0);
+                            const uint64_t bd = dev::smem_desc_sw128(b_stage + cur.z, 0);
+                            const uint32_t d = d_m + (cur.y & 0x7fffffffu);
+                            const uint32_t acc0 = (c > 0 || (cur.y >> 31) == 0) ? 1u : 0u;
 #pragma unroll
                             for (int k8 = 0; k8 < KC / 8; ++k8)
-                                dev::mma_tf32_elect(d, dev::desc_add(ad_t, 32 * k8), dev::desc_add(bd_t, 32 * k8),
-                                                    p.idesc, k8 > 0 ? 1u : acc0);
+                                dev::mma_tf32_elect(d, dev::desc_add(ad, 32 * k8), dev::desc_add(bd, 32 * k8), cur.w,
+                                                    k8 > 0 ? 1u : acc0);
                         }
                     }
                     if (!p.b_resident) {
@@ -562,60 +737,68 @@ __global__ void __launch_bounds__(kTmaA ? kThreadsTmaA : kThreads, 1)
         if (lane == 0) DGRAD_TRACE_ADD(11, t_mend - t_start);
     } else {
         // ------------------------------------------------------- epilogue
-        const int ew = warp;   // 0..3: tensor-memory lanes 32*ew .. 32*ew+31
-        const size_t plane = static_cast<size_t>(p.H) * p.W;
+        // Epilogue group eg (warps 0-3, and 6-9 in tensor-copy mode); warp
+        // ew = warp % 4 reads tensor-memory lanes 32*ew .. 32*ew+31.  With two
+        // groups, group g takes every other unit: those of accumulator set g.
+        const int eg = warp < kEpiWarps ? 0 : 1;
+        const int ew = warp & 3;
+        const int n_groups = epi_groups(p, kTmaA);
+        const int slots = p.max_sub * (p.max_sub - 1) / 2;
+        EpiCtx e;
+        e.p = &p;
+        e.xbase = xchg + static_cast<size_t>(eg) * 2 * 4 * slots * 16;
+        e.slots = slots;
+        e.ew = ew;
+        e.lane = lane;
+        e.bar_id = 1 + eg;
+        e.xcount = 0;
         Ring racc;
-        for (int w = blockIdx.x; w < p.n_work && !bars->abort_flag; w += gridDim.x, racc.next(p.acc_bufs)) {
+        int i = 0;
+        for (int w = blockIdx.x; eg < n_groups && w < p.n_work; w += gridDim.x, ++i) {
+            if (n_groups == 2 && (i & 1) != eg) continue;
+            const int stage = n_groups == 2 ? eg : racc.stage;
+            const uint32_t parity = racc.parity;
+            if (n_groups == 2)
+                racc.parity ^= 1;
+            else
+                racc.next(p.acc_bufs);
             const int tile = w / p.n_slices, slice = w % p.n_slices;
             DGRAD_TRACE_CLOCK(te0);
-            if (!dev::mbar_wait(dev::smem_u32(&bars->acc_full[racc.stage]), racc.parity, tmo)) {
-                fail(bars, p);
+            // All four warps of the group leave together or go on together.
+            const bool got = dev::mbar_wait(dev::smem_u32(&bars->acc_full[stage]), parity, tmo);
+            if (!dev::named_bar_and(e.bar_id, 128, got)) {
+                if (!got) fail(bars, p);
                 break;
             }
             DGRAD_TRACE_CLOCK(te1);
             if (threadIdx.x == 0) DGRAD_TRACE_ADD(6, te1 - te0);
             dev::tc_fence_after();
-            const int ci0 = slice * p.bn;
-            const int nci = min(p.bn, p.Ci - ci0);
+            e.ci0 = slice * p.bn;
+            e.nci = min(p.bn, p.Ci - e.ci0);
+            // One 128-row block per unit when grouped (tm = 1); tm blocks otherwise.
             for (int m = 0; m < p.tm; ++m) {
-                const int P = tile * tile_rows + m * kBlockM + ew * 32 + lane;
-                int n, q, u;
-                dev::decode_position(p, P, n, q, u);
-                const bool pos_ok = P < p.positions;
-                for (int ph = 0; ph < p.n_phases; ++ph) {
-                    const PhaseDesc &pd = p.phase[ph];
-                    const bool valid = pos_ok && q < pd.Hq && u < pd.Wq;
-                    const int ih = p.s * q + pd.a, iw = p.s * u + pd.b;
-                    float *dst =
-                        p.gi + (static_cast<size_t>(n) * p.Ci + ci0) * plane + static_cast<size_t>(ih) * p.W + iw;
-                    if (pd.tap_count == 0) {
-                        if (valid)
-                            for (int j = 0; j < nci; ++j) dst[j * plane] = 0.f;
-                        continue;
-                    }
-                    const uint32_t col0 = tmem_base + (static_cast<uint32_t>(ew * 32) << 16) +
-                                          racc.stage * p.acc_cols + (m * p.n_phases + ph) * p.bn;
-                    for (int c0 = 0; c0 < p.bn; c0 += 32) {
-                        uint32_t r0[16], r1[16];
-                        const bool two = c0 + 16 < p.bn;   // warp-uniform
-                        dev::tmem_ld16(col0 + c0, r0);
-                        if (two) dev::tmem_ld16(col0 + c0 + 16, r1);
-                        dev::tmem_wait_ld();
-                        if (valid) {
-#pragma unroll
-                            for (int j = 0; j < 16; ++j)
-                                if (c0 + j < nci) dst[(c0 + j) * plane] = __uint_as_float(r0[j]);
-                            if (two) {
-#pragma unroll
-                                for (int j = 0; j < 16; ++j)
-                                    if (c0 + 16 + j < nci) dst[(c0 + 16 + j) * plane] = __uint_as_float(r1[j]);
-                            }
-                        }
-                    }
+                const int o = m * kBlockM + ew * 32 + lane;   // row of the unit
+                const int P = tile * tile_step + o;
+                dev::decode_position(p, P, e.n, e.q, e.u);
+                e.row_ok = o < tile_step && P < p.positions;
+                e.tbase = tmem_base + (static_cast<uint32_t>(ew * 32) << 16) +
+                          static_cast<uint32_t>(stage * p.acc_cols + m * m_cols);
+                const bool last = m + 1 == p.tm;
+                const int cf = 0, cs = 16;
+                if (!last) {
+                    // earlier blocks (ungrouped plans only): release nothing yet
+                    float pend[1][16];
+                    float *pd = nullptr;
+                    int pc = 0;
+                    epilogue_unit<1, 1>(e, cf, cs, pend, pd, pc);
+                    if (pd) store_batch<1>(pd, static_cast<size_t>(p.H) * p.W, pc, pend);
+                } else {
+                    // NV column phases stored together, up to SMAX sub-accumulators per phase
+                    constexpr int NV = kEpi == 2 ? 4 : (kEpi == 1 ? 2 : 1);
+                    constexpr int SMAX = kEpi == 2 ? 1 : (kEpi == 1 ? 2 : kMaxSub);
+                    epilogue_run<NV, SMAX>(e, cf, cs, &bars->acc_empty[stage]);
                 }
             }
-            dev::tc_fence_before();
-            dev::mbar_arrive(dev::smem_u32(&bars->acc_empty[racc.stage]));
             DGRAD_TRACE_CLOCK(te2);
             if (threadIdx.x == 0) DGRAD_TRACE_ADD(7, te2 - te1);
         }
@@ -629,9 +812,9 @@ __global__ void __launch_bounds__(kTmaA ? kThreadsTmaA : kThreads, 1)
     if (warp == kMmaWarp) dev::tmem_dealloc(tmem_base, p.tmem_cols);
 }
 
-template <int KC, bool kTmaA>
+template <int KC, bool kTmaA, int kEpi>
 cudaError_t launch_kc(const MainParams &p, const Tiling &t, cudaStream_t stream, bool pdl) {
-    auto kern = tc_dgrad_kernel<KC, kTmaA>;
+    auto kern = tc_dgrad_kernel<KC, kTmaA, kEpi>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, t.smem_bytes);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg{};
@@ -645,6 +828,13 @@ cudaError_t launch_kc(const MainParams &p, const Tiling &t, cudaStream_t stream,
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
     return cudaLaunchKernelEx(&cfg, kern, p);
+}
+
+template <bool kTmaA>
+cudaError_t launch_mode(const MainParams &p, const Tiling &t, cudaStream_t stream, bool pdl) {
+    if (p.vec_w && p.s == 4) return launch_kc<32, kTmaA, 2>(p, t, stream, pdl);
+    if (p.vec_w && p.s == 2) return launch_kc<32, kTmaA, 1>(p, t, stream, pdl);
+    return launch_kc<32, kTmaA, 0>(p, t, stream, pdl);
 }
 
 }  // namespace
@@ -661,7 +851,7 @@ extern "C" int dgrad_trace_read(unsigned long long *host, int n) {
 
 cudaError_t launch_tc(const MainParams &p, const Tiling &t, cudaStream_t stream, bool pdl) {
     if (t.kc != 32) return cudaErrorInvalidValue;
-    return p.a_tma ? launch_kc<32, true>(p, t, stream, pdl) : launch_kc<32, false>(p, t, stream, pdl);
+    return p.a_tma ? launch_mode<true>(p, t, stream, pdl) : launch_mode<false>(p, t, stream, pdl);
 }
 
 }  // namespace dgrad

@@ -88,6 +88,8 @@ typedef struct {
     int sm_count;      /* dgrad_describe only: SM count to plan for */
     int a_source;      /* tcgen05 path, how grad_out reaches the MMA: 0 automatic, 1 packed frame + tensor
                           copies (workspace holds a channels-last copy of grad_out), 2 producer warps */
+    int group_taps;    /* tcgen05 path: 0 automatic, 1 the taps of one kernel row share one MMA
+                          (N = taps x slice_n; DGRAD_ERR_UNSUPPORTED when that cannot fit), 2 never */
 } dgrad_options_t;
 
 /* Everything a plan decided, for tests, benchmarks and logs. */
@@ -108,6 +110,8 @@ typedef struct {
     int a_source;          /* 1: packed frame + tensor copies, 2: producer warps (tcgen05 path) */
     int smem_bytes;        /* dynamic shared memory of the main kernel */
     int tmem_cols;         /* tensor-memory columns allocated per CTA (tcgen05 path) */
+    int group_taps;        /* 1: one MMA per kernel row of taps (tcgen05 path) */
+    int tile_step;         /* output positions per work-unit tile */
     size_t workspace_bytes;/* device workspace owned by the plan */
     size_t packed_weight_bytes;
     double useful_flops;   /* 2*N*Co*oH*oW*Ci*kH*kW */
@@ -137,9 +141,11 @@ dgrad_status_t dgrad_describe(int N, int Ci, int H, int W, int Co, int kH, int k
 
 /* Host-only: the sub-pixel phase and tap tables behind dgrad_describe, for
  * checking the decomposition without a device.  Writes up to `cap` phases
- * (a, b, Hq, Wq, tap_begin, tap_count: 6 ints each, into `phases`) and up to
- * `cap` taps (kh, kw, shift: 3 ints each, into `taps`); *n_phases and *n_taps
- * receive the full counts.  Phase (a, b) holds input rows ih = stride*q + a
+ * (a, b, Hq, Wq, tap_begin, tap_count, row_len: 7 ints each, into `phases`)
+ * and up to `cap` taps (kh, kw, shift: 3 ints each, into `taps`); *n_phases
+ * and *n_taps receive the full counts.  A phase lists its taps kernel row by
+ * kernel row, row_len taps per row, the shift falling by one from each tap
+ * to the next inside a row.  Phase (a, b) holds input rows ih = stride*q + a
  * and columns iw = stride*u + b, q < Hq, u < Wq; its output (n, q, u) is the
  * flattened frame position (n*Hv + q)*Wp + u, and tap t of the phase reads
  * the zero-padded grad_out frame at that position plus shift (see
@@ -229,6 +235,10 @@ void dgrad_plan_destroy(dgrad_plan_t plan);
 
 /* Static English description of a status code. */
 const char *dgrad_status_string(dgrad_status_t status);
+
+/* The CUDA runtime's message for the error behind the last
+ * DGRAD_ERR_CUDA returned to the calling thread ("" if none). */
+const char *dgrad_cuda_error_string(void);
 
 #ifdef __cplusplus
 }

@@ -113,6 +113,8 @@ TILINGS = [
     dict(tile_blocks=1), dict(tile_blocks=2), dict(tile_blocks=1, chunk_k=32, grid=3),
     dict(tile_blocks=2, grid=3), dict(tile_blocks=1, slice_n=16, grid=5), dict(tile_blocks=1, slice_n=32, grid=7),
     dict(tile_blocks=3, grid=2), dict(tile_blocks=4, grid=1), dict(tile_blocks=4, slice_n=16, grid=2),
+    dict(group_taps="on", grid=3), dict(group_taps="on", slice_n=16, grid=5), dict(group_taps="on", grid=1),
+    dict(group_taps="off", grid=3), dict(group_taps="on", slice_n=32),
 ]
 
 
@@ -134,6 +136,8 @@ def test_tc_tilings(shape, opts, a_source):
     for k in ("tile_blocks", "slice_n", "chunk_k", "a_source"):
         if k in opts:
             assert info[k] == opts[k]
+    if "group_taps" in opts:
+        assert info["group_taps"] == (1 if opts["group_taps"] == "on" else 0)
 
 
 @pytest.mark.parametrize("opts", [dict(slice_n=16), dict(slice_n=32, chunk_k=8), dict(chunk_k=32)])
@@ -159,6 +163,21 @@ def test_edge_shapes_both_sources(shape, a_source):
     go, w = make_tensors((N, Co, out_ext(H, kH, s, ph), out_ext(W, kW, s, pw)), (Co, Ci, kH, kW), 72, "uniform")
     info = check((N, Ci, H, W, Co, kH, kW, s, ph, pw), go, w, "tf32", a_source=a_source)
     assert info["a_source"] == a_source
+
+
+@pytest.mark.parametrize("group_taps", ["on", "off"])
+@pytest.mark.parametrize("shape", EDGE)
+def test_edge_shapes_grouped_and_not(shape, group_taps):
+    N, Ci, Co, H, W, kH, kW, s, ph, pw = shape
+    try:
+        dg.describe(N, Ci, H, W, Co, kH, kW, s, ph, pw, "tf32", group_taps=group_taps)
+    except dg.DgradError as e:
+        if e.status == 2:
+            pytest.skip("taps of a kernel row cannot share one MMA here")
+        raise
+    go, w = make_tensors((N, Co, out_ext(H, kH, s, ph), out_ext(W, kW, s, pw)), (Co, Ci, kH, kW), 74, "uniform")
+    info = check((N, Ci, H, W, Co, kH, kW, s, ph, pw), go, w, "tf32", group_taps=group_taps)
+    assert info["group_taps"] == (1 if group_taps == "on" else 0)
 
 
 # ----------------------------------------------------------------- semantics

@@ -141,6 +141,56 @@ def emulate(go, w, H, W, s, ph, pw):
     return gi
 
 
+def emulate_grouped(go, w, H, W, s, ph, pw, block=128):
+    """The grouped MMA's arithmetic in numpy: per tile of tile_step positions,
+    a 128-row block; the taps of one kernel row share the A window at the
+    row's smallest shift, sub-accumulator g holds tap g's products, and the
+    result of row o adds sub-accumulator g at row o + (row_len - 1 - g)."""
+    N, Co, oH, oW = go.shape
+    _, Ci, kH, kW = w.shape
+    info = dg.describe(N, Ci, H, W, Co, kH, kW, s, ph, pw, group_taps="on")
+    assert info["group_taps"] == 1
+    phases, taps = dg.describe_taps(N, Ci, H, W, Co, kH, kW, s, ph, pw)
+    Ph, Pw, Hv, Wp = info["Ph"], info["Pw"], info["Hv"], info["Wp"]
+    max_row = max(p["row_len"] for p in phases)
+    assert info["tile_step"] == 128 - (max_row - 1)
+    T = block - (max_row - 1)   # the same construction on smaller blocks, so that small shapes span many tiles
+    P = N * Hv * Wp
+    n_tiles = -(-P // T)
+    V = np.zeros((n_tiles * T + block + info["max_shift"], Co))
+    frame = np.zeros((N, Hv, Wp, Co))
+    frame[:, Ph:Ph + oH, Pw:Pw + oW, :] = go.transpose(0, 2, 3, 1)
+    V[:P] = frame.reshape(P, Co)
+    gi = np.full((N, Ci, H, W), np.nan)
+    for p in phases:
+        R = max(1, p["row_len"])
+        ptaps = taps[p["tap_begin"]:p["tap_begin"] + p["tap_count"]]
+        for r0 in range(0, len(ptaps), R):          # shifts fall by one inside a kernel row
+            row = ptaps[r0:r0 + R]
+            assert [t["shift"] for t in row] == list(range(row[0]["shift"], row[0]["shift"] - R, -1))
+        for k in range(n_tiles):
+            P0 = k * T
+            D = np.zeros((R, block, Ci))
+            for r0 in range(0, len(ptaps), R):
+                row = ptaps[r0:r0 + R]
+                a0 = P0 + row[-1]["shift"]
+                for g, t in enumerate(row):
+                    D[g] += V[a0:a0 + block] @ w[:, :, t["kh"], t["kw"]].astype(np.float64)
+            out = np.zeros((T, Ci))
+            for g in range(R):
+                sh = R - 1 - g
+                out += D[g, sh:sh + T]
+            for o in range(T):
+                pos = P0 + o
+                if pos >= P:
+                    break
+                n, rem = divmod(pos, Hv * Wp)
+                q, u = divmod(rem, Wp)
+                if q < p["Hq"] and u < p["Wq"]:
+                    gi[n, :, s * q + p["a"], s * u + p["b"]] = out[o] if p["tap_count"] else 0.0
+    return gi
+
+
 EMU_SHAPES = [
     (2, 3, 4, 8, 8, 3, 3, 1, 1, 1), (1, 2, 3, 7, 5, 3, 3, 1, 0, 0), (2, 2, 3, 6, 7, 5, 3, 1, 2, 1),
     (1, 2, 3, 9, 9, 3, 3, 2, 1, 1), (2, 3, 2, 8, 7, 3, 3, 2, 0, 0), (1, 2, 2, 9, 10, 7, 7, 2, 3, 3),
@@ -172,3 +222,30 @@ def test_emulated_decomposition_workload_shapes(name):
     ref, _ = oracle.dgrad(go, w, wl.H, wl.W, wl.stride, wl.pad_h, wl.pad_w)
     emu = emulate(go, w, wl.H, wl.W, wl.stride, wl.pad_h, wl.pad_w)
     np.testing.assert_allclose(emu, ref, rtol=1e-10, atol=1e-10)
+
+
+@pytest.mark.parametrize("shape", EMU_SHAPES)
+def test_emulated_grouped_taps_match_oracle(shape):
+    N, Ci, Co, H, W, kH, kW, s, ph, pw = shape
+    if max(kW, -(-kW // s)) > 4 and s == 1:
+        pytest.skip("rows longer than four taps are not grouped")
+    oH, oW = (H + 2 * ph - kH) // s + 1, (W + 2 * pw - kW) // s + 1
+    go, w = make_tensors((N, Co, oH, oW), (Co, Ci, kH, kW), 63, "uniform")
+    go, w = go.numpy(), w.numpy()
+    ref, _ = oracle.dgrad(go, w, H, W, s, ph, pw)
+    emu = emulate_grouped(go, w, H, W, s, ph, pw, block=16)
+    assert not np.isnan(emu).any(), "an input element was never written"
+    np.testing.assert_allclose(emu, ref, rtol=1e-12, atol=1e-12)
+
+
+def test_grouping_plans():
+    r = dg.describe(*WORKLOADS["resnet_stage"].plan_args(), precision="tf32")
+    assert r["group_taps"] == 1 and r["tile_step"] == 126 and r["tmem_cols"] == 512
+    assert dg.describe(*WORKLOADS["pointwise"].plan_args(), precision="tf32")["group_taps"] == 0
+    st = dg.describe(*WORKLOADS["stem"].plan_args(), precision="tf32")
+    assert st["group_taps"] == 1 and st["tile_step"] == 125
+    off = dg.describe(*WORKLOADS["resnet_stage"].plan_args(), precision="tf32", group_taps="off")
+    assert off["group_taps"] == 0 and off["tile_step"] == 128 * off["tile_blocks"]
+    with pytest.raises(dg.DgradError) as e:    # 5 taps per row cannot share one MMA
+        dg.describe(2, 16, 16, 16, 16, 5, 5, 1, 2, 2, precision="tf32", group_taps="on")
+    assert e.value.status == 2
