@@ -159,7 +159,7 @@ constexpr int kBarrierBytes = 4096;   // mbarriers + TMEM slot (1 KB), MMA group
 constexpr int kMaxResidentChunks = 32;
 constexpr int kMaxTcRows = 1024;   // frame rows one tcgen05 A stage may hold (16 per producer thread)
 constexpr size_t kMaxFrameBytes = size_t(64) << 20;   // packed frames up to half the L2
-constexpr int kEpiGroups = 2;         // epilogue warp groups (tensor-copy mode)
+constexpr int kEpiGroups = 1;         // epilogue warp groups
 
 // Split the MMA groups of one channel chunk into B stages of at most `cap`
 // taps each, balanced; false when one MMA group alone exceeds `cap`.
@@ -358,21 +358,15 @@ dgrad_status_t choose_tiling(const Geometry &g, int precision, const dgrad_optio
     if (!t.a_tma) t.frame_bytes = 0;
     // Grouping the taps of a kernel row into one MMA (N = taps x bn) cuts the
     // shared-memory reads of A per FLOP when bn alone leaves the MMA bound by
-    // its operand reads (bn < 128).  It needs the sub-accumulators to fit in
-    // tensor memory twice (double buffering) unless each CTA gets a single
-    // work unit anyway.
+    // its operand reads (bn < 128), but triples the epilogue's tensor-memory
+    // reads and adds its row shifts; measured, the epilogue then bounds the
+    // kernel and the grouped plans ran slower, so grouping is opt-in.
     if (o.group_taps < 0 || o.group_taps > 2) return DGRAD_ERR_INVALID_ARG;
-    int max_row = 1;
-    for (int p = 0; p < g.n_phases; ++p) max_row = std::max(max_row, g.phase[p].row_len);
-    int group_pref[2] = {0, 0};
-    int n_group = 0;
+    int group_pref[1] = {0};
+    const int n_group = 1;
     if (o.group_taps == 1) {
         if (o.tile_blocks > 1) return DGRAD_ERR_UNSUPPORTED;   // grouped MMAs take one 128-row block per unit
-        group_pref[n_group++] = 1;
-    } else {
-        if (o.tile_blocks > 1) max_row = 1;
-        if (o.group_taps == 0 && max_row > 1 && bn < 128) group_pref[n_group++] = 1;
-        group_pref[n_group++] = 0;
+        group_pref[0] = 1;
     }
     bool ok = false;
     for (int gi = 0; gi < n_group && !ok; ++gi) {
@@ -384,9 +378,6 @@ dgrad_status_t choose_tiling(const Geometry &g, int precision, const dgrad_optio
                 c.bn = bn;
                 c.kc = 32;
                 if (!size_tc(g, c, want_res)) continue;
-                if (c.grouped && o.group_taps == 0 && c.acc_bufs < 2 &&
-                    c.n_work > std::min<long long>(o.grid ? o.grid : sm_count, c.n_work))
-                    continue;   // a single accumulator set would serialise MMA and epilogue
                 t = c;
                 ok = true;
             }

@@ -11,14 +11,13 @@
 // one output row further down per column step, and the epilogue adds the
 // sub-accumulators back with the matching row shifts.
 //
-// Roles (448 threads with producer warps, 320 in tensor-copy mode):
-//   warps 0-3   epilogue group 0: tensor memory -> registers -> grad_input
+// Roles (448 threads with producer warps, 192 in tensor-copy mode):
+//   warps 0-3   epilogue: tensor memory -> registers -> grad_input
 //   warp  4     tensor-memory allocation; the MMA loop (whole warp, one
 //               elected lane issues)
 //   warp  5     one thread streaming packed weights with bulk copies (TMA);
 //               in tensor-copy mode (packed channels-last frame) it also
 //               copies each A stage with 2-D tensor copies
-//   warps 6-9   tensor-copy mode: epilogue group 1 (takes every other unit)
 //   warps 6-13  producer mode: a band of grad_out -> shared memory (A
 //               operand), 32 channels per stage, rows in the 128-byte
 //               swizzled K-major layout of the tensor core
@@ -43,7 +42,7 @@ constexpr int kLoadWarp = 5;
 constexpr int kProdWarp0 = 6;
 constexpr int kProdWarps = 8;
 constexpr int kThreads = (kProdWarp0 + kProdWarps) * 32;
-constexpr int kThreadsTmaA = (kProdWarp0 + kEpiWarps) * 32;   // second epilogue group in warps 6-9
+constexpr int kThreadsTmaA = kProdWarp0 * 32;
 constexpr int kMaxAStages = 4;
 constexpr int kMaxBStages = 32;
 constexpr int kRowSlots = kProdWarps * 32 / 4;   // 4-byte producer: threads per channel lane
@@ -89,12 +88,6 @@ __device__ unsigned long long g_trace[kTraceCtas * kTraceSlots];
 __device__ __forceinline__ void fail(Barriers *bars, const MainParams &p) {
     bars->abort_flag = 1;
     atomicOr(p.err, kErrTimeout);
-}
-
-// Epilogue warp groups: two in tensor-copy mode with two accumulator sets
-// (group g takes the units of set g), else one.
-__device__ __forceinline__ int epi_groups(const MainParams &p, bool tma_mode) {
-    return (tma_mode && p.acc_bufs == 2) ? 2 : 1;
 }
 
 // Ring position: stage index and the parity of its current round.
@@ -390,18 +383,24 @@ __device__ __forceinline__ void combine(const uint32_t (&r)[SMAX][16], float (&o
 // writes the s column phases of one row phase together: positions (q, u) of
 // phases (a, 0..s-1) are the s consecutive elements s*u .. s*u+s-1 of input
 // row s*q + a, one 8- or 16-byte store.
-template <int NV>
-__device__ __forceinline__ void store_batch(float *dst, size_t plane, int ncols, const float (&res)[NV][16]) {
+template <int NV, int CB>
+__device__ __forceinline__ void store_batch(float *dst, size_t plane, int ncols, const float (&res)[NV][CB / 16][16]) {
+    float *d = dst;   // advanced by one channel plane per store
 #pragma unroll
-    for (int j = 0; j < 16; ++j) {
-        if (j >= ncols) break;
-        float *d = dst + static_cast<size_t>(j) * plane;
-        if constexpr (NV == 1) {
-            *d = res[0][j];
-        } else if constexpr (NV == 2) {
-            *reinterpret_cast<float2 *>(d) = make_float2(res[0][j], res[1][j]);
-        } else {
-            *reinterpret_cast<float4 *>(d) = make_float4(res[0][j], res[1][j], res[2][j], res[3][j]);
+    for (int k = 0; k < CB / 16; ++k) {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            if (16 * k + j < ncols) {
+                if constexpr (NV == 1) {
+                    *d = res[0][k][j];
+                } else if constexpr (NV == 2) {
+                    *reinterpret_cast<float2 *>(d) = make_float2(res[0][k][j], res[1][k][j]);
+                } else {
+                    *reinterpret_cast<float4 *>(d) =
+                        make_float4(res[0][k][j], res[1][k][j], res[2][k][j], res[3][k][j]);
+                }
+            }
+            d += plane;
         }
     }
 }
@@ -417,15 +416,16 @@ struct EpiCtx {
     uint32_t xcount;      // row exchanges done (alternates the exchange buffers)
 };
 
-// One work unit's output rows for this warp: every phase, the 16-column
-// batches c0 = c_first, c_first + c_step, ... of the slice.  Software-
-// pipelined: the tensor-memory loads of a batch are issued before the stores
-// of the previous batch, so their latency hides behind those stores.  The
-// last batch's values are returned in `pend` (stored by the caller after it
-// has released the accumulator set).
-template <int NV, int SMAX>
-__device__ __forceinline__ void epilogue_unit(EpiCtx &e, int c_first, int c_step, float (&pend)[NV][16],
-                                              float *&pend_dst, int &pend_cols) {
+// One work unit's output rows for this warp: every phase, every input
+// channel of the slice, in batches of CB columns (CB / 16 slices of 16): a
+// batch's tensor-memory loads (for NV phases, up to SMAX sub-accumulators
+// each) are issued together and waited for once.  The previous batch's
+// stores go out before a batch's loads; the last batch's values are returned
+// in `pend` (stored by the caller after it has released the accumulator set).
+template <int NV, int SMAX, int CB>
+__device__ __forceinline__ void epilogue_unit(EpiCtx &e, float (&pend)[NV][CB / 16][16], float *&pend_dst,
+                                              int &pend_cols) {
+    constexpr int K = CB / 16;
     const MainParams &p = *e.p;
     const size_t plane = static_cast<size_t>(p.H) * p.W;
     for (int ph0 = 0; ph0 < p.n_phases; ph0 += NV) {
@@ -433,75 +433,109 @@ __device__ __forceinline__ void epilogue_unit(EpiCtx &e, int c_first, int c_step
         const bool valid = e.row_ok && e.q < pd0.Hq && e.u < pd0.Wq;
         const int ih = p.s * e.q + pd0.a, iw = p.s * e.u + pd0.b;
         float *dst = p.gi + (static_cast<size_t>(e.n) * p.Ci + e.ci0) * plane + static_cast<size_t>(ih) * p.W + iw;
-        for (int c0 = c_first; c0 < p.bn; c0 += c_step) {
-            uint32_t r[NV][SMAX][16];
+        for (int c0 = 0; c0 < p.bn; c0 += CB) {
+            if (pend_dst) store_batch<NV, CB>(pend_dst, plane, pend_cols, pend);
+            uint32_t r[NV][K][SMAX][16];
             DGRAD_TRACE_CLOCK(tl0);
 #pragma unroll
             for (int v = 0; v < NV; ++v) {
                 const int sub = p.phase[ph0 + v].tap_count ? p.phase[ph0 + v].sub : 0;
                 const int col = p.phase[ph0 + v].col;
 #pragma unroll
-                for (int g = 0; g < SMAX; ++g)
-                    if (g < sub) dev::tmem_ld16(e.tbase + static_cast<uint32_t>(col + g * p.bn + c0), r[v][g]);
+                for (int k = 0; k < K; ++k) {
+                    if (c0 + 16 * k >= p.bn) break;
+#pragma unroll
+                    for (int g = 0; g < SMAX; ++g)
+                        if (g < sub)
+                            dev::tmem_ld16(e.tbase + static_cast<uint32_t>(col + g * p.bn + c0 + 16 * k), r[v][k][g]);
+                }
             }
-            // stores of the previous batch overlap the loads above
-            if (pend_dst) store_batch<NV>(pend_dst, plane, pend_cols, pend);
             dev::tmem_wait_ld();
             DGRAD_TRACE_CLOCK(tl1);
             if (threadIdx.x == 0) DGRAD_TRACE_ADD(4, tl1 - tl0);
 #pragma unroll
             for (int v = 0; v < NV; ++v) {
                 const int sub = p.phase[ph0 + v].tap_count ? p.phase[ph0 + v].sub : 0;
-                float *xb = e.xbase + static_cast<size_t>((e.xcount & 1) * 4) * e.slots * 16;
-                float *xw = xb + e.ew * e.slots * 16;
-                const float *xn = e.ew < 3 ? xw + e.slots * 16 : nullptr;
-                if (sub == 0) {
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) pend[v][j] = 0.f;
-                } else if (sub == 1) {
-                    combine<1, SMAX>(r[v], pend[v], xw, xn, e.lane, e.bar_id);
-                } else {
-                    if constexpr (SMAX >= 2) {
-                        if (sub == 2) combine<2, SMAX>(r[v], pend[v], xw, xn, e.lane, e.bar_id);
+                for (int k = 0; k < K; ++k) {
+                    if (c0 + 16 * k >= p.bn) break;
+                    float *xb = e.xbase + static_cast<size_t>((e.xcount & 1) * 4) * e.slots * 16;
+                    float *xw = xb + e.ew * e.slots * 16;
+                    const float *xn = e.ew < 3 ? xw + e.slots * 16 : nullptr;
+                    if (sub == 0) {
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) pend[v][k][j] = 0.f;
+                    } else if (sub == 1) {
+                        combine<1, SMAX>(r[v][k], pend[v][k], xw, xn, e.lane, e.bar_id);
+                    } else {
+                        if constexpr (SMAX >= 2) {
+                            if (sub == 2) combine<2, SMAX>(r[v][k], pend[v][k], xw, xn, e.lane, e.bar_id);
+                        }
+                        if constexpr (SMAX >= 3) {
+                            if (sub == 3) combine<3, SMAX>(r[v][k], pend[v][k], xw, xn, e.lane, e.bar_id);
+                        }
+                        if constexpr (SMAX >= 4) {
+                            if (sub == 4) combine<4, SMAX>(r[v][k], pend[v][k], xw, xn, e.lane, e.bar_id);
+                        }
+                        ++e.xcount;
                     }
-                    if constexpr (SMAX >= 3) {
-                        if (sub == 3) combine<3, SMAX>(r[v], pend[v], xw, xn, e.lane, e.bar_id);
-                    }
-                    if constexpr (SMAX >= 4) {
-                        if (sub == 4) combine<4, SMAX>(r[v], pend[v], xw, xn, e.lane, e.bar_id);
-                    }
-                    ++e.xcount;
                 }
             }
             pend_dst = valid ? dst + static_cast<size_t>(c0) * plane : nullptr;
-            pend_cols = min(16, e.nci - c0);
+            pend_cols = min(CB, e.nci - c0);
         }
     }
 }
 
-template <int NV, int SMAX>
-__device__ __forceinline__ void epilogue_run(EpiCtx &e, int c_first, int c_step, uint64_t *acc_empty) {
-    float pend[NV][16];
+// A whole work unit for this warp: its tm blocks of 128 rows (one when
+// grouped), then the release of the accumulator set and the last stores.
+template <int NV, int SMAX, int CB>
+__device__ __forceinline__ void epilogue_run(EpiCtx &e, int tile, uint32_t tbase0, int m_cols, uint64_t *acc_empty) {
+    const MainParams &p = *e.p;
+    float pend[NV][CB / 16][16];
     float *pend_dst = nullptr;
     int pend_cols = 0;
-    epilogue_unit<NV, SMAX>(e, c_first, c_step, pend, pend_dst, pend_cols);
+    for (int m = 0; m < p.tm; ++m) {
+        const int o = m * kBlockM + e.ew * 32 + e.lane;   // row of the unit
+        const int P = tile * p.tile_step + o;
+        dev::decode_position(p, P, e.n, e.q, e.u);
+        e.row_ok = o < p.tile_step && P < p.positions;
+        e.tbase = tbase0 + static_cast<uint32_t>(m * m_cols);
+        epilogue_unit<NV, SMAX, CB>(e, pend, pend_dst, pend_cols);
+    }
     // Every value of the unit is in registers: release the accumulator set
     // to the MMA, then store the last batch.
     dev::tc_fence_before();
     dev::mbar_arrive(dev::smem_u32(acc_empty));
     DGRAD_TRACE_CLOCK(ts0);
-    if (pend_dst) store_batch<NV>(pend_dst, static_cast<size_t>(e.p->H) * e.p->W, pend_cols, pend);
+    if (pend_dst) store_batch<NV, CB>(pend_dst, static_cast<size_t>(p.H) * p.W, pend_cols, pend);
     DGRAD_TRACE_CLOCK(ts1);
     if (threadIdx.x == 0) DGRAD_TRACE_ADD(14, ts1 - ts0);
 }
 
-// kEpi selects the epilogue's store form (one instantiation each keeps the
-// register allocation of every form separate): 0 one phase at a time (up to
-// kMaxSub sub-accumulators), 1 two column phases together (stride 2, up to
-// two sub-accumulators), 2 four column phases together (stride 4).
-// Registers: each SM sub-partition holds a quarter of the register file and
-// a quarter of the block's warps (rounded up), so 10 warps leave 168 per
-// thread and 14 warps 128.
+// Epilogue forms, one kernel instantiation each (so that each form's
+// registers are allocated on their own): phases stored together (NV),
+// sub-accumulators per phase (SMAX) and columns per tensor-memory wait (CB),
+// at most 64 loaded registers per batch.
+template <int kEpi> struct EpiForm;
+template <> struct EpiForm<0> { static constexpr int NV = 1, SMAX = 1, CB = 64; };
+template <> struct EpiForm<1> { static constexpr int NV = 1, SMAX = 2, CB = 32; };
+template <> struct EpiForm<2> { static constexpr int NV = 1, SMAX = 3, CB = 16; };
+template <> struct EpiForm<3> { static constexpr int NV = 1, SMAX = 4, CB = 16; };
+template <> struct EpiForm<4> { static constexpr int NV = 2, SMAX = 1, CB = 32; };
+template <> struct EpiForm<5> { static constexpr int NV = 2, SMAX = 2, CB = 16; };
+template <> struct EpiForm<6> { static constexpr int NV = 4, SMAX = 1, CB = 16; };
+
+__host__ __device__ constexpr int epi_form(int vec_w, int s, int max_sub) {
+    return (vec_w && s == 4) ? 6
+         : (vec_w && s == 2) ? (max_sub <= 1 ? 4 : 5)
+         : (max_sub <= 1 ? 0 : max_sub == 2 ? 1 : max_sub == 3 ? 2 : 3);
+}
+
+// kEpi selects the epilogue form (EpiForm).  Registers: each SM sub-
+// partition holds a quarter of the register file and a quarter of the
+// block's warps (rounded up), so 6 warps leave 255 per thread and 14 warps
+// (producer mode) 128.
 template <int KC, bool kTmaA, int kEpi>
 __global__ void __launch_bounds__(kTmaA ? kThreadsTmaA : kThreads, 1)
     tc_dgrad_kernel(const __grid_constant__ MainParams p) {
@@ -737,31 +771,24 @@ __global__ void __launch_bounds__(kTmaA ? kThreadsTmaA : kThreads, 1)
         if (lane == 0) DGRAD_TRACE_ADD(11, t_mend - t_start);
     } else {
         // ------------------------------------------------------- epilogue
-        // Epilogue group eg (warps 0-3, and 6-9 in tensor-copy mode); warp
-        // ew = warp % 4 reads tensor-memory lanes 32*ew .. 32*ew+31.  With two
-        // groups, group g takes every other unit: those of accumulator set g.
-        const int eg = warp < kEpiWarps ? 0 : 1;
+        // Warp ew = warp % 4 reads tensor-memory lanes 32*ew .. 32*ew+31.  (A
+        // second group of four epilogue warps taking alternate units measured
+        // slower: ten warps leave 168 registers per thread, six leave 255.)
         const int ew = warp & 3;
-        const int n_groups = epi_groups(p, kTmaA);
         const int slots = p.max_sub * (p.max_sub - 1) / 2;
         EpiCtx e;
         e.p = &p;
-        e.xbase = xchg + static_cast<size_t>(eg) * 2 * 4 * slots * 16;
+        e.xbase = xchg;
         e.slots = slots;
         e.ew = ew;
         e.lane = lane;
-        e.bar_id = 1 + eg;
+        e.bar_id = 1;
         e.xcount = 0;
         Ring racc;
-        int i = 0;
-        for (int w = blockIdx.x; eg < n_groups && w < p.n_work; w += gridDim.x, ++i) {
-            if (n_groups == 2 && (i & 1) != eg) continue;
-            const int stage = n_groups == 2 ? eg : racc.stage;
+        for (int w = blockIdx.x; w < p.n_work; w += gridDim.x) {
+            const int stage = racc.stage;
             const uint32_t parity = racc.parity;
-            if (n_groups == 2)
-                racc.parity ^= 1;
-            else
-                racc.next(p.acc_bufs);
+            racc.next(p.acc_bufs);
             const int tile = w / p.n_slices, slice = w % p.n_slices;
             DGRAD_TRACE_CLOCK(te0);
             // All four warps of the group leave together or go on together.
@@ -775,30 +802,10 @@ __global__ void __launch_bounds__(kTmaA ? kThreadsTmaA : kThreads, 1)
             dev::tc_fence_after();
             e.ci0 = slice * p.bn;
             e.nci = min(p.bn, p.Ci - e.ci0);
-            // One 128-row block per unit when grouped (tm = 1); tm blocks otherwise.
-            for (int m = 0; m < p.tm; ++m) {
-                const int o = m * kBlockM + ew * 32 + lane;   // row of the unit
-                const int P = tile * tile_step + o;
-                dev::decode_position(p, P, e.n, e.q, e.u);
-                e.row_ok = o < tile_step && P < p.positions;
-                e.tbase = tmem_base + (static_cast<uint32_t>(ew * 32) << 16) +
-                          static_cast<uint32_t>(stage * p.acc_cols + m * m_cols);
-                const bool last = m + 1 == p.tm;
-                const int cf = 0, cs = 16;
-                if (!last) {
-                    // earlier blocks (ungrouped plans only): release nothing yet
-                    float pend[1][16];
-                    float *pd = nullptr;
-                    int pc = 0;
-                    epilogue_unit<1, 1>(e, cf, cs, pend, pd, pc);
-                    if (pd) store_batch<1>(pd, static_cast<size_t>(p.H) * p.W, pc, pend);
-                } else {
-                    // NV column phases stored together, up to SMAX sub-accumulators per phase
-                    constexpr int NV = kEpi == 2 ? 4 : (kEpi == 1 ? 2 : 1);
-                    constexpr int SMAX = kEpi == 2 ? 1 : (kEpi == 1 ? 2 : kMaxSub);
-                    epilogue_run<NV, SMAX>(e, cf, cs, &bars->acc_empty[stage]);
-                }
-            }
+            using F = EpiForm<kEpi>;
+            const uint32_t tbase0 =
+                tmem_base + (static_cast<uint32_t>(ew * 32) << 16) + static_cast<uint32_t>(stage * p.acc_cols);
+            epilogue_run<F::NV, F::SMAX, F::CB>(e, tile, tbase0, m_cols, &bars->acc_empty[stage]);
             DGRAD_TRACE_CLOCK(te2);
             if (threadIdx.x == 0) DGRAD_TRACE_ADD(7, te2 - te1);
         }
@@ -832,9 +839,15 @@ cudaError_t launch_kc(const MainParams &p, const Tiling &t, cudaStream_t stream,
 
 template <bool kTmaA>
 cudaError_t launch_mode(const MainParams &p, const Tiling &t, cudaStream_t stream, bool pdl) {
-    if (p.vec_w && p.s == 4) return launch_kc<32, kTmaA, 2>(p, t, stream, pdl);
-    if (p.vec_w && p.s == 2) return launch_kc<32, kTmaA, 1>(p, t, stream, pdl);
-    return launch_kc<32, kTmaA, 0>(p, t, stream, pdl);
+    switch (epi_form(p.vec_w, p.s, p.max_sub)) {
+        case 0: return launch_kc<32, kTmaA, 0>(p, t, stream, pdl);
+        case 1: return launch_kc<32, kTmaA, 1>(p, t, stream, pdl);
+        case 2: return launch_kc<32, kTmaA, 2>(p, t, stream, pdl);
+        case 3: return launch_kc<32, kTmaA, 3>(p, t, stream, pdl);
+        case 4: return launch_kc<32, kTmaA, 4>(p, t, stream, pdl);
+        case 5: return launch_kc<32, kTmaA, 5>(p, t, stream, pdl);
+        default: return launch_kc<32, kTmaA, 6>(p, t, stream, pdl);
+    }
 }
 
 }  // namespace

@@ -240,12 +240,11 @@ def test_emulated_grouped_taps_match_oracle(shape):
 
 def test_grouping_plans():
     r = dg.describe(*WORKLOADS["resnet_stage"].plan_args(), precision="tf32")
-    assert r["group_taps"] == 1 and r["tile_step"] == 126 and r["tmem_cols"] == 512
-    assert dg.describe(*WORKLOADS["pointwise"].plan_args(), precision="tf32")["group_taps"] == 0
-    st = dg.describe(*WORKLOADS["stem"].plan_args(), precision="tf32")
+    assert r["group_taps"] == 0 and r["tile_step"] == 128 * r["tile_blocks"]   # opt-in
+    on = dg.describe(*WORKLOADS["resnet_stage"].plan_args(), precision="tf32", group_taps="on")
+    assert on["group_taps"] == 1 and on["tile_step"] == 126 and on["tmem_cols"] == 512
+    st = dg.describe(*WORKLOADS["stem"].plan_args(), precision="tf32", group_taps="on")
     assert st["group_taps"] == 1 and st["tile_step"] == 125
-    off = dg.describe(*WORKLOADS["resnet_stage"].plan_args(), precision="tf32", group_taps="off")
-    assert off["group_taps"] == 0 and off["tile_step"] == 128 * off["tile_blocks"]
     with pytest.raises(dg.DgradError) as e:    # 5 taps per row cannot share one MMA
         dg.describe(2, 16, 16, 16, 16, 5, 5, 1, 2, 2, precision="tf32", group_taps="on")
     assert e.value.status == 2
