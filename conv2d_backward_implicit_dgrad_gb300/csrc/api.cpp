@@ -107,8 +107,10 @@ void fill_params(dgrad_plan_s *pl) {
     f.co_v = t.co_v;
     f.round_tf32 = round;
     f.positions = (int)g.positions;
-    f.pos_tiles = (int)((g.positions + dgrad::kFramePackCols - 1) / dgrad::kFramePackCols);
-    f.c_groups = (t.co_v + 31) / 32;
+    f.tile_c = t.co_v >= 128 ? 128 : (t.co_v > 32 ? 64 : 32);
+    const int tile_p = dgrad::kFrameTileElems / f.tile_c;
+    f.pos_tiles = (int)((g.positions + tile_p - 1) / tile_p);
+    f.c_groups = (t.co_v + f.tile_c - 1) / f.tile_c;
 }
 
 // cuTensorMapEncodeTiled from the driver, looked up once through the

@@ -167,10 +167,11 @@ struct FramePackParams {
     int co_v;
     int round_tf32;
     int positions;     // N * Hv * Wp
-    int pos_tiles;     // ceil(positions / kFramePackCols)
-    int c_groups;      // ceil(co_v / 32)
+    int tile_c;        // channels per pack tile: 32, 64 or 128
+    int pos_tiles;     // ceil(positions / (kFrameTileElems / tile_c))
+    int c_groups;      // ceil(co_v / tile_c)
 };
-constexpr int kFramePackCols = 128;
+constexpr int kFrameTileElems = 4096;   // elements of one pack tile (tile_c channels x positions)
 
 // Main-kernel MMA group entry: A window offset (bytes), accumulator column
 // (bit 31: first group of its phase), B offset inside the chunk's tap block

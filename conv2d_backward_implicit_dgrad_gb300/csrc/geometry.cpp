@@ -324,10 +324,30 @@ dgrad_status_t choose_tiling(const Geometry &g, int precision, const dgrad_optio
     int bn_cap = std::min(256, (kTmemCols / g.n_phases) / 16 * 16);
     int bn = std::min(ci16, bn_cap);
     int tiles1 = (int)((g.positions + kBlockM - 1) / kBlockM);
-    // Split the channels when the position tiles alone cannot fill the GPU.
-    while (!o.slice_n && bn > 64 && (long long)tiles1 * ceil_div(g.Ci, bn) < sm_count &&
-           (bn / 2) % 16 == 0)
-        bn /= 2;
+    // Slice width: the fewest waves of work units times the cost of one unit,
+    // counted in shared-memory cycles (the operand port moves 128 B/clk; an
+    // MMA of N columns takes max(N/2, its operand bytes / 128) cycles per K
+    // step of 8, and the tensor copies of A and streamed B add their bytes).
+    if (!o.slice_n) {
+        const int taps = std::max(1, g.n_taps);
+        const double a_band = (double)(kBlockM + g.max_shift) * 128.0;
+        double best = 1e300;
+        int best_bn = bn;
+        for (int cand = bn; cand >= 16 && cand % 16 == 0; cand /= 2) {
+            const int slices = ceil_div(g.Ci, cand);
+            const long long units = (long long)tiles1 * slices;
+            const long long waves = (units + sm_count - 1) / sm_count;
+            const double mma = taps * 4.0 * std::max(cand / 2.0, (4096.0 + cand * 32.0) / 128.0);
+            const bool resident = slices == 1 && (double)ceil_div(g.Co, 32) * taps * cand * 128.0 <= 150.0 * 1024;
+            const double copies = (a_band + (resident ? 0.0 : taps * cand * 128.0)) / 128.0;
+            const double cost = (double)waves * ceil_div(g.Co, 32) * (mma + copies);
+            if (cost < best * 0.98) {
+                best = cost;
+                best_bn = cand;
+            }
+        }
+        bn = best_bn;
+    }
     if (o.slice_n) bn = o.slice_n;
     if (g.n_phases * bn > kTmemCols) return DGRAD_ERR_UNSUPPORTED;
 

@@ -8,10 +8,10 @@
 //     index) by one pass that writes each (slice, chunk) block contiguously,
 //     keeps only the taps each phase uses, zero-pads channels, and (TF32
 //     precision) rounds to TF32 once.
-// (b) grad_out NCHW -> V[P][k] (FramePackParams): one block transposes
-//     kFramePackCols consecutive frame positions x 32 channels through shared
-//     memory, so both the grad_out reads (along positions) and the V writes
-//     (128-byte rows of 32 channels) are coalesced.  Frame positions
+// (b) grad_out NCHW -> V[P][k] (FramePackParams): one block transposes a
+//     tile of kFrameTileElems (consecutive frame positions x 32, 64 or 128
+//     channels) through shared memory, so both the grad_out reads (along
+//     positions) and the V writes (along channels) are coalesced.  Frame positions
 //     outside grad_out, and channels >= Co, are written as zeros; the
 //     meganeura shader's transposed padding becomes these zero rows.
 #include <cuda_runtime.h>
@@ -24,7 +24,7 @@ namespace dgrad {
 namespace {
 
 constexpr int kThreads = 256;
-static_assert(kThreads % kFramePackCols == 0 && 32 % (kThreads / kFramePackCols) == 0, "frame tile split");
+static_assert(kFrameTileElems % kThreads == 0 && kFrameTileElems / 128 <= kThreads, "frame tile split");
 constexpr int kMaxPrepackBlocks = 1024;
 
 struct PackArgs {
@@ -68,15 +68,20 @@ __device__ void pack_weights(const PrepackParams &p, int block, int nblocks) {
     }
 }
 
-__device__ void pack_frame(const FramePackParams &p, int block, float (*tile)[kFramePackCols + 1], int *off) {
-    // block -> (tile of kFramePackCols consecutive frame positions, group of
-    // 32 channels); position tiles vary fastest so neighbouring blocks read
-    // neighbouring grad_out runs.
+// One frame tile of TP = kFrameTileElems / TC consecutive positions x TC
+// channels.  block -> (position tile, channel group); position tiles vary
+// fastest so neighbouring blocks read neighbouring grad_out runs.  Wide
+// frames (many channels per position) take wide channel groups, so each
+// position's row segment written is TC * 4 bytes long.
+template <int TC>
+__device__ void pack_frame(const FramePackParams &p, int block, float *tile, int *off) {
+    constexpr int TP = kFrameTileElems / TC;
+    constexpr int kStride = TP + 1;
     const int pt = block % p.pos_tiles;
-    const int co0 = (block / p.pos_tiles) * 32;
-    const int P0 = pt * kFramePackCols;
+    const int co0 = (block / p.pos_tiles) * TC;
+    const int P0 = pt * TP;
     const int plane = p.oH * p.oW;
-    if (threadIdx.x < kFramePackCols) {   // grad_out offset of channel 0 at each position, or -1
+    if (threadIdx.x < TP) {   // grad_out offset of channel 0 at each position, or -1
         const int P = P0 + threadIdx.x;
         int o = -1;
         if (P < p.positions) {
@@ -89,14 +94,14 @@ __device__ void pack_frame(const FramePackParams &p, int block, float (*tile)[kF
         off[threadIdx.x] = o;
     }
     __syncthreads();
-    // read: 32 channels x kFramePackCols positions, coalesced along positions.
-    // Each thread keeps one position and issues all of its channel loads
-    // before the first shared-memory store, so they are in flight together.
+    // read: TC channels x TP positions, coalesced along positions.  Each
+    // thread keeps one position and issues all of its channel loads before
+    // the first shared-memory store, so they are in flight together.
     {
-        constexpr int kRowsPerPass = kThreads / kFramePackCols;
-        constexpr int kLoads = 32 / kRowsPerPass;
-        const int xi = threadIdx.x % kFramePackCols;
-        const int c0 = threadIdx.x / kFramePackCols;
+        constexpr int kRowsPerPass = kThreads / TP;
+        constexpr int kLoads = TC / kRowsPerPass;
+        const int xi = threadIdx.x % TP;
+        const int c0 = threadIdx.x / TP;
         const int o = off[xi];
         float v[kLoads];
 #pragma unroll
@@ -105,16 +110,17 @@ __device__ void pack_frame(const FramePackParams &p, int block, float (*tile)[kF
             v[k] = (o >= 0 && co < p.Co) ? __ldg(p.go + static_cast<size_t>(o) + static_cast<size_t>(co) * plane) : 0.f;
         }
 #pragma unroll
-        for (int k = 0; k < kLoads; ++k) tile[c0 + kRowsPerPass * k][xi] = p.round_tf32 ? dev::round_tf32(v[k]) : v[k];
+        for (int k = 0; k < kLoads; ++k)
+            tile[(c0 + kRowsPerPass * k) * kStride + xi] = p.round_tf32 ? dev::round_tf32(v[k]) : v[k];
     }
     __syncthreads();
-    // write: rows of 32 channels (128 bytes), coalesced along channels
-    const int ncols = min(kFramePackCols, p.positions - P0);
-    const int cmax = min(32, p.co_v - co0);
+    // write: each position's TC channels (TC * 4 contiguous bytes), coalesced along channels
+    const int ncols = min(TP, p.positions - P0);
+    const int cmax = min(TC, p.co_v - co0);
     float *dst = p.v + static_cast<size_t>(P0) * p.co_v + co0;
-    for (int i = threadIdx.x; i < 32 * ncols; i += kThreads) {
-        const int xi = i / 32, c = i % 32;
-        if (c < cmax) dst[static_cast<size_t>(xi) * p.co_v + c] = tile[c][xi];
+    for (int i = threadIdx.x; i < TC * ncols; i += kThreads) {
+        const int xi = i / TC, c = i % TC;
+        if (c < cmax) dst[static_cast<size_t>(xi) * p.co_v + c] = tile[c * kStride + xi];
     }
 }
 
@@ -122,12 +128,19 @@ __global__ void __launch_bounds__(kThreads) pack_kernel(const __grid_constant__ 
     // Let the main kernel start its prologue while this grid runs; it reads
     // what this grid writes only after griddepcontrol.wait.
     dev::grid_launch_dependents();
-    __shared__ float tile[32][kFramePackCols + 1];
-    __shared__ int off[kFramePackCols];
-    if (static_cast<int>(blockIdx.x) < a.w_blocks)
+    __shared__ float tile[kFrameTileElems + 128];   // TC x (TP + 1) = kFrameTileElems + TC floats, TC <= 128
+    __shared__ int off[kFrameTileElems / 32];
+    if (static_cast<int>(blockIdx.x) < a.w_blocks) {
         pack_weights(a.w, blockIdx.x, a.w_blocks);
-    else
-        pack_frame(a.f, blockIdx.x - a.w_blocks, tile, off);
+    } else {
+        const int b = blockIdx.x - a.w_blocks;
+        if (a.f.tile_c == 128)
+            pack_frame<128>(a.f, b, tile, off);
+        else if (a.f.tile_c == 64)
+            pack_frame<64>(a.f, b, tile, off);
+        else
+            pack_frame<32>(a.f, b, tile, off);
+    }
 }
 
 }  // namespace
@@ -141,7 +154,7 @@ cudaError_t launch_pack(const PrepackParams *pp, const FramePackParams *fp, cuda
     }
     if (fp) {
         a.f = *fp;
-        a.f_blocks = fp->pos_tiles * fp->c_groups;
+        a.f_blocks = fp->pos_tiles * fp->c_groups;   // c_groups = ceil(co_v / tile_c)
     }
     const int blocks = a.w_blocks + a.f_blocks;
     if (blocks == 0) return cudaSuccess;
