@@ -119,7 +119,7 @@ A_SOURCE = {"auto": 0, "frame": 1, "producers": 2}
 A_SOURCE_NAME = {v: k for k, v in A_SOURCE.items()}
 
 
-GROUP_TAPS = {"auto": 0, "on": 1, "off": 2}
+GROUP_TAPS = {"auto": 0, "on": 1, "rows": 1, "off": 2, "phases": 3}
 
 
 def _options(path="auto", tile_blocks=0, slice_n=0, chunk_k=0, grid=0, sm_count=0, a_source="auto",

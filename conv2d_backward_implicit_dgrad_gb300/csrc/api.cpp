@@ -72,7 +72,7 @@ void fill_info(const Geometry &g, const Tiling &t, int precision, size_t ws, dgr
     info->a_source = t.path == DGRAD_PATH_TCGEN05 ? (t.a_tma ? 1 : 2) : 0;
     info->smem_bytes = t.smem_bytes;
     info->tmem_cols = t.tmem_cols;
-    info->group_taps = t.grouped;
+    info->group_taps = t.grouped ? 1 : (t.pgroup ? 2 : 0);
     info->tile_step = t.tile_step;
     info->workspace_bytes = ws;
     info->packed_weight_bytes = t.packed_bytes;

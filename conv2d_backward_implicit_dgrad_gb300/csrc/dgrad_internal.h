@@ -76,16 +76,31 @@ struct Geometry {
 dgrad_status_t make_geometry(int N, int Ci, int H, int W, int Co, int kH, int kW,
                              int stride, int pad_h, int pad_w, Geometry *g);
 
-// One tcgen05 MMA group: `ntaps` consecutive taps of one kernel row of one
-// phase, issued as one MMA of N = ntaps * bn whose A window starts at the
-// row's smallest shift.  Sub-accumulator j (columns j*bn ..) then holds the
-// tap with shift a_shift + (ntaps - 1 - j), i.e. the output position that
-// many rows further down; the epilogue shifts it back.  Ungrouped, every tap
-// is its own group.
+// One tcgen05 MMA group: `ntaps` taps issued as one MMA of N = ntaps * bn
+// over one A window (start row a_shift), writing accumulator columns from
+// col * bn on.  Taps are counted in the packing order of the weights (tap0 is
+// a position in that order; the group's taps are consecutive there).  Forms:
+//  - one tap per group (col = its phase);
+//  - kernel-row groups (`grouped`): the taps of one kernel row of one phase;
+//    sub-accumulator j holds the tap with shift a_shift + (ntaps - 1 - j),
+//    i.e. the output position that many rows further down, and the epilogue
+//    shifts it back;
+//  - shared-shift groups (`pgroup`, stride > 1): the taps of different phases
+//    with the same frame shift; each phase keeps its own accumulator, the
+//    phases sit in tensor memory in an order that makes every group's phases
+//    adjacent, and the first group holds a tap of every phase (it starts
+//    every accumulator).
+// `first`: the group starts its accumulator columns (accumulate = 0 on the
+// first K step of the first chunk).
 struct MGroup {
-    int phase, tap0, ntaps, a_shift, first;
+    int col, tap0, ntaps, a_shift, first;
 };
-int build_mgroups(const Geometry &g, int grouped, MGroup *out);
+struct Tiling;
+// Groups of a plan, the packing order of the taps (perm[i] = geometry tap at
+// packing position i) and each phase's accumulator column in units of bn
+// (phase_units).  Returns the group count, or -1 when the plan's grouping
+// form cannot be built for this geometry.
+int build_mgroups(const Geometry &g, const Tiling &t, MGroup *out, int *perm, int *phase_units);
 
 // Tiling of the main kernel.
 struct Tiling {
@@ -105,6 +120,7 @@ struct Tiling {
     int n_tgroups;     // B stages per channel chunk
     int chunk_bytes;   // bytes of one B stage (tap_group taps)
     int grouped;       // 1: taps of a kernel row share one MMA (MGroup)
+    int pgroup;        // 1: taps of different phases with the same shift share one MMA (MGroup)
     int tile_step;     // output positions per tile (tm*128, less the rows a grouped MMA cannot finish)
     int n_mgroups;
     int bg_first[kMaxTaps + 1];   // B stage i holds MMA groups [bg_first[i], bg_first[i+1])

@@ -130,19 +130,95 @@ dgrad_status_t make_geometry(int N, int Ci, int H, int W, int Co, int kH, int kW
     return DGRAD_OK;
 }
 
-int build_mgroups(const Geometry &g, int grouped, MGroup *out) {
+int build_mgroups(const Geometry &g, const Tiling &t, MGroup *out, int *perm, int *phase_units) {
     int n = 0;
-    for (int ph = 0; ph < g.n_phases; ++ph) {
-        const PhaseDesc &pd = g.phase[ph];
-        const int step = grouped ? pd.row_len : 1;
-        for (int t = pd.tap_begin; t < pd.tap_begin + pd.tap_count; t += step) {
-            MGroup &m = out[n++];
-            m.phase = ph;
-            m.tap0 = t;
-            m.ntaps = step;
-            m.a_shift = g.tap[t + step - 1].shift;   // the row's last tap has the smallest column offset
-            m.first = t == pd.tap_begin ? 1 : 0;
+    if (!t.pgroup) {
+        int units = 0;
+        for (int ph = 0; ph < g.n_phases; ++ph) {
+            const PhaseDesc &pd = g.phase[ph];
+            phase_units[ph] = units;
+            const int step = t.grouped ? std::max(1, pd.row_len) : 1;
+            units += t.grouped ? pd.row_len : 1;
+            for (int tp = pd.tap_begin; tp < pd.tap_begin + pd.tap_count; tp += step) {
+                MGroup &m = out[n++];
+                m.col = phase_units[ph];
+                m.tap0 = tp;
+                m.ntaps = step;
+                m.a_shift = g.tap[tp + step - 1].shift;   // a row's last tap has the smallest column offset
+                m.first = tp == pd.tap_begin ? 1 : 0;
+            }
         }
+        for (int i = 0; i < g.n_taps; ++i) perm[i] = i;
+        return n;
+    }
+    // Shared-shift groups.  Phases with taps, and for every shift the set of
+    // phases that have a tap with it (a phase has at most one tap per shift).
+    int q[kMaxPhases], nq = 0;
+    for (int ph = 0; ph < g.n_phases; ++ph)
+        if (g.phase[ph].tap_count > 0) q[nq++] = ph;
+    if (nq < 2 || nq > 4) return -1;
+    int shifts[kMaxTaps], nsh = 0;
+    unsigned masks[kMaxTaps];
+    for (int i = 0; i < g.n_taps; ++i) {
+        int k = 0;
+        while (k < nsh && shifts[k] != g.tap[i].shift) ++k;
+        if (k == nsh) {
+            shifts[nsh] = g.tap[i].shift;
+            masks[nsh++] = 0;
+        }
+        masks[k] |= 1u << g.tap[i].phase;
+    }
+    unsigned all = 0;
+    for (int i = 0; i < nq; ++i) all |= 1u << q[i];
+    int lead = -1;   // a shift that every phase has: the first group
+    for (int k = 0; k < nsh && lead < 0; ++k)
+        if (masks[k] == all) lead = k;
+    if (lead < 0) return -1;
+    // An order of the phases in tensor memory that makes every group contiguous.
+    int order[4] = {0, 1, 2, 3};
+    bool found = false;
+    do {
+        int pos[kMaxPhases];
+        for (int i = 0; i < nq; ++i) pos[q[order[i]]] = i;
+        bool ok = true;
+        for (int k = 0; k < nsh && ok; ++k) {
+            int lo = nq, hi = -1, cnt = 0;
+            for (int i = 0; i < nq; ++i)
+                if (masks[k] & (1u << q[i])) {
+                    lo = std::min(lo, pos[q[i]]);
+                    hi = std::max(hi, pos[q[i]]);
+                    ++cnt;
+                }
+            ok = hi - lo + 1 == cnt;
+        }
+        found = ok;
+    } while (!found && std::next_permutation(order, order + nq));
+    if (!found) return -1;
+    for (int ph = 0; ph < g.n_phases; ++ph) phase_units[ph] = 0;   // phases without taps: never read
+    for (int i = 0; i < nq; ++i) phase_units[q[order[i]]] = i;
+    // Groups: the lead shift first, then the others by falling size; taps of
+    // a group in tensor-memory order of their phases.
+    int gorder[kMaxTaps], ng = 0;
+    gorder[ng++] = lead;
+    for (int c = nq; c >= 1; --c)
+        for (int k = 0; k < nsh; ++k)
+            if (k != lead && __builtin_popcount(masks[k]) == c) gorder[ng++] = k;
+    int np = 0;
+    for (int gi = 0; gi < ng; ++gi) {
+        const int k = gorder[gi];
+        MGroup &m = out[n++];
+        m.tap0 = np;
+        m.a_shift = shifts[k];
+        m.first = gi == 0 ? 1 : 0;
+        m.col = nq;
+        for (int i = 0; i < nq; ++i) {   // phases in tensor-memory order
+            const int ph = q[order[i]];
+            if (!(masks[k] & (1u << ph))) continue;
+            m.col = std::min(m.col, i);
+            for (int tp = g.phase[ph].tap_begin; tp < g.phase[ph].tap_begin + g.phase[ph].tap_count; ++tp)
+                if (g.tap[tp].shift == shifts[k]) perm[np++] = tp;
+        }
+        m.ntaps = np - m.tap0;
     }
     return n;
 }
@@ -200,11 +276,14 @@ bool size_tc(const Geometry &g, Tiling &t, int want_resident) {
     t.n_slices = ceil_div(g.Ci, t.bn);
     t.n_chunks = ceil_div(g.Co, t.kc);
     MGroup mg[kMaxTaps];
-    t.n_mgroups = build_mgroups(g, t.grouped, mg);
+    int perm[kMaxTaps], units[kMaxPhases];
+    t.n_mgroups = build_mgroups(g, t, mg, perm, units);
+    if (t.n_mgroups < 0) return false;
+    for (int i = 0; i < t.n_mgroups; ++i)
+        if (mg[i].ntaps * t.bn > 256) return false;   // MMA N limit
     int max_sub = 1, sub_cols = 0;
     for (int p = 0; p < g.n_phases; ++p) {
         const int sub = t.grouped ? g.phase[p].row_len : 1;
-        if (sub * t.bn > 256) return false;   // MMA N limit
         max_sub = std::max(max_sub, sub);
         sub_cols += sub * t.bn;
     }
@@ -381,19 +460,29 @@ dgrad_status_t choose_tiling(const Geometry &g, int precision, const dgrad_optio
     // its operand reads (bn < 128), but triples the epilogue's tensor-memory
     // reads and adds its row shifts; measured, the epilogue then bounds the
     // kernel and the grouped plans ran slower, so grouping is opt-in.
-    if (o.group_taps < 0 || o.group_taps > 2) return DGRAD_ERR_INVALID_ARG;
-    int group_pref[1] = {0};
-    const int n_group = 1;
+    // Taps of different phases with the same frame shift share one MMA
+    // whenever the phases can be ordered in tensor memory for it (stride-2
+    // shapes): fewer, wider MMAs, each phase still its own accumulator, so
+    // the epilogue is unchanged.  That is the automatic choice.
+    if (o.group_taps < 0 || o.group_taps > 3) return DGRAD_ERR_INVALID_ARG;
+    int group_pref[2][2];   // (kernel-row groups, shared-shift groups) in order of preference
+    int n_group = 0;
     if (o.group_taps == 1) {
         if (o.tile_blocks > 1) return DGRAD_ERR_UNSUPPORTED;   // grouped MMAs take one 128-row block per unit
-        group_pref[0] = 1;
+        group_pref[n_group][0] = 1, group_pref[n_group++][1] = 0;
+    } else if (o.group_taps == 3) {
+        group_pref[n_group][0] = 0, group_pref[n_group++][1] = 1;
+    } else {
+        if (o.group_taps == 0 && g.n_phases > 1) group_pref[n_group][0] = 0, group_pref[n_group++][1] = 1;
+        group_pref[n_group][0] = 0, group_pref[n_group++][1] = 0;
     }
     bool ok = false;
     for (int gi = 0; gi < n_group && !ok; ++gi) {
         for (int want_res = 1; want_res >= 0 && !ok; --want_res) {
             for (int i = 0; i < n_tm && !ok; ++i) {
                 Tiling c = t;
-                c.grouped = group_pref[gi];
+                c.grouped = group_pref[gi][0];
+                c.pgroup = group_pref[gi][1];
                 c.tm = c.grouped ? 1 : tm_pref[i];
                 c.bn = bn;
                 c.kc = 32;
@@ -431,13 +520,14 @@ void fill_main_params(const Geometry &g, const Tiling &t, int round_tf32, MainPa
     m.tile_step = t.tile_step;
     m.grouped = t.grouped;
     m.xchg_bytes = t.xchg_bytes;
-    int col = 0;
+    MGroup mg[kMaxTaps];
+    int perm[kMaxTaps], units[kMaxPhases];
+    const int n_mg = t.path == DGRAD_PATH_TCGEN05 ? build_mgroups(g, t, mg, perm, units) : 0;
     m.max_sub = 1;
     for (int i = 0; i < g.n_phases; ++i) {
         m.phase[i] = g.phase[i];
         m.phase[i].sub = t.grouped ? g.phase[i].row_len : 1;
-        m.phase[i].col = col;
-        col += m.phase[i].sub * t.bn;
+        m.phase[i].col = t.path == DGRAD_PATH_TCGEN05 ? units[i] * t.bn : i * t.bn;
         m.max_sub = std::max(m.max_sub, m.phase[i].sub);
     }
     // The epilogue stores the s column phases of a row phase together when
@@ -447,13 +537,11 @@ void fill_main_params(const Geometry &g, const Tiling &t, int round_tf32, MainPa
                g.n_phases == g.s * g.s && g.s * m.max_sub <= 4) ? 1 : 0;
     for (int i = 0; i < g.n_taps; ++i) m.tap[i] = g.tap[i];
     if (t.path == DGRAD_PATH_TCGEN05) {
-        MGroup mg[kMaxTaps];
-        m.n_mgroups = build_mgroups(g, t.grouped, mg);
+        m.n_mgroups = n_mg;
         const uint32_t tap_b = (uint32_t)t.bn * 128u;   // bytes of one tap of one chunk of B
         for (int i = 0; i < m.n_mgroups; ++i) {
-            const PhaseDesc &pd = m.phase[mg[i].phase];
             m.mgroup[i].x = (uint32_t)mg[i].a_shift * 128u;
-            m.mgroup[i].y = (uint32_t)pd.col | (mg[i].first ? 0x80000000u : 0u);
+            m.mgroup[i].y = (uint32_t)(mg[i].col * t.bn) | (mg[i].first ? 0x80000000u : 0u);
             m.mgroup[i].z = (uint32_t)mg[i].tap0 * tap_b;
             m.mgroup[i].w = tf32_idesc(kBlockM, mg[i].ntaps * t.bn);
         }
@@ -472,9 +560,14 @@ void fill_prepack_params(const Geometry &g, const Tiling &t, int round_tf32, Pre
     q.round_tf32 = round_tf32;
     q.layout = t.path == DGRAD_PATH_TCGEN05 ? 1 : 0;
     q.total = (long long)(t.packed_bytes / 4);
+    // tcgen05 path: taps in the packing order of the plan's MMA groups
+    MGroup mg[kMaxTaps];
+    int perm[kMaxTaps], units[kMaxPhases];
+    if (t.path != DGRAD_PATH_TCGEN05 || build_mgroups(g, t, mg, perm, units) < 0)
+        for (int i = 0; i < g.n_taps; ++i) perm[i] = i;
     for (int i = 0; i < g.n_taps; ++i) {
-        q.tap_kh[i] = g.tap[i].kh;
-        q.tap_kw[i] = g.tap[i].kw;
+        q.tap_kh[i] = g.tap[perm[i]].kh;
+        q.tap_kw[i] = g.tap[perm[i]].kw;
     }
 }
 

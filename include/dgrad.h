@@ -88,8 +88,11 @@ typedef struct {
     int sm_count;      /* dgrad_describe only: SM count to plan for */
     int a_source;      /* tcgen05 path, how grad_out reaches the MMA: 0 automatic, 1 packed frame + tensor
                           copies (workspace holds a channels-last copy of grad_out), 2 producer warps */
-    int group_taps;    /* tcgen05 path: 0 automatic, 1 the taps of one kernel row share one MMA
-                          (N = taps x slice_n; DGRAD_ERR_UNSUPPORTED when that cannot fit), 2 never */
+    int group_taps;    /* tcgen05 path, taps issued as one MMA: 0 automatic (3 where it applies, else
+                          none), 1 the taps of one kernel row (N = taps x slice_n, sub-accumulators
+                          summed with row shifts by the epilogue; DGRAD_ERR_UNSUPPORTED when that
+                          cannot fit), 2 none, 3 the taps of different sub-pixel phases that read the
+                          same frame shift (stride > 1; DGRAD_ERR_UNSUPPORTED when not possible) */
 } dgrad_options_t;
 
 /* Everything a plan decided, for tests, benchmarks and logs. */
@@ -110,7 +113,7 @@ typedef struct {
     int a_source;          /* 1: packed frame + tensor copies, 2: producer warps (tcgen05 path) */
     int smem_bytes;        /* dynamic shared memory of the main kernel */
     int tmem_cols;         /* tensor-memory columns allocated per CTA (tcgen05 path) */
-    int group_taps;        /* 1: one MMA per kernel row of taps (tcgen05 path) */
+    int group_taps;        /* tcgen05 path: 0 one MMA per tap, 1 per kernel row of taps, 2 per shared shift */
     int tile_step;         /* output positions per work-unit tile */
     size_t workspace_bytes;/* device workspace owned by the plan */
     size_t packed_weight_bytes;

@@ -115,6 +115,8 @@ TILINGS = [
     dict(tile_blocks=3, grid=2), dict(tile_blocks=4, grid=1), dict(tile_blocks=4, slice_n=16, grid=2),
     dict(group_taps="on", grid=3), dict(group_taps="on", slice_n=16, grid=5), dict(group_taps="on", grid=1),
     dict(group_taps="off", grid=3), dict(group_taps="on", slice_n=32),
+    dict(group_taps="phases", grid=3), dict(group_taps="phases", tile_blocks=2, grid=2),
+    dict(group_taps="phases", slice_n=16, grid=5),
 ]
 
 
@@ -137,7 +139,7 @@ def test_tc_tilings(shape, opts, a_source):
         if k in opts:
             assert info[k] == opts[k]
     if "group_taps" in opts:
-        assert info["group_taps"] == (1 if opts["group_taps"] == "on" else 0)
+        assert info["group_taps"] == {"on": 1, "off": 0, "phases": 2}[opts["group_taps"]]
 
 
 @pytest.mark.parametrize("opts", [dict(slice_n=16), dict(slice_n=32, chunk_k=8), dict(chunk_k=32)])
@@ -165,7 +167,7 @@ def test_edge_shapes_both_sources(shape, a_source):
     assert info["a_source"] == a_source
 
 
-@pytest.mark.parametrize("group_taps", ["on", "off"])
+@pytest.mark.parametrize("group_taps", ["on", "off", "phases"])
 @pytest.mark.parametrize("shape", EDGE)
 def test_edge_shapes_grouped_and_not(shape, group_taps):
     N, Ci, Co, H, W, kH, kW, s, ph, pw = shape
@@ -177,7 +179,7 @@ def test_edge_shapes_grouped_and_not(shape, group_taps):
         raise
     go, w = make_tensors((N, Co, out_ext(H, kH, s, ph), out_ext(W, kW, s, pw)), (Co, Ci, kH, kW), 74, "uniform")
     info = check((N, Ci, H, W, Co, kH, kW, s, ph, pw), go, w, "tf32", group_taps=group_taps)
-    assert info["group_taps"] == (1 if group_taps == "on" else 0)
+    assert info["group_taps"] == {"on": 1, "off": 0, "phases": 2}[group_taps]
 
 
 # ----------------------------------------------------------------- semantics

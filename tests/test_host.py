@@ -248,3 +248,15 @@ def test_grouping_plans():
     with pytest.raises(dg.DgradError) as e:    # 5 taps per row cannot share one MMA
         dg.describe(2, 16, 16, 16, 16, 5, 5, 1, 2, 2, precision="tf32", group_taps="on")
     assert e.value.status == 2
+
+
+def test_shared_shift_plans():
+    st = dg.describe(*WORKLOADS["strided_downsample"].plan_args(), precision="tf32")
+    assert st["group_taps"] == 2                       # automatic for stride 2
+    off = dg.describe(*WORKLOADS["strided_downsample"].plan_args(), precision="tf32", group_taps="off")
+    assert off["group_taps"] == 0 and off["packed_weight_bytes"] == st["packed_weight_bytes"]
+    for bad in [(2, 8, 8, 8, 8, 3, 3, 1, 1, 1),        # one phase: nothing to share
+                (1, 20, 40, 40, 40, 3, 3, 4, 1, 1)]:   # sixteen phases
+        with pytest.raises(dg.DgradError) as e:
+            dg.describe(*bad, precision="tf32", group_taps="phases")
+        assert e.value.status == 2
