@@ -28,7 +28,7 @@ PATH_NAME = {v: k for k, v in PATH.items()}
 
 # Every function declared in include/dgrad.h (checked by the CPU tests).
 EXPORTS = ("dgrad_plan", "dgrad_plan_ex", "dgrad_describe", "dgrad_describe_taps", "dgrad_plan_info", "dgrad_run",
-           "dgrad_prepack", "dgrad_run_packed", "dgrad_pack_grad_out", "dgrad_run_main", "dgrad_run_host", "dgrad_run_noalloc", "dgrad_plan_check",
+           "dgrad_run_fused", "dgrad_prepack", "dgrad_run_packed", "dgrad_pack_grad_out", "dgrad_run_main", "dgrad_run_host", "dgrad_run_noalloc", "dgrad_plan_check",
            "dgrad_plan_destroy", "dgrad_status_string", "dgrad_cuda_error_string")
 
 
@@ -95,6 +95,7 @@ def load_library(path: str | None = None):
         lib.dgrad_describe_taps.argtypes = shape + [i, p, ctypes.POINTER(i), p, ctypes.POINTER(i)]
         lib.dgrad_plan_info.argtypes = [vp, ctypes.POINTER(PlanInfo)]
         lib.dgrad_run.argtypes = [vp, p, p, p, vp]
+        lib.dgrad_run_fused.argtypes = [vp, p, p, p, p, i, vp]
         lib.dgrad_prepack.argtypes = [vp, p, vp]
         lib.dgrad_run_packed.argtypes = [vp, p, p, vp]
         lib.dgrad_pack_grad_out.argtypes = [vp, p, vp]
@@ -108,7 +109,7 @@ def load_library(path: str | None = None):
         lib.dgrad_cuda_error_string.argtypes = []
         lib.dgrad_cuda_error_string.restype = ctypes.c_char_p
         for f in ("dgrad_plan", "dgrad_plan_ex", "dgrad_describe", "dgrad_describe_taps", "dgrad_plan_info",
-                  "dgrad_run", "dgrad_prepack", "dgrad_run_packed", "dgrad_pack_grad_out", "dgrad_run_main",
+                  "dgrad_run", "dgrad_run_fused", "dgrad_prepack", "dgrad_run_packed", "dgrad_pack_grad_out", "dgrad_run_main",
                   "dgrad_run_host", "dgrad_plan_check"):
             getattr(lib, f).restype = i
         _LIB = lib
@@ -218,17 +219,32 @@ class Plan:
         if device == "cpu" and t.is_cuda:
             raise ValueError(f"{name} must be a CPU tensor")
 
-    def run(self, grad_out, weight, grad_input=None, stream=None):
+    def run(self, grad_out, weight, grad_input=None, stream=None, relu_in=None, accumulate=False):
+        """grad_input = (accumulate ? grad_input : 0) + (relu_in > 0 if given) * dgrad."""
         import torch
         self._check_tensor(grad_out, self.go_shape, "grad_out", "cuda")
         self._check_tensor(weight, self.w_shape, "weight", "cuda")
         if grad_input is None:
+            if accumulate:
+                raise ValueError("accumulate needs grad_input")
             grad_input = torch.empty(self.gi_shape, dtype=torch.float32, device=grad_out.device)
         self._check_tensor(grad_input, self.gi_shape, "grad_input", "cuda")
-        st = self._lib.dgrad_run(self._h, ctypes.c_void_p(grad_out.data_ptr()), ctypes.c_void_p(weight.data_ptr()),
-                                 ctypes.c_void_p(grad_input.data_ptr()), _stream_handle(stream))
+        if relu_in is None and not accumulate:
+            st = self._lib.dgrad_run(self._h, ctypes.c_void_p(grad_out.data_ptr()),
+                                     ctypes.c_void_p(weight.data_ptr()), ctypes.c_void_p(grad_input.data_ptr()),
+                                     _stream_handle(stream))
+            where = "dgrad_run"
+        else:
+            if relu_in is not None:
+                self._check_tensor(relu_in, self.gi_shape, "relu_in", "cuda")
+            st = self._lib.dgrad_run_fused(
+                self._h, ctypes.c_void_p(grad_out.data_ptr()), ctypes.c_void_p(weight.data_ptr()),
+                ctypes.c_void_p(grad_input.data_ptr()),
+                ctypes.c_void_p(relu_in.data_ptr() if relu_in is not None else 0), 1 if accumulate else 0,
+                _stream_handle(stream))
+            where = "dgrad_run_fused"
         if st != 0:
-            raise DgradError(st, "dgrad_run")
+            raise DgradError(st, where)
         return grad_input
 
     def prepack(self, weight, stream=None):

@@ -174,10 +174,13 @@ dgrad_status_t launch_pack_on(dgrad_plan_s *plan, const float *weight, const flo
     return DGRAD_OK;
 }
 
-dgrad_status_t launch_main_on(dgrad_plan_s *plan, const float *grad_out, float *grad_input, cudaStream_t s) {
+dgrad_status_t launch_main_on(dgrad_plan_s *plan, const float *grad_out, float *grad_input, cudaStream_t s,
+                              const float *relu_in = nullptr, int accumulate = 0) {
     dgrad::MainParams mp = plan->mp;
     mp.go = grad_out;
     mp.gi = grad_input;
+    mp.relu_in = relu_in;
+    mp.accumulate = accumulate;
     cudaError_t e = plan->t.path == DGRAD_PATH_TCGEN05 ? dgrad::launch_tc(mp, plan->t, s, true)
                                                        : dgrad::launch_simt(mp, plan->t, s);
     return cuda_status(e);
@@ -307,23 +310,30 @@ dgrad_status_t dgrad_plan_info(dgrad_plan_t plan, dgrad_plan_info_t *info) {
 
 dgrad_status_t dgrad_run(dgrad_plan_t plan, const float *grad_out, const float *weight, float *grad_input,
                          void *stream) {
-    if (!plan) return DGRAD_ERR_INVALID_ARG;
+    return dgrad_run_fused(plan, grad_out, weight, grad_input, nullptr, 0, stream);
+}
+
+dgrad_status_t dgrad_run_fused(dgrad_plan_t plan, const float *grad_out, const float *weight, float *grad_input,
+                               const float *relu_in, int accumulate, void *stream) {
+    if (!plan || (accumulate != 0 && accumulate != 1)) return DGRAD_ERR_INVALID_ARG;
     if (!aligned16(grad_out) || !aligned16(weight) || !aligned16(grad_input)) return DGRAD_ERR_MISALIGNED;
+    if (relu_in && !aligned16(relu_in)) return DGRAD_ERR_MISALIGNED;
     const Geometry &g = plan->g;
     const size_t gi_bytes = gi_elems(g) * 4;
     if (overlaps(grad_input, gi_bytes, grad_out, go_elems(g) * 4) ||
-        overlaps(grad_input, gi_bytes, weight, w_elems(g) * 4))
+        overlaps(grad_input, gi_bytes, weight, w_elems(g) * 4) ||
+        (relu_in && overlaps(grad_input, gi_bytes, relu_in, gi_bytes)))
         return DGRAD_ERR_ALIAS;
     dgrad_status_t st = check_device(plan);
     if (st != DGRAD_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (g.n_taps == 0) {   // no term reaches any input element
+    if (g.n_taps == 0) {   // no term reaches any input element: dgrad is all zeros
         plan->packed = 1;
-        return cuda_status(cudaMemsetAsync(grad_input, 0, gi_bytes, s));
+        return accumulate ? DGRAD_OK : cuda_status(cudaMemsetAsync(grad_input, 0, gi_bytes, s));
     }
     st = launch_pack_on(plan, weight, grad_out, s);
     if (st != DGRAD_OK) return st;
-    return launch_main_on(plan, grad_out, grad_input, s);
+    return launch_main_on(plan, grad_out, grad_input, s, relu_in, accumulate);
 }
 
 dgrad_status_t dgrad_prepack(dgrad_plan_t plan, const float *weight, void *stream) {

@@ -220,6 +220,10 @@ struct MainParams {
     int xchg_bytes;
     PhaseDesc phase[kMaxPhases];
     TapDesc tap[kMaxTaps];
+    // Fused epilogue: grad_input = (accumulate ? grad_input : 0) + m * dgrad,
+    // m = (relu_in > 0) when relu_in is given (same shape as grad_input), else 1.
+    const float *relu_in;
+    int accumulate;
     uint4 mgroup[kMaxTaps];
     int bg_first[kMaxTaps + 1];
     int bg_tap0[kMaxTaps + 1];   // first tap of each B stage (and n_taps at the end)

@@ -74,7 +74,8 @@ __global__ void __launch_bounds__(kThreads) simt_dgrad_kernel(const __grid_const
         }
     }
 
-    // Overwrite grad_input (phase outputs with no taps are written as 0).
+    // Overwrite grad_input (phase outputs with no taps are written as 0), or
+    // apply the fused epilogue.
     const size_t plane = static_cast<size_t>(p.H) * p.W;
 #pragma unroll
     for (int i = 0; i < PPT; ++i) {
@@ -86,8 +87,13 @@ __global__ void __launch_bounds__(kThreads) simt_dgrad_kernel(const __grid_const
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
             const int ci = slice * BN + cg * 4 + j;
-            if (ci < p.Ci)
-                p.gi[(static_cast<size_t>(n) * p.Ci + ci) * plane + static_cast<size_t>(ih) * p.W + iw] = acc[i][j];
+            if (ci < p.Ci) {
+                const size_t idx = (static_cast<size_t>(n) * p.Ci + ci) * plane + static_cast<size_t>(ih) * p.W + iw;
+                float v = acc[i][j];
+                if (p.relu_in && !(__ldg(p.relu_in + idx) > 0.f)) v = 0.f;   // fused ReLU backward
+                if (p.accumulate) v = p.gi[idx] + v;                         // fused accumulate-into
+                p.gi[idx] = v;
+            }
         }
     }
 }

@@ -383,21 +383,61 @@ __device__ __forceinline__ void combine(const uint32_t (&r)[SMAX][16], float (&o
 // writes the s column phases of one row phase together: positions (q, u) of
 // phases (a, 0..s-1) are the s consecutive elements s*u .. s*u+s-1 of input
 // row s*q + a, one 8- or 16-byte store.
+// Fused epilogue on NV consecutive elements at d: keep the new values where
+// the ReLU input is > 0 (else 0), then add the values already in grad_input.
+template <int NV>
+__device__ __forceinline__ void fuse_values(const MainParams &p, const float *d, float (&v)[NV]) {
+    if (p.relu_in) {
+        const float *m = p.relu_in + (d - p.gi);
+        float mv[NV];
+        if constexpr (NV == 1) {
+            mv[0] = __ldg(m);
+        } else if constexpr (NV == 2) {
+            const float2 t = __ldg(reinterpret_cast<const float2 *>(m));
+            mv[0] = t.x, mv[1] = t.y;
+        } else {
+            const float4 t = __ldg(reinterpret_cast<const float4 *>(m));
+            mv[0] = t.x, mv[1] = t.y, mv[2] = t.z, mv[3] = t.w;
+        }
+#pragma unroll
+        for (int e = 0; e < NV; ++e) v[e] = mv[e] > 0.f ? v[e] : 0.f;
+    }
+    if (p.accumulate) {
+        float ov[NV];
+        if constexpr (NV == 1) {
+            ov[0] = *d;
+        } else if constexpr (NV == 2) {
+            const float2 t = *reinterpret_cast<const float2 *>(d);
+            ov[0] = t.x, ov[1] = t.y;
+        } else {
+            const float4 t = *reinterpret_cast<const float4 *>(d);
+            ov[0] = t.x, ov[1] = t.y, ov[2] = t.z, ov[3] = t.w;
+        }
+#pragma unroll
+        for (int e = 0; e < NV; ++e) v[e] = ov[e] + v[e];
+    }
+}
+
 template <int NV, int CB>
-__device__ __forceinline__ void store_batch(float *dst, size_t plane, int ncols, const float (&res)[NV][CB / 16][16]) {
+__device__ __forceinline__ void store_batch(const MainParams &p, float *dst, size_t plane, int ncols,
+                                            const float (&res)[NV][CB / 16][16]) {
+    const bool fuse = p.relu_in != nullptr || p.accumulate != 0;
     float *d = dst;   // advanced by one channel plane per store
 #pragma unroll
     for (int k = 0; k < CB / 16; ++k) {
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
             if (16 * k + j < ncols) {
+                float v[NV];
+#pragma unroll
+                for (int e = 0; e < NV; ++e) v[e] = res[e][k][j];
+                if (fuse) fuse_values<NV>(p, d, v);
                 if constexpr (NV == 1) {
-                    *d = res[0][k][j];
+                    *d = v[0];
                 } else if constexpr (NV == 2) {
-                    *reinterpret_cast<float2 *>(d) = make_float2(res[0][k][j], res[1][k][j]);
+                    *reinterpret_cast<float2 *>(d) = make_float2(v[0], v[1]);
                 } else {
-                    *reinterpret_cast<float4 *>(d) =
-                        make_float4(res[0][k][j], res[1][k][j], res[2][k][j], res[3][k][j]);
+                    *reinterpret_cast<float4 *>(d) = make_float4(v[0], v[1], v[2], v[3]);
                 }
             }
             d += plane;
@@ -434,7 +474,7 @@ __device__ __forceinline__ void epilogue_unit(EpiCtx &e, float (&pend)[NV][CB / 
         const int ih = p.s * e.q + pd0.a, iw = p.s * e.u + pd0.b;
         float *dst = p.gi + (static_cast<size_t>(e.n) * p.Ci + e.ci0) * plane + static_cast<size_t>(ih) * p.W + iw;
         for (int c0 = 0; c0 < p.bn; c0 += CB) {
-            if (pend_dst) store_batch<NV, CB>(pend_dst, plane, pend_cols, pend);
+            if (pend_dst) store_batch<NV, CB>(p, pend_dst, plane, pend_cols, pend);
             uint32_t r[NV][K][SMAX][16];
             DGRAD_TRACE_CLOCK(tl0);
 #pragma unroll
@@ -508,7 +548,7 @@ __device__ __forceinline__ void epilogue_run(EpiCtx &e, int tile, uint32_t tbase
     dev::tc_fence_before();
     dev::mbar_arrive(dev::smem_u32(acc_empty));
     DGRAD_TRACE_CLOCK(ts0);
-    if (pend_dst) store_batch<NV, CB>(pend_dst, static_cast<size_t>(p.H) * p.W, pend_cols, pend);
+    if (pend_dst) store_batch<NV, CB>(p, pend_dst, static_cast<size_t>(p.H) * p.W, pend_cols, pend);
     DGRAD_TRACE_CLOCK(ts1);
     if (threadIdx.x == 0) DGRAD_TRACE_ADD(14, ts1 - ts0);
 }

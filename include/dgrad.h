@@ -170,6 +170,23 @@ dgrad_status_t dgrad_plan_info(dgrad_plan_t plan, dgrad_plan_info_t *info);
 dgrad_status_t dgrad_run(dgrad_plan_t plan, const float *grad_out, const float *weight,
                          float *grad_input, void *stream);
 
+/* dgrad_run with a fused epilogue, for autograd chains:
+ *   grad_input = (accumulate ? grad_input : 0) + m * dgrad(grad_out, weight),
+ *   m = (relu_in > 0) elementwise when relu_in is not NULL, else 1.
+ * relu_in is the input of a ReLU whose output was this convolution's input
+ * (same shape and layout as grad_input): the product is that ReLU's backward
+ * pass (ferrotensor kernels.wgsl, section 12 "Relu", relu_backward: the
+ * gradient passes where the ReLU input is > 0 and is 0 elsewhere, NaN
+ * included); accumulate = 1 adds the result to what grad_input holds
+ * (section 20 "Gradient Accumulation", grad += new_grad) instead of
+ * overwriting it.  relu_in, when given, is a 16-byte aligned DEVICE pointer
+ * that must not overlap grad_input (DGRAD_ERR_ALIAS); accumulate must be 0 or
+ * 1 (else DGRAD_ERR_INVALID_ARG).  Everything else as dgrad_run, which is
+ * dgrad_run_fused(plan, grad_out, weight, grad_input, NULL, 0, stream). */
+dgrad_status_t dgrad_run_fused(dgrad_plan_t plan, const float *grad_out, const float *weight,
+                               float *grad_input, const float *relu_in, int accumulate,
+                               void *stream);
+
 /* The stages of dgrad_run, for callers whose weights stay fixed over
  * several calls, or who time the stages apart:
  *   dgrad_prepack        packs `weight` into the plan's workspace;

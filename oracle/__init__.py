@@ -19,6 +19,8 @@ Functions (all return float64 numpy arrays):
 * ``dgrad_phase(...)``: the sub-pixel phase split (O-phase).
 * ``dgrad_at(go, w, H, W, stride, pad_h, pad_w, idx)``: the definition at
   sampled elements.
+* ``dgrad_fused(..., relu_in=None, grad_in=None)``: O1 followed by a ReLU
+  backward mask and gradient accumulation, composed elementwise in numpy.
 
 Pins: every function is checked in ``tests/test_oracle.py`` against hand-worked
 fixtures, brute-force adjoints, finite differences, the transposed-padding
@@ -178,4 +180,21 @@ def dgrad_at(go, w, H, W, stride, pad_h, pad_w, idx):
     acc = np.empty(len(idx), np.float64)
     mag = np.empty(len(idx), np.float64)
     _check(_lib().oracle_dgrad_at(*d, _ptr(go), _ptr(w), _ptr(idx), len(idx), _ptr(acc), _ptr(mag)))
+    return acc, mag
+
+
+def dgrad_fused(go, w, H, W, stride, pad_h, pad_w, relu_in=None, grad_in=None, nthreads=None):
+    """O1, then the two elementwise steps of ferrotensor's kernels.wgsl that an
+    autograd chain applies to it: section 12 "Relu", relu_backward (the
+    gradient passes where the ReLU input is > 0, else 0), and section 20
+    "Gradient Accumulation" (grad = grad + new_grad).  Returns (acc, mag):
+    acc float64; mag the per-element sum of |terms| of the dgrad part (0 where
+    masked), the basis of the TF32 bound."""
+    acc, mag = dgrad(go, w, H, W, stride, pad_h, pad_w, nthreads=nthreads)
+    if relu_in is not None:
+        keep = _f32(relu_in) > np.float32(0.0)
+        acc = np.where(keep, acc, 0.0)
+        mag = np.where(keep, mag, 0.0)
+    if grad_in is not None:
+        acc = _f32(grad_in).astype(np.float64) + acc
     return acc, mag

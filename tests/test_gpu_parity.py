@@ -182,6 +182,57 @@ def test_edge_shapes_grouped_and_not(shape, group_taps):
     assert info["group_taps"] == {"on": 1, "off": 0, "phases": 2}[group_taps]
 
 
+# ----------------------------------------------------------------- fused epilogue
+@pytest.mark.parametrize("precision", ["tf32", "fp32"])
+@pytest.mark.parametrize("mode", ["relu", "accumulate", "both"])
+@pytest.mark.parametrize("shape", [(2, 5, 7, 9, 11, 3, 3, 1, 1, 1), (2, 48, 20, 17, 18, 3, 3, 2, 1, 1),
+                                   (3, 33, 70, 9, 14, 1, 1, 1, 0, 0), (1, 20, 40, 40, 40, 3, 3, 4, 1, 1)])
+def test_fused_epilogue(shape, mode, precision):
+    N, Ci, Co, H, W, kH, kW, s, ph, pw = shape
+    go, w = make_tensors((N, Co, out_ext(H, kH, s, ph), out_ext(W, kW, s, pw)), (Co, Ci, kH, kW), 77, "kaiming")
+    gen = torch.Generator().manual_seed(78)
+    relu_in = torch.randn((N, Ci, H, W), generator=gen) if mode in ("relu", "both") else None
+    gi0 = torch.randn((N, Ci, H, W), generator=gen) if mode in ("accumulate", "both") else None
+    ref, mag = oracle.dgrad_fused(go, w, H, W, s, ph, pw, relu_in=relu_in, grad_in=gi0)
+    with dg.Plan(N, Ci, H, W, Co, kH, kW, s, ph, pw, precision=precision) as plan:
+        gi = gi0.cuda() if gi0 is not None else torch.full((N, Ci, H, W), float("nan"), device="cuda")
+        plan.run(go.cuda(), w.cuda(), gi, relu_in=relu_in.cuda() if relu_in is not None else None,
+                 accumulate=gi0 is not None)
+        torch.cuda.synchronize()
+        plan.check()
+    out = gi.cpu().double().numpy()
+    assert np.isfinite(out).all()
+    # bound: the dgrad part's own bound (the TF32 bar, or the classic fp32 dot-product bound
+    # (K + 2) * 2^-24 * sum|terms| with K = Co*kH*kW terms) plus one fp32 rounding of the sum
+    if precision == "tf32":
+        part = TF32_REL_TERMS * mag
+    else:
+        part = (Co * kH * kW + 2) * 2.0 ** -24 * mag
+    bound = part + 2.0 ** -23 * np.abs(ref)
+    err = np.abs(out - ref)
+    assert (err <= bound + 1e-30).all(), f"worst err / bound = {np.max(err / (bound + 1e-30)):.3e}"
+    if relu_in is not None and gi0 is None:
+        assert (out[(relu_in <= 0).numpy()] == 0).all()   # masked elements are exactly 0
+
+
+def test_fused_rejects_bad_arguments():
+    wl = WORKLOADS["tiny"]
+    with dg.Plan(*wl.plan_args(), precision="tf32") as plan:
+        lib = dg.load_library()
+        go = torch.zeros(wl.go_shape, device="cuda")
+        w = torch.zeros(wl.w_shape, device="cuda")
+        gi = torch.zeros(wl.gi_shape, device="cuda")
+        stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+        P = lambda t: ctypes.c_void_p(t.data_ptr())
+        assert lib.dgrad_run_fused(plan._h, P(go), P(w), P(gi), P(gi), 0, stream) == 4      # relu_in over grad_input
+        assert lib.dgrad_run_fused(plan._h, P(go), P(w), P(gi), None, 2, stream) == 1        # accumulate not 0/1
+        buf = torch.zeros(gi.numel() + 16, device="cuda")
+        assert lib.dgrad_run_fused(plan._h, P(go), P(w), P(gi), ctypes.c_void_p(buf.data_ptr() + 4), 0,
+                                   stream) == 3
+        torch.cuda.synchronize()
+        plan.check()
+
+
 # ----------------------------------------------------------------- semantics
 def test_infinite_weight_on_padding_only_tap_stays_finite():
     # H = W = 2, 3x3, pad 1, stride 2: kernel row 0 and column 0 only ever meet

@@ -400,3 +400,35 @@ def test_mutants_are_caught(tmp_path):
         c.write_text(mut)
         subprocess.check_call(["gcc", "-O1", "-fPIC", "-shared", "-pthread", str(c), "-o", str(so), "-lm"])
         assert not _pins_pass(ctypes.CDLL(str(so))), f"mutant survived: {label}"
+
+
+
+# ----------------------------------------------------------------- fused epilogue composition
+def test_fused_oracle_special_cases():
+    """relu_backward (ferrotensor kernels.wgsl section 12) and gradient
+    accumulation (section 20) composed with O1, pinned by special cases."""
+    rng = np.random.default_rng(5)
+    N, Ci, Co, H, W, k, s, p = 2, 3, 4, 7, 6, 3, 2, 1
+    oH, oW = oracle.out_extent(H, k, s, p), oracle.out_extent(W, k, s, p)
+    go = rng.standard_normal((N, Co, oH, oW)).astype(np.float32)
+    w = rng.standard_normal((Co, Ci, k, k)).astype(np.float32)
+    ref, mag = oracle.dgrad(go, w, H, W, s, p, p)
+    pos = np.full((N, Ci, H, W), 0.5, np.float32)
+    a, m = oracle.dgrad_fused(go, w, H, W, s, p, p, relu_in=pos)
+    assert np.array_equal(a, ref) and np.array_equal(m, mag)            # every input > 0: the plain dgrad
+    nonpos = np.zeros((N, Ci, H, W), np.float32)
+    nonpos[0, 0, 0, 0] = -1.0
+    nonpos[1, 2, 3, 4] = np.nan                                        # NaN is not > 0
+    a, m = oracle.dgrad_fused(go, w, H, W, s, p, p, relu_in=nonpos)
+    assert not a.any() and not m.any()                                  # 0 and negatives block everything
+    gi0 = rng.standard_normal((N, Ci, H, W)).astype(np.float32)
+    a, _ = oracle.dgrad_fused(go, w, H, W, s, p, p, grad_in=gi0)
+    np.testing.assert_allclose(a - gi0.astype(np.float64), ref, rtol=0, atol=1e-12)   # accumulate = add the stored gradient
+    a, _ = oracle.dgrad_fused(go, np.zeros_like(w), H, W, s, p, p, grad_in=gi0)
+    assert np.array_equal(a, gi0.astype(np.float64))                   # nothing to add
+    mix = rng.standard_normal((N, Ci, H, W)).astype(np.float32)
+    a, _ = oracle.dgrad_fused(go, w, H, W, s, p, p, relu_in=mix, grad_in=gi0)
+    expect = gi0.astype(np.float64) + np.where(mix > 0, ref, 0.0)
+    assert np.array_equal(a, expect)
+    # the mask applies to the new gradient only, not to what is accumulated into
+    assert (a[mix <= 0] == gi0[mix <= 0]).all()
