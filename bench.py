@@ -9,7 +9,7 @@ programmatic dependent launch, inputs resident in HBM.  L2 is flushed
 kernel is also timed alone (dgrad_run_main after dgrad_prepack and
 dgrad_pack_grad_out) for the roofline line.
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--precision tf32|fp32]
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--precision tf32|tf32x3|fp32]
   python bench.py --impl reference ...   # the CPU oracle on the host cores
 
 With N > 1 (torchrun, one rank per GPU) every rank runs an independent
@@ -36,7 +36,7 @@ METRIC = "dgrad useful TFLOP/s and % of GB300 TF32 roofline at 1 GPU; µs per ca
 TF32_OVER_BF16 = 1.1 / 2.25          # nominal dense TF32 / BF16 ratio
 FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "sm_max_mhz": 2070.0}
 FLUSH_BYTES = 256 << 20
-MAIN_KERNEL_SOURCES = ["tc_kernel.cu", "simt_kernel.cu", "gather.cuh", "ptx.cuh", "dgrad_internal.h"]
+MAIN_KERNEL_SOURCES = ["tc_kernel.cuh", "tc_kernel.cu", "tc_kernel_fused.cu", "simt_kernel.cu", "gather.cuh", "ptx.cuh", "dgrad_internal.h"]
 WORKLOAD_ORDER = ("tiny", "resnet_stage", "strided_downsample", "pointwise", "stem")
 
 
@@ -268,6 +268,10 @@ def roofline(wl, precision, flops, nbytes, main_s, step_s):
     if precision == "tf32":
         peak_tf = peaks["bf16_tflops"] * TF32_OVER_BF16
         note = f"TF32 = {src} bf16 burst {peaks['bf16_tflops']} TFLOP/s x nominal 1.1/2.25"
+    elif precision == "tf32x3":
+        # three TF32 MMAs (hi*lo, lo*hi, hi*hi) per useful product
+        peak_tf = peaks["bf16_tflops"] * TF32_OVER_BF16 / 3
+        note = f"TF32X3 = {src} bf16 burst {peaks['bf16_tflops']} TFLOP/s x nominal 1.1/2.25 / 3 MMAs per product"
     else:
         # FP32 FFMA: 148 SMs x 128 FMA/clk x 2 FLOP at the maximum SM clock.
         peak_tf = 148 * 128 * 2 * peaks.get("sm_max_mhz", 2070.0) * 1e6 / 1e12
@@ -275,14 +279,14 @@ def roofline(wl, precision, flops, nbytes, main_s, step_s):
     t_flop = flops / (peak_tf * 1e12)
     t_hbm = nbytes / (hbm * 1e9)
     if t_flop >= t_hbm:
-        bound = "tensor" if precision == "tf32" else "alu"
+        bound = "alu" if precision == "fp32" else "tensor"
     else:
         bound = "hbm"
     achieved = flops / main_s / 1e12
     return {
         "bound": bound, "achieved": achieved, "peak": peak_tf, "unit": "TFLOP/s", "frac": achieved / peak_tf,
         "traffic": recorded_traffic(wl.name, precision),
-        "kernel": "tc_dgrad_kernel" if precision == "tf32" else "simt_dgrad_kernel",
+        "kernel": "simt_dgrad_kernel" if precision == "fp32" else "tc_dgrad_kernel",
         "peak_source": f"{note} ({src}); HBM {hbm} GB/s ({src})",
         "roofline_us": max(t_flop, t_hbm) * 1e6,
         "frac_of_roofline_step": max(t_flop, t_hbm) / step_s,
@@ -345,7 +349,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="resnet_stage")
-    ap.add_argument("--precision", default="tf32", choices=["tf32", "fp32"])
+    ap.add_argument("--precision", default="tf32", choices=["tf32", "tf32x3", "fp32"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--all", action="store_true", help="also print one info line per workload and precision")
     ap.add_argument("--profile", action="store_true",
@@ -393,8 +397,8 @@ def main():
         print(json.dumps(line), flush=True)
         if args.all:
             for name in WORKLOAD_ORDER:
-                for prec in ("tf32", "fp32"):
-                    x = time_workload(dg, torch, WORKLOADS[name], prec, 50 if prec == "tf32" else 10, 5, rank,
+                for prec in ("tf32", "tf32x3", "fp32"):
+                    x = time_workload(dg, torch, WORKLOADS[name], prec, 10 if prec == "fp32" else 50, 5, rank,
                                       lambda: None, local, clocks=False, e2e=False)
                     rf = roofline(WORKLOADS[name], prec, x["flops"], x["bytes"], x["main_ms"] * 1e-3,
                                   x["ms_per_step"] * 1e-3)

@@ -22,7 +22,7 @@ STATUS = {
     4: "DGRAD_ERR_ALIAS", 5: "DGRAD_ERR_OOM", 6: "DGRAD_ERR_CUDA", 7: "DGRAD_ERR_DEVICE_TIMEOUT",
     8: "DGRAD_ERR_NO_DEVICE", 9: "DGRAD_ERR_WRONG_DEVICE",
 }
-PREC = {"fp32": 0, "tf32": 1}
+PREC = {"fp32": 0, "tf32": 1, "tf32x3": 2}
 PATH = {"auto": 0, "simt": 1, "tcgen05": 2}
 PATH_NAME = {v: k for k, v in PATH.items()}
 
@@ -56,7 +56,7 @@ class PlanInfo(ctypes.Structure):
         d = {name: getattr(self, name) for name, _ in self._fields_}
         d["path"] = PATH_NAME.get(d["path"], d["path"])
         d["a_source"] = A_SOURCE_NAME.get(d["a_source"], d["a_source"])
-        d["precision"] = {0: "fp32", 1: "tf32"}.get(d["precision"], d["precision"])
+        d["precision"] = {0: "fp32", 1: "tf32", 2: "tf32x3"}.get(d["precision"], d["precision"])
         return d
 
 
@@ -169,7 +169,7 @@ def _stream_handle(stream):
 class Plan:
     """A dgrad plan bound to the current CUDA device.
 
-    Plan(N, Ci, H, W, Co, kH, kW, stride, pad_h, pad_w, precision="tf32" | "fp32", path=..., ...)
+    Plan(N, Ci, H, W, Co, kH, kW, stride, pad_h, pad_w, precision="tf32" | "tf32x3" | "fp32", path=..., ...)
     plan.run(grad_out, weight, grad_input=None, stream=None) -> grad_input (device tensors)
     plan.prepack(weight); plan.run_packed(grad_out, grad_input=None) -> the two halves of run
     plan.run_host(grad_out, weight, grad_input) -> grad_input (host tensors; synchronous)

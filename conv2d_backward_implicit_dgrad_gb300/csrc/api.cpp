@@ -83,7 +83,8 @@ void fill_info(const Geometry &g, const Tiling &t, int precision, size_t ws, dgr
 dgrad_status_t plan_host(int N, int Ci, int H, int W, int Co, int kH, int kW, int stride, int pad_h,
                          int pad_w, dgrad_precision_t precision, const dgrad_options_t *opts, int sm_count,
                          Geometry *g, Tiling *t) {
-    if (precision != DGRAD_PREC_FP32 && precision != DGRAD_PREC_TF32) return DGRAD_ERR_INVALID_ARG;
+    if (precision != DGRAD_PREC_FP32 && precision != DGRAD_PREC_TF32 && precision != DGRAD_PREC_TF32X3)
+        return DGRAD_ERR_INVALID_ARG;
     dgrad_status_t st = dgrad::make_geometry(N, Ci, H, W, Co, kH, kW, stride, pad_h, pad_w, g);
     if (st != DGRAD_OK) return st;
     return dgrad::choose_tiling(*g, precision, opts, sm_count, t);
@@ -92,7 +93,7 @@ dgrad_status_t plan_host(int N, int Ci, int H, int W, int Co, int kH, int kW, in
 void fill_params(dgrad_plan_s *pl) {
     const Geometry &g = pl->g;
     const Tiling &t = pl->t;
-    const int round = pl->precision == DGRAD_PREC_TF32 ? 1 : 0;
+    const int round = pl->precision != DGRAD_PREC_FP32 ? 1 : 0;
     dgrad::fill_main_params(g, t, round, &pl->mp);
     pl->mp.wp = pl->wp;
     pl->mp.err = pl->err;
@@ -105,12 +106,15 @@ void fill_params(dgrad_plan_s *pl) {
     f.v = pl->frame;
     f.N = g.N; f.Co = g.Co; f.oH = g.oH; f.oW = g.oW; f.Hv = g.Hv; f.Wp = g.Wp; f.Ph = g.Ph; f.Pw = g.Pw;
     f.co_v = t.co_v;
-    f.round_tf32 = round;
+    f.split = t.split;
+    f.co_h = t.co_h;
+    f.round_tf32 = t.split ? 0 : round;   // split: the write stage rounds both halves
     f.positions = (int)g.positions;
-    f.tile_c = t.co_v >= 128 ? 128 : (t.co_v > 32 ? 64 : 32);
+    const int cw = t.split ? t.co_h : t.co_v;   // channels one pack tile reads per position
+    f.tile_c = cw >= 128 ? 128 : (cw > 32 ? 64 : 32);
     const int tile_p = dgrad::kFrameTileElems / f.tile_c;
     f.pos_tiles = (int)((g.positions + tile_p - 1) / tile_p);
-    f.c_groups = (t.co_v + f.tile_c - 1) / f.tile_c;
+    f.c_groups = (cw + f.tile_c - 1) / f.tile_c;
 }
 
 // cuTensorMapEncodeTiled from the driver, looked up once through the

@@ -129,6 +129,8 @@ struct Tiling {
     int a_box_rows;    // rows of one A tensor copy (<= 256)
     int a_nbox;        // tensor copies per A stage
     int co_v;          // channels per packed frame row
+    int split;         // 1: TF32X3 (frame rows hold hi and lo halves; three K passes per channel chunk)
+    int co_h;          // split: channels of one half of a frame row (a multiple of 32)
     size_t frame_bytes;
     int acc_bufs;      // tensor-memory accumulator sets
     int acc_cols;      // columns of one set
@@ -161,6 +163,9 @@ inline bool use_vec_producer(const Geometry &g, const Tiling &t) {
 //  its 16-byte chunks permuted by the 128-byte swizzle of the tensor core's
 //  K-major operand layout (chunk k/4 stored at position (k/4) ^ (j % 8)):
 //    wp[(((sl*n_chunks + c)*n_taps + t)*bn + j)*32 + (((k/4) ^ (j%8))*4) + k%4]
+// Split precision (split_chunks = C > 0, n_chunks = 3C): chunk c holds output
+// channels of chunk c mod C, as the TF32 low part of the weight for c < C and
+// as the TF32 high part for c >= C (the three K passes hi*lo, lo*hi, hi*hi).
 struct PrepackParams {
     const float *w;
     float *wp;
@@ -168,6 +173,7 @@ struct PrepackParams {
     int n_taps, bn, n_slices, kc, n_chunks;
     int layout;
     int round_tf32;
+    int split_chunks;  // 0, or the channel chunks of one K pass (split precision)
     long long total;   // floats written
     int tap_kh[kMaxTaps];
     int tap_kw[kMaxTaps];
@@ -176,16 +182,20 @@ struct PrepackParams {
 // Packed frame: V[P][k] = grad_out[n][k][y - Ph][x - Pw] at flattened
 // position P = (n*Hv + y)*Wp + x (0 outside grad_out and for k >= Co),
 // TF32-rounded when the plan computes in TF32; co_v channels per row.
+// Split precision: row P holds hi = tf32(x) in channels [0, co_h) and
+// lo = tf32(x - hi) in [co_h, 2*co_h) (co_v = 2*co_h).
 struct FramePackParams {
     const float *go;
     float *v;
     int N, Co, oH, oW, Hv, Wp, Ph, Pw;
     int co_v;
     int round_tf32;
+    int split;         // 1: write hi and lo halves
+    int co_h;          // split: channels per half (channels >= Co are zero)
     int positions;     // N * Hv * Wp
     int tile_c;        // channels per pack tile: 32, 64 or 128
     int pos_tiles;     // ceil(positions / (kFrameTileElems / tile_c))
-    int c_groups;      // ceil(co_v / tile_c)
+    int c_groups;      // ceil(co_v / tile_c), split: ceil(co_h / tile_c)
 };
 constexpr int kFrameTileElems = 4096;   // elements of one pack tile (tile_c channels x positions)
 
@@ -209,6 +219,8 @@ struct MainParams {
     int a_tma, a_box_rows, a_nbox;
     int acc_bufs, acc_cols, tmem_cols;
     int round_tf32;
+    int split_chunks;   // split precision: channel chunks of one K pass (n_chunks = 3 * split_chunks), else 0
+    int co_h;           // split precision: frame channel of the first lo value
     int n_phases, n_taps;
     uint32_t idesc;
     long long timeout_ns;
@@ -239,5 +251,7 @@ cudaError_t launch_pack(const PrepackParams *pp, const FramePackParams *fp, cuda
 inline cudaError_t launch_prepack(const PrepackParams &p, cudaStream_t stream) { return launch_pack(&p, nullptr, stream); }
 cudaError_t launch_simt(const MainParams &p, const Tiling &t, cudaStream_t stream);
 cudaError_t launch_tc(const MainParams &p, const Tiling &t, cudaStream_t stream, bool pdl);
+// Tensor-copy mode with the fused epilogue (called by launch_tc).
+cudaError_t launch_tc_fused(const MainParams &p, const Tiling &t, cudaStream_t stream, bool pdl);
 
 }  // namespace dgrad

@@ -277,7 +277,8 @@ bool split_b_stages(const MGroup *mg, int n_mg, int total_taps, int cap, Tiling 
 // them fit next to two A stages they stay resident instead.
 bool size_tc(const Geometry &g, Tiling &t, int want_resident) {
     t.n_slices = ceil_div(g.Ci, t.bn);
-    t.n_chunks = ceil_div(g.Co, t.kc);
+    // Split precision runs three K passes (hi*lo, lo*hi, hi*hi) per channel chunk.
+    t.n_chunks = ceil_div(g.Co, t.kc) * (t.split ? 3 : 1);
     MGroup mg[kMaxTaps];
     int perm[kMaxTaps], units[kMaxPhases];
     t.n_mgroups = build_mgroups(g, t, mg, perm, units);
@@ -380,15 +381,19 @@ dgrad_status_t choose_tiling(const Geometry &g, int precision, const dgrad_optio
     if (opts) o = *opts;
     if (sm_count < 1) sm_count = 148;
     int path = o.path;
-    if (path == DGRAD_PATH_AUTO) path = (precision == DGRAD_PREC_TF32) ? DGRAD_PATH_TCGEN05 : DGRAD_PATH_SIMT;
+    const bool split = precision == DGRAD_PREC_TF32X3;
+    if (path == DGRAD_PATH_AUTO) path = (precision == DGRAD_PREC_FP32) ? DGRAD_PATH_SIMT : DGRAD_PATH_TCGEN05;
     if (path != DGRAD_PATH_SIMT && path != DGRAD_PATH_TCGEN05) return DGRAD_ERR_INVALID_ARG;
-    if (path == DGRAD_PATH_TCGEN05 && precision != DGRAD_PREC_TF32) return DGRAD_ERR_UNSUPPORTED;
+    if (path == DGRAD_PATH_TCGEN05 && precision == DGRAD_PREC_FP32) return DGRAD_ERR_UNSUPPORTED;
+    if (path == DGRAD_PATH_SIMT && split) return DGRAD_ERR_UNSUPPORTED;
     if (o.slice_n && (o.slice_n % 16 || o.slice_n > 256)) return DGRAD_ERR_INVALID_ARG;
     if (o.chunk_k && (o.chunk_k % 8 || o.chunk_k > 64)) return DGRAD_ERR_INVALID_ARG;
     if (o.tile_blocks < 0 || o.tile_blocks > 4 || o.grid < 0) return DGRAD_ERR_INVALID_ARG;
 
     Tiling t{};
     t.path = path;
+    t.split = split ? 1 : 0;
+    const int passes = split ? 3 : 1;   // K passes per channel chunk
     if (path == DGRAD_PATH_SIMT) {
         int ci16 = round_up(g.Ci, 16);
         t.bn = o.slice_n ? o.slice_n : (ci16 <= 16 ? 16 : ci16 <= 32 ? 32 : 64);
@@ -420,9 +425,10 @@ dgrad_status_t choose_tiling(const Geometry &g, int precision, const dgrad_optio
             const long long units = (long long)tiles1 * slices;
             const long long waves = (units + sm_count - 1) / sm_count;
             const double mma = taps * 4.0 * std::max(cand / 2.0, (4096.0 + cand * 32.0) / 128.0);
-            const bool resident = slices == 1 && (double)ceil_div(g.Co, 32) * taps * cand * 128.0 <= 150.0 * 1024;
+            const bool resident =
+                slices == 1 && (double)ceil_div(g.Co, 32) * passes * taps * cand * 128.0 <= 150.0 * 1024;
             const double copies = (a_band + (resident ? 0.0 : taps * cand * 128.0)) / 128.0;
-            const double cost = (double)waves * ceil_div(g.Co, 32) * (mma + copies);
+            const double cost = (double)waves * ceil_div(g.Co, 32) * passes * (mma + copies);
             if (cost < best * 0.98) {
                 best = cost;
                 best_bn = cand;
@@ -446,10 +452,15 @@ dgrad_status_t choose_tiling(const Geometry &g, int precision, const dgrad_optio
     if (o.chunk_k && o.chunk_k != 32) return DGRAD_ERR_INVALID_ARG;
     if (o.a_source < 0 || o.a_source > 2) return DGRAD_ERR_INVALID_ARG;
     // grad_out reaches the MMA either as tensor copies of a packed,
-    // channels-last frame, or through producer warps.
-    t.co_v = std::max(32, round_up(g.Co, 4));
+    // channels-last frame, or through producer warps.  Split precision takes
+    // the frame at any size: its rows carry the hi and lo halves, each padded
+    // to whole 32-channel chunks so that a chunk's copy never reads the other
+    // half.
+    t.co_h = split ? round_up(g.Co, 32) : 0;
+    t.co_v = split ? 2 * t.co_h : std::max(32, round_up(g.Co, 4));
     t.frame_bytes = (size_t)g.positions * t.co_v * 4;
-    if (o.a_source == 1)
+    if (split && o.a_source == 2) return DGRAD_ERR_UNSUPPORTED;
+    if (o.a_source == 1 || split)
         t.a_tma = 1;
     else if (o.a_source == 2)
         t.a_tma = 0;
@@ -516,6 +527,8 @@ void fill_main_params(const Geometry &g, const Tiling &t, int round_tf32, MainPa
     m.a_tma = t.a_tma; m.a_box_rows = t.a_box_rows; m.a_nbox = t.a_nbox;
     m.acc_bufs = t.acc_bufs; m.acc_cols = t.acc_cols; m.tmem_cols = t.tmem_cols;
     m.round_tf32 = round_tf32;
+    m.split_chunks = t.split ? t.n_chunks / 3 : 0;
+    m.co_h = t.co_h;
     m.n_phases = g.n_phases;
     m.n_taps = g.n_taps;
     m.idesc = tf32_idesc(kBlockM, t.bn);
@@ -560,6 +573,7 @@ void fill_prepack_params(const Geometry &g, const Tiling &t, int round_tf32, Pre
     q.Co = g.Co; q.Ci = g.Ci; q.kH = g.kH; q.kW = g.kW;
     q.n_taps = g.n_taps; q.bn = t.bn; q.n_slices = t.n_slices; q.kc = t.kc; q.n_chunks = t.n_chunks;
     q.round_tf32 = round_tf32;
+    q.split_chunks = t.split ? t.n_chunks / 3 : 0;
     q.layout = t.path == DGRAD_PATH_TCGEN05 ? 1 : 0;
     q.total = (long long)(t.packed_bytes / 4);
     // tcgen05 path: taps in the packing order of the plan's MMA groups

@@ -56,7 +56,8 @@ extern "C" dgrad_status_t dgrad_run_noalloc(int N, int Ci, int H, int W, int Co,
                                             const float *grad_out, const float *weight, float *grad_input,
                                             void *stream) {
     using namespace dgrad;
-    if (precision != DGRAD_PREC_FP32 && precision != DGRAD_PREC_TF32) return DGRAD_ERR_INVALID_ARG;
+    if (precision != DGRAD_PREC_FP32 && precision != DGRAD_PREC_TF32 && precision != DGRAD_PREC_TF32X3)
+        return DGRAD_ERR_INVALID_ARG;
     Geometry g;
     dgrad_status_t st = make_geometry(N, Ci, H, W, Co, kH, kW, stride, pad_h, pad_w, &g);
     if (st != DGRAD_OK) return st;
@@ -69,7 +70,8 @@ extern "C" dgrad_status_t dgrad_run_noalloc(int N, int Ci, int H, int W, int Co,
         return DGRAD_ERR_NO_DEVICE;
     if (major != 10 || minor != 3) return DGRAD_ERR_NO_DEVICE;
 
-    // No frame buffer here: producer warps carry grad_out to the MMA.
+    // No frame buffer here: producer warps carry grad_out to the MMA (so
+    // split precision, which needs the frame, is rejected by the tiling).
     dgrad_options_t opts{};
     opts.a_source = 2;
     Tiling t;

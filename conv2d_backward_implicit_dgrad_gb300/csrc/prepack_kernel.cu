@@ -58,12 +58,19 @@ __device__ void pack_weights(const PrepackParams &p, int block, int nblocks) {
         rest /= p.n_taps;
         const int c = static_cast<int>(rest % p.n_chunks);
         const int sl = static_cast<int>(rest / p.n_chunks);
-        const int co = c * p.kc + 4 * gq + e;
+        // Split precision: chunk c is K pass c / split_chunks of channel chunk c mod split_chunks.
+        const int cc = p.split_chunks ? c % p.split_chunks : c;
+        const int co = cc * p.kc + 4 * gq + e;
         const int ci = sl * p.bn + j;
         float v = 0.f;
         if (co < p.Co && ci < p.Ci)
             v = __ldg(p.w + ((static_cast<size_t>(co) * p.Ci + ci) * p.kH + p.tap_kh[t]) * p.kW + p.tap_kw[t]);
-        if (p.round_tf32) v = dev::round_tf32(v);
+        if (p.split_chunks) {
+            const float hi = dev::round_tf32(v);
+            v = c < p.split_chunks ? dev::round_tf32(v - hi) : hi;   // pass 0 takes the low part
+        } else if (p.round_tf32) {
+            v = dev::round_tf32(v);
+        }
         p.wp[i] = v;
     }
 }
@@ -116,11 +123,21 @@ __device__ void pack_frame(const FramePackParams &p, int block, float *tile, int
     __syncthreads();
     // write: each position's TC channels (TC * 4 contiguous bytes), coalesced along channels
     const int ncols = min(TP, p.positions - P0);
-    const int cmax = min(TC, p.co_v - co0);
+    const int cmax = min(TC, (p.split ? p.co_h : p.co_v) - co0);
     float *dst = p.v + static_cast<size_t>(P0) * p.co_v + co0;
     for (int i = threadIdx.x; i < TC * ncols; i += kThreads) {
         const int xi = i / TC, c = i % TC;
-        if (c < cmax) dst[static_cast<size_t>(xi) * p.co_v + c] = tile[c * kStride + xi];
+        if (c < cmax) {
+            const float x = tile[c * kStride + xi];
+            float *row = dst + static_cast<size_t>(xi) * p.co_v;
+            if (p.split) {   // hi in the first half of the row, lo in the second
+                const float hi = dev::round_tf32(x);
+                row[c] = hi;
+                row[p.co_h + c] = dev::round_tf32(x - hi);
+            } else {
+                row[c] = x;
+            }
+        }
     }
 }
 

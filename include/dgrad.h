@@ -66,16 +66,27 @@ typedef enum {
 } dgrad_status_t;
 
 /* Arithmetic of the contraction.
- *  FP32: exact fp32 products, fp32 accumulation (FFMA on the CUDA cores).
- *  TF32: both operands rounded to TF32 (round to nearest, ties away from zero),
- *        products accumulated in fp32 on the tcgen05 tensor cores. */
-typedef enum { DGRAD_PREC_FP32 = 0, DGRAD_PREC_TF32 = 1 } dgrad_precision_t;
+ *  FP32:   exact fp32 products, fp32 accumulation (FFMA on the CUDA cores).
+ *  TF32:   both operands rounded to TF32 (round to nearest, ties away from zero),
+ *          products accumulated in fp32 on the tcgen05 tensor cores.
+ *  TF32X3: split precision on the tensor cores.  Each operand x is split into
+ *          hi = tf32(x) and lo = tf32(x - hi) (same rounding), so that
+ *          |x - hi - lo| <= 2^-22 |x|; every product is formed as
+ *          hi*lo + lo*hi + hi*hi (three TF32 MMAs, the lo*lo term dropped) and
+ *          accumulated in fp32.  Each product is then off by at most about
+ *          3 * 2^-22 of its size, which with fp32 accumulation gives
+ *          fp32-level accuracy at three times the TF32 MMA work.  tcgen05 path
+ *          only; it needs the packed grad_out frame (the plan's workspace
+ *          holds hi and lo halves), so DGRAD_PATH_SIMT, a_source = 2 and
+ *          dgrad_run_noalloc return DGRAD_ERR_UNSUPPORTED for it.  Not in the
+ *          pages: an accuracy variant of their contraction. */
+typedef enum { DGRAD_PREC_FP32 = 0, DGRAD_PREC_TF32 = 1, DGRAD_PREC_TF32X3 = 2 } dgrad_precision_t;
 
-/* Kernel family.  AUTO picks TCGEN05 for TF32 and SIMT for FP32. */
+/* Kernel family.  AUTO picks TCGEN05 for TF32 and TF32X3, SIMT for FP32. */
 typedef enum {
     DGRAD_PATH_AUTO = 0,
     DGRAD_PATH_SIMT = 1,     /* FFMA implicit GEMM (exact fp32; also accepts TF32-rounded operands) */
-    DGRAD_PATH_TCGEN05 = 2   /* warp-specialised tcgen05/TMEM implicit GEMM (TF32 only) */
+    DGRAD_PATH_TCGEN05 = 2   /* warp-specialised tcgen05/TMEM implicit GEMM (TF32 and TF32X3) */
 } dgrad_path_t;
 
 /* Optional tuning overrides for dgrad_plan_ex / dgrad_describe; 0 = automatic. */

@@ -5,6 +5,11 @@ Bars (fixed by the tolerance the method is held to):
   * FP32 path: relative L2 error ||gpu - ref||_2 / ||ref||_2 <= 1e-5 (fp64).
   * TF32 path: per element |gpu - ref| <= 2e-3 * sum|terms|, and exactly 0
     wherever no term reaches the element (sum|terms| = 0).
+  * TF32X3 (split precision) path: the FP32 bar, and per element
+    |gpu - ref| <= (2^-20 + (3K + 2) 2^-23) * sum|terms| (K = Co*kH*kW): each
+    split product is within 2^-20 of its size of the exact one, and the 3K
+    fp32 additions add at most 2^-23 of the running sum each (truncating
+    accumulation allowed for).
 grad_input is poisoned with NaN before every run, so an element the kernels
 fail to write fails both bars.
 """
@@ -57,26 +62,40 @@ def assert_tf32(gpu, ref, mag):
     assert np.all(gpu[~pos] == 0)
 
 
+def split_bound(Co, kH, kW):
+    return 2.0 ** -20 + (3 * Co * kH * kW + 2) * 2.0 ** -23
+
+
+def assert_split(gpu, ref, mag, Co, kH, kW):
+    assert_fp32(gpu, ref)
+    err = np.abs(gpu - ref)
+    bad = err > split_bound(Co, kH, kW) * mag
+    assert not bad.any(), f"{bad.sum()} elements over the split-precision bound"
+    assert np.all(gpu[mag == 0] == 0)
+
+
 def check(args, go, w, precision, **opts):
     N, Ci, H, W, Co, kH, kW, s, ph, pw = args
     ref, mag = oracle.dgrad(go, w, H, W, s, ph, pw)
     gpu, info = run_gpu(args, go, w, precision, **opts)
     if precision == "fp32":
         assert_fp32(gpu, ref)
+    elif precision == "tf32x3":
+        assert_split(gpu, ref, mag, Co, kH, kW)
     else:
         assert_tf32(gpu, ref, mag)
     return info
 
 
 # ----------------------------------------------------------------- workloads
-@pytest.mark.parametrize("precision", ["tf32", "fp32"])
+@pytest.mark.parametrize("precision", ["tf32", "fp32", "tf32x3"])
 @pytest.mark.parametrize("seed", [0, 1, 2])
 @pytest.mark.parametrize("name", ORDER)
 def test_workload_parity(name, seed, precision):
     wl = WORKLOADS[name]
     go, w = make_inputs(wl, seed)
     info = check(wl.plan_args(), go, w, precision)
-    assert info["path"] == ("tcgen05" if precision == "tf32" else "simt")
+    assert info["path"] == ("simt" if precision == "fp32" else "tcgen05")
 
 
 # ----------------------------------------------------------------- edge sweep
@@ -99,7 +118,7 @@ EDGE = [
 ]
 
 
-@pytest.mark.parametrize("precision", ["tf32", "fp32"])
+@pytest.mark.parametrize("precision", ["tf32", "fp32", "tf32x3"])
 @pytest.mark.parametrize("shape", EDGE)
 def test_edge_shapes(shape, precision):
     N, Ci, Co, H, W, kH, kW, s, ph, pw = shape
@@ -183,7 +202,7 @@ def test_edge_shapes_grouped_and_not(shape, group_taps):
 
 
 # ----------------------------------------------------------------- fused epilogue
-@pytest.mark.parametrize("precision", ["tf32", "fp32"])
+@pytest.mark.parametrize("precision", ["tf32", "fp32", "tf32x3"])
 @pytest.mark.parametrize("mode", ["relu", "accumulate", "both"])
 @pytest.mark.parametrize("shape", [(2, 5, 7, 9, 11, 3, 3, 1, 1, 1), (2, 48, 20, 17, 18, 3, 3, 2, 1, 1),
                                    (3, 33, 70, 9, 14, 1, 1, 1, 0, 0), (1, 20, 40, 40, 40, 3, 3, 4, 1, 1)])
@@ -206,6 +225,8 @@ def test_fused_epilogue(shape, mode, precision):
     # (K + 2) * 2^-24 * sum|terms| with K = Co*kH*kW terms) plus one fp32 rounding of the sum
     if precision == "tf32":
         part = TF32_REL_TERMS * mag
+    elif precision == "tf32x3":
+        part = split_bound(Co, kH, kW) * mag
     else:
         part = (Co * kH * kW + 2) * 2.0 ** -24 * mag
     bound = part + 2.0 ** -23 * np.abs(ref)
@@ -375,16 +396,45 @@ def test_run_packed_before_prepack_is_rejected():
 
 
 # ----------------------------------------------------------------- full size, sampled
+@pytest.mark.parametrize("precision", ["tf32", "tf32x3"])
 @pytest.mark.parametrize("name", ["resnet_stage", "strided_downsample", "pointwise", "stem"])
-def test_full_size_sampled_definition(name):
+def test_full_size_sampled_definition(name, precision):
     """At full size in the benchmark's launch configuration: 4096 sampled
     elements against the definition computed one by one."""
     wl = WORKLOADS[name]
     go, w = make_inputs(wl, 0)
-    gpu, _ = run_gpu(wl.plan_args(), go, w, "tf32")
+    gpu, _ = run_gpu(wl.plan_args(), go, w, precision)
     rng = np.random.default_rng(101)
     idx = np.stack([rng.integers(0, wl.N, 4096), rng.integers(0, wl.Ci, 4096),
                     rng.integers(0, wl.H, 4096), rng.integers(0, wl.W, 4096)], 1)
     acc, mag = oracle.dgrad_at(go, w, wl.H, wl.W, wl.stride, wl.pad_h, wl.pad_w, idx)
     g = gpu[idx[:, 0], idx[:, 1], idx[:, 2], idx[:, 3]]
-    assert np.all(np.abs(g - acc) <= TF32_REL_TERMS * mag)
+    rel = TF32_REL_TERMS if precision == "tf32" else split_bound(wl.Co, wl.kH, wl.kW)
+    assert np.all(np.abs(g - acc) <= rel * mag)
+    if precision == "tf32x3":
+        assert np.linalg.norm(g - acc) <= FP32_REL_L2 * np.linalg.norm(acc)
+
+
+# ----------------------------------------------------------------- split precision
+@pytest.mark.parametrize("shape", [(2, 48, 20, 17, 18, 3, 3, 2, 1, 1), (3, 33, 70, 9, 14, 1, 1, 1, 0, 0),
+                                   (1, 3, 64, 40, 38, 7, 7, 2, 3, 3)])
+def test_split_precision_beats_tf32(shape):
+    """The split path's error is far below the TF32 path's on the same inputs
+    (values with full 24-bit mantissas, where TF32 rounding shows)."""
+    N, Ci, Co, H, W, kH, kW, s, ph, pw = shape
+    go, w = make_tensors((N, Co, out_ext(H, kH, s, ph), out_ext(W, kW, s, pw)), (Co, Ci, kH, kW), 79, "kaiming")
+    ref, _ = oracle.dgrad(go, w, H, W, s, ph, pw)
+    e = {}
+    for prec in ("tf32", "tf32x3"):
+        gpu, _ = run_gpu(shape[:1] + (Ci, H, W, Co, kH, kW, s, ph, pw), go, w, prec)
+        e[prec] = np.linalg.norm(gpu - ref) / np.linalg.norm(ref)
+    assert e["tf32x3"] <= FP32_REL_L2 and e["tf32x3"] * 50 < e["tf32"], e
+
+
+def test_split_precision_rejects_other_sources():
+    with pytest.raises(dg.DgradError) as e:
+        dg.Plan(1, 8, 8, 8, 8, 3, 3, 1, 1, 1, precision="tf32x3", path="simt")
+    assert e.value.status == 2
+    with pytest.raises(dg.DgradError) as e:
+        dg.Plan(1, 8, 8, 8, 8, 3, 3, 1, 1, 1, precision="tf32x3", a_source="producers")
+    assert e.value.status == 2

@@ -260,3 +260,61 @@ def test_shared_shift_plans():
         with pytest.raises(dg.DgradError) as e:
             dg.describe(*bad, precision="tf32", group_taps="phases")
         assert e.value.status == 2
+
+
+# ----------------------------------------------------------------- split precision (TF32X3)
+def test_split_precision_plans():
+    for name in ORDER:
+        wl = WORKLOADS[name]
+        d = dg.describe(*wl.plan_args(), precision="tf32x3")
+        t = dg.describe(*wl.plan_args(), precision="tf32")
+        assert d["path"] == "tcgen05" and d["precision"] == "tf32x3"
+        assert d["a_source"] == "frame"                       # always the packed frame
+        assert d["n_chunks"] == 3 * -(-wl.Co // 32)           # three K passes per channel chunk
+        assert d["smem_bytes"] <= 232448 and d["tmem_cols"] <= 512
+        assert d["useful_flops"] == t["useful_flops"]
+    # a frame above the size at which TF32 plans switch to producer warps stays a frame
+    big = (64, 64, 224, 224, 256, 3, 3, 1, 1, 1)   # a 3.3 GB frame
+    assert dg.describe(*big, precision="tf32")["a_source"] == "producers"
+    assert dg.describe(*big, precision="tf32x3")["a_source"] == "frame"
+    for bad in (dict(path="simt"), dict(a_source="producers")):
+        with pytest.raises(dg.DgradError) as e:
+            dg.describe(2, 8, 8, 8, 8, 3, 3, 1, 1, 1, "tf32x3", **bad)
+        assert e.value.status == 2
+
+
+def _rna_tf32(x):
+    """Round fp32 values to TF32 (10 stored mantissa bits), to nearest with
+    ties away from zero: add half of the dropped part to the magnitude bits,
+    then clear the 13 dropped bits."""
+    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)
+    return ((u + np.uint32(0x1000)) & np.uint32(0xFFFFE000)).view(np.float32)
+
+
+def test_tf32_rounding_model():
+    # values with a known TF32 rounding: 1 + 2^-11 is a tie (rounds away), 1 + 2^-11 + 2^-23 rounds up,
+    # 1 + 2^-12 rounds down, and negative values mirror positive ones
+    x = np.array([1.0, 1 + 2.0 ** -11, 1 + 2.0 ** -11 + 2.0 ** -23, 1 + 2.0 ** -12, -(1 + 2.0 ** -11)], np.float32)
+    assert _rna_tf32(x).tolist() == [1.0, 1 + 2.0 ** -10, 1 + 2.0 ** -10, 1.0, -(1 + 2.0 ** -10)]
+
+
+def test_split_arithmetic_bound():
+    """The split-precision arithmetic, modelled on the CPU with exact products:
+    go = hi + lo + r and w likewise, the three partial products hi*lo, lo*hi
+    and hi*hi summed exactly.  Each product is then within 2^-20 of its size of
+    the true one, so the result is within 2^-20 * sum|terms| of the definition;
+    plain TF32 (hi*hi alone) is not."""
+    rng = np.random.default_rng(9)
+    N, Ci, Co, H, W, k, s, p = 2, 5, 7, 9, 10, 3, 2, 1
+    oH, oW = (H + 2 * p - k) // s + 1, (W + 2 * p - k) // s + 1
+    go = rng.standard_normal((N, Co, oH, oW)).astype(np.float32)
+    w = (rng.standard_normal((Co, Ci, k, k)) * 0.3).astype(np.float32)
+    ref, mag = oracle.dgrad(go, w, H, W, s, p, p)
+    go_hi, w_hi = _rna_tf32(go), _rna_tf32(w)
+    go_lo, w_lo = _rna_tf32(go - go_hi), _rna_tf32(w - w_hi)
+    assert np.all(np.abs(go - go_hi - go_lo) <= 2.0 ** -22 * np.abs(go))
+    split = sum(oracle.dgrad(a, b, H, W, s, p, p, with_mag=False)[0]
+                for a, b in ((go_hi, w_lo), (go_lo, w_hi), (go_hi, w_hi)))
+    assert np.all(np.abs(split - ref) <= 2.0 ** -20 * mag)
+    one = oracle.dgrad(go_hi, w_hi, H, W, s, p, p, with_mag=False)[0]
+    assert np.max(np.abs(one - ref) / np.maximum(mag, 1e-30)) > 2.0 ** -16

@@ -22,7 +22,7 @@ from conv2d_backward_implicit_dgrad_gb300.workloads import WORKLOADS, make_input
 
 pytestmark = pytest.mark.gpu
 
-PREC = {"fp32": 0, "tf32": 1}
+PREC = {"fp32": 0, "tf32": 1, "tf32x3": 2}
 
 
 def call_noalloc(args, precision, go, w, gi):
@@ -64,3 +64,12 @@ def test_noalloc_refuses_oversized_weights():
     w = torch.zeros((1024, 512, 3, 3), device="cuda")
     gi = torch.zeros((1, 512, 8, 8), device="cuda")
     assert call_noalloc(args, "tf32", go, w, gi) == 2
+
+
+def test_noalloc_refuses_split_precision():
+    # split precision needs the packed frame, which only a plan's workspace holds
+    args = (1, 8, 8, 8, 8, 3, 3, 1, 1, 1)
+    go = torch.zeros((1, 8, 8, 8), device="cuda")
+    w = torch.zeros((8, 8, 3, 3), device="cuda")
+    gi = torch.zeros((1, 8, 8, 8), device="cuda")
+    assert call_noalloc(args, "tf32x3", go, w, gi) == 2
