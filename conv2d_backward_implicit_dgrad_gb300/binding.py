@@ -35,7 +35,7 @@ EXPORTS = ("dgrad_plan", "dgrad_plan_ex", "dgrad_describe", "dgrad_describe_taps
 class Options(ctypes.Structure):
     _fields_ = [("path", ctypes.c_int), ("tile_blocks", ctypes.c_int), ("slice_n", ctypes.c_int),
                 ("chunk_k", ctypes.c_int), ("grid", ctypes.c_int), ("sm_count", ctypes.c_int),
-                ("a_source", ctypes.c_int), ("group_taps", ctypes.c_int)]
+                ("a_source", ctypes.c_int), ("group_taps", ctypes.c_int), ("b_stages", ctypes.c_int)]
 
 
 class PlanInfo(ctypes.Structure):
@@ -48,7 +48,7 @@ class PlanInfo(ctypes.Structure):
         ("grid", ctypes.c_int), ("b_resident", ctypes.c_int), ("a_source", ctypes.c_int),
         ("smem_bytes", ctypes.c_int),
         ("tmem_cols", ctypes.c_int), ("group_taps", ctypes.c_int), ("tile_step", ctypes.c_int),
-        ("workspace_bytes", ctypes.c_size_t),
+        ("a_stages", ctypes.c_int), ("b_stages", ctypes.c_int), ("workspace_bytes", ctypes.c_size_t),
         ("packed_weight_bytes", ctypes.c_size_t), ("useful_flops", ctypes.c_double),
         ("algorithmic_bytes", ctypes.c_double)]
 
@@ -124,10 +124,10 @@ GROUP_TAPS = {"auto": 0, "on": 1, "rows": 1, "off": 2, "phases": 3}
 
 
 def _options(path="auto", tile_blocks=0, slice_n=0, chunk_k=0, grid=0, sm_count=0, a_source="auto",
-             group_taps="auto"):
+             group_taps="auto", b_stages=0):
     return Options(PATH[path] if isinstance(path, str) else int(path), tile_blocks, slice_n, chunk_k, grid,
                    sm_count, A_SOURCE[a_source] if isinstance(a_source, str) else int(a_source),
-                   GROUP_TAPS[group_taps] if isinstance(group_taps, str) else int(group_taps))
+                   GROUP_TAPS[group_taps] if isinstance(group_taps, str) else int(group_taps), int(b_stages))
 
 
 def describe(N, Ci, H, W, Co, kH, kW, stride, pad_h, pad_w, precision="tf32", **opts) -> dict:

@@ -74,6 +74,8 @@ void fill_info(const Geometry &g, const Tiling &t, int precision, size_t ws, dgr
     info->tmem_cols = t.tmem_cols;
     info->group_taps = t.grouped ? 1 : (t.pgroup ? 2 : 0);
     info->tile_step = t.tile_step;
+    info->a_stages = t.a_stages;
+    info->b_stages = t.b_stages;
     info->workspace_bytes = ws;
     info->packed_weight_bytes = t.packed_bytes;
     info->useful_flops = 2.0 * g.N * g.Co * g.oH * g.oW * (double)g.Ci * g.kH * g.kW;
@@ -110,11 +112,16 @@ void fill_params(dgrad_plan_s *pl) {
     f.co_h = t.co_h;
     f.round_tf32 = t.split ? 0 : round;   // split: the write stage rounds both halves
     f.positions = (int)g.positions;
-    const int cw = t.split ? t.co_h : t.co_v;   // channels one pack tile reads per position
-    f.tile_c = cw >= 128 ? 128 : (cw > 32 ? 64 : 32);
-    const int tile_p = dgrad::kFrameTileElems / f.tile_c;
-    f.pos_tiles = (int)((g.positions + tile_p - 1) / tile_p);
-    f.c_groups = (cw + f.tile_c - 1) / f.tile_c;
+    // Pack blocks of 32 channels x seg_len plane elements: 256 elements
+    // unless that leaves fewer than 512 blocks (then shorter segments, down
+    // to 32, so that every SM gets a few; measured best of 256/512/1024).
+    const long long plane = (long long)g.oH * g.oW;
+    f.c_groups = (g.Co + dgrad::kPackChannels - 1) / dgrad::kPackChannels;
+    f.seg_len = dgrad::kPackSegMax;
+    while (f.seg_len > 32 && (long long)g.N * f.c_groups * ((plane + f.seg_len - 1) / f.seg_len) < 512)
+        f.seg_len /= 2;
+    f.segs = (int)((plane + f.seg_len - 1) / f.seg_len);
+    f.vec = plane % 4 == 0 ? 1 : 0;
 }
 
 // cuTensorMapEncodeTiled from the driver, looked up once through the
@@ -281,7 +288,11 @@ dgrad_status_t dgrad_plan_ex(int N, int Ci, int H, int W, int Co, int kH, int kW
         delete pl;
         return DGRAD_ERR_OOM;
     }
-    if (cudaMemset(mem, 0, 256) != cudaSuccess) {
+    // Zero everything once: the error word, and the frame's rows and
+    // channels that no pack ever writes (its zero padding).  Completed here,
+    // so that work later queued on any stream sees it.
+    if (cudaMemset(mem, 0, ws) != cudaSuccess || cudaStreamSynchronize(nullptr) != cudaSuccess) {
+        cudaGetLastError();
         cudaFree(mem);
         delete pl;
         return DGRAD_ERR_CUDA;

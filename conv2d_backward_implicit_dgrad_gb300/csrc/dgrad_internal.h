@@ -122,6 +122,7 @@ struct Tiling {
     int grouped;       // 1: taps of a kernel row share one MMA (MGroup)
     int pgroup;        // 1: taps of different phases with the same shift share one MMA (MGroup)
     int tile_step;     // output positions per tile (tm*128, less the rows a grouped MMA cannot finish)
+    int want_b_stages; // requested weight pipeline depth (0: automatic)
     int n_mgroups;
     int bg_first[kMaxTaps + 1];   // B stage i holds MMA groups [bg_first[i], bg_first[i+1])
     int xchg_bytes;    // shared memory for the epilogue's cross-warp row exchange
@@ -184,6 +185,10 @@ struct PrepackParams {
 // TF32-rounded when the plan computes in TF32; co_v channels per row.
 // Split precision: row P holds hi = tf32(x) in channels [0, co_h) and
 // lo = tf32(x - hi) in [co_h, 2*co_h) (co_v = 2*co_h).
+// The frame is zeroed once when the plan is made; a pack writes only the
+// rows of grad_out's positions (the zero rows and channels never change).
+// Pack blocks: (image n, 32-channel group, segment of seg_len consecutive
+// elements of the oH*oW channel plane).
 struct FramePackParams {
     const float *go;
     float *v;
@@ -193,11 +198,13 @@ struct FramePackParams {
     int split;         // 1: write hi and lo halves
     int co_h;          // split: channels per half (channels >= Co are zero)
     int positions;     // N * Hv * Wp
-    int tile_c;        // channels per pack tile: 32, 64 or 128
-    int pos_tiles;     // ceil(positions / (kFrameTileElems / tile_c))
-    int c_groups;      // ceil(co_v / tile_c), split: ceil(co_h / tile_c)
+    int seg_len;       // plane elements per pack block: a multiple of 4, <= kPackSegMax
+    int segs;          // ceil(oH*oW / seg_len)
+    int c_groups;      // ceil(Co / kPackChannels)
+    int vec;           // 1: 16-byte grad_out loads (oH*oW % 4 == 0)
 };
-constexpr int kFrameTileElems = 4096;   // elements of one pack tile (tile_c channels x positions)
+constexpr int kPackChannels = 32;   // channels per pack block (one 128-byte frame row segment)
+constexpr int kPackSegMax = 256;    // plane elements per pack block at most
 
 // Main-kernel MMA group entry: A window offset (bytes), accumulator column
 // (bit 31: first group of its phase), B offset inside the chunk's tap block

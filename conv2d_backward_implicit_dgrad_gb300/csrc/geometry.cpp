@@ -309,7 +309,7 @@ bool size_tc(const Geometry &g, Tiling &t, int want_resident) {
     const long long budget = kMaxSmem - kBarrierBytes - t.xchg_bytes;
     const int taps = std::max(1, g.n_taps);
     t.b_resident = 0;
-    if (want_resident && t.n_slices == 1 && t.n_chunks <= kMaxResidentChunks) {
+    if (want_resident && t.want_b_stages == 0 && t.n_slices == 1 && t.n_chunks <= kMaxResidentChunks) {
         long long b_all = (long long)t.n_chunks * taps * tap_bytes;
         if (b_all + 2 * a_bytes <= budget) {
             t.b_resident = 1;
@@ -324,16 +324,27 @@ bool size_tc(const Geometry &g, Tiling &t, int want_resident) {
     }
     if (want_resident && !t.b_resident) return false;
     if (!t.b_resident) {
-        // Largest B stage with two B stages and at least two A stages
-        // (three when they fit without shrinking the stage below half).
-        long long cap = (budget - 2 * a_bytes) / (2 * tap_bytes);
+        // Largest B stage with nst B stages (two unless requested) and at
+        // least two A stages (three when they fit without shrinking the
+        // stage below half).
+        // Automatic depth: when a whole chunk's taps fit one stage with four
+        // (or three) stages and three A stages, take the deeper pipeline:
+        // such plans (1x1 kernels) run short MMA bursts per chunk, and the
+        // weight copies then need more chunks in flight (measured: pointwise
+        // main kernel 31.4 -> 26.9 us with four stages).  Otherwise two large
+        // stages (more stages measured slower for 3x3 and larger kernels).
+        int nst = t.want_b_stages;
+        for (int cand = 4; nst == 0 && cand >= 3; --cand)
+            if ((budget - 3 * a_bytes) / (cand * tap_bytes) >= taps) nst = cand;
+        if (nst == 0) nst = 2;
+        long long cap = (budget - 2 * a_bytes) / (nst * tap_bytes);
         if (cap < 1) return false;
         cap = std::min<long long>(cap, taps);
-        long long cap3 = (budget - 3 * a_bytes) / (2 * tap_bytes);
+        long long cap3 = (budget - 3 * a_bytes) / (nst * tap_bytes);
         if (cap3 >= std::min<long long>(taps, std::max<long long>(1, (cap + 1) / 2))) cap = std::min<long long>(cap3, taps);
         if (!split_b_stages(mg, t.n_mgroups, g.n_taps, (int)cap, t)) return false;
         t.chunk_bytes = (int)(t.tap_group * tap_bytes);
-        t.b_stages = 2;
+        t.b_stages = nst;
         long long left = budget - (long long)t.b_stages * t.chunk_bytes;
         t.a_stages = (int)std::min<long long>(4, left / a_bytes);
     }
@@ -478,6 +489,8 @@ dgrad_status_t choose_tiling(const Geometry &g, int precision, const dgrad_optio
     // shapes): fewer, wider MMAs, each phase still its own accumulator, so
     // the epilogue is unchanged.  That is the automatic choice.
     if (o.group_taps < 0 || o.group_taps > 3) return DGRAD_ERR_INVALID_ARG;
+    if (o.b_stages != 0 && (o.b_stages < 2 || o.b_stages > 8)) return DGRAD_ERR_INVALID_ARG;
+    t.want_b_stages = o.b_stages;
     int group_pref[2][2];   // (kernel-row groups, shared-shift groups) in order of preference
     int n_group = 0;
     if (o.group_taps == 1) {

@@ -8,12 +8,13 @@
 //     index) by one pass that writes each (slice, chunk) block contiguously,
 //     keeps only the taps each phase uses, zero-pads channels, and (TF32
 //     precision) rounds to TF32 once.
-// (b) grad_out NCHW -> V[P][k] (FramePackParams): one block transposes a
-//     tile of kFrameTileElems (consecutive frame positions x 32, 64 or 128
-//     channels) through shared memory, so both the grad_out reads (along
-//     positions) and the V writes (along channels) are coalesced.  Frame positions
-//     outside grad_out, and channels >= Co, are written as zeros; the
-//     meganeura shader's transposed padding becomes these zero rows.
+// (b) grad_out NCHW -> V[P][k] (FramePackParams): one block transposes 32
+//     channels x up to 256 consecutive plane elements through a swizzled
+//     shared tile, with 16-byte accesses on both sides (grad_out runs along
+//     positions, frame rows along channels).  Only the rows of grad_out's
+//     positions are written: the frame's zero rows and zero channels (the
+//     meganeura shader's transposed padding) are set once when the plan is
+//     made.
 #include <cuda_runtime.h>
 
 #include "dgrad_internal.h"
@@ -24,7 +25,8 @@ namespace dgrad {
 namespace {
 
 constexpr int kThreads = 256;
-static_assert(kFrameTileElems % kThreads == 0 && kFrameTileElems / 128 <= kThreads, "frame tile split");
+static_assert(kPackChannels == 32 && kThreads == 8 * kPackChannels && kPackSegMax % 32 == 0,
+              "frame block: 8 threads per channel row, 32 positions per write step");
 constexpr int kMaxPrepackBlocks = 1024;
 
 struct PackArgs {
@@ -75,68 +77,100 @@ __device__ void pack_weights(const PrepackParams &p, int block, int nblocks) {
     }
 }
 
-// One frame tile of TP = kFrameTileElems / TC consecutive positions x TC
-// channels.  block -> (position tile, channel group); position tiles vary
-// fastest so neighbouring blocks read neighbouring grad_out runs.  Wide
-// frames (many channels per position) take wide channel groups, so each
-// position's row segment written is TC * 4 bytes long.
-template <int TC>
-__device__ void pack_frame(const FramePackParams &p, int block, float *tile, int *off) {
-    constexpr int TP = kFrameTileElems / TC;
-    constexpr int kStride = TP + 1;
-    const int pt = block % p.pos_tiles;
-    const int co0 = (block / p.pos_tiles) * TC;
-    const int P0 = pt * TP;
+// Shared tile of one frame block: 32 channel rows of `pitch` (= seg_len) floats.
+// The 16-byte group g of row j sits at group (g & ~7) | ((g ^ (j >> 2)) & 7):
+// the 16-byte stores of the read phase (8 threads along one row) and the
+// 4-channel column reads of the write phase (a warp: 4 positions x 8 channel
+// quads) both hit 32 distinct banks.
+__device__ __forceinline__ int tile_index(int j, int e, int pitch) {
+    const int g = e >> 2;
+    return j * pitch + (((g & ~7) | ((g ^ (j >> 2)) & 7)) << 2) + (e & 3);
+}
+
+// One frame block: image n, channels [c0, c0 + 32) and plane elements
+// [e0, e0 + len) of grad_out.
+//  read:  thread t takes channel t / 8 and the 16-byte groups t % 8 + 8k of
+//         its run (8 threads cover one 128-byte line), every load in flight
+//         before the shared-memory stores;
+//  write: thread t takes channel quad t % 8 and positions t / 8 + 32k; the
+//         frame row of a position gets 4 channels per 16-byte store (a warp
+//         writes 4 whole 128-byte row segments).
+template <bool kVec>
+__device__ void pack_frame(const FramePackParams &p, int block, float *tile) {
+    constexpr int kSteps = kPackSegMax / 32;   // 16-byte groups per thread (read) and positions per thread (write)
     const int plane = p.oH * p.oW;
-    if (threadIdx.x < TP) {   // grad_out offset of channel 0 at each position, or -1
-        const int P = P0 + threadIdx.x;
-        int o = -1;
-        if (P < p.positions) {
-            const int img = p.Hv * p.Wp;
-            const int n = P / img, rem = P - n * img;
-            const int y = rem / p.Wp, x = rem - y * p.Wp;
-            const int oh = y - p.Ph, ow = x - p.Pw;
-            if (oh >= 0 && oh < p.oH && ow >= 0 && ow < p.oW) o = n * p.Co * plane + oh * p.oW + ow;
-        }
-        off[threadIdx.x] = o;
-    }
-    __syncthreads();
-    // read: TC channels x TP positions, coalesced along positions.  Each
-    // thread keeps one position and issues all of its channel loads before
-    // the first shared-memory store, so they are in flight together.
+    const int seg = block % p.segs;
+    const int rest = block / p.segs;
+    const int cg = rest % p.c_groups;
+    const int n = rest / p.c_groups;
+    const int c0 = cg * kPackChannels;
+    const int e0 = seg * p.seg_len;
+    const int len = min(p.seg_len, plane - e0);
+    const int t = threadIdx.x;
     {
-        constexpr int kRowsPerPass = kThreads / TP;
-        constexpr int kLoads = TC / kRowsPerPass;
-        const int xi = threadIdx.x % TP;
-        const int c0 = threadIdx.x / TP;
-        const int o = off[xi];
-        float v[kLoads];
+        const int j = t >> 3, c = c0 + j;
+        const int eb = (t & 7) << 2;   // first element of this thread's first group
+        const float *src = p.go + (static_cast<size_t>(n) * p.Co + c) * plane + e0 + eb;
+        float4 v[kSteps];
 #pragma unroll
-        for (int k = 0; k < kLoads; ++k) {
-            const int co = co0 + c0 + kRowsPerPass * k;
-            v[k] = (o >= 0 && co < p.Co) ? __ldg(p.go + static_cast<size_t>(o) + static_cast<size_t>(co) * plane) : 0.f;
+        for (int k = 0; k < kSteps; ++k) {
+            const int e = eb + 32 * k;
+            v[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (c < p.Co && e < len) {
+                if (kVec && e + 4 <= len) {
+                    v[k] = __ldg(reinterpret_cast<const float4 *>(src + 32 * k));
+                } else {
+                    v[k].x = __ldg(src + 32 * k);
+                    if (e + 1 < len) v[k].y = __ldg(src + 32 * k + 1);
+                    if (e + 2 < len) v[k].z = __ldg(src + 32 * k + 2);
+                    if (e + 3 < len) v[k].w = __ldg(src + 32 * k + 3);
+                }
+            }
         }
+        float *dst = tile + tile_index(j, eb, p.seg_len);   // group t%8 + 8k sits 32k floats further on
 #pragma unroll
-        for (int k = 0; k < kLoads; ++k)
-            tile[(c0 + kRowsPerPass * k) * kStride + xi] = p.round_tf32 ? dev::round_tf32(v[k]) : v[k];
+        for (int k = 0; k < kSteps; ++k)
+            if (eb + 32 * k < p.seg_len) *reinterpret_cast<float4 *>(dst + 32 * k) = v[k];
     }
     __syncthreads();
-    // write: each position's TC channels (TC * 4 contiguous bytes), coalesced along channels
-    const int ncols = min(TP, p.positions - P0);
-    const int cmax = min(TC, (p.split ? p.co_h : p.co_v) - co0);
-    float *dst = p.v + static_cast<size_t>(P0) * p.co_v + co0;
-    for (int i = threadIdx.x; i < TC * ncols; i += kThreads) {
-        const int xi = i / TC, c = i % TC;
-        if (c < cmax) {
-            const float x = tile[c * kStride + xi];
-            float *row = dst + static_cast<size_t>(xi) * p.co_v;
-            if (p.split) {   // hi in the first half of the row, lo in the second
-                const float hi = dev::round_tf32(x);
-                row[c] = hi;
-                row[p.co_h + c] = dev::round_tf32(x - hi);
-            } else {
-                row[c] = x;
+    const int q = t & 7;
+    const int c = c0 + 4 * q;
+    if (c >= (p.split ? p.co_h : p.co_v)) return;
+    int e = t >> 3;
+    if (e >= len) return;
+    const int pitch = p.seg_len;
+    const float *s0 = tile + tile_index(4 * q, e, pitch);   // rows 4q..4q+3 at position e; +32 floats per step
+    int oh = (e0 + e) / p.oW, ow = (e0 + e) - oh * p.oW;
+    float *vbase = p.v + static_cast<size_t>(c);
+#pragma unroll
+    for (int k = 0; k < kSteps; ++k, e += 32) {
+        if (e >= len) break;
+        float4 x;
+        x.x = s0[32 * k];
+        x.y = s0[32 * k + pitch];
+        x.z = s0[32 * k + 2 * pitch];
+        x.w = s0[32 * k + 3 * pitch];
+        const size_t P = (static_cast<size_t>(n) * p.Hv + oh + p.Ph) * p.Wp + ow + p.Pw;
+        float *row = vbase + P * p.co_v;
+        if (p.split) {   // hi in the first half of the row, lo in the second
+            float4 hi, lo;
+            hi.x = dev::round_tf32(x.x), lo.x = dev::round_tf32(x.x - hi.x);
+            hi.y = dev::round_tf32(x.y), lo.y = dev::round_tf32(x.y - hi.y);
+            hi.z = dev::round_tf32(x.z), lo.z = dev::round_tf32(x.z - hi.z);
+            hi.w = dev::round_tf32(x.w), lo.w = dev::round_tf32(x.w - hi.w);
+            *reinterpret_cast<float4 *>(row) = hi;
+            *reinterpret_cast<float4 *>(row + p.co_h) = lo;
+        } else {
+            if (p.round_tf32) {
+                x.x = dev::round_tf32(x.x), x.y = dev::round_tf32(x.y);
+                x.z = dev::round_tf32(x.z), x.w = dev::round_tf32(x.w);
             }
+            *reinterpret_cast<float4 *>(row) = x;
+        }
+        ow += 32;   // next position of this thread: 32 elements further on in the plane
+        while (ow >= p.oW) {
+            ow -= p.oW;
+            ++oh;
         }
     }
 }
@@ -145,18 +179,15 @@ __global__ void __launch_bounds__(kThreads) pack_kernel(const __grid_constant__ 
     // Let the main kernel start its prologue while this grid runs; it reads
     // what this grid writes only after griddepcontrol.wait.
     dev::grid_launch_dependents();
-    __shared__ float tile[kFrameTileElems + 128];   // TC x (TP + 1) = kFrameTileElems + TC floats, TC <= 128
-    __shared__ int off[kFrameTileElems / 32];
+    extern __shared__ __align__(16) float tile[];   // kPackChannels x seg_len floats
     if (static_cast<int>(blockIdx.x) < a.w_blocks) {
         pack_weights(a.w, blockIdx.x, a.w_blocks);
     } else {
         const int b = blockIdx.x - a.w_blocks;
-        if (a.f.tile_c == 128)
-            pack_frame<128>(a.f, b, tile, off);
-        else if (a.f.tile_c == 64)
-            pack_frame<64>(a.f, b, tile, off);
+        if (a.f.vec)
+            pack_frame<true>(a.f, b, tile);
         else
-            pack_frame<32>(a.f, b, tile, off);
+            pack_frame<false>(a.f, b, tile);
     }
 }
 
@@ -171,11 +202,12 @@ cudaError_t launch_pack(const PrepackParams *pp, const FramePackParams *fp, cuda
     }
     if (fp) {
         a.f = *fp;
-        a.f_blocks = fp->pos_tiles * fp->c_groups;   // c_groups = ceil(co_v / tile_c)
+        a.f_blocks = fp->N * fp->c_groups * fp->segs;
     }
     const int blocks = a.w_blocks + a.f_blocks;
     if (blocks == 0) return cudaSuccess;
-    pack_kernel<<<blocks, kThreads, 0, stream>>>(a);
+    const size_t smem = fp ? static_cast<size_t>(kPackChannels) * fp->seg_len * sizeof(float) : 0;
+    pack_kernel<<<blocks, kThreads, smem, stream>>>(a);
     return cudaGetLastError();
 }
 

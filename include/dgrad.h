@@ -104,6 +104,8 @@ typedef struct {
                           summed with row shifts by the epilogue; DGRAD_ERR_UNSUPPORTED when that
                           cannot fit), 2 none, 3 the taps of different sub-pixel phases that read the
                           same frame shift (stride > 1; DGRAD_ERR_UNSUPPORTED when not possible) */
+    int b_stages;      /* tcgen05 path, packed-weight pipeline: 0 automatic, 2..8 stream the weights
+                          through that many shared-memory stages (never resident) */
 } dgrad_options_t;
 
 /* Everything a plan decided, for tests, benchmarks and logs. */
@@ -126,6 +128,7 @@ typedef struct {
     int tmem_cols;         /* tensor-memory columns allocated per CTA (tcgen05 path) */
     int group_taps;        /* tcgen05 path: 0 one MMA per tap, 1 per kernel row of taps, 2 per shared shift */
     int tile_step;         /* output positions per work-unit tile */
+    int a_stages, b_stages;/* tcgen05 path: operand pipeline stages (b_stages = channel chunks when resident) */
     size_t workspace_bytes;/* device workspace owned by the plan */
     size_t packed_weight_bytes;
     double useful_flops;   /* 2*N*Co*oH*oW*Ci*kH*kW */
