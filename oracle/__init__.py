@@ -21,6 +21,9 @@ Functions (all return float64 numpy arrays):
   sampled elements.
 * ``dgrad_fused(..., relu_in=None, grad_in=None)``: O1 followed by a ReLU
   backward mask and gradient accumulation, composed elementwise in numpy.
+* ``wgrad(go, x, stride, pad_h, pad_w)`` -> ``(acc, mag)``: the weight
+  gradient dW[co,ci,kh,kw] (O-w), as a direct sum over the batch and grad_out
+  positions; ``mag`` the per-element sum of |terms|.
 
 Pins: every function is checked in ``tests/test_oracle.py`` against hand-worked
 fixtures, brute-force adjoints, finite differences, the transposed-padding
@@ -69,9 +72,10 @@ def _lib():
             lib.oracle_dgrad_phase.argtypes = shape + [p, p, p]
             lib.oracle_dgrad_at.argtypes = shape + [p, p, p, ctypes.c_long, p, p]
             lib.oracle_out_extent.argtypes = [i, i, i, i]
+            lib.oracle_wgrad.argtypes = shape + [p, p, p, p, i]
             for f in (lib.oracle_dgrad_scatter, lib.oracle_conv2d_fwd, lib.oracle_dgrad_gather,
                       lib.oracle_dgrad_gemm_p1, lib.oracle_dgrad_phase, lib.oracle_dgrad_at,
-                      lib.oracle_out_extent):
+                      lib.oracle_out_extent, lib.oracle_wgrad):
                 f.restype = ctypes.c_int
             _LIB = lib
     return _LIB
@@ -197,4 +201,23 @@ def dgrad_fused(go, w, H, W, stride, pad_h, pad_w, relu_in=None, grad_in=None, n
         mag = np.where(keep, mag, 0.0)
     if grad_in is not None:
         acc = _f32(grad_in).astype(np.float64) + acc
+    return acc, mag
+
+
+def wgrad(go, x, kH: int, kW: int, stride: int, pad_h: int, pad_w: int, nthreads: int | None = None):
+    """O-w: the weight gradient of the convolution whose grad_out is ``go``
+    [N, Co, oH, oW] and whose forward input is ``x`` [N, Ci, H, W].  Returns
+    (acc, mag) as float64 [Co, Ci, kH, kW]."""
+    go, x = _f32(go), _f32(x)
+    N, Co, oH, oW = go.shape
+    N2, Ci, H, W = x.shape
+    if N2 != N:
+        raise ValueError("batch mismatch")
+    if (oH, oW) != (out_extent(H, kH, stride, pad_h), out_extent(W, kW, stride, pad_w)):
+        raise ValueError("grad_out spatial shape does not match H, W, kernel, stride, padding")
+    acc = np.empty((Co, Ci, kH, kW), np.float64)
+    mag = np.empty_like(acc)
+    nt = default_threads() if nthreads is None else nthreads
+    _check(_lib().oracle_wgrad(N, Ci, H, W, Co, kH, kW, stride, pad_h, pad_w, _ptr(go), _ptr(x),
+                               _ptr(acc), _ptr(mag), nt))
     return acc, mag

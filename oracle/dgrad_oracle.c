@@ -361,3 +361,86 @@ int oracle_out_extent(int in, int k, int stride, int pad)
     if (in < 1 || k < 1 || stride < 1 || pad < 0) return 0;
     return out_extent(in, k, stride, pad);
 }
+
+/* ------------------------------------------------------------------------ */
+/* O-w: the weight gradient (wgrad), the other half of doppler's            */
+/* runConv2DBackward (conv2d_backward.js: with computeGradWeight it runs     */
+/* one invocation per weight element, [outChannels, inChannels, kernelH,     */
+/* kernelW], over gradOutput and the forward input; its shader is not on     */
+/* the page).  Written from the same forward mapping as O1: the forward      */
+/* pass multiplied w[co,ci,kh,kw] by x[n,ci,ih,iw] with                      */
+/* ih = oh*stride - pad_h + kh, iw = ow*stride - pad_w + kw into             */
+/* y[n,co,oh,ow], so                                                         */
+/*   dW[co,ci,kh,kw] = sum over n, oh, ow with (ih,iw) inside the input of   */
+/*                     go[n,co,oh,ow] * x[n,ci,ih,iw].                       */
+/* `mag` gets the sum of |terms|.  The batch is summed (the pages' host      */
+/* code has no batch axis; a batched forward pass shares one weight).        */
+/* ------------------------------------------------------------------------ */
+typedef struct {
+    const shape_t *sh;
+    const float *go, *x;
+    double *acc, *mag;
+    int co0, co1;
+} wgrad_job_t;
+
+static void wgrad_co_range(const wgrad_job_t *j)
+{
+    const shape_t *sh = j->sh;
+    for (int co = j->co0; co < j->co1; ++co)
+        for (int ci = 0; ci < sh->Ci; ++ci)
+            for (int kh = 0; kh < sh->kH; ++kh)
+                for (int kw = 0; kw < sh->kW; ++kw) {
+                    double a = 0.0, m = 0.0;
+                    for (int n = 0; n < sh->N; ++n)
+                        for (int oh = 0; oh < sh->oH; ++oh) {
+                            int ih = oh * sh->s - sh->ph + kh;
+                            if (ih < 0 || ih >= sh->H) continue;
+                            for (int ow = 0; ow < sh->oW; ++ow) {
+                                int iw = ow * sh->s - sh->pw + kw;
+                                if (iw < 0 || iw >= sh->W) continue;
+                                double t = (double)j->go[go_at(sh, n, co, oh, ow)] *
+                                           (double)j->x[gi_at(sh, n, ci, ih, iw)];
+                                a += t;
+                                m += fabs(t);
+                            }
+                        }
+                    size_t o = w_at(sh, co, ci, kh, kw);
+                    j->acc[o] = a;
+                    if (j->mag) j->mag[o] = m;
+                }
+}
+
+static void *wgrad_thread(void *arg)
+{
+    wgrad_co_range((const wgrad_job_t *)arg);
+    return NULL;
+}
+
+int oracle_wgrad(int N, int Ci, int H, int W, int Co, int kH, int kW, int stride,
+                 int pad_h, int pad_w, const float *go, const float *x,
+                 double *acc, double *mag, int nthreads)
+{
+    shape_t sh;
+    if (make_shape(&sh, N, Ci, H, W, Co, kH, kW, stride, pad_h, pad_w)) return -1;
+    /* Output channels own disjoint parts of dW: threads split them. */
+    if (nthreads < 1) nthreads = 1;
+    if (nthreads > Co) nthreads = Co;
+    if (nthreads > 256) nthreads = 256;
+    wgrad_job_t jobs[256];
+    pthread_t tids[256];
+    for (int t = 0; t < nthreads; ++t) {
+        jobs[t].sh = &sh; jobs[t].go = go; jobs[t].x = x;
+        jobs[t].acc = acc; jobs[t].mag = mag;
+        jobs[t].co0 = (int)((long)Co * t / nthreads);
+        jobs[t].co1 = (int)((long)Co * (t + 1) / nthreads);
+    }
+    int started = 0;
+    for (int t = 1; t < nthreads; ++t) {
+        if (pthread_create(&tids[t], NULL, wgrad_thread, &jobs[t]) != 0) break;
+        started = t;
+    }
+    wgrad_co_range(&jobs[0]);
+    for (int t = 1; t <= started; ++t) pthread_join(tids[t], NULL);
+    for (int t = started + 1; t < nthreads; ++t) wgrad_co_range(&jobs[t]);
+    return 0;
+}

@@ -432,3 +432,105 @@ def test_fused_oracle_special_cases():
     assert np.array_equal(a, expect)
     # the mask applies to the new gradient only, not to what is accumulated into
     assert (a[mix <= 0] == gi0[mix <= 0]).all()
+
+
+# ----------------------------------------------------------------- O-w: the weight gradient
+def wgrad_case(shape, seed):
+    N, Ci, Co, H, W, kH, kW, s, ph, pw = shape
+    go, _ = rand_case(*shape, seed=seed)
+    x = np.random.default_rng(seed + 1).uniform(-1, 1, (N, Ci, H, W)).astype(np.float32)
+    return go, x
+
+
+@pytest.mark.parametrize("shape", SMALL)
+def test_wgrad_brute_force(shape):
+    """dW[e] = <conv2d(x, unit weight e), g> for every weight element e: the
+    gradient of the linear map w -> <conv2d(x, w), g>, built element by element."""
+    N, Ci, Co, H, W, kH, kW, s, ph, pw = shape
+    go, x = wgrad_case(shape, 40)
+    acc, mag = oracle.wgrad(go, x, kH, kW, s, ph, pw)
+    g64, x64 = go.astype(np.float64), x.astype(np.float64)
+    ref = np.zeros((Co, Ci, kH, kW))
+    for e in range(ref.size):
+        w = np.zeros(ref.size)
+        w[e] = 1.0
+        y = oracle.conv2d_fwd(x64, w.reshape(ref.shape), s, ph, pw)
+        ref.reshape(-1)[e] = float(np.dot(y.reshape(-1), g64.reshape(-1)))
+    assert np.abs(acc - ref).max() <= 1e-12 * max(1.0, np.abs(ref).max())
+    assert np.all(mag >= np.abs(acc) - 1e-12)
+
+
+@pytest.mark.parametrize("shape", SMALL)
+def test_wgrad_matches_torch_conv2d_weight(shape):
+    N, Ci, Co, H, W, kH, kW, s, ph, pw = shape
+    go, x = wgrad_case(shape, 41)
+    acc, _ = oracle.wgrad(go, x, kH, kW, s, ph, pw)
+    ref = torch.nn.grad.conv2d_weight(torch.from_numpy(x).double(), (Co, Ci, kH, kW),
+                                      torch.from_numpy(go).double(), stride=s, padding=(ph, pw)).numpy()
+    assert rel_err(acc, ref) <= 1e-12
+
+
+@pytest.mark.parametrize("name", ORDER)
+def test_wgrad_dgrad_cross_adjoint(name):
+    """<dgrad(g, w), x> = <g, conv2d(x, w)> = <w, wgrad(x, g)>: O-w against O1 and
+    O-fwd at each workload's shape (batch cut to 2 images)."""
+    wl = WORKLOADS[name]
+    N = min(wl.N, 2)
+    go, w = make_tensors((N, wl.Co, wl.oH, wl.oW), wl.w_shape, 42, wl.dist)
+    go, w = go.numpy(), w.numpy()
+    x = np.random.default_rng(43).standard_normal((N, wl.Ci, wl.H, wl.W)).astype(np.float32)
+    dw, _ = oracle.wgrad(go, x, wl.kH, wl.kW, wl.stride, wl.pad_h, wl.pad_w)
+    gi, _ = oracle.dgrad(go, w, wl.H, wl.W, wl.stride, wl.pad_h, wl.pad_w)
+    y = oracle.conv2d_fwd(x, w, wl.stride, wl.pad_h, wl.pad_w)
+    a = float(np.dot(w.astype(np.float64).reshape(-1), dw.reshape(-1)))
+    b = float(np.dot(gi.reshape(-1), x.astype(np.float64).reshape(-1)))
+    c = float(np.dot(go.astype(np.float64).reshape(-1), y.reshape(-1)))
+    scale = float(np.abs(go.astype(np.float64)).reshape(-1) @ np.abs(y).reshape(-1)) + 1.0
+    assert abs(a - c) <= 1e-11 * scale and abs(b - c) <= 1e-11 * scale
+
+
+def test_wgrad_pointwise_is_a_matmul():
+    """1x1 kernel, stride 1, no padding: dW[co, ci] = sum_n G_n X_n^T."""
+    rng = np.random.default_rng(44)
+    go = rng.standard_normal((3, 5, 4, 6)).astype(np.float32)
+    x = rng.standard_normal((3, 7, 4, 6)).astype(np.float32)
+    acc, _ = oracle.wgrad(go, x, 1, 1, 1, 0, 0)
+    ref = sum(go[n].reshape(5, -1).astype(np.float64) @ x[n].reshape(7, -1).astype(np.float64).T for n in range(3))
+    assert np.abs(acc[:, :, 0, 0] - ref).max() <= 1e-12 * np.abs(ref).max()
+
+
+@pytest.mark.parametrize("shape", [(2, 3, 4, 7, 6, 3, 3, 2, 1, 1), (1, 2, 3, 6, 6, 3, 2, 1, 2, 0)])
+def test_wgrad_delta_input(shape):
+    """x = one unit value at (n0, ci0, ih0, iw0): dW[co, ci0, kh, kw] = go[n0, co, oh, ow]
+    where oh*s - ph + kh = ih0 and ow*s - pw + kw = iw0 (0 when no such oh, ow); other
+    input channels get 0."""
+    N, Ci, Co, H, W, kH, kW, s, ph, pw = shape
+    go, _ = wgrad_case(shape, 45)
+    oH, oW = go.shape[2:]
+    n0, ci0, ih0, iw0 = N - 1, Ci - 1, H // 2, W // 2
+    x = np.zeros((N, Ci, H, W), np.float32)
+    x[n0, ci0, ih0, iw0] = 1.0
+    acc, _ = oracle.wgrad(go, x, kH, kW, s, ph, pw)
+    ref = np.zeros_like(acc)
+    for kh in range(kH):
+        for kw in range(kW):
+            nh, nw = ih0 + ph - kh, iw0 + pw - kw
+            if nh % s or nw % s:
+                continue
+            oh, ow = nh // s, nw // s
+            if 0 <= oh < oH and 0 <= ow < oW:
+                ref[:, ci0, kh, kw] = go[n0, :, oh, ow]
+    assert np.array_equal(acc, ref)
+
+
+def test_wgrad_magnitude_and_linearity():
+    shape = (2, 3, 4, 7, 6, 3, 3, 2, 1, 1)
+    N, Ci, Co, H, W, kH, kW, s, ph, pw = shape
+    go, x = wgrad_case(shape, 46)
+    acc, mag = oracle.wgrad(go, x, kH, kW, s, ph, pw)
+    mabs, _ = oracle.wgrad(np.abs(go), np.abs(x), kH, kW, s, ph, pw)
+    assert np.abs(mag - mabs).max() <= 1e-12 * mabs.max()
+    a2, _ = oracle.wgrad(go, 2 * x, kH, kW, s, ph, pw)   # exact: scaling by 2 is exact in fp32 and fp64
+    assert np.array_equal(a2, 2 * acc)
+    neg, _ = oracle.wgrad(-go, x, kH, kW, s, ph, pw)
+    assert np.array_equal(neg, -acc)
