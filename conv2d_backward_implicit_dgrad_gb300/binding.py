@@ -29,13 +29,29 @@ PATH_NAME = {v: k for k, v in PATH.items()}
 # Every function declared in include/dgrad.h (checked by the CPU tests).
 EXPORTS = ("dgrad_plan", "dgrad_plan_ex", "dgrad_describe", "dgrad_describe_taps", "dgrad_plan_info", "dgrad_run",
            "dgrad_run_fused", "dgrad_prepack", "dgrad_run_packed", "dgrad_pack_grad_out", "dgrad_run_main", "dgrad_run_host", "dgrad_run_noalloc", "dgrad_plan_check",
-           "dgrad_plan_destroy", "dgrad_status_string", "dgrad_cuda_error_string")
+           "dgrad_plan_destroy", "dgrad_status_string", "dgrad_cuda_error_string",
+           "wgrad_describe", "wgrad_describe_taps", "wgrad_plan", "wgrad_plan_info", "wgrad_run", "wgrad_plan_check",
+           "wgrad_plan_destroy")
 
 
 class Options(ctypes.Structure):
     _fields_ = [("path", ctypes.c_int), ("tile_blocks", ctypes.c_int), ("slice_n", ctypes.c_int),
                 ("chunk_k", ctypes.c_int), ("grid", ctypes.c_int), ("sm_count", ctypes.c_int),
                 ("a_source", ctypes.c_int), ("group_taps", ctypes.c_int), ("b_stages", ctypes.c_int)]
+
+
+class WgradPlanInfo(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int) for n in ("N", "Ci", "H", "W", "Co", "kH", "kW", "stride", "pad_h", "pad_w",
+                                            "oH", "oW", "precision", "Wf", "Kimg", "Lx", "n_copies", "seg_rows",
+                                            "n_mt", "n_nt", "n_ks", "slice_n", "n_units", "grid", "stages",
+                                            "smem_bytes", "tmem_cols")] + [
+        ("workspace_bytes", ctypes.c_size_t), ("useful_flops", ctypes.c_double),
+        ("algorithmic_bytes", ctypes.c_double)]
+
+    def as_dict(self):
+        d = {name: getattr(self, name) for name, _ in self._fields_}
+        d["precision"] = {0: "fp32", 1: "tf32", 2: "tf32x3"}.get(d["precision"], d["precision"])
+        return d
 
 
 class PlanInfo(ctypes.Structure):
@@ -108,6 +124,17 @@ def load_library(path: str | None = None):
         lib.dgrad_status_string.restype = ctypes.c_char_p
         lib.dgrad_cuda_error_string.argtypes = []
         lib.dgrad_cuda_error_string.restype = ctypes.c_char_p
+        lib.wgrad_describe.argtypes = shape + [i, i, ctypes.POINTER(WgradPlanInfo)]
+        lib.wgrad_describe_taps.argtypes = shape + [i, p, p, p, p, ctypes.POINTER(i), ctypes.POINTER(i)]
+        lib.wgrad_plan.argtypes = shape + [i, ctypes.POINTER(vp)]
+        lib.wgrad_plan_info.argtypes = [vp, ctypes.POINTER(WgradPlanInfo)]
+        lib.wgrad_run.argtypes = [vp, p, p, p, vp]
+        lib.wgrad_plan_check.argtypes = [vp]
+        lib.wgrad_plan_destroy.argtypes = [vp]
+        lib.wgrad_plan_destroy.restype = None
+        for f in ("wgrad_describe", "wgrad_describe_taps", "wgrad_plan", "wgrad_plan_info", "wgrad_run",
+                  "wgrad_plan_check"):
+            getattr(lib, f).restype = i
         for f in ("dgrad_plan", "dgrad_plan_ex", "dgrad_describe", "dgrad_describe_taps", "dgrad_plan_info",
                   "dgrad_run", "dgrad_run_fused", "dgrad_prepack", "dgrad_run_packed", "dgrad_pack_grad_out", "dgrad_run_main",
                   "dgrad_run_host", "dgrad_plan_check"):
@@ -334,3 +361,93 @@ def dgrad(grad_out, weight, H, W, stride=1, pad_h=0, pad_w=0, precision="tf32", 
         out = p.run(grad_out, weight)
         torch.cuda.current_stream().synchronize()
         return out
+
+
+# ---------------------------------------------------------------- weight gradient
+def wgrad_describe(N, Ci, H, W, Co, kH, kW, stride, pad_h, pad_w, precision="tf32", sm_count=0) -> dict:
+    """Host-only planning decisions of the weight gradient (no GPU needed)."""
+    lib = load_library()
+    info = WgradPlanInfo()
+    st = lib.wgrad_describe(N, Ci, H, W, Co, kH, kW, stride, pad_h, pad_w, PREC[precision], sm_count,
+                            ctypes.byref(info))
+    if st != 0:
+        raise DgradError(st, "wgrad_describe")
+    return info.as_dict()
+
+
+def wgrad_describe_taps(N, Ci, H, W, Co, kH, kW, stride, pad_h, pad_w) -> dict:
+    """Host-only tap table of the weight gradient: per tap (kh*kW + kw) the input
+    copy and K offset it reads; per input copy its kernel column and row phase."""
+    lib = load_library()
+    cap = 1024
+    cp, off = (ctypes.c_int * cap)(), (ctypes.c_int * cap)()
+    ckw, crh = (ctypes.c_int * cap)(), (ctypes.c_int * cap)()
+    nc, ty = ctypes.c_int(), ctypes.c_int()
+    st = lib.wgrad_describe_taps(N, Ci, H, W, Co, kH, kW, stride, pad_h, pad_w, cap, cp, off, ckw, crh,
+                                 ctypes.byref(nc), ctypes.byref(ty))
+    if st != 0:
+        raise DgradError(st, "wgrad_describe_taps")
+    taps = kH * kW
+    return {"copy": list(cp[:taps]), "offset": list(off[:taps]), "copy_kw": list(ckw[:nc.value]),
+            "copy_rh": list(crh[:nc.value]), "Ty": ty.value}
+
+
+class WgradPlan:
+    """A weight-gradient plan bound to the current CUDA device.
+
+    WgradPlan(N, Ci, H, W, Co, kH, kW, stride, pad_h, pad_w, precision="tf32")
+    plan.run(grad_out, input, grad_weight=None, stream=None) -> grad_weight [Co, Ci, kH, kW]
+    """
+
+    def __init__(self, N, Ci, H, W, Co, kH, kW, stride=1, pad_h=0, pad_w=0, precision="tf32"):
+        self._lib = load_library()
+        self._h = ctypes.c_void_p()
+        self.args = (N, Ci, H, W, Co, kH, kW, stride, pad_h, pad_w)
+        st = self._lib.wgrad_plan(*self.args, PREC[precision], ctypes.byref(self._h))
+        if st != 0:
+            raise DgradError(st, "wgrad_plan")
+        info = WgradPlanInfo()
+        self._lib.wgrad_plan_info(self._h, ctypes.byref(info))
+        self.info = info.as_dict()
+        oH, oW = self.info["oH"], self.info["oW"]
+        self.go_shape = (N, Co, oH, oW)
+        self.x_shape = (N, Ci, H, W)
+        self.w_shape = (Co, Ci, kH, kW)
+
+    def run(self, grad_out, input, grad_weight=None, stream=None):
+        import torch
+        for t, shape, name in ((grad_out, self.go_shape, "grad_out"), (input, self.x_shape, "input")):
+            if tuple(t.shape) != shape or t.dtype != torch.float32 or not t.is_contiguous() or not t.is_cuda:
+                raise ValueError(f"{name} must be a contiguous float32 CUDA tensor of shape {shape}")
+        if grad_weight is None:
+            grad_weight = torch.empty(self.w_shape, dtype=torch.float32, device=grad_out.device)
+        if (tuple(grad_weight.shape) != self.w_shape or grad_weight.dtype != torch.float32
+                or not grad_weight.is_contiguous() or not grad_weight.is_cuda):
+            raise ValueError(f"grad_weight must be a contiguous float32 CUDA tensor of shape {self.w_shape}")
+        st = self._lib.wgrad_run(self._h, ctypes.c_void_p(grad_out.data_ptr()), ctypes.c_void_p(input.data_ptr()),
+                                 ctypes.c_void_p(grad_weight.data_ptr()), _stream_handle(stream))
+        if st != 0:
+            raise DgradError(st, "wgrad_run")
+        return grad_weight
+
+    def check(self):
+        st = self._lib.wgrad_plan_check(self._h)
+        if st != 0:
+            raise DgradError(st, "wgrad_plan_check")
+
+    def close(self):
+        if self._h:
+            self._lib.wgrad_plan_destroy(self._h)
+            self._h = ctypes.c_void_p()
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

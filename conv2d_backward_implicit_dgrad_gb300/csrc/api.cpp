@@ -31,6 +31,33 @@ struct dgrad_plan_s {
     int frame_packed;      // grad_out has been packed into the frame at least once
 };
 
+// cuTensorMapEncodeTiled from the driver, looked up once through the
+// runtime (no link-time dependency on the driver library).
+// The CUDA error behind the last DGRAD_ERR_CUDA of this thread.
+static thread_local cudaError_t g_last_cuda = cudaSuccess;
+
+dgrad_status_t dgrad::cuda_status(cudaError_t e) {
+    if (e == cudaSuccess) return DGRAD_OK;
+    g_last_cuda = e;
+    cudaGetLastError();   // clear the (non-sticky) error
+    return DGRAD_ERR_CUDA;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 dgrad::tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+        cudaGetLastError();
+    });
+    return fn;
+}
+
 namespace {
 
 using dgrad::Geometry;
@@ -38,15 +65,7 @@ using dgrad::Tiling;
 
 constexpr long long kTimeoutNs = 1000000000LL;   // bounded in-kernel waits: 1 s
 
-// The CUDA error behind the last DGRAD_ERR_CUDA of this thread.
-thread_local cudaError_t g_last_cuda = cudaSuccess;
-
-dgrad_status_t cuda_status(cudaError_t e) {
-    if (e == cudaSuccess) return DGRAD_OK;
-    g_last_cuda = e;
-    cudaGetLastError();   // clear the (non-sticky) error
-    return DGRAD_ERR_CUDA;
-}
+using dgrad::cuda_status;
 
 size_t go_elems(const Geometry &g) { return (size_t)g.N * g.Co * g.oH * g.oW; }
 size_t w_elems(const Geometry &g) { return (size_t)g.Co * g.Ci * g.kH * g.kW; }
@@ -124,28 +143,11 @@ void fill_params(dgrad_plan_s *pl) {
     f.vec = plane % 4 == 0 ? 1 : 0;
 }
 
-// cuTensorMapEncodeTiled from the driver, looked up once through the
-// runtime (no link-time dependency on the driver library).
-PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void *ptr = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-        cudaGetLastError();
-    });
-    return fn;
-}
-
 // Tensor map of the packed frame [positions][co_v] (fp32): boxes of 32
 // channels (128 bytes, 128-byte swizzle: the MMA's K-major operand layout)
 // by a_box_rows positions; rows past the frame read as zeros.
 dgrad_status_t encode_frame_map(dgrad_plan_s *pl) {
-    auto fn = tensor_map_encoder();
+    auto fn = dgrad::tensor_map_encoder();
     if (!fn) return DGRAD_ERR_CUDA;
     const cuuint64_t dims[2] = {(cuuint64_t)pl->t.co_v, (cuuint64_t)pl->g.positions};
     const cuuint64_t strides[1] = {(cuuint64_t)pl->t.co_v * 4};

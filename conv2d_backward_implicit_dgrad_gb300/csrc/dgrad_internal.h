@@ -6,6 +6,7 @@
 #include <cstdint>
 
 #include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
 #include "dgrad.h"
@@ -72,6 +73,14 @@ struct Geometry {
     long long positions;   // N * Hv * Wp
     int max_shift;
 };
+
+// cuTensorMapEncodeTiled from the driver, looked up once through the runtime
+// (no link-time dependency on the driver library); NULL if unavailable.
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
+
+// DGRAD_OK for cudaSuccess; otherwise records the error for
+// dgrad_cuda_error_string, clears it and returns DGRAD_ERR_CUDA.
+dgrad_status_t cuda_status(cudaError_t e);
 
 dgrad_status_t make_geometry(int N, int Ci, int H, int W, int Co, int kH, int kW,
                              int stride, int pad_h, int pad_w, Geometry *g);

@@ -23,7 +23,7 @@ def header_functions():
             continue
         src = open(os.path.join(ROOT, "include", fn)).read()
         src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
-        for m in re.finditer(r"^[A-Za-z_][\w\s\*]*?\b(dgrad_\w+)\s*\(", src, flags=re.M):
+        for m in re.finditer(r"^[A-Za-z_][\w\s\*]*?\b((?:dgrad|wgrad)_\w+)\s*\(", src, flags=re.M):
             names.add(m.group(1))
     return names
 
@@ -318,3 +318,95 @@ def test_split_arithmetic_bound():
     assert np.all(np.abs(split - ref) <= 2.0 ** -20 * mag)
     one = oracle.dgrad(go_hi, w_hi, H, W, s, p, p, with_mag=False)[0]
     assert np.max(np.abs(one - ref) / np.maximum(mag, 1e-30)) > 2.0 ** -16
+
+
+# ----------------------------------------------------------------- weight gradient: plan tables
+WG_SHAPES = [
+    # N, Ci, Co, H, W, kH, kW, s, ph, pw
+    (2, 3, 4, 8, 8, 3, 3, 1, 1, 1),
+    (1, 5, 33, 10, 9, 3, 3, 2, 0, 0),
+    (3, 65, 4, 7, 13, 3, 3, 3, 1, 1),
+    (1, 129, 33, 6, 10, 1, 1, 2, 0, 0),
+    (1, 3, 4, 23, 21, 7, 7, 2, 3, 3),
+    (2, 5, 20, 12, 14, 2, 2, 2, 0, 0),
+    (1, 3, 1, 11, 17, 3, 5, 1, 2, 1),
+    (1, 65, 33, 17, 19, 4, 3, 2, 1, 2),
+    (1, 3, 4, 2, 2, 3, 3, 2, 1, 1),
+    (2, 4, 300, 9, 7, 3, 3, 1, 1, 1),
+]
+
+
+def emulate_wgrad(go, x, kH, kW, s, ph, pw):
+    """The wgrad kernels' arithmetic in numpy, driven by the library's tables:
+    grad_out and input position frames, one GEMM row per (tap, input channel)
+    reading its input copy at the tap's K offset, row tiles and the reduction's
+    index map back to OIHW."""
+    N, Co, oH, oW = go.shape
+    _, Ci, H, W = x.shape
+    info = dg.wgrad_describe(N, Ci, H, W, Co, kH, kW, s, ph, pw)
+    tab = dg.wgrad_describe_taps(N, Ci, H, W, Co, kH, kW, s, ph, pw)
+    Wf, Kimg, Lx, Ty = info["Wf"], info["Kimg"], info["Lx"], tab["Ty"]
+    assert Wf % 4 == 0 and Kimg % 32 == 0 and Lx % 4 == 0 and Kimg >= oH * Wf
+    gf = np.zeros((N, Co, Kimg))
+    for oh in range(oH):
+        gf[:, :, oh * Wf:oh * Wf + oW] = go[:, :, oh, :]
+    nc = info["n_copies"]
+    xc = np.zeros((nc, N, Ci, Lx))
+    for c in range(nc):
+        kw, rh = tab["copy_kw"][c], tab["copy_rh"][c]
+        for k in range(Lx):
+            y, u = divmod(k, Wf)
+            ih, iw = s * (y - Ty) + rh, s * u + kw - pw
+            if u < oW and 0 <= ih < H and 0 <= iw < W:
+                xc[c, :, :, k] = x[:, :, ih, iw]
+    dw = np.full((Co, Ci, kH * kW), np.nan)
+    seg_rows = info["seg_rows"]
+    cpt = -(-Ci // seg_rows)
+    spt = 128 // seg_rows
+    n_segs = kH * kW * cpt
+    assert info["n_mt"] == -(-n_segs // spt)
+    for t in range(kH * kW):
+        off = tab["offset"][t]
+        assert off % 4 == 0 and Kimg + off <= Lx      # every 32-position window stays in the copy's plane
+        rows = xc[tab["copy"][t], :, :, off:off + Kimg]   # [N, Ci, Kimg]
+        prod = np.einsum("nck,nik->ci", gf, rows)
+        for ci in range(Ci):
+            seg = t * cpt + ci // seg_rows
+            mt, row = divmod(seg, spt)
+            row = row * seg_rows + ci % seg_rows
+            assert mt < info["n_mt"] and row < 128
+            assert np.isnan(dw[0, ci, t])                  # each (tap, ci) row is produced once
+            dw[:, ci, t] = prod[:, ci]
+    assert not np.isnan(dw).any()
+    return dw.reshape(Co, Ci, kH, kW)
+
+
+@pytest.mark.parametrize("shape", WG_SHAPES)
+def test_emulated_wgrad_matches_oracle(shape):
+    N, Ci, Co, H, W, kH, kW, s, ph, pw = shape
+    oH, oW = (H + 2 * ph - kH) // s + 1, (W + 2 * pw - kW) // s + 1
+    rng = np.random.default_rng(60)
+    go = rng.standard_normal((N, Co, oH, oW)).astype(np.float32)
+    x = rng.standard_normal((N, Ci, H, W)).astype(np.float32)
+    emu = emulate_wgrad(go.astype(np.float64), x.astype(np.float64), kH, kW, s, ph, pw)
+    ref, mag = oracle.wgrad(go, x, kH, kW, s, ph, pw)
+    assert np.abs(emu - ref).max() <= 1e-12 * max(1.0, mag.max())
+
+
+def test_wgrad_plans():
+    for name in ORDER:
+        wl = WORKLOADS[name]
+        d = dg.wgrad_describe(*wl.plan_args(), sm_count=152)
+        assert d["oH"] == wl.oH and d["oW"] == wl.oW
+        assert d["smem_bytes"] <= 232448 and d["tmem_cols"] <= 512 and 16 <= d["slice_n"] <= 256
+        assert d["n_units"] == d["n_mt"] * d["n_nt"] * d["n_ks"] and d["grid"] <= 152
+        assert d["useful_flops"] == 2 * wl.N * wl.Co * wl.oH * wl.oW * wl.Ci * wl.kH * wl.kW
+    for bad, status in (((0, 1, 4, 4, 1, 3, 3, 1, 1, 1), 1), ((1, 1, 2, 2, 1, 5, 5, 1, 0, 0), 1),
+                        ((1, 1, 32, 32, 1, 3, 3, 5, 1, 1), 2)):
+        with pytest.raises(dg.DgradError) as e:
+            dg.wgrad_describe(*bad)
+        assert e.value.status == status
+    for prec in ("fp32", "tf32x3"):
+        with pytest.raises(dg.DgradError) as e:
+            dg.wgrad_describe(2, 3, 8, 8, 4, 3, 3, 1, 1, 1, prec)
+        assert e.value.status == 2

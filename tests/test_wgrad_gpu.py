@@ -1,0 +1,129 @@
+"""GPU parity of the weight gradient (wgrad) against the CPU oracle (O-w).
+
+Bar: the TF32 bar of the dgrad path, per element
+|gpu - ref| <= 2e-3 * sum|terms|, and exactly 0 where no term reaches the
+element.  grad_weight is poisoned with NaN before every run, so an element
+the kernels fail to write fails the bar.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import conv2d_backward_implicit_dgrad_gb300 as dg
+from conv2d_backward_implicit_dgrad_gb300.workloads import ORDER, WORKLOADS, make_inputs
+
+pytestmark = pytest.mark.gpu
+
+TF32_REL_TERMS = 2e-3
+
+
+def out_ext(n, k, s, p):
+    return (n + 2 * p - k) // s + 1
+
+
+def inputs(N, Ci, Co, H, W, kH, kW, s, ph, pw, seed):
+    g = torch.Generator().manual_seed(seed)
+    go = torch.randn((N, Co, out_ext(H, kH, s, ph), out_ext(W, kW, s, pw)), generator=g)
+    x = torch.randn((N, Ci, H, W), generator=g)
+    return go, x
+
+
+def run_gpu(args, go, x):
+    N, Ci, H, W, Co, kH, kW, s, ph, pw = args
+    with dg.WgradPlan(*args, precision="tf32") as plan:
+        dw = torch.full((Co, Ci, kH, kW), float("nan"), device="cuda")
+        plan.run(go.cuda(), x.cuda(), dw)
+        torch.cuda.synchronize()
+        plan.check()
+        info = plan.info
+    return dw.cpu().double().numpy(), info
+
+
+def check(args, go, x):
+    N, Ci, H, W, Co, kH, kW, s, ph, pw = args
+    ref, mag = oracle.wgrad(go, x, kH, kW, s, ph, pw)
+    gpu, info = run_gpu(args, go, x)
+    assert np.isfinite(gpu).all(), "non-finite output (unwritten element?)"
+    err = np.abs(gpu - ref)
+    bad = err > TF32_REL_TERMS * mag
+    pos = mag > 0
+    worst = np.max(err[pos] / mag[pos]) if pos.any() else 0.0
+    assert not bad.any(), f"{bad.sum()} elements over the bound; worst err/sum|terms| = {worst:.3e}"
+    assert np.all(gpu[~pos] == 0)
+    rel = np.linalg.norm(gpu - ref) / max(np.linalg.norm(ref), 1e-300)
+    assert rel < 1e-3, rel
+    return info
+
+
+EDGE = [
+    # N, Ci, Co, H, W, kH, kW, s, ph, pw
+    (1, 1, 1, 5, 7, 3, 3, 1, 0, 0),
+    (3, 3, 4, 9, 11, 5, 5, 1, 1, 1),
+    (1, 5, 33, 10, 9, 3, 3, 2, 0, 0),
+    (3, 65, 4, 7, 13, 3, 3, 3, 1, 1),
+    (1, 129, 33, 6, 10, 1, 1, 2, 0, 0),
+    (1, 3, 4, 23, 21, 7, 7, 2, 3, 3),
+    (3, 5, 33, 12, 14, 2, 2, 2, 0, 0),
+    (1, 3, 1, 11, 17, 3, 5, 1, 2, 1),
+    (1, 65, 33, 17, 19, 4, 3, 2, 1, 2),
+    (1, 3, 4, 2, 2, 3, 3, 2, 1, 1),        # a kernel row that only meets padding
+    (1, 4, 3, 1, 1, 1, 1, 2, 1, 1),        # no term reaches any weight element
+    (3, 16, 20, 31, 29, 3, 3, 1, 1, 1),
+    (1, 20, 40, 40, 40, 3, 3, 4, 1, 1),    # stride 4
+    (2, 8, 300, 9, 7, 3, 3, 1, 1, 1),      # two column tiles
+    (2, 200, 16, 6, 6, 3, 3, 1, 1, 1),     # input channels over one segment
+]
+
+
+@pytest.mark.parametrize("shape", EDGE)
+def test_wgrad_edge_shapes(shape):
+    N, Ci, Co, H, W, kH, kW, s, ph, pw = shape
+    go, x = inputs(*shape, seed=90)
+    check((N, Ci, H, W, Co, kH, kW, s, ph, pw), go, x)
+
+
+@pytest.mark.parametrize("name", ORDER)
+def test_wgrad_workloads(name):
+    """Every workload at full size against the whole oracle result."""
+    wl = WORKLOADS[name]
+    go, _ = make_inputs(wl, 0)
+    x = torch.randn((wl.N, wl.Ci, wl.H, wl.W), generator=torch.Generator().manual_seed(91))
+    info = check(wl.plan_args(), go, x)
+    assert info["grid"] <= 152
+
+
+def test_wgrad_overwrites_and_leaves_inputs_alone():
+    args = (2, 16, 12, 12, 24, 3, 3, 1, 1, 1)
+    N, Ci, H, W, Co, kH, kW, s, ph, pw = args
+    go, x = inputs(N, Ci, Co, H, W, kH, kW, s, ph, pw, seed=92)
+    g, xx = go.cuda(), x.cuda()
+    g0, x0 = g.clone(), xx.clone()
+    with dg.WgradPlan(*args) as plan:
+        a = plan.run(g, xx, torch.full((Co, Ci, kH, kW), 7.0, device="cuda"))
+        b = plan.run(g, xx, torch.full((Co, Ci, kH, kW), -3.0, device="cuda"))
+        torch.cuda.synchronize()
+        plan.check()
+    assert torch.equal(a, b)            # deterministic, and nothing of the old contents survives
+    assert torch.equal(g, g0) and torch.equal(xx, x0)
+
+
+def test_wgrad_rejects_bad_arguments():
+    args = (1, 8, 8, 8, 8, 3, 3, 1, 1, 1)
+    with dg.WgradPlan(*args) as plan:
+        lib = dg.load_library()
+        go = torch.zeros((1, 8, 8, 8), device="cuda")
+        x = torch.zeros((1, 8, 8, 8), device="cuda")
+        buf = torch.zeros(8 * 8 * 9 + 16, device="cuda")
+        stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+        P = lambda t, off=0: ctypes.c_void_p(t.data_ptr() + off)
+        assert lib.wgrad_run(plan._h, P(go), P(x), P(buf, 4), stream) == 3      # misaligned
+        assert lib.wgrad_run(plan._h, P(go), P(x), None, stream) == 3           # NULL
+        assert lib.wgrad_run(plan._h, P(go), P(x), P(x), stream) == 4           # grad_weight over the input
+        torch.cuda.synchronize()
+        plan.check()
+    with pytest.raises(dg.DgradError) as e:
+        dg.WgradPlan(*args, precision="fp32")
+    assert e.value.status == 2
