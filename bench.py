@@ -11,6 +11,9 @@ dgrad_pack_grad_out) for the roofline line.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--precision tf32|tf32x3|fp32]
   python bench.py --impl reference ...   # the CPU oracle on the host cores
+  python bench.py --all ...              # plus one info line per workload and precision, and per workload
+                                         # the weight gradient (wgrad_run) of the same convolution
+  python bench.py --profile [--op wgrad] # W + K steps only, for ncu
 
 With N > 1 (torchrun, one rank per GPU) every rank runs an independent
 replica of the workload (the batch shards with no collective on the data
@@ -324,13 +327,54 @@ def build_line(args, wl, r, world):
     return line
 
 
+def time_wgrad(dg, torch, wl, steps, warmup):
+    """The weight gradient of the same convolution (grad_out and the forward
+    input, seeded), each step after the same L2 flush, CUDA events around
+    wgrad_run (frame pack, tcgen05 split-K GEMM, reduction)."""
+    from conv2d_backward_implicit_dgrad_gb300.workloads import make_inputs
+    go_h, _ = make_inputs(wl, seed=0)
+    x_h = torch.randn((wl.N, wl.Ci, wl.H, wl.W), generator=torch.Generator().manual_seed(1))
+    go, x = go_h.cuda(), x_h.cuda()
+    dw = torch.empty((wl.Co, wl.Ci, wl.kH, wl.kW), device="cuda")
+    flush = torch.empty(FLUSH_BYTES // 4, device="cuda")
+    stream = torch.cuda.current_stream()
+    with dg.WgradPlan(*wl.plan_args(), precision="tf32") as plan:
+        for _ in range(max(3, warmup)):
+            flush.zero_()
+            plan.run(go, x, dw, stream)
+        torch.cuda.synchronize()
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(steps)]
+        for i in range(steps):
+            flush.zero_()
+            ev[i][0].record(stream)
+            plan.run(go, x, dw, stream)
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        plan.check()
+        info = plan.info
+    ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
+    return {"ms_per_step": ms, "flops": info["useful_flops"], "bytes": info["algorithmic_bytes"], "plan": info}
+
+
 def profile_steps(dg, torch, wl, args):
     """W warm-up steps then K steps (dgrad_run), each after an L2 flush; nothing else."""
     from conv2d_backward_implicit_dgrad_gb300.workloads import make_inputs
     go_h, w_h = make_inputs(wl, 0)
     go, w = go_h.cuda(), w_h.cuda()
-    gi = torch.empty(wl.gi_shape, device="cuda")
     flush = torch.empty(FLUSH_BYTES // 4, device="cuda")
+    if args.op == "wgrad":
+        x = torch.randn((wl.N, wl.Ci, wl.H, wl.W), generator=torch.Generator().manual_seed(1)).cuda()
+        dw = torch.empty((wl.Co, wl.Ci, wl.kH, wl.kW), device="cuda")
+        with dg.WgradPlan(*wl.plan_args(), precision="tf32") as plan:
+            for _ in range(args.warmup + args.steps):
+                flush.zero_()
+                plan.run(go, x, dw)
+            torch.cuda.synchronize()
+            plan.check()
+            print(json.dumps({"profile": wl.name, "op": "wgrad", "steps": args.steps, "warmup": args.warmup,
+                              "plan": plan.info}), flush=True)
+        return 0
+    gi = torch.empty(wl.gi_shape, device="cuda")
     with dg.Plan(*wl.plan_args(), precision=args.precision) as plan:
         for _ in range(args.warmup + args.steps):
             flush.zero_()
@@ -352,6 +396,8 @@ def main():
     ap.add_argument("--precision", default="tf32", choices=["tf32", "tf32x3", "fp32"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--all", action="store_true", help="also print one info line per workload and precision")
+    ap.add_argument("--op", default="dgrad", choices=["dgrad", "wgrad"],
+                    help="with --profile: which operation's kernels run")
     ap.add_argument("--profile", action="store_true",
                     help="only run W + K steps (for ncu captures: few launches, no extra timing loops)")
     args = ap.parse_args()
@@ -411,6 +457,16 @@ def main():
                                                                          "chunk_k", "grid", "n_work",
                                                                          "b_resident", "smem_bytes")}}),
                           flush=True)
+            peaks, src = load_peaks()
+            tf32_peak = peaks["bf16_tflops"] * TF32_OVER_BF16
+            for name in WORKLOAD_ORDER:
+                x = time_wgrad(dg, torch, WORKLOADS[name], 50, 5)
+                tf = x["flops"] / (x["ms_per_step"] * 1e-3) / 1e12
+                print(json.dumps({"info": "wgrad", "workload": name, "precision": "tf32",
+                                  "ms_per_step": x["ms_per_step"], "tflops": tf, "frac_peak": tf / tf32_peak,
+                                  "plan": {k: x["plan"][k] for k in ("n_mt", "n_nt", "n_ks", "slice_n", "n_units",
+                                                                     "grid", "stages", "n_copies")}}),
+                      flush=True)
     if world > 1:
         dist.destroy_process_group()
     return 0

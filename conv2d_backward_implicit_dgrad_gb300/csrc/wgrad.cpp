@@ -124,6 +124,7 @@ dgrad_status_t make_wgrad_geometry(int N, int Ci, int H, int W, int Co, int kH, 
     g.tmem_cols = pow2_at_least(2 * g.bn);
     g.g_elems = (size_t)N * Co * g.Kimg;
     g.x_elems = (size_t)g.n_copies * N * Ci * g.Lx;
+    if ((g.g_elems + g.x_elems) / 4 > (size_t)INT_MAX) return DGRAD_ERR_UNSUPPORTED;   // 32-bit pack indices
     g.part_elems = (size_t)g.n_units * g.bn * 128;
     *out = g;
     return DGRAD_OK;
@@ -195,7 +196,7 @@ void fill_wgrad_params(wgrad_plan_s *pl) {
     dgrad::WgradMainParams &m = pl->mp;
     m.part = pl->part;
     m.err = pl->err;
-    m.n_nt = g.n_nt; m.n_ks = g.n_ks; m.n_units = g.n_units; m.bn = g.bn;
+    m.n_mt = g.n_mt; m.n_nt = g.n_nt; m.n_ks = g.n_ks; m.n_units = g.n_units; m.bn = g.bn;
     m.seg_rows = g.seg_rows; m.spt = g.spt; m.n_segs = g.n_segs; m.cpi = g.cpi;
     m.total_chunks = g.total_chunks; m.cps = g.cps; m.stages = g.stages; m.tmem_cols = g.tmem_cols;
     m.idesc = dgrad::tf32_idesc(128, g.bn);
@@ -213,7 +214,7 @@ void fill_wgrad_params(wgrad_plan_s *pl) {
     q.x4 = (long long)(g.x_elems / 4);
     dgrad::WgradReduceParams &r = pl->rp;
     r.part = pl->part;
-    r.Co = g.Co; r.Ci = g.Ci; r.taps = g.taps; r.bn = g.bn; r.n_nt = g.n_nt; r.n_ks = g.n_ks;
+    r.Co = g.Co; r.Ci = g.Ci; r.taps = g.taps; r.bn = g.bn; r.n_mt = g.n_mt; r.n_nt = g.n_nt; r.n_ks = g.n_ks;
     r.seg_rows = g.seg_rows; r.cpt = g.cpt; r.spt = g.spt; r.n_segs = g.n_segs;
     r.total = (long long)g.n_mt * g.n_nt * g.bn * 128;
 }

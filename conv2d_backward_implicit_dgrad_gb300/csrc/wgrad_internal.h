@@ -55,9 +55,9 @@ struct WgradPackParams {
 struct WgradMainParams {
     CUtensorMap x_map;   // xc as {Lx, Ci, N, n_copies}, box {32, seg_rows, 1, 1}, 128-byte swizzle
     CUtensorMap g_map;   // gf as {Kimg, Co, N}, box {32, bn, 1}, 128-byte swizzle
-    float *part;         // partial tiles [unit][bn][128]
+    float *part;         // partial tiles [unit][bn][128], unit = (ks * n_mt + mt) * n_nt + nt
     uint32_t *err;
-    int n_nt, n_ks, n_units, bn, seg_rows, spt, n_segs, cpi, total_chunks, cps, stages, tmem_cols;
+    int n_mt, n_nt, n_ks, n_units, bn, seg_rows, spt, n_segs, cpi, total_chunks, cps, stages, tmem_cols;
     uint32_t idesc;
     long long timeout_ns;
     int4 seg[kWgMaxSegs];   // x: input copy, y: first input channel, z: K offset (elements)
@@ -66,7 +66,7 @@ struct WgradMainParams {
 struct WgradReduceParams {
     const float *part;
     float *dw;
-    int Co, Ci, taps, bn, n_nt, n_ks, seg_rows, cpt, spt, n_segs;
+    int Co, Ci, taps, bn, n_mt, n_nt, n_ks, seg_rows, cpt, spt, n_segs;
     long long total;   // n_mt * n_nt * bn * 128 partial elements per split
 };
 

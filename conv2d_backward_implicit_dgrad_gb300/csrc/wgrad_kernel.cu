@@ -61,10 +61,15 @@ struct WUnit {
     int mt, nt, c0, c1, s0, s1;
 };
 
+// Unit w = (ks * n_mt + mt) * n_nt + nt: the K split varies slowest, so the
+// units running at the same time cover every row and column tile of a few
+// K ranges and share their frame data in L2 (an input-copy chunk is read by
+// the kH taps of its column, a grad_out chunk by every row tile).
 __device__ __forceinline__ WUnit decode_unit(const WgradMainParams &p, int w) {
     WUnit u;
-    const int ks = w % p.n_ks;
-    const int rest = w / p.n_ks;
+    const int tiles = p.n_mt * p.n_nt;
+    const int ks = w / tiles;
+    const int rest = w - ks * tiles;
     u.nt = rest % p.n_nt;
     u.mt = rest / p.n_nt;
     u.c0 = ks * p.cps;
@@ -217,50 +222,63 @@ __global__ void __launch_bounds__(kWThreads, 1) wgrad_main_kernel(const __grid_c
 }
 
 // Position frames: gf (grad_out rows padded to Wf, planes to Kimg) and the
-// input copies xc, TF32-rounded; one thread writes 4 consecutive positions.
+// input copies xc, TF32-rounded; one thread writes 4 consecutive positions
+// (32-bit indices: the host keeps both buffers below 2^31 float4 groups).
 __global__ void __launch_bounds__(256) wgrad_pack_kernel(const __grid_constant__ WgradPackParams p) {
-    const long long total = p.g4 + p.x4;
-    const long long step = static_cast<long long>(gridDim.x) * blockDim.x;
-    for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < total; i += step) {
+    const int total = static_cast<int>(p.g4 + p.x4);
+    const int step = gridDim.x * blockDim.x;
+    const int g4 = static_cast<int>(p.g4);
+    const int gper = p.Kimg / 4, xper = p.Lx / 4;
+    const int nci = p.N * p.Ci;
+    const bool g_vec = p.Wf == p.oW;   // frame rows are grad_out rows: 16-byte loads
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < total; i += step) {
         float v[4];
-        if (i < p.g4) {
-            const long long per = p.Kimg / 4;
-            const long long plane = i / per;   // n * Co + co
-            const int k = static_cast<int>(i - plane * per) * 4;
-            const float *src = p.go + plane * static_cast<long long>(p.oH) * p.oW;
+        if (i < g4) {
+            const int plane = i / gper;   // n * Co + co
+            const int k = (i - plane * gper) * 4;
+            const float *src = p.go + static_cast<size_t>(plane) * p.oH * p.oW;
+            int oh = k / p.Wf, ow = k - oh * p.Wf;
+            if (g_vec && oh < p.oH) {
+                const float4 t = __ldg(reinterpret_cast<const float4 *>(src + k));
+                v[0] = t.x, v[1] = t.y, v[2] = t.z, v[3] = t.w;
+            } else {
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int oh = (k + e) / p.Wf, ow = (k + e) - oh * p.Wf;
-                v[e] = (oh < p.oH && ow < p.oW) ? dev::round_tf32(__ldg(src + oh * p.oW + ow)) : 0.f;
+                for (int e = 0; e < 4; ++e) {
+                    v[e] = (oh < p.oH && ow < p.oW) ? __ldg(src + oh * p.oW + ow) : 0.f;
+                    if (++ow == p.Wf) ow = 0, ++oh;
+                }
             }
-            *reinterpret_cast<float4 *>(p.gf + i * 4) = make_float4(v[0], v[1], v[2], v[3]);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) v[e] = dev::round_tf32(v[e]);
+            *reinterpret_cast<float4 *>(p.gf + static_cast<size_t>(i) * 4) = make_float4(v[0], v[1], v[2], v[3]);
         } else {
-            const long long j = i - p.g4;
-            const long long per = p.Lx / 4;
-            const long long plane = j / per;   // (copy * N + n) * Ci + ci
-            const int k = static_cast<int>(j - plane * per) * 4;
-            const long long nci = plane % (static_cast<long long>(p.N) * p.Ci);
-            const int c = static_cast<int>(plane / (static_cast<long long>(p.N) * p.Ci));
-            const int kw = c / p.n_rh, rh = p.rh_list[c % p.n_rh];
-            const float *src = p.x + nci * static_cast<long long>(p.H) * p.W;
+            const int j = i - g4;
+            const int plane = j / xper;   // (copy * N + n) * Ci + ci
+            const int k = (j - plane * xper) * 4;
+            const int c = plane / nci;
+            const int kw = c / p.n_rh, rh = p.rh_list[c - (c / p.n_rh) * p.n_rh];
+            const float *src = p.x + static_cast<size_t>(plane - c * nci) * p.H * p.W;
+            int y = k / p.Wf, u = k - y * p.Wf;
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                const int y = (k + e) / p.Wf, u = (k + e) - y * p.Wf;
                 const int ih = p.s * (y - p.Ty) + rh, iw = p.s * u + kw - p.pw;
                 v[e] = (u < p.oW && ih >= 0 && ih < p.H && iw >= 0 && iw < p.W)
                            ? dev::round_tf32(__ldg(src + ih * p.W + iw))
                            : 0.f;
+                if (++u == p.Wf) u = 0, ++y;
             }
-            *reinterpret_cast<float4 *>(p.xc + j * 4) = make_float4(v[0], v[1], v[2], v[3]);
+            *reinterpret_cast<float4 *>(p.xc + static_cast<size_t>(j) * 4) = make_float4(v[0], v[1], v[2], v[3]);
         }
     }
 }
 
 // grad_weight from the partial tiles: thread i takes partial element (row
 // tile, column tile, column, row), row fastest (coalesced reads), sums its
-// K splits in order and writes the OIHW element the row stands for.
+// K splits (eight independent running sums, combined in a fixed order) and
+// writes the OIHW element the row stands for.
 __global__ void __launch_bounds__(256) wgrad_reduce_kernel(const __grid_constant__ WgradReduceParams p) {
     const long long step = static_cast<long long>(gridDim.x) * blockDim.x;
+    const size_t split_stride = static_cast<size_t>(p.n_mt) * p.n_nt * p.bn * 128;   // one K split of every tile
     for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < p.total; i += step) {
         const int row = static_cast<int>(i & 127);
         long long rest = i >> 7;
@@ -275,10 +293,17 @@ __global__ void __launch_bounds__(256) wgrad_reduce_kernel(const __grid_constant
         const int ci = (seg - t * p.cpt) * p.seg_rows + (row - sl * p.seg_rows);
         const int co = nt * p.bn + col;
         if (ci >= p.Ci || co >= p.Co) continue;
-        const size_t u0 = (static_cast<size_t>(mt) * p.n_nt + nt) * p.n_ks;
-        float sum = 0.f;
-        for (int ks = 0; ks < p.n_ks; ++ks)
-            sum += __ldg(p.part + ((u0 + ks) * p.bn + col) * 128 + row);
+        const float *src = p.part + ((static_cast<size_t>(mt) * p.n_nt + nt) * p.bn + col) * 128 + row;
+        float acc[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[j] = 0.f;
+        int ks = 0;
+        for (; ks + 8 <= p.n_ks; ks += 8) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) acc[j] += __ldg(src + static_cast<size_t>(ks + j) * split_stride);
+        }
+        for (int j = 0; ks < p.n_ks; ++ks, ++j) acc[j] += __ldg(src + static_cast<size_t>(ks) * split_stride);
+        const float sum = ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
         p.dw[(static_cast<size_t>(co) * p.Ci + ci) * p.taps + t] = sum;
     }
 }
