@@ -222,52 +222,68 @@ __global__ void __launch_bounds__(kWThreads, 1) wgrad_main_kernel(const __grid_c
 }
 
 // Position frames: gf (grad_out rows padded to Wf, planes to Kimg) and the
-// input copies xc, TF32-rounded; one thread writes 4 consecutive positions
-// (32-bit indices: the host keeps both buffers below 2^31 float4 groups).
+// input copies xc, TF32-rounded.  Thread item i writes the 4 consecutive
+// positions 4i .. 4i+3 of the concatenated buffers (32-bit indices: the host
+// keeps both below 2^31 groups); a thread takes kUnroll items a grid-stride
+// apart per pass and issues all their loads before any store.
+__device__ __forceinline__ float4 wgrad_pack_item(const WgradPackParams &p, int i, int g4, int gper, int xper,
+                                                  int nci, bool g_vec) {
+    float v[4];
+    if (i < g4) {
+        const int plane = i / gper;   // n * Co + co
+        const int k = (i - plane * gper) * 4;
+        const float *src = p.go + static_cast<size_t>(plane) * p.oH * p.oW;
+        int oh = k / p.Wf, ow = k - oh * p.Wf;
+        if (g_vec && oh < p.oH) {
+            const float4 t = __ldg(reinterpret_cast<const float4 *>(src + k));
+            v[0] = t.x, v[1] = t.y, v[2] = t.z, v[3] = t.w;
+        } else {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                v[e] = (oh < p.oH && ow < p.oW) ? __ldg(src + oh * p.oW + ow) : 0.f;
+                if (++ow == p.Wf) ow = 0, ++oh;
+            }
+        }
+    } else {
+        const int j = i - g4;
+        const int plane = j / xper;   // (copy * N + n) * Ci + ci
+        const int k = (j - plane * xper) * 4;
+        const int c = plane / nci;
+        const int kw = c / p.n_rh, rh = p.rh_list[c - kw * p.n_rh];
+        const float *src = p.x + static_cast<size_t>(plane - c * nci) * p.H * p.W;
+        int y = k / p.Wf, u = k - y * p.Wf;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int ih = p.s * (y - p.Ty) + rh, iw = p.s * u + kw - p.pw;
+            v[e] = (u < p.oW && ih >= 0 && ih < p.H && iw >= 0 && iw < p.W) ? __ldg(src + ih * p.W + iw) : 0.f;
+            if (++u == p.Wf) u = 0, ++y;
+        }
+    }
+    return make_float4(dev::round_tf32(v[0]), dev::round_tf32(v[1]), dev::round_tf32(v[2]), dev::round_tf32(v[3]));
+}
+
 __global__ void __launch_bounds__(256) wgrad_pack_kernel(const __grid_constant__ WgradPackParams p) {
+    constexpr int kUnroll = 4;
     const int total = static_cast<int>(p.g4 + p.x4);
     const int step = gridDim.x * blockDim.x;
     const int g4 = static_cast<int>(p.g4);
     const int gper = p.Kimg / 4, xper = p.Lx / 4;
     const int nci = p.N * p.Ci;
     const bool g_vec = p.Wf == p.oW;   // frame rows are grad_out rows: 16-byte loads
-    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < total; i += step) {
-        float v[4];
-        if (i < g4) {
-            const int plane = i / gper;   // n * Co + co
-            const int k = (i - plane * gper) * 4;
-            const float *src = p.go + static_cast<size_t>(plane) * p.oH * p.oW;
-            int oh = k / p.Wf, ow = k - oh * p.Wf;
-            if (g_vec && oh < p.oH) {
-                const float4 t = __ldg(reinterpret_cast<const float4 *>(src + k));
-                v[0] = t.x, v[1] = t.y, v[2] = t.z, v[3] = t.w;
-            } else {
+    for (int i0 = blockIdx.x * blockDim.x + threadIdx.x; i0 < total; i0 += kUnroll * step) {
+        float4 v[kUnroll];
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    v[e] = (oh < p.oH && ow < p.oW) ? __ldg(src + oh * p.oW + ow) : 0.f;
-                    if (++ow == p.Wf) ow = 0, ++oh;
-                }
+        for (int u = 0; u < kUnroll; ++u) {
+            const int i = i0 + u * step;
+            if (i < total) v[u] = wgrad_pack_item(p, i, g4, gper, xper, nci, g_vec);
+        }
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const int i = i0 + u * step;
+            if (i < total) {
+                float *dst = i < g4 ? p.gf + static_cast<size_t>(i) * 4 : p.xc + static_cast<size_t>(i - g4) * 4;
+                *reinterpret_cast<float4 *>(dst) = v[u];
             }
-#pragma unroll
-            for (int e = 0; e < 4; ++e) v[e] = dev::round_tf32(v[e]);
-            *reinterpret_cast<float4 *>(p.gf + static_cast<size_t>(i) * 4) = make_float4(v[0], v[1], v[2], v[3]);
-        } else {
-            const int j = i - g4;
-            const int plane = j / xper;   // (copy * N + n) * Ci + ci
-            const int k = (j - plane * xper) * 4;
-            const int c = plane / nci;
-            const int kw = c / p.n_rh, rh = p.rh_list[c - (c / p.n_rh) * p.n_rh];
-            const float *src = p.x + static_cast<size_t>(plane - c * nci) * p.H * p.W;
-            int y = k / p.Wf, u = k - y * p.Wf;
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int ih = p.s * (y - p.Ty) + rh, iw = p.s * u + kw - p.pw;
-                v[e] = (u < p.oW && ih >= 0 && ih < p.H && iw >= 0 && iw < p.W)
-                           ? dev::round_tf32(__ldg(src + ih * p.W + iw))
-                           : 0.f;
-                if (++u == p.Wf) u = 0, ++y;
-            }
-            *reinterpret_cast<float4 *>(p.xc + static_cast<size_t>(j) * 4) = make_float4(v[0], v[1], v[2], v[3]);
         }
     }
 }
@@ -312,8 +328,8 @@ __global__ void __launch_bounds__(256) wgrad_reduce_kernel(const __grid_constant
 
 cudaError_t launch_wgrad_pack(const WgradPackParams &p, cudaStream_t stream) {
     const long long total = p.g4 + p.x4;
-    long long blocks = (total + 255) / 256;
-    if (blocks > 152LL * 16) blocks = 152LL * 16;
+    long long blocks = (total + 4 * 256 - 1) / (4 * 256);   // four items per thread
+    if (blocks > 152LL * 64) blocks = 152LL * 64;
     if (blocks < 1) blocks = 1;
     wgrad_pack_kernel<<<static_cast<int>(blocks), 256, 0, stream>>>(p);
     return cudaGetLastError();
