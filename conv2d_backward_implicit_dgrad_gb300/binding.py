@@ -23,7 +23,7 @@ STATUS = {
     8: "DGRAD_ERR_NO_DEVICE", 9: "DGRAD_ERR_WRONG_DEVICE",
 }
 PREC = {"fp32": 0, "tf32": 1, "tf32x3": 2}
-PATH = {"auto": 0, "simt": 1, "tcgen05": 2}
+PATH = {"auto": 0, "simt": 1, "tcgen05": 2, "col2im": 3}
 PATH_NAME = {v: k for k, v in PATH.items()}
 
 # Every function declared in include/dgrad.h (checked by the CPU tests).

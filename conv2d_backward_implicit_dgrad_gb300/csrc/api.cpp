@@ -18,6 +18,7 @@ struct dgrad_plan_s {
     dgrad::Geometry g;
     dgrad::Tiling t;
     dgrad::MainParams mp;
+    dgrad::C2iParams cp;   // col2im path
     dgrad::PrepackParams pp;
     float *wp;             // packed weights (device)
     float *frame;          // packed grad_out frame (device), tensor-copy mode only
@@ -88,7 +89,7 @@ void fill_info(const Geometry &g, const Tiling &t, int precision, size_t ws, dgr
     info->n_work = t.n_work;
     info->grid = t.path == DGRAD_PATH_SIMT ? (int)t.n_work : t.grid;
     info->b_resident = t.b_resident;
-    info->a_source = t.path == DGRAD_PATH_TCGEN05 ? (t.a_tma ? 1 : 2) : 0;
+    info->a_source = t.path == DGRAD_PATH_TCGEN05 ? (t.a_tma ? 1 : 2) : (t.path == DGRAD_PATH_COL2IM ? 1 : 0);
     info->smem_bytes = t.smem_bytes;
     info->tmem_cols = t.tmem_cols;
     info->group_taps = t.grouped ? 1 : (t.pgroup ? 2 : 0);
@@ -121,6 +122,12 @@ void fill_params(dgrad_plan_s *pl) {
     pl->mp.timeout_ns = kTimeoutNs;
     dgrad::fill_prepack_params(g, t, round, &pl->pp);
     pl->pp.wp = pl->wp;
+    if (t.path == DGRAD_PATH_COL2IM) {
+        dgrad::fill_c2i_params(g, t, &pl->cp);
+        pl->cp.wp = pl->wp;
+        pl->cp.err = pl->err;
+        pl->cp.timeout_ns = kTimeoutNs;
+    }
 
     dgrad::FramePackParams &f = pl->fp;
     std::memset(&f, 0, sizeof(f));
@@ -194,6 +201,13 @@ dgrad_status_t launch_main_on(dgrad_plan_s *plan, const float *grad_out, float *
     mp.gi = grad_input;
     mp.relu_in = relu_in;
     mp.accumulate = accumulate;
+    if (plan->t.path == DGRAD_PATH_COL2IM) {
+        dgrad::C2iParams cp = plan->cp;
+        cp.gi = grad_input;
+        cp.relu_in = relu_in;
+        cp.accumulate = accumulate;
+        return cuda_status(dgrad::launch_c2i(cp, plan->t, s, true));
+    }
     cudaError_t e = plan->t.path == DGRAD_PATH_TCGEN05 ? dgrad::launch_tc(mp, plan->t, s, true)
                                                        : dgrad::launch_simt(mp, plan->t, s);
     return cuda_status(e);
@@ -283,7 +297,8 @@ dgrad_status_t dgrad_plan_ex(int N, int Ci, int H, int W, int Co, int kH, int kW
     // Workspace: the error word (256 B), the packed weights, then (tensor-
     // copy mode) the packed grad_out frame, each 256-byte aligned.
     const size_t wp_bytes = (pl->t.packed_bytes + 255) & ~size_t(255);
-    size_t ws = 256 + wp_bytes + (pl->t.path == DGRAD_PATH_TCGEN05 && pl->t.a_tma ? pl->t.frame_bytes : 0);
+    const bool has_frame = (pl->t.path == DGRAD_PATH_TCGEN05 || pl->t.path == DGRAD_PATH_COL2IM) && pl->t.a_tma;
+    size_t ws = 256 + wp_bytes + (has_frame ? pl->t.frame_bytes : 0);
     void *mem = nullptr;
     if (cudaMalloc(&mem, ws) != cudaSuccess) {
         cudaGetLastError();
@@ -301,8 +316,7 @@ dgrad_status_t dgrad_plan_ex(int N, int Ci, int H, int W, int Co, int kH, int kW
     }
     pl->err = static_cast<uint32_t *>(mem);
     pl->wp = reinterpret_cast<float *>(static_cast<uint8_t *>(mem) + 256);
-    if (pl->t.path == DGRAD_PATH_TCGEN05 && pl->t.a_tma)
-        pl->frame = reinterpret_cast<float *>(static_cast<uint8_t *>(mem) + 256 + wp_bytes);
+    if (has_frame) pl->frame = reinterpret_cast<float *>(static_cast<uint8_t *>(mem) + 256 + wp_bytes);
     pl->workspace_bytes = ws;
     fill_params(pl);
     if (pl->frame && (st = encode_frame_map(pl)) != DGRAD_OK) {
@@ -310,6 +324,7 @@ dgrad_status_t dgrad_plan_ex(int N, int Ci, int H, int W, int Co, int kH, int kW
         delete pl;
         return st;
     }
+    if (pl->t.path == DGRAD_PATH_COL2IM) pl->cp.a_map = pl->mp.a_map;
     *plan_out = pl;
     return DGRAD_OK;
 }

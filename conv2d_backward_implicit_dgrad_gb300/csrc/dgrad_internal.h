@@ -142,6 +142,9 @@ struct Tiling {
     int split;         // 1: TF32X3 (frame rows hold hi and lo halves; three K passes per channel chunk)
     int co_h;          // split: channels of one half of a frame row (a multiple of 32)
     size_t frame_bytes;
+    int c2i_R;         // col2im path: input rows per band (a multiple of the stride)
+    int c2i_pitch;     // col2im path: floats per band row, max((oW - 1)*s + kW, W + pw)
+    int c2i_bands;     // col2im path: N * ceil(H / R)
     int acc_bufs;      // tensor-memory accumulator sets
     int acc_cols;      // columns of one set
     int tmem_cols;
@@ -173,6 +176,9 @@ inline bool use_vec_producer(const Geometry &g, const Tiling &t) {
 //  its 16-byte chunks permuted by the 128-byte swizzle of the tensor core's
 //  K-major operand layout (chunk k/4 stored at position (k/4) ^ (j % 8)):
 //    wp[(((sl*n_chunks + c)*n_taps + t)*bn + j)*32 + (((k/4) ^ (j%8))*4) + k%4]
+//  layout 2 (col2im path, kc = 32), one 128-byte row per GEMM column
+//    r = (kh*kW + kw)*Ci + ci (rows up to bn, zero past Ci*kH*kW), swizzled
+//    like layout 1: wp[(c*bn + r)*32 + (((k/4) ^ (r%8))*4) + k%4]
 // Split precision (split_chunks = C > 0, n_chunks = 3C): chunk c holds output
 // channels of chunk c mod C, as the TF32 low part of the weight for c < C and
 // as the TF32 high part for c >= C (the three K passes hi*lo, lo*hi, hi*hi).
@@ -266,6 +272,27 @@ void fill_prepack_params(const Geometry &g, const Tiling &t, int round_tf32, Pre
 cudaError_t launch_pack(const PrepackParams *pp, const FramePackParams *fp, cudaStream_t stream);
 inline cudaError_t launch_prepack(const PrepackParams &p, cudaStream_t stream) { return launch_pack(&p, nullptr, stream); }
 cudaError_t launch_simt(const MainParams &p, const Tiling &t, cudaStream_t stream);
+
+// col2im path: P[position][(ci,kh,kw)] = sum over co of V[position][co] *
+// weight[co][ci][kh][kw] on tcgen05 (V the packed frame), scattered into a
+// shared-memory band of grad_input rows [r0, r0 + R) and written out.
+constexpr int kC2iMaxCols = 256;
+struct C2iParams {
+    CUtensorMap a_map;   // the packed frame, box 32 channels x 128 positions, 128-byte swizzle
+    const float *wp;     // packed weights, layout 2
+    float *gi;
+    uint32_t *err;
+    const float *relu_in;   // fused epilogue, as MainParams
+    int accumulate;
+    int N, Ci, H, W, Co, kH, kW, s, ph, pw, oH, oW, Ph, Pw, Hv, Wp;
+    int n_chunks, bn, ncols, R, pitch, bands_per_img, n_bands, a_stages, tmem_cols, chunk_bytes;
+    uint32_t idesc;
+    long long timeout_ns;
+    int col_kh[kC2iMaxCols];    // kernel row of GEMM column c
+    int col_off[kC2iMaxCols];   // (ci*R + kh)*pitch + kw: offset of column c in a band copy from its position's base
+};
+void fill_c2i_params(const Geometry &g, const Tiling &t, C2iParams *c);
+cudaError_t launch_c2i(const C2iParams &p, const Tiling &t, cudaStream_t stream, bool pdl);
 cudaError_t launch_tc(const MainParams &p, const Tiling &t, cudaStream_t stream, bool pdl);
 // Tensor-copy mode with the fused epilogue (called by launch_tc).
 cudaError_t launch_tc_fused(const MainParams &p, const Tiling &t, cudaStream_t stream, bool pdl);

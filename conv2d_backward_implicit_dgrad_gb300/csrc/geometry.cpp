@@ -384,6 +384,77 @@ bool size_simt(const Geometry &g, Tiling &t) {
     return true;
 }
 
+// col2im path: GEMM N = Ci*kH*kW columns (one 128-byte packed row each),
+// K = Co in 32-channel chunks, M = 128 frame positions per tile; the packed
+// weights stay resident; a band of R input rows (a multiple of the stride)
+// collects the tiles of the positions that reach it.  R minimises the
+// busiest CTA's tile count (bands are dealt round-robin), preferring larger
+// bands on ties (fewer write-outs).
+dgrad_status_t choose_c2i(const Geometry &g, int precision, int sm_count, Tiling *out) {
+    if (precision != DGRAD_PREC_TF32) return DGRAD_ERR_UNSUPPORTED;
+    const int ncols = g.Ci * g.kH * g.kW;
+    if (ncols > kC2iMaxCols || g.Ci > 4) return DGRAD_ERR_UNSUPPORTED;   // stems: up to 4 input channels
+    Tiling t{};
+    t.path = DGRAD_PATH_COL2IM;
+    t.tm = 1;
+    t.bn = round_up(ncols, 16);
+    t.n_slices = 1;
+    t.kc = 32;
+    t.n_chunks = ceil_div(g.Co, 32);
+    if (t.n_chunks > 32) return DGRAD_ERR_UNSUPPORTED;   // one resident-weight barrier per chunk
+    t.co_v = std::max(32, round_up(g.Co, 4));
+    t.frame_bytes = (size_t)g.positions * t.co_v * 4;
+    if ((long long)g.positions * t.co_v > INT_MAX) return DGRAD_ERR_UNSUPPORTED;
+    t.a_tma = 1;
+    t.a_box_rows = kBlockM;
+    t.a_nbox = 1;
+    t.a_rows = kBlockM;
+    t.b_resident = 1;
+    t.chunk_bytes = t.bn * 128;
+    t.packed_bytes = (size_t)t.n_chunks * t.chunk_bytes;
+    // band row: input columns iw at iw + pw; wide enough for every contribution
+    // (iw + pw <= (oW - 1)*s + kW - 1) and for every column written out (< W + pw)
+    t.c2i_pitch = std::max((g.oW - 1) * g.s + g.kW, g.W + g.pw);
+    const long long b_all = (long long)t.packed_bytes;
+    const int a_bytes = kBlockM * 128;
+    long long best = LLONG_MAX;
+    for (int R = g.s; R <= 64; R += g.s) {
+        const long long acc = 4LL * 4 * g.Ci * R * t.c2i_pitch;   // one band copy per epilogue warp
+        const long long left = kMaxSmem - kBarrierBytes - b_all - acc;
+        const int stages = (int)std::min<long long>(4, left / a_bytes);
+        if (stages < 2) break;
+        // positions (frame rows) a band of R rows needs: oh with oh*s - ph + kh in [r0, r0 + R)
+        const int rows = (R - 1 + g.kH - 1) / g.s + 1;
+        const long long tiles = ((long long)rows * g.Wp + kBlockM - 1) / kBlockM;
+        const long long bands = (long long)g.N * ceil_div(g.H, R);
+        const long long grid = std::min<long long>(bands, sm_count);
+        // a tile's chunks fill n_chunks stages: with fewer than two tiles'
+        // worth the next tile's copies cannot start early (measured on the
+        // 7x7 stem: 226 us with two stages of two chunks), so such a band
+        // size costs three times its tiles
+        const long long cost = (bands + grid - 1) / grid * tiles * (stages >= 2 * t.n_chunks ? 1 : 3);
+        if (cost <= best) {
+            best = cost;
+            t.c2i_R = R;
+            t.a_stages = stages;
+            t.smem_bytes = (int)(kBarrierBytes + b_all + (long long)stages * a_bytes + acc);
+        }
+        if (R >= g.H) break;
+    }
+    if (best == LLONG_MAX) return DGRAD_ERR_UNSUPPORTED;
+    t.c2i_bands = g.N * ceil_div(g.H, t.c2i_R);
+    t.b_stages = t.n_chunks;
+    t.n_tiles = t.c2i_bands;
+    t.n_work = t.c2i_bands;
+    t.grid = std::max(1, std::min(t.c2i_bands, sm_count));
+    t.acc_bufs = 2;
+    t.acc_cols = t.bn;
+    t.tmem_cols = pow2_at_least(2 * t.bn);
+    t.tile_step = kBlockM;
+    *out = t;
+    return DGRAD_OK;
+}
+
 }  // namespace
 
 dgrad_status_t choose_tiling(const Geometry &g, int precision, const dgrad_options_t *opts,
@@ -394,6 +465,7 @@ dgrad_status_t choose_tiling(const Geometry &g, int precision, const dgrad_optio
     int path = o.path;
     const bool split = precision == DGRAD_PREC_TF32X3;
     if (path == DGRAD_PATH_AUTO) path = (precision == DGRAD_PREC_FP32) ? DGRAD_PATH_SIMT : DGRAD_PATH_TCGEN05;
+    if (path == DGRAD_PATH_COL2IM) return choose_c2i(g, precision, sm_count, out);
     if (path != DGRAD_PATH_SIMT && path != DGRAD_PATH_TCGEN05) return DGRAD_ERR_INVALID_ARG;
     if (path == DGRAD_PATH_TCGEN05 && precision == DGRAD_PREC_FP32) return DGRAD_ERR_UNSUPPORTED;
     if (path == DGRAD_PATH_SIMT && split) return DGRAD_ERR_UNSUPPORTED;
@@ -587,7 +659,7 @@ void fill_prepack_params(const Geometry &g, const Tiling &t, int round_tf32, Pre
     q.n_taps = g.n_taps; q.bn = t.bn; q.n_slices = t.n_slices; q.kc = t.kc; q.n_chunks = t.n_chunks;
     q.round_tf32 = round_tf32;
     q.split_chunks = t.split ? t.n_chunks / 3 : 0;
-    q.layout = t.path == DGRAD_PATH_TCGEN05 ? 1 : 0;
+    q.layout = t.path == DGRAD_PATH_TCGEN05 ? 1 : (t.path == DGRAD_PATH_COL2IM ? 2 : 0);
     q.total = (long long)(t.packed_bytes / 4);
     // tcgen05 path: taps in the packing order of the plan's MMA groups
     MGroup mg[kMaxTaps];
@@ -597,6 +669,29 @@ void fill_prepack_params(const Geometry &g, const Tiling &t, int round_tf32, Pre
     for (int i = 0; i < g.n_taps; ++i) {
         q.tap_kh[i] = g.tap[perm[i]].kh;
         q.tap_kw[i] = g.tap[perm[i]].kw;
+    }
+}
+
+}  // namespace dgrad
+
+namespace dgrad {
+
+void fill_c2i_params(const Geometry &g, const Tiling &t, C2iParams *cp) {
+    C2iParams &c = *cp;
+    std::memset(&c, 0, sizeof(c));
+    c.N = g.N; c.Ci = g.Ci; c.H = g.H; c.W = g.W; c.Co = g.Co; c.kH = g.kH; c.kW = g.kW;
+    c.s = g.s; c.ph = g.ph; c.pw = g.pw; c.oH = g.oH; c.oW = g.oW;
+    c.Ph = g.Ph; c.Pw = g.Pw; c.Hv = g.Hv; c.Wp = g.Wp;
+    c.n_chunks = t.n_chunks; c.bn = t.bn; c.ncols = g.Ci * g.kH * g.kW;
+    c.R = t.c2i_R; c.pitch = t.c2i_pitch;
+    c.bands_per_img = (g.H + t.c2i_R - 1) / t.c2i_R;
+    c.n_bands = t.c2i_bands;
+    c.a_stages = t.a_stages; c.tmem_cols = t.tmem_cols; c.chunk_bytes = t.chunk_bytes;
+    c.idesc = tf32_idesc(kBlockM, t.bn);
+    for (int r = 0; r < c.ncols && r < kC2iMaxCols; ++r) {   // tap-major columns: r = (kh*kW + kw)*Ci + ci
+        const int tap = r / g.Ci, ci = r % g.Ci, kh = tap / g.kW, kw = tap % g.kW;
+        c.col_kh[r] = kh;
+        c.col_off[r] = (ci * t.c2i_R + kh) * t.c2i_pitch + kw;
     }
 }
 

@@ -43,6 +43,21 @@ __device__ void pack_weights(const PrepackParams &p, int block, int nblocks) {
         long long rest = i;
         const int e = static_cast<int>(rest % 4);
         rest /= 4;
+        if (p.layout == 2) {   // col2im: [chunk][r = (kh*kW + kw)*Ci + ci][swizzled 16-byte group][4]
+            const int pos = static_cast<int>(rest % 8);
+            rest /= 8;
+            const int r = static_cast<int>(rest % p.bn);
+            const int c = static_cast<int>(rest / p.bn);
+            const int co = c * p.kc + 4 * (pos ^ (r & 7)) + e;
+            const int taps = p.kH * p.kW;
+            float v = 0.f;
+            if (co < p.Co && r < p.Ci * taps) {
+                const int tap = r / p.Ci, ci = r - tap * p.Ci;
+                v = __ldg(p.w + (static_cast<size_t>(co) * p.Ci + ci) * taps + tap);
+            }
+            p.wp[i] = p.round_tf32 ? dev::round_tf32(v) : v;
+            continue;
+        }
         int j, gq;
         if (p.layout == 1) {   // [tap][j][swizzled 16-byte chunk][4]
             const int pos = static_cast<int>(rest % G);

@@ -86,7 +86,13 @@ typedef enum { DGRAD_PREC_FP32 = 0, DGRAD_PREC_TF32 = 1, DGRAD_PREC_TF32X3 = 2 }
 typedef enum {
     DGRAD_PATH_AUTO = 0,
     DGRAD_PATH_SIMT = 1,     /* FFMA implicit GEMM (exact fp32; also accepts TF32-rounded operands) */
-    DGRAD_PATH_TCGEN05 = 2   /* warp-specialised tcgen05/TMEM implicit GEMM (TF32 and TF32X3) */
+    DGRAD_PATH_TCGEN05 = 2,  /* warp-specialised tcgen05/TMEM implicit GEMM (TF32 and TF32X3) */
+    DGRAD_PATH_COL2IM = 3    /* for few input channels (stems, Ci <= 4): the GEMM
+                                P[position][(ci,kh,kw)] = sum over co of grad_out x weight on tcgen05
+                                (N = Ci*kH*kW <= 256, no per-tap slices), then col2im: every
+                                P element added into a shared-memory band of grad_input (one copy
+                                per epilogue warp, summed in a fixed order), bands written out
+                                whole.  TF32 only; opt-in (never chosen by AUTO). */
 } dgrad_path_t;
 
 /* Optional tuning overrides for dgrad_plan_ex / dgrad_describe; 0 = automatic. */

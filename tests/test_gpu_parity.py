@@ -438,3 +438,73 @@ def test_split_precision_rejects_other_sources():
     with pytest.raises(dg.DgradError) as e:
         dg.Plan(1, 8, 8, 8, 8, 3, 3, 1, 1, 1, precision="tf32x3", a_source="producers")
     assert e.value.status == 2
+
+
+# ----------------------------------------------------------------- GEMM + col2im path (few input channels)
+C2I_SHAPES = [
+    # N, Ci, Co, H, W, kH, kW, s, ph, pw
+    (2, 3, 64, 40, 38, 7, 7, 2, 3, 3),      # stem-like
+    (3, 3, 4, 9, 11, 5, 5, 1, 1, 1),
+    (1, 1, 1, 5, 7, 3, 3, 1, 0, 0),
+    (1, 3, 33, 23, 21, 7, 7, 2, 3, 3),
+    (3, 4, 33, 12, 14, 2, 2, 2, 0, 0),
+    (1, 3, 1, 11, 17, 3, 5, 1, 2, 1),
+    (1, 3, 4, 2, 2, 3, 3, 2, 1, 1),         # a kernel row that only meets padding
+    (1, 4, 3, 1, 1, 1, 1, 2, 1, 1),         # no term reaches any input element
+    (2, 2, 70, 130, 9, 3, 3, 1, 1, 1),      # several bands per image, ragged last band
+    (1, 4, 40, 40, 40, 3, 3, 4, 1, 1),      # stride 4
+    (2, 4, 16, 20, 22, 8, 8, 1, 3, 4),      # 256 GEMM columns, non-same padding
+]
+
+
+@pytest.mark.parametrize("shape", C2I_SHAPES)
+def test_col2im_path(shape):
+    N, Ci, Co, H, W, kH, kW, s, ph, pw = shape
+    go, w = make_tensors((N, Co, out_ext(H, kH, s, ph), out_ext(W, kW, s, pw)), (Co, Ci, kH, kW), 80, "uniform")
+    info = check((N, Ci, H, W, Co, kH, kW, s, ph, pw), go, w, "tf32", path="col2im")
+    assert info["path"] == "col2im"
+
+
+@pytest.mark.parametrize("mode", ["relu", "accumulate", "both"])
+def test_col2im_fused_epilogue(mode):
+    N, Ci, Co, H, W, kH, kW, s, ph, pw = (2, 3, 20, 17, 18, 7, 7, 2, 3, 3)
+    go, w = make_tensors((N, Co, out_ext(H, kH, s, ph), out_ext(W, kW, s, pw)), (Co, Ci, kH, kW), 81, "kaiming")
+    gen = torch.Generator().manual_seed(82)
+    relu_in = torch.randn((N, Ci, H, W), generator=gen) if mode in ("relu", "both") else None
+    gi0 = torch.randn((N, Ci, H, W), generator=gen) if mode in ("accumulate", "both") else None
+    ref, mag = oracle.dgrad_fused(go, w, H, W, s, ph, pw, relu_in=relu_in, grad_in=gi0)
+    with dg.Plan(N, Ci, H, W, Co, kH, kW, s, ph, pw, precision="tf32", path="col2im") as plan:
+        gi = gi0.cuda() if gi0 is not None else torch.full((N, Ci, H, W), float("nan"), device="cuda")
+        plan.run(go.cuda(), w.cuda(), gi, relu_in=relu_in.cuda() if relu_in is not None else None,
+                 accumulate=gi0 is not None)
+        torch.cuda.synchronize()
+        plan.check()
+    out = gi.cpu().double().numpy()
+    bound = TF32_REL_TERMS * mag + 2.0 ** -23 * np.abs(ref)
+    assert (np.abs(out - ref) <= bound + 1e-30).all()
+
+
+def test_col2im_full_size_stem_sampled():
+    wl = WORKLOADS["stem"]
+    go, w = make_inputs(wl, 0)
+    gpu, info = run_gpu(wl.plan_args(), go, w, "tf32", path="col2im")
+    assert info["path"] == "col2im"
+    rng = np.random.default_rng(103)
+    idx = np.stack([rng.integers(0, wl.N, 4096), rng.integers(0, wl.Ci, 4096),
+                    rng.integers(0, wl.H, 4096), rng.integers(0, wl.W, 4096)], 1)
+    acc, mag = oracle.dgrad_at(go, w, wl.H, wl.W, wl.stride, wl.pad_h, wl.pad_w, idx)
+    g = gpu[idx[:, 0], idx[:, 1], idx[:, 2], idx[:, 3]]
+    assert np.all(np.abs(g - acc) <= TF32_REL_TERMS * mag)
+    assert np.isfinite(gpu).all()
+
+
+def test_col2im_rejects_unsupported():
+    with pytest.raises(dg.DgradError) as e:
+        dg.Plan(1, 3, 16, 16, 8, 3, 3, 1, 1, 1, precision="fp32", path="col2im")
+    assert e.value.status == 2
+    with pytest.raises(dg.DgradError) as e:
+        dg.Plan(1, 4, 16, 16, 8, 9, 9, 1, 1, 1, precision="tf32", path="col2im")   # 324 GEMM columns > 256
+    assert e.value.status == 2
+    with pytest.raises(dg.DgradError) as e:
+        dg.Plan(1, 5, 16, 16, 8, 3, 3, 1, 1, 1, precision="tf32", path="col2im")   # more than 4 input channels
+    assert e.value.status == 2

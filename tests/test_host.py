@@ -410,3 +410,16 @@ def test_wgrad_plans():
         with pytest.raises(dg.DgradError) as e:
             dg.wgrad_describe(2, 3, 8, 8, 4, 3, 3, 1, 1, 1, prec)
         assert e.value.status == 2
+
+
+def test_col2im_plans():
+    wl = WORKLOADS["stem"]
+    d = dg.describe(*wl.plan_args(), path="col2im", sm_count=152)
+    assert d["path"] == "col2im" and d["a_source"] == "frame"
+    assert d["slice_n"] == 160                      # 3 x 7 x 7 = 147 GEMM columns, padded to 16
+    assert d["smem_bytes"] <= 232448 and d["tmem_cols"] <= 512 and d["grid"] <= 152
+    assert dg.describe(*wl.plan_args(), sm_count=152)["path"] == "tcgen05"   # never chosen automatically
+    for bad in (dict(precision="fp32"), dict(precision="tf32x3")):
+        with pytest.raises(dg.DgradError) as e:
+            dg.describe(*wl.plan_args(), path="col2im", **bad)
+        assert e.value.status == 2
