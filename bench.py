@@ -184,13 +184,13 @@ def reference_arm(args, wl):
     return 0
 
 
-def time_workload(dg, torch, wl, precision, steps, warmup, rank, barrier, device_index, clocks, e2e):
+def time_workload(dg, torch, wl, precision, steps, warmup, rank, barrier, device_index, clocks, e2e, **opts):
     from conv2d_backward_implicit_dgrad_gb300.workloads import make_inputs
     go_h, w_h = make_inputs(wl, seed=rank)
     go, w = go_h.cuda(), w_h.cuda()
     gi = torch.empty(wl.gi_shape, device="cuda")
     flush = torch.empty(FLUSH_BYTES // 4, device="cuda")
-    plan = dg.Plan(*wl.plan_args(), precision=precision)
+    plan = dg.Plan(*wl.plan_args(), precision=precision, **opts)
     stream = torch.cuda.current_stream()
 
     def step():
@@ -457,6 +457,16 @@ def main():
                                                                          "chunk_k", "grid", "n_work",
                                                                          "b_resident", "smem_bytes")}}),
                           flush=True)
+            # the opt-in GEMM + col2im path on the few-input-channel stem
+            x = time_workload(dg, torch, WORKLOADS["stem"], "tf32", 50, 5, rank, lambda: None, local, clocks=False,
+                              e2e=False, path="col2im")
+            rf = roofline(WORKLOADS["stem"], "tf32", x["flops"], x["bytes"], x["main_ms"] * 1e-3,
+                          x["ms_per_step"] * 1e-3)
+            print(json.dumps({"info": "workload", "workload": "stem", "precision": "tf32", "path": "col2im",
+                              **{k: x[k] for k in ("ms_per_step", "main_ms", "prepack_ms")},
+                              "tflops": x["flops"] / (x["ms_per_step"] * 1e-3) / 1e12,
+                              "main_tflops": rf["achieved"], "frac_peak": rf["frac"],
+                              "frac_of_roofline_kernel": rf["frac_of_roofline_kernel"]}), flush=True)
             peaks, src = load_peaks()
             tf32_peak = peaks["bf16_tflops"] * TF32_OVER_BF16
             for name in WORKLOAD_ORDER:
