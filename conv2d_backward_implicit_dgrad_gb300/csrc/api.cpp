@@ -3,6 +3,7 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <cstdint>
 #include <cstdlib>
 #include <cstring>
@@ -11,6 +12,8 @@
 
 #include "dgrad.h"
 #include "dgrad_internal.h"
+
+constexpr int kHostChunks = 8;   // batch chunks of dgrad_run_host's copy/compute pipeline
 
 struct dgrad_plan_s {
     int device;
@@ -27,6 +30,15 @@ struct dgrad_plan_s {
     float *stage_go;       // dgrad_run_host staging (device), allocated on first use
     float *stage_w;
     float *stage_gi;
+    // dgrad_run_host pipeline (made on first use): the batch in chunks of
+    // chunk_n images, each run by a sub-plan while the next chunk's input and
+    // the previous chunk's output are in flight on their own streams
+    dgrad_options_t opts;
+    int chunk_n;
+    dgrad_plan_s *sub[2];          // sub-plans for chunk_n images and for the remainder
+    cudaStream_t h2d, d2h;
+    cudaEvent_t ev_in[kHostChunks], ev_out[kHostChunks];
+    int host_ready;
     size_t workspace_bytes;
     int packed;            // dgrad_prepack (or dgrad_run) has run at least once
     int frame_packed;      // grad_out has been packed into the frame at least once
@@ -213,6 +225,33 @@ dgrad_status_t launch_main_on(dgrad_plan_s *plan, const float *grad_out, float *
     return cuda_status(e);
 }
 
+// dgrad_run_host's pipeline: chunks of ceil(N / kHostChunks) images, two
+// sub-plans (full chunk, remainder), two copy streams and their events.
+dgrad_status_t make_host_pipeline(dgrad_plan_s *plan) {
+    const Geometry &g = plan->g;
+    plan->chunk_n = (g.N + kHostChunks - 1) / kHostChunks;   // the same split dgrad_run_host stages
+    const int rem = g.N % plan->chunk_n;
+    const int sizes[2] = {plan->chunk_n, rem};
+    for (int i = 0; i < 2; ++i) {
+        if (sizes[i] == 0) continue;
+        dgrad_status_t st = dgrad_plan_ex(sizes[i], g.Ci, g.H, g.W, g.Co, g.kH, g.kW, g.s, g.ph, g.pw,
+                                          static_cast<dgrad_precision_t>(plan->precision), &plan->opts, &plan->sub[i]);
+        if (st != DGRAD_OK) return st;
+    }
+    if (cudaStreamCreateWithFlags(&plan->h2d, cudaStreamNonBlocking) != cudaSuccess) return cuda_status(cudaGetLastError());
+    if (cudaStreamCreateWithFlags(&plan->d2h, cudaStreamNonBlocking) != cudaSuccess) {
+        cudaStreamDestroy(plan->h2d);
+        return cuda_status(cudaGetLastError());
+    }
+    for (int i = 0; i < kHostChunks; ++i) {
+        if (cudaEventCreateWithFlags(&plan->ev_in[i], cudaEventDisableTiming) != cudaSuccess ||
+            cudaEventCreateWithFlags(&plan->ev_out[i], cudaEventDisableTiming) != cudaSuccess)
+            return cuda_status(cudaGetLastError());
+    }
+    plan->host_ready = 1;
+    return DGRAD_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -288,6 +327,7 @@ dgrad_status_t dgrad_plan_ex(int N, int Ci, int H, int W, int Co, int kH, int kW
     std::memset(pl, 0, sizeof(*pl));
     pl->device = dev;
     pl->precision = precision;
+    if (opts) pl->opts = *opts;
     dgrad_status_t st = plan_host(N, Ci, H, W, Co, kH, kW, stride, pad_h, pad_w, precision, opts,
                                   prop.multiProcessorCount, &pl->g, &pl->t);
     if (st != DGRAD_OK) {
@@ -421,26 +461,72 @@ dgrad_status_t dgrad_run_host(dgrad_plan_t plan, const float *grad_out_host, con
     if (st != DGRAD_OK) return st;
     const Geometry &g = plan->g;
     const size_t go_b = go_elems(g) * 4, w_b = w_elems(g) * 4, gi_b = gi_elems(g) * 4;
+    // Staging: one 256-byte aligned slot per batch chunk for grad_out and for
+    // grad_input (every device pointer a run gets is aligned), and the weights.
+    const size_t go_img = go_b / g.N, gi_img = gi_b / g.N;
+    const int chunk_n = (g.N + kHostChunks - 1) / kHostChunks;
+    const int nck = (g.N + chunk_n - 1) / chunk_n;
+    auto up = [](size_t b) { return (b + 255) & ~size_t(255); };
+    const size_t go_slot = up(chunk_n * go_img), gi_slot = up(chunk_n * gi_img);
     if (!plan->stage_go) {
         void *m = nullptr;
-        auto up = [](size_t b) { return (b + 255) & ~size_t(255); };
-        if (cudaMalloc(&m, up(go_b) + up(w_b) + up(gi_b)) != cudaSuccess) {
+        if (cudaMalloc(&m, nck * go_slot + up(w_b) + nck * gi_slot) != cudaSuccess) {
             cudaGetLastError();
             return DGRAD_ERR_OOM;
         }
         plan->stage_go = static_cast<float *>(m);
-        plan->stage_w = reinterpret_cast<float *>(static_cast<uint8_t *>(m) + up(go_b));
-        plan->stage_gi = reinterpret_cast<float *>(static_cast<uint8_t *>(m) + up(go_b) + up(w_b));
+        plan->stage_w = reinterpret_cast<float *>(static_cast<uint8_t *>(m) + nck * go_slot);
+        plan->stage_gi = reinterpret_cast<float *>(static_cast<uint8_t *>(m) + nck * go_slot + up(w_b));
     }
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (cudaMemcpyAsync(plan->stage_go, grad_out_host, go_b, cudaMemcpyHostToDevice, s) != cudaSuccess ||
-        cudaMemcpyAsync(plan->stage_w, weight_host, w_b, cudaMemcpyHostToDevice, s) != cudaSuccess)
-        return DGRAD_ERR_CUDA;
-    st = dgrad_run(plan, plan->stage_go, plan->stage_w, plan->stage_gi, stream);
-    if (st != DGRAD_OK) return st;
-    if (cudaMemcpyAsync(grad_input_host, plan->stage_gi, gi_b, cudaMemcpyDeviceToHost, s) != cudaSuccess)
-        return DGRAD_ERR_CUDA;
-    return cuda_status(cudaStreamSynchronize(s));
+    if (g.N < 2) {   // one image: copy in, run, copy out
+        if (cudaMemcpyAsync(plan->stage_go, grad_out_host, go_b, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+            cudaMemcpyAsync(plan->stage_w, weight_host, w_b, cudaMemcpyHostToDevice, s) != cudaSuccess)
+            return cuda_status(cudaGetLastError());
+        st = dgrad_run(plan, plan->stage_go, plan->stage_w, plan->stage_gi, stream);
+        if (st != DGRAD_OK) return st;
+        if (cudaMemcpyAsync(grad_input_host, plan->stage_gi, gi_b, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+            return cuda_status(cudaGetLastError());
+        return cuda_status(cudaStreamSynchronize(s));
+    }
+    if (!plan->host_ready && (st = make_host_pipeline(plan)) != DGRAD_OK) return st;
+    // Chunk i: copy in on h2d, run on the caller's stream once its copy is
+    // there, copy out on d2h once its run is done; the copy engines of the
+    // two directions and the SMs work on different chunks at the same time.
+    cudaError_t e = cudaMemcpyAsync(plan->stage_w, weight_host, w_b, cudaMemcpyHostToDevice, plan->h2d);
+    for (int i = 0; e == cudaSuccess && i < nck; ++i) {
+        const int n0 = i * chunk_n, nn = std::min(chunk_n, g.N - n0);
+        dgrad_plan_s *sp = plan->sub[nn == chunk_n ? 0 : 1];
+        uint8_t *dgo = reinterpret_cast<uint8_t *>(plan->stage_go) + i * go_slot;
+        uint8_t *dgi = reinterpret_cast<uint8_t *>(plan->stage_gi) + i * gi_slot;
+        e = cudaMemcpyAsync(dgo, reinterpret_cast<const uint8_t *>(grad_out_host) + n0 * go_img, nn * go_img,
+                            cudaMemcpyHostToDevice, plan->h2d);
+        if (e == cudaSuccess) e = cudaEventRecord(plan->ev_in[i], plan->h2d);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(s, plan->ev_in[i], 0);
+        if (e != cudaSuccess) break;
+        st = dgrad_run(sp, reinterpret_cast<const float *>(dgo), plan->stage_w, reinterpret_cast<float *>(dgi), stream);
+        if (st != DGRAD_OK) {
+            cudaStreamSynchronize(plan->h2d);
+            cudaStreamSynchronize(plan->d2h);
+            return st;
+        }
+        e = cudaEventRecord(plan->ev_out[i], s);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(plan->d2h, plan->ev_out[i], 0);
+        if (e == cudaSuccess)
+            e = cudaMemcpyAsync(reinterpret_cast<uint8_t *>(grad_input_host) + n0 * gi_img, dgi, nn * gi_img,
+                                cudaMemcpyDeviceToHost, plan->d2h);
+    }
+    const cudaError_t e1 = cudaStreamSynchronize(plan->h2d);
+    const cudaError_t e2 = cudaStreamSynchronize(plan->d2h);
+    const cudaError_t e3 = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_status(e);
+    if (e1 != cudaSuccess) return cuda_status(e1);
+    if (e2 != cudaSuccess) return cuda_status(e2);
+    if (e3 != cudaSuccess) return cuda_status(e3);
+    // a bounded wait that ran out in a sub-plan's kernels is reported here
+    for (int i = 0; i < 2; ++i)
+        if (plan->sub[i] && (st = dgrad_plan_check(plan->sub[i])) != DGRAD_OK) return st;
+    return DGRAD_OK;
 }
 
 dgrad_status_t dgrad_plan_check(dgrad_plan_t plan) {
@@ -460,6 +546,16 @@ void dgrad_plan_destroy(dgrad_plan_t plan) {
     cudaDeviceSynchronize();
     cudaFree(plan->err);
     if (plan->stage_go) cudaFree(plan->stage_go);
+    if (plan->host_ready) {
+        for (int i = 0; i < kHostChunks; ++i) {
+            cudaEventDestroy(plan->ev_in[i]);
+            cudaEventDestroy(plan->ev_out[i]);
+        }
+        cudaStreamDestroy(plan->h2d);
+        cudaStreamDestroy(plan->d2h);
+    }
+    for (int i = 0; i < 2; ++i)
+        if (plan->sub[i]) dgrad_plan_destroy(plan->sub[i]);
     if (cur >= 0 && cur != plan->device) cudaSetDevice(cur);
     delete plan;
 }

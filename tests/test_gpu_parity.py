@@ -352,6 +352,29 @@ def test_run_host_matches_device():
         plan.check()
 
 
+@pytest.mark.parametrize("shape,precision,pinned", [
+    ((32, 64, 56, 56, 64, 3, 3, 1, 1, 1), "tf32", True),    # eight chunks of four images
+    ((11, 5, 17, 19, 33, 3, 3, 2, 1, 1), "tf32", True),     # chunks of two and a remainder of one
+    ((11, 5, 17, 19, 33, 3, 3, 2, 1, 1), "fp32", False),    # FFMA path, pageable host memory
+    ((3, 3, 40, 38, 64, 7, 7, 2, 3, 3), "tf32x3", True),
+])
+def test_run_host_pipeline_matches_device(shape, precision, pinned):
+    """The host entry point runs the batch in chunks through sub-plans, copies
+    overlapping the runs; every element is the device run's, bit for bit (the
+    per-element summation order does not depend on the batch)."""
+    N, Ci, H, W, Co, kH, kW, s, ph, pw = shape
+    go, w = make_tensors((N, Co, out_ext(H, kH, s, ph), out_ext(W, kW, s, pw)), (Co, Ci, kH, kW), 83, "kaiming")
+    with dg.Plan(*shape, precision=precision) as plan:
+        dev = plan.run(go.cuda(), w.cuda()).cpu()
+        gh, wh = (go.pin_memory(), w.pin_memory()) if pinned else (go, w)
+        out = torch.empty((N, Ci, H, W), pin_memory=pinned)
+        for _ in range(2):   # the pipeline is made on the first call and reused
+            out.fill_(float("nan"))
+            plan.run_host(gh, wh, out)
+            assert torch.equal(dev, out)
+        plan.check()
+
+
 def test_side_stream():
     wl = WORKLOADS["tiny"]
     go, w = make_inputs(wl, 8)
