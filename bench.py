@@ -327,7 +327,7 @@ def build_line(args, wl, r, world):
     return line
 
 
-def time_wgrad(dg, torch, wl, steps, warmup):
+def time_wgrad(dg, torch, wl, steps, warmup, precision="tf32"):
     """The weight gradient of the same convolution (grad_out and the forward
     input, seeded), each step after the same L2 flush, CUDA events around
     wgrad_run (frame pack, tcgen05 split-K GEMM, reduction)."""
@@ -338,7 +338,7 @@ def time_wgrad(dg, torch, wl, steps, warmup):
     dw = torch.empty((wl.Co, wl.Ci, wl.kH, wl.kW), device="cuda")
     flush = torch.empty(FLUSH_BYTES // 4, device="cuda")
     stream = torch.cuda.current_stream()
-    with dg.WgradPlan(*wl.plan_args(), precision="tf32") as plan:
+    with dg.WgradPlan(*wl.plan_args(), precision=precision) as plan:
         for _ in range(max(3, warmup)):
             flush.zero_()
             plan.run(go, x, dw, stream)
@@ -365,7 +365,7 @@ def profile_steps(dg, torch, wl, args):
     if args.op == "wgrad":
         x = torch.randn((wl.N, wl.Ci, wl.H, wl.W), generator=torch.Generator().manual_seed(1)).cuda()
         dw = torch.empty((wl.Co, wl.Ci, wl.kH, wl.kW), device="cuda")
-        with dg.WgradPlan(*wl.plan_args(), precision="tf32") as plan:
+        with dg.WgradPlan(*wl.plan_args(), precision=args.precision) as plan:
             for _ in range(args.warmup + args.steps):
                 flush.zero_()
                 plan.run(go, x, dw)
@@ -469,10 +469,10 @@ def main():
                               "frac_of_roofline_kernel": rf["frac_of_roofline_kernel"]}), flush=True)
             peaks, src = load_peaks()
             tf32_peak = peaks["bf16_tflops"] * TF32_OVER_BF16
-            for name in WORKLOAD_ORDER:
-                x = time_wgrad(dg, torch, WORKLOADS[name], 50, 5)
+            for name, prec in [(n, p) for p in ("tf32", "tf32x3") for n in WORKLOAD_ORDER]:
+                x = time_wgrad(dg, torch, WORKLOADS[name], 50, 5, prec)
                 tf = x["flops"] / (x["ms_per_step"] * 1e-3) / 1e12
-                print(json.dumps({"info": "wgrad", "workload": name, "precision": "tf32",
+                print(json.dumps({"info": "wgrad", "workload": name, "precision": prec,
                                   "ms_per_step": x["ms_per_step"], "tflops": tf, "frac_peak": tf / tf32_peak,
                                   "plan": {k: x["plan"][k] for k in ("n_mt", "n_nt", "n_ks", "slice_n", "n_units",
                                                                      "grid", "stages", "n_copies")}}),

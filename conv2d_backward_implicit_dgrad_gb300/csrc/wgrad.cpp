@@ -26,6 +26,7 @@ namespace dgrad {
 
 namespace {
 
+constexpr int kWgSplitChunks = 12;      // longest K range of one split-precision unit, in 32-position chunks
 constexpr int kWgBarrierBytes = 2048;   // barrier block + alignment slack of the stage ring
 constexpr long long kWgTimeoutNs = 1000000000LL;
 
@@ -50,13 +51,15 @@ dgrad_status_t make_wgrad_geometry(int N, int Ci, int H, int W, int Co, int kH, 
         return DGRAD_ERR_INVALID_ARG;
     const long long nh = (long long)H + 2LL * pad_h - kH, nw = (long long)W + 2LL * pad_w - kW;
     if (nh < 0 || nw < 0) return DGRAD_ERR_INVALID_ARG;
-    if (precision != DGRAD_PREC_TF32) return DGRAD_ERR_UNSUPPORTED;
+    if (precision == DGRAD_PREC_FP32) return DGRAD_ERR_UNSUPPORTED;
     if (stride > kWgMaxRowPhases || (long long)kH * kW > kMaxTaps) return DGRAD_ERR_UNSUPPORTED;
     if (sm_count < 1) sm_count = 148;
     WgradGeometry g;
     std::memset(&g, 0, sizeof(g));
     g.N = N; g.Ci = Ci; g.H = H; g.W = W; g.Co = Co; g.kH = kH; g.kW = kW;
     g.s = stride; g.ph = pad_h; g.pw = pad_w;
+    g.split = precision == DGRAD_PREC_TF32X3 ? 1 : 0;
+    const int halves = g.split ? 2 : 1;
     g.oH = (int)(nh / stride) + 1;
     g.oW = (int)(nw / stride) + 1;
     g.Wf = round_up(g.oW, 4);
@@ -111,19 +114,25 @@ dgrad_status_t make_wgrad_geometry(int N, int Ci, int H, int W, int Co, int kH, 
     const int tiles = g.n_mt * g.n_nt;
     int n_ks = std::max(1, ceil_div(2 * sm_count, tiles));
     n_ks = std::min(n_ks, std::max(1, g.total_chunks / 8));
+    // Split precision: the tensor cores' fp32 accumulation loses accuracy about
+    // in proportion to the number of MMAs accumulated into one accumulator
+    // (measured near 2e-8 relative error per MMA on random data), so a unit
+    // takes at most kWgSplitChunks chunks (12 MMAs each) and the rest of the
+    // sum goes to the fp32 reduction of the partial tiles.
+    if (g.split) n_ks = std::max(n_ks, ceil_div(g.total_chunks, kWgSplitChunks));
     g.cps = ceil_div(g.total_chunks, n_ks);
     g.n_ks = ceil_div(g.total_chunks, g.cps);
     const long long units = (long long)tiles * g.n_ks;
     if (units > INT_MAX / 2) return DGRAD_ERR_UNSUPPORTED;
     g.n_units = (int)units;
     g.grid = std::min(g.n_units, sm_count);
-    const int stage_bytes = 128 * 128 + g.bn * 128;
+    const int stage_bytes = halves * (128 * 128 + g.bn * 128);
     g.stages = std::min(kWgMaxStages, (kMaxSmem - kWgBarrierBytes) / stage_bytes);
     if (g.stages < 2) return DGRAD_ERR_UNSUPPORTED;
     g.smem_bytes = kWgBarrierBytes + g.stages * stage_bytes;
     g.tmem_cols = pow2_at_least(2 * g.bn);
-    g.g_elems = (size_t)N * Co * g.Kimg;
-    g.x_elems = (size_t)g.n_copies * N * Ci * g.Lx;
+    g.g_elems = (size_t)halves * N * Co * g.Kimg;
+    g.x_elems = (size_t)halves * g.n_copies * N * Ci * g.Lx;
     if ((g.g_elems + g.x_elems) / 4 > (size_t)INT_MAX) return DGRAD_ERR_UNSUPPORTED;   // 32-bit pack indices
     g.part_elems = (size_t)g.n_units * g.bn * 128;
     *out = g;
@@ -141,7 +150,7 @@ void fill_wgrad_info(const WgradGeometry &g, size_t ws, wgrad_plan_info_t *info)
     info->N = g.N; info->Ci = g.Ci; info->H = g.H; info->W = g.W; info->Co = g.Co;
     info->kH = g.kH; info->kW = g.kW; info->stride = g.s; info->pad_h = g.ph; info->pad_w = g.pw;
     info->oH = g.oH; info->oW = g.oW;
-    info->precision = DGRAD_PREC_TF32;
+    info->precision = g.split ? DGRAD_PREC_TF32X3 : DGRAD_PREC_TF32;
     info->Wf = g.Wf; info->Kimg = g.Kimg; info->Lx = g.Lx; info->n_copies = g.n_copies;
     info->seg_rows = g.seg_rows; info->n_mt = g.n_mt; info->n_nt = g.n_nt; info->n_ks = g.n_ks;
     info->slice_n = g.bn; info->n_units = g.n_units; info->grid = g.grid; info->stages = g.stages;
@@ -170,7 +179,8 @@ dgrad_status_t encode_maps(wgrad_plan_s *pl) {
     const WgradGeometry &g = pl->g;
     const cuuint32_t es4[4] = {1u, 1u, 1u, 1u};
     {
-        const cuuint64_t dims[4] = {(cuuint64_t)g.Lx, (cuuint64_t)g.Ci, (cuuint64_t)g.N, (cuuint64_t)g.n_copies};
+        const cuuint64_t dims[4] = {(cuuint64_t)g.Lx, (cuuint64_t)g.Ci, (cuuint64_t)g.N,
+                                    (cuuint64_t)g.n_copies * (g.split ? 2 : 1)};
         const cuuint64_t strides[3] = {(cuuint64_t)g.Lx * 4, (cuuint64_t)g.Lx * 4 * g.Ci,
                                        (cuuint64_t)g.Lx * 4 * g.Ci * g.N};
         const cuuint32_t box[4] = {32u, (cuuint32_t)g.seg_rows, 1u, 1u};
@@ -180,7 +190,7 @@ dgrad_status_t encode_maps(wgrad_plan_s *pl) {
             return DGRAD_ERR_CUDA;
     }
     {
-        const cuuint64_t dims[3] = {(cuuint64_t)g.Kimg, (cuuint64_t)g.Co, (cuuint64_t)g.N};
+        const cuuint64_t dims[3] = {(cuuint64_t)g.Kimg, (cuuint64_t)g.Co, (cuuint64_t)g.N * (g.split ? 2 : 1)};
         const cuuint64_t strides[2] = {(cuuint64_t)g.Kimg * 4, (cuuint64_t)g.Kimg * 4 * g.Co};
         const cuuint32_t box[3] = {32u, (cuuint32_t)g.bn, 1u};
         if (fn(&pl->mp.g_map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, pl->gf, dims, strides, box, es4,
@@ -200,6 +210,7 @@ void fill_wgrad_params(wgrad_plan_s *pl) {
     m.seg_rows = g.seg_rows; m.spt = g.spt; m.n_segs = g.n_segs; m.cpi = g.cpi;
     m.total_chunks = g.total_chunks; m.cps = g.cps; m.stages = g.stages; m.tmem_cols = g.tmem_cols;
     m.idesc = dgrad::tf32_idesc(128, g.bn);
+    m.split = g.split; m.N = g.N; m.n_copies = g.n_copies;
     m.timeout_ns = dgrad::kWgTimeoutNs;
     for (int sidx = 0; sidx < g.n_segs; ++sidx) {
         const int t = sidx / g.cpt;
@@ -210,8 +221,9 @@ void fill_wgrad_params(wgrad_plan_s *pl) {
     q.N = g.N; q.Ci = g.Ci; q.H = g.H; q.W = g.W; q.Co = g.Co; q.oH = g.oH; q.oW = g.oW;
     q.s = g.s; q.pw = g.pw; q.Wf = g.Wf; q.Kimg = g.Kimg; q.Lx = g.Lx; q.Ty = g.Ty; q.n_rh = g.n_rh;
     for (int i = 0; i < dgrad::kWgMaxRowPhases; ++i) q.rh_list[i] = g.rh_list[i];
-    q.g4 = (long long)(g.g_elems / 4);
-    q.x4 = (long long)(g.x_elems / 4);
+    q.split = g.split;
+    q.g4 = (long long)(g.g_elems / 4 / (g.split ? 2 : 1));
+    q.x4 = (long long)(g.x_elems / 4 / (g.split ? 2 : 1));
     dgrad::WgradReduceParams &r = pl->rp;
     r.part = pl->part;
     r.Co = g.Co; r.Ci = g.Ci; r.taps = g.taps; r.bn = g.bn; r.n_mt = g.n_mt; r.n_nt = g.n_nt; r.n_ks = g.n_ks;

@@ -16,6 +16,9 @@
 //    [s*u + kw - pw] (0 outside the input and for u >= oW), and tap t reads
 //    copy c at k + (dh + Ty)*Wf: a whole number of frame rows, so every
 //    tensor copy starts on a 16-byte boundary.
+// Split precision (TF32X3): both frames twice, hi = tf32(v) then
+// lo = tf32(v - hi) (gf planes [half][n][co], xc planes [half][copy][n][ci]),
+// and per chunk three K passes hi*lo, lo*hi, hi*hi.
 #pragma once
 
 #include "dgrad_internal.h"
@@ -38,7 +41,8 @@ struct WgradGeometry {
     int seg_rows, cpt, n_segs, spt;   // rows per segment, segments per tap, all segments, segments per row tile
     int n_mt, bn, n_nt, n_ks, cps;    // tiles of rows / columns, K splits, chunks per split
     int total_chunks, n_units, grid, stages, smem_bytes, tmem_cols;
-    size_t g_elems, x_elems, part_elems;
+    int split;                        // 1: split precision (hi and lo halves of both frames, three K passes)
+    size_t g_elems, x_elems, part_elems;   // frames: both halves when split
 };
 
 dgrad_status_t make_wgrad_geometry(int N, int Ci, int H, int W, int Co, int kH, int kW, int stride, int pad_h,
@@ -49,7 +53,8 @@ struct WgradPackParams {
     float *gf, *xc;
     int N, Ci, H, W, Co, oH, oW, s, pw, Wf, Kimg, Lx, Ty, n_rh;
     int rh_list[kWgMaxRowPhases];
-    long long g4, x4;   // float4 groups of gf and of xc
+    long long g4, x4;   // float4 groups of one half of gf and of xc
+    int split;          // 1: write hi = tf32(v) in half 0 and lo = tf32(v - hi) in half 1
 };
 
 struct WgradMainParams {
@@ -58,6 +63,7 @@ struct WgradMainParams {
     float *part;         // partial tiles [unit][bn][128], unit = (ks * n_mt + mt) * n_nt + nt
     uint32_t *err;
     int n_mt, n_nt, n_ks, n_units, bn, seg_rows, spt, n_segs, cpi, total_chunks, cps, stages, tmem_cols;
+    int split, N, n_copies;   // split precision: lo halves at image N + n (gf) and copy n_copies + c (xc)
     uint32_t idesc;
     long long timeout_ns;
     int4 seg[kWgMaxSegs];   // x: input copy, y: first input channel, z: K offset (elements)

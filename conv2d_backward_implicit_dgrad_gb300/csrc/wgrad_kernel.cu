@@ -10,7 +10,9 @@
 //   warp  5    one thread issuing the tensor copies: per 32-position chunk,
 //              one box of each (tap, input-channel block) segment of the row
 //              tile from the input copies (A) and one box of grad_out's
-//              frame (B)
+//              frame (B); with split precision the same boxes again from the
+//              lo halves, and the MMA warp issues A_hi*B_lo, A_lo*B_hi and
+//              A_hi*B_hi per chunk
 // A work unit is (row tile, column tile, K split); its 128 x bn fp32
 // accumulator lives in tensor memory (two sets, so that one unit's
 // epilogue overlaps the next unit's MMAs).  Every wait is bounded.
@@ -83,7 +85,8 @@ __global__ void __launch_bounds__(kWThreads, 1) wgrad_main_kernel(const __grid_c
     extern __shared__ __align__(1024) uint8_t smem[];
     WBars *bars = reinterpret_cast<WBars *>(smem);
     const uint32_t stage0 = (dev::smem_u32(smem) + kWBarrierBytes + 1023u) & ~1023u;
-    const uint32_t stage_bytes = kWStageA + static_cast<uint32_t>(p.bn) * 128u;
+    const uint32_t half_bytes = kWStageA + static_cast<uint32_t>(p.bn) * 128u;   // A | B of one half
+    const uint32_t stage_bytes = half_bytes * (p.split ? 2u : 1u);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
         for (int i = 0; i < p.stages; ++i) {
@@ -119,8 +122,9 @@ __global__ void __launch_bounds__(kWThreads, 1) wgrad_main_kernel(const __grid_c
             bool ok = true;
             for (int w = blockIdx.x; ok && w < p.n_units && !bars->abort_flag; w += gridDim.x) {
                 const WUnit u = decode_unit(p, w);
-                const uint32_t bytes = static_cast<uint32_t>((u.s1 - u.s0) * p.seg_rows) * 128u +
-                                       static_cast<uint32_t>(p.bn) * 128u;
+                const uint32_t bytes = (static_cast<uint32_t>((u.s1 - u.s0) * p.seg_rows) * 128u +
+                                        static_cast<uint32_t>(p.bn) * 128u) *
+                                       (p.split ? 2u : 1u);
                 for (int c = u.c0; c < u.c1; ++c) {
                     if (!dev::mbar_wait(dev::smem_u32(&bars->empty[ring.stage]), ring.parity ^ 1, tmo)) {
                         wfail(bars, p);
@@ -132,12 +136,15 @@ __global__ void __launch_bounds__(kWThreads, 1) wgrad_main_kernel(const __grid_c
                     const int n = c / p.cpi;
                     const int k0 = (c - n * p.cpi) * 32;
                     const uint32_t dst = stage0 + static_cast<uint32_t>(ring.stage) * stage_bytes;
-                    for (int s = u.s0; s < u.s1; ++s) {
-                        const int4 sg = p.seg[s];
-                        dev::tma_load_4d(dst + static_cast<uint32_t>((s - u.s0) * p.seg_rows) * 128u, &p.x_map,
-                                         k0 + sg.z, sg.y, n, sg.x, bar);
+                    for (int h = 0; h <= p.split; ++h) {   // half h at dst + h * half_bytes
+                        const uint32_t hd = dst + static_cast<uint32_t>(h) * half_bytes;
+                        for (int s = u.s0; s < u.s1; ++s) {
+                            const int4 sg = p.seg[s];
+                            dev::tma_load_4d(hd + static_cast<uint32_t>((s - u.s0) * p.seg_rows) * 128u, &p.x_map,
+                                             k0 + sg.z, sg.y, n, sg.x + h * p.n_copies, bar);
+                        }
+                        dev::tma_load_3d(hd + kWStageA, &p.g_map, k0, u.nt * p.bn, n + h * p.N, bar);
                     }
-                    dev::tma_load_3d(dst + kWStageA, &p.g_map, k0, u.nt * p.bn, n, bar);
                     last_parity[ring.stage] = static_cast<int>(ring.parity);
                     ring.next(p.stages);
                 }
@@ -171,10 +178,23 @@ __global__ void __launch_bounds__(kWThreads, 1) wgrad_main_kernel(const __grid_c
                 const uint32_t a = stage0 + static_cast<uint32_t>(ring.stage) * stage_bytes;
                 const uint64_t ad = dev::smem_desc_sw128(a, 0);
                 const uint64_t bd = dev::smem_desc_sw128(a + kWStageA, 0);
+                if (p.split) {
+                    // lo halves one half further on; the small cross terms first
+                    const uint64_t adl = dev::smem_desc_sw128(a + half_bytes, 0);
+                    const uint64_t bdl = dev::smem_desc_sw128(a + half_bytes + kWStageA, 0);
+                    const uint64_t pa[3] = {ad, adl, ad}, pb[3] = {bdl, bd, bd};
 #pragma unroll
-                for (int k8 = 0; k8 < 4; ++k8)
-                    dev::mma_tf32_elect(d, dev::desc_add(ad, 32 * k8), dev::desc_add(bd, 32 * k8), p.idesc,
-                                        (c > u.c0 || k8 > 0) ? 1u : 0u);
+                    for (int q = 0; q < 3; ++q)
+#pragma unroll
+                        for (int k8 = 0; k8 < 4; ++k8)
+                            dev::mma_tf32_elect(d, dev::desc_add(pa[q], 32 * k8), dev::desc_add(pb[q], 32 * k8),
+                                                p.idesc, (c > u.c0 || q > 0 || k8 > 0) ? 1u : 0u);
+                } else {
+#pragma unroll
+                    for (int k8 = 0; k8 < 4; ++k8)
+                        dev::mma_tf32_elect(d, dev::desc_add(ad, 32 * k8), dev::desc_add(bd, 32 * k8), p.idesc,
+                                            (c > u.c0 || k8 > 0) ? 1u : 0u);
+                }
                 dev::mma_commit_elect(dev::smem_u32(&bars->empty[ring.stage]));
             }
             if (!ok) break;
@@ -225,7 +245,8 @@ __global__ void __launch_bounds__(kWThreads, 1) wgrad_main_kernel(const __grid_c
 // input copies xc, TF32-rounded.  Thread item i writes the 4 consecutive
 // positions 4i .. 4i+3 of the concatenated buffers (32-bit indices: the host
 // keeps both below 2^31 groups); a thread takes kUnroll items a grid-stride
-// apart per pass and issues all their loads before any store.
+// apart per pass and issues all their loads before any store.  With split
+// precision the item also writes lo = tf32(v - hi) one half further on.
 __device__ __forceinline__ float4 wgrad_pack_item(const WgradPackParams &p, int i, int g4, int gper, int xper,
                                                   int nci, bool g_vec) {
     float v[4];
@@ -259,7 +280,7 @@ __device__ __forceinline__ float4 wgrad_pack_item(const WgradPackParams &p, int 
             if (++u == p.Wf) u = 0, ++y;
         }
     }
-    return make_float4(dev::round_tf32(v[0]), dev::round_tf32(v[1]), dev::round_tf32(v[2]), dev::round_tf32(v[3]));
+    return make_float4(v[0], v[1], v[2], v[3]);
 }
 
 __global__ void __launch_bounds__(256) wgrad_pack_kernel(const __grid_constant__ WgradPackParams p) {
@@ -282,7 +303,16 @@ __global__ void __launch_bounds__(256) wgrad_pack_kernel(const __grid_constant__
             const int i = i0 + u * step;
             if (i < total) {
                 float *dst = i < g4 ? p.gf + static_cast<size_t>(i) * 4 : p.xc + static_cast<size_t>(i - g4) * 4;
-                *reinterpret_cast<float4 *>(dst) = v[u];
+                const float4 x = v[u];
+                const float4 hi = make_float4(dev::round_tf32(x.x), dev::round_tf32(x.y), dev::round_tf32(x.z),
+                                              dev::round_tf32(x.w));
+                *reinterpret_cast<float4 *>(dst) = hi;
+                if (p.split) {
+                    const size_t half = static_cast<size_t>(i < g4 ? p.g4 : p.x4) * 4;
+                    *reinterpret_cast<float4 *>(dst + half) =
+                        make_float4(dev::round_tf32(x.x - hi.x), dev::round_tf32(x.y - hi.y),
+                                    dev::round_tf32(x.z - hi.z), dev::round_tf32(x.w - hi.w));
+                }
             }
         }
     }

@@ -23,10 +23,13 @@
  *   grad_weight [Co, Ci, kH, kW]  OIHW, fully OVERWRITTEN
  * with oH = floor((H + 2*pad_h - kH)/stride) + 1 and likewise oW.
  *
- * Arithmetic: DGRAD_PREC_TF32 only (both operands rounded to TF32, round to
+ * Arithmetic: DGRAD_PREC_TF32 (both operands rounded to TF32, round to
  * nearest with ties away from zero; products accumulated in fp32 on the
  * tcgen05 tensor cores, the batch-and-position sum split over CTAs and
- * finished by a second, deterministic pass).  Other precisions return
+ * finished by a second, deterministic pass) or DGRAD_PREC_TF32X3 (each
+ * operand v split into hi = tf32(v) and lo = tf32(v - hi), three tensor-core
+ * products hi*lo + lo*hi + hi*hi per term: fp32-level accuracy, about three
+ * times the tensor work and twice the frame bytes).  DGRAD_PREC_FP32 returns
  * DGRAD_ERR_UNSUPPORTED.
  *
  * Ownership, errors and streams follow dgrad.h: the caller owns the three

@@ -406,10 +406,28 @@ def test_wgrad_plans():
         with pytest.raises(dg.DgradError) as e:
             dg.wgrad_describe(*bad)
         assert e.value.status == status
-    for prec in ("fp32", "tf32x3"):
-        with pytest.raises(dg.DgradError) as e:
-            dg.wgrad_describe(2, 3, 8, 8, 4, 3, 3, 1, 1, 1, prec)
-        assert e.value.status == 2
+    with pytest.raises(dg.DgradError) as e:
+        dg.wgrad_describe(2, 3, 8, 8, 4, 3, 3, 1, 1, 1, "fp32")
+    assert e.value.status == 2
+
+
+def test_wgrad_split_plans():
+    """Split precision: same tiling, both frames twice, a stage ring of at
+    least two (hi | lo) stages within the shared-memory limit."""
+    for name in ORDER:
+        wl = WORKLOADS[name]
+        a = dg.wgrad_describe(*wl.plan_args(), sm_count=152)
+        b = dg.wgrad_describe(*wl.plan_args(), precision="tf32x3", sm_count=152)
+        assert b["precision"] == "tf32x3" and a["precision"] == "tf32"
+        for k in ("n_mt", "n_nt", "slice_n", "seg_rows", "Kimg", "Lx", "n_copies", "useful_flops"):
+            assert a[k] == b[k], k
+        chunks = wl.N * b["Kimg"] // 32
+        assert b["n_ks"] >= a["n_ks"] and -(-chunks // b["n_ks"]) <= 12   # short accumulation chains
+        assert b["n_units"] == b["n_mt"] * b["n_nt"] * b["n_ks"]
+        stage = 2 * (128 * 128 + b["slice_n"] * 128)
+        assert b["stages"] >= 2 and b["smem_bytes"] >= b["stages"] * stage and b["smem_bytes"] <= 232448
+        frames = 4 * (wl.N * wl.Co * a["Kimg"] + a["n_copies"] * wl.N * wl.Ci * a["Lx"])
+        assert b["workspace_bytes"] - a["workspace_bytes"] >= frames - 512   # regions are 256-byte aligned
 
 
 def test_col2im_plans():
