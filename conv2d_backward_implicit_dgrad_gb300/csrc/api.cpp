@@ -38,6 +38,7 @@ struct dgrad_plan_s {
     dgrad_plan_s *sub[2];          // sub-plans for chunk_n images and for the remainder
     cudaStream_t h2d, d2h;
     cudaEvent_t ev_in[kHostChunks], ev_out[kHostChunks];
+    uint32_t *host_err;            // page-locked copies of the sub-plans' error words
     int host_ready;
     size_t workspace_bytes;
     int packed;            // dgrad_prepack (or dgrad_run) has run at least once
@@ -233,20 +234,27 @@ dgrad_status_t make_host_pipeline(dgrad_plan_s *plan) {
     const int rem = g.N % plan->chunk_n;
     const int sizes[2] = {plan->chunk_n, rem};
     for (int i = 0; i < 2; ++i) {
-        if (sizes[i] == 0) continue;
+        if (sizes[i] == 0 || plan->sub[i]) continue;
         dgrad_status_t st = dgrad_plan_ex(sizes[i], g.Ci, g.H, g.W, g.Co, g.kH, g.kW, g.s, g.ph, g.pw,
                                           static_cast<dgrad_precision_t>(plan->precision), &plan->opts, &plan->sub[i]);
         if (st != DGRAD_OK) return st;
     }
-    if (cudaStreamCreateWithFlags(&plan->h2d, cudaStreamNonBlocking) != cudaSuccess) return cuda_status(cudaGetLastError());
-    if (cudaStreamCreateWithFlags(&plan->d2h, cudaStreamNonBlocking) != cudaSuccess) {
-        cudaStreamDestroy(plan->h2d);
+    // Each object is made once; after a failure the next call makes what is
+    // missing and dgrad_plan_destroy releases what exists.
+    if (!plan->h2d && cudaStreamCreateWithFlags(&plan->h2d, cudaStreamNonBlocking) != cudaSuccess)
         return cuda_status(cudaGetLastError());
-    }
+    if (!plan->d2h && cudaStreamCreateWithFlags(&plan->d2h, cudaStreamNonBlocking) != cudaSuccess)
+        return cuda_status(cudaGetLastError());
     for (int i = 0; i < kHostChunks; ++i) {
-        if (cudaEventCreateWithFlags(&plan->ev_in[i], cudaEventDisableTiming) != cudaSuccess ||
-            cudaEventCreateWithFlags(&plan->ev_out[i], cudaEventDisableTiming) != cudaSuccess)
+        if ((!plan->ev_in[i] && cudaEventCreateWithFlags(&plan->ev_in[i], cudaEventDisableTiming) != cudaSuccess) ||
+            (!plan->ev_out[i] && cudaEventCreateWithFlags(&plan->ev_out[i], cudaEventDisableTiming) != cudaSuccess))
             return cuda_status(cudaGetLastError());
+    }
+    if (!plan->host_err) {
+        void *h = nullptr;
+        if (cudaHostAlloc(&h, 2 * sizeof(uint32_t), cudaHostAllocDefault) != cudaSuccess)
+            return cuda_status(cudaGetLastError());
+        plan->host_err = static_cast<uint32_t *>(h);
     }
     plan->host_ready = 1;
     return DGRAD_OK;
@@ -516,6 +524,12 @@ dgrad_status_t dgrad_run_host(dgrad_plan_t plan, const float *grad_out_host, con
             e = cudaMemcpyAsync(reinterpret_cast<uint8_t *>(grad_input_host) + n0 * gi_img, dgi, nn * gi_img,
                                 cudaMemcpyDeviceToHost, plan->d2h);
     }
+    // The sub-plans' error words ride behind the last output copy (which
+    // waits for every run), so no extra synchronisation reads them.
+    for (int i = 0; e == cudaSuccess && i < 2; ++i)
+        if (plan->sub[i])
+            e = cudaMemcpyAsync(&plan->host_err[i], plan->sub[i]->err, sizeof(uint32_t), cudaMemcpyDeviceToHost,
+                                plan->d2h);
     const cudaError_t e1 = cudaStreamSynchronize(plan->h2d);
     const cudaError_t e2 = cudaStreamSynchronize(plan->d2h);
     const cudaError_t e3 = cudaStreamSynchronize(s);
@@ -525,7 +539,11 @@ dgrad_status_t dgrad_run_host(dgrad_plan_t plan, const float *grad_out_host, con
     if (e3 != cudaSuccess) return cuda_status(e3);
     // a bounded wait that ran out in a sub-plan's kernels is reported here
     for (int i = 0; i < 2; ++i)
-        if (plan->sub[i] && (st = dgrad_plan_check(plan->sub[i])) != DGRAD_OK) return st;
+        if (plan->sub[i] && plan->host_err[i] != 0) {
+            plan->host_err[i] = 0;
+            if (cudaMemset(plan->sub[i]->err, 0, sizeof(uint32_t)) != cudaSuccess) return cuda_status(cudaGetLastError());
+            return DGRAD_ERR_DEVICE_TIMEOUT;
+        }
     return DGRAD_OK;
 }
 
@@ -546,14 +564,13 @@ void dgrad_plan_destroy(dgrad_plan_t plan) {
     cudaDeviceSynchronize();
     cudaFree(plan->err);
     if (plan->stage_go) cudaFree(plan->stage_go);
-    if (plan->host_ready) {
-        for (int i = 0; i < kHostChunks; ++i) {
-            cudaEventDestroy(plan->ev_in[i]);
-            cudaEventDestroy(plan->ev_out[i]);
-        }
-        cudaStreamDestroy(plan->h2d);
-        cudaStreamDestroy(plan->d2h);
+    for (int i = 0; i < kHostChunks; ++i) {
+        if (plan->ev_in[i]) cudaEventDestroy(plan->ev_in[i]);
+        if (plan->ev_out[i]) cudaEventDestroy(plan->ev_out[i]);
     }
+    if (plan->h2d) cudaStreamDestroy(plan->h2d);
+    if (plan->d2h) cudaStreamDestroy(plan->d2h);
+    if (plan->host_err) cudaFreeHost(plan->host_err);
     for (int i = 0; i < 2; ++i)
         if (plan->sub[i]) dgrad_plan_destroy(plan->sub[i]);
     if (cur >= 0 && cur != plan->device) cudaSetDevice(cur);

@@ -107,19 +107,33 @@ dgrad_status_t make_wgrad_geometry(int N, int Ci, int H, int W, int Co, int kH, 
     // Column tiles of output channels (MMA N <= 256).
     g.n_nt = ceil_div(Co, 256);
     g.bn = round_up(ceil_div(Co, g.n_nt), 16);
-    // K splits: about two work units per SM, each at least 8 chunks long.
+    // K splits.  A CTA runs units w = blockIdx.x, + grid, ...; the slowest CTA
+    // runs ceil(units / grid) units of up to cps chunks each, plus about two
+    // chunks' worth of time per unit for its partial tile, so the split count
+    // minimises ceil(tiles * n_ks / sm) * (cps + 2) (ties: fewer splits), with
+    // units of at least 8 chunks and at most eight waves of them.
     const long long total_chunks = (long long)N * g.cpi;
     if (total_chunks > INT_MAX / 2) return DGRAD_ERR_UNSUPPORTED;
     g.total_chunks = (int)total_chunks;
     const int tiles = g.n_mt * g.n_nt;
-    int n_ks = std::max(1, ceil_div(2 * sm_count, tiles));
-    n_ks = std::min(n_ks, std::max(1, g.total_chunks / 8));
     // Split precision: the tensor cores' fp32 accumulation loses accuracy about
     // in proportion to the number of MMAs accumulated into one accumulator
     // (measured near 2e-8 relative error per MMA on random data), so a unit
     // takes at most kWgSplitChunks chunks (12 MMAs each) and the rest of the
     // sum goes to the fp32 reduction of the partial tiles.
-    if (g.split) n_ks = std::max(n_ks, ceil_div(g.total_chunks, kWgSplitChunks));
+    const int ks_lo = g.split ? ceil_div(g.total_chunks, kWgSplitChunks) : 1;
+    const int ks_hi = std::max(ks_lo, std::min(std::max(1, g.total_chunks / 8), ceil_div(8 * sm_count, tiles)));
+    long long best_cost = -1;
+    int n_ks = ks_lo;
+    for (int k = ks_lo; k <= ks_hi; ++k) {
+        const int cps = ceil_div(g.total_chunks, k);
+        if (ceil_div(g.total_chunks, cps) != k) continue;   // the same split as a smaller count
+        const long long cost = (long long)ceil_div(tiles * k, sm_count) * (cps + 2);
+        if (best_cost < 0 || cost < best_cost) {
+            best_cost = cost;
+            n_ks = k;
+        }
+    }
     g.cps = ceil_div(g.total_chunks, n_ks);
     g.n_ks = ceil_div(g.total_chunks, g.cps);
     const long long units = (long long)tiles * g.n_ks;
