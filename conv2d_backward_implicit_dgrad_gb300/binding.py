@@ -30,8 +30,8 @@ PATH_NAME = {v: k for k, v in PATH.items()}
 EXPORTS = ("dgrad_plan", "dgrad_plan_ex", "dgrad_describe", "dgrad_describe_taps", "dgrad_plan_info", "dgrad_run",
            "dgrad_run_fused", "dgrad_prepack", "dgrad_run_packed", "dgrad_pack_grad_out", "dgrad_run_main", "dgrad_run_host", "dgrad_run_noalloc", "dgrad_plan_check",
            "dgrad_plan_destroy", "dgrad_status_string", "dgrad_cuda_error_string",
-           "wgrad_describe", "wgrad_describe_taps", "wgrad_plan", "wgrad_plan_info", "wgrad_run", "wgrad_plan_check",
-           "wgrad_plan_destroy")
+           "wgrad_describe", "wgrad_describe_taps", "wgrad_describe_window", "wgrad_plan", "wgrad_plan_info",
+           "wgrad_run", "wgrad_plan_check", "wgrad_plan_destroy")
 
 
 class Options(ctypes.Structure):
@@ -42,7 +42,9 @@ class Options(ctypes.Structure):
 
 class WgradPlanInfo(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int) for n in ("N", "Ci", "H", "W", "Co", "kH", "kW", "stride", "pad_h", "pad_w",
-                                            "oH", "oW", "precision", "Wf", "Kimg", "Lx", "n_copies", "seg_rows",
+                                            "oH", "oW", "precision", "interleave", "mode", "Wf", "Kimg", "Lx",
+                                            "n_copies",
+                                            "seg_rows",
                                             "n_mt", "n_nt", "n_ks", "slice_n", "n_units", "grid", "stages",
                                             "smem_bytes", "tmem_cols")] + [
         ("workspace_bytes", ctypes.c_size_t), ("useful_flops", ctypes.c_double),
@@ -377,19 +379,45 @@ def wgrad_describe(N, Ci, H, W, Co, kH, kW, stride, pad_h, pad_w, precision="tf3
 
 def wgrad_describe_taps(N, Ci, H, W, Co, kH, kW, stride, pad_h, pad_w) -> dict:
     """Host-only tap table of the weight gradient: per tap (kh*kW + kw) the input
-    copy and K offset it reads; per input copy its kernel column and row phase."""
+    copy and K offset it reads; per input copy its row phase, column phase and
+    column shift; the copies' leading zero rows and columns; the number of
+    images interleaved along K."""
     lib = load_library()
     cap = 1024
     cp, off = (ctypes.c_int * cap)(), (ctypes.c_int * cap)()
-    ckw, crh = (ctypes.c_int * cap)(), (ctypes.c_int * cap)()
-    nc, ty = ctypes.c_int(), ctypes.c_int()
-    st = lib.wgrad_describe_taps(N, Ci, H, W, Co, kH, kW, stride, pad_h, pad_w, cap, cp, off, ckw, crh,
-                                 ctypes.byref(nc), ctypes.byref(ty))
+    crh, crw, csh = (ctypes.c_int * cap)(), (ctypes.c_int * cap)(), (ctypes.c_int * cap)()
+    nc, ty, tu, f = ctypes.c_int(), ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
+    st = lib.wgrad_describe_taps(N, Ci, H, W, Co, kH, kW, stride, pad_h, pad_w, cap, cp, off, crh, crw, csh,
+                                 ctypes.byref(nc), ctypes.byref(ty), ctypes.byref(tu), ctypes.byref(f))
     if st != 0:
         raise DgradError(st, "wgrad_describe_taps")
-    taps = kH * kW
-    return {"copy": list(cp[:taps]), "offset": list(off[:taps]), "copy_kw": list(ckw[:nc.value]),
-            "copy_rh": list(crh[:nc.value]), "Ty": ty.value}
+    taps, n = kH * kW, nc.value
+    return {"copy": list(cp[:taps]), "offset": list(off[:taps]), "copy_rh": list(crh[:n]),
+            "copy_rw": list(crw[:n]), "copy_shift": list(csh[:n]), "Ty": ty.value, "Tu": tu.value,
+            "interleave": f.value}
+
+
+def wgrad_describe_window(N, Ci, H, W, Co, kH, kW, stride, pad_h, pad_w, sm_count=0):
+    """Host-only run-mode table of the weight gradient (None when the shape
+    runs the segment mode): tap groups, tiles, stage length and tiles per unit."""
+    lib = load_library()
+    cap = 1024
+    hdr = (ctypes.c_int * 15)()
+    grp, taps, tiles = (ctypes.c_int * (6 * cap))(), (ctypes.c_int * cap)(), (ctypes.c_int * (2 * cap))()
+    st = lib.wgrad_describe_window(N, Ci, H, W, Co, kH, kW, stride, pad_h, pad_w, sm_count, cap, hdr, grp, taps,
+                                   tiles)
+    if st == 2:
+        return None
+    if st != 0:
+        raise DgradError(st, "wgrad_describe_window")
+    keys = ("n_groups", "n_tiles", "spt", "seg_rows", "stages", "Pg", "Px", "cps", "nksq", "cpt", "n_nt", "Q", "L",
+            "tpu", "n_sets")
+    d = dict(zip(keys, hdr[:15]))
+    d["groups"] = [dict(zip(("copy", "base", "n_taps", "n_mt", "unused", "tap0"), grp[6 * i:6 * i + 6]))
+                   for i in range(d["n_groups"])]
+    d["taps"] = list(taps[:kH * kW])
+    d["tiles"] = [(tiles[2 * t], tiles[2 * t + 1]) for t in range(d["n_tiles"])]
+    return d
 
 
 class WgradPlan:

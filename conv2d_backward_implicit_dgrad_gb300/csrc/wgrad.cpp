@@ -15,6 +15,7 @@ struct wgrad_plan_s {
     int device;
     dgrad::WgradGeometry g;
     dgrad::WgradMainParams mp;
+    dgrad::WgradWinParams wp;   // window mode
     dgrad::WgradPackParams pp;
     dgrad::WgradReduceParams rp;
     uint32_t *err;
@@ -43,6 +44,119 @@ size_t align256(size_t b) { return (b + 255) & ~size_t(255); }
 
 }  // namespace
 
+// Run mode (see WgradWinParams).  Taps are grouped by (kernel row, input
+// copy); within a group consecutive taps read consecutive positions, so a
+// tile of spt of them is a contiguous run of position blocks.  The stage
+// length L and the tiles per unit come from a cost model: a tensor copy
+// takes about kWgCopyCycles on an SM whatever its size (up to 32 KB), a
+// 128 x bn x 8 TF32 MMA about kWgMmaCycles(bn); both overlap, the slower
+// bounds a stage.  Returns false where the segment mode stays.
+constexpr int kWgCopyCycles = 550;
+static int mma_cycles(int bn) { return bn <= 32 ? 66 : (bn <= 64 ? 72 : (bn <= 128 ? 84 : 128)); }
+
+static bool plan_window(WgradGeometry &g, int sm_count) {
+    if (!g.blocked || g.split) return false;
+    int sr = 8;   // rows per position block: the input channels rounded up to a power of two, 8 .. 128
+    while (sr < g.Ci && sr < 128) sr *= 2;
+    const int spt = 128 / sr;
+    g.n_groups = 0;
+    int ntap = 0;
+    for (int kh = 0; kh < g.kH; ++kh) {
+        for (int kw = 0; kw < g.kW; ++kw) {
+            const int t = kh * g.kW + kw;
+            bool seen = false;   // a group of this row and copy already holds the tap
+            for (int k2 = 0; k2 < kw; ++k2)
+                if (g.tap_copy[kh * g.kW + k2] == g.tap_copy[t]) seen = true;
+            if (seen) continue;
+            if (g.n_groups == kWgMaxGroups) return false;
+            const int gi = g.n_groups++;
+            g.grp_copy[gi] = g.tap_copy[t];
+            g.grp_base[gi] = g.tap_off[t] / 32;
+            g.grp_tap0[gi] = ntap;
+            g.grp_nt[gi] = 0;
+            for (int k2 = kw; k2 < g.kW; ++k2) {
+                const int t2 = kh * g.kW + k2;
+                if (g.tap_copy[t2] != g.tap_copy[t]) continue;
+                if (g.tap_off[t2] != g.tap_off[t] + 32 * g.grp_nt[gi]) return false;   // not consecutive positions
+                g.grp_taps[ntap++] = t2;
+                ++g.grp_nt[gi];
+            }
+        }
+    }
+    g.n_tiles = 0;
+    for (int gi = 0; gi < g.n_groups; ++gi) {
+        g.grp_nmt[gi] = ceil_div(g.grp_nt[gi], spt);
+        for (int m = 0; m < g.grp_nmt[gi]; ++m) {
+            if (g.n_tiles == kWgMaxTiles) return false;
+            g.tile_grp[g.n_tiles] = gi;
+            g.tile_m0[g.n_tiles++] = m * spt;
+        }
+    }
+    // Stage length L (a copy of L + spt - 1 position blocks of sr rows and
+    // one of L grad_out blocks of bn rows, at most 256 rows each) and tiles per
+    // unit: the least time per (tile, chunk) with at least two stages in
+    // shared memory and the unit's accumulators in tensor memory.
+    const int l_max = std::min(8, std::min(256 / sr - spt + 1, 256 / g.bn));
+    double best = -1.0;
+    int bl = 0, bt = 0, bd = 0;
+    for (int L = 1; L <= l_max; ++L)
+        for (int tpu = 1; tpu <= std::min(g.n_tiles, 512 / g.bn); ++tpu) {
+            const long long stage = (long long)tpu * (L + spt - 1) * sr * 128 + (long long)L * g.bn * 128;
+            const int d = (int)std::min<long long>(kWgMaxStages, (kMaxSmem - kWgBarrierBytes) / stage);
+            if (d < 2) continue;
+            const int sets = ceil_div(g.n_tiles, tpu);
+            const double per_stage = std::max((double)(tpu + 1) * kWgCopyCycles, (double)L * tpu * 4 * mma_cycles(g.bn));
+            const double cost = per_stage / L * sets;   // per chunk, all tiles
+            if (best < 0 || cost < best * 0.999) {
+                best = cost;
+                bl = L; bt = tpu; bd = d;
+            }
+        }
+    // With one position per copy and one tap per tile nothing is shared: the
+    // segment mode does the same copies.
+    if (!bl || (bl == 1 && spt == 1)) return false;
+    g.seg_rows = sr;
+    g.spt = spt;
+    g.cpt = ceil_div(g.Ci, sr);
+    g.run_len = bl;
+    g.tpu = bt;
+    g.n_sets = ceil_div(g.n_tiles, bt);
+    g.stages = bd;
+    g.xbox_bytes = (bl + spt - 1) * sr * 128;
+    g.bbox_bytes = bl * g.bn * 128;
+    g.smem_bytes = kWgBarrierBytes + bd * (bt * g.xbox_bytes + g.bbox_bytes);
+    g.acc_sets = 2 * bt * g.bn <= 512 ? 2 : 1;
+    g.tmem_cols = pow2_at_least(std::max(32, g.acc_sets * bt * g.bn));
+    // K splits within each image group, units of whole stages: minimise
+    // ceil(units / sm) * (stages + about two stages of fill and partial-tile
+    // stores) per unit.
+    const int per = g.n_sets * g.cpt * g.n_nt * g.Q;
+    const int stages_total = ceil_div(g.cpi, bl);
+    const int ks_hi = std::max(1, std::min(stages_total / 2, ceil_div(8 * sm_count, per)));
+    long long bestk = -1;
+    int nk = 1;
+    for (int k = 1; k <= ks_hi; ++k) {
+        const int sps = ceil_div(stages_total, k);
+        if (ceil_div(stages_total, sps) != k) continue;
+        const long long cost = (long long)ceil_div(per * k, sm_count) * (sps + 2);
+        if (bestk < 0 || cost < bestk) {
+            bestk = cost;
+            nk = k;
+        }
+    }
+    g.cps = ceil_div(stages_total, nk) * bl;
+    g.nksq = ceil_div(g.cpi, g.cps);
+    g.n_ks = g.Q * g.nksq;
+    g.n_mt = g.n_tiles;
+    const long long units = (long long)per * g.nksq;
+    if (units > INT_MAX / 2) return false;
+    g.n_units = (int)units;
+    g.grid = std::min(g.n_units, sm_count);
+    g.part_elems = (size_t)g.Q * g.nksq * g.cpt * g.n_nt * g.n_tiles * g.bn * 128;
+    g.win = 1;
+    return true;
+}
+
 dgrad_status_t make_wgrad_geometry(int N, int Ci, int H, int W, int Co, int kH, int kW, int stride, int pad_h,
                                    int pad_w, int precision, int sm_count, WgradGeometry *out) {
     if (N < 1 || Ci < 1 || H < 1 || W < 1 || Co < 1 || kH < 1 || kW < 1 || stride < 1 || pad_h < 0 || pad_w < 0)
@@ -62,41 +176,67 @@ dgrad_status_t make_wgrad_geometry(int N, int Ci, int H, int W, int Co, int kH, 
     const int halves = g.split ? 2 : 1;
     g.oH = (int)(nh / stride) + 1;
     g.oW = (int)(nw / stride) + 1;
-    g.Wf = round_up(g.oW, 4);
-    if ((long long)g.oH * g.Wf > INT_MAX / 2) return DGRAD_ERR_UNSUPPORTED;
-    g.Kimg = round_up(g.oH * g.Wf, 32);
-    g.cpi = g.Kimg / 32;
-    // Row decomposition of the taps: kh - ph = s*dh + rh.
-    int dh_min = INT_MAX, dh_max = INT_MIN;
-    int dh_of[kMaxTaps], rhi_of[kMaxTaps];
-    g.n_rh = 0;
+    // Images interleaved along K.  Batch-blocked frames (f = 32, batches of
+    // 32 or more with at most 1/8 of padding images): a 32-element K chunk is
+    // one frame position of 32 images and a (position, channel block) tile is
+    // one contiguous run of memory.  Otherwise f = 4 (2, 1 for smaller
+    // batches): a tap offset of whole columns is then a multiple of 4
+    // positions (16 bytes, the tensor-copy alignment) once the copies absorb
+    // column shifts mod m = 4/f.
+    g.blocked = N >= 32 && (round_up(N, 32) - N) * 8 <= N;
+    g.f = g.blocked ? 32 : (N >= 4 ? 4 : (N >= 2 ? 2 : 1));
+    g.lf = g.f == 32 ? 5 : (g.f == 4 ? 2 : (g.f == 2 ? 1 : 0));
+    g.m = g.f >= 4 ? 1 : 4 / g.f;
+    g.Q = ceil_div(N, g.f);
+    // Decomposition of the taps: kh - ph = s*dh + rh, kw - pw = s*dw + rw.
+    int dh_of[kMaxTaps], rh_of[kMaxTaps], dw_of[kMaxTaps], rw_of[kMaxTaps];
+    int dh_min = INT_MAX, dh_max = INT_MIN, dw_min = INT_MAX, dw_max = INT_MIN;
     for (int kh = 0; kh < kH; ++kh) {
-        const int e = kh - pad_h;
-        const int dh = floor_div(e, stride), rh = e - dh * stride;
-        int idx = -1;
-        for (int i = 0; i < g.n_rh; ++i)
-            if (g.rh_list[i] == rh) idx = i;
-        if (idx < 0) {
-            idx = g.n_rh;
-            g.rh_list[g.n_rh++] = rh;
-        }
-        dh_of[kh] = dh;
-        rhi_of[kh] = idx;
-        dh_min = std::min(dh_min, dh);
-        dh_max = std::max(dh_max, dh);
+        dh_of[kh] = floor_div(kh - pad_h, stride);
+        rh_of[kh] = kh - pad_h - dh_of[kh] * stride;
+        dh_min = std::min(dh_min, dh_of[kh]);
+        dh_max = std::max(dh_max, dh_of[kh]);
+    }
+    for (int kw = 0; kw < kW; ++kw) {
+        dw_of[kw] = floor_div(kw - pad_w, stride);
+        rw_of[kw] = kw - pad_w - dw_of[kw] * stride;
+        dw_min = std::min(dw_min, dw_of[kw]);
+        dw_max = std::max(dw_max, dw_of[kw]);
     }
     g.Ty = std::max(0, -dh_min);
-    const long long lx = (long long)g.Kimg + (long long)(dh_max + g.Ty) * g.Wf;
-    if (lx > INT_MAX / 2) return DGRAD_ERR_UNSUPPORTED;
-    g.Lx = (int)lx;
-    g.n_copies = kW * g.n_rh;
+    g.Tu = std::max(0, -dw_min);
+    // Frame rows hold grad_out columns 0..oW-1 and every column a tap reads
+    // for them (u = ow + dw + Tu - r <= oW - 1 + dw_max + Tu), a multiple of m.
+    const long long wf = round_up(g.oW + std::max(0, dw_max) + g.Tu, g.m);
+    if (wf * g.oH * g.f > INT_MAX / 4) return DGRAD_ERR_UNSUPPORTED;
+    g.Wf = (int)wf;
+    g.Kimg = round_up(g.oH * g.Wf * g.f, 32);
+    g.cpi = g.Kimg / 32;
+    // Copies: one per (row phase, column phase, column shift r) some tap reads.
+    g.n_copies = 0;
     g.taps = kH * kW;
+    int max_off = 0;
     for (int kh = 0; kh < kH; ++kh)
         for (int kw = 0; kw < kW; ++kw) {
             const int t = kh * kW + kw;
-            g.tap_copy[t] = kw * g.n_rh + rhi_of[kh];
-            g.tap_off[t] = (dh_of[kh] + g.Ty) * g.Wf;
+            const int r = (dw_of[kw] + g.Tu) % g.m;
+            int c = -1;
+            for (int i = 0; i < g.n_copies; ++i)
+                if (g.copy_rh[i] == rh_of[kh] && g.copy_rw[i] == rw_of[kw] && g.copy_r[i] == r) c = i;
+            if (c < 0) {
+                if (g.n_copies == kWgMaxCopies) return DGRAD_ERR_UNSUPPORTED;
+                c = g.n_copies++;
+                g.copy_rh[c] = rh_of[kh];
+                g.copy_rw[c] = rw_of[kw];
+                g.copy_r[c] = r;
+            }
+            g.tap_copy[t] = c;
+            g.tap_off[t] = ((dh_of[kh] + g.Ty) * g.Wf + (dw_of[kw] + g.Tu - r)) * g.f;
+            max_off = std::max(max_off, g.tap_off[t]);
         }
+    const long long lx = (long long)g.Kimg + max_off;
+    if (lx > INT_MAX / 2) return DGRAD_ERR_UNSUPPORTED;
+    g.Lx = (int)lx;   // a multiple of 4 (of 32 when blocked): Kimg of 32, every offset of 4 (32)
     // Row tiles: (tap, input-channel block) segments of seg_rows rows.
     g.seg_rows = std::min(128, round_up(Ci, 8));
     g.cpt = ceil_div(Ci, g.seg_rows);
@@ -112,7 +252,7 @@ dgrad_status_t make_wgrad_geometry(int N, int Ci, int H, int W, int Co, int kH, 
     // chunks' worth of time per unit for its partial tile, so the split count
     // minimises ceil(tiles * n_ks / sm) * (cps + 2) (ties: fewer splits), with
     // units of at least 8 chunks and at most eight waves of them.
-    const long long total_chunks = (long long)N * g.cpi;
+    const long long total_chunks = (long long)g.Q * g.cpi;
     if (total_chunks > INT_MAX / 2) return DGRAD_ERR_UNSUPPORTED;
     g.total_chunks = (int)total_chunks;
     const int tiles = g.n_mt * g.n_nt;
@@ -145,10 +285,11 @@ dgrad_status_t make_wgrad_geometry(int N, int Ci, int H, int W, int Co, int kH, 
     if (g.stages < 2) return DGRAD_ERR_UNSUPPORTED;
     g.smem_bytes = kWgBarrierBytes + g.stages * stage_bytes;
     g.tmem_cols = pow2_at_least(2 * g.bn);
-    g.g_elems = (size_t)halves * N * Co * g.Kimg;
-    g.x_elems = (size_t)halves * g.n_copies * N * Ci * g.Lx;
+    g.g_elems = (size_t)halves * g.Q * Co * g.Kimg;
+    g.x_elems = (size_t)halves * g.n_copies * g.Q * Ci * g.Lx;
     if ((g.g_elems + g.x_elems) / 4 > (size_t)INT_MAX) return DGRAD_ERR_UNSUPPORTED;   // 32-bit pack indices
     g.part_elems = (size_t)g.n_units * g.bn * 128;
+    plan_window(g, sm_count);
     *out = g;
     return DGRAD_OK;
 }
@@ -165,6 +306,8 @@ void fill_wgrad_info(const WgradGeometry &g, size_t ws, wgrad_plan_info_t *info)
     info->kH = g.kH; info->kW = g.kW; info->stride = g.s; info->pad_h = g.ph; info->pad_w = g.pw;
     info->oH = g.oH; info->oW = g.oW;
     info->precision = g.split ? DGRAD_PREC_TF32X3 : DGRAD_PREC_TF32;
+    info->interleave = g.f;
+    info->mode = g.win;
     info->Wf = g.Wf; info->Kimg = g.Kimg; info->Lx = g.Lx; info->n_copies = g.n_copies;
     info->seg_rows = g.seg_rows; info->n_mt = g.n_mt; info->n_nt = g.n_nt; info->n_ks = g.n_ks;
     info->slice_n = g.bn; info->n_units = g.n_units; info->grid = g.grid; info->stages = g.stages;
@@ -192,26 +335,31 @@ dgrad_status_t encode_maps(wgrad_plan_s *pl) {
     if (!fn) return DGRAD_ERR_CUDA;
     const WgradGeometry &g = pl->g;
     const cuuint32_t es4[4] = {1u, 1u, 1u, 1u};
-    {
-        const cuuint64_t dims[4] = {(cuuint64_t)g.Lx, (cuuint64_t)g.Ci, (cuuint64_t)g.N,
-                                    (cuuint64_t)g.n_copies * (g.split ? 2 : 1)};
-        const cuuint64_t strides[3] = {(cuuint64_t)g.Lx * 4, (cuuint64_t)g.Lx * 4 * g.Ci,
-                                       (cuuint64_t)g.Lx * 4 * g.Ci * g.N};
-        const cuuint32_t box[4] = {32u, (cuuint32_t)g.seg_rows, 1u, 1u};
-        if (fn(&pl->mp.x_map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, pl->xc, dims, strides, box, es4,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-            return DGRAD_ERR_CUDA;
+    const cuuint64_t halves = g.split ? 2 : 1;
+    cuuint64_t xd[4], xs[3], gd[3], gs[2];
+    if (g.blocked) {   // [copy][q * Px + position][ci][32 images], [q * Pg + position][co][32 images]
+        const cuuint64_t px = (cuuint64_t)g.Lx / 32, pg = (cuuint64_t)g.cpi;
+        xd[0] = 32; xd[1] = (cuuint64_t)g.Ci; xd[2] = (cuuint64_t)g.Q * px; xd[3] = (cuuint64_t)g.n_copies * halves;
+        xs[0] = 128; xs[1] = 128 * (cuuint64_t)g.Ci; xs[2] = xs[1] * g.Q * px;
+        gd[0] = 32; gd[1] = (cuuint64_t)g.Co; gd[2] = (cuuint64_t)g.Q * pg * halves;
+        gs[0] = 128; gs[1] = 128 * (cuuint64_t)g.Co;
+    } else {           // [copy][q][ci][Lx], [q][co][Kimg]
+        xd[0] = (cuuint64_t)g.Lx; xd[1] = (cuuint64_t)g.Ci; xd[2] = (cuuint64_t)g.Q;
+        xd[3] = (cuuint64_t)g.n_copies * halves;
+        xs[0] = (cuuint64_t)g.Lx * 4; xs[1] = xs[0] * g.Ci; xs[2] = xs[1] * g.Q;
+        gd[0] = (cuuint64_t)g.Kimg; gd[1] = (cuuint64_t)g.Co; gd[2] = (cuuint64_t)g.Q * halves;
+        gs[0] = (cuuint64_t)g.Kimg * 4; gs[1] = gs[0] * g.Co;
     }
-    {
-        const cuuint64_t dims[3] = {(cuuint64_t)g.Kimg, (cuuint64_t)g.Co, (cuuint64_t)g.N * (g.split ? 2 : 1)};
-        const cuuint64_t strides[2] = {(cuuint64_t)g.Kimg * 4, (cuuint64_t)g.Kimg * 4 * g.Co};
-        const cuuint32_t box[3] = {32u, (cuuint32_t)g.bn, 1u};
-        if (fn(&pl->mp.g_map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, pl->gf, dims, strides, box, es4,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-            return DGRAD_ERR_CUDA;
-    }
+    const cuuint32_t xbox[4] = {32u, (cuuint32_t)g.seg_rows, g.win ? (cuuint32_t)(g.run_len + g.spt - 1) : 1u, 1u};
+    if (fn(&pl->mp.x_map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, pl->xc, xd, xs, xbox, es4, CU_TENSOR_MAP_INTERLEAVE_NONE,
+           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return DGRAD_ERR_CUDA;
+    const cuuint32_t gbox[3] = {32u, (cuuint32_t)g.bn, g.win ? (cuuint32_t)g.run_len : 1u};
+    if (fn(&pl->mp.g_map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, pl->gf, gd, gs, gbox, es4, CU_TENSOR_MAP_INTERLEAVE_NONE,
+           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return DGRAD_ERR_CUDA;
     return DGRAD_OK;
 }
 
@@ -224,7 +372,8 @@ void fill_wgrad_params(wgrad_plan_s *pl) {
     m.seg_rows = g.seg_rows; m.spt = g.spt; m.n_segs = g.n_segs; m.cpi = g.cpi;
     m.total_chunks = g.total_chunks; m.cps = g.cps; m.stages = g.stages; m.tmem_cols = g.tmem_cols;
     m.idesc = dgrad::tf32_idesc(128, g.bn);
-    m.split = g.split; m.N = g.N; m.n_copies = g.n_copies;
+    m.split = g.split; m.Q = g.Q; m.n_copies = g.n_copies;
+    m.blocked = g.blocked; m.Px = g.Lx / 32;
     m.timeout_ns = dgrad::kWgTimeoutNs;
     for (int sidx = 0; sidx < g.n_segs; ++sidx) {
         const int t = sidx / g.cpt;
@@ -233,8 +382,11 @@ void fill_wgrad_params(wgrad_plan_s *pl) {
     dgrad::WgradPackParams &q = pl->pp;
     q.gf = pl->gf; q.xc = pl->xc;
     q.N = g.N; q.Ci = g.Ci; q.H = g.H; q.W = g.W; q.Co = g.Co; q.oH = g.oH; q.oW = g.oW;
-    q.s = g.s; q.pw = g.pw; q.Wf = g.Wf; q.Kimg = g.Kimg; q.Lx = g.Lx; q.Ty = g.Ty; q.n_rh = g.n_rh;
-    for (int i = 0; i < dgrad::kWgMaxRowPhases; ++i) q.rh_list[i] = g.rh_list[i];
+    q.s = g.s; q.Wf = g.Wf; q.Kimg = g.Kimg; q.Lx = g.Lx; q.Ty = g.Ty; q.Tu = g.Tu;
+    q.Q = g.Q; q.lf = g.lf; q.blocked = g.blocked; q.Px = g.Lx / 32; q.Pg = g.cpi;
+    q.g_tiles = (long long)g.Q * g.Co * ((g.cpi + dgrad::kWgPackTile - 1) / dgrad::kWgPackTile);
+    q.x_tiles = (long long)g.n_copies * g.Q * g.Ci * ((g.Lx / 32 + dgrad::kWgPackTile - 1) / dgrad::kWgPackTile);
+    for (int c = 0; c < g.n_copies; ++c) q.copy[c] = make_int4(g.copy_rh[c], g.copy_rw[c], g.copy_r[c], 0);
     q.split = g.split;
     q.g4 = (long long)(g.g_elems / 4 / (g.split ? 2 : 1));
     q.x4 = (long long)(g.x_elems / 4 / (g.split ? 2 : 1));
@@ -243,6 +395,28 @@ void fill_wgrad_params(wgrad_plan_s *pl) {
     r.Co = g.Co; r.Ci = g.Ci; r.taps = g.taps; r.bn = g.bn; r.n_mt = g.n_mt; r.n_nt = g.n_nt; r.n_ks = g.n_ks;
     r.seg_rows = g.seg_rows; r.cpt = g.cpt; r.spt = g.spt; r.n_segs = g.n_segs;
     r.total = (long long)g.n_mt * g.n_nt * g.bn * 128;
+    r.win = g.win;
+    if (g.win) {
+        r.n_tiles = g.n_tiles;
+        r.total = (long long)g.cpt * g.n_nt * g.n_tiles * g.bn * 128;
+        for (int t = 0; t < g.n_tiles; ++t) r.tile[t] = make_int2(g.tile_grp[t], g.tile_m0[t]);
+        for (int gi = 0; gi < g.n_groups; ++gi) r.grp[gi] = make_int2(g.grp_tap0[gi], g.grp_nt[gi]);
+        for (int t = 0; t < g.taps; ++t) r.taps_of[t] = g.grp_taps[t];
+        dgrad::WgradWinParams &w = pl->wp;
+        w.part = pl->part;
+        w.err = pl->err;
+        w.n_units = g.n_units; w.n_sets = g.n_sets; w.tpu = g.tpu; w.n_tiles = g.n_tiles;
+        w.cpt = g.cpt; w.n_nt = g.n_nt; w.nksq = g.nksq; w.cps = g.cps;
+        w.Pg = g.cpi; w.Px = g.Lx / 32; w.seg_rows = g.seg_rows; w.L = g.run_len; w.bn = g.bn;
+        w.stages = g.stages; w.acc_sets = g.acc_sets; w.tmem_cols = g.tmem_cols;
+        w.xbox_bytes = g.xbox_bytes; w.bbox_bytes = g.bbox_bytes;
+        w.idesc = dgrad::tf32_idesc(128, g.bn);
+        w.timeout_ns = dgrad::kWgTimeoutNs;
+        for (int t = 0; t < g.n_tiles; ++t) {
+            const int gi = g.tile_grp[t];
+            w.tile[t] = make_int2(g.grp_copy[gi], g.grp_base[gi] + g.tile_m0[t]);
+        }
+    }
 }
 
 }  // namespace
@@ -261,9 +435,10 @@ dgrad_status_t wgrad_describe(int N, int Ci, int H, int W, int Co, int kH, int k
 }
 
 dgrad_status_t wgrad_describe_taps(int N, int Ci, int H, int W, int Co, int kH, int kW, int stride, int pad_h,
-                                   int pad_w, int cap, int *copy, int *offset, int *copy_kw, int *copy_rh,
-                                   int *n_copies, int *ty) {
-    if (!copy || !offset || !copy_kw || !copy_rh || !n_copies || !ty) return DGRAD_ERR_INVALID_ARG;
+                                   int pad_w, int cap, int *copy, int *offset, int *copy_rh, int *copy_rw,
+                                   int *copy_shift, int *n_copies, int *ty, int *tu, int *interleave) {
+    if (!copy || !offset || !copy_rh || !copy_rw || !copy_shift || !n_copies || !ty || !tu || !interleave)
+        return DGRAD_ERR_INVALID_ARG;
     WgradGeometry g;
     dgrad_status_t st =
         dgrad::make_wgrad_geometry(N, Ci, H, W, Co, kH, kW, stride, pad_h, pad_w, DGRAD_PREC_TF32, 0, &g);
@@ -274,11 +449,39 @@ dgrad_status_t wgrad_describe_taps(int N, int Ci, int H, int W, int Co, int kH, 
         offset[t] = g.tap_off[t];
     }
     for (int c = 0; c < g.n_copies; ++c) {
-        copy_kw[c] = c / g.n_rh;
-        copy_rh[c] = g.rh_list[c % g.n_rh];
+        copy_rh[c] = g.copy_rh[c];
+        copy_rw[c] = g.copy_rw[c];
+        copy_shift[c] = g.copy_r[c];
     }
     *n_copies = g.n_copies;
     *ty = g.Ty;
+    *tu = g.Tu;
+    *interleave = g.f;
+    return DGRAD_OK;
+}
+
+dgrad_status_t wgrad_describe_window(int N, int Ci, int H, int W, int Co, int kH, int kW, int stride, int pad_h,
+                                     int pad_w, int sm_count, int cap, int *hdr, int *groups, int *taps, int *tiles) {
+    if (!hdr || !groups || !taps || !tiles) return DGRAD_ERR_INVALID_ARG;
+    WgradGeometry g;
+    dgrad_status_t st =
+        dgrad::make_wgrad_geometry(N, Ci, H, W, Co, kH, kW, stride, pad_h, pad_w, DGRAD_PREC_TF32, sm_count, &g);
+    if (st != DGRAD_OK) return st;
+    if (!g.win) return DGRAD_ERR_UNSUPPORTED;
+    if (g.taps > cap || g.n_groups > cap || g.n_tiles > cap) return DGRAD_ERR_INVALID_ARG;
+    const int h[15] = {g.n_groups, g.n_tiles, g.spt, g.seg_rows, g.stages, g.cpi, g.Lx / 32, g.cps,
+                       g.nksq, g.cpt, g.n_nt, g.Q, g.run_len, g.tpu, g.n_sets};
+    for (int i = 0; i < 15; ++i) hdr[i] = h[i];
+    for (int gi = 0; gi < g.n_groups; ++gi) {
+        int *e = groups + 6 * gi;
+        e[0] = g.grp_copy[gi]; e[1] = g.grp_base[gi]; e[2] = g.grp_nt[gi];
+        e[3] = g.grp_nmt[gi]; e[4] = 0; e[5] = g.grp_tap0[gi];
+    }
+    for (int t = 0; t < g.taps; ++t) taps[t] = g.grp_taps[t];
+    for (int t = 0; t < g.n_tiles; ++t) {
+        tiles[2 * t] = g.tile_grp[t];
+        tiles[2 * t + 1] = g.tile_m0[t];
+    }
     return DGRAD_OK;
 }
 
@@ -327,6 +530,8 @@ dgrad_status_t wgrad_plan(int N, int Ci, int H, int W, int Co, int kH, int kW, i
         delete pl;
         return st;
     }
+    pl->wp.x_map = pl->mp.x_map;
+    pl->wp.g_map = pl->mp.g_map;
     *plan_out = pl;
     return DGRAD_OK;
 }
@@ -354,7 +559,8 @@ dgrad_status_t wgrad_run(wgrad_plan_t plan, const float *grad_out, const float *
     plan->rp.dw = grad_weight;
     dgrad_status_t st = wcuda(dgrad::launch_wgrad_pack(plan->pp, s));
     if (st != DGRAD_OK) return st;
-    st = wcuda(dgrad::launch_wgrad_main(plan->mp, g.grid, g.smem_bytes, s));
+    st = wcuda(g.win ? dgrad::launch_wgrad_window(plan->wp, g.grid, g.smem_bytes, s)
+                     : dgrad::launch_wgrad_main(plan->mp, g.grid, g.smem_bytes, s));
     if (st != DGRAD_OK) return st;
     return wcuda(dgrad::launch_wgrad_reduce(plan->rp, s));
 }

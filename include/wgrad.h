@@ -58,10 +58,14 @@ typedef struct {
     int N, Ci, H, W, Co, kH, kW, stride, pad_h, pad_w;
     int oH, oW;
     int precision;          /* dgrad_precision_t */
-    int Wf;                 /* row pitch of the position frames: oW rounded up to a multiple of 4 */
-    int Kimg;               /* GEMM K per image: oH*Wf rounded up to a multiple of 32 */
+    int interleave;         /* f: images interleaved along K (32: batch-blocked frames; else 4, or 2, 1 for batches below 4) */
+    int mode;               /* main kernel: 0 segment (a tensor copy per tap segment and chunk), 1 run (a tensor copy
+                               per tile of adjacent taps holds a run of positions for several chunks; batch-blocked
+                               TF32 only) */
+    int Wf;                 /* row pitch of the position frames (grad_out columns plus the taps' column reach) */
+    int Kimg;               /* GEMM K per group of f images: oH*Wf*f rounded up to a multiple of 32 */
     int Lx;                 /* length of one input-copy plane (Kimg plus the largest tap offset) */
-    int n_copies;           /* shifted, phase-split copies of the input (one per kw and row phase) */
+    int n_copies;           /* phase-split, shifted copies of the input (one per row and column phase when f = 4) */
     int seg_rows;           /* GEMM rows per (tap, input-channel block) segment */
     int n_mt, n_nt, n_ks;   /* row tiles of (tap, ci), column tiles of co, splits of K */
     int slice_n;            /* output channels per column tile (MMA N) */
@@ -76,14 +80,29 @@ typedef struct {
 dgrad_status_t wgrad_describe(int N, int Ci, int H, int W, int Co, int kH, int kW, int stride, int pad_h,
                               int pad_w, dgrad_precision_t precision, int sm_count, wgrad_plan_info_t *info);
 
-/* Host-only tap table (for tests): for tap t = kh*kW + kw, the input copy it
- * reads (copy[t]) and its K offset in positions (offset[t]); for input copy
- * c, its kernel column (copy_kw[c]) and row phase (copy_rh[c]); and the
- * copies' leading zero rows (*ty).  Arrays hold at least `cap` entries;
+/* Host-only tap table (for tests).  Frames interleave f = *interleave
+ * images along K: position (row y, column u) of image n = f*q + j sits at K
+ * index (y*Wf + u)*f + j of image group q.  For tap t = kh*kW + kw: the input
+ * copy it reads (copy[t]) and its K offset (offset[t], a multiple of 4).
+ * Input copy c holds input row s*(y - *ty) + copy_rh[c] and column
+ * s*(u - *tu + copy_shift[c]) + copy_rw[c] at frame position (y, u) (0
+ * outside the input).  Arrays hold at least `cap` entries;
  * DGRAD_ERR_INVALID_ARG if kH*kW or the copy count exceeds cap. */
 dgrad_status_t wgrad_describe_taps(int N, int Ci, int H, int W, int Co, int kH, int kW, int stride, int pad_h,
-                                   int pad_w, int cap, int *copy, int *offset, int *copy_kw, int *copy_rh,
-                                   int *n_copies, int *ty);
+                                   int pad_w, int cap, int *copy, int *offset, int *copy_rh, int *copy_rw,
+                                   int *copy_shift, int *n_copies, int *ty, int *tu, int *interleave);
+
+/* Host-only run-mode table (for tests); DGRAD_ERR_UNSUPPORTED when the shape
+ * runs the segment mode.  hdr[15] = {groups, tiles, taps per tile (spt),
+ * rows per position block, stages, positions per image group of grad_out
+ * (Pg) and of the input copies (Px), chunks per unit, K splits per image
+ * group, ci blocks, co tiles, image groups, chunks per stage (L), tiles per
+ * unit, tile sets}; per group 6 ints {input copy, base position, taps,
+ * tiles, 0, first entry in taps[]}; taps[] lists the taps group by group in
+ * position order; per tile 2 ints {group, first tap in the group}.  Each
+ * array holds at least `cap` entries of its kind. */
+dgrad_status_t wgrad_describe_window(int N, int Ci, int H, int W, int Co, int kH, int kW, int stride, int pad_h,
+                                     int pad_w, int sm_count, int cap, int *hdr, int *groups, int *taps, int *tiles);
 
 /* Create a plan on the current device: validate, plan the tiles and allocate
  * the workspace (position frames of grad_out and input, the partial-sum

@@ -333,48 +333,69 @@ WG_SHAPES = [
     (1, 65, 33, 17, 19, 4, 3, 2, 1, 2),
     (1, 3, 4, 2, 2, 3, 3, 2, 1, 1),
     (2, 4, 300, 9, 7, 3, 3, 1, 1, 1),
+    (5, 3, 4, 9, 11, 3, 3, 1, 1, 1),       # four images interleaved, a ragged last group
+    (4, 6, 8, 12, 10, 3, 3, 2, 1, 1),
+    (7, 2, 3, 10, 13, 7, 7, 2, 3, 3),
+    (6, 4, 5, 11, 9, 5, 3, 3, 2, 1),
+    (3, 3, 2, 8, 9, 3, 4, 1, 1, 2),
+    (32, 3, 4, 7, 9, 3, 3, 1, 1, 1),       # batch-blocked frames (32 images per K chunk)
+    (35, 5, 3, 8, 6, 3, 3, 2, 1, 1),       # 35 images: four interleaved (blocking would pad 29)
+    (60, 5, 3, 8, 6, 3, 3, 2, 1, 1),       # blocked, four padding images
+    (33, 2, 2, 5, 7, 5, 3, 3, 2, 1),
 ]
 
 
 def emulate_wgrad(go, x, kH, kW, s, ph, pw):
     """The wgrad kernels' arithmetic in numpy, driven by the library's tables:
-    grad_out and input position frames, one GEMM row per (tap, input channel)
-    reading its input copy at the tap's K offset, row tiles and the reduction's
-    index map back to OIHW."""
+    grad_out and input position frames with f images interleaved along K, one
+    GEMM row per (tap, input channel) reading its input copy at the tap's K
+    offset, row tiles and the reduction's index map back to OIHW."""
     N, Co, oH, oW = go.shape
     _, Ci, H, W = x.shape
     info = dg.wgrad_describe(N, Ci, H, W, Co, kH, kW, s, ph, pw)
     tab = dg.wgrad_describe_taps(N, Ci, H, W, Co, kH, kW, s, ph, pw)
-    Wf, Kimg, Lx, Ty = info["Wf"], info["Kimg"], info["Lx"], tab["Ty"]
-    assert Wf % 4 == 0 and Kimg % 32 == 0 and Lx % 4 == 0 and Kimg >= oH * Wf
-    gf = np.zeros((N, Co, Kimg))
-    for oh in range(oH):
-        gf[:, :, oh * Wf:oh * Wf + oW] = go[:, :, oh, :]
+    f, Wf, Kimg, Lx, Ty, Tu = tab["interleave"], info["Wf"], info["Kimg"], info["Lx"], tab["Ty"], tab["Tu"]
+    assert f == info["interleave"] and f in (1, 2, 4, 32) and Wf % max(1, 4 // f) == 0
+    assert f != 32 or all(sh == 0 for sh in tab["copy_shift"])
+    assert Kimg % 32 == 0 and Lx % 4 == 0 and Kimg >= oH * Wf * f and Wf >= oW
+    Q = -(-N // f)
+    k = np.arange(Kimg)
+    j, pos = k % f, k // f
+    oh, ow = pos // Wf, pos % Wf
+    gf = np.zeros((Q, Co, Kimg))
+    for q in range(Q):
+        n = q * f + j
+        ok = (n < N) & (oh < oH) & (ow < oW)
+        gf[q][:, ok] = go[n[ok], :, oh[ok], ow[ok]].T
     nc = info["n_copies"]
-    xc = np.zeros((nc, N, Ci, Lx))
+    xc = np.zeros((nc, Q, Ci, Lx))
+    kx = np.arange(Lx)
+    jx, px = kx % f, kx // f
+    y, u = px // Wf, px % Wf
     for c in range(nc):
-        kw, rh = tab["copy_kw"][c], tab["copy_rh"][c]
-        for k in range(Lx):
-            y, u = divmod(k, Wf)
-            ih, iw = s * (y - Ty) + rh, s * u + kw - pw
-            if u < oW and 0 <= ih < H and 0 <= iw < W:
-                xc[c, :, :, k] = x[:, :, ih, iw]
+        ih = s * (y - Ty) + tab["copy_rh"][c]
+        iw = s * (u - Tu + tab["copy_shift"][c]) + tab["copy_rw"][c]
+        for q in range(Q):
+            n = q * f + jx
+            ok = (n < N) & (ih >= 0) & (ih < H) & (iw >= 0) & (iw < W)
+            xc[c, q][:, ok] = x[n[ok], :, ih[ok], iw[ok]].T
     dw = np.full((Co, Ci, kH * kW), np.nan)
     seg_rows = info["seg_rows"]
     cpt = -(-Ci // seg_rows)
     spt = 128 // seg_rows
     n_segs = kH * kW * cpt
-    assert info["n_mt"] == -(-n_segs // spt)
+    segment = info["mode"] == 0   # the window mode's rows are checked by test_wgrad_window_schedule
+    assert not segment or info["n_mt"] == -(-n_segs // spt)
     for t in range(kH * kW):
         off = tab["offset"][t]
-        assert off % 4 == 0 and Kimg + off <= Lx      # every 32-position window stays in the copy's plane
-        rows = xc[tab["copy"][t], :, :, off:off + Kimg]   # [N, Ci, Kimg]
-        prod = np.einsum("nck,nik->ci", gf, rows)
+        assert off % 4 == 0 and Kimg + off <= Lx      # 16-byte aligned, inside the copy's plane
+        rows = xc[tab["copy"][t], :, :, off:off + Kimg]   # [Q, Ci, Kimg]
+        prod = np.einsum("qck,qik->ci", gf, rows)
         for ci in range(Ci):
             seg = t * cpt + ci // seg_rows
             mt, row = divmod(seg, spt)
             row = row * seg_rows + ci % seg_rows
-            assert mt < info["n_mt"] and row < 128
+            assert not segment or (mt < info["n_mt"] and row < 128)
             assert np.isnan(dw[0, ci, t])                  # each (tap, ci) row is produced once
             dw[:, ci, t] = prod[:, ci]
     assert not np.isnan(dw).any()
@@ -393,13 +414,96 @@ def test_emulated_wgrad_matches_oracle(shape):
     assert np.abs(emu - ref).max() <= 1e-12 * max(1.0, mag.max())
 
 
+WIN_SHAPES = [
+    # N, Ci, Co, H, W, kH, kW, s, ph, pw: batch-blocked TF32 shapes that run the window mode
+    (32, 64, 64, 56, 56, 3, 3, 1, 1, 1),   # the resnet_stage shape
+    (32, 3, 4, 7, 9, 3, 3, 1, 1, 1),
+    (60, 5, 3, 8, 6, 3, 3, 2, 1, 1),
+    (64, 40, 20, 6, 5, 3, 3, 1, 1, 1),     # two image groups
+    (32, 16, 40, 9, 11, 5, 3, 1, 2, 1),
+]
+
+
+@pytest.mark.parametrize("shape", WIN_SHAPES)
+def test_wgrad_run_schedule(shape):
+    """Run mode on the CPU: the tap groups against the tap table; each tile's
+    tensor copy (L + spt - 1 position blocks from the stage's first chunk on)
+    holding, for every chunk of the stage, the spt positions its taps read;
+    the copies within the 256-row box limit and shared memory; the units
+    covering every (tile, chunk) once; and the reduction's map back to
+    (tap, ci) covering each weight row exactly once."""
+    N, Ci, Co, H, W, kH, kW, s, ph, pw = shape
+    args = (N, Ci, H, W, Co, kH, kW, s, ph, pw)
+    info = dg.wgrad_describe(*args, sm_count=152)
+    d = dg.wgrad_describe_window(*args, sm_count=152)
+    tab = dg.wgrad_describe_taps(*args)
+    assert info["mode"] == 1 and d is not None and info["interleave"] == 32
+    spt, sr, L, tpu, bn = d["spt"], d["seg_rows"], d["L"], d["tpu"], info["slice_n"]
+    assert spt * sr == 128 and sr >= min(Ci, 128) and info["stages"] >= 2
+    assert (L + spt - 1) * sr <= 256 and L * bn <= 256           # tensor-copy boxes of at most 256 rows
+    stage = tpu * (L + spt - 1) * sr * 128 + L * bn * 128
+    assert info["smem_bytes"] >= info["stages"] * stage and info["smem_bytes"] <= 232448
+    assert tpu * bn <= 512 and info["tmem_cols"] <= 512
+    seen = []
+    for g in d["groups"]:
+        for j in range(g["n_taps"]):
+            t = d["taps"][g["tap0"] + j]
+            assert tab["copy"][t] == g["copy"] and tab["offset"][t] == 32 * (g["base"] + j)
+            seen.append(t)
+        assert g["n_mt"] == -(-g["n_taps"] // spt)
+    assert sorted(seen) == list(range(kH * kW))
+    assert d["tiles"] == [(gi, m * spt) for gi, g in enumerate(d["groups"]) for m in range(g["n_mt"])]
+    assert d["n_sets"] == -(-d["n_tiles"] // tpu)
+    Pg, cps = d["Pg"], d["cps"]
+    assert cps % L == 0 and d["nksq"] == -(-Pg // cps)
+    assert info["n_units"] == d["Q"] * d["nksq"] * d["cpt"] * d["n_nt"] * d["n_sets"]
+    # a tile's copy for the stage starting at chunk c holds positions c + base + m0 + [0, L + spt - 1); chunk
+    # c + i reads blocks i .. i + spt - 1 of it, i.e. positions c + i + base + m0 + j for its taps j < spt
+    covered = set()
+    for ks in range(d["nksq"]):
+        c0, c1 = ks * cps, min(ks * cps + cps, Pg)
+        for c in range(c0, c1, L):
+            for t, (gi, m0) in enumerate(d["tiles"]):
+                g = d["groups"][gi]
+                copy_pos = [c + g["base"] + m0 + b for b in range(L + spt - 1)]
+                for i in range(min(L, c1 - c)):
+                    rows = copy_pos[i:i + spt]
+                    assert rows == [(c + i) + g["base"] + m0 + j for j in range(spt)]
+                    for j in range(spt):
+                        if m0 + j < g["n_taps"]:
+                            assert rows[j] <= d["Px"] - 1    # a real tap never reads past its image group
+                    covered.add((t, c + i))
+    assert covered == {(t, c) for t in range(d["n_tiles"]) for c in range(Pg)}
+    # the reduction's (tile, row) -> (tap, ci) map: every weight row exactly once
+    rows = []
+    for cb in range(d["cpt"]):
+        for gi, m0 in d["tiles"]:
+            g = d["groups"][gi]
+            for r in range(128):
+                j = m0 + r // sr
+                ci = cb * sr + r % sr
+                if j < g["n_taps"] and ci < Ci:
+                    rows.append((d["taps"][g["tap0"] + j], ci))
+    assert sorted(rows) == [(t, ci) for t in range(kH * kW) for ci in range(Ci)]
+
+
+def test_wgrad_window_mode_choice():
+    assert dg.wgrad_describe_window(2, 3, 8, 8, 4, 3, 3, 1, 1, 1) is None            # small batch: segment mode
+    assert dg.wgrad_describe(32, 64, 56, 56, 64, 3, 3, 1, 1, 1, "tf32x3")["mode"] == 0  # split precision
+    assert dg.wgrad_describe(32, 64, 56, 56, 64, 3, 3, 1, 1, 1)["mode"] == 1
+
+
 def test_wgrad_plans():
     for name in ORDER:
         wl = WORKLOADS[name]
         d = dg.wgrad_describe(*wl.plan_args(), sm_count=152)
         assert d["oH"] == wl.oH and d["oW"] == wl.oW
         assert d["smem_bytes"] <= 232448 and d["tmem_cols"] <= 512 and 16 <= d["slice_n"] <= 256
-        assert d["n_units"] == d["n_mt"] * d["n_nt"] * d["n_ks"] and d["grid"] <= 152
+        if d["mode"] == 0:    # units: row tiles x column tiles x K splits
+            assert d["n_units"] == d["n_mt"] * d["n_nt"] * d["n_ks"]
+        else:                 # units: tile sets x ci blocks x column tiles x K splits
+            assert d["n_units"] % (d["n_nt"] * d["n_ks"]) == 0
+        assert d["grid"] <= 152
         assert d["useful_flops"] == 2 * wl.N * wl.Co * wl.oH * wl.oW * wl.Ci * wl.kH * wl.kW
     for bad, status in (((0, 1, 4, 4, 1, 3, 3, 1, 1, 1), 1), ((1, 1, 2, 2, 1, 5, 5, 1, 0, 0), 1),
                         ((1, 1, 32, 32, 1, 3, 3, 5, 1, 1), 2)):
@@ -419,15 +523,18 @@ def test_wgrad_split_plans():
         a = dg.wgrad_describe(*wl.plan_args(), sm_count=152)
         b = dg.wgrad_describe(*wl.plan_args(), precision="tf32x3", sm_count=152)
         assert b["precision"] == "tf32x3" and a["precision"] == "tf32"
-        for k in ("n_mt", "n_nt", "slice_n", "seg_rows", "Kimg", "Lx", "n_copies", "useful_flops"):
+        assert b["mode"] == 0     # split precision runs the segment mode
+        same = ("n_mt", "n_nt", "slice_n", "seg_rows") if a["mode"] == 0 else ()
+        for k in same + ("Kimg", "Lx", "n_copies", "useful_flops"):
             assert a[k] == b[k], k
-        chunks = wl.N * b["Kimg"] // 32
-        assert b["n_ks"] >= a["n_ks"] and -(-chunks // b["n_ks"]) <= 12   # short accumulation chains
+        chunks = -(-wl.N // b["interleave"]) * b["Kimg"] // 32
+        assert -(-chunks // b["n_ks"]) <= 12   # short accumulation chains
         assert b["n_units"] == b["n_mt"] * b["n_nt"] * b["n_ks"]
         stage = 2 * (128 * 128 + b["slice_n"] * 128)
         assert b["stages"] >= 2 and b["smem_bytes"] >= b["stages"] * stage and b["smem_bytes"] <= 232448
-        frames = 4 * (wl.N * wl.Co * a["Kimg"] + a["n_copies"] * wl.N * wl.Ci * a["Lx"])
-        assert b["workspace_bytes"] - a["workspace_bytes"] >= frames - 512   # regions are 256-byte aligned
+        Q = -(-wl.N // a["interleave"])
+        frames = 4 * (Q * wl.Co * a["Kimg"] + a["n_copies"] * Q * wl.Ci * a["Lx"])
+        assert b["workspace_bytes"] >= 2 * frames and a["workspace_bytes"] >= frames   # hi and lo halves
 
 
 def test_col2im_plans():

@@ -84,6 +84,20 @@ EDGE = [
     (1, 20, 40, 40, 40, 3, 3, 4, 1, 1),    # stride 4
     (2, 8, 300, 9, 7, 3, 3, 1, 1, 1),      # two column tiles
     (2, 200, 16, 6, 6, 3, 3, 1, 1, 1),     # input channels over one segment
+    (5, 3, 4, 9, 11, 3, 3, 1, 1, 1),       # four images interleaved along K, a ragged last group
+    (4, 6, 8, 12, 10, 3, 3, 2, 1, 1),
+    (7, 2, 3, 10, 13, 7, 7, 2, 3, 3),
+    (6, 4, 5, 11, 9, 5, 3, 3, 2, 1),
+    (9, 16, 24, 15, 17, 3, 3, 1, 1, 1),
+    (32, 3, 4, 7, 9, 3, 3, 1, 1, 1),       # batch-blocked frames (32 images per K chunk)
+    (35, 5, 3, 8, 6, 3, 3, 2, 1, 1),       # 35 images: four interleaved (blocking would pad 29)
+    (60, 5, 3, 8, 6, 3, 3, 2, 1, 1),       # blocked, four padding images
+    (33, 2, 2, 5, 7, 5, 3, 3, 2, 1),
+    (64, 70, 20, 6, 5, 3, 3, 1, 1, 1),     # blocked, two image groups (segment mode: windows do not fit)
+    (64, 40, 20, 6, 5, 3, 3, 1, 1, 1),     # window mode, two image groups
+    (32, 16, 40, 9, 11, 5, 3, 1, 2, 1),    # window mode, 5 x 3 taps
+    (32, 3, 8, 40, 44, 3, 3, 1, 1, 1),     # window mode, 16 slots per tile
+    (32, 130, 24, 9, 8, 3, 3, 1, 1, 1),    # two input-channel blocks
 ]
 
 
