@@ -634,18 +634,18 @@ __global__ void __launch_bounds__(256) wgrad_pack_kernel(const __grid_constant__
 __global__ void __launch_bounds__(256) wgrad_pack_blocked_kernel(const __grid_constant__ WgradPackParams p) {
     dev::grid_launch_dependents();   // as wgrad_pack_kernel
     __shared__ float tile[kWgPackTile][33];
-    const long long b = blockIdx.x;
+    const int b = static_cast<int>(blockIdx.x);   // the host keeps the block count below 2^31
     const bool is_g = b < p.g_tiles;
-    const long long bl = is_g ? b : b - p.g_tiles;
+    const int bl = is_g ? b : b - static_cast<int>(p.g_tiles);
     const int C = is_g ? p.Co : p.Ci;
     const int P = is_g ? p.Pg : p.Px;
     const int ntile = (P + kWgPackTile - 1) / kWgPackTile;
-    const int ch = static_cast<int>(bl % C);
-    long long rest = bl / C;
-    const int pt = static_cast<int>(rest % ntile);
+    const int ch = bl % C;
+    int rest = bl / C;
+    const int pt = rest % ntile;
     rest /= ntile;
-    const int q = static_cast<int>(rest % p.Q);
-    const int c = static_cast<int>(rest / p.Q);   // input copy (xc only)
+    const int q = rest % p.Q;
+    const int c = rest / p.Q;   // input copy (xc only)
     const int p0 = pt * kWgPackTile;
     // gather: thread t reads position p0 + (t & 63) of images (t >> 6) + 4e
     {
@@ -666,35 +666,43 @@ __global__ void __launch_bounds__(256) wgrad_pack_blocked_kernel(const __grid_co
             img_stride = static_cast<size_t>(p.Ci) * p.H * p.W;
         }
         const bool ok = pos < P && ih >= 0 && ih < hh && iw >= 0 && iw < ww;
-        const float *src = base + (ok ? static_cast<size_t>(ih) * ww + iw : 0);
+        const int jt = threadIdx.x >> 6;
+        const int n_ok = p.N - q * 32;   // images of this group that exist
+        const float *src = base + (ok ? static_cast<size_t>(ih) * ww + iw : 0) + static_cast<size_t>(q * 32 + jt) * img_stride;
+        const size_t step = 4 * img_stride;
+        float v[8];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            const int j = (threadIdx.x >> 6) + 4 * e;
-            const int n = q * 32 + j;
-            tile[pp][j] = (ok && n < p.N) ? __ldg(src + static_cast<size_t>(n) * img_stride) : 0.f;
-        }
+        for (int e = 0; e < 8; ++e) v[e] = (ok && jt + 4 * e < n_ok) ? __ldg(src + e * step) : 0.f;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) tile[pp][jt + 4 * e] = v[e];
     }
     __syncthreads();
-    // write: thread t writes image t & 31 of positions p0 + (t >> 5) + 8e
-    const int j = threadIdx.x & 31;
+    // write: thread t writes images 4*(t & 7) .. +3 of positions p0 + (t >> 3) + 32e (one 16-byte store each;
+    // eight threads write one position's 128-byte row)
+    const int j4 = (threadIdx.x & 7) * 4;
     float *dst;
     size_t half;
     if (is_g) {
-        dst = p.gf + (static_cast<size_t>(q) * p.Pg * C + ch) * 32 + j;
+        dst = p.gf + (static_cast<size_t>(q) * p.Pg * C + ch) * 32 + j4;
         half = static_cast<size_t>(p.g4) * 4;
     } else {
-        dst = p.xc + ((static_cast<size_t>(c) * p.Q + q) * p.Px * C + ch) * 32 + j;
+        dst = p.xc + ((static_cast<size_t>(c) * p.Q + q) * p.Px * C + ch) * 32 + j4;
         half = static_cast<size_t>(p.x4) * 4;
     }
+    const size_t row = static_cast<size_t>(C) * 32;   // floats between consecutive positions
 #pragma unroll
-    for (int e = 0; e < 8; ++e) {
-        const int pp = (threadIdx.x >> 5) + 8 * e;
+    for (int e = 0; e < kWgPackTile / 32; ++e) {
+        const int pp = (threadIdx.x >> 3) + 32 * e;
         if (p0 + pp >= P) break;
-        const float v = tile[pp][j];
-        const float hi = dev::round_tf32(v);
-        float *d = dst + static_cast<size_t>(p0 + pp) * C * 32;
-        *d = hi;
-        if (p.split) d[half] = dev::round_tf32(v - hi);
+        const float4 v = make_float4(tile[pp][j4], tile[pp][j4 + 1], tile[pp][j4 + 2], tile[pp][j4 + 3]);
+        const float4 hi = make_float4(dev::round_tf32(v.x), dev::round_tf32(v.y), dev::round_tf32(v.z),
+                                      dev::round_tf32(v.w));
+        float *d = dst + static_cast<size_t>(p0 + pp) * row;
+        *reinterpret_cast<float4 *>(d) = hi;
+        if (p.split)
+            *reinterpret_cast<float4 *>(d + half) =
+                make_float4(dev::round_tf32(v.x - hi.x), dev::round_tf32(v.y - hi.y), dev::round_tf32(v.z - hi.z),
+                            dev::round_tf32(v.w - hi.w));
     }
 }
 
