@@ -396,6 +396,8 @@ void fill_wgrad_params(wgrad_plan_s *pl) {
     r.seg_rows = g.seg_rows; r.cpt = g.cpt; r.spt = g.spt; r.n_segs = g.n_segs;
     r.total = (long long)g.n_mt * g.n_nt * g.bn * 128;
     r.win = g.win;
+    r.red_warps = 1;
+    while (r.red_warps < 8 && r.red_warps * 8 < g.n_ks) r.red_warps *= 2;
     if (g.win) {
         r.n_tiles = g.n_tiles;
         r.total = (long long)g.cpt * g.n_nt * g.n_tiles * g.bn * 128;

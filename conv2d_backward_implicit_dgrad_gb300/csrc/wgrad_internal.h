@@ -99,6 +99,7 @@ struct WgradReduceParams {
     long long total;   // partial elements per split (segment mode n_mt * n_nt * bn * 128)
     // window mode: partial tile t of a unit is M-tile tile[t].y of group tile[t].x
     int win, n_tiles;
+    int red_warps;   // warps summing the K splits of one group of 128 elements: 1, 2, 4 or 8
     int2 tile[kWgMaxTiles];
     int2 grp[kWgMaxGroups];   // x: first entry in taps, y: taps in the group
     int taps_of[kMaxTaps];

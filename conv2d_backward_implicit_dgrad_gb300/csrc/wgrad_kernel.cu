@@ -18,6 +18,8 @@
 // epilogue overlaps the next unit's MMAs).  Every wait is bounded.
 #include <cuda_runtime.h>
 
+#include <type_traits>
+
 #include "ptx.cuh"
 #include "wgrad_internal.h"
 
@@ -706,41 +708,21 @@ __global__ void __launch_bounds__(256) wgrad_pack_blocked_kernel(const __grid_co
     }
 }
 
-// grad_weight from the partial tiles.  Block b takes the 32 consecutive
-// partial elements 32b .. 32b + 31 (tile, column, rows); warp w of its eight
-// sums the K splits w, w + 8, w + 16, ... of one element per lane (coalesced
-// 128-byte reads), and warp 0 adds the eight warp sums in a fixed order and
-// writes the OIHW element each element stands for.
-__global__ void __launch_bounds__(256) wgrad_reduce_kernel(const __grid_constant__ WgradReduceParams p) {
-    __shared__ float wsum[8][32];
-    dev::grid_dependency_wait();   // the partial tiles come from the main kernel
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const long long i = static_cast<long long>(blockIdx.x) * 32 + lane;
-    const size_t split_stride = static_cast<size_t>(p.total);   // one K split of every tile
-    float acc = 0.f;
-    if (i < p.total) {
-        const float *src = p.part + static_cast<size_t>(i);
-        float a0 = 0.f, a1 = 0.f;
-        int ks = warp;
-        for (; ks + 8 < p.n_ks; ks += 16) {   // two independent chains
-            a0 += __ldg(src + static_cast<size_t>(ks) * split_stride);
-            a1 += __ldg(src + static_cast<size_t>(ks + 8) * split_stride);
-        }
-        if (ks < p.n_ks) a0 += __ldg(src + static_cast<size_t>(ks) * split_stride);
-        acc = a0 + a1;
-    }
-    wsum[warp][lane] = acc;
-    __syncthreads();
-    if (warp != 0 || i >= p.total) return;
-    const float sum = ((wsum[0][lane] + wsum[1][lane]) + (wsum[2][lane] + wsum[3][lane])) +
-                      ((wsum[4][lane] + wsum[5][lane]) + (wsum[6][lane] + wsum[7][lane]));
+// grad_weight from the partial tiles.  A thread takes four consecutive
+// partial elements (rows of one column: one 16-byte load per split); the
+// eight warps of a block form 8 / W groups of W warps, warp w of a group
+// summing K splits w, w + W, ... of the group's 128 elements (W = the power of
+// two that leaves each warp at most about eight splits), and the group's
+// first warp adds the W sums in a fixed order and writes each element's OIHW
+// position.  Deterministic for a given plan.
+__device__ __forceinline__ void wgrad_reduce_store(const WgradReduceParams &p, long long i, float sum) {
     const int row = static_cast<int>(i & 127);
     long long rest = i >> 7;
     const int col = static_cast<int>(rest % p.bn);
     rest /= p.bn;
     const int sl = row / p.seg_rows;
     int t, ci, nt;
-    if (p.win) {   // element (cb, nt, tile, col, row); tile = M-tile of a tap group
+    if (p.win) {   // element (cb, nt, tile, col, row); tile = taps of one group at adjacent positions
         const int tile = static_cast<int>(rest % p.n_tiles);
         rest /= p.n_tiles;
         nt = static_cast<int>(rest % p.n_nt);
@@ -762,6 +744,57 @@ __global__ void __launch_bounds__(256) wgrad_reduce_kernel(const __grid_constant
     const int co = nt * p.bn + col;
     if (ci >= p.Ci || co >= p.Co) return;
     p.dw[(static_cast<size_t>(co) * p.Ci + ci) * p.taps + t] = sum;
+}
+
+template <int kV>   // partial elements per thread: 4 (16-byte loads) or 1 (more threads for deep split counts)
+__global__ void __launch_bounds__(256) wgrad_reduce_kernel(const __grid_constant__ WgradReduceParams p) {
+    using Vec = typename std::conditional<kV == 4, float4, float>::type;
+    __shared__ Vec wsum[8][32];
+    dev::grid_dependency_wait();   // the partial tiles come from the main kernel
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int W = p.red_warps;                 // warps per element group (1, 2, 4 or 8)
+    const int grp = warp / W, wi = warp - grp * W;
+    const long long e0 = (static_cast<long long>(blockIdx.x) * (8 / W) + grp) * (32 * kV) + lane * kV;
+    const size_t st = static_cast<size_t>(p.total) / kV;   // one K split of every tile, in Vec units
+    float a[4][kV];   // four independent chains: splits wi + W*(4i + c) go to chain c
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+#pragma unroll
+        for (int k = 0; k < kV; ++k) a[c][k] = 0.f;
+    if (e0 < p.total) {
+        const Vec *src = reinterpret_cast<const Vec *>(p.part + static_cast<size_t>(e0));
+        for (int ks = wi; ks < p.n_ks; ks += 4 * W) {
+            Vec u[4];
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+                if (ks + c * W < p.n_ks) u[c] = __ldg(src + static_cast<size_t>(ks + c * W) * st);
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                if (ks + c * W >= p.n_ks) break;
+                const float *uf = reinterpret_cast<const float *>(&u[c]);
+#pragma unroll
+                for (int k = 0; k < kV; ++k) a[c][k] += uf[k];
+            }
+        }
+    }
+    Vec mine;
+    float *mf = reinterpret_cast<float *>(&mine);
+#pragma unroll
+    for (int k = 0; k < kV; ++k) mf[k] = (a[0][k] + a[1][k]) + (a[2][k] + a[3][k]);
+    wsum[warp][lane] = mine;
+    __syncthreads();
+    if (wi != 0 || e0 >= p.total) return;
+    float sum[kV];
+#pragma unroll
+    for (int k = 0; k < kV; ++k) sum[k] = mf[k];
+    for (int j = 1; j < W; ++j) {   // fixed order
+        const Vec v = wsum[warp + j][lane];
+        const float *vf = reinterpret_cast<const float *>(&v);
+#pragma unroll
+        for (int k = 0; k < kV; ++k) sum[k] += vf[k];
+    }
+#pragma unroll
+    for (int k = 0; k < kV; ++k) wgrad_reduce_store(p, e0 + k, sum[k]);
 }
 
 }  // namespace
@@ -813,9 +846,13 @@ cudaError_t launch_wgrad_window(const WgradWinParams &p, int grid, int smem_byte
 }
 
 cudaError_t launch_wgrad_reduce(const WgradReduceParams &p, cudaStream_t stream) {
-    const long long blocks = (p.total + 31) / 32;   // 32 partial elements per block
+    // 16-byte loads unless that leaves too few threads to keep the splits' loads in flight
+    const int v = (p.total / 4) * p.red_warps >= 150000 ? 4 : 1;
+    const long long per_block = 32LL * v * (8 / p.red_warps);   // partial elements per block
+    const long long blocks = (p.total + per_block - 1) / per_block;
     if (blocks < 1 || blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
-    return launch_pdl(wgrad_reduce_kernel, p, static_cast<int>(blocks), 256, 0, stream);
+    return v == 4 ? launch_pdl(wgrad_reduce_kernel<4>, p, static_cast<int>(blocks), 256, 0, stream)
+                  : launch_pdl(wgrad_reduce_kernel<1>, p, static_cast<int>(blocks), 256, 0, stream);
 }
 
 }  // namespace dgrad
