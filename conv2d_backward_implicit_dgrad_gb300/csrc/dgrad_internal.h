@@ -135,6 +135,8 @@ struct Tiling {
     int n_mgroups;
     int bg_first[kMaxTaps + 1];   // B stage i holds MMA groups [bg_first[i], bg_first[i+1])
     int xchg_bytes;    // shared memory for the epilogue's cross-warp row exchange
+    int xchg_unit;     // 1: one exchange per unit (a single phase: every column published before one barrier)
+    int epi_groups;    // epilogue warp groups taking alternate units (2 for grouped tensor-copy launches)
     int a_tma;         // 1: A stages are tensor copies of the packed frame; 0: producer warps gather
     int a_box_rows;    // rows of one A tensor copy (<= 256)
     int a_nbox;        // tensor copies per A stage
@@ -252,6 +254,8 @@ struct MainParams {
     int vec_w;          // epilogue stores the s column phases of a row phase together (s = 2 or 4)
     int n_mgroups;
     int xchg_bytes;
+    int xchg_unit;      // the epilogue publishes a unit's boundary rows once, for all columns
+    int epi_groups;     // 2: a second group of four epilogue warps takes every other unit
     PhaseDesc phase[kMaxPhases];
     TapDesc tap[kMaxTaps];
     // Fused epilogue: grad_input = (accumulate ? grad_input : 0) + m * dgrad,

@@ -238,7 +238,6 @@ constexpr int kMaxTcRows = 1024;   // frame rows one tcgen05 A stage may hold (1
 // the frame does not stay in L2 (7x7 stem, 114 MB frame: 145 us per call
 // against 212 us with producers).
 constexpr size_t kMaxFrameBytes = size_t(2) << 30;
-constexpr int kEpiGroups = 1;         // epilogue warp groups
 
 // Split the MMA groups of one channel chunk into B stages of at most `cap`
 // taps each, balanced; false when one MMA group alone exceeds `cap`.
@@ -293,7 +292,16 @@ bool size_tc(const Geometry &g, Tiling &t, int want_resident) {
     }
     if (t.grouped && (t.tm != 1 || max_sub > kMaxSub)) return false;
     t.tile_step = t.tm * kBlockM - (max_sub - 1);
-    t.xchg_bytes = max_sub > 1 ? kEpiGroups * 2 * 4 * (max_sub * (max_sub - 1) / 2) * 16 * 4 : 0;
+    // Cross-warp row exchange of grouped units: two buffers of 4 warps x slots
+    // rows of 16 columns, or, for a single phase, of the slice's bn columns
+    // (published once per unit).
+    t.xchg_unit = max_sub > 1 && g.n_phases == 1 ? 1 : 0;
+    // Grouped units' epilogues (sub-accumulators, combine) take about twice an
+    // ungrouped one: with two accumulator sets a second epilogue warp group
+    // takes every other unit (tensor-copy launches; 10 warps).
+    t.epi_groups = (t.grouped && t.a_tma && max_sub > 1 && 2 * t.tm * sub_cols <= kTmemCols) ? 2 : 1;
+    t.xchg_bytes = max_sub > 1 ? t.epi_groups * 2 * 4 * (max_sub * (max_sub - 1) / 2) * (t.xchg_unit ? t.bn : 16) * 4
+                               : 0;
     const int raw_rows = t.tm * kBlockM + g.max_shift;
     if (t.a_tma) {   // tensor copies of at most 256 rows each
         t.a_nbox = ceil_div(raw_rows, 256);
@@ -552,14 +560,19 @@ dgrad_status_t choose_tiling(const Geometry &g, int precision, const dgrad_optio
     if (t.a_tma && (long long)g.positions * t.co_v > INT_MAX) return DGRAD_ERR_UNSUPPORTED;
     if (!t.a_tma) t.frame_bytes = 0;
     // Grouping the taps of a kernel row into one MMA (N = taps x bn) cuts the
-    // shared-memory reads of A per FLOP when bn alone leaves the MMA bound by
-    // its operand reads (bn < 128), but triples the epilogue's tensor-memory
-    // reads and adds its row shifts; measured, the epilogue then bounds the
-    // kernel and the grouped plans ran slower, so grouping is opt-in.
-    // Taps of different phases with the same frame shift share one MMA
-    // whenever the phases can be ordered in tensor memory for it (stride-2
-    // shapes): fewer, wider MMAs, each phase still its own accumulator, so
-    // the epilogue is unchanged.  That is the automatic choice.
+    // MMA time when bn alone leaves the MMA bound by its fixed cost of
+    // reading A (a 128 x 64 x 8 TF32 MMA takes ~72 cycles, 128 x 192 x 8 ~106),
+    // but triples the epilogue's tensor-memory reads and adds its row
+    // shifts.  With the boundary rows exchanged once per unit and a second
+    // epilogue warp group (two accumulator sets), the grouped plan is the
+    // faster one for one-phase TF32 shapes with bn < 128 (resnet_stage main
+    // kernel 25.2 us vs 27.2): the automatic choice there, falling back to
+    // ungrouped when it does not fit.  Split precision keeps two 128-row
+    // blocks per unit ungrouped (61.9 us vs 64.1 grouped).  Taps of different phases with the
+    // same frame shift share one MMA whenever the phases can be ordered in
+    // tensor memory for it (stride-2 shapes): fewer, wider MMAs, each phase
+    // still its own accumulator, so the epilogue is unchanged.  That is the
+    // automatic choice for several phases.
     if (o.group_taps < 0 || o.group_taps > 3) return DGRAD_ERR_INVALID_ARG;
     if (o.b_stages != 0 && (o.b_stages < 2 || o.b_stages > 8)) return DGRAD_ERR_INVALID_ARG;
     t.want_b_stages = o.b_stages;
@@ -572,6 +585,9 @@ dgrad_status_t choose_tiling(const Geometry &g, int precision, const dgrad_optio
         group_pref[n_group][0] = 0, group_pref[n_group++][1] = 1;
     } else {
         if (o.group_taps == 0 && g.n_phases > 1) group_pref[n_group][0] = 0, group_pref[n_group++][1] = 1;
+        if (o.group_taps == 0 && g.n_phases == 1 && t.a_tma && !t.split && g.kW >= 2 && bn < 128 &&
+            o.tile_blocks <= 1)
+            group_pref[n_group][0] = 1, group_pref[n_group++][1] = 0;
         group_pref[n_group][0] = 0, group_pref[n_group++][1] = 0;
     }
     bool ok = false;
@@ -620,6 +636,8 @@ void fill_main_params(const Geometry &g, const Tiling &t, int round_tf32, MainPa
     m.tile_step = t.tile_step;
     m.grouped = t.grouped;
     m.xchg_bytes = t.xchg_bytes;
+    m.xchg_unit = t.xchg_unit;
+    m.epi_groups = t.epi_groups;
     MGroup mg[kMaxTaps];
     int perm[kMaxTaps], units[kMaxPhases];
     const int n_mg = t.path == DGRAD_PATH_TCGEN05 ? build_mgroups(g, t, mg, perm, units) : 0;

@@ -570,6 +570,83 @@ __device__ __forceinline__ void epilogue_run(EpiCtx &e, int tile, uint32_t tbase
     if (threadIdx.x == 0) DGRAD_TRACE_ADD(14, ts1 - ts0);
 }
 
+// A whole grouped work unit of a one-phase convolution (stride 1) with S
+// sub-accumulators: first every warp publishes, for all the slice's columns,
+// the first rows the warp above it needs (one named barrier per unit instead
+// of one per 16 columns), then each warp combines and stores its rows batch by
+// batch without waiting for the others.  `ubuf` alternates the exchange
+// buffer between consecutive units: a warp can start the next unit's
+// publishing only after all four warps have passed this unit's barrier, i.e.
+// after the reads of the buffer it would overwrite.
+template <int S, int FUSE>
+__device__ __forceinline__ void epilogue_run_g1(EpiCtx &e, int tile, uint32_t tbase0, uint64_t *acc_empty,
+                                                uint32_t ubuf) {
+    constexpr int kSlots = S * (S - 1) / 2;
+    const MainParams &p = *e.p;
+    const PhaseDesc &pd = p.phase[0];
+    const int bnp = p.bn;
+    const int o = e.ew * 32 + e.lane;   // row of the unit
+    const int P = tile * p.tile_step + o;
+    dev::decode_position(p, P, e.n, e.q, e.u);
+    e.row_ok = o < p.tile_step && P < p.positions;
+    const uint32_t tb = tbase0 + static_cast<uint32_t>(pd.col);
+    float *xb = e.xbase + static_cast<size_t>(ubuf) * 4 * kSlots * bnp;
+    float *xw = xb + static_cast<size_t>(e.ew) * kSlots * bnp;
+    const float *xn = e.ew < 3 ? xw + kSlots * bnp : nullptr;
+    for (int c0 = 0; c0 < bnp; c0 += 16) {   // publish
+        uint32_t r[S - 1][16];
+#pragma unroll
+        for (int g = 0; g < S - 1; ++g) dev::tmem_ld16(tb + static_cast<uint32_t>(g * bnp + c0), r[g]);
+        dev::tmem_wait_ld();
+        int slot = 0;
+#pragma unroll
+        for (int g = 0; g < S - 1; ++g) {
+            const int sh = S - 1 - g;
+            if (e.lane < sh) {
+#pragma unroll
+                for (int j = 0; j < 16; ++j) xw[(slot + e.lane) * bnp + c0 + j] = __uint_as_float(r[g][j]);
+            }
+            slot += sh;
+        }
+    }
+    dev::named_bar(e.bar_id, 128);
+    const size_t plane = static_cast<size_t>(p.H) * p.W;
+    const bool valid = e.row_ok && e.q < pd.Hq && e.u < pd.Wq;
+    const int ih = p.s * e.q + pd.a, iw = p.s * e.u + pd.b;
+    float *dst = p.gi + (static_cast<size_t>(e.n) * p.Ci + e.ci0) * plane + static_cast<size_t>(ih) * p.W + iw;
+    float pend[1][1][16];
+    float *pend_dst = nullptr;
+    int pend_cols = 0;
+    for (int c0 = 0; c0 < bnp; c0 += 16) {   // combine and store
+        if (pend_dst) store_batch<1, 16, FUSE>(p, pend_dst, plane, pend_cols, pend);
+        uint32_t r[S][16];
+#pragma unroll
+        for (int g = 0; g < S; ++g) dev::tmem_ld16(tb + static_cast<uint32_t>(g * bnp + c0), r[g]);
+        dev::tmem_wait_ld();
+#pragma unroll
+        for (int j = 0; j < 16; ++j) pend[0][0][j] = __uint_as_float(r[S - 1][j]);
+        int slot = 0;
+#pragma unroll
+        for (int g = 0; g < S - 1; ++g) {
+            const int sh = S - 1 - g;
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                float v = __shfl_down_sync(0xffffffffu, __uint_as_float(r[g][j]), sh);
+                if (e.lane + sh >= 32) v = xn ? xn[(slot + e.lane + sh - 32) * bnp + c0 + j] : 0.f;
+                pend[0][0][j] += v;
+            }
+            slot += sh;
+        }
+        pend_dst = valid ? dst + static_cast<size_t>(c0) * plane : nullptr;
+        pend_cols = min(16, e.nci - c0);
+    }
+    // Every value of the unit is in registers: release the accumulator set,
+    // then store the last batch.
+    dev::tc_fence_before();
+    dev::mbar_arrive(dev::smem_u32(acc_empty));
+    if (pend_dst) store_batch<1, 16, FUSE>(p, pend_dst, plane, pend_cols, pend);
+}
+
 // Epilogue forms, one kernel instantiation each (so that each form's
 // registers are allocated on their own): phases stored together (NV),
 // sub-accumulators per phase (SMAX) and columns per tensor-memory wait (CB),
@@ -593,9 +670,17 @@ __host__ __device__ constexpr int epi_form(int vec_w, int s, int max_sub) {
 // partition holds a quarter of the register file and a quarter of the
 // block's warps (rounded up), so 6 warps leave 255 per thread and 14 warps
 // (producer mode) 128.
-template <int KC, bool kTmaA, int kEpi, int kFuse>
-__global__ void __launch_bounds__(kTmaA ? kThreadsTmaA : kThreads, 1)
+// kEG: epilogue warp groups (2: warps 6-9 form a second group that takes
+// every other work unit and the second accumulator set; tensor-copy mode).
+template <bool kTmaA, int kEG>
+constexpr int kernel_threads() {
+    return kTmaA ? (kProdWarp0 + (kEG - 1) * kEpiWarps) * 32 : kThreads;
+}
+
+template <int KC, bool kTmaA, int kEpi, int kFuse, int kEG>
+__global__ void __launch_bounds__(kernel_threads<kTmaA, kEG>(), 1)
     tc_dgrad_kernel(const __grid_constant__ MainParams p) {
+    static_assert(kEG == 1 || (kEG == 2 && kTmaA), "a second epilogue group needs the tensor-copy mode");
     static_assert(KC == 32, "operand rows are one 128-byte swizzle row of 32 TF32 values");
     extern __shared__ __align__(1024) uint8_t smem[];
     Barriers *bars = reinterpret_cast<Barriers *>(smem);
@@ -840,19 +925,31 @@ __global__ void __launch_bounds__(kTmaA ? kThreadsTmaA : kThreads, 1)
         // slower: ten warps leave 168 registers per thread, six leave 255.)
         const int ew = warp & 3;
         const int slots = p.max_sub * (p.max_sub - 1) / 2;
+        const int gi = (kEG == 2 && warp >= kProdWarp0) ? 1 : 0;   // epilogue group
         EpiCtx e;
         e.p = &p;
-        e.xbase = xchg;
+        e.xbase = xchg + static_cast<size_t>(gi) * (p.xchg_bytes / 4 / kEG);
         e.slots = slots;
         e.ew = ew;
         e.lane = lane;
-        e.bar_id = 1;
+        e.bar_id = 1 + gi;
         e.xcount = 0;
         Ring racc;
-        for (int w = blockIdx.x; w < p.n_work; w += gridDim.x) {
-            const int stage = racc.stage;
-            const uint32_t parity = racc.parity;
-            racc.next(p.acc_bufs);
+        uint32_t it = 0;
+        // One group: every unit, accumulator sets in turn.  Two groups: group gi
+        // takes the CTA's units gi, gi + 2, ... and always accumulator set gi.
+        for (int w = blockIdx.x + gi * static_cast<int>(gridDim.x); w < p.n_work;
+             w += kEG * static_cast<int>(gridDim.x), ++it) {
+            int stage;
+            uint32_t parity;
+            if constexpr (kEG == 2) {
+                stage = gi;
+                parity = it & 1u;
+            } else {
+                stage = racc.stage;
+                parity = racc.parity;
+                racc.next(p.acc_bufs);
+            }
             const int tile = w / p.n_slices, slice = w % p.n_slices;
             DGRAD_TRACE_CLOCK(te0);
             // All four warps of the group leave together or go on together.
@@ -869,7 +966,14 @@ __global__ void __launch_bounds__(kTmaA ? kThreadsTmaA : kThreads, 1)
             using F = EpiForm<kEpi>;
             const uint32_t tbase0 =
                 tmem_base + (static_cast<uint32_t>(ew * 32) << 16) + static_cast<uint32_t>(stage * p.acc_cols);
-            epilogue_run<F::NV, F::SMAX, F::CB, kFuse>(e, tile, tbase0, m_cols, &bars->acc_empty[stage]);
+            if constexpr (F::NV == 1 && F::SMAX > 1) {
+                if (p.xchg_unit && p.phase[0].tap_count > 0 && p.phase[0].sub == F::SMAX)
+                    epilogue_run_g1<F::SMAX, kFuse>(e, tile, tbase0, &bars->acc_empty[stage], e.xcount++ & 1u);
+                else
+                    epilogue_run<F::NV, F::SMAX, F::CB, kFuse>(e, tile, tbase0, m_cols, &bars->acc_empty[stage]);
+            } else {
+                epilogue_run<F::NV, F::SMAX, F::CB, kFuse>(e, tile, tbase0, m_cols, &bars->acc_empty[stage]);
+            }
             DGRAD_TRACE_CLOCK(te2);
             if (threadIdx.x == 0) DGRAD_TRACE_ADD(7, te2 - te1);
         }
@@ -883,14 +987,14 @@ __global__ void __launch_bounds__(kTmaA ? kThreadsTmaA : kThreads, 1)
     if (warp == kMmaWarp) dev::tmem_dealloc(tmem_base, p.tmem_cols);
 }
 
-template <int KC, bool kTmaA, int kEpi, int kFuse>
+template <int KC, bool kTmaA, int kEpi, int kFuse, int kEG = 1>
 cudaError_t launch_kc(const MainParams &p, const Tiling &t, cudaStream_t stream, bool pdl) {
-    auto kern = tc_dgrad_kernel<KC, kTmaA, kEpi, kFuse>;
+    auto kern = tc_dgrad_kernel<KC, kTmaA, kEpi, kFuse, kEG>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, t.smem_bytes);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(t.grid);
-    cfg.blockDim = dim3(kTmaA ? kThreadsTmaA : kThreads);
+    cfg.blockDim = dim3(kernel_threads<kTmaA, kEG>());
     cfg.dynamicSmemBytes = t.smem_bytes;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
@@ -903,11 +1007,21 @@ cudaError_t launch_kc(const MainParams &p, const Tiling &t, cudaStream_t stream,
 
 template <bool kTmaA, int kFuse>
 cudaError_t launch_mode(const MainParams &p, const Tiling &t, cudaStream_t stream, bool pdl) {
+    // Two epilogue groups for the grouped forms of plain-store tensor-copy
+    // launches (the fused-epilogue instances keep one group).
+    constexpr bool kTwo = kTmaA && kFuse == 0;
+    const bool two = kTwo && p.epi_groups == 2 && p.acc_bufs == 2;
     switch (epi_form(p.vec_w, p.s, p.max_sub)) {
         case 0: return launch_kc<32, kTmaA, 0, kFuse>(p, t, stream, pdl);
-        case 1: return launch_kc<32, kTmaA, 1, kFuse>(p, t, stream, pdl);
-        case 2: return launch_kc<32, kTmaA, 2, kFuse>(p, t, stream, pdl);
-        case 3: return launch_kc<32, kTmaA, 3, kFuse>(p, t, stream, pdl);
+        case 1:
+            return two ? launch_kc<32, kTmaA, 1, kFuse, kTwo ? 2 : 1>(p, t, stream, pdl)
+                       : launch_kc<32, kTmaA, 1, kFuse>(p, t, stream, pdl);
+        case 2:
+            return two ? launch_kc<32, kTmaA, 2, kFuse, kTwo ? 2 : 1>(p, t, stream, pdl)
+                       : launch_kc<32, kTmaA, 2, kFuse>(p, t, stream, pdl);
+        case 3:
+            return two ? launch_kc<32, kTmaA, 3, kFuse, kTwo ? 2 : 1>(p, t, stream, pdl)
+                       : launch_kc<32, kTmaA, 3, kFuse>(p, t, stream, pdl);
         case 4: return launch_kc<32, kTmaA, 4, kFuse>(p, t, stream, pdl);
         case 5: return launch_kc<32, kTmaA, 5, kFuse>(p, t, stream, pdl);
         default: return launch_kc<32, kTmaA, 6, kFuse>(p, t, stream, pdl);

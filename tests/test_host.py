@@ -240,9 +240,15 @@ def test_emulated_grouped_taps_match_oracle(shape):
 
 def test_grouping_plans():
     r = dg.describe(*WORKLOADS["resnet_stage"].plan_args(), precision="tf32")
-    assert r["group_taps"] == 0 and r["tile_step"] == 128 * r["tile_blocks"]   # opt-in
+    assert r["group_taps"] == 1 and r["tile_step"] == 126   # automatic for one phase with bn < 128
     on = dg.describe(*WORKLOADS["resnet_stage"].plan_args(), precision="tf32", group_taps="on")
     assert on["group_taps"] == 1 and on["tile_step"] == 126 and on["tmem_cols"] == 512
+    off = dg.describe(*WORKLOADS["resnet_stage"].plan_args(), precision="tf32", group_taps="off")
+    assert off["group_taps"] == 0 and off["tile_step"] == 128 * off["tile_blocks"]
+    pw = dg.describe(*WORKLOADS["pointwise"].plan_args(), precision="tf32")
+    assert pw["group_taps"] == 0                              # 1x1: one tap per row
+    t2 = dg.describe(*WORKLOADS["resnet_stage"].plan_args(), precision="tf32", tile_blocks=2)
+    assert t2["group_taps"] == 0 and t2["tile_step"] == 256   # two blocks per unit: ungrouped
     st = dg.describe(*WORKLOADS["stem"].plan_args(), precision="tf32", group_taps="on")
     assert st["group_taps"] == 1 and st["tile_step"] == 125
     with pytest.raises(dg.DgradError) as e:    # 5 taps per row cannot share one MMA
