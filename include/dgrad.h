@@ -105,8 +105,9 @@ typedef struct {
     int sm_count;      /* dgrad_describe only: SM count to plan for */
     int a_source;      /* tcgen05 path, how grad_out reaches the MMA: 0 automatic, 1 packed frame + tensor
                           copies (workspace holds a channels-last copy of grad_out), 2 producer warps */
-    int group_taps;    /* tcgen05 path, taps issued as one MMA: 0 automatic (3 where it applies, else
-                          none), 1 the taps of one kernel row (N = taps x slice_n, sub-accumulators
+    int group_taps;    /* tcgen05 path, taps issued as one MMA: 0 automatic (3 where it applies; for
+                          one phase (stride 1) in TF32 with slice_n < 128 and kW >= 2, 1 where it fits;
+                          else none), 1 the taps of one kernel row (N = taps x slice_n, sub-accumulators
                           summed with row shifts by the epilogue; DGRAD_ERR_UNSUPPORTED when that
                           cannot fit), 2 none, 3 the taps of different sub-pixel phases that read the
                           same frame shift (stride > 1; DGRAD_ERR_UNSUPPORTED when not possible) */
