@@ -501,16 +501,22 @@ dgrad_status_t dgrad_run_host(dgrad_plan_t plan, const float *grad_out_host, con
     // Chunk i: copy in on h2d, run on the caller's stream once its copy is
     // there, copy out on d2h once its run is done; the copy engines of the
     // two directions and the SMs work on different chunks at the same time.
+    // Every input copy is queued first, so that the host-to-device engine
+    // never waits for the host to queue the runs.
     cudaError_t e = cudaMemcpyAsync(plan->stage_w, weight_host, w_b, cudaMemcpyHostToDevice, plan->h2d);
+    for (int i = 0; e == cudaSuccess && i < nck; ++i) {
+        const int n0 = i * chunk_n, nn = std::min(chunk_n, g.N - n0);
+        uint8_t *dgo = reinterpret_cast<uint8_t *>(plan->stage_go) + i * go_slot;
+        e = cudaMemcpyAsync(dgo, reinterpret_cast<const uint8_t *>(grad_out_host) + n0 * go_img, nn * go_img,
+                            cudaMemcpyHostToDevice, plan->h2d);
+        if (e == cudaSuccess) e = cudaEventRecord(plan->ev_in[i], plan->h2d);
+    }
     for (int i = 0; e == cudaSuccess && i < nck; ++i) {
         const int n0 = i * chunk_n, nn = std::min(chunk_n, g.N - n0);
         dgrad_plan_s *sp = plan->sub[nn == chunk_n ? 0 : 1];
         uint8_t *dgo = reinterpret_cast<uint8_t *>(plan->stage_go) + i * go_slot;
         uint8_t *dgi = reinterpret_cast<uint8_t *>(plan->stage_gi) + i * gi_slot;
-        e = cudaMemcpyAsync(dgo, reinterpret_cast<const uint8_t *>(grad_out_host) + n0 * go_img, nn * go_img,
-                            cudaMemcpyHostToDevice, plan->h2d);
-        if (e == cudaSuccess) e = cudaEventRecord(plan->ev_in[i], plan->h2d);
-        if (e == cudaSuccess) e = cudaStreamWaitEvent(s, plan->ev_in[i], 0);
+        e = cudaStreamWaitEvent(s, plan->ev_in[i], 0);
         if (e != cudaSuccess) break;
         st = dgrad_run(sp, reinterpret_cast<const float *>(dgo), plan->stage_w, reinterpret_cast<float *>(dgi), stream);
         if (st != DGRAD_OK) {
