@@ -176,6 +176,27 @@ dgrad_status_t make_wgrad_geometry(int N, int Ci, int H, int W, int Co, int kH, 
     const int halves = g.split ? 2 : 1;
     g.oH = (int)(nh / stride) + 1;
     g.oW = (int)(nw / stride) + 1;
+    // Direct mode: a 1x1 kernel with stride 1 and no padding reads the input at
+    // the grad_out position itself, so both operands are K-major in NCHW as
+    // given (K = image, position): no frames; the tensor copies read the
+    // caller's tensors (per-image planes of H*W positions, a multiple of 4 for
+    // the 16-byte stride rule; the last chunk of a plane is zero-filled past its
+    // end) and the MMA takes the TF32 part of the fp32 values.
+    g.direct = !g.split && kH == 1 && kW == 1 && stride == 1 && pad_h == 0 && pad_w == 0 &&
+               ((long long)H * W) % 4 == 0 && (long long)H * W <= INT_MAX / 2;
+    if (g.direct) {
+        g.f = 1; g.lf = 0; g.m = 4; g.Q = N; g.blocked = 0;
+        g.Ty = g.Tu = 0;
+        g.Wf = g.oW;
+        g.Kimg = g.oH * g.oW;
+        g.cpi = ceil_div(g.Kimg, 32);
+        g.Lx = g.Kimg;
+        g.n_copies = 1;
+        g.copy_rh[0] = g.copy_rw[0] = g.copy_r[0] = 0;
+        g.taps = 1;
+        g.tap_copy[0] = 0;
+        g.tap_off[0] = 0;
+    }
     // Images interleaved along K.  Batch-blocked frames (f = 32, batches of
     // 32 or more with at most 1/8 of padding images): a 32-element K chunk is
     // one frame position of 32 images and a (position, channel block) tile is
@@ -183,60 +204,62 @@ dgrad_status_t make_wgrad_geometry(int N, int Ci, int H, int W, int Co, int kH, 
     // batches): a tap offset of whole columns is then a multiple of 4
     // positions (16 bytes, the tensor-copy alignment) once the copies absorb
     // column shifts mod m = 4/f.
-    g.blocked = N >= 32 && (round_up(N, 32) - N) * 8 <= N;
-    g.f = g.blocked ? 32 : (N >= 4 ? 4 : (N >= 2 ? 2 : 1));
-    g.lf = g.f == 32 ? 5 : (g.f == 4 ? 2 : (g.f == 2 ? 1 : 0));
-    g.m = g.f >= 4 ? 1 : 4 / g.f;
-    g.Q = ceil_div(N, g.f);
-    // Decomposition of the taps: kh - ph = s*dh + rh, kw - pw = s*dw + rw.
-    int dh_of[kMaxTaps], rh_of[kMaxTaps], dw_of[kMaxTaps], rw_of[kMaxTaps];
-    int dh_min = INT_MAX, dh_max = INT_MIN, dw_min = INT_MAX, dw_max = INT_MIN;
-    for (int kh = 0; kh < kH; ++kh) {
-        dh_of[kh] = floor_div(kh - pad_h, stride);
-        rh_of[kh] = kh - pad_h - dh_of[kh] * stride;
-        dh_min = std::min(dh_min, dh_of[kh]);
-        dh_max = std::max(dh_max, dh_of[kh]);
-    }
-    for (int kw = 0; kw < kW; ++kw) {
-        dw_of[kw] = floor_div(kw - pad_w, stride);
-        rw_of[kw] = kw - pad_w - dw_of[kw] * stride;
-        dw_min = std::min(dw_min, dw_of[kw]);
-        dw_max = std::max(dw_max, dw_of[kw]);
-    }
-    g.Ty = std::max(0, -dh_min);
-    g.Tu = std::max(0, -dw_min);
-    // Frame rows hold grad_out columns 0..oW-1 and every column a tap reads
-    // for them (u = ow + dw + Tu - r <= oW - 1 + dw_max + Tu), a multiple of m.
-    const long long wf = round_up(g.oW + std::max(0, dw_max) + g.Tu, g.m);
-    if (wf * g.oH * g.f > INT_MAX / 4) return DGRAD_ERR_UNSUPPORTED;
-    g.Wf = (int)wf;
-    g.Kimg = round_up(g.oH * g.Wf * g.f, 32);
-    g.cpi = g.Kimg / 32;
-    // Copies: one per (row phase, column phase, column shift r) some tap reads.
-    g.n_copies = 0;
-    g.taps = kH * kW;
-    int max_off = 0;
-    for (int kh = 0; kh < kH; ++kh)
-        for (int kw = 0; kw < kW; ++kw) {
-            const int t = kh * kW + kw;
-            const int r = (dw_of[kw] + g.Tu) % g.m;
-            int c = -1;
-            for (int i = 0; i < g.n_copies; ++i)
-                if (g.copy_rh[i] == rh_of[kh] && g.copy_rw[i] == rw_of[kw] && g.copy_r[i] == r) c = i;
-            if (c < 0) {
-                if (g.n_copies == kWgMaxCopies) return DGRAD_ERR_UNSUPPORTED;
-                c = g.n_copies++;
-                g.copy_rh[c] = rh_of[kh];
-                g.copy_rw[c] = rw_of[kw];
-                g.copy_r[c] = r;
-            }
-            g.tap_copy[t] = c;
-            g.tap_off[t] = ((dh_of[kh] + g.Ty) * g.Wf + (dw_of[kw] + g.Tu - r)) * g.f;
-            max_off = std::max(max_off, g.tap_off[t]);
+    if (!g.direct) {
+        g.blocked = N >= 32 && (round_up(N, 32) - N) * 8 <= N;
+        g.f = g.blocked ? 32 : (N >= 4 ? 4 : (N >= 2 ? 2 : 1));
+        g.lf = g.f == 32 ? 5 : (g.f == 4 ? 2 : (g.f == 2 ? 1 : 0));
+        g.m = g.f >= 4 ? 1 : 4 / g.f;
+        g.Q = ceil_div(N, g.f);
+        // Decomposition of the taps: kh - ph = s*dh + rh, kw - pw = s*dw + rw.
+        int dh_of[kMaxTaps], rh_of[kMaxTaps], dw_of[kMaxTaps], rw_of[kMaxTaps];
+        int dh_min = INT_MAX, dh_max = INT_MIN, dw_min = INT_MAX, dw_max = INT_MIN;
+        for (int kh = 0; kh < kH; ++kh) {
+            dh_of[kh] = floor_div(kh - pad_h, stride);
+            rh_of[kh] = kh - pad_h - dh_of[kh] * stride;
+            dh_min = std::min(dh_min, dh_of[kh]);
+            dh_max = std::max(dh_max, dh_of[kh]);
         }
-    const long long lx = (long long)g.Kimg + max_off;
-    if (lx > INT_MAX / 2) return DGRAD_ERR_UNSUPPORTED;
-    g.Lx = (int)lx;   // a multiple of 4 (of 32 when blocked): Kimg of 32, every offset of 4 (32)
+        for (int kw = 0; kw < kW; ++kw) {
+            dw_of[kw] = floor_div(kw - pad_w, stride);
+            rw_of[kw] = kw - pad_w - dw_of[kw] * stride;
+            dw_min = std::min(dw_min, dw_of[kw]);
+            dw_max = std::max(dw_max, dw_of[kw]);
+        }
+        g.Ty = std::max(0, -dh_min);
+        g.Tu = std::max(0, -dw_min);
+        // Frame rows hold grad_out columns 0..oW-1 and every column a tap reads
+        // for them (u = ow + dw + Tu - r <= oW - 1 + dw_max + Tu), a multiple of m.
+        const long long wf = round_up(g.oW + std::max(0, dw_max) + g.Tu, g.m);
+        if (wf * g.oH * g.f > INT_MAX / 4) return DGRAD_ERR_UNSUPPORTED;
+        g.Wf = (int)wf;
+        g.Kimg = round_up(g.oH * g.Wf * g.f, 32);
+        g.cpi = g.Kimg / 32;
+        // Copies: one per (row phase, column phase, column shift r) some tap reads.
+        g.n_copies = 0;
+        g.taps = kH * kW;
+        int max_off = 0;
+        for (int kh = 0; kh < kH; ++kh)
+            for (int kw = 0; kw < kW; ++kw) {
+                const int t = kh * kW + kw;
+                const int r = (dw_of[kw] + g.Tu) % g.m;
+                int c = -1;
+                for (int i = 0; i < g.n_copies; ++i)
+                    if (g.copy_rh[i] == rh_of[kh] && g.copy_rw[i] == rw_of[kw] && g.copy_r[i] == r) c = i;
+                if (c < 0) {
+                    if (g.n_copies == kWgMaxCopies) return DGRAD_ERR_UNSUPPORTED;
+                    c = g.n_copies++;
+                    g.copy_rh[c] = rh_of[kh];
+                    g.copy_rw[c] = rw_of[kw];
+                    g.copy_r[c] = r;
+                }
+                g.tap_copy[t] = c;
+                g.tap_off[t] = ((dh_of[kh] + g.Ty) * g.Wf + (dw_of[kw] + g.Tu - r)) * g.f;
+                max_off = std::max(max_off, g.tap_off[t]);
+            }
+        const long long lx = (long long)g.Kimg + max_off;
+        if (lx > INT_MAX / 2) return DGRAD_ERR_UNSUPPORTED;
+        g.Lx = (int)lx;   // a multiple of 4 (of 32 when blocked): Kimg of 32, every offset of 4 (32)
+    }
     // Row tiles: (tap, input-channel block) segments of seg_rows rows.
     g.seg_rows = std::min(128, round_up(Ci, 8));
     g.cpt = ceil_div(Ci, g.seg_rows);
@@ -285,8 +308,8 @@ dgrad_status_t make_wgrad_geometry(int N, int Ci, int H, int W, int Co, int kH, 
     if (g.stages < 2) return DGRAD_ERR_UNSUPPORTED;
     g.smem_bytes = kWgBarrierBytes + g.stages * stage_bytes;
     g.tmem_cols = pow2_at_least(2 * g.bn);
-    g.g_elems = (size_t)halves * g.Q * Co * g.Kimg;
-    g.x_elems = (size_t)halves * g.n_copies * g.Q * Ci * g.Lx;
+    g.g_elems = g.direct ? 0 : (size_t)halves * g.Q * Co * g.Kimg;
+    g.x_elems = g.direct ? 0 : (size_t)halves * g.n_copies * g.Q * Ci * g.Lx;
     if ((g.g_elems + g.x_elems) / 4 > (size_t)INT_MAX) return DGRAD_ERR_UNSUPPORTED;   // 32-bit pack indices
     g.part_elems = (size_t)g.n_units * g.bn * 128;
     plan_window(g, sm_count);
@@ -307,7 +330,7 @@ void fill_wgrad_info(const WgradGeometry &g, size_t ws, wgrad_plan_info_t *info)
     info->oH = g.oH; info->oW = g.oW;
     info->precision = g.split ? DGRAD_PREC_TF32X3 : DGRAD_PREC_TF32;
     info->interleave = g.f;
-    info->mode = g.win;
+    info->mode = g.win ? 1 : (g.direct ? 2 : 0);
     info->Wf = g.Wf; info->Kimg = g.Kimg; info->Lx = g.Lx; info->n_copies = g.n_copies;
     info->seg_rows = g.seg_rows; info->n_mt = g.n_mt; info->n_nt = g.n_nt; info->n_ks = g.n_ks;
     info->slice_n = g.bn; info->n_units = g.n_units; info->grid = g.grid; info->stages = g.stages;
@@ -330,7 +353,9 @@ bool woverlap(const void *a, size_t an, const void *b, size_t bn) {
     return a0 < b1 && b0 < a1;
 }
 
-dgrad_status_t encode_maps(wgrad_plan_s *pl) {
+// Tensor maps of the input copies (xc) and grad_out frame (gf); in direct mode
+// the caller's input and grad_out themselves.
+dgrad_status_t encode_maps(wgrad_plan_s *pl, const float *xsrc, const float *gsrc) {
     auto fn = dgrad::tensor_map_encoder();
     if (!fn) return DGRAD_ERR_CUDA;
     const WgradGeometry &g = pl->g;
@@ -351,12 +376,14 @@ dgrad_status_t encode_maps(wgrad_plan_s *pl) {
         gs[0] = (cuuint64_t)g.Kimg * 4; gs[1] = gs[0] * g.Co;
     }
     const cuuint32_t xbox[4] = {32u, (cuuint32_t)g.seg_rows, g.win ? (cuuint32_t)(g.run_len + g.spt - 1) : 1u, 1u};
-    if (fn(&pl->mp.x_map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, pl->xc, xd, xs, xbox, es4, CU_TENSOR_MAP_INTERLEAVE_NONE,
+    if (fn(&pl->mp.x_map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, const_cast<float *>(xsrc), xd, xs, xbox, es4,
+           CU_TENSOR_MAP_INTERLEAVE_NONE,
            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return DGRAD_ERR_CUDA;
     const cuuint32_t gbox[3] = {32u, (cuuint32_t)g.bn, g.win ? (cuuint32_t)g.run_len : 1u};
-    if (fn(&pl->mp.g_map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, pl->gf, gd, gs, gbox, es4, CU_TENSOR_MAP_INTERLEAVE_NONE,
+    if (fn(&pl->mp.g_map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float *>(gsrc), gd, gs, gbox, es4,
+           CU_TENSOR_MAP_INTERLEAVE_NONE,
            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return DGRAD_ERR_CUDA;
@@ -527,7 +554,8 @@ dgrad_status_t wgrad_plan(int N, int Ci, int H, int W, int Co, int kH, int kW, i
                                          dgrad::align256(pl->g.x_elems * 4));
     pl->workspace_bytes = ws;
     fill_wgrad_params(pl);
-    if ((st = encode_maps(pl)) != DGRAD_OK) {
+    // Direct mode encodes its maps per run, on the caller's tensors.
+    if (!pl->g.direct && (st = encode_maps(pl, pl->xc, pl->gf)) != DGRAD_OK) {
         cudaFree(mem);
         delete pl;
         return st;
@@ -559,8 +587,12 @@ dgrad_status_t wgrad_run(wgrad_plan_t plan, const float *grad_out, const float *
     plan->pp.go = grad_out;
     plan->pp.x = input;
     plan->rp.dw = grad_weight;
-    dgrad_status_t st = wcuda(dgrad::launch_wgrad_pack(plan->pp, s));
-    if (st != DGRAD_OK) return st;
+    dgrad_status_t st = DGRAD_OK;
+    if (g.direct) {   // no frames: the tensor copies read the caller's tensors
+        if ((st = encode_maps(plan, input, grad_out)) != DGRAD_OK) return st;
+    } else if ((st = wcuda(dgrad::launch_wgrad_pack(plan->pp, s))) != DGRAD_OK) {
+        return st;
+    }
     st = wcuda(g.win ? dgrad::launch_wgrad_window(plan->wp, g.grid, g.smem_bytes, s)
                      : dgrad::launch_wgrad_main(plan->mp, g.grid, g.smem_bytes, s));
     if (st != DGRAD_OK) return st;

@@ -44,6 +44,7 @@ struct WgradGeometry {
     int N, Ci, H, W, Co, kH, kW, s, ph, pw, oH, oW;
     int f, lf, m, Q;                  // images interleaved along K (f = 1 << lf), m = max(1, 4 / f), image groups
     int blocked;                      // f = 32, frames [position][channel][32 images]
+    int direct;                       // 1x1, stride 1, no padding: no frames, copies from the caller's tensors
     int Wf, Kimg, Lx, cpi;            // frame row pitch, K per image group, input-copy plane, chunks per group
     int Ty, Tu;                       // leading zero rows and columns of the input copies
     int n_copies;

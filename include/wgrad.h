@@ -61,7 +61,9 @@ typedef struct {
     int interleave;         /* f: images interleaved along K (32: batch-blocked frames; else 4, or 2, 1 for batches below 4) */
     int mode;               /* main kernel: 0 segment (a tensor copy per tap segment and chunk), 1 run (a tensor copy
                                per tile of adjacent taps holds a run of positions for several chunks; batch-blocked
-                               TF32 only) */
+                               TF32 only), 2 direct (1x1, stride 1, no padding, H*W a multiple of 4, TF32: the
+                               segment kernel's tensor copies read the caller's NCHW tensors, no frames; the MMA
+                               takes the TF32 part of each fp32 value instead of rounding it) */
     int Wf;                 /* row pitch of the position frames (grad_out columns plus the taps' column reach) */
     int Kimg;               /* GEMM K per group of f images: oH*Wf*f rounded up to a multiple of 32 */
     int Lx;                 /* length of one input-copy plane (Kimg plus the largest tap offset) */

@@ -344,6 +344,8 @@ WG_SHAPES = [
     (7, 2, 3, 10, 13, 7, 7, 2, 3, 3),
     (6, 4, 5, 11, 9, 5, 3, 3, 2, 1),
     (3, 3, 2, 8, 9, 3, 4, 1, 1, 2),
+    (3, 40, 24, 6, 10, 1, 1, 1, 0, 0),     # 1x1: direct mode, no frames
+    (2, 8, 16, 5, 5, 1, 1, 1, 0, 0),       # 1x1 with 25 positions per plane: frames
     (32, 3, 4, 7, 9, 3, 3, 1, 1, 1),       # batch-blocked frames (32 images per K chunk)
     (35, 5, 3, 8, 6, 3, 3, 2, 1, 1),       # 35 images: four interleaved (blocking would pad 29)
     (60, 5, 3, 8, 6, 3, 3, 2, 1, 1),       # blocked, four padding images
@@ -361,9 +363,12 @@ def emulate_wgrad(go, x, kH, kW, s, ph, pw):
     info = dg.wgrad_describe(N, Ci, H, W, Co, kH, kW, s, ph, pw)
     tab = dg.wgrad_describe_taps(N, Ci, H, W, Co, kH, kW, s, ph, pw)
     f, Wf, Kimg, Lx, Ty, Tu = tab["interleave"], info["Wf"], info["Kimg"], info["Lx"], tab["Ty"], tab["Tu"]
-    assert f == info["interleave"] and f in (1, 2, 4, 32) and Wf % max(1, 4 // f) == 0
+    assert f == info["interleave"] and f in (1, 2, 4, 32) and (info["mode"] == 2 or Wf % max(1, 4 // f) == 0)
     assert f != 32 or all(sh == 0 for sh in tab["copy_shift"])
-    assert Kimg % 32 == 0 and Lx % 4 == 0 and Kimg >= oH * Wf * f and Wf >= oW
+    if info["mode"] == 2:   # direct: the caller's NCHW planes, K = image x position, no frame padding
+        assert f == 1 and Wf == oW and Kimg == Lx == oH * oW and Kimg % 4 == 0 and (kH, kW, s) == (1, 1, 1)
+    else:
+        assert Kimg % 32 == 0 and Lx % 4 == 0 and Kimg >= oH * Wf * f and Wf >= oW
     Q = -(-N // f)
     k = np.arange(Kimg)
     j, pos = k % f, k // f
@@ -493,6 +498,15 @@ def test_wgrad_run_schedule(shape):
     assert sorted(rows) == [(t, ci) for t in range(kH * kW) for ci in range(Ci)]
 
 
+def test_wgrad_direct_mode_choice():
+    pw = WORKLOADS["pointwise"]
+    d = dg.wgrad_describe(*pw.plan_args(), sm_count=152)
+    assert d["mode"] == 2 and d["workspace_bytes"] < 64 << 20      # partial tiles only, no frames
+    assert dg.wgrad_describe(*pw.plan_args(), precision="tf32x3")["mode"] == 0
+    assert dg.wgrad_describe(2, 8, 5, 5, 16, 1, 1, 1, 0, 0)["mode"] == 0     # 25 positions: not a multiple of 4
+    assert dg.wgrad_describe(2, 8, 8, 8, 16, 1, 1, 2, 0, 0)["mode"] == 0     # stride 2
+
+
 def test_wgrad_window_mode_choice():
     assert dg.wgrad_describe_window(2, 3, 8, 8, 4, 3, 3, 1, 1, 1) is None            # small batch: segment mode
     assert dg.wgrad_describe(32, 64, 56, 56, 64, 3, 3, 1, 1, 1, "tf32x3")["mode"] == 0  # split precision
@@ -531,16 +545,18 @@ def test_wgrad_split_plans():
         assert b["precision"] == "tf32x3" and a["precision"] == "tf32"
         assert b["mode"] == 0     # split precision runs the segment mode
         same = ("n_mt", "n_nt", "slice_n", "seg_rows") if a["mode"] == 0 else ()
-        for k in same + ("Kimg", "Lx", "n_copies", "useful_flops"):
+        frames_too = ("Kimg", "Lx", "n_copies") if a["mode"] != 2 else ()   # direct mode has no frames
+        for k in same + frames_too + ("useful_flops",):
             assert a[k] == b[k], k
         chunks = -(-wl.N // b["interleave"]) * b["Kimg"] // 32
         assert -(-chunks // b["n_ks"]) <= 12   # short accumulation chains
         assert b["n_units"] == b["n_mt"] * b["n_nt"] * b["n_ks"]
         stage = 2 * (128 * 128 + b["slice_n"] * 128)
         assert b["stages"] >= 2 and b["smem_bytes"] >= b["stages"] * stage and b["smem_bytes"] <= 232448
-        Q = -(-wl.N // a["interleave"])
-        frames = 4 * (Q * wl.Co * a["Kimg"] + a["n_copies"] * Q * wl.Ci * a["Lx"])
-        assert b["workspace_bytes"] >= 2 * frames and a["workspace_bytes"] >= frames   # hi and lo halves
+        Q = -(-wl.N // b["interleave"])
+        frames = 4 * (Q * wl.Co * b["Kimg"] + b["n_copies"] * Q * wl.Ci * b["Lx"])
+        assert b["workspace_bytes"] >= 2 * frames                                     # hi and lo halves
+        assert a["mode"] == 2 or a["workspace_bytes"] >= frames
 
 
 def test_col2im_plans():

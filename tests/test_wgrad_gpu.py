@@ -98,6 +98,10 @@ EDGE = [
     (32, 16, 40, 9, 11, 5, 3, 1, 2, 1),    # window mode, 5 x 3 taps
     (32, 3, 8, 40, 44, 3, 3, 1, 1, 1),     # window mode, 16 slots per tile
     (32, 130, 24, 9, 8, 3, 3, 1, 1, 1),    # two input-channel blocks
+    (3, 40, 24, 6, 10, 1, 1, 1, 0, 0),     # 1x1: direct mode (the caller's tensors, no frames)
+    (2, 8, 300, 4, 9, 1, 1, 1, 0, 0),      # direct mode, two column tiles
+    (5, 130, 20, 12, 12, 1, 1, 1, 0, 0),   # direct mode, two input-channel segments
+    (2, 8, 16, 5, 5, 1, 1, 1, 0, 0),       # 1x1 with 25 positions per plane: frames
 ]
 
 
