@@ -9,12 +9,12 @@ that needs it does, and raises if it is missing (there is no CPU fallback).
 from __future__ import annotations
 
 __all__ = ["Plan", "DgradError", "dgrad", "describe", "describe_taps", "load_library", "workloads",
-           "WgradPlan", "wgrad_describe", "wgrad_describe_taps", "wgrad_describe_window"]
+           "WgradPlan", "wgrad_describe", "wgrad_describe_taps", "wgrad_describe_run"]
 
 
 def __getattr__(name):
     if name in ("Plan", "DgradError", "dgrad", "describe", "describe_taps", "load_library", "WgradPlan",
-                "wgrad_describe", "wgrad_describe_taps", "wgrad_describe_window"):
+                "wgrad_describe", "wgrad_describe_taps", "wgrad_describe_run"):
         from . import binding
         return getattr(binding, name)
     if name == "workloads":

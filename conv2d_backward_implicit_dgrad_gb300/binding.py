@@ -30,7 +30,7 @@ PATH_NAME = {v: k for k, v in PATH.items()}
 EXPORTS = ("dgrad_plan", "dgrad_plan_ex", "dgrad_describe", "dgrad_describe_taps", "dgrad_plan_info", "dgrad_run",
            "dgrad_run_fused", "dgrad_prepack", "dgrad_run_packed", "dgrad_pack_grad_out", "dgrad_run_main", "dgrad_run_host", "dgrad_run_noalloc", "dgrad_plan_check",
            "dgrad_plan_destroy", "dgrad_status_string", "dgrad_cuda_error_string",
-           "wgrad_describe", "wgrad_describe_taps", "wgrad_describe_window", "wgrad_plan", "wgrad_plan_info",
+           "wgrad_describe", "wgrad_describe_taps", "wgrad_describe_run", "wgrad_plan", "wgrad_plan_info",
            "wgrad_run", "wgrad_plan_check", "wgrad_plan_destroy")
 
 
@@ -397,19 +397,19 @@ def wgrad_describe_taps(N, Ci, H, W, Co, kH, kW, stride, pad_h, pad_w) -> dict:
             "interleave": f.value}
 
 
-def wgrad_describe_window(N, Ci, H, W, Co, kH, kW, stride, pad_h, pad_w, sm_count=0):
+def wgrad_describe_run(N, Ci, H, W, Co, kH, kW, stride, pad_h, pad_w, sm_count=0):
     """Host-only run-mode table of the weight gradient (None when the shape
     runs the segment mode): tap groups, tiles, stage length and tiles per unit."""
     lib = load_library()
     cap = 1024
     hdr = (ctypes.c_int * 15)()
     grp, taps, tiles = (ctypes.c_int * (6 * cap))(), (ctypes.c_int * cap)(), (ctypes.c_int * (2 * cap))()
-    st = lib.wgrad_describe_window(N, Ci, H, W, Co, kH, kW, stride, pad_h, pad_w, sm_count, cap, hdr, grp, taps,
+    st = lib.wgrad_describe_run(N, Ci, H, W, Co, kH, kW, stride, pad_h, pad_w, sm_count, cap, hdr, grp, taps,
                                    tiles)
     if st == 2:
         return None
     if st != 0:
-        raise DgradError(st, "wgrad_describe_window")
+        raise DgradError(st, "wgrad_describe_run")
     keys = ("n_groups", "n_tiles", "spt", "seg_rows", "stages", "Pg", "Px", "cps", "nksq", "cpt", "n_nt", "Q", "L",
             "tpu", "n_sets")
     d = dict(zip(keys, hdr[:15]))

@@ -15,7 +15,7 @@ struct wgrad_plan_s {
     int device;
     dgrad::WgradGeometry g;
     dgrad::WgradMainParams mp;
-    dgrad::WgradWinParams wp;   // window mode
+    dgrad::WgradRunParams wp;   // run mode
     dgrad::WgradPackParams pp;
     dgrad::WgradReduceParams rp;
     uint32_t *err;
@@ -44,7 +44,7 @@ size_t align256(size_t b) { return (b + 255) & ~size_t(255); }
 
 }  // namespace
 
-// Run mode (see WgradWinParams).  Taps are grouped by (kernel row, input
+// Run mode (see WgradRunParams).  Taps are grouped by (kernel row, input
 // copy); within a group consecutive taps read consecutive positions, so a
 // tile of spt of them is a contiguous run of position blocks.  The stage
 // length L and the tiles per unit come from a cost model: a tensor copy
@@ -54,7 +54,7 @@ size_t align256(size_t b) { return (b + 255) & ~size_t(255); }
 constexpr int kWgCopyCycles = 550;
 static int mma_cycles(int bn) { return bn <= 32 ? 66 : (bn <= 64 ? 72 : (bn <= 128 ? 84 : 128)); }
 
-static bool plan_window(WgradGeometry &g, int sm_count) {
+static bool plan_run(WgradGeometry &g, int sm_count) {
     if (!g.blocked || g.split) return false;
     int sr = 8;   // rows per position block: the input channels rounded up to a power of two, 8 .. 128
     while (sr < g.Ci && sr < 128) sr *= 2;
@@ -153,7 +153,7 @@ static bool plan_window(WgradGeometry &g, int sm_count) {
     g.n_units = (int)units;
     g.grid = std::min(g.n_units, sm_count);
     g.part_elems = (size_t)g.Q * g.nksq * g.cpt * g.n_nt * g.n_tiles * g.bn * 128;
-    g.win = 1;
+    g.run_mode = 1;
     return true;
 }
 
@@ -312,7 +312,7 @@ dgrad_status_t make_wgrad_geometry(int N, int Ci, int H, int W, int Co, int kH, 
     g.x_elems = g.direct ? 0 : (size_t)halves * g.n_copies * g.Q * Ci * g.Lx;
     if ((g.g_elems + g.x_elems) / 4 > (size_t)INT_MAX) return DGRAD_ERR_UNSUPPORTED;   // 32-bit pack indices
     g.part_elems = (size_t)g.n_units * g.bn * 128;
-    plan_window(g, sm_count);
+    plan_run(g, sm_count);
     *out = g;
     return DGRAD_OK;
 }
@@ -330,7 +330,7 @@ void fill_wgrad_info(const WgradGeometry &g, size_t ws, wgrad_plan_info_t *info)
     info->oH = g.oH; info->oW = g.oW;
     info->precision = g.split ? DGRAD_PREC_TF32X3 : DGRAD_PREC_TF32;
     info->interleave = g.f;
-    info->mode = g.win ? 1 : (g.direct ? 2 : 0);
+    info->mode = g.run_mode ? 1 : (g.direct ? 2 : 0);
     info->Wf = g.Wf; info->Kimg = g.Kimg; info->Lx = g.Lx; info->n_copies = g.n_copies;
     info->seg_rows = g.seg_rows; info->n_mt = g.n_mt; info->n_nt = g.n_nt; info->n_ks = g.n_ks;
     info->slice_n = g.bn; info->n_units = g.n_units; info->grid = g.grid; info->stages = g.stages;
@@ -375,13 +375,13 @@ dgrad_status_t encode_maps(wgrad_plan_s *pl, const float *xsrc, const float *gsr
         gd[0] = (cuuint64_t)g.Kimg; gd[1] = (cuuint64_t)g.Co; gd[2] = (cuuint64_t)g.Q * halves;
         gs[0] = (cuuint64_t)g.Kimg * 4; gs[1] = gs[0] * g.Co;
     }
-    const cuuint32_t xbox[4] = {32u, (cuuint32_t)g.seg_rows, g.win ? (cuuint32_t)(g.run_len + g.spt - 1) : 1u, 1u};
+    const cuuint32_t xbox[4] = {32u, (cuuint32_t)g.seg_rows, g.run_mode ? (cuuint32_t)(g.run_len + g.spt - 1) : 1u, 1u};
     if (fn(&pl->mp.x_map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, const_cast<float *>(xsrc), xd, xs, xbox, es4,
            CU_TENSOR_MAP_INTERLEAVE_NONE,
            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return DGRAD_ERR_CUDA;
-    const cuuint32_t gbox[3] = {32u, (cuuint32_t)g.bn, g.win ? (cuuint32_t)g.run_len : 1u};
+    const cuuint32_t gbox[3] = {32u, (cuuint32_t)g.bn, g.run_mode ? (cuuint32_t)g.run_len : 1u};
     if (fn(&pl->mp.g_map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float *>(gsrc), gd, gs, gbox, es4,
            CU_TENSOR_MAP_INTERLEAVE_NONE,
            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -422,16 +422,16 @@ void fill_wgrad_params(wgrad_plan_s *pl) {
     r.Co = g.Co; r.Ci = g.Ci; r.taps = g.taps; r.bn = g.bn; r.n_mt = g.n_mt; r.n_nt = g.n_nt; r.n_ks = g.n_ks;
     r.seg_rows = g.seg_rows; r.cpt = g.cpt; r.spt = g.spt; r.n_segs = g.n_segs;
     r.total = (long long)g.n_mt * g.n_nt * g.bn * 128;
-    r.win = g.win;
+    r.run_mode = g.run_mode;
     r.red_warps = 1;
     while (r.red_warps < 8 && r.red_warps * 8 < g.n_ks) r.red_warps *= 2;
-    if (g.win) {
+    if (g.run_mode) {
         r.n_tiles = g.n_tiles;
         r.total = (long long)g.cpt * g.n_nt * g.n_tiles * g.bn * 128;
         for (int t = 0; t < g.n_tiles; ++t) r.tile[t] = make_int2(g.tile_grp[t], g.tile_m0[t]);
         for (int gi = 0; gi < g.n_groups; ++gi) r.grp[gi] = make_int2(g.grp_tap0[gi], g.grp_nt[gi]);
         for (int t = 0; t < g.taps; ++t) r.taps_of[t] = g.grp_taps[t];
-        dgrad::WgradWinParams &w = pl->wp;
+        dgrad::WgradRunParams &w = pl->wp;
         w.part = pl->part;
         w.err = pl->err;
         w.n_units = g.n_units; w.n_sets = g.n_sets; w.tpu = g.tpu; w.n_tiles = g.n_tiles;
@@ -489,14 +489,14 @@ dgrad_status_t wgrad_describe_taps(int N, int Ci, int H, int W, int Co, int kH, 
     return DGRAD_OK;
 }
 
-dgrad_status_t wgrad_describe_window(int N, int Ci, int H, int W, int Co, int kH, int kW, int stride, int pad_h,
+dgrad_status_t wgrad_describe_run(int N, int Ci, int H, int W, int Co, int kH, int kW, int stride, int pad_h,
                                      int pad_w, int sm_count, int cap, int *hdr, int *groups, int *taps, int *tiles) {
     if (!hdr || !groups || !taps || !tiles) return DGRAD_ERR_INVALID_ARG;
     WgradGeometry g;
     dgrad_status_t st =
         dgrad::make_wgrad_geometry(N, Ci, H, W, Co, kH, kW, stride, pad_h, pad_w, DGRAD_PREC_TF32, sm_count, &g);
     if (st != DGRAD_OK) return st;
-    if (!g.win) return DGRAD_ERR_UNSUPPORTED;
+    if (!g.run_mode) return DGRAD_ERR_UNSUPPORTED;
     if (g.taps > cap || g.n_groups > cap || g.n_tiles > cap) return DGRAD_ERR_INVALID_ARG;
     const int h[15] = {g.n_groups, g.n_tiles, g.spt, g.seg_rows, g.stages, g.cpi, g.Lx / 32, g.cps,
                        g.nksq, g.cpt, g.n_nt, g.Q, g.run_len, g.tpu, g.n_sets};
@@ -593,7 +593,7 @@ dgrad_status_t wgrad_run(wgrad_plan_t plan, const float *grad_out, const float *
     } else if ((st = wcuda(dgrad::launch_wgrad_pack(plan->pp, s))) != DGRAD_OK) {
         return st;
     }
-    st = wcuda(g.win ? dgrad::launch_wgrad_window(plan->wp, g.grid, g.smem_bytes, s)
+    st = wcuda(g.run_mode ? dgrad::launch_wgrad_run(plan->wp, g.grid, g.smem_bytes, s)
                      : dgrad::launch_wgrad_main(plan->mp, g.grid, g.smem_bytes, s));
     if (st != DGRAD_OK) return st;
     return wcuda(dgrad::launch_wgrad_reduce(plan->rp, s));

@@ -36,8 +36,8 @@ constexpr int kWgMaxSegs = 256;     // (tap, ci block) segments of all row tiles
 constexpr int kWgMaxRowPhases = 4;  // largest stride
 constexpr int kWgMaxCopies = 32;    // input copies (rh, rw, r)
 constexpr int kWgPackTile = 64;     // frame positions per block of the batch-blocked pack
-constexpr int kWgMaxGroups = 16;    // window mode: tap groups (kernel row, column phase)
-constexpr int kWgMaxTiles = 32;     // window mode: 128-row accumulator tiles of one unit
+constexpr int kWgMaxGroups = 16;    // run mode: tap groups (kernel row, input copy)
+constexpr int kWgMaxTiles = 32;     // run mode: 128-row accumulator tiles (spt adjacent taps each)
 constexpr int kWgMaxStages = 8;
 
 struct WgradGeometry {
@@ -57,8 +57,8 @@ struct WgradGeometry {
     int split;                        // 1: split precision (hi and lo halves of both frames, three K passes)
     // Run mode (batch-blocked frames, TF32): tiles of spt taps at adjacent
     // positions; a tensor copy brings a run of L + spt - 1 positions of one
-    // tile, which feeds L chunks (see WgradWinParams).
-    int win, n_groups, n_tiles, nksq, run_len, tpu, n_sets, acc_sets, xbox_bytes, bbox_bytes;
+    // tile, which feeds L chunks (see WgradRunParams).
+    int run_mode, n_groups, n_tiles, nksq, run_len, tpu, n_sets, acc_sets, xbox_bytes, bbox_bytes;
     int grp_copy[kWgMaxGroups], grp_base[kWgMaxGroups], grp_nt[kWgMaxGroups], grp_nmt[kWgMaxGroups];
     int grp_tap0[kWgMaxGroups];
     int grp_taps[kMaxTaps];
@@ -98,8 +98,8 @@ struct WgradReduceParams {
     float *dw;
     int Co, Ci, taps, bn, n_mt, n_nt, n_ks, seg_rows, cpt, spt, n_segs;
     long long total;   // partial elements per split (segment mode n_mt * n_nt * bn * 128)
-    // window mode: partial tile t of a unit is M-tile tile[t].y of group tile[t].x
-    int win, n_tiles;
+    // run mode: partial tile t holds the taps tile[t].y .. of group tile[t].x
+    int run_mode, n_tiles;
     int red_warps;   // warps summing the K splits of one group of 128 elements: 1, 2, 4 or 8
     int2 tile[kWgMaxTiles];
     int2 grp[kWgMaxGroups];   // x: first entry in taps, y: taps in the group
@@ -113,7 +113,7 @@ struct WgradReduceParams {
 // that holds positions [c, c + L + spt - 1) of the tile (one copy feeds the
 // L chunks of a stage).  A unit is (tile set, ci block, co tile, image group,
 // K range); its grad_out copy holds the stage's L chunks.
-struct WgradWinParams {
+struct WgradRunParams {
     CUtensorMap x_map;   // batch-blocked xc, box {32, seg_rows, L + spt - 1, 1}
     CUtensorMap g_map;   // batch-blocked gf, box {32, bn, L}
     float *part;         // partial tiles [((q * nksq + ks) * cpt + cb) * n_nt + nt][tile][bn][128]
@@ -127,7 +127,7 @@ struct WgradWinParams {
 
 cudaError_t launch_wgrad_pack(const WgradPackParams &p, cudaStream_t stream);
 cudaError_t launch_wgrad_main(const WgradMainParams &p, int grid, int smem_bytes, cudaStream_t stream);
-cudaError_t launch_wgrad_window(const WgradWinParams &p, int grid, int smem_bytes, cudaStream_t stream);
+cudaError_t launch_wgrad_run(const WgradRunParams &p, int grid, int smem_bytes, cudaStream_t stream);
 cudaError_t launch_wgrad_reduce(const WgradReduceParams &p, cudaStream_t stream);
 
 }  // namespace dgrad

@@ -319,7 +319,7 @@ __global__ void __launch_bounds__(kWThreads, 1) wgrad_main_kernel(const __grid_c
 // stage reads tile rows from block i on and grad_out block i.  Accumulators:
 // acc_sets sets of tpu * bn columns (two when they fit, so that one unit's
 // epilogue overlaps the next unit's MMAs).
-__device__ __forceinline__ void run_decode(const WgradWinParams &p, int w, int &q, int &cb, int &nt, int &t0,
+__device__ __forceinline__ void run_decode(const WgradRunParams &p, int w, int &q, int &cb, int &nt, int &t0,
                                            int &t1, int &c0, int &c1, int &slot) {
     const int set = w % p.n_sets;
     slot = w / p.n_sets;   // (q, ks, cb, nt): the unit's row of partial tiles
@@ -336,7 +336,7 @@ __device__ __forceinline__ void run_decode(const WgradWinParams &p, int w, int &
     t1 = min(t0 + p.tpu, p.n_tiles);
 }
 
-__global__ void __launch_bounds__(kWThreads, 1) wgrad_window_kernel(const __grid_constant__ WgradWinParams p) {
+__global__ void __launch_bounds__(kWThreads, 1) wgrad_run_kernel(const __grid_constant__ WgradRunParams p) {
     extern __shared__ __align__(1024) uint8_t smem[];
     WBars *bars = reinterpret_cast<WBars *>(smem);
     const uint32_t base0 = (dev::smem_u32(smem) + kWBarrierBytes + 1023u) & ~1023u;
@@ -722,7 +722,7 @@ __device__ __forceinline__ void wgrad_reduce_store(const WgradReduceParams &p, l
     rest /= p.bn;
     const int sl = row / p.seg_rows;
     int t, ci, nt;
-    if (p.win) {   // element (cb, nt, tile, col, row); tile = taps of one group at adjacent positions
+    if (p.run_mode) {   // element (cb, nt, tile, col, row); tile = taps of one group at adjacent positions
         const int tile = static_cast<int>(rest % p.n_tiles);
         rest /= p.n_tiles;
         nt = static_cast<int>(rest % p.n_nt);
@@ -839,10 +839,10 @@ cudaError_t launch_wgrad_main(const WgradMainParams &p, int grid, int smem_bytes
     return launch_pdl(wgrad_main_kernel, p, grid, kWThreads, smem_bytes, stream);
 }
 
-cudaError_t launch_wgrad_window(const WgradWinParams &p, int grid, int smem_bytes, cudaStream_t stream) {
-    cudaError_t e = cudaFuncSetAttribute(wgrad_window_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+cudaError_t launch_wgrad_run(const WgradRunParams &p, int grid, int smem_bytes, cudaStream_t stream) {
+    cudaError_t e = cudaFuncSetAttribute(wgrad_run_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
     if (e != cudaSuccess) return e;
-    return launch_pdl(wgrad_window_kernel, p, grid, kWThreads, smem_bytes, stream);
+    return launch_pdl(wgrad_run_kernel, p, grid, kWThreads, smem_bytes, stream);
 }
 
 cudaError_t launch_wgrad_reduce(const WgradReduceParams &p, cudaStream_t stream) {

@@ -103,7 +103,7 @@ dgrad_status_t wgrad_describe_taps(int N, int Ci, int H, int W, int Co, int kH, 
  * tiles, 0, first entry in taps[]}; taps[] lists the taps group by group in
  * position order; per tile 2 ints {group, first tap in the group}.  Each
  * array holds at least `cap` entries of its kind. */
-dgrad_status_t wgrad_describe_window(int N, int Ci, int H, int W, int Co, int kH, int kW, int stride, int pad_h,
+dgrad_status_t wgrad_describe_run(int N, int Ci, int H, int W, int Co, int kH, int kW, int stride, int pad_h,
                                      int pad_w, int sm_count, int cap, int *hdr, int *groups, int *taps, int *tiles);
 
 /* Create a plan on the current device: validate, plan the tiles and allocate

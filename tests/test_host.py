@@ -395,7 +395,7 @@ def emulate_wgrad(go, x, kH, kW, s, ph, pw):
     cpt = -(-Ci // seg_rows)
     spt = 128 // seg_rows
     n_segs = kH * kW * cpt
-    segment = info["mode"] == 0   # the window mode's rows are checked by test_wgrad_window_schedule
+    segment = info["mode"] == 0   # the run mode's rows are checked by test_wgrad_run_schedule
     assert not segment or info["n_mt"] == -(-n_segs // spt)
     for t in range(kH * kW):
         off = tab["offset"][t]
@@ -425,8 +425,8 @@ def test_emulated_wgrad_matches_oracle(shape):
     assert np.abs(emu - ref).max() <= 1e-12 * max(1.0, mag.max())
 
 
-WIN_SHAPES = [
-    # N, Ci, Co, H, W, kH, kW, s, ph, pw: batch-blocked TF32 shapes that run the window mode
+RUN_SHAPES = [
+    # N, Ci, Co, H, W, kH, kW, s, ph, pw: batch-blocked TF32 shapes that run the run mode
     (32, 64, 64, 56, 56, 3, 3, 1, 1, 1),   # the resnet_stage shape
     (32, 3, 4, 7, 9, 3, 3, 1, 1, 1),
     (60, 5, 3, 8, 6, 3, 3, 2, 1, 1),
@@ -435,7 +435,7 @@ WIN_SHAPES = [
 ]
 
 
-@pytest.mark.parametrize("shape", WIN_SHAPES)
+@pytest.mark.parametrize("shape", RUN_SHAPES)
 def test_wgrad_run_schedule(shape):
     """Run mode on the CPU: the tap groups against the tap table; each tile's
     tensor copy (L + spt - 1 position blocks from the stage's first chunk on)
@@ -446,7 +446,7 @@ def test_wgrad_run_schedule(shape):
     N, Ci, Co, H, W, kH, kW, s, ph, pw = shape
     args = (N, Ci, H, W, Co, kH, kW, s, ph, pw)
     info = dg.wgrad_describe(*args, sm_count=152)
-    d = dg.wgrad_describe_window(*args, sm_count=152)
+    d = dg.wgrad_describe_run(*args, sm_count=152)
     tab = dg.wgrad_describe_taps(*args)
     assert info["mode"] == 1 and d is not None and info["interleave"] == 32
     spt, sr, L, tpu, bn = d["spt"], d["seg_rows"], d["L"], d["tpu"], info["slice_n"]
@@ -507,8 +507,8 @@ def test_wgrad_direct_mode_choice():
     assert dg.wgrad_describe(2, 8, 8, 8, 16, 1, 1, 2, 0, 0)["mode"] == 0     # stride 2
 
 
-def test_wgrad_window_mode_choice():
-    assert dg.wgrad_describe_window(2, 3, 8, 8, 4, 3, 3, 1, 1, 1) is None            # small batch: segment mode
+def test_wgrad_run_mode_choice():
+    assert dg.wgrad_describe_run(2, 3, 8, 8, 4, 3, 3, 1, 1, 1) is None            # small batch: segment mode
     assert dg.wgrad_describe(32, 64, 56, 56, 64, 3, 3, 1, 1, 1, "tf32x3")["mode"] == 0  # split precision
     assert dg.wgrad_describe(32, 64, 56, 56, 64, 3, 3, 1, 1, 1)["mode"] == 1
 

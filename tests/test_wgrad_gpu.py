@@ -93,10 +93,10 @@ EDGE = [
     (35, 5, 3, 8, 6, 3, 3, 2, 1, 1),       # 35 images: four interleaved (blocking would pad 29)
     (60, 5, 3, 8, 6, 3, 3, 2, 1, 1),       # blocked, four padding images
     (33, 2, 2, 5, 7, 5, 3, 3, 2, 1),
-    (64, 70, 20, 6, 5, 3, 3, 1, 1, 1),     # blocked, two image groups (segment mode: windows do not fit)
-    (64, 40, 20, 6, 5, 3, 3, 1, 1, 1),     # window mode, two image groups
-    (32, 16, 40, 9, 11, 5, 3, 1, 2, 1),    # window mode, 5 x 3 taps
-    (32, 3, 8, 40, 44, 3, 3, 1, 1, 1),     # window mode, 16 slots per tile
+    (64, 70, 20, 6, 5, 3, 3, 1, 1, 1),     # blocked, two image groups (segment mode: run tiles do not fit)
+    (64, 40, 20, 6, 5, 3, 3, 1, 1, 1),     # run mode, two image groups
+    (32, 16, 40, 9, 11, 5, 3, 1, 2, 1),    # run mode, 5 x 3 taps
+    (32, 3, 8, 40, 44, 3, 3, 1, 1, 1),     # run mode, 16 position blocks per tile
     (32, 130, 24, 9, 8, 3, 3, 1, 1, 1),    # two input-channel blocks
     (3, 40, 24, 6, 10, 1, 1, 1, 0, 0),     # 1x1: direct mode (the caller's tensors, no frames)
     (2, 8, 300, 4, 9, 1, 1, 1, 0, 0),      # direct mode, two column tiles
