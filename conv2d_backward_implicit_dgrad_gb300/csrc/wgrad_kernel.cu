@@ -846,8 +846,9 @@ cudaError_t launch_wgrad_run(const WgradRunParams &p, int grid, int smem_bytes, 
 }
 
 cudaError_t launch_wgrad_reduce(const WgradReduceParams &p, cudaStream_t stream) {
-    // 16-byte loads unless that leaves too few threads to keep the splits' loads in flight
-    const int v = (p.total / 4) * p.red_warps >= 150000 ? 4 : 1;
+    // 16-byte loads (four in flight per thread: 64 bytes) unless that leaves
+    // fewer threads than one block per SM
+    const int v = (p.total / 4) * p.red_warps >= 152LL * 256 ? 4 : 1;
     const long long per_block = 32LL * v * (8 / p.red_warps);   // partial elements per block
     const long long blocks = (p.total + per_block - 1) / per_block;
     if (blocks < 1 || blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
