@@ -55,7 +55,8 @@ constexpr int kWgCopyCycles = 550;
 static int mma_cycles(int bn) { return bn <= 32 ? 66 : (bn <= 64 ? 72 : (bn <= 128 ? 84 : 128)); }
 
 static bool plan_run(WgradGeometry &g, int sm_count) {
-    if (!g.blocked || g.split) return false;
+    if (!g.blocked) return false;
+    const int halves = g.split ? 2 : 1;   // split precision: hi and lo copies, three MMA passes
     int sr = 8;   // rows per position block: the input channels rounded up to a power of two, 8 .. 128
     while (sr < g.Ci && sr < 128) sr *= 2;
     const int spt = 128 / sr;
@@ -101,11 +102,14 @@ static bool plan_run(WgradGeometry &g, int sm_count) {
     int bl = 0, bt = 0, bd = 0;
     for (int L = 1; L <= l_max; ++L)
         for (int tpu = 1; tpu <= std::min(g.n_tiles, 512 / g.bn); ++tpu) {
-            const long long stage = (long long)tpu * (L + spt - 1) * sr * 128 + (long long)L * g.bn * 128;
+            if (g.split && L > kWgSplitChunks) continue;
+            const long long stage =
+                halves * ((long long)tpu * (L + spt - 1) * sr * 128 + (long long)L * g.bn * 128);
             const int d = (int)std::min<long long>(kWgMaxStages, (kMaxSmem - kWgBarrierBytes) / stage);
             if (d < 2) continue;
             const int sets = ceil_div(g.n_tiles, tpu);
-            const double per_stage = std::max((double)(tpu + 1) * kWgCopyCycles, (double)L * tpu * 4 * mma_cycles(g.bn));
+            const double per_stage = std::max((double)halves * (tpu + 1) * kWgCopyCycles,
+                                              (double)L * tpu * 4 * (2 * halves - 1) * mma_cycles(g.bn));
             const double cost = per_stage / L * sets;   // per chunk, all tiles
             if (best < 0 || cost < best * 0.999) {
                 best = cost;
@@ -124,7 +128,7 @@ static bool plan_run(WgradGeometry &g, int sm_count) {
     g.stages = bd;
     g.xbox_bytes = (bl + spt - 1) * sr * 128;
     g.bbox_bytes = bl * g.bn * 128;
-    g.smem_bytes = kWgBarrierBytes + bd * (bt * g.xbox_bytes + g.bbox_bytes);
+    g.smem_bytes = kWgBarrierBytes + bd * halves * (bt * g.xbox_bytes + g.bbox_bytes);
     g.acc_sets = 2 * bt * g.bn <= 512 ? 2 : 1;
     g.tmem_cols = pow2_at_least(std::max(32, g.acc_sets * bt * g.bn));
     // K splits within each image group, units of whole stages: minimise
@@ -132,10 +136,13 @@ static bool plan_run(WgradGeometry &g, int sm_count) {
     // stores) per unit.
     const int per = g.n_sets * g.cpt * g.n_nt * g.Q;
     const int stages_total = ceil_div(g.cpi, bl);
-    const int ks_hi = std::max(1, std::min(stages_total / 2, ceil_div(8 * sm_count, per)));
+    // Split precision: at most kWgSplitChunks chunks accumulate in one unit
+    // (see the segment mode's K splits).
+    const int ks_lo = g.split ? ceil_div(stages_total, std::max(1, kWgSplitChunks / bl)) : 1;
+    const int ks_hi = std::max(ks_lo, std::min(stages_total / 2, ceil_div(8 * sm_count, per)));
     long long bestk = -1;
-    int nk = 1;
-    for (int k = 1; k <= ks_hi; ++k) {
+    int nk = ks_lo;
+    for (int k = ks_lo; k <= ks_hi; ++k) {
         const int sps = ceil_div(stages_total, k);
         if (ceil_div(stages_total, sps) != k) continue;
         const long long cost = (long long)ceil_div(per * k, sm_count) * (sps + 2);
@@ -439,6 +446,7 @@ void fill_wgrad_params(wgrad_plan_s *pl) {
         w.Pg = g.cpi; w.Px = g.Lx / 32; w.seg_rows = g.seg_rows; w.L = g.run_len; w.bn = g.bn;
         w.stages = g.stages; w.acc_sets = g.acc_sets; w.tmem_cols = g.tmem_cols;
         w.xbox_bytes = g.xbox_bytes; w.bbox_bytes = g.bbox_bytes;
+        w.split = g.split; w.n_copies = g.n_copies; w.Q = g.Q;
         w.idesc = dgrad::tf32_idesc(128, g.bn);
         w.timeout_ns = dgrad::kWgTimeoutNs;
         for (int t = 0; t < g.n_tiles; ++t) {

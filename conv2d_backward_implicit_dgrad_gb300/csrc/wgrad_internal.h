@@ -120,6 +120,7 @@ struct WgradRunParams {
     uint32_t *err;
     int n_units, n_sets, tpu, n_tiles, cpt, n_nt, nksq, cps, Pg, Px, seg_rows, L, bn, stages, acc_sets, tmem_cols;
     int xbox_bytes, bbox_bytes;
+    int split, n_copies, Q;   // split precision: lo copies at copy + n_copies and group + Q (stage: hi half, lo half)
     uint32_t idesc;
     long long timeout_ns;
     int2 tile[kWgMaxTiles];   // x: input copy, y: position offset of the tile's first tap (base + m0)

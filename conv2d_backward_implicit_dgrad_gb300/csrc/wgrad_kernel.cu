@@ -336,12 +336,14 @@ __device__ __forceinline__ void run_decode(const WgradRunParams &p, int w, int &
     t1 = min(t0 + p.tpu, p.n_tiles);
 }
 
+template <bool kSplit>   // split precision: a template parameter, so the plain kernel carries none of it
 __global__ void __launch_bounds__(kWThreads, 1) wgrad_run_kernel(const __grid_constant__ WgradRunParams p) {
     extern __shared__ __align__(1024) uint8_t smem[];
     WBars *bars = reinterpret_cast<WBars *>(smem);
     const uint32_t base0 = (dev::smem_u32(smem) + kWBarrierBytes + 1023u) & ~1023u;
     const uint32_t xb = static_cast<uint32_t>(p.xbox_bytes);
-    const uint32_t stage_bytes = static_cast<uint32_t>(p.tpu) * xb + static_cast<uint32_t>(p.bbox_bytes);
+    const uint32_t half_bytes = static_cast<uint32_t>(p.tpu) * xb + static_cast<uint32_t>(p.bbox_bytes);
+    const uint32_t stage_bytes = half_bytes * (kSplit ? 2u : 1u);   // split precision: hi half, then lo half
     const uint32_t blk = static_cast<uint32_t>(p.seg_rows) * 128u;   // one position block of a tile copy
     const uint32_t gblk = static_cast<uint32_t>(p.bn) * 128u;        // one grad_out block
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -383,7 +385,8 @@ __global__ void __launch_bounds__(kWThreads, 1) wgrad_run_kernel(const __grid_co
             for (int w = blockIdx.x; ok && w < p.n_units && !bars->abort_flag; w += gridDim.x) {
                 int q, cb, nt, t0, t1, c0, c1, slot;
                 run_decode(p, w, q, cb, nt, t0, t1, c0, c1, slot);
-                const uint32_t bytes = static_cast<uint32_t>(t1 - t0) * xb + static_cast<uint32_t>(p.bbox_bytes);
+                const uint32_t bytes =
+                    (static_cast<uint32_t>(t1 - t0) * xb + static_cast<uint32_t>(p.bbox_bytes)) * (kSplit ? 2u : 1u);
                 for (int c = c0; c < c1; c += p.L) {
                     WG_TRACE_CLOCK(tl0);
                     if (!dev::mbar_wait(dev::smem_u32(&bars->empty[ring.stage]), ring.parity ^ 1, tmo)) {
@@ -395,14 +398,17 @@ __global__ void __launch_bounds__(kWThreads, 1) wgrad_run_kernel(const __grid_co
                     WG_TRACE_ADD(0, tl1 - tl0);
                     const uint32_t bar = dev::smem_u32(&bars->full[ring.stage]);
                     dev::mbar_arrive_expect_tx(bar, bytes);
-                    const uint32_t dst = base0 + static_cast<uint32_t>(ring.stage) * stage_bytes;
-                    for (int t = t0; t < t1; ++t) {
-                        const int2 tl = p.tile[t];   // copy, position offset
-                        dev::tma_load_4d(dst + static_cast<uint32_t>(t - t0) * xb, &p.x_map, 0, cb * p.seg_rows,
-                                         q * p.Px + c + tl.y, tl.x, bar);
+                    for (int h = 0; h <= (kSplit ? 1 : 0); ++h) {
+                        const uint32_t dst =
+                            base0 + static_cast<uint32_t>(ring.stage) * stage_bytes + static_cast<uint32_t>(h) * half_bytes;
+                        for (int t = t0; t < t1; ++t) {
+                            const int2 tl = p.tile[t];   // copy, position offset
+                            dev::tma_load_4d(dst + static_cast<uint32_t>(t - t0) * xb, &p.x_map, 0, cb * p.seg_rows,
+                                             q * p.Px + c + tl.y, tl.x + h * p.n_copies, bar);
+                        }
+                        dev::tma_load_3d(dst + static_cast<uint32_t>(p.tpu) * xb, &p.g_map, 0, nt * p.bn,
+                                         (q + h * p.Q) * p.Pg + c, bar);
                     }
-                    dev::tma_load_3d(dst + static_cast<uint32_t>(p.tpu) * xb, &p.g_map, 0, nt * p.bn, q * p.Pg + c,
-                                     bar);
                     last_parity[ring.stage] = static_cast<int>(ring.parity);
                     ring.next(p.stages);
                 }
@@ -448,6 +454,7 @@ __global__ void __launch_bounds__(kWThreads, 1) wgrad_run_kernel(const __grid_co
                 const uint32_t sbase = base0 + static_cast<uint32_t>(ring.stage) * stage_bytes;
                 const uint64_t xd = dev::smem_desc_sw128(sbase, 0);
                 const uint64_t gd = dev::smem_desc_sw128(sbase + static_cast<uint32_t>(p.tpu) * xb, 0);
+                const uint32_t lo = kSplit ? half_bytes : 0u;   // byte offset of the lo half
                 const int n = min(p.L, c1 - c);
                 for (int i = 0; i < n; ++i) {
                     const uint64_t bd = dev::desc_add(gd, static_cast<uint32_t>(i) * gblk);
@@ -455,10 +462,20 @@ __global__ void __launch_bounds__(kWThreads, 1) wgrad_run_kernel(const __grid_co
                     for (int t = 0; t < t1 - t0; ++t) {
                         const uint64_t ad = dev::desc_add(xd, static_cast<uint32_t>(t) * xb + static_cast<uint32_t>(i) * blk);
                         const uint32_t d = d0 + static_cast<uint32_t>(t * p.bn);
+                        if constexpr (kSplit) {   // hi*lo, lo*hi, hi*hi: the small cross terms first
+#pragma unroll
+                            for (int k8 = 0; k8 < 4; ++k8)
+                                dev::mma_tf32_elect(d, dev::desc_add(ad, 32 * k8), dev::desc_add(bd, lo + 32 * k8),
+                                                    p.idesc, k8 > 0 ? 1u : acc);
+#pragma unroll
+                            for (int k8 = 0; k8 < 4; ++k8)
+                                dev::mma_tf32_elect(d, dev::desc_add(ad, lo + 32 * k8), dev::desc_add(bd, 32 * k8),
+                                                    p.idesc, 1u);
+                        }
 #pragma unroll
                         for (int k8 = 0; k8 < 4; ++k8)
                             dev::mma_tf32_elect(d, dev::desc_add(ad, 32 * k8), dev::desc_add(bd, 32 * k8), p.idesc,
-                                                k8 > 0 ? 1u : acc);
+                                                (k8 > 0 || kSplit) ? 1u : acc);
                     }
                 }
                 dev::mma_commit_elect(dev::smem_u32(&bars->empty[ring.stage]));
@@ -840,9 +857,10 @@ cudaError_t launch_wgrad_main(const WgradMainParams &p, int grid, int smem_bytes
 }
 
 cudaError_t launch_wgrad_run(const WgradRunParams &p, int grid, int smem_bytes, cudaStream_t stream) {
-    cudaError_t e = cudaFuncSetAttribute(wgrad_run_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+    auto kern = p.split ? wgrad_run_kernel<true> : wgrad_run_kernel<false>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
     if (e != cudaSuccess) return e;
-    return launch_pdl(wgrad_run_kernel, p, grid, kWThreads, smem_bytes, stream);
+    return launch_pdl(kern, p, grid, kWThreads, smem_bytes, stream);
 }
 
 cudaError_t launch_wgrad_reduce(const WgradReduceParams &p, cudaStream_t stream) {
