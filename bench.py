@@ -298,6 +298,17 @@ def roofline(wl, precision, flops, nbytes, main_s, step_s):
     }
 
 
+def slowest_rank(torch, dist, r, device):
+    """Replace this rank's times in `r` by the maximum over all ranks (one
+    all-reduce of three numbers, outside the timed region).  A rank without an
+    end-to-end time contributes 0 to that maximum."""
+    t = torch.tensor([r["ms_per_step"], r["main_ms"], r["e2e_s"] or 0.0], device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    r["ms_per_step"], r["main_ms"], e2e_s = t.tolist()
+    r["e2e_s"] = e2e_s or None
+    return r
+
+
 def build_line(args, wl, r, world):
     flops, nbytes = r["flops"], r["bytes"]
     step_s, main_s = r["ms_per_step"] * 1e-3, r["main_ms"] * 1e-3
@@ -428,9 +439,7 @@ def main():
     r = time_workload(dg, torch, wl, args.precision, args.steps, args.warmup, rank, barrier, local,
                       clocks=True, e2e=True)
     if world > 1:
-        t = torch.tensor([r["ms_per_step"], r["main_ms"], r["e2e_s"] or 0.0], device="cuda", dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        r["ms_per_step"], r["main_ms"], r["e2e_s"] = t.tolist()
+        slowest_rank(torch, dist, r, "cuda")
 
     if rank == 0:
         line = build_line(args, wl, r, world)
