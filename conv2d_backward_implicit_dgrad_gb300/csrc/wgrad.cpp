@@ -418,8 +418,10 @@ void fill_wgrad_params(wgrad_plan_s *pl) {
     q.N = g.N; q.Ci = g.Ci; q.H = g.H; q.W = g.W; q.Co = g.Co; q.oH = g.oH; q.oW = g.oW;
     q.s = g.s; q.Wf = g.Wf; q.Kimg = g.Kimg; q.Lx = g.Lx; q.Ty = g.Ty; q.Tu = g.Tu;
     q.Q = g.Q; q.lf = g.lf; q.blocked = g.blocked; q.Px = g.Lx / 32; q.Pg = g.cpi;
-    q.g_tiles = (long long)g.Q * g.Co * ((g.cpi + dgrad::kWgPackTile - 1) / dgrad::kWgPackTile);
-    q.x_tiles = (long long)g.n_copies * g.Q * g.Ci * ((g.Lx / 32 + dgrad::kWgPackTile - 1) / dgrad::kWgPackTile);
+    const long long co_blocks = (g.Co + dgrad::kWgPackCh - 1) / dgrad::kWgPackCh;
+    const long long ci_blocks = (g.Ci + dgrad::kWgPackCh - 1) / dgrad::kWgPackCh;
+    q.g_tiles = (long long)g.Q * co_blocks * ((g.cpi + dgrad::kWgPackTile - 1) / dgrad::kWgPackTile);
+    q.x_tiles = (long long)g.n_copies * g.Q * ci_blocks * ((g.Lx / 32 + dgrad::kWgPackTile - 1) / dgrad::kWgPackTile);
     for (int c = 0; c < g.n_copies; ++c) q.copy[c] = make_int4(g.copy_rh[c], g.copy_rw[c], g.copy_r[c], 0);
     q.split = g.split;
     q.g4 = (long long)(g.g_elems / 4 / (g.split ? 2 : 1));

@@ -36,6 +36,7 @@ constexpr int kWgMaxSegs = 256;     // (tap, ci block) segments of all row tiles
 constexpr int kWgMaxRowPhases = 4;  // largest stride
 constexpr int kWgMaxCopies = 32;    // input copies (rh, rw, r)
 constexpr int kWgPackTile = 64;     // frame positions per block of the batch-blocked pack
+constexpr int kWgPackCh = 4;        // channels per block of the batch-blocked pack
 constexpr int kWgMaxGroups = 16;    // run mode: tap groups (kernel row, input copy)
 constexpr int kWgMaxTiles = 32;     // run mode: 128-row accumulator tiles (spt adjacent taps each)
 constexpr int kWgMaxStages = 8;
@@ -77,7 +78,7 @@ struct WgradPackParams {
     int split;          // 1: write hi = tf32(v) in half 0 and lo = tf32(v - hi) in half 1
     int4 copy[kWgMaxCopies];   // per input copy: rh, rw, r
     int blocked, Px, Pg;       // batch-blocked frames: positions per image group of xc and of gf
-    long long g_tiles, x_tiles;   // blocks of the batch-blocked pack (kWgPackTile positions of one channel)
+    long long g_tiles, x_tiles;   // blocks of the batch-blocked pack (kWgPackTile positions of kWgPackCh channels)
 };
 
 struct WgradMainParams {

@@ -644,29 +644,35 @@ __global__ void __launch_bounds__(256) wgrad_pack_kernel(const __grid_constant__
     }
 }
 
-// Batch-blocked frames: block b transposes kWgPackTile frame positions of one
-// channel for the 32 images of one group, gathered image by image (a warp
-// reads 32 consecutive positions of one image plane) into shared memory and
-// written position by position (a warp writes the 32 images of one position:
-// one 128-byte row).  Blocks [0, g_tiles) fill gf, the rest xc; channels
-// vary fastest, so neighbouring blocks write neighbouring rows.
+// Batch-blocked frames: block b transposes kWgPackTile frame positions of
+// kWgPackCh consecutive channels for the 32 images of one group, gathered
+// image by image (a warp reads 32 consecutive positions of one image plane)
+// into shared memory and written position by position (a warp writes the 32
+// images of one position and channel: one 128-byte row; the block's channels
+// are adjacent rows).  Blocks [0, g_tiles) fill gf, the rest xc; channel
+// blocks vary fastest, so neighbouring blocks write neighbouring rows.  The
+// block's decode and each thread's position arithmetic are shared by its
+// channels, and all of a thread's loads are issued before the first store.
 __global__ void __launch_bounds__(256) wgrad_pack_blocked_kernel(const __grid_constant__ WgradPackParams p) {
     dev::grid_launch_dependents();   // as wgrad_pack_kernel
-    __shared__ float tile[kWgPackTile][33];
+    __shared__ float tile[kWgPackCh][kWgPackTile][33];
     const int b = static_cast<int>(blockIdx.x);   // the host keeps the block count below 2^31
     const bool is_g = b < p.g_tiles;
     const int bl = is_g ? b : b - static_cast<int>(p.g_tiles);
     const int C = is_g ? p.Co : p.Ci;
     const int P = is_g ? p.Pg : p.Px;
     const int ntile = (P + kWgPackTile - 1) / kWgPackTile;
-    const int ch = bl % C;
-    int rest = bl / C;
+    const int ncb = (C + kWgPackCh - 1) / kWgPackCh;
+    const int cb = bl % ncb;
+    int rest = bl / ncb;
     const int pt = rest % ntile;
     rest /= ntile;
     const int q = rest % p.Q;
     const int c = rest / p.Q;   // input copy (xc only)
     const int p0 = pt * kWgPackTile;
-    // gather: thread t reads position p0 + (t & 63) of images (t >> 6) + 4e
+    const int ch0 = cb * kWgPackCh;
+    const int nch = min(kWgPackCh, C - ch0);
+    // gather: thread t reads position p0 + (t & 63) of images (t >> 6) + 4e, for each channel
     {
         const int pp = threadIdx.x & (kWgPackTile - 1);
         const int pos = p0 + pp;
@@ -676,36 +682,42 @@ __global__ void __launch_bounds__(256) wgrad_pack_blocked_kernel(const __grid_co
         size_t img_stride;
         if (is_g) {
             ih = y, iw = u, hh = p.oH, ww = p.oW;
-            base = p.go + static_cast<size_t>(ch) * p.oH * p.oW;
+            base = p.go + static_cast<size_t>(ch0) * p.oH * p.oW;
             img_stride = static_cast<size_t>(p.Co) * p.oH * p.oW;
         } else {
             const int4 cp = p.copy[c];
             ih = p.s * (y - p.Ty) + cp.x, iw = p.s * (u - p.Tu) + cp.y, hh = p.H, ww = p.W;
-            base = p.x + static_cast<size_t>(ch) * p.H * p.W;
+            base = p.x + static_cast<size_t>(ch0) * p.H * p.W;
             img_stride = static_cast<size_t>(p.Ci) * p.H * p.W;
         }
+        const size_t plane = static_cast<size_t>(hh) * ww;
         const bool ok = pos < P && ih >= 0 && ih < hh && iw >= 0 && iw < ww;
         const int jt = threadIdx.x >> 6;
         const int n_ok = p.N - q * 32;   // images of this group that exist
         const float *src = base + (ok ? static_cast<size_t>(ih) * ww + iw : 0) + static_cast<size_t>(q * 32 + jt) * img_stride;
         const size_t step = 4 * img_stride;
-        float v[8];
+        float v[kWgPackCh][8];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) v[e] = (ok && jt + 4 * e < n_ok) ? __ldg(src + e * step) : 0.f;
+        for (int k = 0; k < kWgPackCh; ++k)
 #pragma unroll
-        for (int e = 0; e < 8; ++e) tile[pp][jt + 4 * e] = v[e];
+            for (int e = 0; e < 8; ++e)
+                v[k][e] = (ok && k < nch && jt + 4 * e < n_ok) ? __ldg(src + k * plane + e * step) : 0.f;
+#pragma unroll
+        for (int k = 0; k < kWgPackCh; ++k)
+#pragma unroll
+            for (int e = 0; e < 8; ++e) tile[k][pp][jt + 4 * e] = v[k][e];
     }
     __syncthreads();
-    // write: thread t writes images 4*(t & 7) .. +3 of positions p0 + (t >> 3) + 32e (one 16-byte store each;
-    // eight threads write one position's 128-byte row)
+    // write: thread t writes images 4*(t & 7) .. +3 of positions p0 + (t >> 3) + 32e, each channel (one 16-byte
+    // store each; eight threads write one 128-byte row)
     const int j4 = (threadIdx.x & 7) * 4;
     float *dst;
     size_t half;
     if (is_g) {
-        dst = p.gf + (static_cast<size_t>(q) * p.Pg * C + ch) * 32 + j4;
+        dst = p.gf + (static_cast<size_t>(q) * p.Pg * C + ch0) * 32 + j4;
         half = static_cast<size_t>(p.g4) * 4;
     } else {
-        dst = p.xc + ((static_cast<size_t>(c) * p.Q + q) * p.Px * C + ch) * 32 + j4;
+        dst = p.xc + ((static_cast<size_t>(c) * p.Q + q) * p.Px * C + ch0) * 32 + j4;
         half = static_cast<size_t>(p.x4) * 4;
     }
     const size_t row = static_cast<size_t>(C) * 32;   // floats between consecutive positions
@@ -713,15 +725,19 @@ __global__ void __launch_bounds__(256) wgrad_pack_blocked_kernel(const __grid_co
     for (int e = 0; e < kWgPackTile / 32; ++e) {
         const int pp = (threadIdx.x >> 3) + 32 * e;
         if (p0 + pp >= P) break;
-        const float4 v = make_float4(tile[pp][j4], tile[pp][j4 + 1], tile[pp][j4 + 2], tile[pp][j4 + 3]);
-        const float4 hi = make_float4(dev::round_tf32(v.x), dev::round_tf32(v.y), dev::round_tf32(v.z),
-                                      dev::round_tf32(v.w));
         float *d = dst + static_cast<size_t>(p0 + pp) * row;
-        *reinterpret_cast<float4 *>(d) = hi;
-        if (p.split)
-            *reinterpret_cast<float4 *>(d + half) =
-                make_float4(dev::round_tf32(v.x - hi.x), dev::round_tf32(v.y - hi.y), dev::round_tf32(v.z - hi.z),
-                            dev::round_tf32(v.w - hi.w));
+#pragma unroll
+        for (int k = 0; k < kWgPackCh; ++k) {
+            if (k >= nch) break;
+            const float4 v = make_float4(tile[k][pp][j4], tile[k][pp][j4 + 1], tile[k][pp][j4 + 2], tile[k][pp][j4 + 3]);
+            const float4 hi = make_float4(dev::round_tf32(v.x), dev::round_tf32(v.y), dev::round_tf32(v.z),
+                                          dev::round_tf32(v.w));
+            *reinterpret_cast<float4 *>(d + k * 32) = hi;
+            if (p.split)
+                *reinterpret_cast<float4 *>(d + k * 32 + half) =
+                    make_float4(dev::round_tf32(v.x - hi.x), dev::round_tf32(v.y - hi.y),
+                                dev::round_tf32(v.z - hi.z), dev::round_tf32(v.w - hi.w));
+        }
     }
 }
 
