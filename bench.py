@@ -13,7 +13,7 @@ dgrad_pack_grad_out) for the roofline line.
   python bench.py --impl reference ...   # the CPU oracle on the host cores
   python bench.py --all ...              # plus one info line per workload and precision, and per workload
                                          # the weight gradient (wgrad_run) of the same convolution
-  python bench.py --profile [--op wgrad] # W + K steps only, for ncu
+  python bench.py --profile [--op wgrad] [--path col2im]   # W + K steps only, for ncu
 
 With N > 1 (torchrun, one rank per GPU) every rank runs an independent
 replica of the workload (the batch shards with no collective on the data
@@ -51,6 +51,66 @@ def load_peaks():
     return dict(FALLBACK), "fallback"
 
 
+_LIVE_PEAKS = {}
+
+
+def measure_peaks(torch, dg):
+    """The two compute peaks the driver does not measure, measured here once
+    per process on this GPU (timing only; no clock or power setting changes):
+      * TF32 dense: torch.matmul of two fp32 8192 x 8192 matrices with TF32
+        allowed (cuBLAS on the tensor cores), 2*8192^3 FLOP, best of 10 by
+        CUDA events after warm-up -- the same method as the driver's bf16 peak;
+      * FP32 FFMA: dgrad_probe_ffma (eight independent FMA chains per thread,
+        8 blocks of 256 threads per SM over every SM of the device), best of 5.
+    Returns {"tf32_tflops", "ffma_tflops", "sm_count", "ffma_nominal_tflops"}."""
+    if _LIVE_PEAKS:
+        return _LIVE_PEAKS
+    import ctypes
+    props = torch.cuda.get_device_properties(torch.cuda.current_device())
+    sms = props.multi_processor_count
+    stream = torch.cuda.current_stream()
+    prev = torch.backends.cuda.matmul.allow_tf32
+    torch.backends.cuda.matmul.allow_tf32 = True
+    try:
+        n = 8192
+        g = torch.Generator(device="cuda").manual_seed(0)
+        a = torch.randn((n, n), device="cuda", generator=g)
+        b = torch.randn((n, n), device="cuda", generator=g)
+        for _ in range(3):
+            torch.matmul(a, b)
+        best = float("inf")
+        for _ in range(10):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            torch.matmul(a, b)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            best = min(best, e0.elapsed_time(e1) * 1e-3)
+        tf32 = 2.0 * n ** 3 / best / 1e12
+        del a, b
+    finally:
+        torch.backends.cuda.matmul.allow_tf32 = prev
+    lib = dg.load_library()
+    blocks, iters = sms * 8, 20000
+    out = torch.empty(blocks * 256, device="cuda")
+    h = ctypes.c_void_p(int(stream.cuda_stream))
+    for _ in range(2):
+        assert lib.dgrad_probe_ffma(blocks, iters, ctypes.c_void_p(out.data_ptr()), h) == 0
+    best = float("inf")
+    for _ in range(5):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        assert lib.dgrad_probe_ffma(blocks, iters, ctypes.c_void_p(out.data_ptr()), h) == 0
+        e1.record(stream)
+        torch.cuda.synchronize()
+        best = min(best, e0.elapsed_time(e1) * 1e-3)
+    ffma = 2.0 * blocks * 256 * 8 * iters / best / 1e12
+    peaks, _ = load_peaks()
+    _LIVE_PEAKS.update({"tf32_tflops": tf32, "ffma_tflops": ffma, "sm_count": sms,
+                        "ffma_nominal_tflops": sms * 256 * peaks.get("sm_max_mhz", 2070.0) * 1e6 / 1e12})
+    return _LIVE_PEAKS
+
+
 def kernel_source_hash():
     h = hashlib.sha256()
     for name in MAIN_KERNEL_SOURCES:
@@ -59,9 +119,11 @@ def kernel_source_hash():
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(workload, precision):
-    """DRAM bytes per launch of the main kernel from the committed ncu summary,
-    only while the kernel sources are unchanged since the capture."""
+def recorded_traffic_entry(workload, precision):
+    """The main kernel's ncu counters per launch from the committed summary
+    (DRAM read + write bytes; bytes the SMs wrote into L2, which the DRAM
+    counters miss while the writes stay in L2), only while the kernel sources
+    are unchanged since the capture."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
@@ -70,7 +132,7 @@ def recorded_traffic(workload, precision):
     e = rec.get(f"{workload}/{precision}")
     if not e or e.get("source_hash") != kernel_source_hash():
         return None
-    return e.get("dram_bytes_per_launch")
+    return e
 
 
 class ClockSampler:
@@ -265,20 +327,26 @@ def time_workload(dg, torch, wl, precision, steps, warmup, rank, barrier, device
             "bytes": info["algorithmic_bytes"], "steps": steps}
 
 
-def roofline(wl, precision, flops, nbytes, main_s, step_s):
+def roofline(wl, precision, flops, nbytes, main_s, step_s, live):
+    """Roofline of the main kernel.  `live` = measure_peaks(): the TF32 and
+    FFMA peaks measured in this run on this GPU; HBM bandwidth from
+    MEASURED_PEAKS.json (driver-measured).  The nominal-ratio TF32 figure
+    (measured bf16 burst x 1.1/2.25) is reported beside the measured one."""
     peaks, src = load_peaks()
     hbm = peaks["hbm_gbs"]
+    nominal_tf32 = peaks["bf16_tflops"] * TF32_OVER_BF16
     if precision == "tf32":
-        peak_tf = peaks["bf16_tflops"] * TF32_OVER_BF16
-        note = f"TF32 = {src} bf16 burst {peaks['bf16_tflops']} TFLOP/s x nominal 1.1/2.25"
+        peak_tf, alt = live["tf32_tflops"], nominal_tf32
+        note = ("TF32 measured in this run: cuBLAS fp32 matmul 8192^3 with TF32, best of 10; "
+                f"alt = {src} bf16 burst {peaks['bf16_tflops']} TFLOP/s x nominal 1.1/2.25")
     elif precision == "tf32x3":
         # three TF32 MMAs (hi*lo, lo*hi, hi*hi) per useful product
-        peak_tf = peaks["bf16_tflops"] * TF32_OVER_BF16 / 3
-        note = f"TF32X3 = {src} bf16 burst {peaks['bf16_tflops']} TFLOP/s x nominal 1.1/2.25 / 3 MMAs per product"
+        peak_tf, alt = live["tf32_tflops"] / 3, nominal_tf32 / 3
+        note = "TF32X3 = the TF32 peak measured in this run / 3 MMAs per useful product; alt = nominal-ratio TF32 / 3"
     else:
-        # FP32 FFMA: 148 SMs x 128 FMA/clk x 2 FLOP at the maximum SM clock.
-        peak_tf = 148 * 128 * 2 * peaks.get("sm_max_mhz", 2070.0) * 1e6 / 1e12
-        note = "FP32 FFMA = 148 SMs x 256 FLOP/clk x max SM clock"
+        peak_tf, alt = live["ffma_tflops"], live["ffma_nominal_tflops"]
+        note = (f"FP32 FFMA measured in this run: dgrad_probe_ffma over all {live['sm_count']} SMs, best of 5; "
+                f"alt = {live['sm_count']} SMs x 256 FLOP/clk x max SM clock")
     t_flop = flops / (peak_tf * 1e12)
     t_hbm = nbytes / (hbm * 1e9)
     if t_flop >= t_hbm:
@@ -286,11 +354,14 @@ def roofline(wl, precision, flops, nbytes, main_s, step_s):
     else:
         bound = "hbm"
     achieved = flops / main_s / 1e12
+    rec = recorded_traffic_entry(wl.name, precision)
     return {
         "bound": bound, "achieved": achieved, "peak": peak_tf, "unit": "TFLOP/s", "frac": achieved / peak_tf,
-        "traffic": recorded_traffic(wl.name, precision),
+        "traffic": rec.get("dram_bytes_per_launch") if rec else None,
+        "traffic_l2_write": rec.get("l2_write_bytes_per_launch") if rec else None,
         "kernel": "simt_dgrad_kernel" if precision == "fp32" else "tc_dgrad_kernel",
-        "peak_source": f"{note} ({src}); HBM {hbm} GB/s ({src})",
+        "peak_source": f"{note}; HBM {hbm} GB/s ({src})",
+        "peak_alt": alt, "frac_alt": achieved / alt,
         "roofline_us": max(t_flop, t_hbm) * 1e6,
         "frac_of_roofline_step": max(t_flop, t_hbm) / step_s,
         "frac_of_roofline_kernel": max(t_flop, t_hbm) / main_s,
@@ -324,8 +395,9 @@ def build_line(args, wl, r, world):
         "config": {**wl_config(wl), "precision": args.precision, "parallelism": f"replicas x{world}",
                    "l2": "flushed (256 MiB write) before every timed step",
                    "step": "pack kernel (weights + grad_out frame) + main kernel (C ABI dgrad_run)"},
-        "roofline": roofline(wl, args.precision, flops, nbytes, main_s, step_s),
+        "roofline": roofline(wl, args.precision, flops, nbytes, main_s, step_s, r["peaks"]),
         "main_kernel_us": r["main_ms"] * 1e3, "pack_stages_us": r["prepack_ms"] * 1e3,
+        "peaks_measured": {k: r["peaks"][k] for k in ("tf32_tflops", "ffma_tflops", "sm_count")},
         "gpu_launches": 2 * r["steps"],
         "plan": {k: r["plan"][k] for k in ("path", "tile_blocks", "slice_n", "chunk_k", "n_chunks", "grid",
                                            "n_work", "b_resident", "smem_bytes", "tmem_cols")},
@@ -386,7 +458,7 @@ def profile_steps(dg, torch, wl, args):
                               "plan": plan.info}), flush=True)
         return 0
     gi = torch.empty(wl.gi_shape, device="cuda")
-    with dg.Plan(*wl.plan_args(), precision=args.precision) as plan:
+    with dg.Plan(*wl.plan_args(), precision=args.precision, path=args.path) as plan:
         for _ in range(args.warmup + args.steps):
             flush.zero_()
             plan.run(go, w, gi)
@@ -409,6 +481,8 @@ def main():
     ap.add_argument("--all", action="store_true", help="also print one info line per workload and precision")
     ap.add_argument("--op", default="dgrad", choices=["dgrad", "wgrad"],
                     help="with --profile: which operation's kernels run")
+    ap.add_argument("--path", default="auto", choices=["auto", "simt", "tcgen05", "col2im"],
+                    help="with --profile: the dgrad kernel family (auto: the plan's own choice)")
     ap.add_argument("--profile", action="store_true",
                     help="only run W + K steps (for ncu captures: few launches, no extra timing loops)")
     args = ap.parse_args()
@@ -438,6 +512,7 @@ def main():
 
     r = time_workload(dg, torch, wl, args.precision, args.steps, args.warmup, rank, barrier, local,
                       clocks=True, e2e=True)
+    r["peaks"] = measure_peaks(torch, dg)   # after the timed region: it does not heat the GPU before it
     if world > 1:
         slowest_rank(torch, dist, r, "cuda")
 
@@ -456,7 +531,7 @@ def main():
                     x = time_workload(dg, torch, WORKLOADS[name], prec, 10 if prec == "fp32" else 50, 5, rank,
                                       lambda: None, local, clocks=False, e2e=False)
                     rf = roofline(WORKLOADS[name], prec, x["flops"], x["bytes"], x["main_ms"] * 1e-3,
-                                  x["ms_per_step"] * 1e-3)
+                                  x["ms_per_step"] * 1e-3, r["peaks"])
                     print(json.dumps({"info": "workload", "workload": name, "precision": prec,
                                       **{k: x[k] for k in ("ms_per_step", "main_ms", "prepack_ms")},
                                       "tflops": x["flops"] / (x["ms_per_step"] * 1e-3) / 1e12,
@@ -470,14 +545,13 @@ def main():
             x = time_workload(dg, torch, WORKLOADS["stem"], "tf32", 50, 5, rank, lambda: None, local, clocks=False,
                               e2e=False, path="col2im")
             rf = roofline(WORKLOADS["stem"], "tf32", x["flops"], x["bytes"], x["main_ms"] * 1e-3,
-                          x["ms_per_step"] * 1e-3)
+                          x["ms_per_step"] * 1e-3, r["peaks"])
             print(json.dumps({"info": "workload", "workload": "stem", "precision": "tf32", "path": "col2im",
                               **{k: x[k] for k in ("ms_per_step", "main_ms", "prepack_ms")},
                               "tflops": x["flops"] / (x["ms_per_step"] * 1e-3) / 1e12,
                               "main_tflops": rf["achieved"], "frac_peak": rf["frac"],
                               "frac_of_roofline_kernel": rf["frac_of_roofline_kernel"]}), flush=True)
-            peaks, src = load_peaks()
-            tf32_peak = peaks["bf16_tflops"] * TF32_OVER_BF16
+            tf32_peak = r["peaks"]["tf32_tflops"]
             for name, prec in [(n, p) for p in ("tf32", "tf32x3") for n in WORKLOAD_ORDER]:
                 x = time_wgrad(dg, torch, WORKLOADS[name], 50, 5, prec)
                 tf = x["flops"] / (x["ms_per_step"] * 1e-3) / 1e12

@@ -31,13 +31,14 @@ EXPORTS = ("dgrad_plan", "dgrad_plan_ex", "dgrad_describe", "dgrad_describe_taps
            "dgrad_run_fused", "dgrad_prepack", "dgrad_run_packed", "dgrad_pack_grad_out", "dgrad_run_main", "dgrad_run_host", "dgrad_run_noalloc", "dgrad_plan_check",
            "dgrad_plan_destroy", "dgrad_status_string", "dgrad_cuda_error_string",
            "wgrad_describe", "wgrad_describe_taps", "wgrad_describe_run", "wgrad_plan", "wgrad_plan_info",
-           "wgrad_run", "wgrad_plan_check", "wgrad_plan_destroy")
+           "wgrad_run", "wgrad_plan_check", "wgrad_plan_destroy", "dgrad_probe_ffma")
 
 
 class Options(ctypes.Structure):
     _fields_ = [("path", ctypes.c_int), ("tile_blocks", ctypes.c_int), ("slice_n", ctypes.c_int),
                 ("chunk_k", ctypes.c_int), ("grid", ctypes.c_int), ("sm_count", ctypes.c_int),
-                ("a_source", ctypes.c_int), ("group_taps", ctypes.c_int), ("b_stages", ctypes.c_int)]
+                ("a_source", ctypes.c_int), ("group_taps", ctypes.c_int), ("b_stages", ctypes.c_int),
+                ("timeout_us", ctypes.c_int), ("wait_test", ctypes.c_int)]
 
 
 class WgradPlanInfo(ctypes.Structure):
@@ -134,6 +135,8 @@ def load_library(path: str | None = None):
         lib.wgrad_plan_check.argtypes = [vp]
         lib.wgrad_plan_destroy.argtypes = [vp]
         lib.wgrad_plan_destroy.restype = None
+        lib.dgrad_probe_ffma.argtypes = [i, i, p, vp]
+        lib.dgrad_probe_ffma.restype = i
         for f in ("wgrad_describe", "wgrad_describe_taps", "wgrad_plan", "wgrad_plan_info", "wgrad_run",
                   "wgrad_plan_check"):
             getattr(lib, f).restype = i
@@ -153,10 +156,11 @@ GROUP_TAPS = {"auto": 0, "on": 1, "rows": 1, "off": 2, "phases": 3}
 
 
 def _options(path="auto", tile_blocks=0, slice_n=0, chunk_k=0, grid=0, sm_count=0, a_source="auto",
-             group_taps="auto", b_stages=0):
+             group_taps="auto", b_stages=0, timeout_us=0, wait_test=0):
     return Options(PATH[path] if isinstance(path, str) else int(path), tile_blocks, slice_n, chunk_k, grid,
                    sm_count, A_SOURCE[a_source] if isinstance(a_source, str) else int(a_source),
-                   GROUP_TAPS[group_taps] if isinstance(group_taps, str) else int(group_taps), int(b_stages))
+                   GROUP_TAPS[group_taps] if isinstance(group_taps, str) else int(group_taps), int(b_stages),
+                   int(timeout_us), int(wait_test))
 
 
 def describe(N, Ci, H, W, Co, kH, kW, stride, pad_h, pad_w, precision="tf32", **opts) -> dict:

@@ -132,14 +132,16 @@ void fill_params(dgrad_plan_s *pl) {
     dgrad::fill_main_params(g, t, round, &pl->mp);
     pl->mp.wp = pl->wp;
     pl->mp.err = pl->err;
-    pl->mp.timeout_ns = kTimeoutNs;
+    const long long tmo = pl->opts.timeout_us > 0 ? 1000LL * pl->opts.timeout_us : kTimeoutNs;
+    pl->mp.timeout_ns = tmo;
+    pl->mp.wait_test = pl->opts.wait_test ? 1 : 0;
     dgrad::fill_prepack_params(g, t, round, &pl->pp);
     pl->pp.wp = pl->wp;
     if (t.path == DGRAD_PATH_COL2IM) {
         dgrad::fill_c2i_params(g, t, &pl->cp);
         pl->cp.wp = pl->wp;
         pl->cp.err = pl->err;
-        pl->cp.timeout_ns = kTimeoutNs;
+        pl->cp.timeout_ns = tmo;
     }
 
     dgrad::FramePackParams &f = pl->fp;
@@ -290,7 +292,7 @@ dgrad_status_t dgrad_describe(int N, int Ci, int H, int W, int Co, int kH, int k
     if (!info) return DGRAD_ERR_INVALID_ARG;
     Geometry g;
     Tiling t;
-    int sms = (opts && opts->sm_count > 0) ? opts->sm_count : 148;
+    int sms = (opts && opts->sm_count > 0) ? opts->sm_count : 152;
     dgrad_status_t st = plan_host(N, Ci, H, W, Co, kH, kW, stride, pad_h, pad_w, precision, opts, sms, &g, &t);
     if (st != DGRAD_OK) return st;
     fill_info(g, t, precision, t.packed_bytes + 256, info);

@@ -248,6 +248,7 @@ struct MainParams {
     int n_phases, n_taps;
     uint32_t idesc;
     long long timeout_ns;
+    int wait_test;      // failure-detection test: the MMA warp first waits on a barrier nothing completes
     int tile_step;      // output positions per tile
     int grouped;
     int max_sub;        // largest sub-accumulator count of a phase

@@ -469,7 +469,7 @@ dgrad_status_t choose_tiling(const Geometry &g, int precision, const dgrad_optio
                              int sm_count, Tiling *out) {
     dgrad_options_t o{};
     if (opts) o = *opts;
-    if (sm_count < 1) sm_count = 148;
+    if (sm_count < 1) sm_count = 152;
     int path = o.path;
     const bool split = precision == DGRAD_PREC_TF32X3;
     if (path == DGRAD_PATH_AUTO) path = (precision == DGRAD_PREC_FP32) ? DGRAD_PATH_SIMT : DGRAD_PATH_TCGEN05;

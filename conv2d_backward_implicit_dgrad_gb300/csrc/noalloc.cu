@@ -6,7 +6,15 @@
 // kNoAllocScratchBytes for the life of the process.  Host code never uses
 // the array's name as a device pointer: on the first call on a device, with
 // that device current, cudaGetSymbolAddress gives the array's device address,
-// which is cached per device and handed to the kernels.
+// which is cached per device and handed to the kernels.  The cache does not
+// survive a reset of the device (cudaDeviceReset, or the primary context
+// being released and made again): the library's module is then loaded anew
+// and the cached address is stale, so no call may follow such a reset in the
+// same process.
+//
+// Every CUDA failure goes through dgrad::cuda_status, as in dgrad_run: the
+// error is recorded for dgrad_cuda_error_string and the runtime's last error
+// is cleared.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -31,11 +39,9 @@ dgrad_status_t scratch_address(int dev, unsigned char **out) {
     std::lock_guard<std::mutex> lock(g_setup_mutex);
     if (!g_scratch_addr[dev]) {
         void *p = nullptr;
-        cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-        if (e != cudaSuccess || p == nullptr) {
-            cudaGetLastError();
-            return DGRAD_ERR_CUDA;
-        }
+        const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess) return dgrad::cuda_status(e);
+        if (p == nullptr) return DGRAD_ERR_CUDA;
         g_scratch_addr[dev] = p;
     }
     *out = static_cast<unsigned char *>(g_scratch_addr[dev]);
@@ -94,8 +100,9 @@ extern "C" dgrad_status_t dgrad_run_noalloc(int N, int Ci, int H, int W, int Co,
 
     // The array keeps whatever the previous call left: the error word must
     // start at zero; the packed weights are rewritten in full below.
-    if (cudaMemsetAsync(err, 0, sizeof(uint32_t), s) != cudaSuccess) return DGRAD_ERR_CUDA;
-    if (g.n_taps == 0) return cudaMemsetAsync(grad_input, 0, gi_b, s) == cudaSuccess ? DGRAD_OK : DGRAD_ERR_CUDA;
+    st = cuda_status(cudaMemsetAsync(err, 0, sizeof(uint32_t), s));
+    if (st != DGRAD_OK) return st;
+    if (g.n_taps == 0) return cuda_status(cudaMemsetAsync(grad_input, 0, gi_b, s));
 
     const int round = precision == DGRAD_PREC_TF32 ? 1 : 0;
     PrepackParams q;
@@ -108,7 +115,7 @@ extern "C" dgrad_status_t dgrad_run_noalloc(int N, int Ci, int H, int W, int Co,
     m.go = grad_out; m.wp = wp; m.gi = grad_input; m.err = err;
     m.timeout_ns = 1000000000LL;
 
-    if (launch_prepack(q, s) != cudaSuccess) return DGRAD_ERR_CUDA;
-    cudaError_t e = t.path == DGRAD_PATH_TCGEN05 ? launch_tc(m, t, s, true) : launch_simt(m, t, s);
-    return e == cudaSuccess ? DGRAD_OK : DGRAD_ERR_CUDA;
+    st = cuda_status(launch_prepack(q, s));
+    if (st != DGRAD_OK) return st;
+    return cuda_status(t.path == DGRAD_PATH_TCGEN05 ? launch_tc(m, t, s, true) : launch_simt(m, t, s));
 }

@@ -63,6 +63,7 @@ struct Barriers {
     uint64_t acc_full[2];
     uint64_t acc_empty[2];
     uint64_t drain;
+    uint64_t never;   // failure-detection test: a barrier that nothing completes
     uint32_t tmem_base;
     volatile int abort_flag;
 };
@@ -712,6 +713,7 @@ __global__ void __launch_bounds__(kernel_threads<kTmaA, kEG>(), 1)
             dev::mbar_init(dev::smem_u32(&bars->acc_empty[i]), kEpiWarps * 32);
         }
         dev::mbar_init(dev::smem_u32(&bars->drain), 1);
+        dev::mbar_init(dev::smem_u32(&bars->never), 1);
         bars->abort_flag = 0;
         dev::fence_mbar_init();
     }
@@ -828,6 +830,12 @@ __global__ void __launch_bounds__(kernel_threads<kTmaA, kEG>(), 1)
         Ring ra, rb, racc;
         bool ok = true;
         bool first_chunk = true;
+        // Failure-detection test: a bounded wait on a barrier that nothing
+        // completes runs out; the whole CTA then takes its abort path.
+        if (p.wait_test && !__all_sync(0xffffffffu, dev::mbar_wait(dev::smem_u32(&bars->never), 0, tmo))) {
+            if (lane == 0) fail(bars, p);
+            ok = false;
+        }
         for (int w = blockIdx.x; ok && w < p.n_work && !bars->abort_flag; w += gridDim.x, racc.next(p.acc_bufs)) {
             DGRAD_TRACE_CLOCK(tm0);
             if (!__all_sync(0xffffffffu,

@@ -174,7 +174,7 @@ dgrad_status_t make_wgrad_geometry(int N, int Ci, int H, int W, int Co, int kH, 
     if (nh < 0 || nw < 0) return DGRAD_ERR_INVALID_ARG;
     if (precision == DGRAD_PREC_FP32) return DGRAD_ERR_UNSUPPORTED;
     if (stride > kWgMaxRowPhases || (long long)kH * kW > kMaxTaps) return DGRAD_ERR_UNSUPPORTED;
-    if (sm_count < 1) sm_count = 148;
+    if (sm_count < 1) sm_count = 152;
     WgradGeometry g;
     std::memset(&g, 0, sizeof(g));
     g.N = N; g.Ci = Ci; g.H = H; g.W = W; g.Co = Co; g.kH = kH; g.kW = kW;

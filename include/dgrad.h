@@ -113,6 +113,13 @@ typedef struct {
                           same frame shift (stride > 1; DGRAD_ERR_UNSUPPORTED when not possible) */
     int b_stages;      /* tcgen05 path, packed-weight pipeline: 0 automatic, 2..8 stream the weights
                           through that many shared-memory stages (never resident) */
+    int timeout_us;    /* limit of every bounded in-kernel wait, in microseconds (0: one second) */
+    int wait_test;     /* failure-detection test only, tcgen05 path: 1 makes the main
+                          kernel's MMA warp first wait on a barrier that nothing ever completes, so
+                          that this bounded wait runs out after timeout_us; the kernel then records
+                          DGRAD_ERR_DEVICE_TIMEOUT (read by dgrad_plan_check), lets its copies land,
+                          frees its tensor memory and exits with grad_input incomplete.  Nothing
+                          faults or traps.  0 for every real use. */
 } dgrad_options_t;
 
 /* Everything a plan decided, for tests, benchmarks and logs. */
@@ -157,7 +164,7 @@ dgrad_status_t dgrad_plan_ex(int N, int Ci, int H, int W, int Co, int kH, int kW
                              dgrad_plan_t *plan_out);
 
 /* Host-only: the decisions dgrad_plan_ex would take for opts->sm_count SMs
- * (148 if 0), without touching any device.  Fills *info. */
+ * (152, the GB300's SM count, if 0), without touching any device.  Fills *info. */
 dgrad_status_t dgrad_describe(int N, int Ci, int H, int W, int Co, int kH, int kW,
                               int stride, int pad_h, int pad_w,
                               dgrad_precision_t precision, const dgrad_options_t *opts,
@@ -260,13 +267,21 @@ dgrad_status_t dgrad_run_host(dgrad_plan_t plan, const float *grad_out_host,
  * DGRAD_ERR_UNSUPPORTED before anything is launched.  The first call on a
  * device looks up that array's device address (cudaGetSymbolAddress, with the
  * device current) and caches it; make that first call before any stream
- * capture.  Every call on a device shares the one array and it keeps the last
- * call's contents (each call clears the error word and rewrites the packed
- * weights), so calls whose kernels can overlap on the GPU (different streams
- * or threads) race and give wrong results: serialise them.  In-kernel wait
- * timeouts are not reported here (use a plan and dgrad_plan_check for that).
- * Pointer rules, layouts, stream semantics and the other errors are those of
- * dgrad_run; tiles are chosen as dgrad_plan would choose them. */
+ * capture.  The cached address does not survive a reset of the device
+ * (cudaDeviceReset, or the primary context released and made again): do not
+ * call this function again in a process after such a reset.  Every call on a
+ * device shares the one array and it keeps the last call's contents (each
+ * call clears the error word and rewrites the packed weights), so calls whose
+ * kernels can overlap on the GPU (different streams or threads) race and give
+ * wrong results: serialise them.  In-kernel wait timeouts are recorded in the
+ * array, which no caller can read: they are not reported (use a plan and
+ * dgrad_plan_check where that matters).  Pointer rules, layouts, stream
+ * semantics and the other errors are those of dgrad_run, and a DGRAD_ERR_CUDA
+ * is explained by dgrad_cuda_error_string as there.  There is no frame
+ * buffer, so grad_out reaches the tensor cores through producer warps: the
+ * tiles are those dgrad_plan_ex would choose with a_source = 2, which can
+ * differ from dgrad_plan's own choice (and run slower) where a plan would
+ * use the packed frame. */
 dgrad_status_t dgrad_run_noalloc(int N, int Ci, int H, int W, int Co, int kH, int kW,
                                  int stride, int pad_h, int pad_w, dgrad_precision_t precision,
                                  const float *grad_out, const float *weight, float *grad_input,

@@ -78,7 +78,7 @@ typedef struct {
 } wgrad_plan_info_t;
 
 /* Host-only planning (no device, no allocation): what wgrad_plan would
- * decide for this shape on `sm_count` SMs (0: 148). */
+ * decide for this shape on `sm_count` SMs (0: 152). */
 dgrad_status_t wgrad_describe(int N, int Ci, int H, int W, int Co, int kH, int kW, int stride, int pad_h,
                               int pad_w, dgrad_precision_t precision, int sm_count, wgrad_plan_info_t *info);
 

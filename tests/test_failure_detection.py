@@ -1,0 +1,85 @@
+"""Failure detection on the GPU without a fault: a bounded in-kernel wait that
+runs out is reported, and the CUDA context stays usable.
+
+The main kernel bounds every wait on an mbarrier (tensor copies, MMA
+completion, the epilogue's accumulator hand-off) by a time limit; when one
+runs out the CTA records DGRAD_ERR_DEVICE_TIMEOUT in the plan's device error
+word, lets its copies land, frees its tensor memory and exits.  The plan
+option ``wait_test=1`` makes the MMA warp first wait on a barrier that
+nothing completes, so that this path runs on purpose: nothing faults, traps
+or hangs, and the whole launch ends within a few multiples of the
+(here short) wait limit.  The pages' own error handling is the host-side
+argument checks of doppler's conv2d_backward.js / bias_add_backward.js,
+covered by the CPU tests; this file covers the device half.
+"""
+import time
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import conv2d_backward_implicit_dgrad_gb300 as dg
+from conv2d_backward_implicit_dgrad_gb300.workloads import WORKLOADS, make_inputs
+
+pytestmark = pytest.mark.gpu
+
+TIMEOUT_STATUS = 7   # DGRAD_ERR_DEVICE_TIMEOUT
+SHORT_US = 2000      # wait limit of the stalled launches: 2 ms
+
+
+def assert_tf32(gpu, ref, mag):
+    assert np.isfinite(gpu).all()
+    assert np.all(np.abs(gpu - ref) <= 2e-3 * mag)
+
+
+@pytest.mark.parametrize("a_source", ["frame", "producers"])
+@pytest.mark.parametrize("name", ["tiny", "resnet_stage", "strided_downsample"])
+def test_wait_that_runs_out_is_reported_and_context_survives(name, a_source):
+    wl = WORKLOADS[name]
+    go_h, w_h = make_inputs(wl, 5)
+    go, w = go_h.cuda(), w_h.cuda()
+    with dg.Plan(*wl.plan_args(), precision="tf32", a_source=a_source, timeout_us=SHORT_US, wait_test=1) as plan:
+        gi = torch.full(wl.gi_shape, float("nan"), device="cuda")
+        t0 = time.perf_counter()
+        plan.run(go, w, gi)
+        torch.cuda.synchronize()   # the launch ends by itself: every wait is bounded
+        elapsed = time.perf_counter() - t0
+        with pytest.raises(dg.DgradError) as exc:
+            plan.check()
+        assert exc.value.status == TIMEOUT_STATUS
+        plan.check()   # reading the error word cleared it
+    # a handful of sequential 2 ms limits, not a hang (generous for a shared box)
+    assert elapsed < 5.0
+    # the context is intact: a normal plan on the same inputs is correct
+    ref, mag = oracle.dgrad(go_h, w_h, wl.H, wl.W, wl.stride, wl.pad_h, wl.pad_w)
+    with dg.Plan(*wl.plan_args(), precision="tf32", a_source=a_source) as plan:
+        out = plan.run(go, w)
+        torch.cuda.synchronize()
+        plan.check()
+    assert_tf32(out.cpu().double().numpy(), ref, mag)
+
+
+def test_short_wait_limit_alone_raises_nothing():
+    # A 50 ms limit is far above any wait of a normal launch: no false timeout.
+    wl = WORKLOADS["resnet_stage"]
+    go_h, w_h = make_inputs(wl, 6)
+    go, w = go_h.cuda(), w_h.cuda()
+    ref, mag = oracle.dgrad(go_h, w_h, wl.H, wl.W, wl.stride, wl.pad_h, wl.pad_w)
+    with dg.Plan(*wl.plan_args(), precision="tf32", timeout_us=50000) as plan:
+        for _ in range(3):
+            out = plan.run(go, w)
+        torch.cuda.synchronize()
+        plan.check()
+    assert_tf32(out.cpu().double().numpy(), ref, mag)
+
+
+def test_host_pipeline_reports_a_sub_plan_timeout():
+    # dgrad_run_host runs the batch through sub-plans and reads their error
+    # words behind its last copy: a stalled sub-plan surfaces as the call's status.
+    wl = WORKLOADS["tiny"]
+    go_h, w_h = make_inputs(wl, 7)
+    with dg.Plan(*wl.plan_args(), precision="tf32", timeout_us=SHORT_US, wait_test=1) as plan:
+        with pytest.raises(dg.DgradError) as exc:
+            plan.run_host(go_h.contiguous(), w_h.contiguous(), torch.empty(wl.gi_shape, pin_memory=True))
+        assert exc.value.status == TIMEOUT_STATUS

@@ -11,7 +11,9 @@ Bars (fixed by the tolerance the method is held to):
     fp32 additions add at most 2^-23 of the running sum each (truncating
     accumulation allowed for).
 grad_input is poisoned with NaN before every run, so an element the kernels
-fail to write fails both bars.
+fail to write fails both bars, and it sits between two guard bands of canary
+values that must come back unchanged, so a store past either end of it fails
+too.
 """
 import ctypes
 
@@ -33,14 +35,34 @@ def out_ext(n, k, s, p):
     return (n + 2 * p - k) // s + 1
 
 
+GUARD = 4096          # floats of canary on each side of an output tensor (16 KiB: keeps 16-byte alignment)
+CANARY = -1234.5625   # exactly representable, and no dgrad of these inputs produces it by chance
+
+
+def guarded(shape, fill=float("nan")):
+    """An output tensor in the middle of a larger buffer whose two ends hold
+    canary values; returns (buffer, tensor view)."""
+    n = int(np.prod(shape))
+    buf = torch.full((n + 2 * GUARD,), CANARY, device="cuda")
+    buf[GUARD:GUARD + n] = fill
+    return buf, buf[GUARD:GUARD + n].view(shape)
+
+
+def assert_guards(buf):
+    """Both guard bands still hold the canary: nothing was stored past either end."""
+    head, tail = buf[:GUARD].cpu(), buf[-GUARD:].cpu()
+    assert bool((head == CANARY).all()) and bool((tail == CANARY).all()), "a store landed outside grad_input"
+
+
 def run_gpu(args, go, w, precision, **opts):
     N, Ci, H, W, Co, kH, kW, s, ph, pw = args
     with dg.Plan(*args, precision=precision, **opts) as plan:
-        gi = torch.full((N, Ci, H, W), float("nan"), device="cuda")
+        buf, gi = guarded((N, Ci, H, W))
         plan.run(go.cuda(), w.cuda(), gi)
         torch.cuda.synchronize()
         plan.check()
         info = plan.info
+    assert_guards(buf)
     return gi.cpu().double().numpy(), info
 
 

@@ -37,8 +37,9 @@ def _fake_result(rank):
     nbytes = 4.0 * (wl.N * wl.Co * wl.oH * wl.oW + wl.Co * wl.Ci * wl.kH * wl.kW + wl.N * wl.Ci * wl.H * wl.W)
     plan = {k: 0 for k in ("path", "tile_blocks", "slice_n", "chunk_k", "n_chunks", "grid", "n_work",
                            "b_resident", "smem_bytes", "tmem_cols")}
+    peaks = {"tf32_tflops": 1000.0, "ffma_tflops": 70.0, "sm_count": 152, "ffma_nominal_tflops": 80.5}
     return wl, {**_rank_times(rank), "prepack_ms": 0.008, "fused_ms": 0.0, "clocks": None, "plan": plan,
-                "flops": flops, "bytes": nbytes, "steps": 5}
+                "flops": flops, "bytes": nbytes, "steps": 5, "peaks": peaks}
 
 
 def _worker(rank, world, port, queue):

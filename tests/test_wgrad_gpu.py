@@ -8,7 +8,8 @@ off by at most about 3 * 2^-22 of its size (the dropped lo*lo term and the
 rounding of lo), and the fp32 accumulation adds a few 2^-24 per addition of
 similar size, far below 1e-5 for the K lengths here.  grad_weight is
 poisoned with NaN before every run, so an element the kernels fail to write
-fails the bar.
+fails the bar, and it sits between two guard bands of canary values that must
+come back unchanged (no store past either end).
 """
 import ctypes
 
@@ -38,14 +39,23 @@ def inputs(N, Ci, Co, H, W, kH, kW, s, ph, pw, seed):
     return go, x
 
 
+GUARD = 4096          # floats of canary on each side of grad_weight (16 KiB: keeps 16-byte alignment)
+CANARY = -1234.5625
+
+
 def run_gpu(args, go, x, precision="tf32"):
     N, Ci, H, W, Co, kH, kW, s, ph, pw = args
+    n = Co * Ci * kH * kW
     with dg.WgradPlan(*args, precision=precision) as plan:
-        dw = torch.full((Co, Ci, kH, kW), float("nan"), device="cuda")
+        buf = torch.full((n + 2 * GUARD,), CANARY, device="cuda")
+        buf[GUARD:GUARD + n] = float("nan")
+        dw = buf[GUARD:GUARD + n].view((Co, Ci, kH, kW))
         plan.run(go.cuda(), x.cuda(), dw)
         torch.cuda.synchronize()
         plan.check()
         info = plan.info
+    head, tail = buf[:GUARD].cpu(), buf[-GUARD:].cpu()
+    assert bool((head == CANARY).all()) and bool((tail == CANARY).all()), "a store landed outside grad_weight"
     return dw.cpu().double().numpy(), info
 
 
