@@ -69,7 +69,8 @@ class PlanInfo(ctypes.Structure):
         ("tmem_cols", ctypes.c_int), ("group_taps", ctypes.c_int), ("tile_step", ctypes.c_int),
         ("a_stages", ctypes.c_int), ("b_stages", ctypes.c_int), ("workspace_bytes", ctypes.c_size_t),
         ("packed_weight_bytes", ctypes.c_size_t), ("useful_flops", ctypes.c_double),
-        ("algorithmic_bytes", ctypes.c_double)]
+        ("algorithmic_bytes", ctypes.c_double), ("band_rows", ctypes.c_int), ("stg_box", ctypes.c_int),
+        ("img_tiles", ctypes.c_int), ("a_rows", ctypes.c_int)]
 
     def as_dict(self):
         d = {name: getattr(self, name) for name, _ in self._fields_}
@@ -148,7 +149,7 @@ def load_library(path: str | None = None):
         return lib
 
 
-A_SOURCE = {"auto": 0, "frame": 1, "producers": 2}
+A_SOURCE = {"auto": 0, "frame": 1, "producers": 2, "staged": 3}
 A_SOURCE_NAME = {v: k for k, v in A_SOURCE.items()}
 
 

@@ -43,6 +43,10 @@ struct dgrad_plan_s {
     size_t workspace_bytes;
     int packed;            // dgrad_prepack (or dgrad_run) has run at least once
     int frame_packed;      // grad_out has been packed into the frame at least once
+    // staged A source: the tensor map of the caller's grad_out, encoded for
+    // the last pointer seen (re-encoded when the pointer changes)
+    const float *go_map_ptr;
+    CUtensorMap go_map;
 };
 
 // cuTensorMapEncodeTiled from the driver, looked up once through the
@@ -102,7 +106,8 @@ void fill_info(const Geometry &g, const Tiling &t, int precision, size_t ws, dgr
     info->n_work = t.n_work;
     info->grid = t.path == DGRAD_PATH_SIMT ? (int)t.n_work : t.grid;
     info->b_resident = t.b_resident;
-    info->a_source = t.path == DGRAD_PATH_TCGEN05 ? (t.a_tma ? 1 : 2) : (t.path == DGRAD_PATH_COL2IM ? 1 : 0);
+    info->a_source = t.path == DGRAD_PATH_TCGEN05 ? (t.a_staged ? 3 : t.a_tma ? 1 : 2)
+                                                  : (t.path == DGRAD_PATH_COL2IM ? 1 : 0);
     info->smem_bytes = t.smem_bytes;
     info->tmem_cols = t.tmem_cols;
     info->group_taps = t.grouped ? 1 : (t.pgroup ? 2 : 0);
@@ -113,6 +118,10 @@ void fill_info(const Geometry &g, const Tiling &t, int precision, size_t ws, dgr
     info->packed_weight_bytes = t.packed_bytes;
     info->useful_flops = 2.0 * g.N * g.Co * g.oH * g.oW * (double)g.Ci * g.kH * g.kW;
     info->algorithmic_bytes = 4.0 * ((double)go_elems(g) + (double)w_elems(g) + (double)gi_elems(g));
+    info->band_rows = t.band_rows;
+    info->stg_box = t.a_staged ? t.stg_box : 0;
+    info->img_tiles = t.img_tiles;
+    info->a_rows = t.a_rows;
 }
 
 dgrad_status_t plan_host(int N, int Ci, int H, int W, int Co, int kH, int kW, int stride, int pad_h,
@@ -181,6 +190,32 @@ dgrad_status_t encode_frame_map(dgrad_plan_s *pl) {
     return r == CUDA_SUCCESS ? DGRAD_OK : DGRAD_ERR_CUDA;
 }
 
+// Staged A source: grad_out viewed as [N][Co][oH*oW] (fp32), boxes of
+// stg_box plane elements x 32 channels x 1 image, no swizzle; channels past
+// Co and elements past the plane read as zeros.  Encoded on the caller's
+// pointer (16-byte aligned; the plane stride oH*oW*4 is a multiple of 16 for
+// every staged plan).
+dgrad_status_t encode_staged_map(dgrad_plan_s *pl, const float *grad_out) {
+    if (pl->go_map_ptr == grad_out) return DGRAD_OK;
+    auto fn = dgrad::tensor_map_encoder();
+    if (!fn) return DGRAD_ERR_CUDA;
+    const Geometry &g = pl->g;
+    const cuuint64_t plane = (cuuint64_t)g.oH * g.oW;
+    const cuuint64_t dims[3] = {plane, (cuuint64_t)g.Co, (cuuint64_t)g.N};
+    const cuuint64_t strides[2] = {plane * 4, plane * 4 * (cuuint64_t)g.Co};
+    const cuuint32_t box[3] = {(cuuint32_t)pl->t.stg_box, 32u, 1u};
+    const cuuint32_t es[3] = {1u, 1u, 1u};
+    CUresult r = fn(&pl->go_map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float *>(grad_out), dims, strides,
+                    box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        pl->go_map_ptr = nullptr;
+        return DGRAD_ERR_CUDA;
+    }
+    pl->go_map_ptr = grad_out;
+    return DGRAD_OK;
+}
+
 bool overlaps(const void *a, size_t abytes, const void *b, size_t bbytes) {
     uintptr_t a0 = (uintptr_t)a, a1 = a0 + abytes, b0 = (uintptr_t)b, b1 = b0 + bbytes;
     return a0 < b1 && b0 < a1;
@@ -222,6 +257,11 @@ dgrad_status_t launch_main_on(dgrad_plan_s *plan, const float *grad_out, float *
         cp.relu_in = relu_in;
         cp.accumulate = accumulate;
         return cuda_status(dgrad::launch_c2i(cp, plan->t, s, true));
+    }
+    if (plan->t.path == DGRAD_PATH_TCGEN05 && plan->t.a_staged) {
+        dgrad_status_t st = encode_staged_map(plan, grad_out);
+        if (st != DGRAD_OK) return st;
+        mp.a_map = plan->go_map;
     }
     cudaError_t e = plan->t.path == DGRAD_PATH_TCGEN05 ? dgrad::launch_tc(mp, plan->t, s, true)
                                                        : dgrad::launch_simt(mp, plan->t, s);
@@ -347,7 +387,8 @@ dgrad_status_t dgrad_plan_ex(int N, int Ci, int H, int W, int Co, int kH, int kW
     // Workspace: the error word (256 B), the packed weights, then (tensor-
     // copy mode) the packed grad_out frame, each 256-byte aligned.
     const size_t wp_bytes = (pl->t.packed_bytes + 255) & ~size_t(255);
-    const bool has_frame = (pl->t.path == DGRAD_PATH_TCGEN05 || pl->t.path == DGRAD_PATH_COL2IM) && pl->t.a_tma;
+    const bool has_frame =
+        (pl->t.path == DGRAD_PATH_TCGEN05 || pl->t.path == DGRAD_PATH_COL2IM) && pl->t.a_tma && !pl->t.a_staged;
     size_t ws = 256 + wp_bytes + (has_frame ? pl->t.frame_bytes : 0);
     void *mem = nullptr;
     if (cudaMalloc(&mem, ws) != cudaSuccess) {

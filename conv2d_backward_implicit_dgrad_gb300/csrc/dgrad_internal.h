@@ -137,7 +137,12 @@ struct Tiling {
     int xchg_bytes;    // shared memory for the epilogue's cross-warp row exchange
     int xchg_unit;     // 1: one exchange per unit (a single phase: every column published before one barrier)
     int epi_groups;    // epilogue warp groups taking alternate units (2 for grouped tensor-copy launches)
-    int a_tma;         // 1: A stages are tensor copies of the packed frame; 0: producer warps gather
+    int a_tma;         // 1: A stages are tensor copies (of the packed frame, or staged); 0: producer warps gather
+    int a_staged;      // 1: each A stage is one tensor copy of the caller's NCHW grad_out, transposed in place
+                       //    by two transposer warps (no frame, no grad_out pack)
+    int stg_box;       // staged: plane elements per copy (box width, a multiple of 4, <= 256)
+    int band_rows;     // frame rows an A stage must hold for the MMAs (tm*128 + the largest tap shift)
+    int img_tiles;     // tiles per image when tiles never cross an image (staged); 0: tiles run across images
     int a_box_rows;    // rows of one A tensor copy (<= 256)
     int a_nbox;        // tensor copies per A stage
     int co_v;          // channels per packed frame row
@@ -227,7 +232,8 @@ constexpr int kPackSegMax = 256;    // plane elements per pack block at most
 // (bit 31: first group of its phase), B offset inside the chunk's tap block
 // (bytes), instruction descriptor (N = ntaps * bn).
 struct MainParams {
-    CUtensorMap a_map;   // packed frame [positions][co_v], box 32 x a_box_rows, 128-byte swizzle
+    CUtensorMap a_map;   // packed frame [positions][co_v], box 32 x a_box_rows, 128-byte swizzle; staged:
+                         // grad_out as [N][Co][oH*oW], box stg_box x 32 x 1, no swizzle (encoded per call)
     const float *go;
     const float *wp;
     float *gi;
@@ -241,6 +247,8 @@ struct MainParams {
     int tap_group, n_tgroups;
     int vec_producer;   // 1: 16-byte quad loads + register transpose; 0: 4-byte asynchronous copies
     int a_tma, a_box_rows, a_nbox;
+    int a_staged, stg_box, band_rows, img_tiles;   // see Tiling
+    int prefetch_ahead; // staged: stages whose grad_out boxes are prefetched into L2 ahead of their copy
     int acc_bufs, acc_cols, tmem_cols;
     int round_tf32;
     int split_chunks;   // split precision: channel chunks of one K pass (n_chunks = 3 * split_chunks), else 0
@@ -299,7 +307,10 @@ struct C2iParams {
 void fill_c2i_params(const Geometry &g, const Tiling &t, C2iParams *c);
 cudaError_t launch_c2i(const C2iParams &p, const Tiling &t, cudaStream_t stream, bool pdl);
 cudaError_t launch_tc(const MainParams &p, const Tiling &t, cudaStream_t stream, bool pdl);
-// Tensor-copy mode with the fused epilogue (called by launch_tc).
+// Tensor-copy mode with the fused epilogue, and the staged mode (plain and
+// fused stores); called by launch_tc.
 cudaError_t launch_tc_fused(const MainParams &p, const Tiling &t, cudaStream_t stream, bool pdl);
+cudaError_t launch_tc_staged(const MainParams &p, const Tiling &t, cudaStream_t stream, bool pdl);
+cudaError_t launch_tc_staged_fused(const MainParams &p, const Tiling &t, cudaStream_t stream, bool pdl);
 
 }  // namespace dgrad

@@ -303,7 +303,19 @@ bool size_tc(const Geometry &g, Tiling &t, int want_resident) {
     t.xchg_bytes = max_sub > 1 ? t.epi_groups * 2 * 4 * (max_sub * (max_sub - 1) / 2) * (t.xchg_unit ? t.bn : 16) * 4
                                : 0;
     const int raw_rows = t.tm * kBlockM + g.max_shift;
-    if (t.a_tma) {   // tensor copies of at most 256 rows each
+    t.band_rows = raw_rows;
+    if (t.a_staged) {
+        // One tensor copy per A stage of the plane elements the band holds:
+        // at most one per frame row, plus up to 3 before them (the copy
+        // starts on a 16-byte boundary of the plane).  The copy lands in the
+        // stage itself (stg_box elements x 32 channels = stg_box 128-byte
+        // rows) and is transposed there.
+        t.stg_box = round_up(raw_rows + 3, 4);
+        if (t.tm != 1 || t.stg_box > 256) return false;
+        t.a_nbox = 1;
+        t.a_box_rows = 0;
+        t.a_rows = round_up(std::max(raw_rows, t.stg_box), 8);
+    } else if (t.a_tma) {   // tensor copies of at most 256 rows each
         t.a_nbox = ceil_div(raw_rows, 256);
         t.a_box_rows = round_up(ceil_div(raw_rows, t.a_nbox), 8);
         t.a_rows = t.a_nbox * t.a_box_rows;
@@ -362,7 +374,19 @@ bool size_tc(const Geometry &g, Tiling &t, int want_resident) {
     if (t.acc_cols > kTmemCols) return false;
     t.acc_bufs = (2 * t.acc_cols <= kTmemCols) ? 2 : 1;
     t.tmem_cols = pow2_at_least(t.acc_bufs * t.acc_cols);
-    t.n_tiles = (int)((g.positions + t.tile_step - 1) / t.tile_step);
+    if (t.a_staged) {
+        // Tiles never cross an image (a band is one copy from one image):
+        // each image's tiles cover its frame positions up to the last one
+        // that is an output of some phase.
+        int nq = 0, nu = 0;
+        for (int p = 0; p < g.n_phases; ++p) nq = std::max(nq, g.phase[p].Hq), nu = std::max(nu, g.phase[p].Wq);
+        const int out_span = (nq - 1) * g.Wp + nu;
+        t.img_tiles = ceil_div(out_span, t.tile_step);
+        t.n_tiles = g.N * t.img_tiles;
+    } else {
+        t.img_tiles = 0;
+        t.n_tiles = (int)((g.positions + t.tile_step - 1) / t.tile_step);
+    }
     t.n_work = (long long)t.n_tiles * t.n_slices;
     t.packed_bytes = (size_t)t.n_slices * t.n_chunks * (size_t)taps * (size_t)tap_bytes;
     return true;
@@ -541,7 +565,7 @@ dgrad_status_t choose_tiling(const Geometry &g, int precision, const dgrad_optio
     }
     // Operand rows are one 128-byte swizzle row: 32 output channels per chunk.
     if (o.chunk_k && o.chunk_k != 32) return DGRAD_ERR_INVALID_ARG;
-    if (o.a_source < 0 || o.a_source > 2) return DGRAD_ERR_INVALID_ARG;
+    if (o.a_source < 0 || o.a_source > 3) return DGRAD_ERR_INVALID_ARG;
     // grad_out reaches the MMA either as tensor copies of a packed,
     // channels-last frame, or through producer warps.  Split precision takes
     // the frame at any size: its rows carry the hi and lo halves, each padded
@@ -557,7 +581,23 @@ dgrad_status_t choose_tiling(const Geometry &g, int precision, const dgrad_optio
         t.a_tma = 0;
     else
         t.a_tma = t.frame_bytes <= kMaxFrameBytes ? 1 : 0;
-    if (t.a_tma && (long long)g.positions * t.co_v > INT_MAX) return DGRAD_ERR_UNSUPPORTED;
+    // Staged A source (no frame, no grad_out pack): each A stage is one
+    // tensor copy of grad_out viewed as [N][Co][oH*oW] (the plane stride
+    // must be a multiple of 16 bytes) holding the band's plane elements,
+    // which needs a band of at most 253 rows (one 128-row block).  Opt-in:
+    // measured slower than the frame on every workload (resnet_stage main
+    // kernel 50 us vs 25), because the in-place transposition's shared-
+    // memory reads and writes compete with the tensor core's operand reads
+    // for the shared-memory port.
+    const bool stg_ok = (long long)g.oH * g.oW % 4 == 0 && kBlockM + g.max_shift + 3 <= 256;
+    t.a_staged = 0;
+    if (o.a_source == 3) {
+        if (!stg_ok || o.tile_blocks > 1) return DGRAD_ERR_UNSUPPORTED;
+        t.a_tma = 1;
+        t.a_staged = 1;
+    }
+    if (t.a_staged) t.frame_bytes = 0;
+    if (t.a_tma && !t.a_staged && (long long)g.positions * t.co_v > INT_MAX) return DGRAD_ERR_UNSUPPORTED;
     if (!t.a_tma) t.frame_bytes = 0;
     // Grouping the taps of a kernel row into one MMA (N = taps x bn) cuts the
     // MMA time when bn alone leaves the MMA bound by its fixed cost of
@@ -597,7 +637,7 @@ dgrad_status_t choose_tiling(const Geometry &g, int precision, const dgrad_optio
                 Tiling c = t;
                 c.grouped = group_pref[gi][0];
                 c.pgroup = group_pref[gi][1];
-                c.tm = c.grouped ? 1 : tm_pref[i];
+                c.tm = (c.grouped || c.a_staged) ? 1 : tm_pref[i];
                 c.bn = bn;
                 c.kc = 32;
                 if (!size_tc(g, c, want_res)) continue;
@@ -626,6 +666,11 @@ void fill_main_params(const Geometry &g, const Tiling &t, int round_tf32, MainPa
     m.tap_group = t.tap_group; m.n_tgroups = t.n_tgroups;
     m.vec_producer = use_vec_producer(g, t) ? 1 : 0;
     m.a_tma = t.a_tma; m.a_box_rows = t.a_box_rows; m.a_nbox = t.a_nbox;
+    m.a_staged = t.a_staged; m.stg_box = t.stg_box; m.band_rows = t.band_rows; m.img_tiles = t.img_tiles;
+    // staged: about 128 KB of grad_out boxes in flight to L2 per CTA, ahead
+    // of the copies (HBM latency times a CTA's share of the bandwidth is
+    // ~70 KB), at least two stages
+    m.prefetch_ahead = t.a_staged ? std::max(2, std::min(16, (128 * 1024) / (t.stg_box * 128))) : 0;
     m.acc_bufs = t.acc_bufs; m.acc_cols = t.acc_cols; m.tmem_cols = t.tmem_cols;
     m.round_tf32 = round_tf32;
     m.split_chunks = t.split ? t.n_chunks / 3 : 0;

@@ -128,6 +128,14 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const void *tmap, int 
         : "memory");
 }
 
+// Prefetch the box of a 3-D tensor copy into L2 (TMA engine; nothing is
+// written to shared memory and no barrier is involved).
+__device__ __forceinline__ void tma_prefetch_3d(const void *tmap, int c0, int c1, int c2) {
+    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(tmap), "r"(c0),
+                 "r"(c1), "r"(c2)
+                 : "memory");
+}
+
 __device__ __forceinline__ void prefetch_tensormap(const void *tmap) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
 }
@@ -152,6 +160,16 @@ __device__ __forceinline__ float round_tf32(float x) {
     uint32_t r;
     asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
     return __uint_as_float(r);
+}
+
+// The same rounding with two integer operations on the bit pattern: adding
+// half of the 13 dropped bits' unit to the magnitude and clearing them rounds
+// the magnitude to nearest with ties away from zero (the sign bit is not
+// touched; a carry out of the mantissa moves the exponent up, which is the
+// correct result, up to infinity).  For every non-NaN input it equals
+// round_tf32; NaNs stay NaNs.
+__device__ __forceinline__ float round_tf32_int(float x) {
+    return __uint_as_float((__float_as_uint(x) + 0x1000u) & 0xffffe000u);
 }
 
 // ---------------------------------------------------------------- tcgen05

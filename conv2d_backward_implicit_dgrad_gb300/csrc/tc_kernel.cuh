@@ -21,6 +21,9 @@
 //   warps 6-13  producer mode: a band of grad_out -> shared memory (A
 //               operand), 32 channels per stage, rows in the 128-byte
 //               swizzled K-major layout of the tensor core
+//   staged mode (tensor copies of the caller's grad_out itself): two
+//               transposer warps after the epilogue warps turn each copied
+//               stage, in place, into that layout
 // Pipelines (all mbarriers, all waits bounded):
 //   A ring   a_stages  loader/producers -> MMA (A_full / A_empty)
 //   B ring   b_stages  weight loader -> MMA    (B_full / B_empty); when the
@@ -55,9 +58,15 @@ constexpr int kGroupTableOffset = 1024;          // bytes into shared memory: MM
 constexpr int kXchgOffset = 3072;                // epilogue row exchange; operand stages follow at the next
                                                  // 1024-byte boundary
 
+constexpr int kTransWarps = 2;                   // staged mode: transposer warps
+constexpr int kTransThreads = kTransWarps * 32;
+constexpr int kTransRows = 4;                    // rows per transposer thread (A stages of <= 256 rows)
+constexpr int kTransBar = 3;                     // named barrier of the transposers (1, 2: epilogue groups)
+
 struct Barriers {
     uint64_t a_full[kMaxAStages];
     uint64_t a_empty[kMaxAStages];
+    uint64_t stg_full[kMaxAStages];   // staged mode: the stage's tensor copy has landed
     uint64_t b_full[kMaxBStages];
     uint64_t b_empty[kMaxBStages];
     uint64_t acc_full[2];
@@ -114,6 +123,119 @@ __device__ __forceinline__ int plane_elems_below(const MainParams &p, int n, int
     const int oh = rel / p.Wp;
     if (oh >= p.oH) return p.oH * p.oW;
     return oh * p.oW + min(rel - oh * p.Wp, p.oW);
+}
+
+// First frame position of a tile and the end of the positions its outputs
+// may lie in.  Tiles run across images, or (img_tiles > 0, staged mode)
+// each image has img_tiles tiles of its own, so that a band never holds two
+// images; positions past the tile's image are then never outputs of it.
+__device__ __forceinline__ int tile_origin(const MainParams &p, int tile, int &lim) {
+    if (p.img_tiles) {
+        const int n = tile / p.img_tiles;
+        lim = (n + 1) * p.HvWp;
+        return n * p.HvWp + (tile - n * p.img_tiles) * p.tile_step;
+    }
+    lim = p.positions;
+    return tile * p.tile_step;
+}
+
+// Staged mode.  The loader's tensor copy writes the band's grad_out elements
+// channel by channel at the start of the A stage: element x0 + e of channel
+// 32c + k of the image's plane at float k*stg_box + e (x0 = the band's first
+// element rounded down to a multiple of 4, channels past Co and elements past
+// the plane read as zeros).  The transposer warps read every value they will
+// write into registers, meet at a named barrier (after which nothing of the
+// copy is read again), and write the band in the MMA's layout: row r (frame
+// position P0 + r) holds its element's 32 channels, TF32-rounded (split
+// precision: the hi or lo part), in the 128-byte swizzle; rows with no
+// element (frame padding, other images) are zeros.  Thread t takes rows
+// t, t + 64, ...: a warp's loads of one channel read consecutive words, and
+// its 16-byte stores of one chunk land in eight different bank groups.
+template <int KC, int kEG>
+__device__ __forceinline__ void transpose_stages(const MainParams &p, Barriers *bars, float *a_base,
+                                                 int a_stage_floats, long long tmo) {
+    constexpr int kW0 = kProdWarp0 + (kEG - 1) * kEpiWarps;
+    const int tt = static_cast<int>(threadIdx.x) - kW0 * 32;
+    const uint32_t a0 = dev::smem_u32(a_base);
+    Ring ring;
+    // The two warps leave together: whether to go on is agreed at the named
+    // barrier of every stage (a wait that ran out, or an abort, in either).
+    for (int w = blockIdx.x; w < p.n_work; w += gridDim.x) {
+        int lim;
+        const int P0 = tile_origin(p, w / p.n_slices, lim);
+        const int n = P0 / p.HvWp;
+        const int x0 = plane_elems_below(p, n, P0) & ~3;
+        int loc[kTransRows];   // element of row tt + 64*i in the copy, or -1
+#pragma unroll
+        for (int i = 0; i < kTransRows; ++i) {
+            const int r = tt + kTransThreads * i;
+            const int P = P0 + r;
+            loc[i] = -1;
+            if (r < p.band_rows && P < lim) {
+                const int rel = P - n * p.HvWp;
+                const int y = rel / p.Wp;
+                const int oh = y - p.Ph, ow = rel - y * p.Wp - p.Pw;
+                if (static_cast<unsigned>(oh) < static_cast<unsigned>(p.oH) &&
+                    static_cast<unsigned>(ow) < static_cast<unsigned>(p.oW))
+                    loc[i] = oh * p.oW + ow - x0;
+            }
+        }
+        for (int c = 0; c < p.n_chunks; ++c, ring.next(p.a_stages)) {
+            DGRAD_TRACE_CLOCK(tw0);
+            const bool got = !bars->abort_flag &&
+                             dev::mbar_wait(dev::smem_u32(&bars->stg_full[ring.stage]), ring.parity, tmo);
+            DGRAD_TRACE_CLOCK(tw1);
+            if (tt == 0) DGRAD_TRACE_ADD(4, tw1 - tw0);
+            const float *stg = a_base + static_cast<size_t>(ring.stage) * a_stage_floats;
+            float v[kTransRows][KC];
+#pragma unroll
+            for (int i = 0; i < kTransRows; ++i) {
+#pragma unroll
+                for (int k = 0; k < KC; ++k)
+                    v[i][k] = (got && loc[i] >= 0) ? stg[k * p.stg_box + loc[i]] : 0.f;
+            }
+            // Every read of the copy is done (nothing of it is read again),
+            // and every transposer thread has its data.
+            if (!dev::named_bar_and(kTransBar, kTransThreads, got)) {
+                if (!got) fail(bars, p);
+                return;
+            }
+            DGRAD_TRACE_CLOCK(tw15);
+            if (tt == 0) DGRAD_TRACE_ADD(15, tw15 - tw1);
+            const int pass = p.split_chunks ? c / p.split_chunks : 0;
+            const uint32_t as = a0 + static_cast<uint32_t>(ring.stage) * a_stage_floats * 4;
+#pragma unroll
+            for (int i = 0; i < kTransRows; ++i) {
+                const int r = tt + kTransThreads * i;
+                if (r < p.a_rows) {
+#pragma unroll
+                    for (int k = 0; k < KC; ++k) {
+                        float x = v[i][k];
+                        if (p.split_chunks) {
+                            const float hi = dev::round_tf32_int(x);
+                            x = pass == 1 ? dev::round_tf32_int(x - hi) : hi;
+                        } else if (p.round_tf32) {
+                            x = dev::round_tf32_int(x);
+                        }
+                        v[i][k] = x;
+                    }
+                    const uint32_t row = as + static_cast<uint32_t>(r) * 128;
+#pragma unroll
+                    for (int g = 0; g < KC / 4; ++g)
+                        asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(
+                                         row + (static_cast<uint32_t>(g ^ (r & 7)) << 4)),
+                                     "f"(v[i][4 * g]), "f"(v[i][4 * g + 1]), "f"(v[i][4 * g + 2]),
+                                     "f"(v[i][4 * g + 3])
+                                     : "memory");
+                }
+            }
+            // The stores reach the tensor core's (async-proxy) operand reads.
+            dev::fence_proxy_async_smem();
+            dev::mbar_arrive(dev::smem_u32(&bars->a_full[ring.stage]));
+            DGRAD_TRACE_CLOCK(tw2);
+            if (tt == 0) DGRAD_TRACE_ADD(5, tw2 - tw15);
+        }
+    }
 }
 
 // Quad producer.  The 256 producer threads form two groups of 128 that fill
@@ -553,11 +675,13 @@ __device__ __forceinline__ void epilogue_run(EpiCtx &e, int tile, uint32_t tbase
     float pend[NV][CB / 16][16];
     float *pend_dst = nullptr;
     int pend_cols = 0;
+    int lim;
+    const int T0 = tile_origin(p, tile, lim);
     for (int m = 0; m < p.tm; ++m) {
         const int o = m * kBlockM + e.ew * 32 + e.lane;   // row of the unit
-        const int P = tile * p.tile_step + o;
+        const int P = T0 + o;
         dev::decode_position(p, P, e.n, e.q, e.u);
-        e.row_ok = o < p.tile_step && P < p.positions;
+        e.row_ok = o < p.tile_step && P < lim;
         e.tbase = tbase0 + static_cast<uint32_t>(m * m_cols);
         epilogue_unit<NV, SMAX, CB, FUSE>(e, pend, pend_dst, pend_cols);
     }
@@ -587,9 +711,10 @@ __device__ __forceinline__ void epilogue_run_g1(EpiCtx &e, int tile, uint32_t tb
     const PhaseDesc &pd = p.phase[0];
     const int bnp = p.bn;
     const int o = e.ew * 32 + e.lane;   // row of the unit
-    const int P = tile * p.tile_step + o;
+    int lim;
+    const int P = tile_origin(p, tile, lim) + o;
     dev::decode_position(p, P, e.n, e.q, e.u);
-    e.row_ok = o < p.tile_step && P < p.positions;
+    e.row_ok = o < p.tile_step && P < lim;
     const uint32_t tb = tbase0 + static_cast<uint32_t>(pd.col);
     float *xb = e.xbase + static_cast<size_t>(ubuf) * 4 * kSlots * bnp;
     float *xw = xb + static_cast<size_t>(e.ew) * kSlots * bnp;
@@ -673,15 +798,18 @@ __host__ __device__ constexpr int epi_form(int vec_w, int s, int max_sub) {
 // (producer mode) 128.
 // kEG: epilogue warp groups (2: warps 6-9 form a second group that takes
 // every other work unit and the second accumulator set; tensor-copy mode).
-template <bool kTmaA, int kEG>
+// kStg: staged mode (tensor copies of the caller's grad_out, transposed by
+// kTransWarps warps placed after the epilogue warps).
+template <bool kTmaA, int kEG, bool kStg>
 constexpr int kernel_threads() {
-    return kTmaA ? (kProdWarp0 + (kEG - 1) * kEpiWarps) * 32 : kThreads;
+    return kTmaA ? (kProdWarp0 + (kEG - 1) * kEpiWarps + (kStg ? kTransWarps : 0)) * 32 : kThreads;
 }
 
-template <int KC, bool kTmaA, int kEpi, int kFuse, int kEG>
-__global__ void __launch_bounds__(kernel_threads<kTmaA, kEG>(), 1)
+template <int KC, bool kTmaA, int kEpi, int kFuse, int kEG, bool kStg>
+__global__ void __launch_bounds__(kernel_threads<kTmaA, kEG, kStg>(), 1)
     tc_dgrad_kernel(const __grid_constant__ MainParams p) {
     static_assert(kEG == 1 || (kEG == 2 && kTmaA), "a second epilogue group needs the tensor-copy mode");
+    static_assert(!kStg || kTmaA, "staged copies are tensor copies");
     static_assert(KC == 32, "operand rows are one 128-byte swizzle row of 32 TF32 values");
     extern __shared__ __align__(1024) uint8_t smem[];
     Barriers *bars = reinterpret_cast<Barriers *>(smem);
@@ -699,10 +827,12 @@ __global__ void __launch_bounds__(kernel_threads<kTmaA, kEG>(), 1)
     const int lane = threadIdx.x % 32;
 
     if (threadIdx.x == 0) {
-        const uint32_t a_arrivals = kTmaA ? 1 : (p.vec_producer ? kGroupThreads : kProdWarps * 32);
+        const uint32_t a_arrivals =
+            kStg ? kTransThreads : kTmaA ? 1 : (p.vec_producer ? kGroupThreads : kProdWarps * 32);
         for (int i = 0; i < p.a_stages; ++i) {
             dev::mbar_init(dev::smem_u32(&bars->a_full[i]), a_arrivals);
             dev::mbar_init(dev::smem_u32(&bars->a_empty[i]), 1);
+            dev::mbar_init(dev::smem_u32(&bars->stg_full[i]), 1);
         }
         for (int i = 0; i < p.b_stages; ++i) {
             dev::mbar_init(dev::smem_u32(&bars->b_full[i]), 1);
@@ -740,13 +870,39 @@ __global__ void __launch_bounds__(kernel_threads<kTmaA, kEG>(), 1)
             produce_async4<KC>(p, bars, a_base, a_stage_floats, tile_step, tmo);
         DGRAD_TRACE_CLOCK(t_pend);
         if (threadIdx.x == kProdWarp0 * 32) DGRAD_TRACE_ADD(12, t_pend - t_start);
+    } else if (kStg && warp >= kProdWarp0 + (kEG - 1) * kEpiWarps) {
+        // ---------------------------------------------------- transposers
+        transpose_stages<KC, kEG>(p, bars, a_base, a_stage_floats, tmo);
+        DGRAD_TRACE_CLOCK(t_pend);
+        if (threadIdx.x == (kProdWarp0 + (kEG - 1) * kEpiWarps) * 32) DGRAD_TRACE_ADD(12, t_pend - t_start);
     } else if (warp == kLoadWarp) {
         // ------------------------------------------------- weight loader
         // B stage (c, tg) = taps [bg_tap0[tg], bg_tap0[tg+1]) of channel
         // chunk c of the work unit's slice: one contiguous block of the
         // packed weights.
+        // Staged mode: grad_out comes from HBM, so the boxes of the stages
+        // kPrefetchAhead ahead of the one being loaded are prefetched into
+        // L2 (a CTA's stages are its units' chunks in order); the stage
+        // copies then hit L2.  grad_out is the caller's input, not an output
+        // of the preceding kernel, so the first ones go out before the wait.
+        const int n_seq = kStg ? ((p.n_work - static_cast<int>(blockIdx.x) + static_cast<int>(gridDim.x) - 1) /
+                                  static_cast<int>(gridDim.x)) * p.n_chunks
+                               : 0;
+        const int ahead = kStg ? p.prefetch_ahead : 0;
+        auto prefetch_stage = [&](int s) {
+            if (s >= n_seq) return;
+            const int c = s % p.n_chunks;
+            if (p.split_chunks && c >= p.split_chunks) return;   // passes 1 and 2 re-read pass 0's boxes
+            const int w = static_cast<int>(blockIdx.x) + (s / p.n_chunks) * static_cast<int>(gridDim.x);
+            int lim;
+            const int P0 = tile_origin(p, w / p.n_slices, lim);
+            const int n = P0 / p.HvWp;
+            dev::tma_prefetch_3d(&p.a_map, plane_elems_below(p, n, P0) & ~3, c * KC, n);
+        };
         if (lane == 0) {
             if (kTmaA) dev::prefetch_tensormap(&p.a_map);
+            if (kStg)
+                for (int s = 0; s < ahead; ++s) prefetch_stage(s);
             dev::grid_dependency_wait();   // packed weights (and frame) come from the preceding kernel
             int last_parity[kMaxBStages];   // parity of each stage's last fill, -1 if never filled
             for (int i = 0; i < kMaxBStages; ++i) last_parity[i] = -1;
@@ -765,10 +921,16 @@ __global__ void __launch_bounds__(kernel_threads<kTmaA, kEG>(), 1)
             if (kTmaA || !p.b_resident) {
                 Ring ring, aring;
                 bool ok = true;
+                int seq = 0;   // staged: this CTA's stages loaded so far
                 const uint32_t a_stage_bytes = static_cast<uint32_t>(a_stage_floats) * 4;
                 for (int w = blockIdx.x; ok && w < p.n_work && !bars->abort_flag; w += gridDim.x) {
                     const int slice = w % p.n_slices;
-                    const int P0 = (w / p.n_slices) * tile_step;
+                    int lim;
+                    const int P0 = tile_origin(p, w / p.n_slices, lim);
+                    // staged: the band's image and its first plane element, rounded down to a
+                    // 16-byte boundary (the tensor copy's innermost coordinate must be one)
+                    const int sn = kStg ? P0 / p.HvWp : 0;
+                    const int sx0 = kStg ? plane_elems_below(p, sn, P0) & ~3 : 0;
                     for (int c = 0; ok && c < p.n_chunks; ++c) {
                         if (kTmaA) {
                             // A stage: frame rows [P0, P0 + a_rows) x channels [32c, 32c + 32)
@@ -777,19 +939,30 @@ __global__ void __launch_bounds__(kernel_threads<kTmaA, kEG>(), 1)
                                 ok = false;
                                 break;
                             }
-                            const uint32_t bar = dev::smem_u32(&bars->a_full[aring.stage]);
-                            dev::mbar_arrive_expect_tx(bar, a_stage_bytes);
                             const uint32_t dst = dev::smem_u32(a_base) + aring.stage * a_stage_bytes;
-                            // Split precision: K pass c / split_chunks = 0, 1, 2 reads the
-                            // hi, lo, hi half of the frame rows (B holds lo, hi, hi).
-                            int x = c * KC;
-                            if (p.split_chunks) {
-                                const int pass = c / p.split_chunks;
-                                x = (c - pass * p.split_chunks) * KC + (pass == 1 ? p.co_h : 0);
+                            if constexpr (kStg) {
+                                // grad_out elements [sx0, sx0 + stg_box) of 32 channels of image sn; split
+                                // precision reads channel chunk c mod split_chunks in every K pass
+                                prefetch_stage(seq + ahead);
+                                ++seq;
+                                const uint32_t bar = dev::smem_u32(&bars->stg_full[aring.stage]);
+                                dev::mbar_arrive_expect_tx(bar, static_cast<uint32_t>(p.stg_box) * KC * 4);
+                                const int cc = p.split_chunks ? c % p.split_chunks : c;
+                                dev::tma_load_3d(dst, &p.a_map, sx0, cc * KC, sn, bar);
+                            } else {
+                                const uint32_t bar = dev::smem_u32(&bars->a_full[aring.stage]);
+                                dev::mbar_arrive_expect_tx(bar, a_stage_bytes);
+                                // Split precision: K pass c / split_chunks = 0, 1, 2 reads the
+                                // hi, lo, hi half of the frame rows (B holds lo, hi, hi).
+                                int x = c * KC;
+                                if (p.split_chunks) {
+                                    const int pass = c / p.split_chunks;
+                                    x = (c - pass * p.split_chunks) * KC + (pass == 1 ? p.co_h : 0);
+                                }
+                                for (int b = 0; b < p.a_nbox; ++b)
+                                    dev::tma_load_2d(dst + static_cast<uint32_t>(b * p.a_box_rows) * 128, &p.a_map,
+                                                     x, P0 + b * p.a_box_rows, bar);
                             }
-                            for (int b = 0; b < p.a_nbox; ++b)
-                                dev::tma_load_2d(dst + static_cast<uint32_t>(b * p.a_box_rows) * 128, &p.a_map, x,
-                                                 P0 + b * p.a_box_rows, bar);
                             a_last_parity[aring.stage] = static_cast<int>(aring.parity);
                             aring.next(p.a_stages);
                         }
@@ -817,7 +990,8 @@ __global__ void __launch_bounds__(kernel_threads<kTmaA, kEG>(), 1)
             for (int i = 0; i < p.b_stages && i < kMaxBStages; ++i)
                 if (last_parity[i] >= 0) dev::mbar_wait(dev::smem_u32(&bars->b_full[i]), last_parity[i], tmo);
             for (int i = 0; i < p.a_stages && i < kMaxAStages; ++i)
-                if (a_last_parity[i] >= 0) dev::mbar_wait(dev::smem_u32(&bars->a_full[i]), a_last_parity[i], tmo);
+                if (a_last_parity[i] >= 0)
+                    dev::mbar_wait(dev::smem_u32(kStg ? &bars->stg_full[i] : &bars->a_full[i]), a_last_parity[i], tmo);
         }
         __syncwarp();
     } else if (warp == kMmaWarp) {
@@ -995,14 +1169,14 @@ __global__ void __launch_bounds__(kernel_threads<kTmaA, kEG>(), 1)
     if (warp == kMmaWarp) dev::tmem_dealloc(tmem_base, p.tmem_cols);
 }
 
-template <int KC, bool kTmaA, int kEpi, int kFuse, int kEG = 1>
+template <int KC, bool kTmaA, int kEpi, int kFuse, int kEG = 1, bool kStg = false>
 cudaError_t launch_kc(const MainParams &p, const Tiling &t, cudaStream_t stream, bool pdl) {
-    auto kern = tc_dgrad_kernel<KC, kTmaA, kEpi, kFuse, kEG>;
+    auto kern = tc_dgrad_kernel<KC, kTmaA, kEpi, kFuse, kEG, kStg>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, t.smem_bytes);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(t.grid);
-    cfg.blockDim = dim3(kernel_threads<kTmaA, kEG>());
+    cfg.blockDim = dim3(kernel_threads<kTmaA, kEG, kStg>());
     cfg.dynamicSmemBytes = t.smem_bytes;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
@@ -1013,26 +1187,27 @@ cudaError_t launch_kc(const MainParams &p, const Tiling &t, cudaStream_t stream,
     return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
-template <bool kTmaA, int kFuse>
+template <bool kTmaA, int kFuse, bool kStg = false>
 cudaError_t launch_mode(const MainParams &p, const Tiling &t, cudaStream_t stream, bool pdl) {
     // Two epilogue groups for the grouped forms of plain-store tensor-copy
     // launches (the fused-epilogue instances keep one group).
     constexpr bool kTwo = kTmaA && kFuse == 0;
+    constexpr int kEG2 = kTwo ? 2 : 1;
     const bool two = kTwo && p.epi_groups == 2 && p.acc_bufs == 2;
     switch (epi_form(p.vec_w, p.s, p.max_sub)) {
-        case 0: return launch_kc<32, kTmaA, 0, kFuse>(p, t, stream, pdl);
+        case 0: return launch_kc<32, kTmaA, 0, kFuse, 1, kStg>(p, t, stream, pdl);
         case 1:
-            return two ? launch_kc<32, kTmaA, 1, kFuse, kTwo ? 2 : 1>(p, t, stream, pdl)
-                       : launch_kc<32, kTmaA, 1, kFuse>(p, t, stream, pdl);
+            return two ? launch_kc<32, kTmaA, 1, kFuse, kEG2, kStg>(p, t, stream, pdl)
+                       : launch_kc<32, kTmaA, 1, kFuse, 1, kStg>(p, t, stream, pdl);
         case 2:
-            return two ? launch_kc<32, kTmaA, 2, kFuse, kTwo ? 2 : 1>(p, t, stream, pdl)
-                       : launch_kc<32, kTmaA, 2, kFuse>(p, t, stream, pdl);
+            return two ? launch_kc<32, kTmaA, 2, kFuse, kEG2, kStg>(p, t, stream, pdl)
+                       : launch_kc<32, kTmaA, 2, kFuse, 1, kStg>(p, t, stream, pdl);
         case 3:
-            return two ? launch_kc<32, kTmaA, 3, kFuse, kTwo ? 2 : 1>(p, t, stream, pdl)
-                       : launch_kc<32, kTmaA, 3, kFuse>(p, t, stream, pdl);
-        case 4: return launch_kc<32, kTmaA, 4, kFuse>(p, t, stream, pdl);
-        case 5: return launch_kc<32, kTmaA, 5, kFuse>(p, t, stream, pdl);
-        default: return launch_kc<32, kTmaA, 6, kFuse>(p, t, stream, pdl);
+            return two ? launch_kc<32, kTmaA, 3, kFuse, kEG2, kStg>(p, t, stream, pdl)
+                       : launch_kc<32, kTmaA, 3, kFuse, 1, kStg>(p, t, stream, pdl);
+        case 4: return launch_kc<32, kTmaA, 4, kFuse, 1, kStg>(p, t, stream, pdl);
+        case 5: return launch_kc<32, kTmaA, 5, kFuse, 1, kStg>(p, t, stream, pdl);
+        default: return launch_kc<32, kTmaA, 6, kFuse, 1, kStg>(p, t, stream, pdl);
     }
 }
 

@@ -103,8 +103,15 @@ typedef struct {
     int chunk_k;       /* output channels per pipeline stage, multiple of 8 */
     int grid;          /* CTAs launched (persistent kernels) */
     int sm_count;      /* dgrad_describe only: SM count to plan for */
-    int a_source;      /* tcgen05 path, how grad_out reaches the MMA: 0 automatic, 1 packed frame + tensor
-                          copies (workspace holds a channels-last copy of grad_out), 2 producer warps */
+    int a_source;      /* tcgen05 path, how grad_out reaches the MMA: 0 automatic (1 when the frame fits
+                          in 2 GiB, else 2), 1 packed frame + tensor copies (workspace holds a channels-
+                          last copy of grad_out, written by the pack kernel), 2 producer warps, 3 staged
+                          (opt-in): each A stage is one tensor copy of the caller's NCHW grad_out (the
+                          band's plane elements x 32 channels), transposed in shared memory by two warps
+                          of the main kernel -- no frame and no grad_out pass, results bit for bit those
+                          of the frame; needs oH*oW % 4 == 0 and one 128-row block whose band plus
+                          alignment fits one copy (128 + largest tap shift + 3 <= 256 rows), else
+                          DGRAD_ERR_UNSUPPORTED */
     int group_taps;    /* tcgen05 path, taps issued as one MMA: 0 automatic (3 where it applies; for
                           one phase (stride 1) in TF32 with slice_n < 128 and kW >= 2, 1 where it fits;
                           else none), 1 the taps of one kernel row (N = taps x slice_n, sub-accumulators
@@ -137,7 +144,7 @@ typedef struct {
     long long n_work;      /* work units of the main kernel */
     int grid;              /* CTAs of the main kernel */
     int b_resident;        /* 1: packed weights stay in shared memory for the whole launch */
-    int a_source;          /* 1: packed frame + tensor copies, 2: producer warps (tcgen05 path) */
+    int a_source;          /* tcgen05 path: 1 packed frame + tensor copies, 2 producer warps, 3 staged */
     int smem_bytes;        /* dynamic shared memory of the main kernel */
     int tmem_cols;         /* tensor-memory columns allocated per CTA (tcgen05 path) */
     int group_taps;        /* tcgen05 path: 0 one MMA per tap, 1 per kernel row of taps, 2 per shared shift */
@@ -147,6 +154,10 @@ typedef struct {
     size_t packed_weight_bytes;
     double useful_flops;   /* 2*N*Co*oH*oW*Ci*kH*kW */
     double algorithmic_bytes; /* 4*(|grad_out| + |weight| + |grad_input|) */
+    int band_rows;         /* tcgen05 path: frame rows the MMAs of one A stage read (tile rows + largest shift) */
+    int stg_box;           /* staged (a_source 3): plane elements per tensor copy of grad_out */
+    int img_tiles;         /* staged: tiles per image (tiles never cross an image); 0 otherwise */
+    int a_rows;            /* tcgen05 path: rows of one A stage in shared memory */
 } dgrad_plan_info_t;
 
 /* Create a plan on the current CUDA device: validates the shape, derives the
@@ -231,7 +242,7 @@ dgrad_status_t dgrad_run_fused(dgrad_plan_t plan, const float *grad_out, const f
  * dgrad_run_main before any dgrad_prepack/dgrad_run, or dgrad_run_main on
  * the frame path before any grad_out was packed, returns
  * DGRAD_ERR_INVALID_ARG.  dgrad_plan_info's a_source tells whether the plan
- * uses a frame (1) or not. */
+ * uses a frame (1) or not (2, 3). */
 dgrad_status_t dgrad_prepack(dgrad_plan_t plan, const float *weight, void *stream);
 dgrad_status_t dgrad_run_packed(dgrad_plan_t plan, const float *grad_out, float *grad_input,
                                 void *stream);

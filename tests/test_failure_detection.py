@@ -33,7 +33,7 @@ def assert_tf32(gpu, ref, mag):
     assert np.all(np.abs(gpu - ref) <= 2e-3 * mag)
 
 
-@pytest.mark.parametrize("a_source", ["frame", "producers"])
+@pytest.mark.parametrize("a_source", ["frame", "producers", "staged"])
 @pytest.mark.parametrize("name", ["tiny", "resnet_stage", "strided_downsample"])
 def test_wait_that_runs_out_is_reported_and_context_survives(name, a_source):
     wl = WORKLOADS[name]

@@ -120,6 +120,43 @@ def test_workload_parity(name, seed, precision):
     assert info["path"] == ("simt" if precision == "fp32" else "tcgen05")
 
 
+@pytest.mark.parametrize("a_source", ["frame", "staged", "producers"])
+@pytest.mark.parametrize("name", ["tiny", "resnet_stage", "strided_downsample", "pointwise"])
+def test_workload_parity_each_source(name, a_source):
+    """The TF32 path with every way grad_out can reach the MMA, on the
+    workloads: the packed frame, tensor copies of grad_out transposed in
+    shared memory (staged), and producer warps."""
+    wl = WORKLOADS[name]
+    go, w = make_inputs(wl, 5)
+    info = check(wl.plan_args(), go, w, "tf32", a_source=a_source)
+    assert info["a_source"] == a_source
+
+
+@pytest.mark.parametrize("precision", ["tf32", "tf32x3"])
+@pytest.mark.parametrize("name", ["tiny", "resnet_stage", "strided_downsample", "pointwise"])
+def test_staged_equals_frame_bitwise(name, precision):
+    """Both sources feed the MMAs the same TF32 operands (round to nearest,
+    ties away) in the same K order, and every output's sum is formed in the
+    same order whatever tile it falls in: the results agree bit for bit."""
+    wl = WORKLOADS[name]
+    go, w = make_inputs(wl, 7)
+    a, ia = run_gpu(wl.plan_args(), go, w, precision, a_source="staged")
+    b, ib = run_gpu(wl.plan_args(), go, w, precision, a_source="frame")
+    assert ia["a_source"] == "staged" and ib["a_source"] == "frame"
+    assert ia["group_taps"] == ib["group_taps"]
+    assert np.array_equal(a, b)
+
+
+@pytest.mark.parametrize("name", ["tiny", "resnet_stage", "strided_downsample", "pointwise"])
+def test_split_precision_staged(name):
+    """Split precision with the staged source (hi and lo parts formed in
+    shared memory from one copy per K pass)."""
+    wl = WORKLOADS[name]
+    go, w = make_inputs(wl, 6)
+    info = check(wl.plan_args(), go, w, "tf32x3", a_source="staged")
+    assert info["a_source"] == "staged"
+
+
 # ----------------------------------------------------------------- edge sweep
 EDGE = [
     # N, Ci, Co, H, W, kH, kW, s, ph, pw
@@ -161,10 +198,12 @@ TILINGS = [
 ]
 
 
-@pytest.mark.parametrize("a_source", ["frame", "producers"])
+@pytest.mark.parametrize("a_source", ["frame", "producers", "staged"])
 @pytest.mark.parametrize("opts", TILINGS)
 @pytest.mark.parametrize("shape", [(2, 40, 36, 19, 23, 3, 3, 1, 1, 1), (2, 48, 20, 17, 18, 3, 3, 2, 1, 1),
-                                   (3, 33, 70, 9, 14, 1, 1, 1, 0, 0), (2, 24, 40, 16, 16, 3, 3, 1, 1, 1)])
+                                   (3, 33, 70, 9, 14, 1, 1, 1, 0, 0), (2, 24, 40, 16, 16, 3, 3, 1, 1, 1),
+                                   (2, 40, 36, 20, 24, 3, 3, 1, 1, 1), (2, 48, 20, 16, 16, 3, 3, 2, 1, 1),
+                                   (3, 33, 70, 8, 14, 1, 1, 1, 0, 0)])
 def test_tc_tilings(shape, opts, a_source):
     opts = dict(opts, a_source=a_source)
     N, Ci, Co, H, W, kH, kW, s, ph, pw = shape
@@ -172,7 +211,7 @@ def test_tc_tilings(shape, opts, a_source):
         dg.describe(N, Ci, H, W, Co, kH, kW, s, ph, pw, "tf32", path="tcgen05", **opts)
     except dg.DgradError as e:
         if e.status == 2:
-            pytest.skip("accumulators of this tiling exceed tensor memory")
+            pytest.skip("this tiling does not fit (tensor memory, or one staged copy per band)")
         raise
     go, w = make_tensors((N, Co, out_ext(H, kH, s, ph), out_ext(W, kW, s, pw)), (Co, Ci, kH, kW), 73, "kaiming")
     info = check((N, Ci, H, W, Co, kH, kW, s, ph, pw), go, w, "tf32", path="tcgen05", **opts)
@@ -199,10 +238,25 @@ def test_simt_with_tf32_operands():
     check((N, Ci, H, W, Co, kH, kW, s, ph, pw), go, w, "tf32", path="simt")
 
 
-@pytest.mark.parametrize("a_source", ["frame", "producers"])
-@pytest.mark.parametrize("shape", EDGE[:10])
+STAGED_EDGE = [
+    (1, 1, 1, 6, 6, 3, 3, 1, 1, 1), (3, 3, 4, 8, 12, 5, 5, 1, 2, 2), (1, 5, 33, 10, 9, 3, 3, 2, 1, 0),
+    (3, 65, 4, 12, 12, 3, 3, 3, 1, 1), (1, 129, 33, 8, 8, 1, 1, 2, 0, 0), (3, 5, 33, 12, 16, 2, 2, 2, 0, 0),
+    (1, 3, 1, 12, 16, 3, 5, 1, 2, 2), (3, 1, 4, 16, 8, 5, 3, 1, 2, 1), (1, 3, 4, 2, 8, 3, 3, 2, 1, 1),
+    (3, 16, 20, 32, 28, 3, 3, 1, 1, 1), (1, 20, 40, 40, 40, 3, 3, 4, 1, 1), (5, 7, 9, 20, 4, 3, 3, 1, 1, 1),
+]
+
+
+@pytest.mark.parametrize("a_source", ["frame", "producers", "staged"])
+@pytest.mark.parametrize("shape", EDGE[:10] + STAGED_EDGE)
 def test_edge_shapes_both_sources(shape, a_source):
     N, Ci, Co, H, W, kH, kW, s, ph, pw = shape
+    if a_source == "staged":
+        try:
+            dg.describe(N, Ci, H, W, Co, kH, kW, s, ph, pw, "tf32", a_source="staged")
+        except dg.DgradError as e:
+            if e.status == 2:
+                pytest.skip("grad_out planes not 16-byte aligned, or the band does not fit one copy")
+            raise
     go, w = make_tensors((N, Co, out_ext(H, kH, s, ph), out_ext(W, kW, s, pw)), (Co, Ci, kH, kW), 72, "uniform")
     info = check((N, Ci, H, W, Co, kH, kW, s, ph, pw), go, w, "tf32", a_source=a_source)
     assert info["a_source"] == a_source
@@ -227,7 +281,9 @@ def test_edge_shapes_grouped_and_not(shape, group_taps):
 @pytest.mark.parametrize("precision", ["tf32", "fp32", "tf32x3"])
 @pytest.mark.parametrize("mode", ["relu", "accumulate", "both"])
 @pytest.mark.parametrize("shape", [(2, 5, 7, 9, 11, 3, 3, 1, 1, 1), (2, 48, 20, 17, 18, 3, 3, 2, 1, 1),
-                                   (3, 33, 70, 9, 14, 1, 1, 1, 0, 0), (1, 20, 40, 40, 40, 3, 3, 4, 1, 1)])
+                                   (3, 33, 70, 9, 14, 1, 1, 1, 0, 0), (1, 20, 40, 40, 40, 3, 3, 4, 1, 1),
+                                   (2, 16, 24, 12, 12, 3, 3, 1, 1, 1), (2, 48, 20, 16, 16, 3, 3, 2, 1, 1),
+                                   (3, 33, 70, 8, 14, 1, 1, 1, 0, 0)])
 def test_fused_epilogue(shape, mode, precision):
     N, Ci, Co, H, W, kH, kW, s, ph, pw = shape
     go, w = make_tensors((N, Co, out_ext(H, kH, s, ph), out_ext(W, kW, s, pw)), (Co, Ci, kH, kW), 77, "kaiming")

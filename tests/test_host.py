@@ -191,6 +191,99 @@ def emulate_grouped(go, w, H, W, s, ph, pw, block=128):
     return gi
 
 
+def emulate_staged(go, w, H, W, s, ph, pw, block=None):
+    """The staged A source in numpy, driven only by the library's plan: per
+    image, img_tiles tiles of tile_step positions; each tile's band is built
+    from ONE copy of grad_out's plane elements [x0, x0 + stg_box) (x0 = the
+    band's first element rounded down to a multiple of 4, zeros past the
+    plane), row r taking the element at frame position P0 + r of the tile's
+    image (zero for padding and for positions past the image); then one GEMM
+    per tap over the band's shifted windows.  Checks that every element a
+    row needs lies inside the copy."""
+    N, Co, oH, oW = go.shape
+    _, Ci, kH, kW = w.shape
+    info = dg.describe(N, Ci, H, W, Co, kH, kW, s, ph, pw, a_source="staged", group_taps="off")
+    assert info["a_source"] == "staged"
+    phases, taps = dg.describe_taps(N, Ci, H, W, Co, kH, kW, s, ph, pw)
+    Ph, Pw, Hv, Wp = info["Ph"], info["Pw"], info["Hv"], info["Wp"]
+    img, plane = Hv * Wp, oH * oW
+    T, rows, box = info["tile_step"], info["band_rows"], info["stg_box"]
+    assert rows == T + info["max_shift"] and box % 4 == 0 and box <= 256 and info["a_rows"] >= max(rows, box)
+    # the frame position of every plane element of an image
+    el_pos = np.array([(oh + Ph) * Wp + ow + Pw for oh in range(oH) for ow in range(oW)])
+    gi = np.full((N, Ci, H, W), np.nan)
+    for n in range(N):
+        flat = go[n].reshape(Co, plane)
+        for k in range(info["img_tiles"]):
+            r0 = k * T                                        # tile origin inside the image
+            x0 = int(np.sum(el_pos < r0)) & ~3
+            copy = np.zeros((Co, box))
+            seg = flat[:, x0:x0 + box]
+            copy[:, :seg.shape[1]] = seg
+            band = np.zeros((rows, Co))
+            for r in range(rows):
+                rel = r0 + r
+                if rel >= img:
+                    continue
+                y, x = divmod(rel, Wp)
+                oh, ow = y - Ph, x - Pw
+                if 0 <= oh < oH and 0 <= ow < oW:
+                    loc = oh * oW + ow - x0
+                    assert 0 <= loc < box, (loc, box)
+                    band[r] = copy[:, loc]
+            for p in phases:
+                D = np.zeros((T, Ci))
+                for t in taps[p["tap_begin"]:p["tap_begin"] + p["tap_count"]]:
+                    D += band[t["shift"]:t["shift"] + T] @ w[:, :, t["kh"], t["kw"]].astype(np.float64)
+                for o in range(T):
+                    rel = r0 + o
+                    if rel >= img:
+                        break
+                    q, u = divmod(rel, Wp)
+                    if q < p["Hq"] and u < p["Wq"]:
+                        gi[n, :, s * q + p["a"], s * u + p["b"]] = D[o]
+    return gi
+
+
+STAGED_SHAPES = [
+    (2, 3, 4, 8, 8, 3, 3, 1, 1, 1), (1, 2, 3, 7, 8, 3, 3, 1, 0, 0), (2, 2, 3, 6, 8, 5, 3, 1, 2, 1),
+    (1, 2, 3, 9, 9, 3, 3, 2, 1, 1), (2, 3, 2, 8, 7, 3, 3, 2, 0, 0), (1, 2, 3, 10, 9, 3, 3, 3, 1, 1),
+    (2, 3, 2, 6, 6, 1, 1, 2, 0, 0), (1, 2, 2, 8, 8, 2, 2, 2, 0, 0), (3, 2, 3, 4, 13, 1, 3, 1, 0, 1),
+    (2, 2, 3, 30, 22, 3, 3, 1, 1, 1), (3, 2, 2, 28, 28, 1, 1, 1, 0, 0), (2, 2, 3, 29, 31, 3, 3, 2, 1, 1),
+]
+
+
+@pytest.mark.parametrize("shape", STAGED_SHAPES)
+def test_emulated_staged_bands_match_oracle(shape):
+    N, Ci, Co, H, W, kH, kW, s, ph, pw = shape
+    oH, oW = (H + 2 * ph - kH) // s + 1, (W + 2 * pw - kW) // s + 1
+    if (oH * oW) % 4:
+        with pytest.raises(dg.DgradError) as e:
+            dg.describe(N, Ci, H, W, Co, kH, kW, s, ph, pw, a_source="staged")
+        assert e.value.status == 2
+        return
+    go, w = make_tensors((N, Co, oH, oW), (Co, Ci, kH, kW), 64, "uniform")
+    go, w = go.numpy(), w.numpy()
+    ref, _ = oracle.dgrad(go, w, H, W, s, ph, pw)
+    emu = emulate_staged(go, w, H, W, s, ph, pw)
+    assert not np.isnan(emu).any(), "an input element was never written"
+    np.testing.assert_allclose(emu, ref, rtol=1e-12, atol=1e-12)
+
+
+@pytest.mark.parametrize("name", ["resnet_stage", "strided_downsample", "pointwise"])
+def test_staged_source_plans(name):
+    wl = WORKLOADS[name]
+    assert dg.describe(*wl.plan_args(), precision="tf32", sm_count=152)["a_source"] == "frame"   # opt-in
+    d = dg.describe(*wl.plan_args(), precision="tf32", sm_count=152, a_source="staged")
+    assert d["a_source"] == "staged" and d["workspace_bytes"] == d["packed_weight_bytes"] + 256   # no frame
+    assert d["stg_box"] <= 256 and d["a_rows"] >= max(d["band_rows"], d["stg_box"])
+    # every output position of an image lies in one of its tiles
+    assert d["img_tiles"] * d["tile_step"] >= (wl.H - 1) // wl.stride * d["Wp"] + 1
+    # the stem's band does not fit one copy
+    with pytest.raises(dg.DgradError):
+        dg.describe(*WORKLOADS["stem"].plan_args(), precision="tf32", a_source="staged")
+
+
 EMU_SHAPES = [
     (2, 3, 4, 8, 8, 3, 3, 1, 1, 1), (1, 2, 3, 7, 5, 3, 3, 1, 0, 0), (2, 2, 3, 6, 7, 5, 3, 1, 2, 1),
     (1, 2, 3, 9, 9, 3, 3, 2, 1, 1), (2, 3, 2, 8, 7, 3, 3, 2, 0, 0), (1, 2, 2, 9, 10, 7, 7, 2, 3, 3),
