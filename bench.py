@@ -39,7 +39,8 @@ METRIC = "dgrad useful TFLOP/s and % of GB300 TF32 roofline at 1 GPU; µs per ca
 TF32_OVER_BF16 = 1.1 / 2.25          # nominal dense TF32 / BF16 ratio
 FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "sm_max_mhz": 2070.0}
 FLUSH_BYTES = 256 << 20
-MAIN_KERNEL_SOURCES = ["tc_kernel.cuh", "tc_kernel.cu", "tc_kernel_fused.cu", "simt_kernel.cu", "gather.cuh", "ptx.cuh", "dgrad_internal.h"]
+MAIN_KERNEL_SOURCES = ["tc_kernel.cuh", "tc_kernel.cu", "tc_kernel_fused.cu", "tc_kernel_tmem.cu", "tc_kernel_staged.cu",
+                       "tc_kernel_staged_fused.cu", "simt_kernel.cu", "gather.cuh", "ptx.cuh", "dgrad_internal.h"]
 WORKLOAD_ORDER = ("tiny", "resnet_stage", "strided_downsample", "pointwise", "stem")
 
 

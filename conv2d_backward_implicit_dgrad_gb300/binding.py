@@ -149,7 +149,7 @@ def load_library(path: str | None = None):
         return lib
 
 
-A_SOURCE = {"auto": 0, "frame": 1, "producers": 2, "staged": 3}
+A_SOURCE = {"auto": 0, "frame": 1, "producers": 2, "staged": 3, "tmem": 4}
 A_SOURCE_NAME = {v: k for k, v in A_SOURCE.items()}
 
 

@@ -106,7 +106,7 @@ void fill_info(const Geometry &g, const Tiling &t, int precision, size_t ws, dgr
     info->n_work = t.n_work;
     info->grid = t.path == DGRAD_PATH_SIMT ? (int)t.n_work : t.grid;
     info->b_resident = t.b_resident;
-    info->a_source = t.path == DGRAD_PATH_TCGEN05 ? (t.a_staged ? 3 : t.a_tma ? 1 : 2)
+    info->a_source = t.path == DGRAD_PATH_TCGEN05 ? (t.a_tmem ? 4 : t.a_staged ? 3 : t.a_tma ? 1 : 2)
                                                   : (t.path == DGRAD_PATH_COL2IM ? 1 : 0);
     info->smem_bytes = t.smem_bytes;
     info->tmem_cols = t.tmem_cols;
@@ -190,11 +190,11 @@ dgrad_status_t encode_frame_map(dgrad_plan_s *pl) {
     return r == CUDA_SUCCESS ? DGRAD_OK : DGRAD_ERR_CUDA;
 }
 
-// Staged A source: grad_out viewed as [N][Co][oH*oW] (fp32), boxes of
-// stg_box plane elements x 32 channels x 1 image, no swizzle; channels past
-// Co and elements past the plane read as zeros.  Encoded on the caller's
-// pointer (16-byte aligned; the plane stride oH*oW*4 is a multiple of 16 for
-// every staged plan).
+// Staged and tensor-memory A sources: grad_out viewed as [N][Co][oH*oW]
+// (fp32), boxes of stg_box plane elements x 32 channels x 1 image, no
+// swizzle; channels past Co and elements past the plane read as zeros.
+// Encoded on the caller's pointer (16-byte aligned; the plane stride
+// oH*oW*4 is a multiple of 16 for every such plan).
 dgrad_status_t encode_staged_map(dgrad_plan_s *pl, const float *grad_out) {
     if (pl->go_map_ptr == grad_out) return DGRAD_OK;
     auto fn = dgrad::tensor_map_encoder();
@@ -258,7 +258,7 @@ dgrad_status_t launch_main_on(dgrad_plan_s *plan, const float *grad_out, float *
         cp.accumulate = accumulate;
         return cuda_status(dgrad::launch_c2i(cp, plan->t, s, true));
     }
-    if (plan->t.path == DGRAD_PATH_TCGEN05 && plan->t.a_staged) {
+    if (plan->t.path == DGRAD_PATH_TCGEN05 && (plan->t.a_staged || plan->t.a_tmem)) {
         dgrad_status_t st = encode_staged_map(plan, grad_out);
         if (st != DGRAD_OK) return st;
         mp.a_map = plan->go_map;
@@ -388,7 +388,8 @@ dgrad_status_t dgrad_plan_ex(int N, int Ci, int H, int W, int Co, int kH, int kW
     // copy mode) the packed grad_out frame, each 256-byte aligned.
     const size_t wp_bytes = (pl->t.packed_bytes + 255) & ~size_t(255);
     const bool has_frame =
-        (pl->t.path == DGRAD_PATH_TCGEN05 || pl->t.path == DGRAD_PATH_COL2IM) && pl->t.a_tma && !pl->t.a_staged;
+        (pl->t.path == DGRAD_PATH_TCGEN05 || pl->t.path == DGRAD_PATH_COL2IM) && pl->t.a_tma && !pl->t.a_staged &&
+        !pl->t.a_tmem;
     size_t ws = 256 + wp_bytes + (has_frame ? pl->t.frame_bytes : 0);
     void *mem = nullptr;
     if (cudaMalloc(&mem, ws) != cudaSuccess) {

@@ -143,6 +143,10 @@ struct Tiling {
     int stg_box;       // staged: plane elements per copy (box width, a multiple of 4, <= 256)
     int band_rows;     // frame rows an A stage must hold for the MMAs (tm*128 + the largest tap shift)
     int img_tiles;     // tiles per image when tiles never cross an image (staged); 0: tiles run across images
+    int a_tmem;        // 1 (1x1, stride 1, no padding): grad_out is copied from NCHW into shared memory and
+                       //    written by the epilogue warps into tensor memory, where the MMA reads A; no frame
+    int a_tslots;      // a_tmem: tensor-memory A slots (32 columns each)
+    int a_tcol;        // a_tmem: first tensor-memory column of the A slots (after the accumulators)
     int a_box_rows;    // rows of one A tensor copy (<= 256)
     int a_nbox;        // tensor copies per A stage
     int co_v;          // channels per packed frame row
@@ -248,6 +252,7 @@ struct MainParams {
     int vec_producer;   // 1: 16-byte quad loads + register transpose; 0: 4-byte asynchronous copies
     int a_tma, a_box_rows, a_nbox;
     int a_staged, stg_box, band_rows, img_tiles;   // see Tiling
+    int a_tmem, a_tslots, a_tcol;                  // see Tiling
     int prefetch_ahead; // staged: stages whose grad_out boxes are prefetched into L2 ahead of their copy
     int acc_bufs, acc_cols, tmem_cols;
     int round_tf32;
@@ -312,5 +317,6 @@ cudaError_t launch_tc(const MainParams &p, const Tiling &t, cudaStream_t stream,
 cudaError_t launch_tc_fused(const MainParams &p, const Tiling &t, cudaStream_t stream, bool pdl);
 cudaError_t launch_tc_staged(const MainParams &p, const Tiling &t, cudaStream_t stream, bool pdl);
 cudaError_t launch_tc_staged_fused(const MainParams &p, const Tiling &t, cudaStream_t stream, bool pdl);
+cudaError_t launch_tc_tmem(const MainParams &p, const Tiling &t, cudaStream_t stream, bool pdl);
 
 }  // namespace dgrad

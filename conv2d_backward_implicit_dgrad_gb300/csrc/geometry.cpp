@@ -304,7 +304,16 @@ bool size_tc(const Geometry &g, Tiling &t, int want_resident) {
                                : 0;
     const int raw_rows = t.tm * kBlockM + g.max_shift;
     t.band_rows = raw_rows;
-    if (t.a_staged) {
+    if (t.a_tmem) {
+        // Each shared-memory stage holds two tensor copies of 128 plane
+        // elements x 32 channels (a tile of 128 positions spans at most two
+        // images when the plane has >= 128 elements): 256 rows of 128 B.
+        if (t.tm != 1 || t.grouped || t.pgroup || g.max_shift != 0) return false;
+        t.stg_box = kBlockM;
+        t.a_nbox = 2;
+        t.a_box_rows = 0;
+        t.a_rows = 2 * kBlockM;
+    } else if (t.a_staged) {
         // One tensor copy per A stage of the plane elements the band holds:
         // at most one per frame row, plus up to 3 before them (the copy
         // starts on a 16-byte boundary of the plane).  The copy lands in the
@@ -371,9 +380,13 @@ bool size_tc(const Geometry &g, Tiling &t, int want_resident) {
     if (t.a_stages < 2) return false;
     t.smem_bytes = (int)(kBarrierBytes + t.xchg_bytes + t.a_stages * a_bytes + (long long)t.b_stages * t.chunk_bytes);
     t.acc_cols = t.tm * sub_cols;
-    if (t.acc_cols > kTmemCols) return false;
-    t.acc_bufs = (2 * t.acc_cols <= kTmemCols) ? 2 : 1;
-    t.tmem_cols = pow2_at_least(t.acc_bufs * t.acc_cols);
+    // a_tmem: four 32-column A slots after the accumulators
+    const int a_cols = t.a_tmem ? 4 * t.kc : 0;
+    if (t.acc_cols + a_cols > kTmemCols) return false;
+    t.acc_bufs = (2 * t.acc_cols + a_cols <= kTmemCols) ? 2 : 1;
+    t.a_tslots = t.a_tmem ? 4 : 0;
+    t.a_tcol = t.acc_bufs * t.acc_cols;
+    t.tmem_cols = pow2_at_least(t.acc_bufs * t.acc_cols + a_cols);
     if (t.a_staged) {
         // Tiles never cross an image (a band is one copy from one image):
         // each image's tiles cover its frame positions up to the last one
@@ -565,7 +578,7 @@ dgrad_status_t choose_tiling(const Geometry &g, int precision, const dgrad_optio
     }
     // Operand rows are one 128-byte swizzle row: 32 output channels per chunk.
     if (o.chunk_k && o.chunk_k != 32) return DGRAD_ERR_INVALID_ARG;
-    if (o.a_source < 0 || o.a_source > 3) return DGRAD_ERR_INVALID_ARG;
+    if (o.a_source < 0 || o.a_source > 4) return DGRAD_ERR_INVALID_ARG;
     // grad_out reaches the MMA either as tensor copies of a packed,
     // channels-last frame, or through producer warps.  Split precision takes
     // the frame at any size: its rows carry the hi and lo halves, each padded
@@ -596,8 +609,29 @@ dgrad_status_t choose_tiling(const Geometry &g, int precision, const dgrad_optio
         t.a_tma = 1;
         t.a_staged = 1;
     }
+    // 1x1 kernel, stride 1, no padding: the operand A of a tile is grad_out
+    // itself, with no shifted windows, so it can sit in tensor memory
+    // (tcgen05.mma reads A from there): the epilogue warps write each
+    // 32-channel chunk of a tile there from a tensor copy of the NCHW planes
+    // (no frame, no grad_out pass).  Needs planes of at least 128 elements
+    // (a tile then spans at most two images) that start 16-byte aligned.
+    // The automatic choice for such shapes (pointwise step 47.4 -> 36.6 us in
+    // TF32, 88.6 -> 75.2 in split precision: the frame pass is gone).
+    const long long plane = (long long)g.oH * g.oW;
+    const bool tm_ok = g.kH == 1 && g.kW == 1 && g.s == 1 && g.ph == 0 && g.pw == 0 && plane % 4 == 0 &&
+                       plane >= kBlockM && g.n_taps == 1;
+    t.a_tmem = 0;
+    if (o.a_source == 4) {
+        if (!tm_ok || o.tile_blocks > 1 || o.group_taps == 1 || o.group_taps == 3) return DGRAD_ERR_UNSUPPORTED;
+        t.a_tma = 1;
+        t.a_tmem = 1;
+    } else if (o.a_source == 0 && tm_ok && o.tile_blocks <= 1) {
+        t.a_tma = 1;
+        t.a_tmem = 1;
+    }
+    if (t.a_tmem) t.frame_bytes = 0;
     if (t.a_staged) t.frame_bytes = 0;
-    if (t.a_tma && !t.a_staged && (long long)g.positions * t.co_v > INT_MAX) return DGRAD_ERR_UNSUPPORTED;
+    if (t.a_tma && !t.a_staged && !t.a_tmem && (long long)g.positions * t.co_v > INT_MAX) return DGRAD_ERR_UNSUPPORTED;
     if (!t.a_tma) t.frame_bytes = 0;
     // Grouping the taps of a kernel row into one MMA (N = taps x bn) cuts the
     // MMA time when bn alone leaves the MMA bound by its fixed cost of
@@ -637,7 +671,7 @@ dgrad_status_t choose_tiling(const Geometry &g, int precision, const dgrad_optio
                 Tiling c = t;
                 c.grouped = group_pref[gi][0];
                 c.pgroup = group_pref[gi][1];
-                c.tm = (c.grouped || c.a_staged) ? 1 : tm_pref[i];
+                c.tm = (c.grouped || c.a_staged || c.a_tmem) ? 1 : tm_pref[i];
                 c.bn = bn;
                 c.kc = 32;
                 if (!size_tc(g, c, want_res)) continue;
@@ -667,9 +701,12 @@ void fill_main_params(const Geometry &g, const Tiling &t, int round_tf32, MainPa
     m.vec_producer = use_vec_producer(g, t) ? 1 : 0;
     m.a_tma = t.a_tma; m.a_box_rows = t.a_box_rows; m.a_nbox = t.a_nbox;
     m.a_staged = t.a_staged; m.stg_box = t.stg_box; m.band_rows = t.band_rows; m.img_tiles = t.img_tiles;
+    m.a_tmem = t.a_tmem; m.a_tslots = t.a_tslots; m.a_tcol = t.a_tcol;
     // staged: about 128 KB of grad_out boxes in flight to L2 per CTA, ahead
     // of the copies (HBM latency times a CTA's share of the bandwidth is
     // ~70 KB), at least two stages
+    // (tensor-memory A: none -- the prefetches queue on the copy engine ahead
+    // of the weight and grad_out copies the MMAs wait for; measured slower)
     m.prefetch_ahead = t.a_staged ? std::max(2, std::min(16, (128 * 1024) / (t.stg_box * 128))) : 0;
     m.acc_bufs = t.acc_bufs; m.acc_cols = t.acc_cols; m.tmem_cols = t.tmem_cols;
     m.round_tf32 = round_tf32;

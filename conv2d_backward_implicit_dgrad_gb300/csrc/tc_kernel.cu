@@ -20,6 +20,7 @@ extern "C" int dgrad_trace_read(unsigned long long *host, int n) {
 cudaError_t launch_tc(const MainParams &p, const Tiling &t, cudaStream_t stream, bool pdl) {
     if (t.kc != 32) return cudaErrorInvalidValue;
     if (!p.a_tma) return launch_mode<false, 2>(p, t, stream, pdl);
+    if (p.a_tmem) return launch_tc_tmem(p, t, stream, pdl);
     if (p.a_staged) return launch_tc_staged(p, t, stream, pdl);
     if (p.relu_in != nullptr || p.accumulate != 0) return launch_tc_fused(p, t, stream, pdl);
     return launch_mode<true, 0>(p, t, stream, pdl);

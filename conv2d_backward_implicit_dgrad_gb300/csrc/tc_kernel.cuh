@@ -24,6 +24,9 @@
 //   staged mode (tensor copies of the caller's grad_out itself): two
 //               transposer warps after the epilogue warps turn each copied
 //               stage, in place, into that layout
+//   tensor-memory A mode (1x1, stride 1, no padding): the epilogue warps
+//               also move each copied 32-channel chunk of a tile from shared
+//               into tensor memory, where the MMA reads its A operand
 // Pipelines (all mbarriers, all waits bounded):
 //   A ring   a_stages  loader/producers -> MMA (A_full / A_empty)
 //   B ring   b_stages  weight loader -> MMA    (B_full / B_empty); when the
@@ -66,7 +69,10 @@ constexpr int kTransBar = 3;                     // named barrier of the transpo
 struct Barriers {
     uint64_t a_full[kMaxAStages];
     uint64_t a_empty[kMaxAStages];
-    uint64_t stg_full[kMaxAStages];   // staged mode: the stage's tensor copy has landed
+    uint64_t stg_full[kMaxAStages];   // staged / tensor-memory A modes: the stage's tensor copies have landed
+    uint64_t stg_empty[kMaxAStages];  // tensor-memory A mode: the stage's copies have been read
+    uint64_t ta_full[4];              // tensor-memory A mode: an A slot in tensor memory is written
+    uint64_t ta_empty[4];             // tensor-memory A mode: the MMAs reading an A slot are done
     uint64_t b_full[kMaxBStages];
     uint64_t b_empty[kMaxBStages];
     uint64_t acc_full[2];
@@ -236,6 +242,76 @@ __device__ __forceinline__ void transpose_stages(const MainParams &p, Barriers *
             if (tt == 0) DGRAD_TRACE_ADD(5, tw2 - tw15);
         }
     }
+}
+
+// Tensor-memory A mode (1x1 kernel, stride 1, no padding: a tile's A rows
+// are 128 consecutive grad_out positions with no shifted windows).  For each
+// 32-channel chunk the loader copies the tile's plane elements from NCHW
+// grad_out into a shared-memory stage: a copy of 128 elements x 32 channels
+// of the tile's first image, and when the tile runs into the next image a
+// second one from that image's first element (channel k, element e of copy
+// b at float (b*32 + k)*128 + e).  Epilogue thread t (tensor-memory lane t =
+// tile row t) reads its position's 32 channels (a warp's loads of one
+// channel are consecutive words), TF32-rounds them (split precision: the
+// hi or lo part) and writes them as 32 columns of an A slot in tensor
+// memory; the MMA then reads A from there.  Waits are agreed by the warp
+// (the tensor-memory store is a warp-wide instruction).  Returns false if a
+// wait ran out (recorded; the caller's unit ends).
+template <int KC>
+__device__ __forceinline__ bool write_tmem_a(const MainParams &p, Barriers *bars, const float *a_base,
+                                             int a_stage_floats, uint32_t tmem_base, int tile, int ew, int lane,
+                                             Ring &rs, Ring &rt, long long tmo) {
+    const int t = ew * 32 + lane;
+    const int plane = p.oH * p.oW;
+    const int P0 = tile * kBlockM;
+    const int n0 = P0 / plane, x0 = P0 - n0 * plane;
+    const int P = P0 + t;
+    const bool valid = P < p.positions;
+    int off = 0;
+    if (valid) {
+        const int n = P / plane, j = P - n * plane;
+        off = n == n0 ? j - x0 : KC * kBlockM + j;
+    }
+    const uint32_t tl = tmem_base + (static_cast<uint32_t>(ew * 32) << 16) + static_cast<uint32_t>(p.a_tcol);
+    // (Issuing chunk c's store before fetching chunk c + 1 measured slower:
+    // it holds chunk c's slot back while chunk c + 1's copy is awaited.)
+    for (int c = 0; c < p.n_chunks; ++c, rs.next(p.a_stages), rt.next(p.a_tslots)) {
+        DGRAD_TRACE_CLOCK(tw0);
+        if (!__all_sync(0xffffffffu, dev::mbar_wait(dev::smem_u32(&bars->stg_full[rs.stage]), rs.parity, tmo))) {
+            if (lane == 0) fail(bars, p);
+            return false;
+        }
+        DGRAD_TRACE_CLOCK(tw1);
+        if (t == 0) DGRAD_TRACE_ADD(4, tw1 - tw0);
+        const float *stg = a_base + static_cast<size_t>(rs.stage) * a_stage_floats;
+        float v[KC];
+#pragma unroll
+        for (int k = 0; k < KC; ++k) v[k] = valid ? stg[k * kBlockM + off] : 0.f;
+        dev::mbar_arrive(dev::smem_u32(&bars->stg_empty[rs.stage]));   // the stage may be refilled
+        const int pass = p.split_chunks ? c / p.split_chunks : 0;
+#pragma unroll
+        for (int k = 0; k < KC; ++k) {
+            if (p.split_chunks) {
+                const float hi = dev::round_tf32_int(v[k]);
+                v[k] = pass == 1 ? dev::round_tf32_int(v[k] - hi) : hi;
+            } else if (p.round_tf32) {
+                v[k] = dev::round_tf32_int(v[k]);
+            }
+        }
+        DGRAD_TRACE_CLOCK(tw2);
+        if (t == 0) DGRAD_TRACE_ADD(15, tw2 - tw1);
+        if (!__all_sync(0xffffffffu, dev::mbar_wait(dev::smem_u32(&bars->ta_empty[rt.stage]), rt.parity ^ 1, tmo))) {
+            if (lane == 0) fail(bars, p);
+            return false;
+        }
+        dev::tmem_st32(tl + static_cast<uint32_t>(rt.stage * KC), v);
+        dev::tmem_wait_st();
+        dev::tc_fence_before();
+        dev::mbar_arrive(dev::smem_u32(&bars->ta_full[rt.stage]));
+        DGRAD_TRACE_CLOCK(tw3);
+        if (t == 0) DGRAD_TRACE_ADD(5, tw3 - tw2);
+    }
+    return true;
 }
 
 // Quad producer.  The 256 producer threads form two groups of 128 that fill
@@ -805,11 +881,13 @@ constexpr int kernel_threads() {
     return kTmaA ? (kProdWarp0 + (kEG - 1) * kEpiWarps + (kStg ? kTransWarps : 0)) * 32 : kThreads;
 }
 
-template <int KC, bool kTmaA, int kEpi, int kFuse, int kEG, bool kStg>
+// kTA: tensor-memory A mode (the epilogue warps write A into tensor memory).
+template <int KC, bool kTmaA, int kEpi, int kFuse, int kEG, bool kStg, bool kTA = false>
 __global__ void __launch_bounds__(kernel_threads<kTmaA, kEG, kStg>(), 1)
     tc_dgrad_kernel(const __grid_constant__ MainParams p) {
     static_assert(kEG == 1 || (kEG == 2 && kTmaA), "a second epilogue group needs the tensor-copy mode");
     static_assert(!kStg || kTmaA, "staged copies are tensor copies");
+    static_assert(!kTA || (kTmaA && !kStg && kEG == 1), "tensor-memory A: tensor copies, one epilogue group");
     static_assert(KC == 32, "operand rows are one 128-byte swizzle row of 32 TF32 values");
     extern __shared__ __align__(1024) uint8_t smem[];
     Barriers *bars = reinterpret_cast<Barriers *>(smem);
@@ -833,6 +911,11 @@ __global__ void __launch_bounds__(kernel_threads<kTmaA, kEG, kStg>(), 1)
             dev::mbar_init(dev::smem_u32(&bars->a_full[i]), a_arrivals);
             dev::mbar_init(dev::smem_u32(&bars->a_empty[i]), 1);
             dev::mbar_init(dev::smem_u32(&bars->stg_full[i]), 1);
+            dev::mbar_init(dev::smem_u32(&bars->stg_empty[i]), kEpiWarps * 32);
+        }
+        for (int i = 0; i < 4; ++i) {
+            dev::mbar_init(dev::smem_u32(&bars->ta_full[i]), kEpiWarps * 32);
+            dev::mbar_init(dev::smem_u32(&bars->ta_empty[i]), 1);
         }
         for (int i = 0; i < p.b_stages; ++i) {
             dev::mbar_init(dev::smem_u32(&bars->b_full[i]), 1);
@@ -885,23 +968,32 @@ __global__ void __launch_bounds__(kernel_threads<kTmaA, kEG, kStg>(), 1)
         // L2 (a CTA's stages are its units' chunks in order); the stage
         // copies then hit L2.  grad_out is the caller's input, not an output
         // of the preceding kernel, so the first ones go out before the wait.
-        const int n_seq = kStg ? ((p.n_work - static_cast<int>(blockIdx.x) + static_cast<int>(gridDim.x) - 1) /
-                                  static_cast<int>(gridDim.x)) * p.n_chunks
-                               : 0;
-        const int ahead = kStg ? p.prefetch_ahead : 0;
+        // Tensor-memory A mode likewise, with the boxes of the one or two
+        // images of each tile.
+        const int n_seq = (kStg || kTA) ? ((p.n_work - static_cast<int>(blockIdx.x) +
+                                            static_cast<int>(gridDim.x) - 1) / static_cast<int>(gridDim.x)) * p.n_chunks
+                                        : 0;
+        const int ahead = (kStg || kTA) ? p.prefetch_ahead : 0;
         auto prefetch_stage = [&](int s) {
-            if (s >= n_seq) return;
+            if (ahead == 0 || s >= n_seq) return;
             const int c = s % p.n_chunks;
             if (p.split_chunks && c >= p.split_chunks) return;   // passes 1 and 2 re-read pass 0's boxes
             const int w = static_cast<int>(blockIdx.x) + (s / p.n_chunks) * static_cast<int>(gridDim.x);
             int lim;
             const int P0 = tile_origin(p, w / p.n_slices, lim);
-            const int n = P0 / p.HvWp;
-            dev::tma_prefetch_3d(&p.a_map, plane_elems_below(p, n, P0) & ~3, c * KC, n);
+            if constexpr (kTA) {
+                const int plane = p.oH * p.oW;
+                const int n0 = P0 / plane, x0 = P0 - n0 * plane;
+                dev::tma_prefetch_3d(&p.a_map, x0, c * KC, n0);
+                if (x0 + kBlockM > plane && n0 + 1 < p.N) dev::tma_prefetch_3d(&p.a_map, 0, c * KC, n0 + 1);
+            } else {
+                const int n = P0 / p.HvWp;
+                dev::tma_prefetch_3d(&p.a_map, plane_elems_below(p, n, P0) & ~3, c * KC, n);
+            }
         };
         if (lane == 0) {
             if (kTmaA) dev::prefetch_tensormap(&p.a_map);
-            if (kStg)
+            if (kStg || kTA)
                 for (int s = 0; s < ahead; ++s) prefetch_stage(s);
             dev::grid_dependency_wait();   // packed weights (and frame) come from the preceding kernel
             int last_parity[kMaxBStages];   // parity of each stage's last fill, -1 if never filled
@@ -931,16 +1023,33 @@ __global__ void __launch_bounds__(kernel_threads<kTmaA, kEG, kStg>(), 1)
                     // 16-byte boundary (the tensor copy's innermost coordinate must be one)
                     const int sn = kStg ? P0 / p.HvWp : 0;
                     const int sx0 = kStg ? plane_elems_below(p, sn, P0) & ~3 : 0;
+                    // tensor-memory A: the tile's first image and element, and whether it runs into the next image
+                    const int tplane = p.oH * p.oW;
+                    const int tn0 = kTA ? P0 / tplane : 0;
+                    const int tx0 = kTA ? P0 - tn0 * tplane : 0;
+                    const bool tcross = kTA && tx0 + kBlockM > tplane && tn0 + 1 < p.N;
                     for (int c = 0; ok && c < p.n_chunks; ++c) {
                         if (kTmaA) {
                             // A stage: frame rows [P0, P0 + a_rows) x channels [32c, 32c + 32)
-                            if (!dev::mbar_wait(dev::smem_u32(&bars->a_empty[aring.stage]), aring.parity ^ 1, tmo)) {
+                            const uint32_t empty = dev::smem_u32(kTA ? &bars->stg_empty[aring.stage]
+                                                                     : &bars->a_empty[aring.stage]);
+                            if (!dev::mbar_wait(empty, aring.parity ^ 1, tmo)) {
                                 fail(bars, p);
                                 ok = false;
                                 break;
                             }
                             const uint32_t dst = dev::smem_u32(a_base) + aring.stage * a_stage_bytes;
-                            if constexpr (kStg) {
+                            if constexpr (kTA) {
+                                // channels [32cc, 32cc + 32) of the tile's positions (one or two images)
+                                prefetch_stage(seq + ahead);
+                                ++seq;
+                                const uint32_t bar = dev::smem_u32(&bars->stg_full[aring.stage]);
+                                const uint32_t box = kBlockM * KC * 4;
+                                dev::mbar_arrive_expect_tx(bar, tcross ? 2 * box : box);
+                                const int cc = p.split_chunks ? c % p.split_chunks : c;
+                                dev::tma_load_3d(dst, &p.a_map, tx0, cc * KC, tn0, bar);
+                                if (tcross) dev::tma_load_3d(dst + box, &p.a_map, 0, cc * KC, tn0 + 1, bar);
+                            } else if constexpr (kStg) {
                                 // grad_out elements [sx0, sx0 + stg_box) of 32 channels of image sn; split
                                 // precision reads channel chunk c mod split_chunks in every K pass
                                 prefetch_stage(seq + ahead);
@@ -991,7 +1100,8 @@ __global__ void __launch_bounds__(kernel_threads<kTmaA, kEG, kStg>(), 1)
                 if (last_parity[i] >= 0) dev::mbar_wait(dev::smem_u32(&bars->b_full[i]), last_parity[i], tmo);
             for (int i = 0; i < p.a_stages && i < kMaxAStages; ++i)
                 if (a_last_parity[i] >= 0)
-                    dev::mbar_wait(dev::smem_u32(kStg ? &bars->stg_full[i] : &bars->a_full[i]), a_last_parity[i], tmo);
+                    dev::mbar_wait(dev::smem_u32((kStg || kTA) ? &bars->stg_full[i] : &bars->a_full[i]),
+                                   a_last_parity[i], tmo);
         }
         __syncwarp();
     } else if (warp == kMmaWarp) {
@@ -1024,9 +1134,10 @@ __global__ void __launch_bounds__(kernel_threads<kTmaA, kEG, kStg>(), 1)
             }
             dev::tc_fence_after();
             const uint32_t d_base = tmem_base + racc.stage * p.acc_cols;
-            for (int c = 0; ok && c < p.n_chunks; ++c, ra.next(p.a_stages)) {
+            for (int c = 0; ok && c < p.n_chunks; ++c, ra.next(kTA ? p.a_tslots : p.a_stages)) {
                 DGRAD_TRACE_CLOCK(tc0);
-                if (!__all_sync(0xffffffffu, dev::mbar_wait(dev::smem_u32(&bars->a_full[ra.stage]), ra.parity, tmo))) {
+                const uint32_t a_ready = dev::smem_u32(kTA ? &bars->ta_full[ra.stage] : &bars->a_full[ra.stage]);
+                if (!__all_sync(0xffffffffu, dev::mbar_wait(a_ready, ra.parity, tmo))) {
                     if (lane == 0) fail(bars, p);
                     ok = false;
                     break;
@@ -1075,10 +1186,19 @@ __global__ void __launch_bounds__(kernel_threads<kTmaA, kEG, kStg>(), 1)
                             const uint64_t bd = dev::smem_desc_sw128(b_stage + cur.z, 0);
                             const uint32_t d = d_m + (cur.y & 0x7fffffffu);
                             const uint32_t acc0 = (c > 0 || (cur.y >> 31) == 0) ? 1u : 0u;
+                            if constexpr (kTA) {
+                                // A from tensor memory: slot ra.stage, K columns 8*k8 ..
+                                const uint32_t at = tmem_base + static_cast<uint32_t>(p.a_tcol + ra.stage * KC);
 #pragma unroll
-                            for (int k8 = 0; k8 < KC / 8; ++k8)
-                                dev::mma_tf32_elect(d, dev::desc_add(ad, 32 * k8), dev::desc_add(bd, 32 * k8), cur.w,
-                                                    k8 > 0 ? 1u : acc0);
+                                for (int k8 = 0; k8 < KC / 8; ++k8)
+                                    dev::mma_tf32_ts_elect(d, at + 8 * k8, dev::desc_add(bd, 32 * k8), cur.w,
+                                                           k8 > 0 ? 1u : acc0);
+                            } else {
+#pragma unroll
+                                for (int k8 = 0; k8 < KC / 8; ++k8)
+                                    dev::mma_tf32_elect(d, dev::desc_add(ad, 32 * k8), dev::desc_add(bd, 32 * k8),
+                                                        cur.w, k8 > 0 ? 1u : acc0);
+                            }
                         }
                     }
                     if (!p.b_resident) {
@@ -1089,7 +1209,7 @@ __global__ void __launch_bounds__(kernel_threads<kTmaA, kEG, kStg>(), 1)
                     if (lane == 0) DGRAD_TRACE_ADD(3, tb2 - tb1);
                 }
                 if (!ok) break;
-                dev::mma_commit_elect(dev::smem_u32(&bars->a_empty[ra.stage]));
+                dev::mma_commit_elect(dev::smem_u32(kTA ? &bars->ta_empty[ra.stage] : &bars->a_empty[ra.stage]));
             }
             if (!ok) break;
             dev::mma_commit_elect(dev::smem_u32(&bars->acc_full[racc.stage]));
@@ -1117,6 +1237,7 @@ __global__ void __launch_bounds__(kernel_threads<kTmaA, kEG, kStg>(), 1)
         e.bar_id = 1 + gi;
         e.xcount = 0;
         Ring racc;
+        Ring ta_rs, ta_rt;   // tensor-memory A mode: shared-memory stages and tensor-memory slots
         uint32_t it = 0;
         // One group: every unit, accumulator sets in turn.  Two groups: group gi
         // takes the CTA's units gi, gi + 2, ... and always accumulator set gi.
@@ -1133,11 +1254,15 @@ __global__ void __launch_bounds__(kernel_threads<kTmaA, kEG, kStg>(), 1)
                 racc.next(p.acc_bufs);
             }
             const int tile = w / p.n_slices, slice = w % p.n_slices;
+            // Tensor-memory A mode: first this unit's A, chunk by chunk, into tensor memory.
+            bool wrote = true;
+            if constexpr (kTA)
+                wrote = write_tmem_a<KC>(p, bars, a_base, a_stage_floats, tmem_base, tile, ew, lane, ta_rs, ta_rt, tmo);
             DGRAD_TRACE_CLOCK(te0);
             // All four warps of the group leave together or go on together.
-            const bool got = dev::mbar_wait(dev::smem_u32(&bars->acc_full[stage]), parity, tmo);
+            const bool got = wrote && dev::mbar_wait(dev::smem_u32(&bars->acc_full[stage]), parity, tmo);
             if (!dev::named_bar_and(e.bar_id, 128, got)) {
-                if (!got) fail(bars, p);
+                if (!got && wrote) fail(bars, p);
                 break;
             }
             DGRAD_TRACE_CLOCK(te1);
@@ -1169,9 +1294,9 @@ __global__ void __launch_bounds__(kernel_threads<kTmaA, kEG, kStg>(), 1)
     if (warp == kMmaWarp) dev::tmem_dealloc(tmem_base, p.tmem_cols);
 }
 
-template <int KC, bool kTmaA, int kEpi, int kFuse, int kEG = 1, bool kStg = false>
+template <int KC, bool kTmaA, int kEpi, int kFuse, int kEG = 1, bool kStg = false, bool kTA = false>
 cudaError_t launch_kc(const MainParams &p, const Tiling &t, cudaStream_t stream, bool pdl) {
-    auto kern = tc_dgrad_kernel<KC, kTmaA, kEpi, kFuse, kEG, kStg>;
+    auto kern = tc_dgrad_kernel<KC, kTmaA, kEpi, kFuse, kEG, kStg, kTA>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, t.smem_bytes);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg{};

@@ -76,10 +76,11 @@ typedef enum {
  *          accumulated in fp32.  Each product is then off by at most about
  *          3 * 2^-22 of its size, which with fp32 accumulation gives
  *          fp32-level accuracy at three times the TF32 MMA work.  tcgen05 path
- *          only; it needs the packed grad_out frame (the plan's workspace
- *          holds hi and lo halves), so DGRAD_PATH_SIMT, a_source = 2 and
- *          dgrad_run_noalloc return DGRAD_ERR_UNSUPPORTED for it.  Not in the
- *          pages: an accuracy variant of their contraction. */
+ *          only, with the packed grad_out frame (the plan's workspace holds hi
+ *          and lo halves) or a source that forms hi and lo on chip (a_source
+ *          3 and 4); DGRAD_PATH_SIMT, a_source = 2 and dgrad_run_noalloc
+ *          return DGRAD_ERR_UNSUPPORTED for it.  Not in the pages: an
+ *          accuracy variant of their contraction. */
 typedef enum { DGRAD_PREC_FP32 = 0, DGRAD_PREC_TF32 = 1, DGRAD_PREC_TF32X3 = 2 } dgrad_precision_t;
 
 /* Kernel family.  AUTO picks TCGEN05 for TF32 and TF32X3, SIMT for FP32. */
@@ -103,9 +104,15 @@ typedef struct {
     int chunk_k;       /* output channels per pipeline stage, multiple of 8 */
     int grid;          /* CTAs launched (persistent kernels) */
     int sm_count;      /* dgrad_describe only: SM count to plan for */
-    int a_source;      /* tcgen05 path, how grad_out reaches the MMA: 0 automatic (1 when the frame fits
-                          in 2 GiB, else 2), 1 packed frame + tensor copies (workspace holds a channels-
-                          last copy of grad_out, written by the pack kernel), 2 producer warps, 3 staged
+    int a_source;      /* tcgen05 path, how grad_out reaches the MMA: 0 automatic (4 where it applies,
+                          else 1 when the frame fits in 2 GiB, else 2), 1 packed frame + tensor copies
+                          (workspace holds a channels-last copy of grad_out, written by the pack kernel),
+                          2 producer warps, 4 tensor memory (1x1 kernels, stride 1, no padding,
+                          oH*oW % 4 == 0 and oH*oW >= 128; else DGRAD_ERR_UNSUPPORTED): per 32-channel
+                          chunk the main kernel copies the tile's NCHW grad_out elements into shared
+                          memory and its epilogue warps write them into tensor memory, where the MMA
+                          reads A -- no frame and no grad_out pass, results bit for bit those of the
+                          frame; 3 staged
                           (opt-in): each A stage is one tensor copy of the caller's NCHW grad_out (the
                           band's plane elements x 32 channels), transposed in shared memory by two warps
                           of the main kernel -- no frame and no grad_out pass, results bit for bit those
@@ -144,7 +151,8 @@ typedef struct {
     long long n_work;      /* work units of the main kernel */
     int grid;              /* CTAs of the main kernel */
     int b_resident;        /* 1: packed weights stay in shared memory for the whole launch */
-    int a_source;          /* tcgen05 path: 1 packed frame + tensor copies, 2 producer warps, 3 staged */
+    int a_source;          /* tcgen05 path: 1 packed frame + tensor copies, 2 producer warps, 3 staged,
+                              4 tensor memory */
     int smem_bytes;        /* dynamic shared memory of the main kernel */
     int tmem_cols;         /* tensor-memory columns allocated per CTA (tcgen05 path) */
     int group_taps;        /* tcgen05 path: 0 one MMA per tap, 1 per kernel row of taps, 2 per shared shift */
@@ -242,7 +250,7 @@ dgrad_status_t dgrad_run_fused(dgrad_plan_t plan, const float *grad_out, const f
  * dgrad_run_main before any dgrad_prepack/dgrad_run, or dgrad_run_main on
  * the frame path before any grad_out was packed, returns
  * DGRAD_ERR_INVALID_ARG.  dgrad_plan_info's a_source tells whether the plan
- * uses a frame (1) or not (2, 3). */
+ * uses a frame (1) or not (2, 3, 4). */
 dgrad_status_t dgrad_prepack(dgrad_plan_t plan, const float *weight, void *stream);
 dgrad_status_t dgrad_run_packed(dgrad_plan_t plan, const float *grad_out, float *grad_input,
                                 void *stream);

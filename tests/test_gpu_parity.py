@@ -120,16 +120,42 @@ def test_workload_parity(name, seed, precision):
     assert info["path"] == ("simt" if precision == "fp32" else "tcgen05")
 
 
-@pytest.mark.parametrize("a_source", ["frame", "staged", "producers"])
+@pytest.mark.parametrize("a_source", ["frame", "staged", "producers", "tmem"])
 @pytest.mark.parametrize("name", ["tiny", "resnet_stage", "strided_downsample", "pointwise"])
 def test_workload_parity_each_source(name, a_source):
     """The TF32 path with every way grad_out can reach the MMA, on the
     workloads: the packed frame, tensor copies of grad_out transposed in
-    shared memory (staged), and producer warps."""
+    shared memory (staged), producer warps, and (1x1 only) tensor copies
+    moved into tensor memory as the MMA's A operand."""
     wl = WORKLOADS[name]
+    if a_source == "tmem" and name != "pointwise":
+        pytest.skip("A in tensor memory is for 1x1, stride-1, unpadded kernels")
     go, w = make_inputs(wl, 5)
     info = check(wl.plan_args(), go, w, "tf32", a_source=a_source)
     assert info["a_source"] == a_source
+
+
+@pytest.mark.parametrize("precision", ["tf32", "tf32x3"])
+@pytest.mark.parametrize("shape", [WORKLOADS["pointwise"].plan_args(),   # (N, Ci, H, W, Co, kH, kW, s, ph, pw)
+                                   (3, 33, 12, 12, 70, 1, 1, 1, 0, 0), (2, 300, 16, 16, 40, 1, 1, 1, 0, 0),
+                                   (1, 17, 8, 16, 9, 1, 1, 1, 0, 0)])
+def test_tmem_equals_frame_bitwise(shape, precision):
+    """A in tensor memory holds the same TF32 operands (rounded to nearest,
+    ties away) as the frame path's shared-memory A, and the K order is the
+    same: the results agree bit for bit.  Shapes: the workload, tiles running
+    across images, two input-channel slices (several units per tile), one
+    image (no next image to copy from)."""
+    N, Ci, H, W, Co, kH, kW, s, ph, pw = shape
+    go, w = make_tensors((N, Co, H, W), (Co, Ci, 1, 1), 88, "kaiming")
+    a, ia = run_gpu(shape, go, w, precision, a_source="tmem")
+    b, ib = run_gpu(shape, go, w, precision, a_source="frame")
+    assert ia["a_source"] == "tmem" and ib["a_source"] == "frame"
+    assert np.array_equal(a, b)
+    ref, mag = oracle.dgrad(go, w, H, W, s, ph, pw)
+    if precision == "tf32":
+        assert_tf32(a, ref, mag)
+    else:
+        assert_split(a, ref, mag, Co, kH, kW)
 
 
 @pytest.mark.parametrize("precision", ["tf32", "tf32x3"])
@@ -198,12 +224,12 @@ TILINGS = [
 ]
 
 
-@pytest.mark.parametrize("a_source", ["frame", "producers", "staged"])
+@pytest.mark.parametrize("a_source", ["frame", "producers", "staged", "tmem"])
 @pytest.mark.parametrize("opts", TILINGS)
 @pytest.mark.parametrize("shape", [(2, 40, 36, 19, 23, 3, 3, 1, 1, 1), (2, 48, 20, 17, 18, 3, 3, 2, 1, 1),
                                    (3, 33, 70, 9, 14, 1, 1, 1, 0, 0), (2, 24, 40, 16, 16, 3, 3, 1, 1, 1),
                                    (2, 40, 36, 20, 24, 3, 3, 1, 1, 1), (2, 48, 20, 16, 16, 3, 3, 2, 1, 1),
-                                   (3, 33, 70, 8, 14, 1, 1, 1, 0, 0)])
+                                   (3, 33, 70, 8, 14, 1, 1, 1, 0, 0), (3, 33, 70, 12, 12, 1, 1, 1, 0, 0)])
 def test_tc_tilings(shape, opts, a_source):
     opts = dict(opts, a_source=a_source)
     N, Ci, Co, H, W, kH, kW, s, ph, pw = shape
@@ -211,7 +237,7 @@ def test_tc_tilings(shape, opts, a_source):
         dg.describe(N, Ci, H, W, Co, kH, kW, s, ph, pw, "tf32", path="tcgen05", **opts)
     except dg.DgradError as e:
         if e.status == 2:
-            pytest.skip("this tiling does not fit (tensor memory, or one staged copy per band)")
+            pytest.skip("this tiling does not fit (tensor memory, one staged copy per band, or not 1x1)")
         raise
     go, w = make_tensors((N, Co, out_ext(H, kH, s, ph), out_ext(W, kW, s, pw)), (Co, Ci, kH, kW), 73, "kaiming")
     info = check((N, Ci, H, W, Co, kH, kW, s, ph, pw), go, w, "tf32", path="tcgen05", **opts)
@@ -283,7 +309,7 @@ def test_edge_shapes_grouped_and_not(shape, group_taps):
 @pytest.mark.parametrize("shape", [(2, 5, 7, 9, 11, 3, 3, 1, 1, 1), (2, 48, 20, 17, 18, 3, 3, 2, 1, 1),
                                    (3, 33, 70, 9, 14, 1, 1, 1, 0, 0), (1, 20, 40, 40, 40, 3, 3, 4, 1, 1),
                                    (2, 16, 24, 12, 12, 3, 3, 1, 1, 1), (2, 48, 20, 16, 16, 3, 3, 2, 1, 1),
-                                   (3, 33, 70, 8, 14, 1, 1, 1, 0, 0)])
+                                   (3, 33, 70, 8, 14, 1, 1, 1, 0, 0), (3, 33, 70, 12, 12, 1, 1, 1, 0, 0)])
 def test_fused_epilogue(shape, mode, precision):
     N, Ci, Co, H, W, kH, kW, s, ph, pw = shape
     go, w = make_tensors((N, Co, out_ext(H, kH, s, ph), out_ext(W, kW, s, pw)), (Co, Ci, kH, kW), 77, "kaiming")

@@ -270,10 +270,25 @@ def test_emulated_staged_bands_match_oracle(shape):
     np.testing.assert_allclose(emu, ref, rtol=1e-12, atol=1e-12)
 
 
+def test_tmem_source_plans():
+    """1x1 / stride 1 / no padding with planes of >= 128 elements: A in tensor
+    memory automatically (no frame in the workspace); other shapes refuse it."""
+    pw = WORKLOADS["pointwise"]
+    d = dg.describe(*pw.plan_args(), precision="tf32", sm_count=152)
+    assert d["a_source"] == "tmem" and d["workspace_bytes"] == d["packed_weight_bytes"] + 256
+    assert d["tmem_cols"] <= 512 and d["tile_blocks"] == 1 and d["n_phases"] == 1 and d["n_taps"] == 1
+    assert dg.describe(*pw.plan_args(), precision="tf32x3", sm_count=152)["a_source"] == "tmem"
+    for bad in [WORKLOADS["resnet_stage"].plan_args(), (2, 8, 8, 8, 8, 1, 1, 1, 0, 0),   # 3x3; plane of 64
+                (2, 8, 14, 14, 8, 1, 1, 2, 0, 0), (2, 8, 15, 15, 8, 1, 1, 1, 0, 0)]:   # stride 2; plane % 4
+        with pytest.raises(dg.DgradError) as e:
+            dg.describe(*bad, precision="tf32", a_source="tmem")
+        assert e.value.status == 2
+
+
 @pytest.mark.parametrize("name", ["resnet_stage", "strided_downsample", "pointwise"])
 def test_staged_source_plans(name):
     wl = WORKLOADS[name]
-    assert dg.describe(*wl.plan_args(), precision="tf32", sm_count=152)["a_source"] == "frame"   # opt-in
+    assert dg.describe(*wl.plan_args(), precision="tf32", sm_count=152)["a_source"] in ("frame", "tmem")   # opt-in
     d = dg.describe(*wl.plan_args(), precision="tf32", sm_count=152, a_source="staged")
     assert d["a_source"] == "staged" and d["workspace_bytes"] == d["packed_weight_bytes"] + 256   # no frame
     assert d["stg_box"] <= 256 and d["a_rows"] >= max(d["band_rows"], d["stg_box"])
@@ -368,7 +383,8 @@ def test_split_precision_plans():
         d = dg.describe(*wl.plan_args(), precision="tf32x3")
         t = dg.describe(*wl.plan_args(), precision="tf32")
         assert d["path"] == "tcgen05" and d["precision"] == "tf32x3"
-        assert d["a_source"] == "frame"                       # always the packed frame
+        # the packed frame, except 1x1 unpadded stride-1 shapes, whose A goes to tensor memory
+        assert d["a_source"] == ("tmem" if name == "pointwise" else "frame")
         assert d["n_chunks"] == 3 * -(-wl.Co // 32)           # three K passes per channel chunk
         assert d["smem_bytes"] <= 232448 and d["tmem_cols"] <= 512
         assert d["useful_flops"] == t["useful_flops"]
