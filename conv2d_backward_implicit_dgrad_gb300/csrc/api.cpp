@@ -119,7 +119,7 @@ void fill_info(const Geometry &g, const Tiling &t, int precision, size_t ws, dgr
     info->useful_flops = 2.0 * g.N * g.Co * g.oH * g.oW * (double)g.Ci * g.kH * g.kW;
     info->algorithmic_bytes = 4.0 * ((double)go_elems(g) + (double)w_elems(g) + (double)gi_elems(g));
     info->band_rows = t.band_rows;
-    info->stg_box = t.a_staged ? t.stg_box : 0;
+    info->stg_box = (t.a_staged || t.a_tmem) ? t.stg_box : 0;
     info->img_tiles = t.img_tiles;
     info->a_rows = t.a_rows;
 }
