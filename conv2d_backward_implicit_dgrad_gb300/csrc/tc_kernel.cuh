@@ -90,15 +90,20 @@ static_assert(kGroupTableOffset + kMaxTaps * 16 <= kXchgOffset, "MMA group table
 // acc_empty / A_full / B_full, MMA issue, producer waits on A_empty,
 // producer issue, epilogue waits on acc_full, epilogue work, units, chunks,
 // launch-relative cycle of the first MMA, of the MMA loop's end, of the
-// producers' end, of the epilogue's end.
+// producers' end, of the epilogue's end; global-timer ns at the CTA's start
+// and end, and its span in cycles.  In the grouped one-phase epilogue, slots
+// 4, 5, 14 and 15 hold its publish pass, barrier, combine-and-store loop and
+// last stores instead.
 #ifdef DGRAD_TRACE
-constexpr int kTraceSlots = 16;
+constexpr int kTraceSlots = 20;
 constexpr int kTraceCtas = 1024;
 __device__ unsigned long long g_trace[kTraceCtas * kTraceSlots];
 #define DGRAD_TRACE_ADD(slot, v) \
     atomicAdd(&g_trace[(blockIdx.x % kTraceCtas) * kTraceSlots + (slot)], (unsigned long long)(v))
 #define DGRAD_TRACE_CLOCK(x) const long long x = clock64()
+#define DGRAD_TRACE_SET(slot, v) (g_trace[(blockIdx.x % kTraceCtas) * kTraceSlots + (slot)] = (unsigned long long)(v))
 #else
+#define DGRAD_TRACE_SET(slot, v) ((void)0)
 #define DGRAD_TRACE_ADD(slot, v) ((void)0)
 #define DGRAD_TRACE_CLOCK(x) ((void)0)
 #endif
@@ -795,6 +800,7 @@ __device__ __forceinline__ void epilogue_run_g1(EpiCtx &e, int tile, uint32_t tb
     float *xb = e.xbase + static_cast<size_t>(ubuf) * 4 * kSlots * bnp;
     float *xw = xb + static_cast<size_t>(e.ew) * kSlots * bnp;
     const float *xn = e.ew < 3 ? xw + kSlots * bnp : nullptr;
+    DGRAD_TRACE_CLOCK(tg0);
     for (int c0 = 0; c0 < bnp; c0 += 16) {   // publish
         uint32_t r[S - 1][16];
 #pragma unroll
@@ -811,7 +817,13 @@ __device__ __forceinline__ void epilogue_run_g1(EpiCtx &e, int tile, uint32_t tb
             slot += sh;
         }
     }
+    DGRAD_TRACE_CLOCK(tg1);
     dev::named_bar(e.bar_id, 128);
+    DGRAD_TRACE_CLOCK(tg2);
+    if (threadIdx.x == 0) {
+        DGRAD_TRACE_ADD(4, tg1 - tg0);
+        DGRAD_TRACE_ADD(5, tg2 - tg1);
+    }
     const size_t plane = static_cast<size_t>(p.H) * p.W;
     const bool valid = e.row_ok && e.q < pd.Hq && e.u < pd.Wq;
     const int ih = p.s * e.q + pd.a, iw = p.s * e.u + pd.b;
@@ -846,7 +858,13 @@ __device__ __forceinline__ void epilogue_run_g1(EpiCtx &e, int tile, uint32_t tb
     // then store the last batch.
     dev::tc_fence_before();
     dev::mbar_arrive(dev::smem_u32(acc_empty));
+    DGRAD_TRACE_CLOCK(tg3);
     if (pend_dst) store_batch<1, 16, FUSE>(p, pend_dst, plane, pend_cols, pend);
+    DGRAD_TRACE_CLOCK(tg4);
+    if (threadIdx.x == 0) {
+        DGRAD_TRACE_ADD(14, tg3 - tg2);
+        DGRAD_TRACE_ADD(15, tg4 - tg3);
+    }
 }
 
 // Epilogue forms, one kernel instantiation each (so that each form's
@@ -941,6 +959,7 @@ __global__ void __launch_bounds__(kernel_threads<kTmaA, kEG, kStg>(), 1)
     const uint32_t tmem_base = bars->tmem_base;
     const long long tmo = p.timeout_ns;
     DGRAD_TRACE_CLOCK(t_start);
+    if (threadIdx.x == 0) DGRAD_TRACE_SET(16, dev::globaltimer_ns());
     const int tile_step = p.tile_step;
     const uint32_t tap_b_bytes = static_cast<uint32_t>(p.bn) * 128;   // one tap of one chunk of B
     const int m_cols = p.acc_cols / p.tm;                              // accumulator columns of one M block
@@ -1292,6 +1311,11 @@ __global__ void __launch_bounds__(kernel_threads<kTmaA, kEG, kStg>(), 1)
     __syncthreads();
     dev::tc_fence_after();
     if (warp == kMmaWarp) dev::tmem_dealloc(tmem_base, p.tmem_cols);
+    DGRAD_TRACE_CLOCK(t_cta_end);
+    if (threadIdx.x == 0) {
+        DGRAD_TRACE_SET(17, dev::globaltimer_ns());
+        DGRAD_TRACE_SET(18, t_cta_end - t_start);
+    }
 }
 
 template <int KC, bool kTmaA, int kEpi, int kFuse, int kEG = 1, bool kStg = false, bool kTA = false>
