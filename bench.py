@@ -307,6 +307,7 @@ def time_workload(dg, torch, wl, precision, steps, warmup, rank, barrier, device
     fused_ms = step_ms
 
     e2e_s = None
+    copy_floor = None
     if e2e:
         go_p, w_p = go_h.pin_memory(), w_h.pin_memory()
         gi_p = torch.empty(wl.gi_shape, pin_memory=True)
@@ -321,10 +322,29 @@ def time_workload(dg, torch, wl, precision, steps, warmup, rank, barrier, device
             ts.append(time.perf_counter() - t0)
         e2e_s = statistics.mean(ts)
         plan.check()
+        # The host link's floor for the same bytes: plain copies of the same
+        # pinned buffers (grad_out and W up, grad_input down), one after the
+        # other on one stream, and with the download on a second stream.
+        go_d, w_d, gi_d = torch.empty_like(go), torch.empty_like(w), torch.empty_like(gi)
+        down = torch.cuda.Stream()
+
+        def copies(overlap):
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            go_d.copy_(go_p, non_blocking=True)
+            w_d.copy_(w_p, non_blocking=True)
+            with torch.cuda.stream(down if overlap else stream):
+                gi_p.copy_(gi_d, non_blocking=True)
+            torch.cuda.synchronize()
+            return time.perf_counter() - t0
+
+        for ov in (False, True):
+            copies(ov)
+        copy_floor = {ov: statistics.mean(copies(ov) for _ in range(max(5, min(steps, 50)))) for ov in (False, True)}
     info = plan.info
     plan.close()
     return {"ms_per_step": step_ms, "main_ms": main_ms, "prepack_ms": prepack_ms, "fused_ms": fused_ms,
-            "e2e_s": e2e_s, "clocks": clock_info, "plan": info, "flops": info["useful_flops"],
+            "e2e_s": e2e_s, "copy_floor_s": copy_floor, "clocks": clock_info, "plan": info, "flops": info["useful_flops"],
             "bytes": info["algorithmic_bytes"], "steps": steps}
 
 
@@ -408,6 +428,10 @@ def build_line(args, wl, r, world):
         line["e2e"] = {"value": world * flops / r["e2e_s"] / 1e12, "unit": "TFLOP/s",
                        "h2d_bytes_per_step": go_b + w_b, "d2h_bytes_per_step": gi_b,
                        "us_per_call": r["e2e_s"] * 1e6, "api": "dgrad_run_host (pinned host buffers)"}
+        if r.get("copy_floor_s"):
+            # plain pinned copies of the same bytes, no kernels: the host link's floor
+            line["e2e"]["copy_floor_us"] = {"serial": r["copy_floor_s"][False] * 1e6,
+                                            "up_and_down_overlapped": r["copy_floor_s"][True] * 1e6}
     return line
 
 

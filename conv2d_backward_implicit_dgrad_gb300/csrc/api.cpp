@@ -104,10 +104,9 @@ void fill_info(const Geometry &g, const Tiling &t, int precision, size_t ws, dgr
     info->tile_blocks = t.tm; info->slice_n = t.bn; info->n_slices = t.n_slices;
     info->chunk_k = t.kc; info->n_chunks = t.n_chunks;
     info->n_work = t.n_work;
-    info->grid = t.path == DGRAD_PATH_SIMT ? (int)t.n_work : t.grid;
+    info->grid = t.path == DGRAD_PATH_SIMT && !t.a_tma ? (int)t.n_work : t.grid;
     info->b_resident = t.b_resident;
-    info->a_source = t.path == DGRAD_PATH_TCGEN05 ? (t.a_tmem ? 4 : t.a_staged ? 3 : t.a_tma ? 1 : 2)
-                                                  : (t.path == DGRAD_PATH_COL2IM ? 1 : 0);
+    info->a_source = t.path == DGRAD_PATH_COL2IM ? 1 : t.a_tmem ? 4 : t.a_staged ? 3 : t.a_tma ? 1 : 2;
     info->smem_bytes = t.smem_bytes;
     info->tmem_cols = t.tmem_cols;
     info->group_taps = t.grouped ? 1 : (t.pgroup ? 2 : 0);
@@ -174,19 +173,22 @@ void fill_params(dgrad_plan_s *pl) {
     f.vec = plane % 4 == 0 ? 1 : 0;
 }
 
-// Tensor map of the packed frame [positions][co_v] (fp32): boxes of 32
-// channels (128 bytes, 128-byte swizzle: the MMA's K-major operand layout)
-// by a_box_rows positions; rows past the frame read as zeros.
+// Tensor map of the packed frame [positions][co_v] (fp32) by a_box_rows
+// positions; rows past the frame read as zeros.  tcgen05 and col2im: boxes
+// of 32 channels (128 bytes, 128-byte swizzle: the MMA's K-major operand
+// layout); FFMA path: boxes of 4 channels (16 bytes, no swizzle), one per
+// 4-channel group of the FFMA loop's band layout.
 dgrad_status_t encode_frame_map(dgrad_plan_s *pl) {
     auto fn = dgrad::tensor_map_encoder();
     if (!fn) return DGRAD_ERR_CUDA;
+    const bool ffma = pl->t.path == DGRAD_PATH_SIMT;
     const cuuint64_t dims[2] = {(cuuint64_t)pl->t.co_v, (cuuint64_t)pl->g.positions};
     const cuuint64_t strides[1] = {(cuuint64_t)pl->t.co_v * 4};
-    const cuuint32_t box[2] = {32u, (cuuint32_t)pl->t.a_box_rows};
+    const cuuint32_t box[2] = {ffma ? 4u : 32u, (cuuint32_t)pl->t.a_box_rows};
     const cuuint32_t es[2] = {1u, 1u};
     CUresult r = fn(&pl->mp.a_map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, pl->frame, dims, strides, box, es,
-                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, ffma ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? DGRAD_OK : DGRAD_ERR_CUDA;
 }
 
@@ -387,9 +389,7 @@ dgrad_status_t dgrad_plan_ex(int N, int Ci, int H, int W, int Co, int kH, int kW
     // Workspace: the error word (256 B), the packed weights, then (tensor-
     // copy mode) the packed grad_out frame, each 256-byte aligned.
     const size_t wp_bytes = (pl->t.packed_bytes + 255) & ~size_t(255);
-    const bool has_frame =
-        (pl->t.path == DGRAD_PATH_TCGEN05 || pl->t.path == DGRAD_PATH_COL2IM) && pl->t.a_tma && !pl->t.a_staged &&
-        !pl->t.a_tmem;
+    const bool has_frame = pl->t.a_tma && !pl->t.a_staged && !pl->t.a_tmem;
     size_t ws = 256 + wp_bytes + (has_frame ? pl->t.frame_bytes : 0);
     void *mem = nullptr;
     if (cudaMalloc(&mem, ws) != cudaSuccess) {

@@ -176,6 +176,18 @@ inline bool use_vec_producer(const Geometry &g, const Tiling &t) {
     return t.path == DGRAD_PATH_TCGEN05 && (g.oH * g.oW) % 4 == 0 && (t.a_rows + img - 1) / img + 1 <= kMaxBandImages;
 }
 
+// FFMA path with a frame (simt_pipe_kernel): eight compute warps and one
+// loader warp; a barrier block, then a ring of stages, each the band's KC/4
+// groups of a_rows 16-byte rows followed by the phase's weights (at most
+// `taps` taps of KC x bn), padded to 128 bytes.
+constexpr int kSimtCompute = 256;
+constexpr int kSimtPipeThreads = kSimtCompute + 32;
+constexpr int kSimtMaxStages = 6;
+constexpr int kSimtPipeHeader = 1024;
+__host__ __device__ constexpr int simt_stage_bytes(int a_rows, int kc, int bn, int taps) {
+    return ((kc / 4) * a_rows * 16 + taps * kc * bn * 4 + 127) / 128 * 128;
+}
+
 // ---------------------------------------------------------------- kernels
 // Packed weights.  One (slice sl, chunk c) is one contiguous block of
 // chunk_bytes holding, for every tap t, input channel j of the slice and

@@ -405,27 +405,46 @@ bool size_tc(const Geometry &g, Tiling &t, int want_resident) {
     return true;
 }
 
-bool size_simt(const Geometry &g, Tiling &t) {
+// FFMA path.  Frame plans (a_tma): the band is a_nbox tensor copies of
+// a_box_rows <= 256 rows per 4-channel group, a ring of as many stages as
+// fit (at least two), one persistent CTA per SM.  Without a frame: one stage,
+// one CTA per work unit.
+bool size_simt(const Geometry &g, Tiling &t, int sm_count) {
     t.tm = 1;
     t.n_slices = ceil_div(g.Ci, t.bn);
     t.n_chunks = ceil_div(g.Co, t.kc);
-    t.a_rows = round_up(kBlockM + g.max_shift, 8);
     t.chunk_bytes = g.n_taps * t.kc * t.bn * 4;
     int max_phase_taps = 0;
     for (int p = 0; p < g.n_phases; ++p) max_phase_taps = std::max(max_phase_taps, g.phase[p].tap_count);
-    int a_bytes = t.a_rows * t.kc * 4;
-    int b_bytes = max_phase_taps * t.kc * t.bn * 4;
-    t.a_stages = 1;
-    t.b_stages = 1;
+    t.tap_group = std::max(1, max_phase_taps);
     t.b_resident = 0;
-    t.smem_bytes = a_bytes + b_bytes;
-    if (t.smem_bytes > kMaxSmem) return false;
     t.acc_bufs = t.acc_cols = t.tmem_cols = 0;
     t.tile_step = kBlockM;
     t.n_tiles = (int)((g.positions + kBlockM - 1) / kBlockM);
     t.n_work = (long long)t.n_tiles * t.n_slices * g.n_phases;
-    t.grid = 0;
     t.packed_bytes = (size_t)t.n_slices * t.n_chunks * (size_t)t.chunk_bytes;
+    const int raw = kBlockM + g.max_shift;
+    t.band_rows = raw;
+    if (t.a_tma) {
+        t.a_nbox = ceil_div(raw, 256);
+        t.a_box_rows = round_up(ceil_div(raw, t.a_nbox), 8);
+        t.a_rows = t.a_nbox * t.a_box_rows;
+        const int stage = simt_stage_bytes(t.a_rows, t.kc, t.bn, t.tap_group);
+        const int stages = std::min(kSimtMaxStages, (kMaxSmem - kSimtPipeHeader) / stage);
+        if (stages < 2 || t.n_work > INT_MAX) return false;
+        t.a_stages = t.b_stages = stages;
+        t.smem_bytes = kSimtPipeHeader + stages * stage;
+        t.grid = (int)std::min<long long>(t.n_work, sm_count);
+        return true;
+    }
+    t.a_rows = round_up(raw, 8);
+    const int a_bytes = t.a_rows * t.kc * 4;
+    const int b_bytes = max_phase_taps * t.kc * t.bn * 4;
+    t.a_stages = 1;
+    t.b_stages = 1;
+    t.smem_bytes = a_bytes + b_bytes;
+    if (t.smem_bytes > kMaxSmem) return false;
+    t.grid = 0;
     return true;
 }
 
@@ -528,7 +547,31 @@ dgrad_status_t choose_tiling(const Geometry &g, int precision, const dgrad_optio
         if (t.bn != 16 && t.bn != 32 && t.bn != 64) return DGRAD_ERR_INVALID_ARG;
         t.kc = o.chunk_k ? o.chunk_k : 16;
         if (t.kc != 8 && t.kc != 16 && t.kc != 32) return DGRAD_ERR_INVALID_ARG;
-        if (!size_simt(g, t)) return DGRAD_ERR_UNSUPPORTED;
+        if (o.a_source < 0 || o.a_source > 4) return DGRAD_ERR_INVALID_ARG;
+        if (o.a_source == 3 || o.a_source == 4) return DGRAD_ERR_UNSUPPORTED;
+        // grad_out reaches the FFMA loop as tensor copies of the packed frame
+        // (the pipelined kernel), or gathered by the CTA's own threads
+        // (a_source 2, and plans without a frame buffer).  Automatic: the
+        // frame where every phase has at most 4 taps.  The frame costs a pack
+        // pass and its kernel's FFMA loop runs no faster than the gather's
+        // (both are bound by the shared-memory reads of the register tiles);
+        // it wins where the band fill is a large share of a chunk's work,
+        // i.e. few taps per chunk (measured: pointwise step 244 us vs 341,
+        // strided_downsample 175 vs 184; resnet_stage 204 vs 200, the stem
+        // 1625 vs 1268).
+        t.co_v = std::max(32, round_up(g.Co, 4));
+        t.frame_bytes = (size_t)g.positions * t.co_v * 4;
+        const bool frame_fits = t.frame_bytes <= kMaxFrameBytes && (long long)g.positions * t.co_v <= INT_MAX;
+        if (o.a_source == 1 && (long long)g.positions * t.co_v > INT_MAX) return DGRAD_ERR_UNSUPPORTED;
+        int max_phase_taps = 0;
+        for (int p = 0; p < g.n_phases; ++p) max_phase_taps = std::max(max_phase_taps, g.phase[p].tap_count);
+        t.a_tma = o.a_source == 2 ? 0 : o.a_source == 1 ? 1 : (frame_fits && max_phase_taps <= 4) ? 1 : 0;
+        if (!size_simt(g, t, sm_count)) {
+            if (o.a_source != 0 || !t.a_tma) return DGRAD_ERR_UNSUPPORTED;
+            t.a_tma = 0;   // automatic: a ring of two stages does not fit; gather instead
+            if (!size_simt(g, t, sm_count)) return DGRAD_ERR_UNSUPPORTED;
+        }
+        if (!t.a_tma) t.frame_bytes = 0;
         *out = t;
         return DGRAD_OK;
     }

@@ -118,7 +118,12 @@ typedef struct {
                           of the main kernel -- no frame and no grad_out pass, results bit for bit those
                           of the frame; needs oH*oW % 4 == 0 and one 128-row block whose band plus
                           alignment fits one copy (128 + largest tap shift + 3 <= 256 rows), else
-                          DGRAD_ERR_UNSUPPORTED */
+                          DGRAD_ERR_UNSUPPORTED.
+                          FFMA path (DGRAD_PATH_SIMT): 0 automatic (1 where every phase has at most 4
+                          taps and the frame fits in 2 GiB, else 2), 1 packed frame + a loader warp's
+                          tensor copies into a ring of stages under mbarriers, persistent CTAs (the
+                          pack kernel writes the frame, fp32), 2 every thread of the CTA gathers the
+                          band from NCHW grad_out (no frame); 3 and 4 DGRAD_ERR_UNSUPPORTED */
     int group_taps;    /* tcgen05 path, taps issued as one MMA: 0 automatic (3 where it applies; for
                           one phase (stride 1) in TF32 with slice_n < 128 and kW >= 2, 1 where it fits;
                           else none), 1 the taps of one kernel row (N = taps x slice_n, sub-accumulators
@@ -151,8 +156,8 @@ typedef struct {
     long long n_work;      /* work units of the main kernel */
     int grid;              /* CTAs of the main kernel */
     int b_resident;        /* 1: packed weights stay in shared memory for the whole launch */
-    int a_source;          /* tcgen05 path: 1 packed frame + tensor copies, 2 producer warps, 3 staged,
-                              4 tensor memory */
+    int a_source;          /* 1 packed frame + tensor copies, 2 producer warps (FFMA path: the CTA's
+                              own gather), 3 staged, 4 tensor memory; col2im path: 1 */
     int smem_bytes;        /* dynamic shared memory of the main kernel */
     int tmem_cols;         /* tensor-memory columns allocated per CTA (tcgen05 path) */
     int group_taps;        /* tcgen05 path: 0 one MMA per tap, 1 per kernel row of taps, 2 per shared shift */

@@ -89,3 +89,32 @@ def test_host_pipeline_reports_a_sub_plan_timeout():
         with pytest.raises(dg.DgradError) as exc:
             plan.run_host(go_h.contiguous(), w_h.contiguous(), torch.empty(wl.gi_shape, pin_memory=True))
         assert exc.value.status == TIMEOUT_STATUS
+
+
+@pytest.mark.parametrize("name", ["tiny", "pointwise"])
+def test_ffma_pipeline_wait_that_runs_out(name):
+    # The FFMA path's frame pipeline bounds its waits the same way: with
+    # wait_test the compute warps first wait on a barrier nothing completes,
+    # the loader's wait for a free stage then runs out too, and the launch
+    # ends by itself with the timeout recorded.
+    wl = WORKLOADS[name]
+    go_h, w_h = make_inputs(wl, 8)
+    go, w = go_h.cuda(), w_h.cuda()
+    with dg.Plan(*wl.plan_args(), precision="fp32", a_source="frame", timeout_us=SHORT_US, wait_test=1) as plan:
+        gi = torch.full(wl.gi_shape, float("nan"), device="cuda")
+        t0 = time.perf_counter()
+        plan.run(go, w, gi)
+        torch.cuda.synchronize()
+        elapsed = time.perf_counter() - t0
+        with pytest.raises(dg.DgradError) as exc:
+            plan.check()
+        assert exc.value.status == TIMEOUT_STATUS
+        plan.check()
+    assert elapsed < 5.0
+    ref, _ = oracle.dgrad(go_h, w_h, wl.H, wl.W, wl.stride, wl.pad_h, wl.pad_w)
+    with dg.Plan(*wl.plan_args(), precision="fp32", a_source="frame") as plan:
+        out = plan.run(go, w)
+        torch.cuda.synchronize()
+        plan.check()
+    got = out.cpu().double().numpy()
+    assert np.linalg.norm((got - ref).ravel()) <= 1e-5 * np.linalg.norm(ref.ravel())

@@ -260,6 +260,43 @@ def test_simt_tilings(opts):
     check((N, Ci, H, W, Co, kH, kW, s, ph, pw), go, w, "fp32", path="simt", **opts)
 
 
+# FFMA path: grad_out reaches the FFMA loop either as tensor copies of the
+# packed frame (the pipelined kernel) or through the CTA's own gather.  Both
+# agree with the oracle, and, summing the same products in the same order,
+# with each other bit for bit.  Shapes in plan order (N, Ci, H, W, Co, kH, kW,
+# s, ph, pw): the workloads, ragged channel counts, several phases, a band of
+# more than 256 rows (two tensor copies per channel group), a kernel wider
+# than the stride, and phases without taps.
+FFMA_SHAPES = [WORKLOADS[n].plan_args() for n in ("tiny", "strided_downsample", "pointwise")] + [
+    (2, 64, 20, 20, 64, 3, 3, 1, 1, 1), (3, 33, 12, 12, 70, 3, 3, 1, 1, 1), (2, 40, 36, 19, 23, 3, 3, 2, 1, 1),
+    (1, 3, 80, 80, 8, 7, 7, 2, 3, 3), (3, 5, 17, 19, 33, 1, 1, 2, 0, 0), (2, 17, 9, 11, 5, 5, 3, 3, 2, 1),
+    (1, 20, 40, 40, 40, 3, 3, 4, 1, 1)]
+
+
+@pytest.mark.parametrize("args", FFMA_SHAPES)
+def test_ffma_sources_agree(args):
+    N, Ci, H, W, Co, kH, kW, s, ph, pw = args
+    go, w = make_tensors((N, Co, out_ext(H, kH, s, ph), out_ext(W, kW, s, pw)), (Co, Ci, kH, kW), 91, "kaiming")
+    ref, _ = oracle.dgrad(go, w, H, W, s, ph, pw)
+    outs = {}
+    for src in ("frame", "producers"):
+        gpu, info = run_gpu(args, go, w, "fp32", a_source=src)
+        assert info["path"] == "simt" and info["a_source"] == src
+        assert_fp32(gpu, ref)
+        outs[src] = gpu
+    assert np.array_equal(outs["frame"], outs["producers"])
+
+
+@pytest.mark.parametrize("a_source", ["frame", "producers"])
+@pytest.mark.parametrize("opts", [dict(slice_n=16), dict(slice_n=32, chunk_k=8), dict(chunk_k=32)])
+def test_simt_tilings_each_source(opts, a_source):
+    shape = (2, 40, 36, 19, 23, 3, 3, 2, 1, 1)
+    N, Ci, Co, H, W, kH, kW, s, ph, pw = shape
+    go, w = make_tensors((N, Co, out_ext(H, kH, s, ph), out_ext(W, kW, s, pw)), (Co, Ci, kH, kW), 79, "kaiming")
+    info = check((N, Ci, H, W, Co, kH, kW, s, ph, pw), go, w, "fp32", path="simt", a_source=a_source, **opts)
+    assert info["a_source"] == a_source
+
+
 def test_simt_with_tf32_operands():
     # The FFMA path on TF32-rounded operands satisfies the TF32 bar too.
     shape = (2, 24, 40, 13, 15, 3, 3, 1, 1, 1)

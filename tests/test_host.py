@@ -680,3 +680,28 @@ def test_col2im_plans():
         with pytest.raises(dg.DgradError) as e:
             dg.describe(*wl.plan_args(), path="col2im", **bad)
         assert e.value.status == 2
+
+
+def test_ffma_source_plans():
+    # FFMA path: the frame pipeline automatically where every phase has at most
+    # 4 taps (the band fill is then a large share of a chunk's work), the
+    # CTA's own gather elsewhere; either on request; no staged or tensor-memory
+    # source.
+    expect = {"tiny": "producers", "resnet_stage": "producers", "strided_downsample": "frame",
+              "pointwise": "frame", "stem": "producers"}
+    for name, src in expect.items():
+        wl = WORKLOADS[name]
+        d = dg.describe(*wl.plan_args(), "fp32")
+        assert d["path"] == "simt" and d["a_source"] == src, name
+        f = dg.describe(*wl.plan_args(), "fp32", a_source="frame")
+        assert f["a_source"] == "frame"
+        assert f["grid"] == min(f["n_work"], 152) and 2 <= f["a_stages"] <= 6
+        assert f["smem_bytes"] <= 232448
+        # the band: 128 rows plus the largest tap shift, in copies of at most 256 rows
+        assert f["a_rows"] >= 128 + f["max_shift"] and f["a_rows"] % 8 == 0
+        g = dg.describe(*wl.plan_args(), "fp32", a_source="producers")
+        assert g["a_source"] == "producers" and g["grid"] == g["n_work"]
+        for bad in ("staged", "tmem"):
+            with pytest.raises(dg.DgradError) as e:
+                dg.describe(*wl.plan_args(), "fp32", a_source=bad)
+            assert e.value.status == 2
