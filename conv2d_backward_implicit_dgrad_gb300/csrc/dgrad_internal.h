@@ -18,6 +18,7 @@ constexpr int kMaxPhases = 16;
 constexpr int kMaxStride = 4;
 constexpr int kBlockM = 128;          // GEMM rows (output positions) per MMA block
 constexpr int kMaxSmem = 232448;      // opt-in dynamic shared memory per CTA on sm_103
+constexpr int kSmemPerSm = 233472;    // shared memory of one SM (each resident CTA also reserves 1 KB)
 constexpr int kTmemCols = 512;        // tensor-memory columns per SM
 constexpr int kMaxSub = 4;            // taps of one kernel row grouped into one MMA (sub-accumulators)
 
@@ -147,6 +148,7 @@ struct Tiling {
                        //    written by the epilogue warps into tensor memory, where the MMA reads A; no frame
     int a_tslots;      // a_tmem: tensor-memory A slots (32 columns each)
     int a_tcol;        // a_tmem: first tensor-memory column of the A slots (after the accumulators)
+    int simt_wide;     // FFMA frame pipeline: 8 x 8 register tiles, 128 compute threads, two CTAs per SM
     int a_box_rows;    // rows of one A tensor copy (<= 256)
     int a_nbox;        // tensor copies per A stage
     int co_v;          // channels per packed frame row
@@ -176,12 +178,12 @@ inline bool use_vec_producer(const Geometry &g, const Tiling &t) {
     return t.path == DGRAD_PATH_TCGEN05 && (g.oH * g.oW) % 4 == 0 && (t.a_rows + img - 1) / img + 1 <= kMaxBandImages;
 }
 
-// FFMA path with a frame (simt_pipe_kernel): eight compute warps and one
-// loader warp; a barrier block, then a ring of stages, each the band's KC/4
-// groups of a_rows 16-byte rows followed by the phase's weights (at most
-// `taps` taps of KC x bn), padded to 128 bytes.
-constexpr int kSimtCompute = 256;
-constexpr int kSimtPipeThreads = kSimtCompute + 32;
+// FFMA path with a frame (simt_pipe_kernel): eight compute warps (8 x 4
+// register tiles; `wide`: four, 8 x 8 tiles, two CTAs per SM) and one loader
+// warp; a barrier block, then a ring of stages, each the band's KC/4 groups of
+// a_rows 16-byte rows followed by the phase's weights (at most `taps` taps of
+// KC x bn), padded to 128 bytes.
+__host__ __device__ constexpr int simt_pipe_threads(bool wide) { return (wide ? 128 : 256) + 32; }
 constexpr int kSimtMaxStages = 6;
 constexpr int kSimtPipeHeader = 1024;
 __host__ __device__ constexpr int simt_stage_bytes(int a_rows, int kc, int bn, int taps) {

@@ -430,11 +430,22 @@ bool size_simt(const Geometry &g, Tiling &t, int sm_count) {
         t.a_box_rows = round_up(ceil_div(raw, t.a_nbox), 8);
         t.a_rows = t.a_nbox * t.a_box_rows;
         const int stage = simt_stage_bytes(t.a_rows, t.kc, t.bn, t.tap_group);
-        const int stages = std::min(kSimtMaxStages, (kMaxSmem - kSimtPipeHeader) / stage);
-        if (stages < 2 || t.n_work > INT_MAX) return false;
+        if (t.n_work > INT_MAX) return false;
+        // 64-channel slices of phases with more than 4 taps (the FFMA loop,
+        // not the fill, sets the pace): 8 x 8 register tiles, two CTAs per
+        // SM, when two stages each fit in half of the SM's shared memory
+        // (228 KB, 1 KB per CTA reserved).  Measured (main kernel, frame):
+        // resnet_stage 182 us vs 194 with 8 x 4 tiles; with few taps the
+        // half-size CTAs lose on balance (strided_downsample: 456 units on
+        // 304 CTAs, 203 us vs 170) or, resident early under the dependent
+        // launch, slow the pack (pointwise step 259 us vs 244).
+        const int half = (kSmemPerSm / 2 - 1024 - kSimtPipeHeader) / stage;
+        t.simt_wide = t.bn == 64 && t.tap_group > 4 && half >= 2 ? 1 : 0;
+        const int stages = std::min(kSimtMaxStages, t.simt_wide ? half : (kMaxSmem - kSimtPipeHeader) / stage);
+        if (stages < 2) return false;
         t.a_stages = t.b_stages = stages;
         t.smem_bytes = kSimtPipeHeader + stages * stage;
-        t.grid = (int)std::min<long long>(t.n_work, sm_count);
+        t.grid = (int)std::min<long long>(t.n_work, (long long)(t.simt_wide ? 2 : 1) * sm_count);
         return true;
     }
     t.a_rows = round_up(raw, 8);
@@ -552,23 +563,27 @@ dgrad_status_t choose_tiling(const Geometry &g, int precision, const dgrad_optio
         // grad_out reaches the FFMA loop as tensor copies of the packed frame
         // (the pipelined kernel), or gathered by the CTA's own threads
         // (a_source 2, and plans without a frame buffer).  Automatic: the
-        // frame where every phase has at most 4 taps.  The frame costs a pack
-        // pass and its kernel's FFMA loop runs no faster than the gather's
-        // (both are bound by the shared-memory reads of the register tiles);
-        // it wins where the band fill is a large share of a chunk's work,
-        // i.e. few taps per chunk (measured: pointwise step 244 us vs 341,
-        // strided_downsample 175 vs 184; resnet_stage 204 vs 200, the stem
-        // 1625 vs 1268).
+        // frame where every phase has at most 4 taps, or where the frame
+        // pipeline runs 8 x 8 register tiles; else the gather.  The frame
+        // costs a pack pass, and with the same 8 x 4 tiles its FFMA loop runs
+        // no faster than the gather's (both are bound by the shared-memory
+        // reads of the register tiles): it wins where the band fill is a large
+        // share of a chunk's work, i.e. few taps per chunk (measured steps:
+        // pointwise 244 us vs 341, strided_downsample 175 vs 184), or with
+        // the larger tiles (resnet_stage 195 vs 200; with 8 x 4 tiles 204);
+        // the stem (16-channel slices) 1625 vs 1268.
         t.co_v = std::max(32, round_up(g.Co, 4));
         t.frame_bytes = (size_t)g.positions * t.co_v * 4;
         const bool frame_fits = t.frame_bytes <= kMaxFrameBytes && (long long)g.positions * t.co_v <= INT_MAX;
         if (o.a_source == 1 && (long long)g.positions * t.co_v > INT_MAX) return DGRAD_ERR_UNSUPPORTED;
         int max_phase_taps = 0;
         for (int p = 0; p < g.n_phases; ++p) max_phase_taps = std::max(max_phase_taps, g.phase[p].tap_count);
-        t.a_tma = o.a_source == 2 ? 0 : o.a_source == 1 ? 1 : (frame_fits && max_phase_taps <= 4) ? 1 : 0;
-        if (!size_simt(g, t, sm_count)) {
-            if (o.a_source != 0 || !t.a_tma) return DGRAD_ERR_UNSUPPORTED;
-            t.a_tma = 0;   // automatic: a ring of two stages does not fit; gather instead
+        t.a_tma = o.a_source == 2 ? 0 : o.a_source == 1 ? 1 : frame_fits ? 1 : 0;
+        bool sized = size_simt(g, t, sm_count);
+        if (!sized && (o.a_source != 0 || !t.a_tma)) return DGRAD_ERR_UNSUPPORTED;
+        if (o.a_source == 0 && t.a_tma && (!sized || (max_phase_taps > 4 && !t.simt_wide))) {
+            t.a_tma = 0;   // automatic: no ring of two stages, or 8 x 4 tiles on many taps; gather instead
+            t.simt_wide = 0;
             if (!size_simt(g, t, sm_count)) return DGRAD_ERR_UNSUPPORTED;
         }
         if (!t.a_tma) t.frame_bytes = 0;

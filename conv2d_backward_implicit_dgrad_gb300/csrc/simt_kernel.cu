@@ -156,13 +156,23 @@ __device__ __forceinline__ void decode_unit(const MainParams &p, int u, int &til
     phase = rem - slice * p.n_phases;
 }
 
-template <int BN, int KC>
-__global__ void __launch_bounds__(kSimtPipeThreads, 1) simt_pipe_kernel(const __grid_constant__ MainParams p) {
+// kWide (BN = 64): 128 compute threads, each an 8 x 8 register tile --
+// positions w*32 + tp + 4i (i < 8) of compute warp w and channels tc + 8j
+// (j < 8), lane = (tc << 2) | tp -- and two CTAs per SM.  A 16-byte warp load
+// takes four shared-memory passes (one per quarter warp): the 8 x 4 tiles'
+// 12 loads per 128 FFMAs ask 0.375 passes per FFMA instruction of a port that
+// serves 0.25 (four FFMA pipes, one pass per clock); the 8 x 8 tiles' 16 loads
+// per 256 FFMAs ask 0.25.
+template <int BN, int KC, bool kWide>
+__global__ void __launch_bounds__(simt_pipe_threads(kWide), kWide ? 2 : 1)
+    simt_pipe_kernel(const __grid_constant__ MainParams p) {
     extern __shared__ __align__(1024) uint8_t smem[];
+    static_assert(!kWide || BN == 64, "8 x 8 tiles: 64-channel slices");
+    constexpr int NC = simt_pipe_threads(kWide) - 32;   // compute threads
     constexpr int G = KC / 4;           // 4-channel groups per chunk
-    constexpr int CG = BN / 4;          // threads along input channels
-    constexpr int PG = kSimtCompute / CG;   // threads along positions
-    constexpr int PPT = kBlockM / PG;   // positions per thread
+    constexpr int CG = BN / 4;          // threads along input channels (8 x 4 tiles)
+    constexpr int PG = kWide ? 1 : NC / CG;   // threads along positions (8 x 4 tiles)
+    constexpr int PPT = kWide ? 8 : kBlockM / PG;   // positions per thread
     PipeBars *bars = reinterpret_cast<PipeBars *>(smem);
     uint8_t *stages = smem + kSimtPipeHeader;
     const int a_bytes = G * p.a_rows * 16;
@@ -174,7 +184,7 @@ __global__ void __launch_bounds__(kSimtPipeThreads, 1) simt_pipe_kernel(const __
     if (tid == 0) {
         for (int i = 0; i < p.a_stages; ++i) {
             dev::mbar_init(dev::smem_u32(&bars->full[i]), 1);
-            dev::mbar_init(dev::smem_u32(&bars->empty[i]), kSimtCompute / 32);
+            dev::mbar_init(dev::smem_u32(&bars->empty[i]), NC / 32);
         }
         dev::mbar_init(dev::smem_u32(&bars->never), 1);
         bars->abort_flag = 0;
@@ -182,7 +192,7 @@ __global__ void __launch_bounds__(kSimtPipeThreads, 1) simt_pipe_kernel(const __
     }
     __syncthreads();
 
-    if (warp == kSimtCompute / 32) {
+    if (warp == NC / 32) {
         // ------------------------------------------------------------ loader
         if (lane == 0) {
             dev::prefetch_tensormap(&p.a_map);
@@ -230,7 +240,10 @@ __global__ void __launch_bounds__(kSimtPipeThreads, 1) simt_pipe_kernel(const __
     }
 
     // --------------------------------------------------------- compute warps
+    // 8 x 4 tiles: positions pg + i*PG, channels cg*4 + j; 8 x 8 tiles:
+    // positions prow + 4i, channels tc + 8j
     const int cg = tid / PG, pg = tid % PG;
+    const int tp = lane & 3, tc = lane >> 2, prow = warp * 32 + tp;
     Ring ring;
     bool ok = true;
     // Failure-detection test: a bounded wait on a barrier that nothing
@@ -245,11 +258,12 @@ __global__ void __launch_bounds__(kSimtPipeThreads, 1) simt_pipe_kernel(const __
         decode_unit(p, u, tile, slice, phase);
         const PhaseDesc &pd = p.phase[phase];
         const int P0 = tile * kBlockM;
-        float acc[PPT][4];
+        constexpr int CPT = kWide ? 8 : 4;   // channels per thread
+        float acc[PPT][CPT];
 #pragma unroll
         for (int i = 0; i < PPT; ++i)
 #pragma unroll
-            for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
+            for (int j = 0; j < CPT; ++j) acc[i][j] = 0.f;
         for (int c = 0; pd.tap_count > 0 && c < p.n_chunks; ++c) {
             if (!__all_sync(0xffffffffu, dev::mbar_wait(dev::smem_u32(&bars->full[ring.stage]), ring.parity, tmo))) {
                 if (lane == 0) pipe_fail(bars, p);
@@ -261,20 +275,42 @@ __global__ void __launch_bounds__(kSimtPipeThreads, 1) simt_pipe_kernel(const __
             const float4 *B4 = reinterpret_cast<const float4 *>(st + a_bytes);
             for (int t = 0; t < pd.tap_count; ++t) {
                 const int shift = p.tap[pd.tap_begin + t].shift;
+                if constexpr (kWide) {
+                    const float4 *Ab = A4 + prow + shift;
+                    const float4 *Bb = B4 + t * G * BN + tc;
 #pragma unroll
-                for (int g = 0; g < G; ++g) {
-                    float4 b[4];
+                    for (int g = 0; g < G; ++g) {
+                        float4 a[8], b[8];
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) b[j] = B4[(t * G + g) * BN + cg * 4 + j];
+                        for (int i = 0; i < 8; ++i) a[i] = Ab[g * p.a_rows + 4 * i];
 #pragma unroll
-                    for (int i = 0; i < PPT; ++i) {
-                        const float4 a = A4[g * p.a_rows + pg + i * PG + shift];
+                        for (int j = 0; j < 8; ++j) b[j] = Bb[g * BN + 8 * j];
 #pragma unroll
-                        for (int j = 0; j < 4; ++j) {
-                            acc[i][j] = fmaf(a.x, b[j].x, acc[i][j]);
-                            acc[i][j] = fmaf(a.y, b[j].y, acc[i][j]);
-                            acc[i][j] = fmaf(a.z, b[j].z, acc[i][j]);
-                            acc[i][j] = fmaf(a.w, b[j].w, acc[i][j]);
+                        for (int i = 0; i < 8; ++i)
+#pragma unroll
+                            for (int j = 0; j < 8; ++j) {
+                                acc[i][j] = fmaf(a[i].x, b[j].x, acc[i][j]);
+                                acc[i][j] = fmaf(a[i].y, b[j].y, acc[i][j]);
+                                acc[i][j] = fmaf(a[i].z, b[j].z, acc[i][j]);
+                                acc[i][j] = fmaf(a[i].w, b[j].w, acc[i][j]);
+                            }
+                    }
+                } else {
+#pragma unroll
+                    for (int g = 0; g < G; ++g) {
+                        float4 b[4];
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) b[j] = B4[(t * G + g) * BN + cg * 4 + j];
+#pragma unroll
+                        for (int i = 0; i < PPT; ++i) {
+                            const float4 a = A4[g * p.a_rows + pg + i * PG + shift];
+#pragma unroll
+                            for (int j = 0; j < 4; ++j) {
+                                acc[i][j] = fmaf(a.x, b[j].x, acc[i][j]);
+                                acc[i][j] = fmaf(a.y, b[j].y, acc[i][j]);
+                                acc[i][j] = fmaf(a.z, b[j].z, acc[i][j]);
+                                acc[i][j] = fmaf(a.w, b[j].w, acc[i][j]);
+                            }
                         }
                     }
                 }
@@ -289,14 +325,14 @@ __global__ void __launch_bounds__(kSimtPipeThreads, 1) simt_pipe_kernel(const __
         // or apply the fused epilogue.
 #pragma unroll
         for (int i = 0; i < PPT; ++i) {
-            const int P = P0 + pg + i * PG;
+            const int P = P0 + (kWide ? prow + 4 * i : pg + i * PG);
             int n, q, uu;
             dev::decode_position(p, P, n, q, uu);
             if (P >= p.positions || q >= pd.Hq || uu >= pd.Wq) continue;
             const int ih = p.s * q + pd.a, iw = p.s * uu + pd.b;
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const int ci = slice * BN + cg * 4 + j;
+            for (int j = 0; j < CPT; ++j) {
+                const int ci = slice * BN + (kWide ? tc + 8 * j : cg * 4 + j);
                 if (ci < p.Ci) {
                     const size_t idx = (static_cast<size_t>(n) * p.Ci + ci) * plane + static_cast<size_t>(ih) * p.W + iw;
                     float v = acc[i][j];
@@ -309,14 +345,14 @@ __global__ void __launch_bounds__(kSimtPipeThreads, 1) simt_pipe_kernel(const __
     }
 }
 
-template <int BN, int KC>
+template <int BN, int KC, bool kWide>
 cudaError_t launch_pipe_kc(const MainParams &p, const Tiling &t, cudaStream_t stream) {
-    auto kern = simt_pipe_kernel<BN, KC>;
+    auto kern = simt_pipe_kernel<BN, KC, kWide>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, t.smem_bytes);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(t.grid);
-    cfg.blockDim = dim3(kSimtPipeThreads);
+    cfg.blockDim = dim3(simt_pipe_threads(kWide));
     cfg.dynamicSmemBytes = t.smem_bytes;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
@@ -329,10 +365,20 @@ cudaError_t launch_pipe_kc(const MainParams &p, const Tiling &t, cudaStream_t st
 
 template <int BN>
 cudaError_t launch_pipe_bn(const MainParams &p, const Tiling &t, cudaStream_t stream) {
+    if constexpr (BN == 64) {
+        if (t.simt_wide) {
+            switch (t.kc) {
+                case 8: return launch_pipe_kc<BN, 8, true>(p, t, stream);
+                case 16: return launch_pipe_kc<BN, 16, true>(p, t, stream);
+                case 32: return launch_pipe_kc<BN, 32, true>(p, t, stream);
+                default: return cudaErrorInvalidValue;
+            }
+        }
+    }
     switch (t.kc) {
-        case 8: return launch_pipe_kc<BN, 8>(p, t, stream);
-        case 16: return launch_pipe_kc<BN, 16>(p, t, stream);
-        case 32: return launch_pipe_kc<BN, 32>(p, t, stream);
+        case 8: return launch_pipe_kc<BN, 8, false>(p, t, stream);
+        case 16: return launch_pipe_kc<BN, 16, false>(p, t, stream);
+        case 32: return launch_pipe_kc<BN, 32, false>(p, t, stream);
         default: return cudaErrorInvalidValue;
     }
 }

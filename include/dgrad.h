@@ -119,8 +119,9 @@ typedef struct {
                           of the frame; needs oH*oW % 4 == 0 and one 128-row block whose band plus
                           alignment fits one copy (128 + largest tap shift + 3 <= 256 rows), else
                           DGRAD_ERR_UNSUPPORTED.
-                          FFMA path (DGRAD_PATH_SIMT): 0 automatic (1 where every phase has at most 4
-                          taps and the frame fits in 2 GiB, else 2), 1 packed frame + a loader warp's
+                          FFMA path (DGRAD_PATH_SIMT): 0 automatic (1 where the frame fits in 2 GiB and
+                          every phase has at most 4 taps or the slice is 64 channels wide, else 2), 1
+                          packed frame + a loader warp's
                           tensor copies into a ring of stages under mbarriers, persistent CTAs (the
                           pack kernel writes the frame, fp32), 2 every thread of the CTA gathers the
                           band from NCHW grad_out (no frame); 3 and 4 DGRAD_ERR_UNSUPPORTED */
