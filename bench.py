@@ -199,13 +199,14 @@ def cpu_cores():
         return os.cpu_count() or 1
 
 
-def cpu_oracle_run(wl, images, seed=0, reps=1):
-    """Time the oracle (as it stands) on the first `images` images of the workload."""
+def cpu_oracle_run(wl, images, seed=0, reps=1, threads=None):
+    """Time the oracle (as it stands) on the first `images` images of the
+    workload, on all host cores (or `threads` of them)."""
     import oracle
     from conv2d_backward_implicit_dgrad_gb300.workloads import make_tensors
     go, w = make_tensors((images, wl.Co, wl.oH, wl.oW), wl.w_shape, seed, wl.dist)
     go, w = go.numpy(), w.numpy()
-    cores = cpu_cores()
+    cores = cpu_cores() if threads is None else threads
     oracle.build()
     times = []
     for _ in range(reps):
@@ -245,6 +246,57 @@ def reference_arm(args, wl):
     }
     print(json.dumps(line), flush=True)
     return 0
+
+
+def graph_timings(torch, plan, go, w, gi, flush, calls=20, reps=10):
+    """Per-call times from CUDA graphs of `calls` dgrad_run calls, best of
+    `reps` replays: back to back (warm L2: inputs, frame and output stay in
+    L2 between calls), and each call after the L2-flush fill (cold), less a
+    graph of the fills alone.  None if the graphs cannot be captured."""
+    def capture(body):
+        g = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            body()   # warm-up outside the capture
+        torch.cuda.current_stream().wait_stream(side)
+        with torch.cuda.graph(g):
+            body()
+        return g
+
+    def replay_us(g):
+        best = float("inf")
+        s = torch.cuda.current_stream()
+        for _ in range(reps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(s)
+            g.replay()
+            e1.record(s)
+            torch.cuda.synchronize()
+            best = min(best, e0.elapsed_time(e1) * 1e3)
+        return best
+
+    def calls_only():
+        for _ in range(calls):
+            plan.run(go, w, gi, torch.cuda.current_stream())
+
+    def flushed_calls():
+        for _ in range(calls):
+            flush.zero_()
+            plan.run(go, w, gi, torch.cuda.current_stream())
+
+    def flushes():
+        for _ in range(calls):
+            flush.zero_()
+
+    try:
+        warm = replay_us(capture(calls_only)) / calls
+        cold = (replay_us(capture(flushed_calls)) - replay_us(capture(flushes))) / calls
+    except Exception as ex:   # capture not possible on this stack: report why, time nothing
+        torch.cuda.synchronize()
+        return {"error": str(ex).splitlines()[0][:200]}
+    plan.check()
+    return {"warm_us_per_call": warm, "cold_us_per_call": cold, "calls_per_graph": calls, "replays": reps}
 
 
 def time_workload(dg, torch, wl, precision, steps, warmup, rank, barrier, device_index, clocks, e2e, **opts):
@@ -306,6 +358,8 @@ def time_workload(dg, torch, wl, precision, steps, warmup, rank, barrier, device
     main_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in se)
     fused_ms = step_ms
 
+    graph = graph_timings(torch, plan, go, w, gi, flush) if e2e else None
+
     e2e_s = None
     copy_floor = None
     if e2e:
@@ -344,7 +398,7 @@ def time_workload(dg, torch, wl, precision, steps, warmup, rank, barrier, device
     info = plan.info
     plan.close()
     return {"ms_per_step": step_ms, "main_ms": main_ms, "prepack_ms": prepack_ms, "fused_ms": fused_ms,
-            "e2e_s": e2e_s, "copy_floor_s": copy_floor, "clocks": clock_info, "plan": info, "flops": info["useful_flops"],
+            "e2e_s": e2e_s, "copy_floor_s": copy_floor, "graph": graph, "clocks": clock_info, "plan": info, "flops": info["useful_flops"],
             "bytes": info["algorithmic_bytes"], "steps": steps}
 
 
@@ -428,6 +482,10 @@ def build_line(args, wl, r, world):
         line["e2e"] = {"value": world * flops / r["e2e_s"] / 1e12, "unit": "TFLOP/s",
                        "h2d_bytes_per_step": go_b + w_b, "d2h_bytes_per_step": gi_b,
                        "us_per_call": r["e2e_s"] * 1e6, "api": "dgrad_run_host (pinned host buffers)"}
+        if r.get("graph"):
+            line["graph"] = dict(r["graph"], method="CUDA graphs of dgrad_run calls, best of the replays; warm: "
+                                 "back to back; cold: each call after the 256 MiB L2-flush fill, less a graph of "
+                                 "the fills alone")
         if r.get("copy_floor_s"):
             # plain pinned copies of the same bytes, no kernels: the host link's floor
             line["e2e"]["copy_floor_us"] = {"serial": r["copy_floor_s"][False] * 1e6,
@@ -549,6 +607,11 @@ def main():
                 "value": flops / min(times) / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
                 "sample": f"the whole batch ({wl.N} images) of {wl.name}, fp64 scatter oracle, "
                           f"best of {len(times)}"}
+            one = min(wl.N, 2)
+            f1, t1, _ = cpu_oracle_run(wl, one, reps=2, threads=1)
+            line["cpu_baseline"]["single_thread"] = {
+                "value": f1 / min(t1) / 1e12, "unit": "TFLOP/s", "cores": 1,
+                "sample": f"{one} images of {wl.name}, one thread, best of {len(t1)}"}
         print(json.dumps(line), flush=True)
         if args.all:
             for name in WORKLOAD_ORDER:
