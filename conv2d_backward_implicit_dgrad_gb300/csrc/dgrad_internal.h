@@ -184,6 +184,9 @@ inline bool use_vec_producer(const Geometry &g, const Tiling &t) {
 // a_rows 16-byte rows followed by the phase's weights (at most `taps` taps of
 // KC x bn), padded to 128 bytes.
 __host__ __device__ constexpr int simt_pipe_threads(bool wide) { return (wide ? 128 : 256) + 32; }
+// Output positions per work unit of the FFMA gather kernel: 128, or 1024 for
+// 4-channel slices (inputs with at most 4 channels: 256 threads x 4 positions)
+__host__ __device__ constexpr int simt_unit_rows(int bn) { return bn == 4 ? 1024 : 128; }
 constexpr int kSimtMaxStages = 6;
 constexpr int kSimtPipeHeader = 1024;
 __host__ __device__ constexpr int simt_stage_bytes(int a_rows, int kc, int bn, int taps) {

@@ -2,7 +2,8 @@
 // phase split, zero-padded frame geometry and packed weights as the tcgen05
 // path.
 //
-// One work unit is 128 output positions x BN input channels of one phase.
+// One work unit is 128 output positions x BN input channels of one phase
+// (1024 positions for 4-channel slices, inputs with at most 4 channels).
 // For each chunk of KC output channels the frame band [P0, P0 + a_rows) and
 // the phase's packed weights sit in shared memory, and every thread
 // accumulates PPT positions x 4 channels in registers: for each tap and
@@ -18,7 +19,8 @@
 //    persistent over work units, so copies for the next chunks and units run
 //    under the FFMAs and the stores.
 //  - no frame (simt_dgrad_kernel: plans without a frame buffer, such as
-//    dgrad_run_noalloc's): every thread of the CTA gathers the band from NCHW
+//    dgrad_run_noalloc's, and the few-channel, many-tap shapes where the
+//    frame does not pay): every thread of the CTA gathers the band from NCHW
 //    grad_out, then all compute, one stage per chunk.
 #include <cuda_runtime.h>
 
@@ -50,13 +52,14 @@ __global__ void __launch_bounds__(kThreads) simt_dgrad_kernel(const __grid_const
     constexpr int G = KC / 4;           // 4-channel groups per chunk
     constexpr int CG = BN / 4;          // threads along input channels
     constexpr int PG = kThreads / CG;   // threads along positions
-    constexpr int PPT = kBlockM / PG;   // positions per thread
+    constexpr int UM = simt_unit_rows(BN);   // positions per unit
+    constexpr int PPT = UM / PG;        // positions per thread
     float *As = sm;                                            // [G][a_rows][4]
     float *Bs = sm + static_cast<size_t>(G) * p.a_rows * 4;    // [taps][G][BN][4]
 
     const int tile = blockIdx.x, slice = blockIdx.y;
     const PhaseDesc pd = p.phase[blockIdx.z];
-    const int P0 = tile * kBlockM;
+    const int P0 = tile * UM;
     const int tid = threadIdx.x;
     const int cg = tid / PG, pg = tid % PG;
 
@@ -396,6 +399,7 @@ cudaError_t launch_bn(const MainParams &p, const Tiling &t, cudaStream_t stream)
 }  // namespace
 
 cudaError_t launch_simt(const MainParams &p, const Tiling &t, cudaStream_t stream) {
+    if (t.bn == 4) return t.a_tma ? cudaErrorInvalidValue : launch_bn<4>(p, t, stream);
     if (t.a_tma) {
         switch (t.bn) {
             case 16: return launch_pipe_bn<16>(p, t, stream);

@@ -287,6 +287,28 @@ def test_ffma_sources_agree(args):
     assert np.array_equal(outs["frame"], outs["producers"])
 
 
+# Inputs of at most 4 channels large enough for the gather kernel's
+# 4-channel slices (1024-position units): against the oracle, and bit for bit
+# against the frame pipeline's 16-channel slices (the same products summed in
+# the same order).  Plan order (N, Ci, H, W, Co, kH, kW, s, ph, pw).
+NARROW_SHAPES = [(4, 3, 200, 200, 8, 3, 3, 1, 1, 1), (3, 1, 300, 260, 5, 5, 5, 2, 2, 2),
+                 (3, 4, 230, 230, 16, 7, 7, 2, 3, 3), (2, 2, 330, 250, 33, 3, 5, 1, 1, 2)]
+
+
+@pytest.mark.parametrize("args", NARROW_SHAPES)
+def test_ffma_four_channel_slices(args):
+    N, Ci, H, W, Co, kH, kW, s, ph, pw = args
+    assert dg.describe(*args, "fp32")["slice_n"] == 4
+    go, w = make_tensors((N, Co, out_ext(H, kH, s, ph), out_ext(W, kW, s, pw)), (Co, Ci, kH, kW), 93, "kaiming")
+    ref, _ = oracle.dgrad(go, w, H, W, s, ph, pw)
+    narrow, info = run_gpu(args, go, w, "fp32")
+    assert info["slice_n"] == 4 and info["a_source"] == "producers"
+    assert_fp32(narrow, ref)
+    frame, info = run_gpu(args, go, w, "fp32", a_source="frame")
+    assert info["slice_n"] == 16
+    assert np.array_equal(narrow, frame)
+
+
 @pytest.mark.parametrize("a_source", ["frame", "producers"])
 @pytest.mark.parametrize("opts", [dict(slice_n=16), dict(slice_n=32, chunk_k=8), dict(chunk_k=32)])
 def test_simt_tilings_each_source(opts, a_source):

@@ -708,3 +708,18 @@ def test_ffma_source_plans():
             with pytest.raises(dg.DgradError) as e:
                 dg.describe(*wl.plan_args(), "fp32", a_source=bad)
             assert e.value.status == 2
+
+
+def test_ffma_four_channel_slices_plans():
+    # At most 4 input channels: 4-channel slices (1024-position units) in the
+    # gather kernel where those units fill a wave of CTAs; 16 otherwise, and
+    # always in the frame pipeline.
+    stem = WORKLOADS["stem"].plan_args()
+    d = dg.describe(*stem, "fp32")
+    assert d["slice_n"] == 4 and d["tile_step"] == 1024 and d["a_source"] == "producers"
+    assert d["n_work"] == -(-d["positions"] // 1024) * d["n_phases"]
+    assert dg.describe(*stem, "fp32", a_source="frame")["slice_n"] == 16
+    assert dg.describe(*WORKLOADS["tiny"].plan_args(), "fp32")["slice_n"] == 16
+    assert dg.describe(4, 3, 200, 200, 8, 3, 3, 1, 1, 1, "fp32")["slice_n"] == 4
+    assert dg.describe(4, 5, 200, 200, 8, 3, 3, 1, 1, 1, "fp32")["slice_n"] == 16
+    assert dg.describe(*stem, "fp32", slice_n=16)["slice_n"] == 16
