@@ -402,11 +402,14 @@ def time_workload(dg, torch, wl, precision, steps, warmup, rank, barrier, device
             "bytes": info["algorithmic_bytes"], "steps": steps}
 
 
-def roofline(wl, precision, flops, nbytes, main_s, step_s, live):
+def roofline(wl, precision, flops, nbytes, main_s, step_s, live, plan=None):
     """Roofline of the main kernel.  `live` = measure_peaks(): the TF32 and
     FFMA peaks measured in this run on this GPU; HBM bandwidth from
-    MEASURED_PEAKS.json (driver-measured).  The nominal-ratio TF32 figure
-    (measured bf16 burst x 1.1/2.25) is reported beside the measured one."""
+    MEASURED_PEAKS.json (driver-measured).  `achieved` / `peak` / `frac` are
+    in the bound's own unit: GB/s of algorithmic bytes against the HBM peak
+    when the workload is bound by HBM at its roofline, else TFLOP/s of useful
+    FLOP against the compute peak; `compute` always gives the latter (and the
+    nominal-ratio TF32 figure, measured bf16 burst x 1.1/2.25, beside it)."""
     peaks, src = load_peaks()
     hbm = peaks["hbm_gbs"]
     nominal_tf32 = peaks["bf16_tflops"] * TF32_OVER_BF16
@@ -428,15 +431,25 @@ def roofline(wl, precision, flops, nbytes, main_s, step_s, live):
         bound = "alu" if precision == "fp32" else "tensor"
     else:
         bound = "hbm"
-    achieved = flops / main_s / 1e12
+    achieved_tf = flops / main_s / 1e12
+    gbs = nbytes / main_s / 1e9
+    if bound == "hbm":
+        achieved, peak, unit = gbs, hbm, "GB/s"
+    else:
+        achieved, peak, unit = achieved_tf, peak_tf, "TFLOP/s"
     rec = recorded_traffic_entry(wl.name, precision)
+    if precision != "fp32":
+        kernel = "tc_dgrad_kernel"
+    else:
+        kernel = "simt_pipe_kernel" if plan and plan.get("a_source") == "frame" else "simt_dgrad_kernel"
     return {
-        "bound": bound, "achieved": achieved, "peak": peak_tf, "unit": "TFLOP/s", "frac": achieved / peak_tf,
+        "bound": bound, "achieved": achieved, "peak": peak, "unit": unit, "frac": achieved / peak,
         "traffic": rec.get("dram_bytes_per_launch") if rec else None,
         "traffic_l2_write": rec.get("l2_write_bytes_per_launch") if rec else None,
-        "kernel": "simt_dgrad_kernel" if precision == "fp32" else "tc_dgrad_kernel",
+        "kernel": kernel,
+        "compute": {"achieved": achieved_tf, "peak": peak_tf, "unit": "TFLOP/s", "frac": achieved_tf / peak_tf,
+                    "peak_alt": alt, "frac_alt": achieved_tf / alt},
         "peak_source": f"{note}; HBM {hbm} GB/s ({src})",
-        "peak_alt": alt, "frac_alt": achieved / alt,
         "roofline_us": max(t_flop, t_hbm) * 1e6,
         "frac_of_roofline_step": max(t_flop, t_hbm) / step_s,
         "frac_of_roofline_kernel": max(t_flop, t_hbm) / main_s,
@@ -470,7 +483,7 @@ def build_line(args, wl, r, world):
         "config": {**wl_config(wl), "precision": args.precision, "parallelism": f"replicas x{world}",
                    "l2": "flushed (256 MiB write) before every timed step",
                    "step": "pack kernel (weights + grad_out frame) + main kernel (C ABI dgrad_run)"},
-        "roofline": roofline(wl, args.precision, flops, nbytes, main_s, step_s, r["peaks"]),
+        "roofline": roofline(wl, args.precision, flops, nbytes, main_s, step_s, r["peaks"], r["plan"]),
         "main_kernel_us": r["main_ms"] * 1e3, "pack_stages_us": r["prepack_ms"] * 1e3,
         "peaks_measured": {k: r["peaks"][k] for k in ("tf32_tflops", "ffma_tflops", "sm_count")},
         "gpu_launches": 2 * r["steps"],
@@ -619,11 +632,11 @@ def main():
                     x = time_workload(dg, torch, WORKLOADS[name], prec, 10 if prec == "fp32" else 50, 5, rank,
                                       lambda: None, local, clocks=False, e2e=False)
                     rf = roofline(WORKLOADS[name], prec, x["flops"], x["bytes"], x["main_ms"] * 1e-3,
-                                  x["ms_per_step"] * 1e-3, r["peaks"])
+                                  x["ms_per_step"] * 1e-3, r["peaks"], x["plan"])
                     print(json.dumps({"info": "workload", "workload": name, "precision": prec,
                                       **{k: x[k] for k in ("ms_per_step", "main_ms", "prepack_ms")},
                                       "tflops": x["flops"] / (x["ms_per_step"] * 1e-3) / 1e12,
-                                      "main_tflops": rf["achieved"], "frac_peak": rf["frac"],
+                                      "main_tflops": rf["compute"]["achieved"], "frac_peak": rf["compute"]["frac"],
                                       "frac_of_roofline_kernel": rf["frac_of_roofline_kernel"],
                                       "plan": {k: x["plan"][k] for k in ("path", "tile_blocks", "slice_n",
                                                                          "chunk_k", "grid", "n_work",
@@ -637,7 +650,7 @@ def main():
             print(json.dumps({"info": "workload", "workload": "stem", "precision": "tf32", "path": "col2im",
                               **{k: x[k] for k in ("ms_per_step", "main_ms", "prepack_ms")},
                               "tflops": x["flops"] / (x["ms_per_step"] * 1e-3) / 1e12,
-                              "main_tflops": rf["achieved"], "frac_peak": rf["frac"],
+                              "main_tflops": rf["compute"]["achieved"], "frac_peak": rf["compute"]["frac"],
                               "frac_of_roofline_kernel": rf["frac_of_roofline_kernel"]}), flush=True)
             tf32_peak = r["peaks"]["tf32_tflops"]
             for name, prec in [(n, p) for p in ("tf32", "tf32x3") for n in WORKLOAD_ORDER]:
