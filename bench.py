@@ -614,6 +614,19 @@ def main():
 
     if rank == 0:
         line = build_line(args, wl, r, world)
+        if world == 1 and wl.name == "resnet_stage" and args.precision == "tf32" and not args.all:
+            # the other target workloads, TF32, same method (flushed steps, events); informational
+            line["other_configs"] = []
+            for name in ("strided_downsample", "pointwise", "stem"):
+                x = time_workload(dg, torch, WORKLOADS[name], "tf32", 50, 5, rank, lambda: None, local,
+                                  clocks=False, e2e=False)
+                rf = roofline(WORKLOADS[name], "tf32", x["flops"], x["bytes"], x["main_ms"] * 1e-3,
+                              x["ms_per_step"] * 1e-3, r["peaks"], x["plan"])
+                line["other_configs"].append({
+                    "workload": name, "precision": "tf32", "us_per_call": x["ms_per_step"] * 1e3,
+                    "tflops": x["flops"] / (x["ms_per_step"] * 1e-3) / 1e12, "main_kernel_us": x["main_ms"] * 1e3,
+                    "roofline": {k: rf[k] for k in ("bound", "achieved", "peak", "unit", "frac", "roofline_us")},
+                    "compute_frac": rf["compute"]["frac"]})
         if world == 1 and not args.no_cpu_baseline:
             flops, times, cores = cpu_oracle_run(wl, wl.N, reps=2)
             line["cpu_baseline"] = {
