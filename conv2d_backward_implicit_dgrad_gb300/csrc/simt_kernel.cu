@@ -46,6 +46,16 @@ struct Ring {
     }
 };
 
+__device__ __forceinline__ void decode_unit(const MainParams &p, int u, int &tile, int &slice, int &phase) {
+    // the units of one tile (its slices and phases) are consecutive: they
+    // read the same frame band, so later copies of it hit L2
+    const int per_tile = p.n_slices * p.n_phases;
+    tile = u / per_tile;
+    const int rem = u - tile * per_tile;
+    slice = rem / p.n_phases;
+    phase = rem - slice * p.n_phases;
+}
+
 template <int BN, int KC>
 __global__ void __launch_bounds__(kThreads) simt_dgrad_kernel(const __grid_constant__ MainParams p) {
     extern __shared__ __align__(16) float sm[];
@@ -57,8 +67,9 @@ __global__ void __launch_bounds__(kThreads) simt_dgrad_kernel(const __grid_const
     float *As = sm;                                            // [G][a_rows][4]
     float *Bs = sm + static_cast<size_t>(G) * p.a_rows * 4;    // [taps][G][BN][4]
 
-    const int tile = blockIdx.x, slice = blockIdx.y;
-    const PhaseDesc pd = p.phase[blockIdx.z];
+    int tile, slice, phase;
+    decode_unit(p, blockIdx.x, tile, slice, phase);
+    const PhaseDesc pd = p.phase[phase];
     const int P0 = tile * UM;
     const int tid = threadIdx.x;
     const int cg = tid / PG, pg = tid % PG;
@@ -130,7 +141,8 @@ cudaError_t launch_bn_kc(const MainParams &p, const Tiling &t, cudaStream_t stre
     auto kern = simt_dgrad_kernel<BN, KC>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, t.smem_bytes);
     if (e != cudaSuccess) return e;
-    dim3 grid(t.n_tiles, t.n_slices, p.n_phases);
+    if (t.n_work > 0x7fffffffLL) return cudaErrorInvalidValue;
+    dim3 grid(static_cast<unsigned>(t.n_work));   // one CTA per unit; a tile's slices and phases are consecutive
     kern<<<grid, kThreads, t.smem_bytes, stream>>>(p);
     return cudaGetLastError();
 }
@@ -149,15 +161,6 @@ __device__ __forceinline__ void pipe_fail(PipeBars *bars, const MainParams &p) {
     atomicOr(p.err, kErrTimeout);
 }
 
-__device__ __forceinline__ void decode_unit(const MainParams &p, int u, int &tile, int &slice, int &phase) {
-    // the units of one tile (its slices and phases) are consecutive: they
-    // read the same frame band, so later copies of it hit L2
-    const int per_tile = p.n_slices * p.n_phases;
-    tile = u / per_tile;
-    const int rem = u - tile * per_tile;
-    slice = rem / p.n_phases;
-    phase = rem - slice * p.n_phases;
-}
 
 // kWide (BN = 64): 128 compute threads, each an 8 x 8 register tile --
 // positions w*32 + tp + 4i (i < 8) of compute warp w and channels tc + 8j
