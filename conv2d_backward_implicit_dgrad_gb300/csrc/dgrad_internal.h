@@ -148,6 +148,8 @@ struct Tiling {
                        //    written by the epilogue warps into tensor memory, where the MMA reads A; no frame
     int a_tslots;      // a_tmem: tensor-memory A slots (32 columns each)
     int a_tcol;        // a_tmem: first tensor-memory column of the A slots (after the accumulators)
+    int img_align_sms; // a_tmem: tiles aligned to images (one copy per chunk, never a second image) when all
+                       //    units then fit in this many CTAs (the SM count); 0: never
     int simt_wide;     // FFMA frame pipeline: 8 x 8 register tiles, 128 compute threads, two CTAs per SM
     int a_box_rows;    // rows of one A tensor copy (<= 256)
     int a_nbox;        // tensor copies per A stage

@@ -51,7 +51,7 @@ constexpr int kProdWarp0 = 6;
 constexpr int kProdWarps = 8;
 constexpr int kThreads = (kProdWarp0 + kProdWarps) * 32;
 constexpr int kThreadsTmaA = kProdWarp0 * 32;
-constexpr int kMaxAStages = 4;
+constexpr int kMaxAStages = 8;
 constexpr int kMaxBStages = 32;
 constexpr int kRowSlots = kProdWarps * 32 / 4;   // 4-byte producer: threads per channel lane
 constexpr int kMaxRowsPerThread = 16;            // a_rows <= kRowSlots * kMaxRowsPerThread
@@ -268,10 +268,11 @@ __device__ __forceinline__ bool write_tmem_a(const MainParams &p, Barriers *bars
                                              Ring &rs, Ring &rt, long long tmo) {
     const int t = ew * 32 + lane;
     const int plane = p.oH * p.oW;
-    const int P0 = tile * kBlockM;
+    int lim;
+    const int P0 = tile_origin(p, tile, lim);   // image-aligned tiles: every valid row is in box 0
     const int n0 = P0 / plane, x0 = P0 - n0 * plane;
     const int P = P0 + t;
-    const bool valid = P < p.positions;
+    const bool valid = P < lim;
     int off = 0;
     if (valid) {
         const int n = P / plane, j = P - n * plane;
@@ -1046,7 +1047,7 @@ __global__ void __launch_bounds__(kernel_threads<kTmaA, kEG, kStg>(), 1)
                     const int tplane = p.oH * p.oW;
                     const int tn0 = kTA ? P0 / tplane : 0;
                     const int tx0 = kTA ? P0 - tn0 * tplane : 0;
-                    const bool tcross = kTA && tx0 + kBlockM > tplane && tn0 + 1 < p.N;
+                    const bool tcross = kTA && !p.img_tiles && tx0 + kBlockM > tplane && tn0 + 1 < p.N;
                     for (int c = 0; ok && c < p.n_chunks; ++c) {
                         if (kTmaA) {
                             // A stage: frame rows [P0, P0 + a_rows) x channels [32c, 32c + 32)
