@@ -365,7 +365,9 @@ cudaError_t launch_pipe_kc(const MainParams &p, const Tiling &t, cudaStream_t st
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    // 8 x 8 tiles on few taps: no dependent launch (two of these CTAs fit
+    // beside the pack's blocks on an SM and, resident early, slow the pack)
+    cfg.numAttrs = kWide && t.tap_group <= 4 ? 0 : 1;
     return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
