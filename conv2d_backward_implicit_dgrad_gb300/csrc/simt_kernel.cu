@@ -169,7 +169,66 @@ __device__ __forceinline__ void pipe_fail(PipeBars *bars, const MainParams &p) {
 // 12 loads per 128 FFMAs ask 0.375 passes per FFMA instruction of a port that
 // serves 0.25 (four FFMA pipes, one pass per clock); the 8 x 8 tiles' 16 loads
 // per 256 FFMAs ask 0.25.
-template <int BN, int KC, bool kWide>
+// Unit schedules of the frame pipeline.  Round-robin (kSnake = false): CTA b
+// of G takes units b, b + G, ..., the units of a tile consecutive.  For plans
+// whose phases differ in tap count (kSnake = true): CTA b takes the units at
+// positions b, 2G-1-b, 2G+b, 4G-1-b, ... of the units sorted by their phase's
+// tap count, most first (a tile's slices consecutive within a phase), so that
+// every CTA gets a similar share of taps -- round-robin with the phase fastest
+// gave each CTA one phase (with 4 phases and 152 CTAs the 4-tap phase's CTAs
+// did four times the 1-tap phase's work).  The plain form is its own instance:
+// the schedule code in the same kernel slowed the one-phase plans by 1-5 %.
+__device__ __forceinline__ int phase_rank(const MainParams &p, int ph) {
+    const int t = p.phase[ph].tap_count;
+    int rank = 0;
+    for (int q = 0; q < p.n_phases; ++q) {
+        const int tq = p.phase[q].tap_count;
+        rank += (tq > t || (tq == t && q < ph)) ? 1 : 0;
+    }
+    return rank;
+}
+
+// Unit at schedule position k of the sorted schedule.
+__device__ __forceinline__ void sorted_unit(const MainParams &p, long long k, int &tile, int &slice, int &phase) {
+    const int per_phase = p.n_tiles * p.n_slices;
+    const int r = static_cast<int>(k / per_phase), rem = static_cast<int>(k - static_cast<long long>(r) * per_phase);
+    phase = 0;
+    for (int ph = 0; ph < p.n_phases; ++ph)
+        if (phase_rank(p, ph) == r) phase = ph;
+    tile = rem / p.n_slices;
+    slice = rem - tile * p.n_slices;
+}
+
+template <bool kSnake>
+struct UnitIter;
+template <>
+struct UnitIter<false> {
+    int u = static_cast<int>(blockIdx.x);
+    // The next unit of this CTA; false past its last one.
+    __device__ __forceinline__ bool next(const MainParams &p, int &tile, int &slice, int &phase) {
+        if (u >= p.n_work) return false;
+        decode_unit(p, u, tile, slice, phase);
+        u += static_cast<int>(gridDim.x);
+        return true;
+    }
+};
+template <>
+struct UnitIter<true> {
+    long long j = 0;   // round
+    __device__ __forceinline__ bool next(const MainParams &p, int &tile, int &slice, int &phase) {
+        const long long G = gridDim.x, b = blockIdx.x;
+        while (j * G < p.n_work) {
+            const long long k = (j & 1) ? (j + 1) * G - 1 - b : j * G + b;
+            ++j;
+            if (k >= p.n_work) continue;   // a partial last round
+            sorted_unit(p, k, tile, slice, phase);
+            return true;
+        }
+        return false;
+    }
+};
+
+template <int BN, int KC, bool kWide, bool kSnake = false>
 __global__ void __launch_bounds__(simt_pipe_threads(kWide), kWide ? 2 : 1)
     simt_pipe_kernel(const __grid_constant__ MainParams p) {
     extern __shared__ __align__(1024) uint8_t smem[];
@@ -207,9 +266,9 @@ __global__ void __launch_bounds__(simt_pipe_threads(kWide), kWide ? 2 : 1)
             for (int i = 0; i < kSimtMaxStages; ++i) last_parity[i] = -1;
             Ring ring;
             bool ok = true;
-            for (int u = blockIdx.x; ok && u < p.n_work && !bars->abort_flag; u += gridDim.x) {
-                int tile, slice, phase;
-                decode_unit(p, u, tile, slice, phase);
+            int tile, slice, phase;
+            UnitIter<kSnake> it;
+            while (ok && !bars->abort_flag && it.next(p, tile, slice, phase)) {
                 const PhaseDesc &pd = p.phase[phase];
                 if (pd.tap_count == 0) continue;
                 const int P0 = tile * kBlockM;
@@ -259,9 +318,9 @@ __global__ void __launch_bounds__(simt_pipe_threads(kWide), kWide ? 2 : 1)
         ok = false;
     }
     const size_t plane = static_cast<size_t>(p.H) * p.W;
-    for (int u = blockIdx.x; ok && u < p.n_work && !bars->abort_flag; u += gridDim.x) {
-        int tile, slice, phase;
-        decode_unit(p, u, tile, slice, phase);
+    UnitIter<kSnake> it;
+    int tile, slice, phase;
+    while (ok && !bars->abort_flag && it.next(p, tile, slice, phase)) {
         const PhaseDesc &pd = p.phase[phase];
         const int P0 = tile * kBlockM;
         constexpr int CPT = kWide ? 8 : 4;   // channels per thread
@@ -351,9 +410,9 @@ __global__ void __launch_bounds__(simt_pipe_threads(kWide), kWide ? 2 : 1)
     }
 }
 
-template <int BN, int KC, bool kWide>
+template <int BN, int KC, bool kWide, bool kSnake = false>
 cudaError_t launch_pipe_kc(const MainParams &p, const Tiling &t, cudaStream_t stream) {
-    auto kern = simt_pipe_kernel<BN, KC, kWide>;
+    auto kern = simt_pipe_kernel<BN, KC, kWide, kSnake>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, t.smem_bytes);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg{};
@@ -373,14 +432,27 @@ cudaError_t launch_pipe_kc(const MainParams &p, const Tiling &t, cudaStream_t st
 
 template <int BN>
 cudaError_t launch_pipe_bn(const MainParams &p, const Tiling &t, cudaStream_t stream) {
+    bool differ = false;   // phases of different tap counts: the sorted schedule
+    for (int q = 1; q < p.n_phases; ++q) differ = differ || p.phase[q].tap_count != p.phase[0].tap_count;
     if constexpr (BN == 64) {
         if (t.simt_wide) {
-            switch (t.kc) {
+            switch (t.kc + (differ ? 1 : 0)) {
                 case 8: return launch_pipe_kc<BN, 8, true>(p, t, stream);
                 case 16: return launch_pipe_kc<BN, 16, true>(p, t, stream);
                 case 32: return launch_pipe_kc<BN, 32, true>(p, t, stream);
+                case 9: return launch_pipe_kc<BN, 8, true, true>(p, t, stream);
+                case 17: return launch_pipe_kc<BN, 16, true, true>(p, t, stream);
+                case 33: return launch_pipe_kc<BN, 32, true, true>(p, t, stream);
                 default: return cudaErrorInvalidValue;
             }
+        }
+    }
+    if (differ) {
+        switch (t.kc) {
+            case 8: return launch_pipe_kc<BN, 8, false, true>(p, t, stream);
+            case 16: return launch_pipe_kc<BN, 16, false, true>(p, t, stream);
+            case 32: return launch_pipe_kc<BN, 32, false, true>(p, t, stream);
+            default: return cudaErrorInvalidValue;
         }
     }
     switch (t.kc) {

@@ -270,7 +270,11 @@ def test_simt_tilings(opts):
 FFMA_SHAPES = [WORKLOADS[n].plan_args() for n in ("tiny", "strided_downsample", "pointwise")] + [
     (2, 64, 20, 20, 64, 3, 3, 1, 1, 1), (3, 33, 12, 12, 70, 3, 3, 1, 1, 1), (2, 40, 36, 19, 23, 3, 3, 2, 1, 1),
     (1, 3, 80, 80, 8, 7, 7, 2, 3, 3), (3, 5, 17, 19, 33, 1, 1, 2, 0, 0), (2, 17, 9, 11, 5, 5, 3, 3, 2, 1),
-    (1, 20, 40, 40, 40, 3, 3, 4, 1, 1)]
+    (1, 20, 40, 40, 40, 3, 3, 4, 1, 1),
+    # phases of different tap counts over several rounds of persistent CTAs with
+    # a partial last one (the sorted schedule): 276 units on 152 CTAs, and with
+    # 8 x 8 tiles 352 units on 304 CTAs
+    (8, 40, 64, 64, 24, 3, 3, 2, 1, 1), (16, 64, 48, 48, 16, 5, 5, 2, 2, 2)]
 
 
 @pytest.mark.parametrize("args", FFMA_SHAPES)
