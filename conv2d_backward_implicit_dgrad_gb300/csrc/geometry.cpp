@@ -445,15 +445,13 @@ bool size_simt(const Geometry &g, Tiling &t, int sm_count) {
         if (t.n_work > INT_MAX) return false;
         // 64-channel slices: 8 x 8 register tiles, two CTAs per SM, when two
         // stages each fit in half of the SM's shared memory (228 KB, 1 KB per
-        // CTA reserved), for phases with more than 4 taps (the FFMA loop, not
-        // the fill, sets the pace) and for one-phase plans.  Measured (frame):
-        // resnet_stage main kernel 182 us vs 194 with 8 x 4 tiles, pointwise
-        // step 219 us vs 244 (launched without the dependent launch: its
-        // half-size CTAs, resident early, slowed the pack: 259 us); several
-        // phases with few taps lose on balance (strided_downsample: 456 units
-        // on 304 CTAs, 203 us vs 170).
+        // CTA reserved).  Measured steps (frame): resnet_stage 195 us vs 204
+        // with 8 x 4 tiles, pointwise 219 vs 244 (few taps: launched without
+        // the dependent launch -- its half-size CTAs, resident early, slowed
+        // the pack: 259 us), strided_downsample 118 vs 131 (with the
+        // tap-balanced schedule; round-robin, 203 us vs 170).
         const int half = (kSmemPerSm / 2 - 1024 - kSimtPipeHeader) / stage;
-        t.simt_wide = t.bn == 64 && half >= 2 && (t.tap_group > 4 || g.n_phases == 1) ? 1 : 0;
+        t.simt_wide = t.bn == 64 && half >= 2 ? 1 : 0;
         const int stages = std::min(kSimtMaxStages, t.simt_wide ? half : (kMaxSmem - kSimtPipeHeader) / stage);
         if (stages < 2) return false;
         t.a_stages = t.b_stages = stages;

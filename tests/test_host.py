@@ -697,7 +697,7 @@ def test_ffma_source_plans():
         assert f["a_source"] == "frame"
         # one persistent CTA per SM, or two (8 x 8 tiles for 64-channel slices,
         # each CTA then within half of the SM's 228 KB less its reserved 1 KB)
-        two = f["slice_n"] == 64 and name in ("resnet_stage", "pointwise")
+        two = f["slice_n"] == 64
         assert f["grid"] == min(f["n_work"], 152 * (2 if two else 1)) and 2 <= f["a_stages"] <= 6
         assert f["smem_bytes"] <= 232448
         # the band: 128 rows plus the largest tap shift, in copies of at most 256 rows
