@@ -13,7 +13,8 @@
 #include "dgrad.h"
 #include "dgrad_internal.h"
 
-constexpr int kHostChunks = 8;   // batch chunks of dgrad_run_host's copy/compute pipeline
+constexpr int kHostChunks = 4;   // batch chunks of dgrad_run_host's copy/compute pipeline (4: 252 us e2e on
+                                 // resnet_stage; 6: 255, 8: 260, 12: 266 -- per-chunk costs against fill and drain)
 
 struct dgrad_plan_s {
     int device;

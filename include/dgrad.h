@@ -267,7 +267,7 @@ dgrad_status_t dgrad_run_main(dgrad_plan_t plan, const float *grad_out, float *g
 /* The same computation from HOST buffers: copies grad_out and weight to
  * device staging buffers owned by the plan (allocated on the first call),
  * runs dgrad_run, copies grad_input back and synchronises `stream` (and the
- * plan's own copy streams).  With N >= 2 the batch goes through in up to 8
+ * plan's own copy streams).  With N >= 2 the batch goes through in up to 4
  * chunks, each run by a sub-plan (made on the first call) on `stream` while
  * the next chunk is copied in and the previous one copied out on two
  * non-blocking streams the plan owns; the result is bit-for-bit that of

@@ -524,8 +524,8 @@ def test_run_host_matches_device():
 
 
 @pytest.mark.parametrize("shape,precision,pinned", [
-    ((32, 64, 56, 56, 64, 3, 3, 1, 1, 1), "tf32", True),    # eight chunks of four images
-    ((11, 5, 17, 19, 33, 3, 3, 2, 1, 1), "tf32", True),     # chunks of two and a remainder of one
+    ((32, 64, 56, 56, 64, 3, 3, 1, 1, 1), "tf32", True),    # four chunks of eight images
+    ((11, 5, 17, 19, 33, 3, 3, 2, 1, 1), "tf32", True),     # chunks of three and a remainder of two
     ((11, 5, 17, 19, 33, 3, 3, 2, 1, 1), "fp32", False),    # FFMA path, pageable host memory
     ((3, 3, 40, 38, 64, 7, 7, 2, 3, 3), "tf32x3", True),
 ])
