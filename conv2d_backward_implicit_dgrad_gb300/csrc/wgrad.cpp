@@ -16,6 +16,8 @@ struct wgrad_plan_s {
     dgrad::WgradGeometry g;
     dgrad::WgradMainParams mp;
     dgrad::WgradRunParams wp;   // run mode
+    dgrad::WgradPlaneParams np;   // plane mode
+    const void *map_x, *map_g;    // the tensors the per-call tensor maps were last encoded on (plane, direct)
     dgrad::WgradPackParams pp;
     dgrad::WgradReduceParams rp;
     uint32_t *err;
@@ -164,8 +166,53 @@ static bool plan_run(WgradGeometry &g, int sm_count) {
     return true;
 }
 
+// Plane mode (see WgradPlaneParams): stride 1, oH = H and oW = W, rows of a
+// multiple of 4 positions (whole-row shifts of grad_out are then 16-byte
+// tensor-copy coordinates), more than one tap (a 1x1 kernel takes the
+// direct mode), TF32 (the MMA reads the caller's values, so there is no
+// hi/lo split).  A's kW * ci_rows rows fill n_mt tiles of 128, B's kH *
+// co_rows rows one MMA N; all n_mt * nb accumulator columns must fit tensor
+// memory.  One CTA per SM, each over a contiguous range of chunks.
+static void plan_plane(WgradGeometry &g, int sm_count) {
+    if (g.split || g.s != 1 || g.oH != g.H || g.oW != g.W || g.kH * g.kW < 2 || g.W % 4 != 0) return;
+    if (g.kW > 7) return;   // column shifts |kw - pw| <= 3: within one 16-byte piece
+    const long long hw = (long long)g.H * g.W;
+    const int ci_rows = round_up(g.Ci, 8), co_rows = round_up(g.Co, 8);
+    const int nb = round_up(g.kH * co_rows, 16);
+    const int n_mt = ceil_div(g.kW * ci_rows, 128);
+    if (ci_rows > 256 || co_rows > 256 || nb > 256 || n_mt * nb > 512) return;
+    if ((g.kW - 1) * ci_rows > 4 * 128) return;   // shifted rows: at most four per shifting thread
+    const long long cpi = (hw + 31) / 32, chunks = cpi * g.N;
+    if (hw > INT_MAX / 2 || chunks > INT_MAX / 2) return;
+    const int stage_bytes = n_mt * 128 * 128 + nb * 128;
+    const int stages = std::min(kWgMaxStages, (kMaxSmem - kWgBarrierBytes) / stage_bytes);
+    if (stages < 2) return;
+    g.plane = 1;
+    g.run_mode = 0;
+    g.f = 1;   // K = image, position: no images interleaved
+    g.lf = 0;
+    g.Q = g.N;
+    g.ci_rows = ci_rows;
+    g.co_rows = co_rows;
+    g.seg_rows = ci_rows;
+    g.bn = nb;
+    g.n_mt = n_mt;
+    g.n_nt = 1;
+    g.cpi = (int)cpi;
+    g.total_chunks = (int)chunks;
+    g.grid = (int)std::min<long long>(sm_count, chunks);
+    g.n_ks = g.grid;
+    g.n_units = g.grid;
+    g.cps = ceil_div(g.total_chunks, g.grid);
+    g.stages = stages;
+    g.smem_bytes = kWgBarrierBytes + stages * stage_bytes;
+    g.tmem_cols = pow2_at_least(n_mt * nb);
+    g.g_elems = g.x_elems = 0;
+    g.part_elems = (size_t)g.grid * g.kW * ci_rows * nb;
+}
+
 dgrad_status_t make_wgrad_geometry(int N, int Ci, int H, int W, int Co, int kH, int kW, int stride, int pad_h,
-                                   int pad_w, int precision, int sm_count, WgradGeometry *out) {
+                                   int pad_w, int precision, int sm_count, WgradGeometry *out, bool allow_plane) {
     if (N < 1 || Ci < 1 || H < 1 || W < 1 || Co < 1 || kH < 1 || kW < 1 || stride < 1 || pad_h < 0 || pad_w < 0)
         return DGRAD_ERR_INVALID_ARG;
     if (precision != DGRAD_PREC_FP32 && precision != DGRAD_PREC_TF32 && precision != DGRAD_PREC_TF32X3)
@@ -320,6 +367,7 @@ dgrad_status_t make_wgrad_geometry(int N, int Ci, int H, int W, int Co, int kH, 
     if ((g.g_elems + g.x_elems) / 4 > (size_t)INT_MAX) return DGRAD_ERR_UNSUPPORTED;   // 32-bit pack indices
     g.part_elems = (size_t)g.n_units * g.bn * 128;
     plan_run(g, sm_count);
+    if (allow_plane) plan_plane(g, sm_count);
     *out = g;
     return DGRAD_OK;
 }
@@ -337,7 +385,7 @@ void fill_wgrad_info(const WgradGeometry &g, size_t ws, wgrad_plan_info_t *info)
     info->oH = g.oH; info->oW = g.oW;
     info->precision = g.split ? DGRAD_PREC_TF32X3 : DGRAD_PREC_TF32;
     info->interleave = g.f;
-    info->mode = g.run_mode ? 1 : (g.direct ? 2 : 0);
+    info->mode = g.plane ? 3 : (g.run_mode ? 1 : (g.direct ? 2 : 0));
     info->Wf = g.Wf; info->Kimg = g.Kimg; info->Lx = g.Lx; info->n_copies = g.n_copies;
     info->seg_rows = g.seg_rows; info->n_mt = g.n_mt; info->n_nt = g.n_nt; info->n_ks = g.n_ks;
     info->slice_n = g.bn; info->n_units = g.n_units; info->grid = g.grid; info->stages = g.stages;
@@ -397,6 +445,29 @@ dgrad_status_t encode_maps(wgrad_plan_s *pl, const float *xsrc, const float *gsr
     return DGRAD_OK;
 }
 
+// Plane mode: the caller's input and grad_out as {H*W, channels, N} with
+// boxes of 32 positions x all channels (rows past the channel count read as
+// zeros).
+dgrad_status_t encode_plane_maps(wgrad_plan_s *pl, const float *x, const float *go) {
+    auto fn = dgrad::tensor_map_encoder();
+    if (!fn) return DGRAD_ERR_CUDA;
+    const WgradGeometry &g = pl->g;
+    const cuuint32_t es[3] = {1u, 1u, 1u};
+    const cuuint64_t hw = (cuuint64_t)g.H * g.W;
+    const cuuint64_t xd[3] = {hw, (cuuint64_t)g.Ci, (cuuint64_t)g.N}, xs[2] = {hw * 4, hw * 4 * g.Ci};
+    const cuuint64_t gd[3] = {hw, (cuuint64_t)g.Co, (cuuint64_t)g.N}, gs[2] = {hw * 4, hw * 4 * g.Co};
+    const cuuint32_t xb[3] = {32u, (cuuint32_t)g.ci_rows, 1u}, gb[3] = {32u, (cuuint32_t)g.co_rows, 1u};
+    if (fn(&pl->np.x_map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float *>(x), xd, xs, xb, es,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return DGRAD_ERR_CUDA;
+    if (fn(&pl->np.g_map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float *>(go), gd, gs, gb, es,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return DGRAD_ERR_CUDA;
+    return DGRAD_OK;
+}
+
 void fill_wgrad_params(wgrad_plan_s *pl) {
     const WgradGeometry &g = pl->g;
     dgrad::WgradMainParams &m = pl->mp;
@@ -432,6 +503,21 @@ void fill_wgrad_params(wgrad_plan_s *pl) {
     r.seg_rows = g.seg_rows; r.cpt = g.cpt; r.spt = g.spt; r.n_segs = g.n_segs;
     r.total = (long long)g.n_mt * g.n_nt * g.bn * 128;
     r.run_mode = g.run_mode;
+    if (g.plane) {
+        r.plane = 1;
+        r.ci_rows = g.ci_rows; r.co_rows = g.co_rows; r.kH = g.kH; r.kW = g.kW; r.a_rows = g.kW * g.ci_rows;
+        r.total = (long long)r.a_rows * g.bn;
+        dgrad::WgradPlaneParams &n = pl->np;
+        n.part = pl->part;
+        n.err = pl->err;
+        n.N = g.N; n.Ci = g.Ci; n.HW = g.H * g.W; n.W = g.W; n.kH = g.kH; n.kW = g.kW; n.ph = g.ph; n.pw = g.pw;
+        n.ci_rows = g.ci_rows; n.co_rows = g.co_rows; n.nb = g.bn; n.n_mt = g.n_mt; n.cpi = g.cpi;
+        n.total_chunks = g.total_chunks; n.stages = g.stages; n.tmem_cols = g.tmem_cols;
+        n.a_bytes = (uint32_t)g.n_mt * 128u * 128u;
+        n.stage_bytes = n.a_bytes + (uint32_t)g.bn * 128u;
+        n.idesc = dgrad::tf32_idesc(128, g.bn);
+        n.timeout_ns = dgrad::kWgTimeoutNs;
+    }
     r.red_warps = 1;
     while (r.red_warps < 8 && r.red_warps * 8 < g.n_ks) r.red_warps *= 2;
     if (g.run_mode) {
@@ -480,7 +566,7 @@ dgrad_status_t wgrad_describe_taps(int N, int Ci, int H, int W, int Co, int kH, 
         return DGRAD_ERR_INVALID_ARG;
     WgradGeometry g;
     dgrad_status_t st =
-        dgrad::make_wgrad_geometry(N, Ci, H, W, Co, kH, kW, stride, pad_h, pad_w, DGRAD_PREC_TF32, 0, &g);
+        dgrad::make_wgrad_geometry(N, Ci, H, W, Co, kH, kW, stride, pad_h, pad_w, DGRAD_PREC_TF32, 0, &g, false);
     if (st != DGRAD_OK) return st;
     if (g.taps > cap || g.n_copies > cap) return DGRAD_ERR_INVALID_ARG;
     for (int t = 0; t < g.taps; ++t) {
@@ -503,8 +589,8 @@ dgrad_status_t wgrad_describe_run(int N, int Ci, int H, int W, int Co, int kH, i
                                      int pad_w, int sm_count, int cap, int *hdr, int *groups, int *taps, int *tiles) {
     if (!hdr || !groups || !taps || !tiles) return DGRAD_ERR_INVALID_ARG;
     WgradGeometry g;
-    dgrad_status_t st =
-        dgrad::make_wgrad_geometry(N, Ci, H, W, Co, kH, kW, stride, pad_h, pad_w, DGRAD_PREC_TF32, sm_count, &g);
+    dgrad_status_t st = dgrad::make_wgrad_geometry(N, Ci, H, W, Co, kH, kW, stride, pad_h, pad_w, DGRAD_PREC_TF32,
+                                                   sm_count, &g, false);
     if (st != DGRAD_OK) return st;
     if (!g.run_mode) return DGRAD_ERR_UNSUPPORTED;
     if (g.taps > cap || g.n_groups > cap || g.n_tiles > cap) return DGRAD_ERR_INVALID_ARG;
@@ -564,8 +650,8 @@ dgrad_status_t wgrad_plan(int N, int Ci, int H, int W, int Co, int kH, int kW, i
                                          dgrad::align256(pl->g.x_elems * 4));
     pl->workspace_bytes = ws;
     fill_wgrad_params(pl);
-    // Direct mode encodes its maps per run, on the caller's tensors.
-    if (!pl->g.direct && (st = encode_maps(pl, pl->xc, pl->gf)) != DGRAD_OK) {
+    // Direct and plane modes encode their maps at run time, on the caller's tensors.
+    if (!pl->g.direct && !pl->g.plane && (st = encode_maps(pl, pl->xc, pl->gf)) != DGRAD_OK) {
         cudaFree(mem);
         delete pl;
         return st;
@@ -598,14 +684,27 @@ dgrad_status_t wgrad_run(wgrad_plan_t plan, const float *grad_out, const float *
     plan->pp.x = input;
     plan->rp.dw = grad_weight;
     dgrad_status_t st = DGRAD_OK;
-    if (g.direct) {   // no frames: the tensor copies read the caller's tensors
-        if ((st = encode_maps(plan, input, grad_out)) != DGRAD_OK) return st;
-    } else if ((st = wcuda(dgrad::launch_wgrad_pack(plan->pp, s))) != DGRAD_OK) {
-        return st;
+    // Direct and plane modes: no frames, the tensor copies read the caller's
+    // tensors (maps re-encoded only when the pointers change).
+    const bool remap = plan->map_x != input || plan->map_g != grad_out;
+    if (g.plane) {
+        if (remap && (st = encode_plane_maps(plan, input, grad_out)) != DGRAD_OK) return st;
+        plan->np.x = input;
+        st = wcuda(dgrad::launch_wgrad_plane(plan->np, g.grid, g.smem_bytes, s));
+    } else {
+        if (g.direct) {
+            if (remap && (st = encode_maps(plan, input, grad_out)) != DGRAD_OK) return st;
+        } else if ((st = wcuda(dgrad::launch_wgrad_pack(plan->pp, s))) != DGRAD_OK) {
+            return st;
+        }
+        st = wcuda(g.run_mode ? dgrad::launch_wgrad_run(plan->wp, g.grid, g.smem_bytes, s)
+                         : dgrad::launch_wgrad_main(plan->mp, g.grid, g.smem_bytes, s));
     }
-    st = wcuda(g.run_mode ? dgrad::launch_wgrad_run(plan->wp, g.grid, g.smem_bytes, s)
-                     : dgrad::launch_wgrad_main(plan->mp, g.grid, g.smem_bytes, s));
     if (st != DGRAD_OK) return st;
+    if (g.plane || g.direct) {
+        plan->map_x = input;
+        plan->map_g = grad_out;
+    }
     return wcuda(dgrad::launch_wgrad_reduce(plan->rp, s));
 }
 

@@ -64,11 +64,16 @@ struct WgradGeometry {
     int grp_tap0[kWgMaxGroups];
     int grp_taps[kMaxTaps];
     int tile_grp[kWgMaxTiles], tile_m0[kWgMaxTiles];
+    // Plane mode (see WgradPlaneParams): rows of one kernel column's input
+    // channels and of one kernel row's output channels, each a multiple of 8.
+    int plane, ci_rows, co_rows;
     size_t g_elems, x_elems, part_elems;   // frames: both halves when split
 };
 
+// allow_plane = false plans as if plane mode did not exist (the frame
+// modes' tables, for the host-only descriptions).
 dgrad_status_t make_wgrad_geometry(int N, int Ci, int H, int W, int Co, int kH, int kW, int stride, int pad_h,
-                                   int pad_w, int precision, int sm_count, WgradGeometry *g);
+                                   int pad_w, int precision, int sm_count, WgradGeometry *g, bool allow_plane = true);
 
 struct WgradPackParams {
     const float *go, *x;
@@ -105,6 +110,8 @@ struct WgradReduceParams {
     int2 tile[kWgMaxTiles];
     int2 grp[kWgMaxGroups];   // x: first entry in taps, y: taps in the group
     int taps_of[kMaxTaps];
+    // plane mode: a split is [row tile][column][rows of the tile] (rows (kw, ci), columns (kh, co))
+    int plane, ci_rows, co_rows, kH, kW, a_rows;
 };
 
 // Run-mode main kernel.  Chunk = one frame position of 32 images.  Tile t
@@ -127,6 +134,36 @@ struct WgradRunParams {
     int2 tile[kWgMaxTiles];   // x: input copy, y: position offset of the tile's first tap (base + m0)
 };
 
+// Plane mode (stride 1, oH = H, oW = W, W a multiple of 4, TF32): no
+// frames.  K runs over the positions q = ih*W + ow of each image's input
+// plane, so that the kernel row kh moves grad_out by whole rows and the
+// kernel column kw moves the input by kw - pw columns:
+//   A[(kw, ci)][q] = input[n][ci][q + kw - pw]   (0 where the column leaves
+//                    the row, and for q >= H*W)
+//   B[(kh, co)][q] = grad_out[n][co][q - (kh - ph)*W]   (0 off the plane)
+//   grad_weight[co][ci][kh][kw] = sum over n, q of A[(kw, ci)][q] * B[(kh, co)][q].
+// Per 32-position chunk: each kernel row of B is one tensor copy of grad_out
+// at a shifted position (a multiple of 4 positions, so 16-byte aligned); A's
+// unshifted column (kw = pw) is one tensor copy of the input; the other
+// columns are gathered by SIMT threads (4-byte asynchronous copies, zero
+// fill) into the same 128-byte-swizzled rows.  A's rows (kw, ci) fill n_mt
+// tiles of 128, B's rows (kh, co) one MMA N (nb <= 256); every CTA keeps
+// all n_mt x nb accumulators in tensor memory over a contiguous range of
+// chunks (images in order) and writes one partial split.
+struct WgradPlaneParams {
+    CUtensorMap x_map;   // input as {H*W, Ci, N}, box {32, ci_rows, 1}, 128-byte swizzle
+    CUtensorMap g_map;   // grad_out as {H*W, Co, N}, box {32, co_rows, 1}, 128-byte swizzle
+    const float *x;      // the input (the gathered columns read it directly)
+    float *part;         // split b: [row tile][nb columns][rows of the tile], rows (kw, ci), columns (kh, co)
+    uint32_t *err;
+    int N, Ci, HW, W, kH, kW, ph, pw;
+    int ci_rows, co_rows, nb, n_mt, cpi, total_chunks, stages, tmem_cols;
+    uint32_t a_bytes, stage_bytes;   // A region (n_mt x 16 KB), A + B
+    uint32_t idesc;
+    long long timeout_ns;
+};
+
+cudaError_t launch_wgrad_plane(const WgradPlaneParams &p, int grid, int smem_bytes, cudaStream_t stream);
 cudaError_t launch_wgrad_pack(const WgradPackParams &p, cudaStream_t stream);
 cudaError_t launch_wgrad_main(const WgradMainParams &p, int grid, int smem_bytes, cudaStream_t stream);
 cudaError_t launch_wgrad_run(const WgradRunParams &p, int grid, int smem_bytes, cudaStream_t stream);

@@ -749,6 +749,18 @@ __global__ void __launch_bounds__(256) wgrad_pack_blocked_kernel(const __grid_co
 // first warp adds the W sums in a fixed order and writes each element's OIHW
 // position.  Deterministic for a given plan.
 __device__ __forceinline__ void wgrad_reduce_store(const WgradReduceParams &p, long long i, float sum) {
+    if (p.plane) {   // split = [row tile][column][rows of the tile]; rows (kw, ci), columns (kh, co)
+        const long long tile = 128LL * p.bn;
+        const int mt = static_cast<int>(i / tile);
+        const long long w = i - mt * tile;
+        const int rows = min(128, p.a_rows - mt * 128);
+        const int col = static_cast<int>(w / rows), r = mt * 128 + static_cast<int>(w - static_cast<long long>(col) * rows);
+        const int kw = r / p.ci_rows, ci = r - kw * p.ci_rows;
+        const int kh = col / p.co_rows, co = col - kh * p.co_rows;
+        if (ci >= p.Ci || co >= p.Co || kh >= p.kH) return;
+        p.dw[(static_cast<size_t>(co) * p.Ci + ci) * p.taps + kh * p.kW + kw] = sum;
+        return;
+    }
     const int row = static_cast<int>(i & 127);
     long long rest = i >> 7;
     const int col = static_cast<int>(rest % p.bn);

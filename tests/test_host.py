@@ -470,6 +470,8 @@ def emulate_wgrad(go, x, kH, kW, s, ph, pw):
     N, Co, oH, oW = go.shape
     _, Ci, H, W = x.shape
     info = dg.wgrad_describe(N, Ci, H, W, Co, kH, kW, s, ph, pw)
+    if info["mode"] == 3:   # TF32 runs the plane mode here; split precision keeps the frames
+        info = dg.wgrad_describe(N, Ci, H, W, Co, kH, kW, s, ph, pw, "tf32x3")
     tab = dg.wgrad_describe_taps(N, Ci, H, W, Co, kH, kW, s, ph, pw)
     f, Wf, Kimg, Lx, Ty, Tu = tab["interleave"], info["Wf"], info["Kimg"], info["Lx"], tab["Ty"], tab["Tu"]
     assert f == info["interleave"] and f in (1, 2, 4, 32) and (info["mode"] == 2 or Wf % max(1, 4 // f) == 0)
@@ -534,9 +536,111 @@ def test_emulated_wgrad_matches_oracle(shape):
     assert np.abs(emu - ref).max() <= 1e-12 * max(1.0, mag.max())
 
 
+PLANE_SHAPES = [
+    # N, Ci, Co, H, W, kH, kW, s, ph, pw: stride 1, oH = H, oW = W, W a multiple of 4
+    (2, 5, 7, 6, 8, 3, 3, 1, 1, 1),        # channel rows padded to 8, B columns padded to 32
+    (3, 40, 24, 6, 12, 3, 3, 1, 1, 1),     # one row tile of 120 rows
+    (2, 64, 64, 8, 8, 3, 3, 1, 1, 1),      # two row tiles, the second half used
+    (2, 3, 4, 5, 4, 5, 5, 1, 2, 2),        # 5 x 5 taps, 20 positions: one ragged chunk per image
+    (1, 16, 16, 7, 12, 3, 5, 1, 1, 2),     # 3 x 5 taps
+    (2, 130, 40, 6, 8, 3, 3, 1, 1, 1),     # four row tiles x 128 columns: all of tensor memory
+    (1, 8, 8, 3, 4, 3, 3, 1, 1, 1),        # one chunk in all
+    (9, 8, 8, 8, 8, 3, 3, 1, 1, 1),        # K splits crossing images
+]
+
+
+def emulate_wgrad_plane(go, x, kH, kW, ph, pw, sm_count):
+    """Plane mode in numpy, driven by the library's plan: per image, A rows
+    (kw, ci) = the input shifted by kw - pw columns within each row, B rows
+    (kh, co) = grad_out moved down by kh - ph rows, both over the input
+    plane's positions in 32-position chunks (zero past the plane and where a
+    shift leaves it); each CTA sums its contiguous chunk range into one
+    partial split laid out as the kernel writes it ([row tile][column][rows
+    of the tile]); the splits are added and mapped back to OIHW as the
+    reduction does."""
+    N, Co, H, W = go.shape
+    Ci = x.shape[1]
+    info = dg.wgrad_describe(N, Ci, H, W, Co, kH, kW, 1, ph, pw, sm_count=sm_count)
+    assert info["mode"] == 3 and info["interleave"] == 1 and W % 4 == 0
+    ci_rows, nb, n_mt, G = info["seg_rows"], info["slice_n"], info["n_mt"], info["grid"]
+    co_rows = -(-Co // 8) * 8
+    assert ci_rows == -(-Ci // 8) * 8 and nb == -(-kH * co_rows // 16) * 16 and nb <= 256
+    a_rows = kW * ci_rows
+    assert n_mt == -(-a_rows // 128) and n_mt * nb <= info["tmem_cols"] <= 512
+    HW = H * W
+    cpi = -(-HW // 32)
+    T = N * cpi
+    assert G == min(sm_count, T) and info["n_ks"] == G
+    K = cpi * 32
+    q = np.arange(K)
+    col = q % W
+    A = np.zeros((N, n_mt * 128, K))
+    B = np.zeros((N, nb, K))
+    xf, gf = x.reshape(N, Ci, HW), go.reshape(N, Co, HW)
+    for kw in range(kW):
+        d = kw - pw
+        ok = (q < HW) & (col + d >= 0) & (col + d < W)
+        A[:, kw * ci_rows:kw * ci_rows + Ci, ok] = xf[:, :, q[ok] + d]
+    for kh in range(kH):
+        src = q - (kh - ph) * W
+        ok = (src >= 0) & (src < HW)
+        B[:, kh * co_rows:kh * co_rows + Co, ok] = gf[:, :, src[ok]]
+    total = np.zeros(a_rows * nb)
+    for b in range(G):
+        c0, c1 = b * T // G, (b + 1) * T // G
+        assert c1 > c0
+        acc = np.zeros((n_mt * 128, nb))
+        for c in range(c0, c1):
+            n, k0 = divmod(c, cpi)
+            acc += A[n, :, 32 * k0:32 * k0 + 32] @ B[n, :, 32 * k0:32 * k0 + 32].T
+        split = np.zeros(a_rows * nb)
+        for mt in range(n_mt):
+            rows = min(128, a_rows - mt * 128)
+            split[mt * 128 * nb:mt * 128 * nb + rows * nb] = acc[mt * 128:mt * 128 + rows].T.reshape(-1)
+        total += split
+    dw = np.full((Co, Ci, kH, kW), np.nan)
+    for i in range(a_rows * nb):
+        mt, w = divmod(i, 128 * nb)
+        rows = min(128, a_rows - mt * 128)
+        c, row = divmod(w, rows)
+        kw, ci = divmod(mt * 128 + row, ci_rows)
+        kh, co = divmod(c, co_rows)
+        if ci < Ci and co < Co and kh < kH:
+            assert np.isnan(dw[co, ci, kh, kw])   # each weight element is produced once
+            dw[co, ci, kh, kw] = total[i]
+    assert not np.isnan(dw).any()
+    return dw
+
+
+@pytest.mark.parametrize("shape", PLANE_SHAPES)
+def test_emulated_wgrad_plane_matches_oracle(shape):
+    N, Ci, Co, H, W, kH, kW, s, ph, pw = shape
+    rng = np.random.default_rng(61)
+    go = rng.standard_normal((N, Co, H, W))
+    x = rng.standard_normal((N, Ci, H, W))
+    for sms in (152, 5):
+        emu = emulate_wgrad_plane(go, x, kH, kW, ph, pw, sms)
+        ref, mag = oracle.wgrad(go.astype(np.float32), x.astype(np.float32), kH, kW, s, ph, pw)
+        assert np.abs(emu - ref).max() <= 1e-5 * max(1.0, mag.max())   # inputs rounded to fp32 for the oracle
+
+
+def test_wgrad_plane_mode_choice():
+    assert dg.wgrad_describe(32, 64, 56, 56, 64, 3, 3, 1, 1, 1)["mode"] == 3
+    assert dg.wgrad_describe(32, 64, 56, 56, 64, 3, 3, 1, 1, 1, "tf32x3")["mode"] == 1   # split: the run mode
+    assert dg.wgrad_describe(32, 64, 56, 54, 64, 3, 3, 1, 1, 1)["mode"] != 3            # rows of 54 positions
+    assert dg.wgrad_describe(2, 8, 8, 8, 8, 3, 3, 2, 1, 1)["mode"] != 3                 # stride 2
+    assert dg.wgrad_describe(2, 8, 8, 8, 8, 3, 3, 1, 0, 0)["mode"] != 3                 # oH < H
+    assert dg.wgrad_describe(2, 8, 8, 8, 8, 1, 1, 1, 0, 0)["mode"] == 2                 # 1x1: direct
+    assert dg.wgrad_describe(2, 256, 8, 8, 64, 3, 3, 1, 1, 1)["mode"] != 3              # 6 x 192 accumulator columns
+    assert dg.wgrad_describe(2, 256, 8, 8, 8, 3, 3, 1, 1, 1)["mode"] == 3               # 6 x 32 fit
+    d = dg.wgrad_describe(32, 64, 56, 56, 64, 3, 3, 1, 1, 1, sm_count=152)
+    assert d["workspace_bytes"] < (24 << 20)   # partial splits only, no frames
+    assert d["stages"] >= 3 and d["smem_bytes"] <= 232448 and d["slice_n"] == 192 and d["n_mt"] == 2
+
+
 RUN_SHAPES = [
     # N, Ci, Co, H, W, kH, kW, s, ph, pw: batch-blocked TF32 shapes that run the run mode
-    (32, 64, 64, 56, 56, 3, 3, 1, 1, 1),   # the resnet_stage shape
+    (32, 64, 64, 56, 54, 3, 3, 1, 1, 1),   # the resnet_stage channels on rows of 54 (no plane mode)
     (32, 3, 4, 7, 9, 3, 3, 1, 1, 1),
     (60, 5, 3, 8, 6, 3, 3, 2, 1, 1),
     (64, 40, 20, 6, 5, 3, 3, 1, 1, 1),     # two image groups
@@ -619,7 +723,7 @@ def test_wgrad_direct_mode_choice():
 def test_wgrad_run_mode_choice():
     assert dg.wgrad_describe_run(2, 3, 8, 8, 4, 3, 3, 1, 1, 1) is None            # small batch: segment mode
     assert dg.wgrad_describe(32, 64, 56, 56, 64, 3, 3, 1, 1, 1, "tf32x3")["mode"] == 1  # split precision too
-    assert dg.wgrad_describe(32, 64, 56, 56, 64, 3, 3, 1, 1, 1)["mode"] == 1
+    assert dg.wgrad_describe(32, 64, 56, 54, 64, 3, 3, 1, 1, 1)["mode"] == 1
 
 
 def test_wgrad_plans():
@@ -666,7 +770,7 @@ def test_wgrad_split_plans():
         Q = -(-wl.N // b["interleave"])
         frames = 4 * (Q * wl.Co * b["Kimg"] + b["n_copies"] * Q * wl.Ci * b["Lx"])
         assert b["workspace_bytes"] >= 2 * frames                                     # hi and lo halves
-        assert a["mode"] == 2 or a["workspace_bytes"] >= frames
+        assert a["mode"] in (2, 3) or a["workspace_bytes"] >= frames   # direct and plane modes: no frames
 
 
 def test_col2im_plans():

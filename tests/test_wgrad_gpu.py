@@ -10,6 +10,15 @@ similar size, far below 1e-5 for the K lengths here.  grad_weight is
 poisoned with NaN before every run, so an element the kernels fail to write
 fails the bar, and it sits between two guard bands of canary values that must
 come back unchanged (no store past either end).
+
+TF32 runs are also held to the products they compute: the oracle on the
+inputs reduced to TF32 the way the mode reduces them (the frame modes round
+to nearest, ties away from zero, when they pack; the direct and plane modes
+let the tensor core take the TF32 part of the caller's values, i.e.
+truncate) gives the exact sum of those products, and the GPU must match it
+within fp32 accumulation error, 2e-6 * sum|terms|.  A term dropped or taken
+from the wrong position moves an element by about 1 / (N*oH*oW) of its
+sum|terms|, far below the TF32 bar but above this one.
 """
 import ctypes
 
@@ -24,8 +33,22 @@ from conv2d_backward_implicit_dgrad_gb300.workloads import ORDER, WORKLOADS, mak
 pytestmark = pytest.mark.gpu
 
 TF32_REL_TERMS = 2e-3
+TF32_PRODUCTS_REL_TERMS = 2e-6
 SPLIT_REL_TERMS = 1e-5
 SPLIT_REL_L2 = 1e-5
+
+
+def tf32_truncate(t):
+    """The TF32 part of fp32 values: the 13 low mantissa bits cleared."""
+    b = t.contiguous().view(torch.int32) & -8192
+    return b.view(torch.float32)
+
+
+def tf32_round(t):
+    """fp32 rounded to TF32, to nearest with ties away from zero: half of the
+    dropped bits' unit added to the magnitude, then those bits cleared."""
+    b = (t.contiguous().view(torch.int32) + 4096) & -8192
+    return b.view(torch.float32)
 
 
 def out_ext(n, k, s, p):
@@ -74,6 +97,12 @@ def check(args, go, x, precision="tf32"):
     assert np.all(gpu[~pos] == 0)
     rel = np.linalg.norm(gpu - ref) / max(np.linalg.norm(ref), 1e-300)
     assert rel < (SPLIT_REL_L2 if precision == "tf32x3" else 1e-3), rel
+    if precision == "tf32":
+        reduce = tf32_truncate if info["mode"] in (2, 3) else tf32_round
+        pref, pmag = oracle.wgrad(reduce(go), reduce(x), kH, kW, s, ph, pw)
+        perr = np.abs(gpu - pref)
+        assert np.all(perr <= TF32_PRODUCTS_REL_TERMS * pmag), \
+            f"mode {info['mode']}: worst |gpu - sum of TF32 products| / sum|terms| = {np.max(perr[pmag > 0] / pmag[pmag > 0]):.3e}"
     return info
 
 
@@ -114,12 +143,55 @@ EDGE = [
     (2, 8, 16, 5, 5, 1, 1, 1, 0, 0),       # 1x1 with 25 positions per plane: frames
 ]
 
+PLANE = [
+    # N, Ci, Co, H, W, kH, kW, s, ph, pw: TF32 plane mode (stride 1, oH = H, oW = W, W a multiple of 4)
+    (2, 5, 7, 6, 8, 3, 3, 1, 1, 1),        # channel rows padded to 8, B columns padded to 32
+    (3, 40, 24, 6, 12, 3, 3, 1, 1, 1),     # one row tile of 120 rows
+    (2, 64, 64, 8, 8, 3, 3, 1, 1, 1),      # two row tiles
+    (2, 3, 4, 5, 4, 5, 5, 1, 2, 2),        # 5 x 5 taps, a ragged chunk per image
+    (1, 16, 16, 7, 12, 3, 5, 1, 1, 2),     # 3 x 5 taps
+    (2, 130, 40, 6, 8, 3, 3, 1, 1, 1),     # four row tiles x 128 columns: all of tensor memory
+    (1, 8, 8, 3, 4, 3, 3, 1, 1, 1),        # one chunk in all: a grid of one CTA
+    (200, 8, 8, 8, 8, 3, 3, 1, 1, 1),      # 400 chunks on 152 CTAs, ranges crossing images
+    (2, 256, 8, 8, 8, 3, 3, 1, 1, 1),      # six row tiles of a 32-column B
+    (32, 3, 8, 40, 44, 3, 3, 1, 1, 1),
+    (32, 130, 24, 9, 8, 3, 3, 1, 1, 1),
+]
+
 
 @pytest.mark.parametrize("shape", EDGE)
 def test_wgrad_edge_shapes(shape):
     N, Ci, Co, H, W, kH, kW, s, ph, pw = shape
     go, x = inputs(*shape, seed=90)
     check((N, Ci, H, W, Co, kH, kW, s, ph, pw), go, x)
+
+
+@pytest.mark.parametrize("shape", PLANE)
+def test_wgrad_plane_shapes(shape):
+    N, Ci, Co, H, W, kH, kW, s, ph, pw = shape
+    go, x = inputs(*shape, seed=95)
+    info = check((N, Ci, H, W, Co, kH, kW, s, ph, pw), go, x)
+    assert info["mode"] == 3
+
+
+def test_wgrad_plane_maps_follow_the_tensors():
+    """Plane mode encodes its tensor maps on the caller's tensors and keeps
+    them while the pointers stay the same: runs on other tensors, then on the
+    first ones again, are each correct."""
+    args = (3, 16, 8, 12, 24, 3, 3, 1, 1, 1)
+    N, Ci, H, W, Co, kH, kW, s, ph, pw = args
+    pairs = [inputs(N, Ci, Co, H, W, kH, kW, s, ph, pw, seed=96 + i) for i in range(2)]
+    refs = [oracle.wgrad(go, x, kH, kW, s, ph, pw) for go, x in pairs]
+    dev = [(go.cuda(), x.cuda()) for go, x in pairs]
+    with dg.WgradPlan(*args, precision="tf32") as plan:
+        assert plan.info["mode"] == 3
+        for i in (0, 1, 0, 1):
+            dw = torch.full((Co, Ci, kH, kW), float("nan"), device="cuda")
+            plan.run(dev[i][0], dev[i][1], dw)
+            torch.cuda.synchronize()
+            plan.check()
+            ref, mag = refs[i]
+            assert np.all(np.abs(dw.cpu().double().numpy() - ref) <= TF32_REL_TERMS * mag)
 
 
 @pytest.mark.parametrize("name", ORDER)
