@@ -122,11 +122,13 @@ __device__ __forceinline__ void shift_row_any(int d, uint32_t src, uint32_t dst,
 }
 
 struct PBars {
-    uint64_t tfull[kWgMaxStages];   // the stage's tensor copies have landed (expect_tx)
+    uint64_t xfull[kWgMaxStages];   // the stage's input copy has landed (expect_tx)
+    uint64_t bfull[kWgMaxStages];   // its grad_out copies have landed (expect_tx)
     uint64_t sfull[kWgMaxStages];   // its shifted rows are written (one arrival per shifting thread)
     uint64_t empty[kWgMaxStages];   // the stage's MMAs have read it
     uint64_t acc_full;
     uint64_t drain;
+    uint64_t tmem_ready;   // the MMA warp has allocated tensor memory (tmem_base is written)
     uint32_t tmem_base;
     volatile int abort_flag;
 };
@@ -159,12 +161,14 @@ __global__ void __launch_bounds__(kPThreads, 1) wgrad_plane_kernel(const __grid_
     const int a_rows = p.kW * p.ci_rows, b_rows = p.kH * p.co_rows;
     if (threadIdx.x == 0) {
         for (int i = 0; i < p.stages; ++i) {
-            dev::mbar_init(dev::smem_u32(&bars->tfull[i]), 1);
+            dev::mbar_init(dev::smem_u32(&bars->xfull[i]), 1);
+            dev::mbar_init(dev::smem_u32(&bars->bfull[i]), 1);
             dev::mbar_init(dev::smem_u32(&bars->sfull[i]), kPGatherWarps * 32);
             dev::mbar_init(dev::smem_u32(&bars->empty[i]), 1);
         }
         dev::mbar_init(dev::smem_u32(&bars->acc_full), 1);
         dev::mbar_init(dev::smem_u32(&bars->drain), 1);
+        dev::mbar_init(dev::smem_u32(&bars->tmem_ready), 1);
         bars->abort_flag = 0;
         dev::fence_mbar_init();
     }
@@ -183,14 +187,9 @@ __global__ void __launch_bounds__(kPThreads, 1) wgrad_plane_kernel(const __grid_
         }
         dev::fence_proxy_async_smem();
     }
-    if (warp == kPMmaWarp) {
-        dev::tmem_alloc(dev::smem_u32(&bars->tmem_base), p.tmem_cols);
-        dev::tmem_relinquish();
-    }
-    dev::tc_fence_before();
+    // The loader starts at once; the MMA warp allocates tensor memory after
+    // this barrier (the allocation's latency overlaps the first copies).
     __syncthreads();
-    dev::tc_fence_after();
-    const uint32_t tmem = bars->tmem_base;
     const long long tmo = p.timeout_ns;
     dev::grid_launch_dependents();   // the reduction reads the partial splits only after griddepcontrol.wait
 
@@ -200,7 +199,8 @@ __global__ void __launch_bounds__(kPThreads, 1) wgrad_plane_kernel(const __grid_
             dev::prefetch_tensormap(&p.x_map);
             dev::prefetch_tensormap(&p.g_map);
             dev::grid_dependency_wait();   // the inputs may come from the previous kernel
-            const uint32_t bytes = static_cast<uint32_t>(p.ci_rows + b_rows) * 128u;
+            const uint32_t xbytes = static_cast<uint32_t>(p.ci_rows) * 128u;
+            const uint32_t bbytes = static_cast<uint32_t>(b_rows) * 128u;
             int last_parity[kWgMaxStages];
             for (int i = 0; i < kWgMaxStages; ++i) last_parity[i] = -1;
             PRing ring;
@@ -213,31 +213,44 @@ __global__ void __launch_bounds__(kPThreads, 1) wgrad_plane_kernel(const __grid_
                 WP_TRACE_CLOCK(tl1);
                 WP_TRACE_ADD(0, tl1 - tl0);
                 if (c == c0) WP_TRACE_ADD(11, tl1 - t_start);
-                const uint32_t bar = dev::smem_u32(&bars->tfull[ring.stage]);
-                dev::mbar_arrive_expect_tx(bar, bytes);
                 const int n = c / p.cpi;
                 const int q0 = (c - n * p.cpi) * 32;
                 const uint32_t dst = base0 + static_cast<uint32_t>(ring.stage) * p.stage_bytes;
-                dev::tma_load_3d(dst + static_cast<uint32_t>(p.pw * p.ci_rows) * 128u, &p.x_map, q0, 0, n, bar);
+                // the input first: the shifting threads wait for it alone
+                const uint32_t xbar = dev::smem_u32(&bars->xfull[ring.stage]);
+                dev::mbar_arrive_expect_tx(xbar, xbytes);
+                dev::tma_load_3d(dst + static_cast<uint32_t>(p.pw * p.ci_rows) * 128u, &p.x_map, q0, 0, n, xbar);
+                const uint32_t bbar = dev::smem_u32(&bars->bfull[ring.stage]);
+                dev::mbar_arrive_expect_tx(bbar, bbytes);
                 for (int kh = 0; kh < p.kH; ++kh)   // row shift: a multiple of 4 positions (W is)
                     dev::tma_load_3d(dst + p.a_bytes + static_cast<uint32_t>(kh * p.co_rows) * 128u, &p.g_map,
-                                     q0 - (kh - p.ph) * p.W, 0, n, bar);
+                                     q0 - (kh - p.ph) * p.W, 0, n, bbar);
                 last_parity[ring.stage] = static_cast<int>(ring.parity);
                 ring.next(p.stages);
             }
             // Never leave with a copy in flight into this CTA's shared memory.
             for (int i = 0; i < p.stages; ++i)
-                if (last_parity[i] >= 0)
-                    dev::mbar_wait(dev::smem_u32(&bars->tfull[i]), static_cast<uint32_t>(last_parity[i]), tmo);
+                if (last_parity[i] >= 0) {
+                    dev::mbar_wait(dev::smem_u32(&bars->xfull[i]), static_cast<uint32_t>(last_parity[i]), tmo);
+                    dev::mbar_wait(dev::smem_u32(&bars->bfull[i]), static_cast<uint32_t>(last_parity[i]), tmo);
+                }
         }
         __syncwarp();
     } else if (warp == kPMmaWarp) {
         // ---------------------------------------------------- MMA issuer
+        dev::tmem_alloc(dev::smem_u32(&bars->tmem_base), p.tmem_cols);
+        dev::tmem_relinquish();
+        dev::tc_fence_before();
+        __syncwarp();
+        dev::tc_fence_after();
+        const uint32_t tmem = bars->tmem_base;
+        if (lane == 0) dev::mbar_arrive(dev::smem_u32(&bars->tmem_ready));   // for the epilogue warps
         PRing ring;
         bool ok = true;
         for (int c = c0; c < c1 && !bars->abort_flag; ++c, ring.next(p.stages)) {
             WP_TRACE_CLOCK(tf0);
-            const bool landed = dev::mbar_wait(dev::smem_u32(&bars->tfull[ring.stage]), ring.parity, tmo) &&
+            const bool landed = dev::mbar_wait(dev::smem_u32(&bars->xfull[ring.stage]), ring.parity, tmo) &&
+                                dev::mbar_wait(dev::smem_u32(&bars->bfull[ring.stage]), ring.parity, tmo) &&
                                 dev::mbar_wait(dev::smem_u32(&bars->sfull[ring.stage]), ring.parity, tmo);
             if (!__all_sync(0xffffffffu, landed)) {
                 if (lane == 0) pfail(bars, p.err);
@@ -336,7 +349,7 @@ __global__ void __launch_bounds__(kPThreads, 1) wgrad_plane_kernel(const __grid_
                     kp[i] = r_j[i] == jj ? b : kp[i];
                 }
             }
-            if (!dev::mbar_wait(dev::smem_u32(&bars->tfull[ring.stage]), ring.parity, tmo)) {
+            if (!dev::mbar_wait(dev::smem_u32(&bars->xfull[ring.stage]), ring.parity, tmo)) {
                 pfail(bars, p.err);
                 ok = false;
                 break;
@@ -366,12 +379,17 @@ __global__ void __launch_bounds__(kPThreads, 1) wgrad_plane_kernel(const __grid_
         WP_TRACE_CLOCK(t_gend);
         if (threadIdx.x == 0) WP_TRACE_ADD(10, t_gend - t_start);
         // Epilogue: warps 0-3 read tensor-memory lanes 32*warp .. 32*warp + 31.
-        const bool got = ok && dev::mbar_wait(dev::smem_u32(&bars->acc_full), 0, tmo);
+        const bool got = ok && dev::mbar_wait(dev::smem_u32(&bars->tmem_ready), 0, tmo) &&
+                         dev::mbar_wait(dev::smem_u32(&bars->acc_full), 0, tmo);
         if (dev::named_bar_and(1, kPGatherWarps * 32, got)) {
+            const uint32_t tmem = bars->tmem_base;
             WP_TRACE_CLOCK(te1);
             if (threadIdx.x == 0) WP_TRACE_ADD(5, te1 - t_gend);
             dev::tc_fence_after();
             float *split = p.part + static_cast<size_t>(blockIdx.x) * a_rows * p.nb;
+            // Each warp stores 32 consecutive rows of one column per
+            // instruction.  (Assembling the split in the free stage ring and
+            // writing it with one bulk copy measured slower: 12k cycles vs 6k.)
             for (int mt = 0; mt < p.n_mt; ++mt) {
                 const int rows = min(128, a_rows - mt * 128);
                 if (warp * 32 >= rows) continue;   // warp-uniform: rows is a multiple of 8
@@ -405,7 +423,7 @@ __global__ void __launch_bounds__(kPThreads, 1) wgrad_plane_kernel(const __grid_
     dev::tc_fence_before();
     __syncthreads();
     dev::tc_fence_after();
-    if (warp == kPMmaWarp) dev::tmem_dealloc(tmem, p.tmem_cols);
+    if (warp == kPMmaWarp) dev::tmem_dealloc(bars->tmem_base, p.tmem_cols);
 }
 
 // Launch with programmatic dependent launch: the kernel may start while the

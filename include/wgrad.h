@@ -63,7 +63,11 @@ typedef struct {
                                per tile of adjacent taps holds a run of positions for several chunks; batch-blocked
                                TF32 only), 2 direct (1x1, stride 1, no padding, H*W a multiple of 4, TF32: the
                                segment kernel's tensor copies read the caller's NCHW tensors, no frames; the MMA
-                               takes the TF32 part of each fp32 value instead of rounding it) */
+                               takes the TF32 part of each fp32 value instead of rounding it), 3 plane (stride 1,
+                               oH = H, oW = W, W a multiple of 4, kW <= 7, TF32: no frames and no pack; K runs over
+                               the input plane's positions, each kernel row of grad_out is a tensor copy shifted
+                               by whole rows, each kernel column of the input a copy shifted in shared memory;
+                               the MMA takes the TF32 part of each value) */
     int Wf;                 /* row pitch of the position frames (grad_out columns plus the taps' column reach) */
     int Kimg;               /* GEMM K per group of f images: oH*Wf*f rounded up to a multiple of 32 */
     int Lx;                 /* length of one input-copy plane (Kimg plus the largest tap offset) */
@@ -82,7 +86,8 @@ typedef struct {
 dgrad_status_t wgrad_describe(int N, int Ci, int H, int W, int Co, int kH, int kW, int stride, int pad_h,
                               int pad_w, dgrad_precision_t precision, int sm_count, wgrad_plan_info_t *info);
 
-/* Host-only tap table (for tests).  Frames interleave f = *interleave
+/* Host-only tap table of the frame modes (for tests; planned as if plane
+ * mode did not exist).  Frames interleave f = *interleave
  * images along K: position (row y, column u) of image n = f*q + j sits at K
  * index (y*Wf + u)*f + j of image group q.  For tap t = kh*kW + kw: the input
  * copy it reads (copy[t]) and its K offset (offset[t], a multiple of 4).
@@ -95,7 +100,8 @@ dgrad_status_t wgrad_describe_taps(int N, int Ci, int H, int W, int Co, int kH, 
                                    int *copy_shift, int *n_copies, int *ty, int *tu, int *interleave);
 
 /* Host-only run-mode table (for tests); DGRAD_ERR_UNSUPPORTED when the shape
- * runs the segment mode.  hdr[15] = {groups, tiles, taps per tile (spt),
+ * runs the segment mode.  Planned as if plane mode did not exist (the table a
+ * TF32 shape that runs plane mode would have in the frame modes).  hdr[15] = {groups, tiles, taps per tile (spt),
  * rows per position block, stages, positions per image group of grad_out
  * (Pg) and of the input copies (Px), chunks per unit, K splits per image
  * group, ci blocks, co tiles, image groups, chunks per stage (L), tiles per
@@ -116,8 +122,9 @@ dgrad_status_t wgrad_plan(int N, int Ci, int H, int W, int Co, int kH, int kW, i
 dgrad_status_t wgrad_plan_info(wgrad_plan_t plan, wgrad_plan_info_t *info);
 
 /* grad_weight = wgrad(grad_out, input), asynchronously on `stream` (three
- * kernels: frame pack, tcgen05 main kernel, reduction).  One plan must not
- * run on two streams at once (its workspace is shared). */
+ * kernels: frame pack, tcgen05 main kernel, reduction; two in the direct and
+ * plane modes, which read the caller's tensors and have no pack).  One plan
+ * must not run on two streams at once (its workspace is shared). */
 dgrad_status_t wgrad_run(wgrad_plan_t plan, const float *grad_out, const float *input, float *grad_weight,
                          void *stream);
 
