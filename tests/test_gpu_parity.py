@@ -10,6 +10,16 @@ Bars (fixed by the tolerance the method is held to):
     split product is within 2^-20 of its size of the exact one, and the 3K
     fp32 additions add at most 2^-23 of the running sum each (truncating
     accumulation allowed for).
+TF32 runs of the tensor-core path are also held to the products they
+compute: the weights are rounded to TF32 (to nearest, ties away from zero)
+when packed, and grad_out likewise by the frame, staged and tensor-memory
+sources, while the producer warps either round it the same way (16-byte
+loads) or let the tensor core truncate it (4-byte asynchronous copies).  The
+oracle on the inputs so reduced gives the exact sum of those products, and
+the GPU must match it within 1e-5 * sum|terms| (fp32 accumulation over at
+most a few hundred MMAs); a dropped or misplaced term moves an element by
+about 1/K of its sum|terms| (K = Co*kH*kW), which the TF32 bar alone would
+miss for long K.
 grad_input is poisoned with NaN before every run, so an element the kernels
 fail to write fails both bars, and it sits between two guard bands of canary
 values that must come back unchanged, so a store past either end of it fails
@@ -28,6 +38,36 @@ from conv2d_backward_implicit_dgrad_gb300.workloads import ORDER, WORKLOADS, mak
 pytestmark = pytest.mark.gpu
 
 FP32_REL_L2 = 1e-5
+TF32_PRODUCTS_REL_TERMS = 1e-5
+
+
+def tf32_round(t):
+    """fp32 rounded to TF32, to nearest with ties away from zero: half of the
+    dropped bits' unit added to the magnitude, then those bits cleared."""
+    b = (t.contiguous().view(torch.int32) + 4096) & -8192
+    return b.view(torch.float32)
+
+
+def tf32_truncate(t):
+    """The TF32 part of fp32 values: the 13 low mantissa bits cleared."""
+    return (t.contiguous().view(torch.int32) & -8192).view(torch.float32)
+
+
+def assert_tf32_products(gpu, go, w, args, info):
+    """The tensor-core TF32 result against the exact sum of the products it
+    computes (see the module docstring)."""
+    N, Ci, H, W, Co, kH, kW, s, ph, pw = args
+    wr = tf32_round(w)
+    reductions = (tf32_round, tf32_truncate) if info["a_source"] == "producers" else (tf32_round,)
+    worst = []
+    for red in reductions:
+        pref, pmag = oracle.dgrad(red(go), wr, H, W, s, ph, pw)
+        err = np.abs(gpu - pref)
+        if np.all(err <= TF32_PRODUCTS_REL_TERMS * pmag):
+            return
+        pos = pmag > 0
+        worst.append(float(np.max(err[pos] / pmag[pos])))
+    raise AssertionError(f"{info['a_source']}: worst |gpu - sum of TF32 products| / sum|terms| = {worst}")
 TF32_REL_TERMS = 2e-3
 
 
@@ -106,6 +146,8 @@ def check(args, go, w, precision, **opts):
         assert_split(gpu, ref, mag, Co, kH, kW)
     else:
         assert_tf32(gpu, ref, mag)
+        if info["path"] == "tcgen05":
+            assert_tf32_products(gpu, go, w, args, info)
     return info
 
 
