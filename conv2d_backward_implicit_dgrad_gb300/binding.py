@@ -30,7 +30,7 @@ PATH_NAME = {v: k for k, v in PATH.items()}
 EXPORTS = ("dgrad_plan", "dgrad_plan_ex", "dgrad_describe", "dgrad_describe_taps", "dgrad_plan_info", "dgrad_run",
            "dgrad_run_fused", "dgrad_prepack", "dgrad_run_packed", "dgrad_pack_grad_out", "dgrad_run_main", "dgrad_run_host", "dgrad_run_noalloc", "dgrad_plan_check",
            "dgrad_plan_destroy", "dgrad_status_string", "dgrad_cuda_error_string",
-           "wgrad_describe", "wgrad_describe_taps", "wgrad_describe_run", "wgrad_plan", "wgrad_plan_info",
+           "wgrad_describe", "wgrad_describe_taps", "wgrad_describe_run", "wgrad_plan", "wgrad_plan_ex", "wgrad_plan_info",
            "wgrad_run", "wgrad_plan_check", "wgrad_plan_destroy", "dgrad_probe_ffma")
 
 
@@ -55,6 +55,10 @@ class WgradPlanInfo(ctypes.Structure):
         d = {name: getattr(self, name) for name, _ in self._fields_}
         d["precision"] = {0: "fp32", 1: "tf32", 2: "tf32x3"}.get(d["precision"], d["precision"])
         return d
+
+
+class WgradOptions(ctypes.Structure):
+    _fields_ = [("timeout_us", ctypes.c_int), ("wait_test", ctypes.c_int)]
 
 
 class PlanInfo(ctypes.Structure):
@@ -131,6 +135,7 @@ def load_library(path: str | None = None):
         lib.wgrad_describe.argtypes = shape + [i, i, ctypes.POINTER(WgradPlanInfo)]
         lib.wgrad_describe_taps.argtypes = shape + [i, p, p, p, p, ctypes.POINTER(i), ctypes.POINTER(i)]
         lib.wgrad_plan.argtypes = shape + [i, ctypes.POINTER(vp)]
+        lib.wgrad_plan_ex.argtypes = shape + [i, ctypes.POINTER(WgradOptions), ctypes.POINTER(vp)]
         lib.wgrad_plan_info.argtypes = [vp, ctypes.POINTER(WgradPlanInfo)]
         lib.wgrad_run.argtypes = [vp, p, p, p, vp]
         lib.wgrad_plan_check.argtypes = [vp]
@@ -138,8 +143,8 @@ def load_library(path: str | None = None):
         lib.wgrad_plan_destroy.restype = None
         lib.dgrad_probe_ffma.argtypes = [i, i, p, vp]
         lib.dgrad_probe_ffma.restype = i
-        for f in ("wgrad_describe", "wgrad_describe_taps", "wgrad_plan", "wgrad_plan_info", "wgrad_run",
-                  "wgrad_plan_check"):
+        for f in ("wgrad_describe", "wgrad_describe_taps", "wgrad_plan", "wgrad_plan_ex", "wgrad_plan_info",
+                  "wgrad_run", "wgrad_plan_check"):
             getattr(lib, f).restype = i
         for f in ("dgrad_plan", "dgrad_plan_ex", "dgrad_describe", "dgrad_describe_taps", "dgrad_plan_info",
                   "dgrad_run", "dgrad_run_fused", "dgrad_prepack", "dgrad_run_packed", "dgrad_pack_grad_out", "dgrad_run_main",
@@ -428,15 +433,18 @@ def wgrad_describe_run(N, Ci, H, W, Co, kH, kW, stride, pad_h, pad_w, sm_count=0
 class WgradPlan:
     """A weight-gradient plan bound to the current CUDA device.
 
-    WgradPlan(N, Ci, H, W, Co, kH, kW, stride, pad_h, pad_w, precision="tf32")
+    WgradPlan(N, Ci, H, W, Co, kH, kW, stride, pad_h, pad_w, precision="tf32", timeout_us=0, wait_test=0)
     plan.run(grad_out, input, grad_weight=None, stream=None) -> grad_weight [Co, Ci, kH, kW]
+    (timeout_us, wait_test: the in-kernel wait limit and the failure-detection test hook, see wgrad.h)
     """
 
-    def __init__(self, N, Ci, H, W, Co, kH, kW, stride=1, pad_h=0, pad_w=0, precision="tf32"):
+    def __init__(self, N, Ci, H, W, Co, kH, kW, stride=1, pad_h=0, pad_w=0, precision="tf32", timeout_us=0,
+                 wait_test=0):
         self._lib = load_library()
         self._h = ctypes.c_void_p()
         self.args = (N, Ci, H, W, Co, kH, kW, stride, pad_h, pad_w)
-        st = self._lib.wgrad_plan(*self.args, PREC[precision], ctypes.byref(self._h))
+        opts = WgradOptions(timeout_us, wait_test)
+        st = self._lib.wgrad_plan_ex(*self.args, PREC[precision], ctypes.byref(opts), ctypes.byref(self._h))
         if st != 0:
             raise DgradError(st, "wgrad_plan")
         info = WgradPlanInfo()

@@ -612,7 +612,14 @@ dgrad_status_t wgrad_describe_run(int N, int Ci, int H, int W, int Co, int kH, i
 
 dgrad_status_t wgrad_plan(int N, int Ci, int H, int W, int Co, int kH, int kW, int stride, int pad_h, int pad_w,
                           dgrad_precision_t precision, wgrad_plan_t *plan_out) {
+    return wgrad_plan_ex(N, Ci, H, W, Co, kH, kW, stride, pad_h, pad_w, precision, nullptr, plan_out);
+}
+
+dgrad_status_t wgrad_plan_ex(int N, int Ci, int H, int W, int Co, int kH, int kW, int stride, int pad_h,
+                             int pad_w, dgrad_precision_t precision, const wgrad_options_t *opts,
+                             wgrad_plan_t *plan_out) {
     if (!plan_out) return DGRAD_ERR_INVALID_ARG;
+    if (opts && (opts->timeout_us < 0 || opts->wait_test < 0 || opts->wait_test > 1)) return DGRAD_ERR_INVALID_ARG;
     *plan_out = nullptr;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return DGRAD_ERR_NO_DEVICE;
@@ -650,6 +657,11 @@ dgrad_status_t wgrad_plan(int N, int Ci, int H, int W, int Co, int kH, int kW, i
                                          dgrad::align256(pl->g.x_elems * 4));
     pl->workspace_bytes = ws;
     fill_wgrad_params(pl);
+    if (opts) {
+        const long long tmo = opts->timeout_us > 0 ? 1000LL * opts->timeout_us : dgrad::kWgTimeoutNs;
+        pl->mp.timeout_ns = pl->wp.timeout_ns = pl->np.timeout_ns = tmo;
+        pl->mp.wait_test = pl->wp.wait_test = pl->np.wait_test = opts->wait_test;
+    }
     // Direct and plane modes encode their maps at run time, on the caller's tensors.
     if (!pl->g.direct && !pl->g.plane && (st = encode_maps(pl, pl->xc, pl->gf)) != DGRAD_OK) {
         cudaFree(mem);

@@ -96,6 +96,7 @@ struct WgradMainParams {
     int blocked, Px;          // batch-blocked frames (chunk = one position; Px positions per xc group)
     uint32_t idesc;
     long long timeout_ns;
+    int wait_test;   // failure-detection test: the MMA warp first waits on a barrier nothing completes
     int4 seg[kWgMaxSegs];   // x: input copy, y: first input channel, z: K offset (elements)
 };
 
@@ -131,6 +132,7 @@ struct WgradRunParams {
     int split, n_copies, Q;   // split precision: lo copies at copy + n_copies and group + Q (stage: hi half, lo half)
     uint32_t idesc;
     long long timeout_ns;
+    int wait_test;   // failure-detection test: the MMA warp first waits on a barrier nothing completes
     int2 tile[kWgMaxTiles];   // x: input copy, y: position offset of the tile's first tap (base + m0)
 };
 
@@ -161,6 +163,7 @@ struct WgradPlaneParams {
     uint32_t a_bytes, stage_bytes;   // A region (n_mt x 16 KB), A + B
     uint32_t idesc;
     long long timeout_ns;
+    int wait_test;   // failure-detection test: the MMA warp first waits on a barrier nothing completes
 };
 
 cudaError_t launch_wgrad_plane(const WgradPlaneParams &p, int grid, int smem_bytes, cudaStream_t stream);

@@ -76,6 +76,7 @@ struct WBars {
     uint64_t acc_full[2];
     uint64_t acc_empty[2];
     uint64_t drain;
+    uint64_t never;   // failure-detection test: a barrier nothing completes
     uint32_t tmem_base;
     volatile int abort_flag;
 };
@@ -126,6 +127,7 @@ __global__ void __launch_bounds__(kWThreads, 1) wgrad_main_kernel(const __grid_c
             dev::mbar_init(dev::smem_u32(&bars->acc_empty[i]), kWEpiWarps * 32);
         }
         dev::mbar_init(dev::smem_u32(&bars->drain), 1);
+        dev::mbar_init(dev::smem_u32(&bars->never), 1);
         bars->abort_flag = 0;
         dev::fence_mbar_init();
     }
@@ -198,6 +200,10 @@ __global__ void __launch_bounds__(kWThreads, 1) wgrad_main_kernel(const __grid_c
         // ---------------------------------------------------- MMA issuer
         WRing ring, racc;
         bool ok = true;
+        if (p.wait_test && !__all_sync(0xffffffffu, dev::mbar_wait(dev::smem_u32(&bars->never), 0, tmo))) {
+            if (lane == 0) wfail(bars, p);   // the test's wait ran out: no MMA is issued
+            ok = false;
+        }
         WG_TRACE_CLOCK(t_start);
         bool first = true;
         for (int w = blockIdx.x; ok && w < p.n_units && !bars->abort_flag; w += gridDim.x, racc.next(2)) {
@@ -357,6 +363,7 @@ __global__ void __launch_bounds__(kWThreads, 1) wgrad_run_kernel(const __grid_co
             dev::mbar_init(dev::smem_u32(&bars->acc_empty[i]), kWEpiWarps * 32);
         }
         dev::mbar_init(dev::smem_u32(&bars->drain), 1);
+        dev::mbar_init(dev::smem_u32(&bars->never), 1);
         bars->abort_flag = 0;
         dev::fence_mbar_init();
     }
@@ -423,6 +430,10 @@ __global__ void __launch_bounds__(kWThreads, 1) wgrad_run_kernel(const __grid_co
         // ---------------------------------------------------- MMA issuer
         WRing ring, racc;
         bool ok = true;
+        if (p.wait_test && !__all_sync(0xffffffffu, dev::mbar_wait(dev::smem_u32(&bars->never), 0, tmo))) {
+            if (lane == 0) wfail(bars, p.err, bars);   // the test's wait ran out: no MMA is issued
+            ok = false;
+        }
         WG_TRACE_CLOCK(t_start);
         bool firstc = true;
         for (int w = blockIdx.x; ok && w < p.n_units && !bars->abort_flag; w += gridDim.x, racc.next(p.acc_sets)) {

@@ -128,6 +128,7 @@ struct PBars {
     uint64_t empty[kWgMaxStages];   // the stage's MMAs have read it
     uint64_t acc_full;
     uint64_t drain;
+    uint64_t never;        // failure-detection test: a barrier nothing completes
     uint64_t tmem_ready;   // the MMA warp has allocated tensor memory (tmem_base is written)
     uint32_t tmem_base;
     volatile int abort_flag;
@@ -168,6 +169,7 @@ __global__ void __launch_bounds__(kPThreads, 1) wgrad_plane_kernel(const __grid_
         }
         dev::mbar_init(dev::smem_u32(&bars->acc_full), 1);
         dev::mbar_init(dev::smem_u32(&bars->drain), 1);
+        dev::mbar_init(dev::smem_u32(&bars->never), 1);
         dev::mbar_init(dev::smem_u32(&bars->tmem_ready), 1);
         bars->abort_flag = 0;
         dev::fence_mbar_init();
@@ -247,7 +249,11 @@ __global__ void __launch_bounds__(kPThreads, 1) wgrad_plane_kernel(const __grid_
         if (lane == 0) dev::mbar_arrive(dev::smem_u32(&bars->tmem_ready));   // for the epilogue warps
         PRing ring;
         bool ok = true;
-        for (int c = c0; c < c1 && !bars->abort_flag; ++c, ring.next(p.stages)) {
+        if (p.wait_test && !__all_sync(0xffffffffu, dev::mbar_wait(dev::smem_u32(&bars->never), 0, tmo))) {
+            if (lane == 0) pfail(bars, p.err);   // the test's wait ran out: no MMA is issued
+            ok = false;
+        }
+        for (int c = c0; ok && c < c1 && !bars->abort_flag; ++c, ring.next(p.stages)) {
             WP_TRACE_CLOCK(tf0);
             const bool landed = dev::mbar_wait(dev::smem_u32(&bars->xfull[ring.stage]), ring.parity, tmo) &&
                                 dev::mbar_wait(dev::smem_u32(&bars->bfull[ring.stage]), ring.parity, tmo) &&

@@ -112,12 +112,27 @@ dgrad_status_t wgrad_describe_taps(int N, int Ci, int H, int W, int Co, int kH, 
 dgrad_status_t wgrad_describe_run(int N, int Ci, int H, int W, int Co, int kH, int kW, int stride, int pad_h,
                                      int pad_w, int sm_count, int cap, int *hdr, int *groups, int *taps, int *tiles);
 
+/* Optional settings for wgrad_plan_ex; 0 = default. */
+typedef struct {
+    int timeout_us;   /* limit of every bounded in-kernel wait, in microseconds (0: one second) */
+    int wait_test;    /* failure-detection test only: 1 makes the main kernel's MMA warp first wait on a
+                         barrier that nothing ever completes, so that this bounded wait runs out after
+                         timeout_us; the kernel then records DGRAD_ERR_DEVICE_TIMEOUT (read by
+                         wgrad_plan_check), lets its copies land, frees its tensor memory and exits with
+                         grad_weight incomplete.  Nothing faults or traps.  0 for every real use. */
+} wgrad_options_t;
+
 /* Create a plan on the current device: validate, plan the tiles and allocate
  * the workspace (position frames of grad_out and input, the partial-sum
  * tiles, an error word).  *plan_out owns that memory until
  * wgrad_plan_destroy; it is NULL on failure. */
 dgrad_status_t wgrad_plan(int N, int Ci, int H, int W, int Co, int kH, int kW, int stride, int pad_h, int pad_w,
                           dgrad_precision_t precision, wgrad_plan_t *plan_out);
+
+/* Same as wgrad_plan with options (opts may be NULL: the defaults). */
+dgrad_status_t wgrad_plan_ex(int N, int Ci, int H, int W, int Co, int kH, int kW, int stride, int pad_h,
+                             int pad_w, dgrad_precision_t precision, const wgrad_options_t *opts,
+                             wgrad_plan_t *plan_out);
 
 dgrad_status_t wgrad_plan_info(wgrad_plan_t plan, wgrad_plan_info_t *info);
 

@@ -118,3 +118,39 @@ def test_ffma_pipeline_wait_that_runs_out(name):
         plan.check()
     got = out.cpu().double().numpy()
     assert np.linalg.norm((got - ref).ravel()) <= 1e-5 * np.linalg.norm(ref.ravel())
+
+
+@pytest.mark.parametrize("name,precision,mode", [
+    ("resnet_stage", "tf32", 3),          # plane mode
+    ("resnet_stage", "tf32x3", 1),        # run mode
+    ("strided_downsample", "tf32", 0),    # segment mode
+    ("pointwise", "tf32", 2),             # direct mode
+])
+def test_wgrad_wait_that_runs_out(name, precision, mode):
+    # Each weight-gradient main kernel bounds its waits the same way: with
+    # wait_test its MMA warp first waits on a barrier nothing completes, the
+    # copy and epilogue waits then run out in turn, the launch (and the
+    # reduction after it) ends by itself with the timeout recorded, and a
+    # normal plan on the same context is correct afterwards.
+    wl = WORKLOADS[name]
+    go_h, _ = make_inputs(wl, 9)
+    x_h = torch.randn((wl.N, wl.Ci, wl.H, wl.W), generator=torch.Generator().manual_seed(10))
+    go, x = go_h.cuda(), x_h.cuda()
+    with dg.WgradPlan(*wl.plan_args(), precision=precision, timeout_us=SHORT_US, wait_test=1) as plan:
+        assert plan.info["mode"] == mode
+        t0 = time.perf_counter()
+        plan.run(go, x)
+        torch.cuda.synchronize()
+        elapsed = time.perf_counter() - t0
+        with pytest.raises(dg.DgradError) as exc:
+            plan.check()
+        assert exc.value.status == TIMEOUT_STATUS
+        plan.check()
+    assert elapsed < 5.0
+    ref, mag = oracle.wgrad(go_h, x_h, wl.kH, wl.kW, wl.stride, wl.pad_h, wl.pad_w)
+    with dg.WgradPlan(*wl.plan_args(), precision=precision) as plan:
+        dw = plan.run(go, x)
+        torch.cuda.synchronize()
+        plan.check()
+    bound = 1e-5 if precision == "tf32x3" else 2e-3
+    assert np.all(np.abs(dw.cpu().double().numpy() - ref) <= bound * mag)
