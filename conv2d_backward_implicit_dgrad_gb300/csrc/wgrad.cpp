@@ -619,8 +619,8 @@ dgrad_status_t wgrad_plan_ex(int N, int Ci, int H, int W, int Co, int kH, int kW
                              int pad_w, dgrad_precision_t precision, const wgrad_options_t *opts,
                              wgrad_plan_t *plan_out) {
     if (!plan_out) return DGRAD_ERR_INVALID_ARG;
-    if (opts && (opts->timeout_us < 0 || opts->wait_test < 0 || opts->wait_test > 1)) return DGRAD_ERR_INVALID_ARG;
     *plan_out = nullptr;
+    if (opts && (opts->timeout_us < 0 || opts->wait_test < 0 || opts->wait_test > 1)) return DGRAD_ERR_INVALID_ARG;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return DGRAD_ERR_NO_DEVICE;
     cudaDeviceProp prop;

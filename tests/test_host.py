@@ -726,6 +726,23 @@ def test_wgrad_run_mode_choice():
     assert dg.wgrad_describe(32, 64, 56, 54, 64, 3, 3, 1, 1, 1)["mode"] == 1
 
 
+def test_wgrad_plan_ex_rejects_bad_options():
+    """wgrad_plan_ex validates its options before it touches a device: a
+    negative wait limit or a wait_test other than 0 or 1 is an argument error,
+    and a NULL plan pointer too."""
+    import ctypes
+    from conv2d_backward_implicit_dgrad_gb300 import binding
+    lib = binding.load_library()
+    h = ctypes.c_void_p()
+    args = (2, 8, 8, 8, 8, 3, 3, 1, 1, 1, 1)
+    for timeout_us, wait_test in ((-1, 0), (0, 2), (0, -1)):
+        opts = binding.WgradOptions(timeout_us, wait_test)
+        h.value = 0x1234   # NULL on failure
+        assert lib.wgrad_plan_ex(*args, ctypes.byref(opts), ctypes.byref(h)) == 1
+        assert not h.value
+    assert lib.wgrad_plan_ex(*args, None, None) == 1
+
+
 def test_wgrad_plans():
     for name in ORDER:
         wl = WORKLOADS[name]
