@@ -323,7 +323,9 @@ __global__ void __launch_bounds__(kPThreads, 1) wgrad_plane_kernel(const __grid_
         int col = (q0 + lane) % p.W;   // column of position q0 + lane
         PRing ring;
         bool ok = true;
-        for (int c = c0; c < c1 && !bars->abort_flag; ++c, ring.next(p.stages)) {
+        // Every exit from this loop is agreed by the whole warp (the loop
+        // body holds warp-wide ballots).
+        for (int c = c0; c < c1 && !__any_sync(0xffffffffu, bars->abort_flag != 0); ++c, ring.next(p.stages)) {
             WP_TRACE_CLOCK(tg0);
             const float *plane = p.x + static_cast<size_t>(n) * p.Ci * p.HW + q0;
             // The 16-byte piece past the chunk's edge, for each row of this
@@ -355,8 +357,8 @@ __global__ void __launch_bounds__(kPThreads, 1) wgrad_plane_kernel(const __grid_
                     kp[i] = r_j[i] == jj ? b : kp[i];
                 }
             }
-            if (!dev::mbar_wait(dev::smem_u32(&bars->xfull[ring.stage]), ring.parity, tmo)) {
-                pfail(bars, p.err);
+            if (!__all_sync(0xffffffffu, dev::mbar_wait(dev::smem_u32(&bars->xfull[ring.stage]), ring.parity, tmo))) {
+                if (lane == 0) pfail(bars, p.err);
                 ok = false;
                 break;
             }
