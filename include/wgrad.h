@@ -64,7 +64,10 @@ typedef struct {
                                TF32 only), 2 direct (1x1, stride 1, no padding, H*W a multiple of 4, TF32: the
                                segment kernel's tensor copies read the caller's NCHW tensors, no frames; the MMA
                                takes the TF32 part of each fp32 value instead of rounding it), 3 plane (stride 1,
-                               oH = H, oW = W, W a multiple of 4, kW <= 7, TF32: no frames and no pack; K runs over
+                               oH = H, oW = W, W a multiple of 4, 1 < kH*kW, kW <= 7, TF32, and tiles that fit:
+                               kH*round8(Co) <= 256, the kW*round8(Ci) rows in tiles of 128 with all
+                               accumulators in 512 tensor-memory columns, (kW-1)*round8(Ci) <= 512; no frames and
+                               no pack; K runs over
                                the input plane's positions, each kernel row of grad_out is a tensor copy shifted
                                by whole rows, each kernel column of the input a copy shifted in shared memory;
                                the MMA takes the TF32 part of each value) */
