@@ -61,16 +61,16 @@ typedef struct {
     int interleave;         /* f: images interleaved along K (32: batch-blocked frames; else 4, or 2, 1 for batches below 4) */
     int mode;               /* main kernel: 0 segment (a tensor copy per tap segment and chunk), 1 run (a tensor copy
                                per tile of adjacent taps holds a run of positions for several chunks; batch-blocked
-                               TF32 only), 2 direct (1x1, stride 1, no padding, H*W a multiple of 4, TF32: the
-                               segment kernel's tensor copies read the caller's NCHW tensors, no frames; the MMA
-                               takes the TF32 part of each fp32 value instead of rounding it), 3 plane (stride 1,
-                               oH = H, oW = W, W a multiple of 4, 1 < kH*kW, kW <= 7, TF32, and tiles that fit:
-                               kH*round8(Co) <= 256, the kW*round8(Ci) rows in tiles of 128 with all
-                               accumulators in 512 tensor-memory columns, (kW-1)*round8(Ci) <= 512; no frames and
-                               no pack; K runs over
-                               the input plane's positions, each kernel row of grad_out is a tensor copy shifted
-                               by whole rows, each kernel column of the input a copy shifted in shared memory;
-                               the MMA takes the TF32 part of each value) */
+                               frames, TF32 and split precision), 2 direct (1x1, stride 1, no padding, H*W a
+                               multiple of 4, TF32: the segment kernel's tensor copies read the caller's NCHW
+                               tensors, no frames; the MMA takes the TF32 part of each fp32 value instead of
+                               rounding it), 3 plane (stride 1, oH = H, oW = W, W a multiple of 4, 1 < kH*kW,
+                               kW <= 7, TF32, and tiles that fit: kH*round8(Co) <= 256, the kW*round8(Ci) rows in
+                               tiles of 128 with all accumulators in 512 tensor-memory columns,
+                               (kW-1)*round8(Ci) <= 512; no frames and no pack: K runs over the input plane's
+                               positions, each kernel row of grad_out is a tensor copy shifted by whole rows, each
+                               kernel column of the input a copy shifted in shared memory; the MMA takes the TF32
+                               part of each value) */
     int Wf;                 /* row pitch of the position frames (grad_out columns plus the taps' column reach) */
     int Kimg;               /* GEMM K per group of f images: oH*Wf*f rounded up to a multiple of 32 */
     int Lx;                 /* length of one input-copy plane (Kimg plus the largest tap offset) */
